@@ -1,0 +1,289 @@
+"""CSA2 oracle -- TEST INFRASTRUCTURE ONLY.
+
+ctypes wrapper over ``csa2_oracle.c``, the plain CPU restatement of the CSA2
+decode path and cache writer (fp64 except where the cache format fixes fp32).
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  It shares no code with the CUDA library.
+
+Parity status of each function (what pins it independently of itself) is in
+``tests/test_oracle_*.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB = os.path.join(_HERE, "libcsa2oracle.so")
+_lib = None
+
+D_MAIN, D_IDX, H_IDX, H_ATT = 512, 128, 32, 64
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            from . import build as _b
+
+            _b.build()
+        lib = ctypes.CDLL(LIB)
+        vp, i64, i32, f32, f64 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float,
+                                  ctypes.c_double)
+        lib.o_e2m1_value.argtypes = [ctypes.c_int]
+        lib.o_e2m1_value.restype = f64
+        lib.o_e2m1_encode.argtypes = [f32]
+        lib.o_e2m1_encode.restype = ctypes.c_int
+        lib.o_e4m3_value.argtypes = [ctypes.c_int]
+        lib.o_e4m3_value.restype = f64
+        lib.o_e4m3_encode.argtypes = [f32]
+        lib.o_e4m3_encode.restype = ctypes.c_int
+        lib.o_e8m0_value.argtypes = [ctypes.c_int]
+        lib.o_e8m0_value.restype = f64
+        for f in ("o_quantize_main", "o_quantize_index", "o_dequant_main", "o_dequant_index"):
+            getattr(lib, f).argtypes = [vp, i64, vp, vp] if "quantize" in f and "de" not in f \
+                else [vp, vp, i64, vp]
+            getattr(lib, f).restype = None
+        lib.o_main_group_margin.argtypes = [vp]
+        lib.o_main_group_margin.restype = f64
+        lib.o_index_group_margin.argtypes = [vp]
+        lib.o_index_group_margin.restype = f64
+        lib.o_cache_write.argtypes = [vp, i64, ctypes.c_int, vp, vp, vp, ctypes.c_int, vp, vp, vp,
+                                      vp, vp, vp, ctypes.c_int]
+        lib.o_cache_write.restype = ctypes.c_int
+        lib.o_pool.argtypes = [vp, vp, i64, ctypes.c_int, ctypes.c_int, vp]
+        lib.o_pool.restype = None
+        lib.o_index_scores.argtypes = [vp, vp, i64, vp, vp, vp, ctypes.c_int]
+        lib.o_index_scores.restype = None
+        lib.o_index_scores_at.argtypes = [vp, vp, vp, i64, vp, vp, vp]
+        lib.o_index_scores_at.restype = None
+        lib.o_topk.argtypes = [vp, i64, ctypes.c_int, vp]
+        lib.o_topk.restype = ctypes.c_int
+        lib.o_block_max.argtypes = [vp, i64, ctypes.c_int, vp]
+        lib.o_block_max.restype = None
+        lib.o_hier_pool.argtypes = [vp, i64, ctypes.c_int, vp]
+        lib.o_hier_pool.restype = ctypes.c_int
+        lib.o_pool_topk.argtypes = [vp, i64, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp]
+        lib.o_pool_topk.restype = ctypes.c_int
+        lib.o_attention.argtypes = [vp, vp, vp, ctypes.c_int, vp, ctypes.c_int, vp, f64, vp, vp]
+        lib.o_attention.restype = None
+        lib.o_e2m1_encode_array.argtypes = [vp, i64, vp]
+        lib.o_e2m1_encode_array.restype = None
+        lib.o_e4m3_encode_array.argtypes = [vp, i64, vp]
+        lib.o_e4m3_encode_array.restype = None
+        _lib = lib
+    return _lib
+
+
+def _p(a: np.ndarray | None) -> int | None:
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data
+
+
+def _threads() -> int:
+    return max(1, min(128, os.cpu_count() or 1))
+
+
+# ----------------------------------------------------------------------------- formats
+
+def e2m1_value(code: int) -> float:
+    return _load().o_e2m1_value(code)
+
+
+def e2m1_encode(x: float) -> int:
+    return _load().o_e2m1_encode(x)
+
+
+def e2m1_encode_array(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, np.float32).ravel()
+    out = np.empty(x.shape[0], np.uint8)
+    _load().o_e2m1_encode_array(_p(x), x.shape[0], _p(out))
+    return out
+
+
+def e4m3_encode_array(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, np.float32).ravel()
+    out = np.empty(x.shape[0], np.uint8)
+    _load().o_e4m3_encode_array(_p(x), x.shape[0], _p(out))
+    return out
+
+
+def e4m3_value(b: int) -> float:
+    return _load().o_e4m3_value(b)
+
+
+def e4m3_encode(x: float) -> int:
+    return _load().o_e4m3_encode(x)
+
+
+def e8m0_value(b: int) -> float:
+    return _load().o_e8m0_value(b)
+
+
+# ----------------------------------------------------------------------------- quantizers
+
+def quantize_main(x: np.ndarray):
+    """fp32 [n,512] -> (codes u8 [n,256], scales u8 [n,32])."""
+    x = np.ascontiguousarray(x, np.float32)
+    n = x.shape[0]
+    codes = np.zeros((n, 256), np.uint8)
+    scales = np.zeros((n, 32), np.uint8)
+    _load().o_quantize_main(_p(x), n, _p(codes), _p(scales))
+    return codes, scales
+
+
+def quantize_index(x: np.ndarray):
+    """fp32 [n,128] -> (codes u8 [n,64], scales u8 [n,4])."""
+    x = np.ascontiguousarray(x, np.float32)
+    n = x.shape[0]
+    codes = np.zeros((n, 64), np.uint8)
+    scales = np.zeros((n, 4), np.uint8)
+    _load().o_quantize_index(_p(x), n, _p(codes), _p(scales))
+    return codes, scales
+
+
+def dequant_main(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.uint8)
+    n = codes.shape[0]
+    out = np.empty((n, D_MAIN), np.float64)
+    _load().o_dequant_main(_p(codes), _p(scales), n, _p(out))
+    return out
+
+
+def dequant_index(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.uint8)
+    n = codes.shape[0]
+    out = np.empty((n, D_IDX), np.float64)
+    _load().o_dequant_index(_p(codes), _p(scales), n, _p(out))
+    return out
+
+
+def main_group_margins(x: np.ndarray) -> np.ndarray:
+    """Relative distance of each 16-channel group to its nearest rounding decision point."""
+    x = np.ascontiguousarray(np.asarray(x, np.float64).reshape(-1, 16))
+    lib = _load()
+    return np.array([lib.o_main_group_margin(_p(np.ascontiguousarray(r))) for r in x])
+
+
+def index_group_margins(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(np.asarray(x, np.float64).reshape(-1, 32))
+    lib = _load()
+    return np.array([lib.o_index_group_margin(_p(np.ascontiguousarray(r))) for r in x])
+
+
+# ----------------------------------------------------------------------------- cache write
+
+def cache_write(H: np.ndarray, Wkv: np.ndarray, Wz: np.ndarray, Wik: np.ndarray, m: int,
+                return_prequant: bool = False):
+    """H bf16 bits [T,d]; W_KV, W_Z bf16 bits [d,512]; W_IK bf16 bits [512,128].
+
+    Returns (kv_codes, kv_scales, ix_codes, ix_scales) for T/m entries and, if
+    asked, the fp64 pooled latents Cbar [T/m,512] and indexer keys K^I [T/m,128].
+    """
+    H = np.ascontiguousarray(H, np.uint16)
+    T, d = H.shape
+    n = T // m
+    kvc = np.zeros((n, 256), np.uint8)
+    kvs = np.zeros((n, 32), np.uint8)
+    ixc = np.zeros((n, 64), np.uint8)
+    ixs = np.zeros((n, 4), np.uint8)
+    cb = np.zeros((n, D_MAIN), np.float64) if return_prequant else None
+    ki = np.zeros((n, D_IDX), np.float64) if return_prequant else None
+    rc = _load().o_cache_write(_p(H), T, d, _p(np.ascontiguousarray(Wkv, np.uint16)),
+                               _p(np.ascontiguousarray(Wz, np.uint16)),
+                               _p(np.ascontiguousarray(Wik, np.uint16)), m, _p(kvc), _p(kvs),
+                               _p(ixc), _p(ixs), _p(cb), _p(ki), _threads())
+    if rc != 0:
+        raise ValueError("oracle cache_write: bad arguments")
+    if return_prequant:
+        return kvc, kvs, ixc, ixs, cb, ki
+    return kvc, kvs, ixc, ixs
+
+
+def pool(C: np.ndarray, Z: np.ndarray, m: int) -> np.ndarray:
+    C = np.ascontiguousarray(C, np.float64)
+    Z = np.ascontiguousarray(Z, np.float64)
+    T, width = C.shape
+    out = np.empty((T // m, width), np.float64)
+    _load().o_pool(_p(C), _p(Z), T, width, m, _p(out))
+    return out
+
+
+# ----------------------------------------------------------------------------- indexer
+
+def index_scores(ix_codes, ix_scales, q_bits, w, n=None, nthreads=None) -> np.ndarray:
+    """Scores of entries 0..n-1.  q_bits bf16 [32,128]; w fp32 [32]."""
+    ix_codes = np.ascontiguousarray(ix_codes, np.uint8)
+    ix_scales = np.ascontiguousarray(ix_scales, np.uint8)
+    n = ix_codes.shape[0] if n is None else n
+    out = np.empty(n, np.float64)
+    _load().o_index_scores(_p(ix_codes), _p(ix_scales), n,
+                           _p(np.ascontiguousarray(q_bits, np.uint16)),
+                           _p(np.ascontiguousarray(w, np.float32)), _p(out),
+                           _threads() if nthreads is None else nthreads)
+    return out
+
+
+def index_scores_at(ix_codes, ix_scales, idx, q_bits, w) -> np.ndarray:
+    idx = np.ascontiguousarray(idx, np.int64)
+    out = np.empty(idx.shape[0], np.float64)
+    _load().o_index_scores_at(_p(np.ascontiguousarray(ix_codes, np.uint8)),
+                              _p(np.ascontiguousarray(ix_scales, np.uint8)), _p(idx),
+                              idx.shape[0], _p(np.ascontiguousarray(q_bits, np.uint16)),
+                              _p(np.ascontiguousarray(w, np.float32)), _p(out))
+    return out
+
+
+def topk(scores: np.ndarray, k: int, n: int | None = None) -> np.ndarray:
+    scores = np.ascontiguousarray(scores, np.float64)
+    n = scores.shape[0] if n is None else n
+    out = np.empty(k, np.int32)
+    _load().o_topk(_p(scores), n, k, _p(out))
+    return out
+
+
+def block_max(scores: np.ndarray, blk: int, n: int | None = None) -> np.ndarray:
+    scores = np.ascontiguousarray(scores, np.float64)
+    n = scores.shape[0] if n is None else n
+    out = np.empty((n + blk - 1) // blk, np.float64)
+    _load().o_block_max(_p(scores), n, blk, _p(out))
+    return out
+
+
+def hier_pool(bmax: np.ndarray, keep: int) -> np.ndarray:
+    bmax = np.ascontiguousarray(bmax, np.float64)
+    out = np.empty(keep, np.int32)
+    _load().o_hier_pool(_p(bmax), bmax.shape[0], keep, _p(out))
+    return out
+
+
+def pool_topk(scores: np.ndarray, pool_blocks: np.ndarray, blk: int, k: int,
+              n: int | None = None) -> np.ndarray:
+    scores = np.ascontiguousarray(scores, np.float64)
+    n = scores.shape[0] if n is None else n
+    pool_blocks = np.ascontiguousarray(pool_blocks, np.int32)
+    out = np.empty(k, np.int32)
+    _load().o_pool_topk(_p(scores), n, _p(pool_blocks), pool_blocks.shape[0], blk, k, _p(out))
+    return out
+
+
+# ----------------------------------------------------------------------------- attention
+
+def attention(kv_codes, kv_scales, topk_idx, swa, q_bits, scale):
+    """One query: returns (out fp64 [64,512], lse fp64 [64])."""
+    topk_idx = np.ascontiguousarray(topk_idx, np.int32)
+    swa = np.ascontiguousarray(swa, np.uint8).reshape(-1, D_MAIN)
+    out = np.empty((H_ATT, D_MAIN), np.float64)
+    lse = np.empty(H_ATT, np.float64)
+    _load().o_attention(_p(np.ascontiguousarray(kv_codes, np.uint8)),
+                        _p(np.ascontiguousarray(kv_scales, np.uint8)), _p(topk_idx),
+                        topk_idx.shape[0], _p(swa) if swa.size else None, swa.shape[0],
+                        _p(np.ascontiguousarray(q_bits, np.uint16)), float(scale), _p(out),
+                        _p(lse))
+    return out, lse
