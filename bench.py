@@ -1,0 +1,365 @@
+#!/usr/bin/env python3
+"""CSA2 decode benchmark on one GB300.
+
+Default workload: batch 32 decode queries, each over its own 1,048,576-entry
+decoder Full-layer cache (m = 1, 356 B/entry, 11.95 GB resident), hierarchical
+indexer (131,072 blocks of 8 -> top 2,048 blocks -> token top-512) followed by
+64-head x 512 sparse MQA over the 512 selected entries plus a 128-row FP8
+sliding window.  One step = one csa2_index_topk(HIER_BUILD) + one
+csa2_sparse_attn_decode over the whole batch.  Metric: decode queries/s.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CSA2 decode queries/s at 1M ctx; achieved HBM GB/s vs GB300 peak"
+UNIT = "queries/s"
+WORKLOAD = ("batch 32 decode queries, 1,048,576-entry decoder Full-layer FP4 cache per query (m=1), "
+            "hierarchical indexer 131,072 blocks -> 2,048 blocks -> top-512, "
+            "64x512 sparse MQA over 512 selected + 128 FP8 SWA rows")
+B, N, K_TOP, KEEP, BLOCK, NSWA, SEED = 32, 1 << 20, 512, 2048, 8, 128, 2
+IDX_BYTES, MAIN_BYTES, SWA_ROW = 68, 288, 512
+
+
+def kernel_fingerprint() -> str:
+    """Hash of the sources of the indexer call (scan + select), to match ncu traffic records."""
+    h = hashlib.sha256()
+    for f in ("index.cu", "index_scan.cu", "index_scan.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "compressed_sparse_attention_nvfp4_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(fp: str):
+    """DRAM bytes per indexer call from profiles/traffic_indexer.txt if taken on these sources."""
+    path = os.path.join(ROOT, "profiles", "traffic_indexer.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        parts = line.split("#", 1)[0].split()
+        if len(parts) >= 2 and parts[0] == fp:
+            return float(parts[1])
+    return None
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while running."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            self.proc.wait()
+
+    def summary(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        rows = []
+        for line in open(self.file.name):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 8:
+                try:
+                    rows.append((float(f[0]), float(f[1]), f[4:8]))
+                except ValueError:
+                    pass
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- oracle sample
+
+def oracle_sample(n_queries: int, steps: int):
+    """Time the CPU oracle on `n_queries` of the workload's queries (full 1M-entry caches).
+    Returns (queries/s, threads, description).  Setup (input synthesis, encoding) is untimed."""
+    import numpy as np
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    from synth import workloads as W
+
+    threads = os.cpu_count() or 1
+    q, w = W.index_query(SEED, 0, B)
+    hv = W.hot_vectors(q, w, 3.0)
+    qa = W.attn_query(SEED, 0, B)
+    swa = W.swa_rows(SEED, 0, B)
+    chunk = 1 << 16
+
+    def encode(b, j0):
+        cnt = min(chunk, N - j0)
+        kv = oracle.quantize_main(W.main_latents(SEED, 0, B, N, b, j0, cnt))
+        ix = oracle.quantize_index(W.index_latents(SEED, 0, B, N, b, j0, cnt, 0.02, hv[b]))
+        return j0, kv, ix
+
+    planes = []
+    with ThreadPoolExecutor(threads) as ex:
+        for b in range(n_queries):
+            kvc = np.empty((N, 256), np.uint8)
+            kvs = np.empty((N, 32), np.uint8)
+            ixc = np.empty((N, 64), np.uint8)
+            ixs = np.empty((N, 4), np.uint8)
+            for j0, (c1, s1), (c2, s2) in ex.map(lambda j: encode(b, j), range(0, N, chunk)):
+                kvc[j0:j0 + c1.shape[0]] = c1
+                kvs[j0:j0 + c1.shape[0]] = s1
+                ixc[j0:j0 + c2.shape[0]] = c2
+                ixs[j0:j0 + c2.shape[0]] = s2
+            planes.append((kvc, kvs, ixc, ixs))
+
+    def one(b):
+        kvc, kvs, ixc, ixs = planes[b]
+        s = oracle.index_scores(ixc, ixs, q[b], w[b], nthreads=threads)
+        pool = oracle.hier_pool(oracle.block_max(s, BLOCK), KEEP)
+        sel = oracle.pool_topk(s, pool, BLOCK, K_TOP)
+        oracle.attention(kvc, kvs, sel, swa[b], qa[b], 1 / math.sqrt(512))
+
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        for b in range(n_queries):
+            one(b)
+    dt = time.perf_counter() - t0
+    desc = (f"{n_queries} of the {B} queries at the full 1,048,576-entry context, {steps} pass(es): "
+            f"oracle scores (fp64, {threads} threads), block max, pool, top-512, attention")
+    return n_queries * steps / dt, threads, desc
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import compressed_sparse_attention_nvfp4_gb300 as csa2
+    from compressed_sparse_attention_nvfp4_gb300 import workload as WL
+    from synth import workloads as W
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    csa2.lib()
+    st = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(st):
+        planes = csa2.Planes.empty(B, N, dev)
+        qd, wd, q_h, w_h = WL.index_query_dev(SEED, 0, B, dev)
+        hv = W.hot_vectors(q_h, w_h, 3.0)
+        WL.fill_planes(planes, SEED, 0, B, N, hot_prob=0.02, hotvecs=hv, stream=st)
+        qa_d, qa_h = WL.attn_query_dev(SEED, 0, B, dev)
+        swa_d = WL.swa_dev(SEED, 0, B, NSWA, dev, stream=st)
+        ne = torch.full((B,), N, dtype=torch.int32, device=dev)
+        topk = torch.empty((B, K_TOP), dtype=torch.int32, device=dev)
+        pool = torch.empty((B, KEEP), dtype=torch.int32, device=dev)
+        out = torch.empty((B, 64, 512), dtype=torch.float32, device=dev)
+        lse = torch.empty((B, 64), dtype=torch.float32, device=dev)
+        ws_i = csa2.workspace(csa2.index_topk_workspace_size(B, N, K_TOP, BLOCK, KEEP), dev)
+        ws_a = csa2.workspace(csa2.sparse_attn_workspace_size(B, K_TOP, NSWA), dev)
+    torch.cuda.synchronize()
+    scale = 1.0 / math.sqrt(512)
+
+    def index_call():
+        csa2.index_topk(planes, B, ne, N, qd, wd, K_TOP, csa2.TOPK_HIER_BUILD, topk, ws_i, BLOCK, KEEP,
+                        pool_out=pool, stream=st)
+
+    def attn_call():
+        csa2.sparse_attn_decode(planes, B, topk, K_TOP, swa_d, NSWA, qa_d, scale, out, ws_a,
+                                lse_out=lse, stream=st)
+
+    for _ in range(args.warmup):
+        index_call()
+        attn_call()
+    torch.cuda.synchronize()
+    assert csa2.check(ws_i, st)[0] == 0 and csa2.check(ws_a, st)[0] == 0
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        start.record(st)
+        for s in range(args.steps):
+            ev[s][0].record(st)
+            index_call()
+            ev[s][1].record(st)
+            attn_call()
+            ev[s][2].record(st)
+        stop.record(st)
+        torch.cuda.synchronize()
+        barrier()
+    elapsed_ms = start.elapsed_time(stop)
+    idx_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    att_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    clocks = clk.summary()
+
+    # end to end through the same C-ABI calls with host buffers: per step the
+    # query-side inputs go up from pinned memory and the output comes back
+    h_q = torch.from_numpy(q_h.view(np.int16)).pin_memory()
+    h_w = torch.from_numpy(w_h).pin_memory()
+    h_qa = torch.from_numpy(qa_h.view(np.int16)).pin_memory()
+    h_swa = swa_d.cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_w, h_qa, h_swa))
+    d2h = h_out.numel() * 4 + h_lse.numel() * 4
+    e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e_start.record(st)
+    with torch.cuda.stream(st):
+        for _ in range(args.steps):
+            qd.copy_(h_q, non_blocking=True)
+            wd.copy_(h_w, non_blocking=True)
+            qa_d.copy_(h_qa, non_blocking=True)
+            swa_d.copy_(h_swa, non_blocking=True)
+            index_call()
+            attn_call()
+            h_out.copy_(out, non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
+    e_stop.record(st)
+    torch.cuda.synchronize()
+    e2e_ms = e_start.elapsed_time(e_stop)
+    assert csa2.check(ws_i, st)[0] == 0 and csa2.check(ws_a, st)[0] == 0
+
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([elapsed_ms, e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms, e2e_ms = t.tolist()
+    if rank != 0:
+        return None
+    hbm, peak_kind = peaks()
+    idx_bytes = B * N * IDX_BYTES
+    achieved = idx_bytes / (idx_ms * 1e-3) / 1e9
+    fp = kernel_fingerprint()
+    traffic = recorded_traffic(fp)
+    value = world * B * args.steps / (elapsed_ms * 1e-3)
+    step_bytes = B * (N * IDX_BYTES + K_TOP * MAIN_BYTES + NSWA * SWA_ROW)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": args.dtype_label, "data": "synthetic (seeded counter-based generator)",
+        "config": {"workload": WORKLOAD, "B": B, "N_entries": N, "k": K_TOP, "block": BLOCK,
+                   "n_blocks_keep": KEEP, "n_swa": NSWA, "seed": SEED,
+                   "l2": "inputs larger than L2 (11.95 GB cache resident in HBM); no flush",
+                   "parallelism": f"replicas x{world}"},
+        "step_breakdown_ms": {"index_topk": round(idx_ms, 4), "sparse_attn": round(att_ms, 4)},
+        "step_hbm": {"algorithmic_bytes": step_bytes,
+                     "achieved_gbs": round(step_bytes / (elapsed_ms / args.steps * 1e-3) / 1e9, 1)},
+        "roofline": {"kernel": "csa2_index_topk HIER_BUILD (scan + selects)", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": hbm, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "traffic": traffic, "algorithmic_bytes_per_launch": idx_bytes,
+                     "sources": fp},
+        "e2e": {"value": round(world * B * args.steps / (e2e_ms * 1e-3), 2), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * args.launches_per_step,
+        "clocks": clocks,
+    }
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    args.dtype_label = "f32"
+    # kernels per step: scan + pool select + token select (index), chunk + merge (attention)
+    args.launches_per_step = 5
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        steps = max(1, min(args.steps, 5))
+        v, cores, desc = oracle_sample(1, steps)
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": UNIT, "n_gpus": 0,
+            "steps": steps, "warmup": 0, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded counter-based generator)",
+            "config": {"workload": WORKLOAD, "B": B, "N_entries": N, "k": K_TOP, "block": BLOCK,
+                       "n_blocks_keep": KEEP, "n_swa": NSWA, "seed": SEED},
+            "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}))
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    line = run_ours(args, rank, world, local_rank)
+    if line is not None:
+        if world == 1 and not args.no_cpu_baseline:
+            v, cores, desc = oracle_sample(2, 1)
+            line["cpu_baseline"] = {"value": round(v, 4), "unit": UNIT, "cores": cores,
+                                    "kind": "oracle", "sample": desc}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

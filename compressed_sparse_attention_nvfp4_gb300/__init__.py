@@ -1,0 +1,206 @@
+"""CSA2 decode over the FP4 global KV cache, GB300 (sm_103a).
+
+Thin ctypes binding of ``libcsa2.so`` (declared in ``include/csa2.h``): the
+functions below only marshal arguments -- every step of the path runs in the
+library's CUDA kernels.  PyTorch, when used by a caller, only provides device
+memory and streams: tensors are accepted wherever a device pointer is expected.
+
+There is no CPU fallback: importing works without a GPU (for the ABI checks),
+but any call needs the built library and a CUDA device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libcsa2.so")
+
+D_MAIN, D_IDX, H_IDX, H_ATT = 512, 128, 32, 64
+ENTRY_BYTES = 356
+TOPK_FLAT, TOPK_HIER_BUILD, TOPK_POOL = 0, 1, 2
+LAYER_SWA, LAYER_FULL, LAYER_REINDEX, LAYER_REUSE = 0, 1, 2, 3
+
+STATUS = {0: "CSA2_OK", 1: "CSA2_ERR_INVALID_ARG", 2: "CSA2_ERR_UNSUPPORTED",
+          3: "CSA2_ERR_WORKSPACE", 4: "CSA2_ERR_CUDA", 5: "CSA2_ERR_DEVICE_TIMEOUT",
+          6: "CSA2_ERR_INDEX_RANGE"}
+
+
+class Csa2Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+class KVPlanes(ctypes.Structure):
+    """csa2_kv_planes: device pointers of the four planes and the slot stride."""
+    _fields_ = [("kv_codes", ctypes.c_void_p), ("kv_scales", ctypes.c_void_p),
+                ("ix_codes", ctypes.c_void_p), ("ix_scales", ctypes.c_void_p),
+                ("seq_stride", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C-ABI library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"CSA2 CUDA library not built ({LIB_PATH}); "
+                               "run `python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                                 ctypes.c_size_t)
+        pl = ctypes.POINTER(KVPlanes)
+        sig = {
+            "csa2_quantize_entries": ([vp, vp, i64, pl, i64, vp], ctypes.c_int),
+            "csa2_cache_write": ([vp, i64, i32, vp, vp, vp, i32, pl, i32, i64, vp, sz, vp],
+                                 ctypes.c_int),
+            "csa2_cache_write_workspace_size": ([i64, i32], sz),
+            "csa2_index_topk": ([pl, i32, vp, i64, vp, vp, i32, ctypes.c_int, i32, i32, vp, vp, vp,
+                                 vp, vp, sz, vp], ctypes.c_int),
+            "csa2_index_topk_workspace_size": ([i32, i64, i32, i32, i32], sz),
+            "csa2_sparse_attn_decode": ([pl, i32, vp, i32, vp, i32, vp, f32, vp, vp, vp, sz, vp],
+                                        ctypes.c_int),
+            "csa2_sparse_attn_workspace_size": ([i32, i32, i32], sz),
+            "csa2_v41_layer_table": ([i32, vp, vp, vp, vp, vp], ctypes.c_int),
+            "csa2_check": ([vp, vp, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
+            "csa2_status_string": ([ctypes.c_int], ctypes.c_char_p),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _nbytes(x) -> int:
+    return x.numel() * x.element_size()
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        try:
+            import torch
+
+            if torch.cuda.is_available():
+                return torch.cuda.current_stream().cuda_stream
+        except ImportError:
+            pass
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _ok(rc: int, where: str) -> None:
+    if rc != 0:
+        raise Csa2Error(rc, where)
+
+
+# ----------------------------------------------------------------------------- planes
+
+@dataclass
+class Planes:
+    """Device planes of one Full layer's global KV plus the C struct that points at them."""
+    kv_codes: object
+    kv_scales: object
+    ix_codes: object
+    ix_scales: object
+    seq_stride: int
+
+    @property
+    def c(self) -> KVPlanes:
+        return KVPlanes(_ptr(self.kv_codes), _ptr(self.kv_scales), _ptr(self.ix_codes),
+                        _ptr(self.ix_scales), self.seq_stride)
+
+    @staticmethod
+    def empty(n_seq: int, seq_stride: int, device="cuda") -> "Planes":
+        import torch
+
+        n = n_seq * seq_stride
+        u8 = dict(dtype=torch.uint8, device=device)
+        return Planes(torch.empty((n, 256), **u8), torch.empty((n, 32), **u8),
+                      torch.empty((n, 64), **u8), torch.empty((n, 4), **u8), seq_stride)
+
+    def nbytes(self) -> int:
+        return sum(_nbytes(t) for t in (self.kv_codes, self.kv_scales, self.ix_codes, self.ix_scales))
+
+
+def workspace(nbytes: int, device="cuda"):
+    """A device workspace (torch allocations are at least 256-byte aligned)."""
+    import torch
+
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+# ----------------------------------------------------------------------------- entry points
+
+def quantize_entries(planes: Planes, Cbar, KI, n: int, e0: int = 0, stream=None) -> None:
+    _ok(lib().csa2_quantize_entries(_ptr(Cbar), _ptr(KI), n, ctypes.byref(planes.c), e0,
+                                    _stream(stream)), "csa2_quantize_entries")
+
+
+def cache_write_workspace_size(T: int, m: int) -> int:
+    return lib().csa2_cache_write_workspace_size(T, m)
+
+
+def cache_write(H, T: int, d_model: int, Wkv, Wz, Wik, m: int, planes: Planes, seq: int,
+                entry_offset: int, ws, stream=None) -> None:
+    _ok(lib().csa2_cache_write(_ptr(H), T, d_model, _ptr(Wkv), _ptr(Wz), _ptr(Wik), m,
+                               ctypes.byref(planes.c), seq, entry_offset, _ptr(ws), _nbytes(ws),
+                               _stream(stream)), "csa2_cache_write")
+
+
+def index_topk_workspace_size(B: int, n_max: int, k: int, block: int = 8,
+                              n_blocks_keep: int = 0) -> int:
+    return lib().csa2_index_topk_workspace_size(B, n_max, k, block, n_blocks_keep)
+
+
+def index_topk(planes: Planes, B: int, n_entries, n_max: int, qidx, w, k: int, mode: int,
+               topk_out, ws, block: int = 8, n_blocks_keep: int = 0, pool_in=None, pool_out=None,
+               scores_out=None, stream=None) -> None:
+    _ok(lib().csa2_index_topk(ctypes.byref(planes.c), B, _ptr(n_entries), n_max, _ptr(qidx), _ptr(w),
+                              k, mode, block, n_blocks_keep, _ptr(pool_in), _ptr(topk_out),
+                              _ptr(pool_out), _ptr(scores_out), _ptr(ws), _nbytes(ws),
+                              _stream(stream)), "csa2_index_topk")
+
+
+def sparse_attn_workspace_size(B: int, k: int, n_swa: int) -> int:
+    return lib().csa2_sparse_attn_workspace_size(B, k, n_swa)
+
+
+def sparse_attn_decode(planes: Planes, B: int, topk, k: int, swa, n_swa: int, q,
+                       softmax_scale: float, out, ws, lse_out=None, stream=None) -> None:
+    _ok(lib().csa2_sparse_attn_decode(ctypes.byref(planes.c), B, _ptr(topk), k, _ptr(swa), n_swa,
+                                      _ptr(q), softmax_scale, _ptr(out), _ptr(lse_out), _ptr(ws),
+                                      _nbytes(ws), _stream(stream)), "csa2_sparse_attn_decode")
+
+
+def check(ws, stream=None) -> tuple[int, int]:
+    """(status, detail) of the device-side error word of `ws`, cleared afterwards."""
+    d = ctypes.c_int64(0)
+    rc = lib().csa2_check(_ptr(ws), _stream(stream), ctypes.byref(d))
+    return rc, d.value
+
+
+def status_string(s: int) -> str:
+    return lib().csa2_status_string(s).decode()
+
+
+def v41_layer_table() -> dict[str, list[int]]:
+    arrs = {k: (ctypes.c_int32 * 40)() for k in ("mode", "m", "kv_src", "topk_src", "pool_src")}
+    _ok(lib().csa2_v41_layer_table(40, *[ctypes.addressof(a) for a in arrs.values()]),
+        "csa2_v41_layer_table")
+    return {k: list(a) for k, a in arrs.items()}

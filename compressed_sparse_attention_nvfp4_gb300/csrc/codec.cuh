@@ -1,0 +1,99 @@
+// Group quantizers of the cache format, usable from any kernel (the codec entry
+// point and the cache-write epilogue share them so the bytes always agree).
+#pragma once
+
+#include "common.cuh"
+
+namespace csa2 {
+
+// Main KV: 16 channels -> 8 bytes of E2M1 codes + 1 E4M3 scale byte.
+// x16 must be 16-byte aligned; codes8 8-byte aligned.
+__device__ __forceinline__ void quantize_main_group_vals(const float (&v)[16], uint8_t* codes8,
+                                                         uint8_t* scale1) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  float t = __fdiv_rn(amax, 6.0f);
+  uint32_t sb = float_to_e4m3(t);
+  float s = e4m3_to_float(sb);
+  uint32_t c0 = 0, c1 = 0;
+  if (s != 0.0f) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      c0 |= float2_to_e2m1x2(__fdiv_rn(v[2 * i], s), __fdiv_rn(v[2 * i + 1], s)) << (8 * i);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      c1 |= float2_to_e2m1x2(__fdiv_rn(v[8 + 2 * i], s), __fdiv_rn(v[9 + 2 * i], s)) << (8 * i);
+  }
+  *reinterpret_cast<uint2*>(codes8) = make_uint2(c0, c1);
+  *scale1 = (uint8_t)sb;
+}
+
+__device__ __forceinline__ void quantize_main_group(const float* __restrict__ x16, uint8_t* codes8,
+                                                    uint8_t* scale1) {
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float4 f = reinterpret_cast<const float4*>(x16)[i];
+    v[4 * i] = f.x;
+    v[4 * i + 1] = f.y;
+    v[4 * i + 2] = f.z;
+    v[4 * i + 3] = f.w;
+  }
+  quantize_main_group_vals(v, codes8, scale1);
+}
+
+// floor(log2 a) of a finite fp32 a > 0 (normal or subnormal), exactly
+__device__ __forceinline__ int floor_log2_f32(float a) {
+  uint32_t u = __float_as_uint(a);
+  int ef = (int)((u >> 23) & 0xFFu);
+  if (ef) return ef - 127;
+  return (31 - __clz((int)(u & 0x7FFFFFu))) - 149;
+}
+
+// 2^k as fp32 for k in [-127, 127] (2^-127 is the subnormal 0x00400000)
+__device__ __forceinline__ float exp2i_f32(int k) {
+  return k >= -126 ? __uint_as_float((uint32_t)(k + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// Indexer key (MXFP4): 32 elements -> 16 bytes of codes + 1 E8M0 byte.
+__device__ __forceinline__ void quantize_index_group_vals(const float (&v)[32], uint8_t* codes16,
+                                                          uint8_t* scale1) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  int e = -127;
+  if (amax > 0.0f) {
+    e = floor_log2_f32(amax) - 2;
+    e = e < -127 ? -127 : (e > 127 ? 127 : e);
+  }
+  uint32_t c[4] = {0u, 0u, 0u, 0u};
+  if (amax > 0.0f) {
+    float inv = exp2i_f32(-e);  // x / 2^e = x * 2^-e, exact where a code can be nonzero
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      c[i / 4] |= float2_to_e2m1x2(__fmul_rn(v[2 * i], inv), __fmul_rn(v[2 * i + 1], inv))
+                  << (8 * (i % 4));
+  }
+  *reinterpret_cast<uint4*>(codes16) = make_uint4(c[0], c[1], c[2], c[3]);
+  *scale1 = (uint8_t)(e + 127);
+}
+
+__device__ __forceinline__ void quantize_index_group(const float* __restrict__ x32, uint8_t* codes16,
+                                                     uint8_t* scale1) {
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float4 f = reinterpret_cast<const float4*>(x32)[i];
+    v[4 * i] = f.x;
+    v[4 * i + 1] = f.y;
+    v[4 * i + 2] = f.z;
+    v[4 * i + 3] = f.w;
+  }
+  quantize_index_group_vals(v, codes16, scale1);
+}
+
+void launch_quantize(const float* Cbar, const float* KI, int64_t n, const csa2_kv_planes* dst,
+                     int64_t e0, cudaStream_t st);
+
+}  // namespace csa2

@@ -1,0 +1,211 @@
+/*
+ * csa2.h -- C ABI of the CSA2 decode path over the FP4 global KV cache (sm_103a).
+ *
+ * Compressed Sparse Attention 2 as described in
+ *   "DeepSeek-V4.1-Flash: pushing the limits of KV cache compression"
+ *      section 2 (890 bytes/token), 4.1 (single-layer computation), 4.2 (Full /
+ *      Reindex / Reuse), 4.3 (Hierarchical Sparse Indexer), 5 (FP4 Main KV Cache);
+ *   "DeepSeek-V4.1-Flash course, 02 Architecture"
+ *      2.2 Eq. (1), 2.3 CSA2, 2.3.1 cross-layer KV and index reuse, 2.3.2
+ *      hierarchical sparse indexer (Fig. 5), 2.4.4 FP4 main KV cache;
+ *   "DeepSeek-V4: Towards Highly Efficient Million-Token Context Intelligence"
+ *      CSA step 2 (lightning indexer, top-k), step 3 (shared-KV MQA), the
+ *      sliding-window branch.
+ *
+ * Conventions (all entry points):
+ *  - Every pointer argument is DEVICE memory unless stated otherwise; the caller
+ *    owns all memory and the stream.  The library allocates nothing and keeps no
+ *    mutable global state; calls on different streams with different workspaces
+ *    may run concurrently.
+ *  - Tensors are dense and row-major.  bf16 tensors are passed as their 16-bit
+ *    patterns.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  Invalid arguments are reported synchronously and launch
+ *    nothing.  A failed launch returns CSA2_ERR_CUDA.
+ *  - Errors found on the device (an index out of range, a wait that timed out)
+ *    are recorded in the first 16 bytes of the workspace `ws` and read by
+ *    csa2_check().  Kernels never trap.
+ *  - Workspaces must be 256-byte aligned and at least as large as the matching
+ *    *_workspace_size() query; their contents need not be initialised.
+ */
+#ifndef CSA2_H
+#define CSA2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- constants */
+#define CSA2_D_MAIN 512          /* main-KV latent channels                    */
+#define CSA2_D_IDX 128           /* indexer head dimension                     */
+#define CSA2_H_IDX 32            /* indexer heads                              */
+#define CSA2_H_ATT 64            /* attention query heads (MQA over the latent)*/
+#define CSA2_MAIN_CODE_BYTES 256 /* 512 E2M1 codes, 2 per byte                 */
+#define CSA2_MAIN_SCALE_BYTES 32 /* one E4M3 scale per 16 channels             */
+#define CSA2_IDX_CODE_BYTES 64   /* 128 E2M1 codes                             */
+#define CSA2_IDX_SCALE_BYTES 4   /* one E8M0 scale per 32 elements             */
+#define CSA2_ENTRY_BYTES 356     /* 288 main + 68 indexer                      */
+#define CSA2_MAX_TOPK 2048
+#define CSA2_MAX_SWA 128
+
+typedef enum {
+  CSA2_OK = 0,
+  CSA2_ERR_INVALID_ARG = 1,   /* a pointer, size or alignment is not acceptable   */
+  CSA2_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. an unusual m)    */
+  CSA2_ERR_WORKSPACE = 3,     /* workspace missing, misaligned or too small       */
+  CSA2_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed             */
+  CSA2_ERR_DEVICE_TIMEOUT = 5,/* a bounded device-side wait gave up               */
+  CSA2_ERR_INDEX_RANGE = 6    /* a top-k / pool index outside the sequence slot   */
+} csa2_status;
+
+typedef void* csa2_stream; /* a cudaStream_t */
+
+/* One Full layer's global KV: four structure-of-arrays planes, 356 B/entry.
+ * Entry j of sequence slot s lives at flat index e = s * seq_stride + j.
+ *   kv_codes  [e][256]  E2M1 codes of the 512 channels; channel 2i in the low
+ *                       nibble of byte i, 2i+1 in the high nibble.
+ *   kv_scales [e][32]   E4M3 scale of channels 16g..16g+15 in byte g.
+ *   ix_codes  [e][64]   E2M1 codes of the 128-d indexer key, same nibble order.
+ *   ix_scales [e][4]    E8M0 scale (2^(b-127)) of elements 32g..32g+31 in byte g.
+ * ("DeepSeek-V4.1-Flash: pushing the limits of KV cache compression", section 2:
+ *  288 + 68 = 356 bytes per entry.)  Base pointers must be 16-byte aligned. */
+typedef struct {
+  uint8_t* kv_codes;
+  uint8_t* kv_scales;
+  uint8_t* ix_codes;
+  uint8_t* ix_scales;
+  int64_t seq_stride; /* entries per sequence slot (capacity) */
+} csa2_kv_planes;
+
+typedef enum {
+  CSA2_TOPK_FLAT = 0,       /* top-k over entries [0, n_entries)                    */
+  CSA2_TOPK_HIER_BUILD = 1, /* also build the candidate pool: the n_blocks_keep     */
+                            /* blocks of `block` entries with the largest block max */
+  CSA2_TOPK_POOL = 2        /* top-k restricted to a given pool (Reindex layers)    */
+} csa2_topk_mode;
+
+/* ------------------------------------------------------------- cache format */
+
+/* Quantize fp32 latents into cache entries (the cache format's codec alone).
+ *   Cbar [n][512] fp32 -> kv planes; per 16-channel group g:
+ *        s = E4M3_rne_satfinite(fp32(amax/6)), code_i = E2M1_rne_satfinite(fp32(x_i/s)),
+ *        all-zero codes when s == 0.
+ *   KI   [n][128] fp32 -> ix planes; per 32-element group (OCP MXFP4):
+ *        X = 2^(floor(log2 amax) - 2) clamped to [2^-127, 2^127], byte = log2 X + 127,
+ *        code_i = E2M1_rne_satfinite(x_i / X); amax == 0 gives byte 0, zero codes.
+ *   A negative value that rounds to zero keeps its sign (code 8).
+ * ("DeepSeek-V4.1-Flash: pushing the limits of KV cache compression", section 5;
+ *  "DeepSeek-V4.1-Flash course, 02 Architecture", 2.4.4.)
+ * Writes flat entries e0 .. e0+n-1 of `dst`.  Either input may be NULL to skip
+ * that half.  Returns CSA2_ERR_INVALID_ARG for n < 0 or misaligned pointers. */
+csa2_status csa2_quantize_entries(const float* Cbar, const float* KI, int64_t n,
+                                  const csa2_kv_planes* dst, int64_t e0, csa2_stream stream);
+
+/* -------------------------------------------------------------- cache write */
+
+/* Prefill cache write of one sequence slot (CED Eq. (1) and the CSA2 compressor):
+ *   C = H W_KV, Z = H W_Z  (bf16 inputs, fp32 accumulation),
+ *   Cbar_j[c] = sum_{i in B_j} softmax_i(Z_i[c]) C_i[c] over non-overlapping groups
+ *   B_j of m consecutive tokens (aligned at token 0),
+ *   K^I_j = Cbar_j W_IK  (from the fp32 Cbar, before quantization),
+ *   then the codec of csa2_quantize_entries writes entries
+ *   entry_offset .. entry_offset + T/m - 1 of slot `seq`.
+ * ("DeepSeek-V4.1-Flash course, 02 Architecture", 2.2 Eq. (1) and 2.3;
+ *  "DeepSeek-V4.1-Flash: pushing the limits of KV cache compression", 4.1.)
+ *   H [T][d_model] bf16; W_KV, W_Z [d_model][512] bf16; W_IK [512][128] bf16.
+ * Requires T % m == 0, 1 <= m <= 64 with 64 % m == 0, d_model % 64 == 0. */
+csa2_status csa2_cache_write(const void* H_bf16, int64_t T, int32_t d_model, const void* Wkv_bf16,
+                             const void* Wz_bf16, const void* Wik_bf16, int32_t m,
+                             const csa2_kv_planes* dst, int32_t seq, int64_t entry_offset,
+                             void* ws, size_t ws_bytes, csa2_stream stream);
+size_t csa2_cache_write_workspace_size(int64_t T, int32_t m);
+
+/* ---------------------------------------------------------- indexer + top-k */
+
+/* Lightning-indexer scores and top-k selection for B decode queries; query b
+ * reads sequence slot b of `kv`:
+ *   I_j = sum_h w[b,h] * ReLU(q[b,h,:] . K^I_j),  h over 32 heads of dim 128,
+ *   K^I_j the dequantized MXFP4 key of entry j.
+ * Selection order: score descending, then entry index ascending.
+ *   FLAT:       the k best of entries [0, n_entries[b]).
+ *   HIER_BUILD: block score s_u = max of I_j over block u = [u*block, u*block+block)
+ *               (partial last block allowed); the pool is the n_blocks_keep best
+ *               blocks (ties to the lower block); topk = the k best entries of the
+ *               pool, which equals the FLAT result when n_blocks_keep >= k.
+ *   POOL:       the k best entries of the blocks listed in pool_in[b] (ascending
+ *               block ids, -1 padded), scored with this call's own q and w.
+ * ("DeepSeek-V4.1-Flash: pushing the limits of KV cache compression", 4.1, 4.3;
+ *  "DeepSeek-V4: Towards Highly Efficient Million-Token Context Intelligence",
+ *  CSA step 2.)
+ *   n_entries  [B] int32 (device)   visible entries per query, <= n_max
+ *   n_max      host upper bound of n_entries, <= kv->seq_stride
+ *   qidx_bf16  [B][32][128] bf16;   w [B][32] fp32
+ *   topk_out   [B][k] int32: the chosen entry indices in ascending order, -1 padded
+ *   pool_out   [B][n_blocks_keep] int32 (HIER_BUILD, optional): block ids ascending
+ *   scores_out optional fp32: FLAT/HIER_BUILD [B][n_max] entry scores;
+ *              POOL [B][n_blocks_keep*block] candidate scores in pool order
+ * Limits: 1 <= k <= 2048; block == 8; n_blocks_keep*block <= 16384; n_max < 2^31. */
+csa2_status csa2_index_topk(const csa2_kv_planes* kv, int32_t B, const int32_t* n_entries,
+                            int64_t n_max, const void* qidx_bf16, const float* w, int32_t k,
+                            csa2_topk_mode mode, int32_t block, int32_t n_blocks_keep,
+                            const int32_t* pool_in, int32_t* topk_out, int32_t* pool_out,
+                            float* scores_out, void* ws, size_t ws_bytes, csa2_stream stream);
+size_t csa2_index_topk_workspace_size(int32_t B, int64_t n_max, int32_t k, int32_t block,
+                                      int32_t n_blocks_keep);
+
+/* ------------------------------------------------------- sparse attention */
+
+/* Sparse MQA decode over the selected entries joined with the sliding window:
+ *   X_b = [ dequant(main KV of topk[b][i], i < k, skipping -1) ; SWA rows of b ]
+ *   out[b,h,:] = sum_s softmax_s(softmax_scale * q[b,h,:] . X_b[s]) X_b[s]
+ *   lse[b,h]   = natural log of the softmax denominator, max included
+ * with K = V = X (one 512-channel latent per entry), 64 heads sharing X.
+ * ("DeepSeek-V4: Towards Highly Efficient Million-Token Context Intelligence",
+ *  CSA step 3 and the sliding-window branch; "DeepSeek-V4.1-Flash: pushing the
+ *  limits of KV cache compression", 4.1.)
+ *   topk      [B][k] int32 entry indices of slot b (-1 = skip)
+ *   swa_e4m3  [B][n_swa][512] FP8 E4M3 bytes (no scale), 0 <= n_swa <= 128
+ *   q_bf16    [B][64][512] bf16 (unscaled);  out [B][64][512] fp32;  lse_out [B][64] or NULL
+ * An index outside [0, seq_stride) is skipped and reported as CSA2_ERR_INDEX_RANGE
+ * through the workspace error word.  With no rows, out = 0 and lse = -inf. */
+csa2_status csa2_sparse_attn_decode(const csa2_kv_planes* kv, int32_t B, const int32_t* topk,
+                                    int32_t k, const uint8_t* swa_e4m3, int32_t n_swa,
+                                    const void* q_bf16, float softmax_scale, float* out,
+                                    float* lse_out, void* ws, size_t ws_bytes, csa2_stream stream);
+size_t csa2_sparse_attn_workspace_size(int32_t B, int32_t k, int32_t n_swa);
+
+/* ---------------------------------------------------------------- schedule */
+
+typedef enum { CSA2_LAYER_SWA = 0, CSA2_LAYER_FULL = 1, CSA2_LAYER_REINDEX = 2,
+               CSA2_LAYER_REUSE = 3 } csa2_layer_mode;
+
+/* The 40-layer V4.1-Flash layer table ("DeepSeek-V4.1-Flash: pushing the limits of
+ * KV cache compression", section 2 layer layout and 4.2/4.3; "DeepSeek-V4.1-Flash
+ * course, 02 Architecture", 2.1 and 2.3.1).  For layer l (0-based) it writes
+ *   mode[l]      csa2_layer_mode
+ *   m[l]         compression ratio of the KV the layer reads (0 for SWA-only)
+ *   kv_src[l]    the Full layer p(l) whose main KV and indexer K the layer reads (-1: none)
+ *   topk_src[l]  the layer p'(l) whose top-k the layer uses (itself for Full/Reindex, -1: none)
+ *   pool_src[l]  for Reindex layers, the decoder Full layer that built the pool (-1: none)
+ * Host pointers, n_layers entries each; returns CSA2_ERR_INVALID_ARG unless
+ * n_layers == 40. */
+csa2_status csa2_v41_layer_table(int32_t n_layers, int32_t* mode, int32_t* m, int32_t* kv_src,
+                                 int32_t* topk_src, int32_t* pool_src);
+
+/* ------------------------------------------------------------------ errors */
+
+/* Synchronises `stream`, returns the first device-side error recorded in the
+ * workspace `ws` since the last check (CSA2_OK if none) and clears it.
+ * *detail (host, may be NULL) receives the offending value. */
+csa2_status csa2_check(void* ws, csa2_stream stream, int64_t* detail);
+
+const char* csa2_status_string(csa2_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA2_H */

@@ -1,0 +1,136 @@
+"""csa2_index_topk against the oracle: scores, FLAT / HIER_BUILD / POOL
+selection on ragged sizes spanning several tiles, and the degenerate cases."""
+import numpy as np
+import pytest
+
+from gpu_common import SmallCache, csa2, require_gpu, to_dev, torch
+from parity import check_topk
+from synth import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+@pytest.fixture(scope="module")
+def cache(oracle_mod):
+    q, w = W.index_query(0, 0, 3)
+    hv = W.hot_vectors(q, w, 3.0)
+    return SmallCache(oracle_mod, 0, 3, 4133, hot_prob=0.02, hotvecs=hv, stride=4224), q, w
+
+
+def _run(c, q, w, n_entries, k, mode, keep=0, pool_in=None, n_max=None):
+    B = len(n_entries)
+    n_max = n_max or c.n_max
+    ne = to_dev(np.array(n_entries, np.int32))
+    qd, wd = to_dev(q.view(np.int16)), to_dev(w)
+    topk = torch.empty((B, k), dtype=torch.int32, device="cuda")
+    pool = torch.empty((B, max(keep, 1)), dtype=torch.int32, device="cuda")
+    ncols = keep * 8 if mode == csa2.TOPK_POOL else n_max
+    scores = torch.empty((B, ncols), dtype=torch.float32, device="cuda")
+    ws = csa2.workspace(csa2.index_topk_workspace_size(B, n_max, k, 8, keep))
+    csa2.index_topk(c.planes, B, ne, n_max, qd, wd, k, mode, topk, ws, 8, keep,
+                    pool_in=None if pool_in is None else to_dev(pool_in.astype(np.int32)),
+                    pool_out=pool if mode == csa2.TOPK_HIER_BUILD else None, scores_out=scores)
+    st, _ = csa2.check(ws)
+    assert st == 0
+    return topk.cpu().numpy(), pool.cpu().numpy(), scores.cpu().numpy()
+
+
+def test_planes_identical(cache, oracle_mod):
+    c, _, _ = cache
+    for b in range(c.B):
+        for g, o in zip(c.gpu_slot(b), c.oracle_slot(b)):
+            assert np.array_equal(g, o)
+
+
+def test_scores_match_oracle(cache, oracle_mod):
+    c, q, w = cache
+    n_entries = [4133, 4096, 700]
+    topk, _, scores = _run(c, q, w, n_entries, 512, csa2.TOPK_FLAT)
+    for b, n in enumerate(n_entries):
+        _, _, ixc, ixs = c.oracle_slot(b)
+        ref = oracle_mod.index_scores(ixc, ixs, q[b], w[b], n=n)
+        assert np.allclose(scores[b, :n], ref, rtol=2e-5, atol=2e-5 * np.abs(ref).max())
+        check_topk(topk[b], ref, 512, what=f"flat[{b}]")
+
+
+@pytest.mark.parametrize("k,keep", [(64, 100), (512, 2048), (128, 16)])
+def test_hier_build(cache, oracle_mod, k, keep):
+    c, q, w = cache
+    n_entries = [4133, 1000, 9]
+    topk, pool, _ = _run(c, q, w, n_entries, k, csa2.TOPK_HIER_BUILD, keep=keep)
+    for b, n in enumerate(n_entries):
+        _, _, ixc, ixs = c.oracle_slot(b)
+        s = oracle_mod.index_scores(ixc, ixs, q[b], w[b], n=n)
+        bm = oracle_mod.block_max(s, 8)
+        check_topk(pool[b], bm, keep, what=f"pool[{b}]")
+        # token top-k inside the GPU's pool (the oracle scores decide)
+        valid = np.zeros(n, bool)
+        for u in pool[b][pool[b] >= 0]:
+            valid[8 * u:min(8 * u + 8, n)] = True
+        check_topk(topk[b], s, k, valid=valid, what=f"hier[{b}]")
+        if keep >= k:  # the hierarchy invariant: same as the flat top-k (up to near-ties)
+            check_topk(topk[b], s, k, what=f"hier-vs-flat[{b}]")
+
+
+def test_pool_mode(cache, oracle_mod):
+    c, q, w = cache
+    n_entries = [4133, 4096, 700]
+    keep = 300
+    # the pool comes from the oracle with another query (a Reindex layer's pool)
+    q2, w2 = W.index_query(0, 1, 3)
+    pools = []
+    for b, n in enumerate(n_entries):
+        _, _, ixc, ixs = c.oracle_slot(b)
+        pools.append(oracle_mod.hier_pool(oracle_mod.block_max(
+            oracle_mod.index_scores(ixc, ixs, q2[b], w2[b], n=n), 8), keep))
+    pools = np.stack(pools)
+    topk, _, scores = _run(c, q, w, n_entries, 512, csa2.TOPK_POOL, keep=keep, pool_in=pools)
+    for b, n in enumerate(n_entries):
+        _, _, ixc, ixs = c.oracle_slot(b)
+        s = oracle_mod.index_scores(ixc, ixs, q[b], w[b], n=n)
+        valid = np.zeros(n, bool)
+        for u in pools[b][pools[b] >= 0]:
+            valid[8 * u:min(8 * u + 8, n)] = True
+        check_topk(topk[b], s, 512, valid=valid, what=f"pool-mode[{b}]")
+        ref = oracle_mod.pool_topk(s, pools[b], 8, 512)
+        agree = np.intersect1d(topk[b][topk[b] >= 0], ref[ref >= 0]).size
+        assert agree >= min(512, valid.sum()) - 2
+
+
+def test_degenerate_sizes(cache, oracle_mod):
+    c, q, w = cache
+    for n_entries in ([1, 511, 513], [0, 8, 7]):
+        topk, _, _ = _run(c, q, w, n_entries, 512, csa2.TOPK_FLAT)
+        for b, n in enumerate(n_entries):
+            _, _, ixc, ixs = c.oracle_slot(b)
+            s = oracle_mod.index_scores(ixc, ixs, q[b], w[b], n=n)
+            check_topk(topk[b], s, 512, what=f"n={n}")
+    topk, pool, _ = _run(c, q, w, [0, 3, 17], 4, csa2.TOPK_HIER_BUILD, keep=2)
+    assert np.all(topk[0] == -1) and np.all(pool[0] == -1)
+    assert list(topk[1][:3]) == [0, 1, 2] and topk[1][3] == -1
+
+
+def test_equal_scores_take_lowest_indices(cache):
+    """A zero query scores every entry exactly 0: the k lowest indices win."""
+    c, q, w = cache
+    qz = np.zeros_like(q)
+    topk, _, _ = _run(c, qz, w, [4133, 4096, 700], 512, csa2.TOPK_FLAT)
+    for b in range(3):
+        assert np.array_equal(topk[b], np.arange(512))
+    topk, pool, _ = _run(c, qz, w, [4133, 4096, 700], 64, csa2.TOPK_HIER_BUILD, keep=100)
+    assert np.array_equal(pool[0], np.arange(100)) and np.array_equal(topk[0], np.arange(64))
+
+
+def test_negative_weights_general_sign(cache, oracle_mod):
+    c, q, w = cache
+    wn = (w - 0.5).astype(np.float32)
+    topk, _, scores = _run(c, q, wn, [4133, 4096, 700], 256, csa2.TOPK_FLAT)
+    for b, n in enumerate([4133, 4096, 700]):
+        _, _, ixc, ixs = c.oracle_slot(b)
+        s = oracle_mod.index_scores(ixc, ixs, q[b], wn[b], n=n)
+        check_topk(topk[b], s, 256, what=f"signed[{b}]")
