@@ -27,8 +27,9 @@ def _attn(c, topk, swa, q, k, n_swa, lse=True):
     out = torch.empty((B, 64, 512), dtype=torch.float32, device="cuda")
     lse_t = torch.empty((B, 64), dtype=torch.float32, device="cuda")
     ws = csa2.workspace(csa2.sparse_attn_workspace_size(B, k, n_swa))
+    swa_c = np.ascontiguousarray(swa[:, :n_swa])  # [B][n_swa][512] contiguous
     csa2.sparse_attn_decode(c.planes, B, to_dev(topk.astype(np.int32)), k,
-                            to_dev(swa) if n_swa else None, n_swa, to_dev(q.view(np.int16)), SCALE,
+                            to_dev(swa_c) if n_swa else None, n_swa, to_dev(q.view(np.int16)), SCALE,
                             out, ws, lse_out=lse_t if lse else None)
     st, det = csa2.check(ws)
     return out.cpu().numpy(), lse_t.cpu().numpy(), st, det
