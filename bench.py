@@ -317,9 +317,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
-    args.dtype_label = "f32"
-    # kernels per step: scan + pool select + token select (index), chunk + merge (attention)
-    args.launches_per_step = 5
+    args.dtype_label = "f16"  # tensor-core operands (exact E2M1 and prescaled q), fp32 accumulate
+    # kernels per step: full scan + pool select + pool re-scan + token select (index),
+    # chunk + merge (attention)
+    args.launches_per_step = 6
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

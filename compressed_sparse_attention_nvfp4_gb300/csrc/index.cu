@@ -29,6 +29,7 @@ struct SelectArgs {
   int k;
   int32_t* out;         // [B][out_stride]
   int64_t out_stride;
+  int64_t n_max;        // visible entries are clamped to this bound
 };
 
 template <int NT>
@@ -58,7 +59,7 @@ __global__ void __launch_bounds__(NT) k_select(SelectArgs a) {
   __shared__ int s_base_eq, s_base_out;
 
   const int b = blockIdx.x;
-  const int64_t n = a.n_entries[b];
+  const int64_t n = max((int64_t)0, min((int64_t)a.n_entries[b], a.n_max));
   const int64_t ncand = a.pool ? a.ncand_fixed : (a.count_blocks ? cdiv(n, a.block) : n);
   int32_t* out = a.out + (int64_t)b * a.out_stride;
 
@@ -216,29 +217,42 @@ extern "C" csa2_status csa2_index_topk(const csa2_kv_planes* kv, int32_t B, cons
   if (mode == CSA2_TOPK_POOL) {
     float* sc = scores_out ? scores_out : L.scores;
     int64_t sc_stride = scores_out ? keep_c : L.score_cols;
-    launch_scan(kv, B, n_entries, keep_c, q, w, pool_in, n_blocks_keep, block, sc, sc_stride,
-                nullptr, 0, ws, st);
+    csa2_status rs = launch_scan(kv, B, n_entries, n_max, keep_c, q, w, pool_in, n_blocks_keep, sc,
+                                 sc_stride, nullptr, 0, ws, st);
+    if (rs != CSA2_OK) return rs;
     SelectArgs a{sc, sc_stride, n_entries, pool_in, n_blocks_keep, block, 0, 0, keep_c, k,
-                 topk_out, k};
+                 topk_out, k, n_max};
     k_select<1024><<<B, 1024, 0, st>>>(a);
     return launch_status();
   }
 
-  float* sc = scores_out ? scores_out : L.scores;
-  int64_t sc_stride = scores_out ? n_max : L.score_cols;
-  bool hier = mode == CSA2_TOPK_HIER_BUILD;
-  launch_scan(kv, B, n_entries, n_max, q, w, nullptr, 0, block, sc, sc_stride,
-              hier ? L.bmax : nullptr, L.bmax_cols, ws, st);
-  if (!hier) {
-    SelectArgs a{sc, sc_stride, n_entries, nullptr, 0, block, 1, 0, 0, k, topk_out, k};
+  if (mode == CSA2_TOPK_FLAT) {
+    float* sc = scores_out ? scores_out : L.scores;
+    int64_t sc_stride = scores_out ? n_max : L.score_cols;
+    csa2_status rs = launch_scan(kv, B, n_entries, n_max, n_max, q, w, nullptr, 0, sc, sc_stride,
+                                 nullptr, 0, ws, st);
+    if (rs != CSA2_OK) return rs;
+    SelectArgs a{sc, sc_stride, n_entries, nullptr, 0, block, 1, 0, 0, k, topk_out, k, n_max};
     k_select<1024><<<B, 1024, 0, st>>>(a);
     return launch_status();
   }
+
+  // HIER_BUILD: one full scan keeps only the block maxima (entry scores only when
+  // asked for); the pool is selected from them; the token top-k re-scores the
+  // pool's entries, which costs n_blocks_keep*block entries instead of a 4-byte
+  // score per scanned entry.
+  csa2_status rs = launch_scan(kv, B, n_entries, n_max, n_max, q, w, nullptr, 0, scores_out, n_max,
+                               L.bmax, L.bmax_cols, ws, st);
+  if (rs != CSA2_OK) return rs;
   int32_t* pool = pool_out ? pool_out : L.pool;
   SelectArgs pa{L.bmax, L.bmax_cols, n_entries, nullptr, 0, block, 1, 1, 0, n_blocks_keep, pool,
-                n_blocks_keep};
+                n_blocks_keep, n_max};
   k_select<1024><<<B, 1024, 0, st>>>(pa);
-  SelectArgs ta{sc, sc_stride, n_entries, pool, n_blocks_keep, block, 1, 0, keep_c, k, topk_out, k};
+  rs = launch_scan(kv, B, n_entries, n_max, keep_c, q, w, pool, n_blocks_keep, L.scores,
+                   L.score_cols, nullptr, 0, ws, st);
+  if (rs != CSA2_OK) return rs;
+  SelectArgs ta{L.scores, L.score_cols, n_entries, pool, n_blocks_keep, block, 0, 0, keep_c, k,
+                topk_out, k, n_max};
   k_select<1024><<<B, 1024, 0, st>>>(ta);
   return launch_status();
 }

@@ -6,12 +6,15 @@
 
 namespace csa2 {
 
-// ncand_max: entries (pool == nullptr) or pool candidates keep*block per query.
-// scores[b*score_stride + c] receives the score of candidate c (-inf if invalid);
-// bmax[b*bmax_stride + u] (if non-null) the max over entries 8u..8u+7.
-void launch_scan(const csa2_kv_planes* kv, int32_t B, const int32_t* n_entries, int64_t ncand_max,
-                 const uint16_t* q, const float* w, const int32_t* pool, int keep, int block,
-                 float* scores, int64_t score_stride, float* bmax, int64_t bmax_stride, void* ws,
-                 cudaStream_t st);
+// Scores the candidates of B queries (query b reads sequence slot b).
+// ncand_max: entries (pool == nullptr; n_entries[b] <= n_max are visible) or
+// pool candidates keep*8 per query (pool blocks of 8 entries).
+// scores[b*score_stride + c] (if non-null) receives the score of candidate c
+// (-inf if invalid); bmax[b*bmax_stride + u] (if non-null) the max over entries
+// 8u..8u+7.
+csa2_status launch_scan(const csa2_kv_planes* kv, int32_t B, const int32_t* n_entries, int64_t n_max,
+                        int64_t ncand_max, const uint16_t* q, const float* w, const int32_t* pool,
+                        int keep, float* scores, int64_t score_stride, float* bmax, int64_t bmax_stride,
+                        void* ws, cudaStream_t st);
 
 }  // namespace csa2
