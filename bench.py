@@ -315,7 +315,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=32,
+                    help="queries per step; values other than 32 are for small profiling cases, "
+                         "not for the reported metric")
     args = ap.parse_args()
+    global B
+    B = args.batch
     args.warmup = max(args.warmup, 3)
     args.dtype_label = "f16"  # tensor-core operands (exact E2M1 and prescaled q), fp32 accumulate
     # kernels per step: full scan + pool select + pool re-scan + token select (index),

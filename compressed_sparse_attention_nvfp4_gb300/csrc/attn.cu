@@ -4,144 +4,295 @@
 // sliding-window branch; "DeepSeek-V4.1-Flash: pushing the limits of KV cache
 // compression", 4.1).  K = V = the 512-channel latent; 64 heads share it.
 //
-// Each CTA takes a chunk of 64 rows of one query: it dequantizes them into
-// shared memory (exact), computes the 64x64 logits, a chunk-local softmax
-// (max m, sum l) and the unnormalised P X; a merge kernel combines the chunks
-// with their log-sum-exp.
-#include "common.cuh"
+// Each CTA takes a chunk of 128 rows of one query and runs it on the tensor
+// cores (tcgen05, kind::f16, fp32 accumulation in tensor memory):
+//   1. gathers and dequantizes its rows into shared memory as f16 (exact:
+//      E2M1 x E4M3 has at most 6 significant bits), in an interleaved layout
+//      X[c/8][row][c%8] that is K-major for S and M-major for O;
+//   2. stages q with a power-of-two prescale per head (exact for bf16 q);
+//   3. S^T[128 rows x 64 heads] = X q'^T (one thread issues 32 MMAs);
+//   4. chunk-local softmax per head over its rows (max m, sum l), P in f16;
+//   5. O^T[512 x 64] = X^T P^T (four 128-channel M tiles), written unnormalised
+//      with (m, l) per head; a merge kernel combines the chunks by log-sum-exp.
+#include "codec.cuh"
+#include "ptx.cuh"
 
 namespace csa2 {
 
 namespace {
 
-constexpr int kRows = 64;
-constexpr int kAT = 256;
-constexpr int kXPad = kDMain + 4;   // fp32 row pitch of X in shared memory
-constexpr int kQPad = kDMain + 8;   // bf16 row pitch of q
-constexpr int kPPad = kRows + 1;
+constexpr int kRows = 128;
+constexpr int kAT = 128;
+constexpr uint32_t kAttnTmemCols = 256;
+constexpr long long kAttnWaitBudget = 1LL << 32;
 
-struct AttnSmem {
-  float X[kRows][kXPad];
-  __nv_bfloat16 q[kHAtt][kQPad];
-  float p[kHAtt][kPPad];
+struct __align__(1024) AttnSmem {
+  uint16_t X[kDMain / 8][kRows * 8];  // f16, channel-chunk major: [c/8][row][c%8]
+  union {
+    uint16_t q[kDMain / 8][kHAtt * 8];  // f16 q': [c/8][head][c%8]
+    float S[kRows][kHAtt + 1];          // logits, then probabilities (column reductions)
+  } u;
+  uint16_t P[kHAtt / 8][kRows * 8];     // f16 probabilities: [h/8][row][h%8]
+  float colscale[kHAtt];                // softmax_scale * 2^s_h
+  float red[2][kHAtt];
+  float m[kHAtt], l[kHAtt];
   int valid[kRows];
+  uint64_t bar;
+  uint32_t tmem_base;
+  int abort_flag;
 };
 
-__global__ void __launch_bounds__(kAT) k_attn_chunk(
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ void e2m1x8_to_f16(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\tmov.b32 {t0, t1, t2, t3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, t0;\n\tcvt.rn.f16x2.e2m1x2 %1, t1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, t2;\n\tcvt.rn.f16x2.e2m1x2 %3, t3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t h;
+  uint16_t v = (uint16_t)two;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(v));
+  return h;
+}
+
+__global__ void __launch_bounds__(kAT, 1) k_attn_tc(
     const uint8_t* __restrict__ kv_codes, const uint8_t* __restrict__ kv_scales, int64_t seq_stride,
     const int32_t* __restrict__ topk, int k, const uint8_t* __restrict__ swa, int n_swa,
     const uint16_t* __restrict__ qg, float scale, int nchunks, float* __restrict__ part_o,
     float2* __restrict__ part_ml, void* ws) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
   AttnSmem& S = *reinterpret_cast<AttnSmem*>(smem_raw);
+  volatile int* abort_flag = &S.abort_flag;
   const int b = blockIdx.y, chunk = blockIdx.x;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
 
-  // 1. rows -> fp32 in shared memory (each lane: one 16-channel group)
-  for (int r = warp; r < kRows; r += kAT / 32) {
+  if (tid == 0) {
+    ptx::mbar_init(&S.bar, 1);
+    S.abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0) ptx::tmem_alloc(&S.tmem_base, kAttnTmemCols);
+
+  // ---- q' = q 2^-s_h in f16 (two threads per head, 256 channels each)
+  {
+    const int h = tid / 2, half = tid % 2;
+    const uint4* src = reinterpret_cast<const uint4*>(qg + ((int64_t)b * kHAtt + h) * kDMain + half * 256);
+    float mx = 0.0f;
+#pragma unroll 8
+    for (int i = 0; i < 32; ++i) {
+      const uint4 raw = src[i];
+      const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w4[j] << 16)), fabsf(__uint_as_float(w4[j] & 0xFFFF0000u))));
+    }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    const int sig = mx > 0.0f ? floor_log2_f32(mx) - 14 : 0;
+#pragma unroll 8
+    for (int i = 0; i < 32; ++i) {  // 8 channels per uint4 -> one 16-byte chunk of q' (second read hits cache)
+      const uint4 raw = src[i];
+      const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const __half lo = __float2half_rn(ldexpf(__uint_as_float(w4[j] << 16), -sig));
+        const __half hi = __float2half_rn(ldexpf(__uint_as_float(w4[j] & 0xFFFF0000u), -sig));
+        o[j] = (uint32_t)*reinterpret_cast<const uint16_t*>(&lo) |
+               ((uint32_t)*reinterpret_cast<const uint16_t*>(&hi) << 16);
+      }
+      const int cc = half * 32 + i;  // channel chunk c/8
+      *reinterpret_cast<uint4*>(&S.u.q[cc][h * 8]) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (half == 0) S.colscale[h] = ldexpf(scale, sig);
+  }
+
+  // ---- rows -> f16 X (thread r owns row r of the chunk)
+  {
+    const int r = tid;
     const int gr = chunk * kRows + r;
-    float* xr = S.X[r];
     bool ok = false;
     if (gr < k) {
       const int64_t idx = topk[(int64_t)b * k + gr];
       if (idx >= 0 && idx < seq_stride) {
         ok = true;
         const int64_t e = (int64_t)b * seq_stride + idx;
-        const uint2 c = *reinterpret_cast<const uint2*>(kv_codes + e * 256 + lane * 8);
-        const float s = e4m3_to_float(kv_scales[e * 32 + lane]);
-        const uint32_t words[2] = {c.x, c.y};
+        const uint4* cs = reinterpret_cast<const uint4*>(kv_codes + e * 256);
+        const uint4* ss = reinterpret_cast<const uint4*>(kv_scales + e * 32);
+        uint4 c16[16];
 #pragma unroll
-        for (int wi = 0; wi < 2; ++wi)
+        for (int i = 0; i < 16; ++i) c16[i] = cs[i];
+        const uint4 s0 = ss[0], s1 = ss[1];
+        const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
-          for (int bi = 0; bi < 4; ++bi) {
-            float2 v = e2m1x2_to_float2((words[wi] >> (8 * bi)) & 0xFFu);
-            xr[lane * 16 + wi * 8 + bi * 2] = v.x * s;
-            xr[lane * 16 + wi * 8 + bi * 2 + 1] = v.y * s;
-          }
-      } else if (idx != -1 && lane == 0) {
+        for (int g = 0; g < 32; ++g) {  // 16 channels: 8 code bytes, one E4M3 scale
+          const uint32_t sb = (sw[g / 4] >> (8 * (g % 4))) & 0xFFu;
+          const uint32_t s2 = e4m3x2_to_f16x2(sb | (sb << 8));
+          const uint4 cw = c16[g / 2];
+          const uint32_t w0 = (g & 1) ? cw.z : cw.x, w1 = (g & 1) ? cw.w : cw.y;
+          uint32_t h0[4], h1[4];
+          e2m1x8_to_f16(w0, h0);
+          e2m1x8_to_f16(w1, h1);
+          *reinterpret_cast<uint4*>(&S.X[2 * g][r * 8]) =
+              make_uint4(hmul2_u32(h0[0], s2), hmul2_u32(h0[1], s2), hmul2_u32(h0[2], s2), hmul2_u32(h0[3], s2));
+          *reinterpret_cast<uint4*>(&S.X[2 * g + 1][r * 8]) =
+              make_uint4(hmul2_u32(h1[0], s2), hmul2_u32(h1[1], s2), hmul2_u32(h1[2], s2), hmul2_u32(h1[3], s2));
+        }
+      } else if (idx != -1) {
         report_error(ws, CSA2_ERR_INDEX_RANGE, idx);
       }
     } else if (gr - k < n_swa) {
       ok = true;
-      const uint8_t* srow = swa + ((int64_t)b * n_swa + (gr - k)) * kDMain + lane * 16;
-      const uint4 c = *reinterpret_cast<const uint4*>(srow);
-      const uint32_t words[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-      for (int wi = 0; wi < 4; ++wi) {
-        float2 v0 = e4m3x2_to_float2(words[wi] & 0xFFFFu);
-        float2 v1 = e4m3x2_to_float2(words[wi] >> 16);
-        xr[lane * 16 + wi * 4 + 0] = v0.x;
-        xr[lane * 16 + wi * 4 + 1] = v0.y;
-        xr[lane * 16 + wi * 4 + 2] = v1.x;
-        xr[lane * 16 + wi * 4 + 3] = v1.y;
+      const uint4* src = reinterpret_cast<const uint4*>(swa + ((int64_t)b * n_swa + (gr - k)) * kDMain);
+#pragma unroll 4
+      for (int i = 0; i < 32; ++i) {  // 16 channels per uint4 -> two chunks
+        const uint4 v = src[i];
+        *reinterpret_cast<uint4*>(&S.X[2 * i][r * 8]) =
+            make_uint4(e4m3x2_to_f16x2(v.x), e4m3x2_to_f16x2(v.x >> 16), e4m3x2_to_f16x2(v.y),
+                       e4m3x2_to_f16x2(v.y >> 16));
+        *reinterpret_cast<uint4*>(&S.X[2 * i + 1][r * 8]) =
+            make_uint4(e4m3x2_to_f16x2(v.z), e4m3x2_to_f16x2(v.z >> 16), e4m3x2_to_f16x2(v.w),
+                       e4m3x2_to_f16x2(v.w >> 16));
       }
     }
     if (!ok)
-      for (int c = lane; c < kDMain; c += 32) xr[c] = 0.0f;
-    if (lane == 0) S.valid[r] = ok ? 1 : 0;
+#pragma unroll 8
+      for (int cc = 0; cc < kDMain / 8; ++cc) *reinterpret_cast<uint4*>(&S.X[cc][r * 8]) = make_uint4(0, 0, 0, 0);
+    S.valid[r] = ok ? 1 : 0;
   }
-  // 2. q -> shared memory
-  const uint4* qsrc = reinterpret_cast<const uint4*>(qg + (int64_t)b * kHAtt * kDMain);
-  for (int i = threadIdx.x; i < kHAtt * kDMain / 8; i += kAT) {
-    const int h = i / (kDMain / 8), c8 = i % (kDMain / 8);
-    *reinterpret_cast<uint4*>(&S.q[h][c8 * 8]) = qsrc[i];
-  }
+  ptx::fence_proxy_async_smem();
+  ptx::tc_fence_before();
   __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
 
-  // 3. logits: thread -> head h, rows r = j + 4 i (16 rows)
-  const int h = threadIdx.x / 4, j = threadIdx.x % 4;
-  float acc[16];
+  // ---- S^T = X q'^T : M = 128 rows, N = 64 heads, K = 512
+  if (tid == 0) {
+    constexpr uint32_t idesc = ptx::idesc_f16(128, 64, 0);
+#pragma unroll 4
+    for (int ks = 0; ks < kDMain / 16; ++ks) {
+      const uint64_t ad = ptx::smem_desc_noswizzle(&S.X[2 * ks][0], kRows * 16, 128);
+      const uint64_t bd = ptx::smem_desc_noswizzle(&S.u.q[2 * ks][0], kHAtt * 16, 128);
+      ptx::mma_f16_ss(tmem, ad, bd, idesc, ks > 0 ? 1u : 0u);
+    }
+    ptx::mma_commit(&S.bar);
+  }
+  bool ok = ptx::mbar_wait_warp(&S.bar, 0, abort_flag, kAttnWaitBudget);
+  if (!ok && lane == 0) {
+    *abort_flag = 1;
+    report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 21);
+  }
+  ptx::tc_fence_after();
+  const int r = tid;
+  const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+  float sv[kHAtt];
+  {
+    uint32_t a0[32], a1[32];
+    ptx::tmem_ld_32x32b_x32(lane_addr, a0);
+    ptx::tmem_ld_32x32b_x32(lane_addr + 32, a1);
+    ptx::tmem_wait_ld();
+    const bool v = S.valid[r] != 0;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
-  for (int c = 0; c < kDMain; c += 4) {
-    const __nv_bfloat162 q01 = *reinterpret_cast<const __nv_bfloat162*>(&S.q[h][c]);
-    const __nv_bfloat162 q23 = *reinterpret_cast<const __nv_bfloat162*>(&S.q[h][c + 2]);
-    const float2 qa = __bfloat1622float2(q01), qb = __bfloat1622float2(q23);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float4 x = *reinterpret_cast<const float4*>(&S.X[j + 4 * i][c]);
-      acc[i] = fmaf(qa.x, x.x, fmaf(qa.y, x.y, fmaf(qb.x, x.z, fmaf(qb.y, x.w, acc[i]))));
+    for (int h = 0; h < 32; ++h) {
+      sv[h] = v ? __uint_as_float(a0[h]) * S.colscale[h] : -INFINITY;
+      sv[32 + h] = v ? __uint_as_float(a1[h]) * S.colscale[32 + h] : -INFINITY;
     }
   }
-  float mloc = -INFINITY;
+  ptx::tc_fence_before();
+  __syncthreads();  // D1 read by everyone; q' no longer needed (its MMAs completed)
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    acc[i] = S.valid[j + 4 * i] ? acc[i] * scale : -INFINITY;
-    mloc = fmaxf(mloc, acc[i]);
+  for (int h = 0; h < kHAtt; ++h) S.u.S[r][h] = sv[h];
+  __syncthreads();
+  {  // column max
+    const int h = tid % kHAtt, half = tid / kHAtt;
+    float mx = -INFINITY;
+    for (int rr = half * 64; rr < half * 64 + 64; ++rr) mx = fmaxf(mx, S.u.S[rr][h]);
+    S.red[half][h] = mx;
   }
-  mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
-  mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
-  float lsum = 0.0f;
+  __syncthreads();
+  if (tid < kHAtt) S.m[tid] = fmaxf(S.red[0][tid], S.red[1][tid]);
+  __syncthreads();
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float p = (mloc == -INFINITY || acc[i] == -INFINITY) ? 0.0f : expf(acc[i] - mloc);
-    S.p[h][j + 4 * i] = p;
-    lsum += p;
+  for (int hc = 0; hc < kHAtt / 8; ++hc) {  // probabilities, rounded to f16 once
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float pv[2];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int h = hc * 8 + 2 * j + t;
+        const float mh = S.m[h];
+        const float p = (sv[h] == -INFINITY || mh == -INFINITY) ? 0.0f : expf(sv[h] - mh);
+        const __half ph = __float2half_rn(p);
+        pv[t] = __half2float(ph);
+        S.u.S[r][h] = pv[t];
+      }
+      const __half2 h2 = __floats2half2_rn(pv[0], pv[1]);
+      o[j] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    *reinterpret_cast<uint4*>(&S.P[hc][r * 8]) = make_uint4(o[0], o[1], o[2], o[3]);
   }
-  lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
-  lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+  __syncthreads();
+  {  // column sums of the (rounded) probabilities
+    const int h = tid % kHAtt, half = tid / kHAtt;
+    float sm = 0.0f;
+    for (int rr = half * 64; rr < half * 64 + 64; ++rr) sm += S.u.S[rr][h];
+    S.red[half][h] = sm;
+  }
+  ptx::fence_proxy_async_smem();
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (tid < kHAtt) S.l[tid] = S.red[0][tid] + S.red[1][tid];
+
+  // ---- O^T = X^T P^T : four M tiles of 128 channels, N = 64 heads, K = 128 rows
+  if (tid == 0 && !*abort_flag) {
+    constexpr uint32_t idesc = ptx::idesc_f16(128, 64, 0) | (1u << 15) | (1u << 16);  // both M/N-major
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+      for (int ks = 0; ks < kRows / 16; ++ks) {
+        const uint64_t ad = ptx::smem_desc_noswizzle(&S.X[mt * 16][ks * 16 * 8], 128, kRows * 16);
+        const uint64_t bd = ptx::smem_desc_noswizzle(&S.P[0][ks * 16 * 8], 128, kRows * 16);
+        ptx::mma_f16_ss(tmem + (uint32_t)mt * 64u, ad, bd, idesc, ks > 0 ? 1u : 0u);
+      }
+    ptx::mma_commit(&S.bar);
+  }
+  ok = ok && ptx::mbar_wait_warp(&S.bar, 1, abort_flag, kAttnWaitBudget);
+  if (!ok && lane == 0) {
+    *abort_flag = 1;
+    report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 22);
+  }
+  ptx::tc_fence_after();
   const int64_t pc = ((int64_t)b * nchunks + chunk) * kHAtt;
-  if (j == 0) part_ml[pc + h] = make_float2(mloc, lsum);
-  __syncthreads();
-
-  // 4. O = P X : thread -> head h, columns 16 t + 4 j .. +3 for t = 0..31
-  float4 o[32];
+  if (ok) {
+#pragma unroll 1
+    for (int mt = 0; mt < 4; ++mt) {
+      uint32_t a0[32], a1[32];
+      ptx::tmem_ld_32x32b_x32(lane_addr + (uint32_t)mt * 64u, a0);
+      ptx::tmem_ld_32x32b_x32(lane_addr + (uint32_t)mt * 64u + 32u, a1);
+      ptx::tmem_wait_ld();
+      const int c = mt * kRows + r;  // channel
 #pragma unroll
-  for (int t = 0; t < 32; ++t) o[t] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int r = 0; r < kRows; ++r) {
-    const float p = S.p[h][r];
-#pragma unroll
-    for (int t = 0; t < 32; ++t) {
-      const float4 x = *reinterpret_cast<const float4*>(&S.X[r][16 * t + 4 * j]);
-      o[t].x = fmaf(p, x.x, o[t].x);
-      o[t].y = fmaf(p, x.y, o[t].y);
-      o[t].z = fmaf(p, x.z, o[t].z);
-      o[t].w = fmaf(p, x.w, o[t].w);
+      for (int h = 0; h < 32; ++h) {
+        part_o[(pc + h) * kDMain + c] = __uint_as_float(a0[h]);
+        part_o[(pc + 32 + h) * kDMain + c] = __uint_as_float(a1[h]);
+      }
     }
   }
-  float* dst = part_o + (pc + h) * kDMain;
-#pragma unroll
-  for (int t = 0; t < 32; ++t) *reinterpret_cast<float4*>(dst + 16 * t + 4 * j) = o[t];
+  __syncthreads();
+  if (tid < kHAtt) part_ml[pc + tid] = ok ? make_float2(S.m[tid], S.l[tid]) : make_float2(-INFINITY, 0.0f);
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kAttnTmemCols);
+  }
 }
 
 __global__ void __launch_bounds__(128) k_attn_merge(const float* __restrict__ part_o,
@@ -219,12 +370,11 @@ extern "C" csa2_status csa2_sparse_attn_decode(const csa2_kv_planes* kv, int32_t
   if (ws_bytes < L.bytes) return CSA2_ERR_WORKSPACE;
   if (reset_error(ws, st) != CSA2_OK) return CSA2_ERR_CUDA;
   const int smem = (int)sizeof(AttnSmem);
-  if (cudaFuncSetAttribute(k_attn_chunk, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-      cudaSuccess)
+  if (cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return CSA2_ERR_CUDA;
-  k_attn_chunk<<<dim3(nchunks, B), kAT, smem, st>>>(kv->kv_codes, kv->kv_scales, kv->seq_stride, topk,
-                                                    k, swa_e4m3, n_swa, (const uint16_t*)q_bf16,
-                                                    softmax_scale, nchunks, L.part_o, L.part_ml, ws);
+  k_attn_tc<<<dim3(nchunks, B), kAT, smem, st>>>(kv->kv_codes, kv->kv_scales, kv->seq_stride, topk, k,
+                                                 swa_e4m3, n_swa, (const uint16_t*)q_bf16, softmax_scale,
+                                                 nchunks, L.part_o, L.part_ml, ws);
   k_attn_merge<<<B * kHAtt, 128, 0, st>>>(L.part_o, L.part_ml, nchunks, out, lse_out);
   return launch_status();
 }

@@ -13,18 +13,18 @@ namespace csa2 {
 // ------------------------------------------------------------------ selection
 // Radix select of the k largest keys of one query (one CTA per query), then an
 // ordered collection pass: everything above the k-th key, plus the first
-// (lowest-index) entries equal to it, written in ascending candidate order.
-// Candidates are either entries [0, n) / blocks [0, ceil(n/block)) of the query,
-// or the entries of the blocks listed in `pool` (ascending) -- in every case the
-// candidate order is the entry (or block) order, so ties go to the lower index.
+// (lowest-index) candidates equal to it, written in ascending candidate order.
+// Candidates are entries [0, n), blocks [0, ceil(n/8)), or the entries of the
+// 8-entry blocks listed in `pool` (ascending) -- in every case candidate order
+// is entry (or block) order, so ties go to the lower index.  The key of
+// candidate c is keys[b*key_stride + c].
 struct SelectArgs {
   const float* keys;    // [B][key_stride]
   int64_t key_stride;
   const int32_t* n_entries;
   const int32_t* pool;  // [B][keep] or nullptr
-  int keep, block;
-  int key_by_entry;     // key index = entry id (1) or candidate index (0)
-  int count_blocks;     // candidates are the blocks of [0, n)
+  int keep;
+  int count_blocks;     // candidates are the 8-entry blocks of [0, n)
   int64_t ncand_fixed;  // candidate count when pool != nullptr
   int k;
   int32_t* out;         // [B][out_stride]
@@ -32,119 +32,171 @@ struct SelectArgs {
   int64_t n_max;        // visible entries are clamped to this bound
 };
 
-template <int NT>
-__device__ __forceinline__ void select_candidate(const SelectArgs& a, int b, int64_t c, int64_t ncand,
-                                                 int64_t n, uint32_t& key, int64_t& id) {
-  bool valid;
-  if (a.pool) {
-    int p = a.pool[(int64_t)b * a.keep + c / a.block];
-    id = (int64_t)p * a.block + c % a.block;
-    valid = c < ncand && p >= 0 && id < n;
+constexpr int kSelItems = 4;   // consecutive candidates per thread per chunk
+constexpr int kSelUnroll = 4;  // chunks whose loads are in flight together
+
+// Keys (order-preserving u32, 0 = not a candidate) and entry ids of the four
+// candidates c0..c0+3 (c0 a multiple of 4, so they share one pool block).
+__device__ __forceinline__ void load_candidates(const SelectArgs& a, int b, int64_t n, int64_t ncand,
+                                                int64_t c0, bool vec_ok, uint32_t (&key)[kSelItems],
+                                                int64_t (&id)[kSelItems]) {
+  const float* kb = a.keys + (int64_t)b * a.key_stride;
+  float v[kSelItems];
+  if (vec_ok && c0 + kSelItems <= ncand) {
+    const float4 f = *reinterpret_cast<const float4*>(kb + c0);
+    v[0] = f.x;
+    v[1] = f.y;
+    v[2] = f.z;
+    v[3] = f.w;
   } else {
-    id = c;
-    valid = c < ncand;
+#pragma unroll
+    for (int i = 0; i < kSelItems; ++i) v[i] = (c0 + i < ncand) ? kb[c0 + i] : -INFINITY;
   }
-  key = 0u;
-  if (valid) key = score_key(a.keys[(int64_t)b * a.key_stride + (a.key_by_entry ? id : c)]);
+  if (a.pool) {
+    const int p = c0 < ncand ? a.pool[(int64_t)b * a.keep + c0 / 8] : -1;
+#pragma unroll
+    for (int i = 0; i < kSelItems; ++i) {
+      id[i] = (int64_t)p * 8 + (c0 + i) % 8;
+      key[i] = (c0 + i < ncand && p >= 0 && id[i] < n) ? score_key(v[i]) : 0u;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < kSelItems; ++i) {
+      id[i] = c0 + i;
+      key[i] = c0 + i < ncand ? score_key(v[i]) : 0u;
+    }
+  }
 }
 
+// Digit passes over the four bytes of the key, most significant first.  Loads
+// are vectorised and kept 16 deep per thread so a pass is bandwidth-, not
+// latency-bound.  Each warp counts into its own 256-bin histogram (no
+// contention between warps); a warp whose 32 digits agree -- the common case
+// for the leading byte of similar scores -- adds 32 with one atomic.
 template <int NT>
 __global__ void __launch_bounds__(NT) k_select(SelectArgs a) {
-  using Scan = cub::BlockScan<int, NT>;
-  __shared__ typename Scan::TempStorage scan_tmp;
-  __shared__ unsigned hist[256];
+  constexpr int kBins = 256;
+  constexpr int kWarpsSel = NT / 32;
+  constexpr int64_t kChunk = (int64_t)NT * kSelItems;
+  using ScanU = cub::BlockScan<unsigned, NT>;
+  using ScanI = cub::BlockScan<int, NT>;
+  __shared__ union {
+    typename ScanU::TempStorage u;
+    typename ScanI::TempStorage i;
+  } scan_tmp;
+  __shared__ unsigned whist[kWarpsSel][kBins];
   __shared__ unsigned s_valid;
   __shared__ uint32_t s_prefix, s_mask;
-  __shared__ int s_need, s_gt;
+  __shared__ int s_need;
   __shared__ int s_base_eq, s_base_out;
 
   const int b = blockIdx.x;
+  const int tid = threadIdx.x, lane = threadIdx.x % 32, wid = threadIdx.x / 32;
   const int64_t n = max((int64_t)0, min((int64_t)a.n_entries[b], a.n_max));
-  const int64_t ncand = a.pool ? a.ncand_fixed : (a.count_blocks ? cdiv(n, a.block) : n);
+  const int64_t ncand = a.pool ? a.ncand_fixed : (a.count_blocks ? cdiv(n, 8) : n);
+  const int64_t nchunks = cdiv(ncand, kChunk);
+  const bool vec_ok = (a.key_stride % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.keys) & 15) == 0);
   int32_t* out = a.out + (int64_t)b * a.out_stride;
+  unsigned* myhist = whist[wid];
 
-  if (threadIdx.x == 0) {
+  if (tid == 0) {
     s_valid = 0;
     s_prefix = 0;
     s_mask = 0;
-    s_gt = 0;
   }
-  for (int d = threadIdx.x; d < 256; d += NT) hist[d] = 0;
   __syncthreads();
 
-  // count the valid candidates
-  unsigned myvalid = 0;
-  for (int64_t c = threadIdx.x; c < ncand; c += NT) {
-    uint32_t key;
-    int64_t id;
-    select_candidate<NT>(a, b, c, ncand, n, key, id);
-    myvalid += key != 0u;
-  }
-  atomicAdd(&s_valid, myvalid);
-  __syncthreads();
-  if (threadIdx.x == 0) s_need = (int)min((int64_t)a.k, (int64_t)s_valid);
-  __syncthreads();
-  const int need_total = s_need;
-
-  if (need_total > 0) {
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int d = threadIdx.x; d < 256; d += NT) hist[d] = 0;
-      __syncthreads();
-      const uint32_t prefix = s_prefix, mask = s_mask;
-      for (int64_t c = threadIdx.x; c < ncand; c += NT) {
-        uint32_t key;
-        int64_t id;
-        select_candidate<NT>(a, b, c, ncand, n, key, id);
-        if (key != 0u && (key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
-      }
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        int need = s_need;
-        unsigned above = 0;
-        int d = 255;
-        for (; d > 0; --d) {
-          if (above + hist[d] >= (unsigned)need) break;
-          above += hist[d];
+  int need_total = 0;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int d = lane; d < kBins; d += 32) myhist[d] = 0;
+    __syncthreads();
+    const uint32_t prefix = s_prefix, mask = s_mask;
+    unsigned myvalid = 0;
+    for (int64_t g = 0; g < nchunks; g += kSelUnroll) {
+      uint32_t key[kSelUnroll][kSelItems];
+      int64_t id[kSelUnroll][kSelItems];
+#pragma unroll
+      for (int u = 0; u < kSelUnroll; ++u)
+        load_candidates(a, b, n, ncand, (g + u) * kChunk + (int64_t)tid * kSelItems, vec_ok, key[u], id[u]);
+#pragma unroll
+      for (int u = 0; u < kSelUnroll; ++u)
+#pragma unroll
+        for (int i = 0; i < kSelItems; ++i) {
+          const uint32_t kk = key[u][i];
+          myvalid += kk != 0u;
+          const bool in = kk != 0u && (kk & mask) == prefix;
+          const uint32_t d = in ? ((kk >> shift) & 255u) : 0xFFFFFFFFu;
+          const uint32_t d0 = __shfl_sync(0xffffffffu, d, 0);
+          if (__all_sync(0xffffffffu, d == d0)) {
+            if (lane == 0 && d0 != 0xFFFFFFFFu) atomicAdd(&myhist[d0], 32u);
+          } else if (in) {
+            atomicAdd(&myhist[d], 1u);
+          }
         }
-        s_need = need - (int)above;
-        s_gt += (int)above;
-        s_prefix = prefix | ((uint32_t)d << shift);
-        s_mask = mask | (255u << shift);
-      }
-      __syncthreads();
     }
+    if (shift == 24) {
+      myvalid = __reduce_add_sync(0xffffffffu, myvalid);
+      if (lane == 0) atomicAdd(&s_valid, myvalid);
+    }
+    __syncthreads();
+    if (shift == 24) {
+      if (tid == 0) s_need = (int)min((int64_t)a.k, (int64_t)s_valid);
+      __syncthreads();
+      need_total = s_need;
+      if (need_total == 0) break;
+    }
+    // bin totals, then the bin where the count from the top reaches `need`
+    const int need = s_need;
+    unsigned h = 0;
+    const int bin = kBins - 1 - tid;  // thread t holds bin 255 - t (t < 256)
+    if (tid < kBins)
+      for (int w = 0; w < kWarpsSel; ++w) h += whist[w][bin];
+    unsigned cum = h;
+    ScanU(scan_tmp.u).InclusiveSum(cum, cum);
+    if (tid < kBins && cum >= (unsigned)need && cum - h < (unsigned)need) {
+      s_prefix = prefix | ((uint32_t)bin << shift);
+      s_mask = mask | (255u << shift);
+      s_need = need - (int)(cum - h);
+    }
+    __syncthreads();
   }
   const uint32_t T = s_prefix;
-  const int take_eq = s_need;  // entries equal to T to take (lowest indices first)
-  if (threadIdx.x == 0) {
+  const int take_eq = s_need;  // candidates equal to T to take (lowest indices first)
+  if (tid == 0) {
     s_base_eq = 0;
     s_base_out = 0;
   }
   __syncthreads();
 
   if (need_total > 0) {
-    for (int64_t c0 = 0; c0 < ncand; c0 += NT) {
-      int64_t c = c0 + threadIdx.x;
-      uint32_t key = 0u;
-      int64_t id = -1;
-      if (c < ncand) select_candidate<NT>(a, b, c, ncand, n, key, id);
-      int is_eq = (key != 0u && key == T) ? 1 : 0;
-      int eq_rank, eq_total;
-      Scan(scan_tmp).ExclusiveSum(is_eq, eq_rank, eq_total);
+    for (int64_t ch = 0; ch < nchunks; ++ch) {
+      uint32_t key[kSelItems];
+      int64_t id[kSelItems];
+      load_candidates(a, b, n, ncand, ch * kChunk + (int64_t)tid * kSelItems, vec_ok, key, id);
+      int is_eq[kSelItems], eq_rank[kSelItems], take[kSelItems], pos[kSelItems];
+#pragma unroll
+      for (int i = 0; i < kSelItems; ++i) is_eq[i] = (key[i] != 0u && key[i] == T) ? 1 : 0;
+      int eq_total, take_total;
+      ScanI(scan_tmp.i).ExclusiveSum(is_eq, eq_rank, eq_total);
       __syncthreads();
-      int take = (key != 0u && key > T) || (is_eq && s_base_eq + eq_rank < take_eq);
-      int pos, take_total;
-      Scan(scan_tmp).ExclusiveSum(take, pos, take_total);
-      if (take) out[s_base_out + pos] = (int32_t)id;
+      const int base_eq = s_base_eq;
+#pragma unroll
+      for (int i = 0; i < kSelItems; ++i)
+        take[i] = (key[i] != 0u && key[i] > T) || (is_eq[i] && base_eq + eq_rank[i] < take_eq);
+      ScanI(scan_tmp.i).ExclusiveSum(take, pos, take_total);
+      const int base_out = s_base_out;
+#pragma unroll
+      for (int i = 0; i < kSelItems; ++i)
+        if (take[i]) out[base_out + pos[i]] = (int32_t)id[i];
       __syncthreads();
-      if (threadIdx.x == 0) {
+      if (tid == 0) {
         s_base_eq += eq_total;
         s_base_out += take_total;
       }
       __syncthreads();
     }
   }
-  for (int i = (need_total > 0 ? s_base_out : 0) + threadIdx.x; i < a.k; i += NT) out[i] = -1;
+  for (int i = (need_total > 0 ? s_base_out : 0) + tid; i < a.k; i += NT) out[i] = -1;
 }
 
 // ------------------------------------------------------------------ workspace
@@ -220,8 +272,7 @@ extern "C" csa2_status csa2_index_topk(const csa2_kv_planes* kv, int32_t B, cons
     csa2_status rs = launch_scan(kv, B, n_entries, n_max, keep_c, q, w, pool_in, n_blocks_keep, sc,
                                  sc_stride, nullptr, 0, ws, st);
     if (rs != CSA2_OK) return rs;
-    SelectArgs a{sc, sc_stride, n_entries, pool_in, n_blocks_keep, block, 0, 0, keep_c, k,
-                 topk_out, k, n_max};
+    SelectArgs a{sc, sc_stride, n_entries, pool_in, n_blocks_keep, 0, keep_c, k, topk_out, k, n_max};
     k_select<1024><<<B, 1024, 0, st>>>(a);
     return launch_status();
   }
@@ -232,7 +283,7 @@ extern "C" csa2_status csa2_index_topk(const csa2_kv_planes* kv, int32_t B, cons
     csa2_status rs = launch_scan(kv, B, n_entries, n_max, n_max, q, w, nullptr, 0, sc, sc_stride,
                                  nullptr, 0, ws, st);
     if (rs != CSA2_OK) return rs;
-    SelectArgs a{sc, sc_stride, n_entries, nullptr, 0, block, 1, 0, 0, k, topk_out, k, n_max};
+    SelectArgs a{sc, sc_stride, n_entries, nullptr, 0, 0, 0, k, topk_out, k, n_max};
     k_select<1024><<<B, 1024, 0, st>>>(a);
     return launch_status();
   }
@@ -245,14 +296,14 @@ extern "C" csa2_status csa2_index_topk(const csa2_kv_planes* kv, int32_t B, cons
                                L.bmax, L.bmax_cols, ws, st);
   if (rs != CSA2_OK) return rs;
   int32_t* pool = pool_out ? pool_out : L.pool;
-  SelectArgs pa{L.bmax, L.bmax_cols, n_entries, nullptr, 0, block, 1, 1, 0, n_blocks_keep, pool,
-                n_blocks_keep, n_max};
+  SelectArgs pa{L.bmax, L.bmax_cols, n_entries, nullptr, 0, 1, 0, n_blocks_keep, pool, n_blocks_keep,
+                n_max};
   k_select<1024><<<B, 1024, 0, st>>>(pa);
   rs = launch_scan(kv, B, n_entries, n_max, keep_c, q, w, pool, n_blocks_keep, L.scores,
                    L.score_cols, nullptr, 0, ws, st);
   if (rs != CSA2_OK) return rs;
-  SelectArgs ta{L.scores, L.score_cols, n_entries, pool, n_blocks_keep, block, 0, 0, keep_c, k,
-                topk_out, k, n_max};
+  SelectArgs ta{L.scores, L.score_cols, n_entries, pool, n_blocks_keep, 0, keep_c, k, topk_out, k,
+                n_max};
   k_select<1024><<<B, 1024, 0, st>>>(ta);
   return launch_status();
 }

@@ -5,6 +5,11 @@
 
 #include <stdint.h>
 
+// Upper bound (ns) a waiting thread lets the hardware suspend it per try_wait.
+#ifndef CSA2_WAIT_SLEEP_NS
+#define CSA2_WAIT_SLEEP_NS 20000u
+#endif
+
 namespace csa2 {
 namespace ptx {
 
@@ -38,6 +43,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that lets the hardware suspend the thread for up to `ns` nanoseconds
+// (or until the phase completes) instead of returning at once, so waiting warps
+// do not spend issue slots polling.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase of `parity` to complete.  Gives up (returns false) when
 // *abort becomes nonzero or after `budget` clock cycles.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
@@ -45,7 +64,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
+#if CSA2_WAIT_SLEEP_NS > 0
+    if (mbar_try_wait_sleep(bar, parity, CSA2_WAIT_SLEEP_NS)) return true;
+#else
     if (mbar_try_wait(bar, parity)) return true;
+#endif
     if (*abort) return false;
     if (clock64() - t0 > budget) return false;
   }
