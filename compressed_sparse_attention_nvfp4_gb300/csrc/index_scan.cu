@@ -38,10 +38,26 @@ namespace csa2 {
 namespace {
 
 constexpr int kTile = 128;
-constexpr int kStages = 8;
+#ifndef CSA2_SCAN_STAGES
+#define CSA2_SCAN_STAGES 8
+#endif
+constexpr int kStages = CSA2_SCAN_STAGES;  // shared-memory ring depth (tiles in flight)
 constexpr int kAcc = 2;
-constexpr int kWarps = 10;
+// Dequant warps per TMEM lane quarter; each converts 1/kSplit of every row.
+// Epilogue form of sum_h w_h ReLU(x_h): 1 = max then FMA, 0 = two FMAs with |x|.
+#ifndef CSA2_SCAN_RELU_MAX
+#define CSA2_SCAN_RELU_MAX 0
+#endif
+#ifndef CSA2_SCAN_SPLIT
+#define CSA2_SCAN_SPLIT 1
+#endif
+constexpr int kSplit = CSA2_SCAN_SPLIT;
+static_assert(kSplit == 1 || kSplit == 2, "row split must be 1 or 2");
+constexpr int kDequantWarps = 4 * kSplit;
+constexpr int kWordsPerThread = 16 / kSplit;  // 32-bit code words (8 elements each)
+constexpr int kWarps = 2 + kDequantWarps + 4;
 constexpr int kThreads = kWarps * 32;
+constexpr int kEpiWarp0 = 2 + kDequantWarps;
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kDCol0 = 128;
 constexpr long long kWaitBudget = 1LL << 32;  // clock cycles (about 2 s)
@@ -84,13 +100,9 @@ __device__ __forceinline__ void scan_abort(ScanSmem& S, void* ws, int where) {
 
 // f16x2 holding 2^g in both halves, g <= 0 (0 below the f16 subnormal range)
 __device__ __forceinline__ uint32_t pow2_f16x2(int g) {
-  uint32_t h;
-  if (g >= -14)
-    h = (uint32_t)(15 + g) << 10;
-  else if (g >= -24)
-    h = 1u << (g + 24);
-  else
-    h = 0u;
+  const uint32_t normal = (uint32_t)(15 + max(g, -14)) << 10;
+  const uint32_t sub = g >= -24 ? (1u << ((g + 24) & 31)) : 0u;
+  const uint32_t h = g >= -14 ? normal : sub;
   return h | (h << 16);
 }
 
@@ -140,8 +152,7 @@ __device__ __forceinline__ RowInfo row_info(const ScanParams& p, int b, int64_t 
   return ri;
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
-    k_scan_tc(const __grid_constant__ ScanParams p, const __grid_constant__ CUtensorMap map_tile,
+__global__ void __launch_bounds__(kThreads, 2) k_scan_tc(const __grid_constant__ ScanParams p, const __grid_constant__ CUtensorMap map_tile,
               const __grid_constant__ CUtensorMap map_block) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   ScanSmem& S = *reinterpret_cast<ScanSmem*>(smem_raw);
@@ -167,10 +178,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&S.full[s], 1);
-      ptx::mbar_init(&S.empty[s], 4);
+      ptx::mbar_init(&S.empty[s], kDequantWarps);
     }
     for (int a = 0; a < kAcc; ++a) {
-      ptx::mbar_init(&S.a_full[a], 4);
+      ptx::mbar_init(&S.a_full[a], kDequantWarps);
       ptx::mbar_init(&S.mma_done[a], 1);
       ptx::mbar_init(&S.d_free[a], 4);
     }
@@ -270,11 +281,15 @@ __global__ void __launch_bounds__(kThreads, 2)
           ptx::mma_commit(&S.mma_done[a]);
         }
       }
-    } else if (warp < 6) {
+    } else if (warp < kEpiWarp0) {
       // ------------------------------------------------------------ dequant
+      // warps w, w+4, ... share a TMEM lane quarter; part hf converts code
+      // words hf*kWordsPerThread .. +kWordsPerThread-1 of each row
       const int sub = warp % 4;
+      const int hf = (warp - 2) / 4;
       const int r = sub * 32 + lane;
-      const uint32_t lane_addr = tmem + ((uint32_t)(sub * 32) << 16);
+      const uint32_t lane_addr =
+          tmem + ((uint32_t)(sub * 32) << 16) + (uint32_t)(hf * kWordsPerThread * 4);
       for (int i = 0; i < my_tiles; ++i) {
         const int s = i % kStages;
         const uint32_t ph = (uint32_t)(i / kStages) & 1u;
@@ -285,37 +300,39 @@ __global__ void __launch_bounds__(kThreads, 2)
           break;
         }
         const RowInfo ri = row_info(p, b, n, t_begin + i, r, scale_bulk);
-        uint32_t words[16];
+        uint32_t words[kWordsPerThread];
         uint32_t sc = 0;
         if (ri.valid) {
           // 64-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ ((r >> 1) & 3)
           const unsigned char* row = S.codes[s] + r * 64;
           const int sw = (r >> 1) & 3;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c2 = 0; c2 < kWordsPerThread / 4; ++c2) {
+            const int c = hf * (kWordsPerThread / 4) + c2;
             const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * (c ^ sw));
-            words[4 * c + 0] = v.x;
-            words[4 * c + 1] = v.y;
-            words[4 * c + 2] = v.z;
-            words[4 * c + 3] = v.w;
+            words[4 * c2 + 0] = v.x;
+            words[4 * c2 + 1] = v.y;
+            words[4 * c2 + 2] = v.z;
+            words[4 * c2 + 3] = v.w;
           }
           sc = ri.scale_in_smem ? *reinterpret_cast<const uint32_t*>(S.scales[s] + r * 4)
                                 : *reinterpret_cast<const uint32_t*>(scales_b + ri.j * 4);
         } else {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) words[k] = 0u;
+          for (int k = 0; k < kWordsPerThread; ++k) words[k] = 0u;
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&S.empty[s]);
 
-        int e[4];
+        const int e0 = (int)(sc & 0xFFu), e1 = (int)((sc >> 8) & 0xFFu);
+        const int e2 = (int)((sc >> 16) & 0xFFu), e3 = (int)(sc >> 24);
+        const int emax = max(max(e0, e1), max(e2, e3));
+        uint32_t mult[kWordsPerThread / 4];  // one per 32-element block this thread converts
 #pragma unroll
-        for (int c = 0; c < 4; ++c) e[c] = (int)((sc >> (8 * c)) & 0xFFu);
-        const int emax = max(max(e[0], e[1]), max(e[2], e[3]));
-        uint32_t mult[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) mult[c] = pow2_f16x2(e[c] - emax);
-        const float es = ri.valid ? exp2i_f32(emax - 127) : 0.0f;
+        for (int c2 = 0; c2 < kWordsPerThread / 4; ++c2) {
+          const int blk = hf * (kWordsPerThread / 4) + c2;
+          mult[c2] = pow2_f16x2((blk == 0 ? e0 : blk == 1 ? e1 : blk == 2 ? e2 : e3) - emax);
+        }
 
         // A[a] and entry_scale[a] are free once the epilogue released tile i-2
         if (!ptx::mbar_wait_warp(&S.d_free[a], u ^ 1u, abort_flag, kWaitBudget)) {
@@ -324,19 +341,19 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         ptx::tc_fence_after();
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        for (int st32 = 0; st32 < kWordsPerThread / 8; ++st32) {
           uint32_t v[32];
 #pragma unroll
           for (int wi = 0; wi < 8; ++wi) {  // code word -> elements 8*word .. 8*word+7
-            const int word = half * 8 + wi;
+            const int word = st32 * 8 + wi;
             uint32_t h[4];
             e2m1x8_to_f16x2x4(words[word], h);
 #pragma unroll
             for (int k = 0; k < 4; ++k) v[4 * wi + k] = hmul2_bits(h[k], mult[word / 4]);
           }
-          ptx::tmem_st_32x32b_x32(lane_addr + (uint32_t)a * 64u + (uint32_t)half * 32u, v);
+          ptx::tmem_st_32x32b_x32(lane_addr + (uint32_t)a * 64u + (uint32_t)st32 * 32u, v);
         }
-        S.entry_scale[a][r] = es;
+        if (hf == 0) S.entry_scale[a][r] = ri.valid ? exp2i_f32(emax - 127) : 0.0f;
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
@@ -347,9 +364,6 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int sub = warp % 4;
       const int r = sub * 32 + lane;
       const uint32_t lane_addr = tmem + ((uint32_t)(sub * 32) << 16);
-      float wq[32];
-#pragma unroll
-      for (int h = 0; h < 32; ++h) wq[h] = S.wq[h];
       for (int i = 0; i < my_tiles; ++i) {
         const int a = i % kAcc;
         const uint32_t u = (uint32_t)(i / kAcc) & 1u;
@@ -369,10 +383,32 @@ __global__ void __launch_bounds__(kThreads, 2)
 
         const int64_t t = t_begin + i;
         const RowInfo ri = row_info(p, b, n, t, r, scale_bulk);
+#if CSA2_SCAN_RELU_MAX
         float sum = 0.0f;
 #pragma unroll
-        for (int h = 0; h < 32; ++h) sum = fmaf(wq[h], fmaxf(__uint_as_float(acc[h]), 0.0f), sum);
-        const float score = ri.valid ? sum * es : -INFINITY;
+        for (int h = 0; h < 32; ++h) sum = fmaf(S.wq[h], fmaxf(__uint_as_float(acc[h]), 0.0f), sum);
+        const float sp = sum, sa = sum;
+#else
+        // sum_h w_h max(x_h, 0) = (sum_h w_h x_h + sum_h w_h |x_h|) / 2 (|.| is a free
+        // operand modifier, so this stays on the FMA pipe)
+        float sp = 0.0f, sa = 0.0f;
+        const float4* wq4 = reinterpret_cast<const float4*>(S.wq);
+#pragma unroll
+        for (int h4 = 0; h4 < 8; ++h4) {
+          const float4 wv = wq4[h4];
+          const float x0 = __uint_as_float(acc[4 * h4]), x1 = __uint_as_float(acc[4 * h4 + 1]);
+          const float x2 = __uint_as_float(acc[4 * h4 + 2]), x3 = __uint_as_float(acc[4 * h4 + 3]);
+          sp = fmaf(wv.x, x0, sp);
+          sa = fmaf(wv.x, fabsf(x0), sa);
+          sp = fmaf(wv.y, x1, sp);
+          sa = fmaf(wv.y, fabsf(x1), sa);
+          sp = fmaf(wv.z, x2, sp);
+          sa = fmaf(wv.z, fabsf(x2), sa);
+          sp = fmaf(wv.w, x3, sp);
+          sa = fmaf(wv.w, fabsf(x3), sa);
+        }
+#endif
+        const float score = ri.valid ? 0.5f * (sp + sa) * es : -INFINITY;
         const int64_t c = t * kTile + r;  // candidate index
         if (p.scores && c < ncand) p.scores[(int64_t)b * p.score_stride + c] = score;
         if (p.bmax) {
