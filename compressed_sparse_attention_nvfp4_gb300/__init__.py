@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
             "csa2_index_topk": ([pl, i32, vp, i64, vp, vp, i32, ctypes.c_int, i32, i32, vp, vp, vp,
                                  vp, vp, sz, vp], ctypes.c_int),
             "csa2_index_topk_workspace_size": ([i32, i64, i32, i32, i32], sz),
+            "csa2_index_topk_noalloc": ([pl, i32, vp, i64, vp, vp, i32, ctypes.c_int, i32, i32, vp,
+                                         vp, vp, vp], ctypes.c_int),
             "csa2_sparse_attn_decode": ([pl, i32, vp, i32, vp, i32, vp, f32, vp, vp, vp, sz, vp],
                                         ctypes.c_int),
             "csa2_sparse_attn_workspace_size": ([i32, i32, i32], sz),
@@ -175,6 +177,20 @@ def index_topk(planes: Planes, B: int, n_entries, n_max: int, qidx, w, k: int, m
                               k, mode, block, n_blocks_keep, _ptr(pool_in), _ptr(topk_out),
                               _ptr(pool_out), _ptr(scores_out), _ptr(ws), _nbytes(ws),
                               _stream(stream)), "csa2_index_topk")
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def index_topk_noalloc(planes: Planes, B: int, n_entries, n_max: int, qidx, w, k: int, mode: int,
+                       topk_out, block: int = 8, n_blocks_keep: int = 0, pool_in=None, pool_out=None,
+                       stream=None) -> None:
+    """csa2_index_topk without a workspace: scratch lives in a fixed device array
+    of NOALLOC_SCRATCH_BYTES inside the library (for callers that cannot allocate)."""
+    _ok(lib().csa2_index_topk_noalloc(ctypes.byref(planes.c), B, _ptr(n_entries), n_max, _ptr(qidx),
+                                      _ptr(w), k, mode, block, n_blocks_keep, _ptr(pool_in),
+                                      _ptr(topk_out), _ptr(pool_out), _stream(stream)),
+        "csa2_index_topk_noalloc")
 
 
 def sparse_attn_workspace_size(B: int, k: int, n_swa: int) -> int:

@@ -3,6 +3,8 @@
 //   Million-Token Context Intelligence", CSA step 2; "DeepSeek-V4.1-Flash: pushing
 //   the limits of KV cache compression", 4.1), the hierarchical pool of the first
 //   decoder Full layer and the Reindex layers' pool-restricted top-k (4.3).
+#include <atomic>
+
 #include <cub/block/block_scan.cuh>
 
 #include "common.cuh"
@@ -304,6 +306,116 @@ extern "C" csa2_status csa2_index_topk(const csa2_kv_planes* kv, int32_t B, cons
   if (rs != CSA2_OK) return rs;
   SelectArgs ta{L.scores, L.score_cols, n_entries, pool, n_blocks_keep, 0, keep_c, k, topk_out, k,
                 n_max};
+  k_select<1024><<<B, 1024, 0, st>>>(ta);
+  return launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of csa2_index_topk.
+//
+// Some callers cannot allocate device memory at the point where they run the
+// indexer: an inference-engine plugin that is handed only its input and output
+// buffers, a serving loop whose memory is carved up once at start-up with no
+// allocator reachable from the hot path, or a runtime that forbids allocation
+// while it records a replayable command sequence.  For them this entry point
+// keeps its scratch (block maxima, candidate scores, the pool, the error word)
+// in one file-scope device array of CSA2_NOALLOC_SCRATCH_BYTES, which every GPU
+// that loads the library holds until the process exits.  The host code below
+// looks up that array's device address once per device and passes it to the
+// same kernels csa2_index_topk launches.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[CSA2_NOALLOC_SCRATCH_BYTES];
+
+namespace csa2 {
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<void*> g_noalloc_addr[kMaxDevices];
+
+// Device address of the scratch array on the current device (looked up on the
+// first call per device, with that device current).
+csa2_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CSA2_ERR_CUDA;
+  void* p = g_noalloc_addr[dev].load(std::memory_order_acquire);
+  if (!p) {
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return CSA2_ERR_CUDA;
+    g_noalloc_addr[dev].store(p, std::memory_order_release);
+  }
+  *out = p;
+  return CSA2_OK;
+}
+
+}  // namespace
+}  // namespace csa2
+
+extern "C" csa2_status csa2_index_topk_noalloc(const csa2_kv_planes* kv, int32_t B,
+                                               const int32_t* n_entries, int64_t n_max,
+                                               const void* qidx_bf16, const float* w, int32_t k,
+                                               csa2_topk_mode mode, int32_t block,
+                                               int32_t n_blocks_keep, const int32_t* pool_in,
+                                               int32_t* topk_out, int32_t* pool_out,
+                                               csa2_stream stream) {
+  using namespace csa2;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (!planes_ok(kv) || B <= 0 || !n_entries || !qidx_bf16 || !w || !topk_out) return CSA2_ERR_INVALID_ARG;
+  if (k < 1 || k > CSA2_MAX_TOPK || n_max < 0 || n_max > kv->seq_stride || n_max >= ((int64_t)1 << 31))
+    return CSA2_ERR_INVALID_ARG;
+  if (mode != CSA2_TOPK_FLAT && mode != CSA2_TOPK_HIER_BUILD && mode != CSA2_TOPK_POOL)
+    return CSA2_ERR_INVALID_ARG;
+  if (mode != CSA2_TOPK_FLAT) {
+    if (block != 8) return CSA2_ERR_UNSUPPORTED;
+    if (n_blocks_keep < 1 || (int64_t)n_blocks_keep * block > 16384) return CSA2_ERR_INVALID_ARG;
+    if (mode == CSA2_TOPK_POOL && !pool_in) return CSA2_ERR_INVALID_ARG;
+  } else {
+    block = 8;
+    n_blocks_keep = 0;
+  }
+  if (!aligned(qidx_bf16, 16) || !aligned(w, 16)) return CSA2_ERR_INVALID_ARG;
+
+  // scratch layout of this mode: [error word | scores | block maxima | pool]
+  const int64_t keep_c = (int64_t)n_blocks_keep * block;
+  const int64_t score_cols = (int64_t)align_up((size_t)(mode == CSA2_TOPK_FLAT ? n_max : keep_c), 64);
+  const int64_t bmax_cols = mode == CSA2_TOPK_HIER_BUILD ? (int64_t)align_up((size_t)cdiv(n_max, 8), 64) : 0;
+  const size_t s_bytes = align_up((size_t)B * score_cols * 4, 256);
+  const size_t b_bytes = align_up((size_t)B * bmax_cols * 4, 256);
+  const size_t p_bytes = mode == CSA2_TOPK_HIER_BUILD ? align_up((size_t)B * n_blocks_keep * 4, 256) : 0;
+  if (kWsHeader + s_bytes + b_bytes + p_bytes > (size_t)CSA2_NOALLOC_SCRATCH_BYTES) return CSA2_ERR_WORKSPACE;
+
+  void* ws = nullptr;
+  csa2_status rs = noalloc_scratch(&ws);
+  if (rs != CSA2_OK) return rs;
+  char* base = (char*)ws;
+  float* scores = (float*)(base + kWsHeader);
+  float* bmax = (float*)(base + kWsHeader + s_bytes);
+  int32_t* pool_tmp = (int32_t*)(base + kWsHeader + s_bytes + b_bytes);
+  if (reset_error(ws, st) != CSA2_OK) return CSA2_ERR_CUDA;  // the error word starts at zero
+  const uint16_t* q = (const uint16_t*)qidx_bf16;
+
+  if (mode == CSA2_TOPK_POOL) {
+    rs = launch_scan(kv, B, n_entries, n_max, keep_c, q, w, pool_in, n_blocks_keep, scores, score_cols,
+                     nullptr, 0, ws, st);
+    if (rs != CSA2_OK) return rs;
+    SelectArgs a{scores, score_cols, n_entries, pool_in, n_blocks_keep, 0, keep_c, k, topk_out, k, n_max};
+    k_select<1024><<<B, 1024, 0, st>>>(a);
+    return launch_status();
+  }
+  if (mode == CSA2_TOPK_FLAT) {
+    rs = launch_scan(kv, B, n_entries, n_max, n_max, q, w, nullptr, 0, scores, score_cols, nullptr, 0, ws,
+                     st);
+    if (rs != CSA2_OK) return rs;
+    SelectArgs a{scores, score_cols, n_entries, nullptr, 0, 0, 0, k, topk_out, k, n_max};
+    k_select<1024><<<B, 1024, 0, st>>>(a);
+    return launch_status();
+  }
+  rs = launch_scan(kv, B, n_entries, n_max, n_max, q, w, nullptr, 0, nullptr, 0, bmax, bmax_cols, ws, st);
+  if (rs != CSA2_OK) return rs;
+  int32_t* pool = pool_out ? pool_out : pool_tmp;
+  SelectArgs pa{bmax, bmax_cols, n_entries, nullptr, 0, 1, 0, n_blocks_keep, pool, n_blocks_keep, n_max};
+  k_select<1024><<<B, 1024, 0, st>>>(pa);
+  rs = launch_scan(kv, B, n_entries, n_max, keep_c, q, w, pool, n_blocks_keep, scores, score_cols, nullptr,
+                   0, ws, st);
+  if (rs != CSA2_OK) return rs;
+  SelectArgs ta{scores, score_cols, n_entries, pool, n_blocks_keep, 0, keep_c, k, topk_out, k, n_max};
   k_select<1024><<<B, 1024, 0, st>>>(ta);
   return launch_status();
 }

@@ -156,6 +156,34 @@ csa2_status csa2_index_topk(const csa2_kv_planes* kv, int32_t B, const int32_t* 
 size_t csa2_index_topk_workspace_size(int32_t B, int64_t n_max, int32_t k, int32_t block,
                                       int32_t n_blocks_keep);
 
+/* Allocation-free form of csa2_index_topk (the design pages have no counterpart;
+ * this exists for the library's users).  Some callers cannot allocate device
+ * memory where they run the indexer -- a plugin handed only its input and output
+ * buffers, a serving loop whose memory is partitioned once at start-up with no
+ * allocator on the hot path.  This entry point takes the same inputs and outputs
+ * (no scores_out, no workspace) and keeps its scratch in a file-scope device
+ * array of CSA2_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds
+ * until the process exits.  It never allocates or frees device memory.
+ *  - Limit: the scratch needed is 256 B + 4*B*(round64(cand) + round64(nb)) +
+ *    4*B*keep rounded to 256 B per part, with cand = n_max (FLAT) or
+ *    n_blocks_keep*block (HIER_BUILD, POOL) and nb = ceil(n_max/8) (HIER_BUILD
+ *    only, plus the pool when pool_out is NULL); a request beyond
+ *    CSA2_NOALLOC_SCRATCH_BYTES returns CSA2_ERR_WORKSPACE before any launch.
+ *    (Batch 32 at a 1,048,576-entry context in HIER_BUILD needs about 18 MB.)
+ *  - The first call on a device looks up the array's device address with that
+ *    device current; make that first call before any stream capture.
+ *  - All calls share the one array and it keeps the last call's contents; the
+ *    call clears the part that must start at zero.  Calls that overlap on the
+ *    GPU (other streams, other threads) race on it and must be serialised.
+ *  - Device-side error reports go to the array's error word and are not
+ *    readable through csa2_check; results equal csa2_index_topk's. */
+#define CSA2_NOALLOC_SCRATCH_BYTES (32u << 20)
+csa2_status csa2_index_topk_noalloc(const csa2_kv_planes* kv, int32_t B, const int32_t* n_entries,
+                                    int64_t n_max, const void* qidx_bf16, const float* w, int32_t k,
+                                    csa2_topk_mode mode, int32_t block, int32_t n_blocks_keep,
+                                    const int32_t* pool_in, int32_t* topk_out, int32_t* pool_out,
+                                    csa2_stream stream);
+
 /* ------------------------------------------------------- sparse attention */
 
 /* Sparse MQA decode over the selected entries joined with the sliding window:
