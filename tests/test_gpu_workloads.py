@@ -1,0 +1,202 @@
+"""Parity on the decode workloads, in the launch configuration the benchmark
+uses: the single-query 4K workload in full, the batch-64 encoder workload (one
+index pass shared by six attention passes) and the batch-32 1M-context
+hierarchical workload at full size, checked on sampled queries whose whole
+caches the oracle regenerates from the same seeded generator."""
+import math
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+import pytest
+
+from gpu_common import csa2, require_gpu, to_dev, torch
+from parity import check_attention, check_topk
+from synth import workloads as W
+
+pytestmark = pytest.mark.gpu
+SCALE = 1.0 / math.sqrt(512)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def oracle_planes(oracle, seed, f, B, N, b, hot_prob=0.0, hotvec=None, chunk=1 << 16):
+    """The oracle's encoding of sequence b's cache (generated on the host)."""
+    kvc = np.empty((N, 256), np.uint8)
+    kvs = np.empty((N, 32), np.uint8)
+    ixc = np.empty((N, 64), np.uint8)
+    ixs = np.empty((N, 4), np.uint8)
+
+    def enc(j0):
+        cnt = min(chunk, N - j0)
+        a = oracle.quantize_main(W.main_latents(seed, f, B, N, b, j0, cnt))
+        c = oracle.quantize_index(W.index_latents(seed, f, B, N, b, j0, cnt, hot_prob, hotvec))
+        return j0, cnt, a, c
+
+    with ThreadPoolExecutor(16) as ex:
+        for j0, cnt, (c1, s1), (c2, s2) in ex.map(enc, range(0, N, chunk)):
+            kvc[j0:j0 + cnt], kvs[j0:j0 + cnt] = c1, s1
+            ixc[j0:j0 + cnt], ixs[j0:j0 + cnt] = c2, s2
+    return kvc, kvs, ixc, ixs
+
+
+def gpu_decode(wl, planes, layers_q, layers_swa, qd, wd, hier=False, keep=2048):
+    B, N, k = wl.B, wl.N, wl.k
+    ne = torch.full((B,), N, dtype=torch.int32, device="cuda")
+    topk = torch.empty((B, k), dtype=torch.int32, device="cuda")
+    pool = torch.empty((B, keep), dtype=torch.int32, device="cuda")
+    ws = csa2.workspace(csa2.index_topk_workspace_size(B, N, k, 8, keep if hier else 0))
+    if hier:
+        csa2.index_topk(planes, B, ne, N, qd, wd, k, csa2.TOPK_HIER_BUILD, topk, ws, 8, keep, pool_out=pool)
+    else:
+        csa2.index_topk(planes, B, ne, N, qd, wd, k, csa2.TOPK_FLAT, topk, ws)
+    assert csa2.check(ws)[0] == 0
+    outs = []
+    wsa = csa2.workspace(csa2.sparse_attn_workspace_size(B, k, wl.n_swa))
+    for qa, swa in zip(layers_q, layers_swa):
+        out = torch.empty((B, 64, 512), dtype=torch.float32, device="cuda")
+        csa2.sparse_attn_decode(planes, B, topk, k, swa, wl.n_swa, qa, SCALE, out, wsa)
+        assert csa2.check(wsa)[0] == 0
+        outs.append(out.cpu().numpy())
+    return topk.cpu().numpy(), pool.cpu().numpy(), outs
+
+
+def test_single_query_4k(oracle_mod):
+    """B=1, N=4096, FLAT top-512 + 64x512 attention over 512 + 128 rows: every output."""
+    from compressed_sparse_attention_nvfp4_gb300 import workload as WL
+
+    wl = W.SINGLE_4K
+    planes = csa2.Planes.empty(wl.B, wl.N)
+    WL.fill_planes(planes, wl.seed, 0, wl.B, wl.N)
+    qd, wd, q, w = WL.index_query_dev(wl.seed, 0, wl.B)
+    qa_d, qa = WL.attn_query_dev(wl.seed, 0, wl.B)
+    swa_d = WL.swa_dev(wl.seed, 0, wl.B)
+    topk, _, outs = gpu_decode(wl, planes, [qa_d], [swa_d], qd, wd)
+    kvc, kvs, ixc, ixs = oracle_planes(oracle_mod, wl.seed, 0, wl.B, wl.N, 0)
+    s = oracle_mod.index_scores(ixc, ixs, q[0], w[0])
+    check_topk(topk[0], s, wl.k, what="4k topk")
+    sel = oracle_mod.topk(s, wl.k)
+    ref, _ = oracle_mod.attention(kvc, kvs, sel, W.swa_rows(wl.seed, 0, 1)[0], qa[0], SCALE)
+    check_attention(outs[0], ref[None])
+
+
+def test_encoder_batch64_six_attention_passes(oracle_mod):
+    """B=64, N=32,768 (65,536 tokens at m=2): one FLAT index pass, six attention
+    passes (Full + 5 Reuse) each with its own q and window; queries 0 and 63 checked."""
+    from compressed_sparse_attention_nvfp4_gb300 import workload as WL
+
+    wl = W.ENCODER_B64
+    planes = csa2.Planes.empty(wl.B, wl.N)
+    WL.fill_planes(planes, wl.seed, 0, wl.B, wl.N)
+    qd, wd, q, w = WL.index_query_dev(wl.seed, 0, wl.B)
+    qs = [WL.attn_query_dev(wl.seed, l, wl.B) for l in range(wl.n_attn)]
+    swas = [WL.swa_dev(wl.seed, l, wl.B) for l in range(wl.n_attn)]
+    topk, _, outs = gpu_decode(wl, planes, [a for a, _ in qs], swas, qd, wd)
+    for b in (0, 63):
+        kvc, kvs, ixc, ixs = oracle_planes(oracle_mod, wl.seed, 0, wl.B, wl.N, b)
+        s = oracle_mod.index_scores(ixc, ixs, q[b], w[b])
+        check_topk(topk[b], s, wl.k, what=f"encoder topk[{b}]")
+        sel = oracle_mod.topk(s, wl.k)
+        for l in range(wl.n_attn):
+            sw = W.swa_rows(wl.seed, l, wl.B)[b]
+            ref, _ = oracle_mod.attention(kvc, kvs, sel, sw, qs[l][1][b], SCALE)
+            check_attention(outs[l][b:b + 1], ref[None], what=f"encoder attn[{b}, layer {l}]")
+
+
+def test_decoder_1m_hierarchical_full_size(oracle_mod):
+    """B=32 at 1,048,576 entries, HIER_BUILD (131,072 blocks -> 2,048 -> top-512) +
+    attention: the benchmark's configuration; queries 0 and 31 checked against the
+    oracle over their whole caches (pool, top-k and attention)."""
+    from compressed_sparse_attention_nvfp4_gb300 import workload as WL
+
+    wl = W.DECODER_1M
+    planes = csa2.Planes.empty(wl.B, wl.N)
+    qd, wd, q, w = WL.index_query_dev(wl.seed, 0, wl.B)
+    hv = W.hot_vectors(q, w, wl.hot_gain)
+    WL.fill_planes(planes, wl.seed, 0, wl.B, wl.N, hot_prob=wl.hot_prob, hotvecs=hv)
+    qa_d, qa = WL.attn_query_dev(wl.seed, 0, wl.B)
+    swa_d = WL.swa_dev(wl.seed, 0, wl.B)
+    topk, pool, outs = gpu_decode(wl, planes, [qa_d], [swa_d], qd, wd, hier=True)
+    del planes
+    torch.cuda.empty_cache()
+    for b in (0, 31):
+        kvc, kvs, ixc, ixs = oracle_planes(oracle_mod, wl.seed, 0, wl.B, wl.N, b, wl.hot_prob, hv[b])
+        s = oracle_mod.index_scores(ixc, ixs, q[b], w[b])
+        bm = oracle_mod.block_max(s, 8)
+        check_topk(pool[b], bm, 2048, what=f"1M pool[{b}]")
+        check_topk(topk[b], s, wl.k, what=f"1M topk[{b}]")
+        sel = oracle_mod.pool_topk(s, oracle_mod.hier_pool(bm, 2048), 8, wl.k)
+        ref, _ = oracle_mod.attention(kvc, kvs, sel, W.swa_rows(wl.seed, 0, wl.B)[b], qa[b], SCALE)
+        check_attention(outs[0][b:b + 1], ref[None], what=f"1M attn[{b}]")
+
+
+def test_v41_forty_layer_step_reduced(oracle_mod):
+    """The 40-layer decode step (SWA-only, Full, Reuse, Reindex layers) at batch 2
+    and a 16,384-token context (8,192 encoder entries at m=2, 16,384 decoder entries
+    at m=1, a 256-block pool): every index layer and all 40 outputs vs the oracle
+    following the same schedule with its own selections."""
+    from compressed_sparse_attention_nvfp4_gb300 import schedule as SCH
+    from compressed_sparse_attention_nvfp4_gb300 import workload as WL
+
+    seed, B, T, keep, k = 4, 2, 16384, 256, 512
+    t = csa2.v41_layer_table()
+    full = [l for l in range(40) if t["mode"][l] == csa2.LAYER_FULL]
+    n_of = {f: T // t["m"][f] for f in full}
+    kv, ne, nm = {}, {}, {}
+    for f in full:
+        kv[f] = csa2.Planes.empty(B, n_of[f])
+        WL.fill_planes(kv[f], seed, f, B, n_of[f])
+        ne[f] = torch.full((B,), n_of[f], dtype=torch.int32, device="cuda")
+        nm[f] = n_of[f]
+    qidx, w, q, swa, out, qh, wh, qah = {}, {}, {}, {}, {}, {}, {}, {}
+    for l in range(40):
+        if t["mode"][l] in (csa2.LAYER_FULL, csa2.LAYER_REINDEX):
+            qidx[l], w[l], qh[l], wh[l] = WL.index_query_dev(seed, l, B)
+        q[l], qah[l] = WL.attn_query_dev(seed, l, B)
+        swa[l] = WL.swa_dev(seed, l, B)
+        out[l] = torch.empty((B, 64, 512), dtype=torch.float32, device="cuda")
+    buf = SCH.StepBuffers(B=B, kv=kv, n_entries=ne, n_max=nm, qidx=qidx, w=w, q=q, swa=swa, out=out,
+                          k=k, n_blocks_keep=keep)
+    SCH.allocate_scratch(buf)
+    calls = SCH.run_step(buf)
+    torch.cuda.synchronize()
+    assert calls == 40 + 8  # 40 attention calls, 8 indexer calls
+    assert csa2.check(buf.ws_index)[0] == 0 and csa2.check(buf.ws_attn)[0] == 0
+    gtopk = {l: buf.topk[l].cpu().numpy() for l in buf.topk}
+    gpool = buf.pool[20].cpu().numpy()
+    gout = {l: out[l].cpu().numpy() for l in range(40)}
+
+    for b in range(B):
+        planes = {f: oracle_planes(oracle_mod, seed, f, B, n_of[f], b) for f in full}
+        sel = {}
+        opool = None
+        for l in range(40):
+            mode = t["mode"][l]
+            if mode == csa2.LAYER_SWA:
+                sel_l = np.zeros(0, np.int32)
+            else:
+                f = t["kv_src"][l]
+                kvc, kvs, ixc, ixs = planes[f]
+                if mode in (csa2.LAYER_FULL, csa2.LAYER_REINDEX):
+                    s = oracle_mod.index_scores(ixc, ixs, qh[l][b], wh[l][b])
+                    if mode == csa2.LAYER_FULL and t["m"][l] == 2:
+                        check_topk(gtopk[l][b], s, k, what=f"L{l} flat[{b}]")
+                        sel[l] = oracle_mod.topk(s, k)
+                    else:
+                        if mode == csa2.LAYER_FULL:
+                            bm = oracle_mod.block_max(s, 8)
+                            check_topk(gpool[b], bm, keep, what=f"L{l} pool[{b}]")
+                            opool = oracle_mod.hier_pool(bm, keep)
+                        valid = np.zeros(n_of[f], bool)
+                        for u in gpool[b][gpool[b] >= 0]:
+                            valid[8 * u:8 * u + 8] = True
+                        check_topk(gtopk[l][b], s, k, valid=valid, what=f"L{l} in-pool[{b}]")
+                        sel[l] = oracle_mod.pool_topk(s, opool, 8, k)
+                sel_l = sel[t["topk_src"][l]]
+                kv_o = (kvc, kvs)
+            if mode == csa2.LAYER_SWA:
+                kv_o = planes[full[0]][:2]
+            ref, _ = oracle_mod.attention(kv_o[0], kv_o[1], sel_l, W.swa_rows(seed, l, B)[b], qah[l][b], SCALE)
+            check_attention(gout[l][b:b + 1], ref[None], what=f"L{l} attn[{b}]")
