@@ -5,12 +5,15 @@
 //   decoder Full layer and the Reindex layers' pool-restricted top-k (4.3).
 #include <atomic>
 
+#include <cooperative_groups.h>
 #include <cub/block/block_scan.cuh>
 
 #include "common.cuh"
 #include "index_scan.cuh"
 
 namespace csa2 {
+
+namespace cg = cooperative_groups;
 
 // ------------------------------------------------------------------ selection
 // Radix select of the k largest keys of one query (one CTA per query), then an
@@ -70,13 +73,21 @@ __device__ __forceinline__ void load_candidates(const SelectArgs& a, int b, int6
   }
 }
 
-// Digit passes over the four bytes of the key, most significant first.  Loads
-// are vectorised and kept 16 deep per thread so a pass is bandwidth-, not
-// latency-bound.  Each warp counts into its own 256-bin histogram (no
-// contention between warps); a warp whose 32 digits agree -- the common case
-// for the leading byte of similar scores -- adds 32 with one atomic.
-template <int NT>
-__global__ void __launch_bounds__(NT) k_select(SelectArgs a) {
+// Digit passes over the four bytes of the key, most significant first, by a
+// cluster of kSelCluster CTAs per query: CTA r owns the r-th contiguous slice of
+// the candidates.  Each pass, every warp counts its keys into its own 256-bin
+// histogram (a warp whose 32 digits agree adds 32 with one atomic), the CTA sums
+// its warps, and every CTA of the cluster reads the other CTAs' sums through
+// distributed shared memory, so all of them choose the same digit without a
+// round trip through global memory.  The ordered collect uses the per-CTA
+// counts of keys above / equal to the threshold the same way to place each
+// CTA's output.  Loads are vectorised, 16 keys in flight per thread.
+constexpr int kSelCluster = 8;
+constexpr int kSelThreads = 256;
+
+__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads)
+    k_select(SelectArgs a) {
+  constexpr int NT = kSelThreads;
   constexpr int kBins = 256;
   constexpr int kWarpsSel = NT / 32;
   constexpr int64_t kChunk = (int64_t)NT * kSelItems;
@@ -87,22 +98,28 @@ __global__ void __launch_bounds__(NT) k_select(SelectArgs a) {
     typename ScanI::TempStorage i;
   } scan_tmp;
   __shared__ unsigned whist[kWarpsSel][kBins];
-  __shared__ unsigned s_valid;
+  __shared__ unsigned chist[kBins];   // this CTA's histogram, read by the whole cluster
+  __shared__ unsigned cvalid;         // this CTA's valid-candidate count
+  __shared__ int ccount[2];           // this CTA's keys > T and == T
   __shared__ uint32_t s_prefix, s_mask;
-  __shared__ int s_need;
+  __shared__ int s_need, s_total_valid;
   __shared__ int s_base_eq, s_base_out;
 
-  const int b = blockIdx.x;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int b = blockIdx.x / kSelCluster;
   const int tid = threadIdx.x, lane = threadIdx.x % 32, wid = threadIdx.x / 32;
   const int64_t n = max((int64_t)0, min((int64_t)a.n_entries[b], a.n_max));
   const int64_t ncand = a.pool ? a.ncand_fixed : (a.count_blocks ? cdiv(n, 8) : n);
-  const int64_t nchunks = cdiv(ncand, kChunk);
+  const int64_t per = (int64_t)align_up((size_t)cdiv(ncand, kSelCluster), kSelItems);
+  const int64_t lo = min(ncand, rank * per), hi = min(ncand, lo + per);
+  const int64_t nchunks = cdiv(hi - lo, kChunk);
   const bool vec_ok = (a.key_stride % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.keys) & 15) == 0);
   int32_t* out = a.out + (int64_t)b * a.out_stride;
   unsigned* myhist = whist[wid];
 
   if (tid == 0) {
-    s_valid = 0;
+    cvalid = 0;
     s_prefix = 0;
     s_mask = 0;
   }
@@ -118,8 +135,15 @@ __global__ void __launch_bounds__(NT) k_select(SelectArgs a) {
       uint32_t key[kSelUnroll][kSelItems];
       int64_t id[kSelUnroll][kSelItems];
 #pragma unroll
-      for (int u = 0; u < kSelUnroll; ++u)
-        load_candidates(a, b, n, ncand, (g + u) * kChunk + (int64_t)tid * kSelItems, vec_ok, key[u], id[u]);
+      for (int u = 0; u < kSelUnroll; ++u) {
+        const int64_t c0 = lo + (g + u) * kChunk + (int64_t)tid * kSelItems;
+        if (c0 < hi) {
+          load_candidates(a, b, n, hi, c0, vec_ok, key[u], id[u]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < kSelItems; ++i) key[u][i] = 0u;
+        }
+      }
 #pragma unroll
       for (int u = 0; u < kSelUnroll; ++u)
 #pragma unroll
@@ -138,43 +162,90 @@ __global__ void __launch_bounds__(NT) k_select(SelectArgs a) {
     }
     if (shift == 24) {
       myvalid = __reduce_add_sync(0xffffffffu, myvalid);
-      if (lane == 0) atomicAdd(&s_valid, myvalid);
+      if (lane == 0) atomicAdd(&cvalid, myvalid);
     }
     __syncthreads();
+    {  // this CTA's bin totals (thread t <-> bin 255 - t)
+      unsigned h = 0;
+      const int bin = kBins - 1 - tid;
+      for (int w = 0; w < kWarpsSel; ++w) h += whist[w][bin];
+      chist[bin] = h;
+    }
+    cluster.sync();
     if (shift == 24) {
-      if (tid == 0) s_need = (int)min((int64_t)a.k, (int64_t)s_valid);
+      if (tid == 0) {
+        unsigned tv = 0;
+        for (int r = 0; r < kSelCluster; ++r) tv += *cluster.map_shared_rank(&cvalid, r);
+        s_total_valid = (int)tv;
+        s_need = (int)min((int64_t)a.k, (int64_t)tv);
+      }
       __syncthreads();
       need_total = s_need;
-      if (need_total == 0) break;
+      if (need_total == 0) break;  // uniform across the cluster
     }
-    // bin totals, then the bin where the count from the top reaches `need`
     const int need = s_need;
+    const int bin = kBins - 1 - tid;
     unsigned h = 0;
-    const int bin = kBins - 1 - tid;  // thread t holds bin 255 - t (t < 256)
-    if (tid < kBins)
-      for (int w = 0; w < kWarpsSel; ++w) h += whist[w][bin];
+    for (int r = 0; r < kSelCluster; ++r) h += *cluster.map_shared_rank(&chist[bin], r);
     unsigned cum = h;
     ScanU(scan_tmp.u).InclusiveSum(cum, cum);
-    if (tid < kBins && cum >= (unsigned)need && cum - h < (unsigned)need) {
+    if (cum >= (unsigned)need && cum - h < (unsigned)need) {
       s_prefix = prefix | ((uint32_t)bin << shift);
       s_mask = mask | (255u << shift);
       s_need = need - (int)(cum - h);
     }
-    __syncthreads();
+    cluster.sync();  // every CTA has read the histograms before they are reused
   }
   const uint32_t T = s_prefix;
   const int take_eq = s_need;  // candidates equal to T to take (lowest indices first)
-  if (tid == 0) {
-    s_base_eq = 0;
-    s_base_out = 0;
-  }
-  __syncthreads();
 
   if (need_total > 0) {
+    // counts of this CTA's keys above and equal to T, shared with the cluster
+    int gt = 0, eq = 0;
+    for (int64_t c0 = lo + (int64_t)tid * kSelItems; c0 < hi; c0 += kChunk) {
+      uint32_t key[kSelItems];
+      int64_t id[kSelItems];
+      load_candidates(a, b, n, hi, c0, vec_ok, key, id);
+#pragma unroll
+      for (int i = 0; i < kSelItems; ++i) {
+        gt += key[i] != 0u && key[i] > T;
+        eq += key[i] != 0u && key[i] == T;
+      }
+    }
+    gt = __reduce_add_sync(0xffffffffu, (unsigned)gt);
+    eq = __reduce_add_sync(0xffffffffu, (unsigned)eq);
+    if (tid == 0) ccount[0] = ccount[1] = 0;
+    __syncthreads();
+    if (lane == 0) {
+      atomicAdd(&ccount[0], gt);
+      atomicAdd(&ccount[1], eq);
+    }
+    cluster.sync();
+    if (tid == 0) {
+      int eq_before = 0, out_before = 0;
+      for (int r = 0; r < rank; ++r) {
+        const int* cc = cluster.map_shared_rank(ccount, r);
+        const int g_r = cc[0], e_r = cc[1];
+        out_before += g_r + max(0, min(e_r, take_eq - eq_before));
+        eq_before += e_r;
+      }
+      s_base_eq = eq_before;
+      s_base_out = out_before;
+    }
+    __syncthreads();
     for (int64_t ch = 0; ch < nchunks; ++ch) {
       uint32_t key[kSelItems];
       int64_t id[kSelItems];
-      load_candidates(a, b, n, ncand, ch * kChunk + (int64_t)tid * kSelItems, vec_ok, key, id);
+      const int64_t c0 = lo + ch * kChunk + (int64_t)tid * kSelItems;
+      if (c0 < hi) {
+        load_candidates(a, b, n, hi, c0, vec_ok, key, id);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kSelItems; ++i) {
+          key[i] = 0u;
+          id[i] = -1;
+        }
+      }
       int is_eq[kSelItems], eq_rank[kSelItems], take[kSelItems], pos[kSelItems];
 #pragma unroll
       for (int i = 0; i < kSelItems; ++i) is_eq[i] = (key[i] != 0u && key[i] == T) ? 1 : 0;
@@ -198,7 +269,15 @@ __global__ void __launch_bounds__(NT) k_select(SelectArgs a) {
       __syncthreads();
     }
   }
-  for (int i = (need_total > 0 ? s_base_out : 0) + tid; i < a.k; i += NT) out[i] = -1;
+  if (rank == kSelCluster - 1) {  // padding after the last selected id
+    const int taken = need_total > 0 ? need_total : 0;
+    for (int i = taken + tid; i < a.k; i += NT) out[i] = -1;
+  }
+  cluster.sync();  // no CTA leaves while another may still read its shared memory
+}
+
+void launch_select(const SelectArgs& a, int B, cudaStream_t st) {
+  k_select<<<B * kSelCluster, kSelThreads, 0, st>>>(a);
 }
 
 // ------------------------------------------------------------------ workspace
@@ -275,7 +354,7 @@ extern "C" csa2_status csa2_index_topk(const csa2_kv_planes* kv, int32_t B, cons
                                  sc_stride, nullptr, 0, ws, st);
     if (rs != CSA2_OK) return rs;
     SelectArgs a{sc, sc_stride, n_entries, pool_in, n_blocks_keep, 0, keep_c, k, topk_out, k, n_max};
-    k_select<1024><<<B, 1024, 0, st>>>(a);
+    launch_select(a, B, st);
     return launch_status();
   }
 
@@ -286,7 +365,7 @@ extern "C" csa2_status csa2_index_topk(const csa2_kv_planes* kv, int32_t B, cons
                                  nullptr, 0, ws, st);
     if (rs != CSA2_OK) return rs;
     SelectArgs a{sc, sc_stride, n_entries, nullptr, 0, 0, 0, k, topk_out, k, n_max};
-    k_select<1024><<<B, 1024, 0, st>>>(a);
+    launch_select(a, B, st);
     return launch_status();
   }
 
@@ -300,13 +379,13 @@ extern "C" csa2_status csa2_index_topk(const csa2_kv_planes* kv, int32_t B, cons
   int32_t* pool = pool_out ? pool_out : L.pool;
   SelectArgs pa{L.bmax, L.bmax_cols, n_entries, nullptr, 0, 1, 0, n_blocks_keep, pool, n_blocks_keep,
                 n_max};
-  k_select<1024><<<B, 1024, 0, st>>>(pa);
+  launch_select(pa, B, st);
   rs = launch_scan(kv, B, n_entries, n_max, keep_c, q, w, pool, n_blocks_keep, L.scores,
                    L.score_cols, nullptr, 0, ws, st);
   if (rs != CSA2_OK) return rs;
   SelectArgs ta{L.scores, L.score_cols, n_entries, pool, n_blocks_keep, 0, keep_c, k, topk_out, k,
                 n_max};
-  k_select<1024><<<B, 1024, 0, st>>>(ta);
+  launch_select(ta, B, st);
   return launch_status();
 }
 
@@ -396,7 +475,7 @@ extern "C" csa2_status csa2_index_topk_noalloc(const csa2_kv_planes* kv, int32_t
                      nullptr, 0, ws, st);
     if (rs != CSA2_OK) return rs;
     SelectArgs a{scores, score_cols, n_entries, pool_in, n_blocks_keep, 0, keep_c, k, topk_out, k, n_max};
-    k_select<1024><<<B, 1024, 0, st>>>(a);
+    launch_select(a, B, st);
     return launch_status();
   }
   if (mode == CSA2_TOPK_FLAT) {
@@ -404,18 +483,18 @@ extern "C" csa2_status csa2_index_topk_noalloc(const csa2_kv_planes* kv, int32_t
                      st);
     if (rs != CSA2_OK) return rs;
     SelectArgs a{scores, score_cols, n_entries, nullptr, 0, 0, 0, k, topk_out, k, n_max};
-    k_select<1024><<<B, 1024, 0, st>>>(a);
+    launch_select(a, B, st);
     return launch_status();
   }
   rs = launch_scan(kv, B, n_entries, n_max, n_max, q, w, nullptr, 0, nullptr, 0, bmax, bmax_cols, ws, st);
   if (rs != CSA2_OK) return rs;
   int32_t* pool = pool_out ? pool_out : pool_tmp;
   SelectArgs pa{bmax, bmax_cols, n_entries, nullptr, 0, 1, 0, n_blocks_keep, pool, n_blocks_keep, n_max};
-  k_select<1024><<<B, 1024, 0, st>>>(pa);
+  launch_select(pa, B, st);
   rs = launch_scan(kv, B, n_entries, n_max, keep_c, q, w, pool, n_blocks_keep, scores, score_cols, nullptr,
                    0, ws, st);
   if (rs != CSA2_OK) return rs;
   SelectArgs ta{scores, score_cols, n_entries, pool, n_blocks_keep, 0, keep_c, k, topk_out, k, n_max};
-  k_select<1024><<<B, 1024, 0, st>>>(ta);
+  launch_select(ta, B, st);
   return launch_status();
 }
