@@ -154,6 +154,17 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+      "[%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16, issued by one thread.
 __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                            uint32_t idesc, uint32_t accumulate) {
@@ -174,6 +185,65 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uin
       : "memory");
 }
 
+// D[tmem] (+)= (A[tmem] * 2^sfA) * (B[smem desc] * 2^sfB)^T, block-scaled
+// kind::mxf8f6f4 with one UE8M0 scale per row and per 32-element K step
+// (scale_vec::1X).  Tensor-memory layouts (measured on sm_103a):
+//   A (8-bit containers, K-major): element k of row m at lane m, column k/4,
+//     byte k%4; an E2M1 code sits in bits [5:2] of its byte;
+//   scale of A row m: lane m, column sfa + m/32, byte a_sf_id;
+//   scale of B column n: lane 32*(m/32) + n%32 for the lane quarter of every
+//     row m (so it is replicated in all four quarters), column sfb + n/32,
+//     byte b_sf_id.
+__device__ __forceinline__ void mma_mxf8f6f4_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [%1], %2, %3, [%4], [%5], "
+      "p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Same with A read from shared memory.  For an E2M1 A the shared-memory
+// layout is the one the tensor-memory-access unit writes for its packed 4-bit
+// type: 16 codes (8 bytes, element 2i in the low nibble) per 16-byte slot.
+__device__ __forceinline__ void mma_mxf8f6f4_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], "
+      "p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Copies a 32-row x 16-byte shared-memory matrix (descriptor `src`) into
+// tensor memory at columns taddr..taddr+3 of all four lane quarters: lane
+// 32 q + l, column taddr + j receives bytes 4j..4j+3 of row l.  Asynchronous,
+// ordered with the MMAs the same thread issues afterwards.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t src) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src) : "memory");
+}
+
+// Element types of the block-scaled kinds (A/B format fields).
+constexpr uint32_t kFmtE4M3 = 0, kFmtE2M1 = 5;
+
+// Instruction descriptor of a block-scaled MMA with UE8M0 scales, both
+// operands K-major, fp32 accumulate; sf ids pick the scale byte of A and B.
+__host__ __device__ constexpr uint32_t idesc_block_scaled(uint32_t M, uint32_t N, uint32_t a_fmt,
+                                                          uint32_t b_fmt, uint32_t a_sf_id,
+                                                          uint32_t b_sf_id) {
+  return (b_sf_id << 4) | (a_fmt << 7) | (b_fmt << 10) | ((N >> 3) << 17) | (1u << 23) |
+         ((M >> 4) << 24) | (a_sf_id << 29);
+}
+
+// one 32-bit column of this warp's lane quarter: thread i <-> lane i
+__device__ __forceinline__ void tmem_st_32x32b_x1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
 // Arrive on `bar` once all previously issued tcgen05.mma of this thread completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
@@ -190,6 +260,16 @@ __device__ __forceinline__ uint64_t smem_desc_noswizzle(const void* base, uint32
   d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
   d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
   d |= (uint64_t)1 << 46;  // descriptor version for tcgen05
+  return d;
+}
+
+// K-major operand in 128-byte swizzled rows (the layout a tensor load with
+// 128-byte swizzle writes): row r at 128 r, its 16-byte slot c at c ^ (r % 8),
+// 8-row groups `sbo` bytes apart; `base` must be 1024-byte aligned up to the
+// K offset added for later K steps (0, 32, 64 or 96 bytes).
+__device__ __forceinline__ uint64_t smem_desc_sw128(const void* base, uint32_t sbo) {
+  uint64_t d = smem_desc_noswizzle(base, 16, sbo);
+  d |= (uint64_t)2 << 61;  // 128-byte swizzle
   return d;
 }
 
