@@ -26,10 +26,14 @@
 // pool mode, tiles of 16 pool blocks x 8 entries).  Warp roles:
 //   warp 0      producer: the tile's codes (one 2-D tensor load, 8 KB) and
 //               scale words (one bulk copy, 512 B) into a shared-memory ring;
-//   warp 1      allocates tensor memory; one thread copies the tile's scales
-//               into tensor memory (tcgen05.cp) and issues the four MMAs
+//   warps 1, 7  MMA issue, even and odd tiles (warp 1 also allocates tensor
+//               memory): one thread copies the tile's scales into tensor
+//               memory (tcgen05.cp) and issues the four MMAs
 //               D[128 entries x 64] += A[128 x 32] * B[64 x 32]^T, both
-//               operands read from shared memory;
+//               operands read from shared memory, into one of three
+//               accumulators (tile i -> i mod 3); two issuers and three
+//               accumulators keep the tensor core fed while the epilogue
+//               drains earlier tiles;
 //   warp 2      reorders the tile's 128 scale words into the layout the copy
 //               replicates into the four lane quarters of tensor memory;
 //   warps 3-6   epilogue: read the row's 64 half-dots from tensor memory,
@@ -54,17 +58,18 @@ constexpr int kTile = 128;
 #define CSA2_SCAN_STAGES 6
 #endif
 constexpr int kStages = CSA2_SCAN_STAGES;  // shared-memory ring depth (tiles in flight)
-constexpr int kAcc = 2;                    // accumulators in tensor memory
-constexpr int kWarps = 7;
+constexpr int kAcc = 3;                    // accumulators in tensor memory
+constexpr int kWarps = 8;
+constexpr int kMmaWarp1 = 7;               // issues the odd tiles
 constexpr int kThreads = kWarps * 32;
 constexpr uint32_t kCodeBytes = kTile * 64;  // bytes a tile of codes moves from global memory
-// Tensor memory columns: accumulators (64 fp32 columns each), then one scale
-// slot per ring stage and one for the query (4 columns used of each 16).
+// Tensor memory columns: accumulators (64 fp32 columns each), then a 4-column
+// scale slot per ring stage and a query-scale slot per MMA warp.
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kDCol0 = 0;
 constexpr uint32_t kSfaCol0 = 64u * kAcc;
-constexpr uint32_t kSfbCol = kSfaCol0 + 16u * kStages;
-static_assert(kSfbCol + 4 <= kTmemCols, "tensor memory layout");
+constexpr uint32_t kSfbCol0 = kSfaCol0 + 4u * kStages;
+static_assert(kSfbCol0 + 8u <= kTmemCols, "tensor memory layout");
 constexpr long long kWaitBudget = 1LL << 32;  // clock cycles (about 2 s)
 
 struct __align__(1024) ScanSmem {
@@ -79,7 +84,7 @@ struct __align__(1024) ScanSmem {
   uint32_t sfT[kStages][32][4];        // sfT[l][j] = scale word of row 32 j + l
   uint32_t qsfT[32][4];                // query scales: [head][hi, lo, -, -]
   float w[32];
-  uint64_t full[kStages], sf_ready[kStages], tile_done[kStages];
+  uint64_t full[kStages], sfull[kStages], sf_ready[kStages], tile_done[kStages];
   uint64_t d_free[kAcc];
   uint32_t tmem_base;
   int abort_flag;
@@ -108,6 +113,21 @@ __device__ __forceinline__ void scan_abort(ScanSmem& S, void* ws, int where) {
   *reinterpret_cast<volatile int*>(&S.abort_flag) = 1;
   report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, where);
 }
+
+// Slot and pass parity in a ring of N slots, stepped without divisions.
+template <int N>
+struct Ring {
+  int slot;
+  uint32_t phase;
+  __device__ __forceinline__ explicit Ring(int start) : slot(start % N), phase((uint32_t)(start / N) & 1u) {}
+  __device__ __forceinline__ void step(int k) {  // k <= N
+    slot += k;
+    if (slot >= N) {
+      slot -= N;
+      phase ^= 1u;
+    }
+  }
+};
 
 // packed fp32 pairs (one instruction for two lanes of arithmetic)
 __device__ __forceinline__ float2 add_f32x2(float2 a, float2 b) {
@@ -183,6 +203,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&S.full[s], 1);
+      ptx::mbar_init(&S.sfull[s], 1);
       ptx::mbar_init(&S.sf_ready[s], 1);
       ptx::mbar_init(&S.tile_done[s], 1);
     }
@@ -240,9 +261,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (warp == 0) {
       // ------------------------------------------------------------ producer
       if (lane == 0) {
-        for (int i = 0; i < my_tiles; ++i) {
-          const int s = i % kStages;
-          const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+        Ring<kStages> st(0);
+        for (int i = 0; i < my_tiles; ++i, st.step(1)) {
+          const int s = st.slot;
+          const uint32_t ph = st.phase;
           // stage s is free once the MMAs of tile i - kStages completed
           if (!ptx::mbar_wait(&S.tile_done[s], ph ^ 1u, abort_flag, kWaitBudget)) {
             scan_abort(S, p.ws, 1);
@@ -253,98 +275,128 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int64_t j0 = t * kTile;
             const uint32_t cnt = (uint32_t)min((int64_t)kTile, n - j0);
             const uint32_t cnt4 = scale_bulk ? (cnt & ~3u) : 0u;
-            ptx::mbar_arrive_expect_tx(&S.full[s], kCodeBytes + cnt4 * 4u);
+            // scales first, on their own barrier, so that their reorder overlaps the codes' arrival
+            ptx::mbar_arrive_expect_tx(&S.sfull[s], cnt4 * 4u);
+            if (cnt4) ptx::bulk_g2s(S.scales[s], scales_b + j0 * 4, cnt4 * 4u, &S.sfull[s]);
+            ptx::mbar_arrive_expect_tx(&S.full[s], kCodeBytes);
             ptx::tma_load_2d(S.codes[s], &map_tile, 0, (int)(b * p.seq_stride + j0), &S.full[s]);
-            if (cnt4) ptx::bulk_g2s(S.scales[s], scales_b + j0 * 4, cnt4 * 4u, &S.full[s]);
           } else {
             int pbv[16];
             uint32_t cnt[16];
-            uint32_t bytes = 0;
+            uint32_t cbytes = 0, sbytes = 0;
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
               const int64_t slot = t * 16 + u;
               pbv[u] = slot < p.keep ? p.pool[(int64_t)b * p.keep + slot] : -1;
               const int64_t base = (int64_t)pbv[u] * 8;
               cnt[u] = (pbv[u] >= 0 && base < n) ? (uint32_t)min((int64_t)8, n - base) : 0u;
-              bytes += (cnt[u] ? 8u * 64u : 0u) + (scale_bulk ? (cnt[u] & ~3u) * 4u : 0u);
+              cbytes += cnt[u] ? 8u * 64u : 0u;
+              sbytes += scale_bulk ? (cnt[u] & ~3u) * 4u : 0u;
             }
-            ptx::mbar_arrive_expect_tx(&S.full[s], bytes);
+            ptx::mbar_arrive_expect_tx(&S.sfull[s], sbytes);
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              const uint32_t c4 = scale_bulk ? (cnt[u] & ~3u) : 0u;
+              if (c4) ptx::bulk_g2s(S.scales[s] + u * 32, scales_b + (int64_t)pbv[u] * 8 * 4, c4 * 4u, &S.sfull[s]);
+            }
+            ptx::mbar_arrive_expect_tx(&S.full[s], cbytes);
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
               if (!cnt[u]) continue;
               const int64_t base = (int64_t)pbv[u] * 8;
               ptx::tma_load_2d(S.codes[s] + u * 1024, &map_block, 0, (int)(b * p.seq_stride + base),
                                &S.full[s]);
-              const uint32_t c4 = scale_bulk ? (cnt[u] & ~3u) : 0u;
-              if (c4) ptx::bulk_g2s(S.scales[s] + u * 32, scales_b + base * 4, c4 * 4u, &S.full[s]);
             }
           }
         }
       }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == kMmaWarp1) {
       // ------------------------------------------------------------ MMA issue
+      const int par = warp == 1 ? 0 : 1;  // tile parity this warp issues
       if (lane == 0) {
         uint64_t bd[4];
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) bd[ks] = ptx::smem_desc_noswizzle(S.qB[ks], 1024, 128);
-        // query scales, replicated into the four lane quarters
-        ptx::tmem_cp_32x128b_warpx4(tmem + kSfbCol, ptx::smem_desc_noswizzle(S.qsfT, 128, 128));
-        for (int i = 0; i < my_tiles; ++i) {
-          const int s = i % kStages;
-          const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-          const int a = i % kAcc;
-          const uint32_t u = (uint32_t)(i / kAcc) & 1u;
+        // query scales, replicated into the four lane quarters; each issuer
+        // copies them into its own slot, ordered before its MMAs
+        const uint32_t sfb_t = tmem + kSfbCol0 + 4u * (uint32_t)par;
+        ptx::tmem_cp_32x128b_warpx4(sfb_t, ptx::smem_desc_noswizzle(S.qsfT, 128, 128));
+        // A operand descriptors of stage 0, K step 0; stage s and K step ks add
+        // (s * stage bytes + 32 ks) / 16 to the start-address field
+        const uint64_t ad0 = ptx::smem_desc_sw128(S.codes[0], 1024);
+        Ring<kStages> st(par);
+        Ring<kAcc> acc(par);
+        for (int i = par; i < my_tiles; i += 2, st.step(2), acc.step(2)) {
+          const int s = st.slot;
+          const uint32_t ph = st.phase;
+          const int a = acc.slot;
+          const uint32_t u = acc.phase;
           if (!ptx::mbar_wait(&S.sf_ready[s], ph, abort_flag, kWaitBudget) ||
+              !ptx::mbar_wait(&S.full[s], ph, abort_flag, kWaitBudget) ||
               !ptx::mbar_wait(&S.d_free[a], u ^ 1u, abort_flag, kWaitBudget)) {
             scan_abort(S, p.ws, 2);
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t sfa_t = tmem + kSfaCol0 + (uint32_t)s * 16u;
+          const uint32_t sfa_t = tmem + kSfaCol0 + (uint32_t)s * 4u;
           const uint32_t d_t = tmem + kDCol0 + (uint32_t)a * 64u;
           ptx::tmem_cp_32x128b_warpx4(sfa_t, ptx::smem_desc_noswizzle(S.sfT[s], 128, 128));
+          const uint64_t ads = ad0 + (uint64_t)(s * (kTile * 128 / 16));
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
             const uint32_t idesc = ptx::idesc_block_scaled(128, 64, ptx::kFmtE2M1, ptx::kFmtE4M3, ks, ks);
-            const uint64_t ad = ptx::smem_desc_sw128(S.codes[s] + ks * 32, 1024);
-            ptx::mma_mxf8f6f4_ss(d_t, ad, bd[ks], idesc, sfa_t, tmem + kSfbCol, ks > 0 ? 1u : 0u);
+            ptx::mma_mxf8f6f4_ss(d_t, ads + (uint64_t)(2 * ks), bd[ks], idesc, sfa_t, sfb_t, ks > 0 ? 1u : 0u);
           }
           ptx::mma_commit(&S.tile_done[s]);
         }
       }
     } else if (warp == 2) {
       // ------------------------------------------------------------ scale reorder
-      for (int i = 0; i < my_tiles; ++i) {
-        const int s = i % kStages;
-        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-        if (!ptx::mbar_wait_warp(&S.full[s], ph, abort_flag, kWaitBudget)) {
+      Ring<kStages> st(0);
+      for (int i = 0; i < my_tiles; ++i, st.step(1)) {
+        const int s = st.slot;
+        const uint32_t ph = st.phase;
+        if (!ptx::mbar_wait_warp(&S.sfull[s], ph, abort_flag, kWaitBudget)) {
           scan_abort(S, p.ws, 3);
           break;
         }
         const int64_t t = t_begin + i;
         uint32_t w4[4];
+        const uint32_t* sc = reinterpret_cast<const uint32_t*>(S.scales[s]);
+        if (!pooled && scale_bulk && (t + 1) * kTile <= n) {  // a full tile: every word came in
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int r = 32 * j + lane;
-          const RowInfo ri = row_info(p, b, n, t, r, scale_bulk);
-          w4[j] = !ri.valid ? 0u
-                  : ri.scale_in_smem ? *reinterpret_cast<const uint32_t*>(S.scales[s] + r * 4)
-                                     : *reinterpret_cast<const uint32_t*>(scales_b + ri.j * 4);
+          for (int j = 0; j < 4; ++j) w4[j] = sc[32 * j + lane];
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int r = 32 * j + lane;
+            const RowInfo ri = row_info(p, b, n, t, r, scale_bulk);
+            w4[j] = !ri.valid ? 0u
+                    : ri.scale_in_smem ? sc[r]
+                                       : *reinterpret_cast<const uint32_t*>(scales_b + ri.j * 4);
+          }
         }
         *reinterpret_cast<uint4*>(S.sfT[s][lane]) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&S.sf_ready[s]);
       }
-    } else {
+    } else if (warp < kMmaWarp1) {
       // ------------------------------------------------------------ epilogue
       const int sub = warp % 4;  // lane quarter this warp may access
+      float wr[32];
+#pragma unroll
+      for (int h = 0; h < 32; ++h) wr[h] = S.w[h];
       const int r = sub * 32 + lane;
       const uint32_t lane_addr = tmem + ((uint32_t)(sub * 32) << 16);
-      for (int i = 0; i < my_tiles; ++i) {
-        const int s = i % kStages;
-        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-        const int a = i % kAcc;
+      float* const score_row = p.scores ? p.scores + (int64_t)b * p.score_stride : nullptr;
+      float* const bmax_row = p.bmax ? p.bmax + (int64_t)b * p.bmax_stride : nullptr;
+      Ring<kStages> st(0);
+      Ring<kAcc> acc(0);
+      for (int i = 0; i < my_tiles; ++i, st.step(1), acc.step(1)) {
+        const int s = st.slot;
+        const uint32_t ph = st.phase;
+        const int a = acc.slot;
         if (!ptx::mbar_wait_warp(&S.tile_done[s], ph, abort_flag, kWaitBudget)) {
           scan_abort(S, p.ws, 5);
           break;
@@ -363,10 +415,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (lane == 0) ptx::mbar_arrive(&S.d_free[a]);
         // sum_h w_h max(dot_h, 0) on head pairs, two accumulators
         float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
-        const float4* w4 = reinterpret_cast<const float4*>(S.w);
 #pragma unroll
         for (int h4 = 0; h4 < 8; ++h4) {
-          const float4 wv = w4[h4];
+          const float4 wv = make_float4(wr[4 * h4], wr[4 * h4 + 1], wr[4 * h4 + 2], wr[4 * h4 + 3]);
           float2 x01 = add_f32x2(make_float2(__uint_as_float(hi[4 * h4]), __uint_as_float(hi[4 * h4 + 1])),
                                  make_float2(__uint_as_float(lo[4 * h4]), __uint_as_float(lo[4 * h4 + 1])));
           float2 x23 = add_f32x2(make_float2(__uint_as_float(hi[4 * h4 + 2]), __uint_as_float(hi[4 * h4 + 3])),
@@ -379,16 +430,17 @@ __global__ void __launch_bounds__(kThreads, 2)
         const float sum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
 
         const int64_t t = t_begin + i;
-        const RowInfo ri = row_info(p, b, n, t, r, scale_bulk);
-        const float score = ri.valid ? sum : -INFINITY;
         const int64_t c = t * kTile + r;  // candidate index
-        if (p.scores && c < ncand) p.scores[(int64_t)b * p.score_stride + c] = score;
-        if (p.bmax) {
+        const bool full_tile = !pooled && (t + 1) * kTile <= n;
+        const bool valid = full_tile || row_info(p, b, n, t, r, scale_bulk).valid;
+        const float score = valid ? sum : -INFINITY;
+        if (score_row && c < ncand) score_row[c] = score;
+        if (bmax_row) {
           float m = score;
           m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
           m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
           m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-          if ((lane & 7) == 0 && c < ncand) p.bmax[(int64_t)b * p.bmax_stride + c / 8] = m;
+          if ((lane & 7) == 0 && c < ncand) bmax_row[c >> 3] = m;
         }
       }
     }
