@@ -22,7 +22,8 @@ namespace cg = cooperative_groups;
 // Candidates are entries [0, n), blocks [0, ceil(n/8)), or the entries of the
 // 8-entry blocks listed in `pool` (ascending) -- in every case candidate order
 // is entry (or block) order, so ties go to the lower index.  The key of
-// candidate c is keys[b*key_stride + c].
+// candidate c is keys[b*key_stride + c], or, with keys_by_entry (pool mode),
+// the key of the candidate's entry: keys[b*key_stride + entry].
 struct SelectArgs {
   const float* keys;    // [B][key_stride]
   int64_t key_stride;
@@ -35,6 +36,7 @@ struct SelectArgs {
   int32_t* out;         // [B][out_stride]
   int64_t out_stride;
   int64_t n_max;        // visible entries are clamped to this bound
+  int keys_by_entry;    // pool mode: keys are indexed by entry id, not by candidate
 };
 
 constexpr int kSelItems = 4;   // consecutive candidates per thread per chunk
@@ -47,6 +49,27 @@ __device__ __forceinline__ void load_candidates(const SelectArgs& a, int b, int6
                                                 int64_t (&id)[kSelItems]) {
   const float* kb = a.keys + (int64_t)b * a.key_stride;
   float v[kSelItems];
+  if (a.pool && a.keys_by_entry) {
+    // four consecutive entries of one pool block (c0 % 8 is 0 or 4)
+    const int p = c0 < ncand ? a.pool[(int64_t)b * a.keep + c0 / 8] : -1;
+    const int64_t e0 = (int64_t)p * 8 + c0 % 8;
+    if (p >= 0 && vec_ok && e0 + kSelItems <= n) {
+      const float4 f = *reinterpret_cast<const float4*>(kb + e0);
+      v[0] = f.x;
+      v[1] = f.y;
+      v[2] = f.z;
+      v[3] = f.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < kSelItems; ++i) v[i] = (p >= 0 && e0 + i < n) ? kb[e0 + i] : -INFINITY;
+    }
+#pragma unroll
+    for (int i = 0; i < kSelItems; ++i) {
+      id[i] = e0 + i;
+      key[i] = (c0 + i < ncand && p >= 0 && id[i] < n) ? score_key(v[i]) : 0u;
+    }
+    return;
+  }
   if (vec_ok && c0 + kSelItems <= ncand) {
     const float4 f = *reinterpret_cast<const float4*>(kb + c0);
     v[0] = f.x;
@@ -102,7 +125,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
   __shared__ unsigned cvalid;         // this CTA's valid-candidate count
   __shared__ int ccount[2];           // this CTA's keys > T and == T
   __shared__ uint32_t s_prefix, s_mask;
-  __shared__ int s_need, s_total_valid;
+  __shared__ int s_need;
   __shared__ int s_base_eq, s_base_out;
 
   cg::cluster_group cluster = cg::this_cluster();
@@ -176,7 +199,6 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
       if (tid == 0) {
         unsigned tv = 0;
         for (int r = 0; r < kSelCluster; ++r) tv += *cluster.map_shared_rank(&cvalid, r);
-        s_total_valid = (int)tv;
         s_need = (int)min((int64_t)a.k, (int64_t)tv);
       }
       __syncthreads();
@@ -369,22 +391,20 @@ extern "C" csa2_status csa2_index_topk(const csa2_kv_planes* kv, int32_t B, cons
     return launch_status();
   }
 
-  // HIER_BUILD: one full scan keeps only the block maxima (entry scores only when
-  // asked for); the pool is selected from them; the token top-k re-scores the
-  // pool's entries, which costs n_blocks_keep*block entries instead of a 4-byte
-  // score per scanned entry.
-  csa2_status rs = launch_scan(kv, B, n_entries, n_max, n_max, q, w, nullptr, 0, scores_out, n_max,
-                               L.bmax, L.bmax_cols, ws, st);
+  // HIER_BUILD: one full scan writes every entry's score and the block maxima;
+  // the pool is selected from the maxima, and the token top-k reads the scores
+  // of the pool's entries where the scan left them (4 bytes written per entry
+  // instead of a second pass over the pool's keys).
+  float* sc = scores_out ? scores_out : L.scores;
+  const int64_t sc_stride = scores_out ? n_max : L.score_cols;
+  csa2_status rs = launch_scan(kv, B, n_entries, n_max, n_max, q, w, nullptr, 0, sc, sc_stride, L.bmax,
+                               L.bmax_cols, ws, st);
   if (rs != CSA2_OK) return rs;
   int32_t* pool = pool_out ? pool_out : L.pool;
   SelectArgs pa{L.bmax, L.bmax_cols, n_entries, nullptr, 0, 1, 0, n_blocks_keep, pool, n_blocks_keep,
                 n_max};
   launch_select(pa, B, st);
-  rs = launch_scan(kv, B, n_entries, n_max, keep_c, q, w, pool, n_blocks_keep, L.scores,
-                   L.score_cols, nullptr, 0, ws, st);
-  if (rs != CSA2_OK) return rs;
-  SelectArgs ta{L.scores, L.score_cols, n_entries, pool, n_blocks_keep, 0, keep_c, k, topk_out, k,
-                n_max};
+  SelectArgs ta{sc, sc_stride, n_entries, pool, n_blocks_keep, 0, keep_c, k, topk_out, k, n_max, 1};
   launch_select(ta, B, st);
   return launch_status();
 }

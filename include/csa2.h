@@ -134,7 +134,9 @@ size_t csa2_cache_write_workspace_size(int64_t T, int32_t m);
  *   HIER_BUILD: block score s_u = max of I_j over block u = [u*block, u*block+block)
  *               (partial last block allowed); the pool is the n_blocks_keep best
  *               blocks (ties to the lower block); topk = the k best entries of the
- *               pool, which equals the FLAT result when n_blocks_keep >= k.
+ *               pool, which equals the FLAT result when n_blocks_keep >= k.  The
+ *               scan writes every entry's score (into scores_out, else the
+ *               workspace) and the token top-k reads the pool's from there.
  *   POOL:       the k best entries of the blocks listed in pool_in[b] (ascending
  *               block ids, -1 padded), scored with this call's own q and w.
  * ("DeepSeek-V4.1-Flash: pushing the limits of KV cache compression", 4.1, 4.3;
