@@ -298,8 +298,264 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
   cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
+// Resident form of the same selection, for slices of at most kResCap
+// candidates per CTA: each CTA loads its slice once into shared memory (thread t
+// owns a contiguous run of kper candidates), runs the four digit passes there,
+// and collects with one scan: a thread's run is contiguous, so per-thread counts
+// of keys above / equal to the threshold, scanned in thread order and offset by
+// the cluster's earlier CTAs, place every chosen id in candidate order.
+// Histogram updates are run-length coded per thread (one shared atomic per run
+// of equal digits), and the per-CTA histograms alternate between two buffers so
+// that one cluster barrier per pass suffices.
+constexpr int kResThreads = 256;
+constexpr int kResMaxPer = 64;  // candidates per thread
+constexpr int64_t kResCap = (int64_t)kResThreads * kResMaxPer;
+
+// keys of candidates c0..c0+3 (c0 a multiple of 4; 0 = not a candidate)
+__device__ __forceinline__ uint4 load_keys4(const SelectArgs& a, int b, int64_t n, int64_t ncand, int64_t c0,
+                                            bool vec_ok) {
+  const float* kb = a.keys + (int64_t)b * a.key_stride;
+  float v[4];
+  int64_t e0 = c0;  // index into the key row of candidate c0
+  int64_t lim = ncand;
+  bool ok = c0 < ncand;
+  if (a.pool) {
+    const int p = ok ? a.pool[(int64_t)b * a.keep + c0 / 8] : -1;
+    ok = ok && p >= 0;
+    if (a.keys_by_entry) {
+      e0 = (int64_t)p * 8 + c0 % 8;
+      lim = n;
+    } else {
+      lim = min(ncand, c0 + max((int64_t)0, n - ((int64_t)p * 8 + c0 % 8)));  // entries beyond n are out
+    }
+  }
+  if (ok && vec_ok && e0 + 4 <= lim) {
+    const float4 f = *reinterpret_cast<const float4*>(kb + e0);
+    v[0] = f.x;
+    v[1] = f.y;
+    v[2] = f.z;
+    v[3] = f.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = (ok && e0 + i < lim) ? kb[e0 + i] : -INFINITY;
+  }
+  uint32_t k[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) k[i] = v[i] == -INFINITY ? 0u : score_key(v[i]);
+  return make_uint4(k[0], k[1], k[2], k[3]);
+}
+
+__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kResThreads)
+    k_select_res(SelectArgs a) {
+  constexpr int NT = kResThreads;
+  constexpr int kBins = 256;
+  constexpr int kWarpsSel = NT / 32;
+  using ScanI = cub::BlockScan<int, NT>;
+  __shared__ typename ScanI::TempStorage scan_tmp;
+  extern __shared__ uint4 keys_s[];  // thread t: 4-key slots t*S .. t*S+S-1, swizzled
+  __shared__ unsigned whist[kWarpsSel][kBins];
+  __shared__ unsigned chist[2][kBins];  // this CTA's histogram of pass p in chist[p & 1]
+  __shared__ unsigned cvalid;
+  __shared__ int ccount[2];
+  __shared__ uint32_t s_prefix, s_mask;
+  __shared__ int s_need;
+  __shared__ int s_base_eq, s_base_out;
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int b = blockIdx.x / kSelCluster;
+  const int tid = threadIdx.x, lane = threadIdx.x % 32, wid = threadIdx.x / 32;
+  const int64_t n = max((int64_t)0, min((int64_t)a.n_entries[b], a.n_max));
+  const int64_t ncand = a.pool ? a.ncand_fixed : (a.count_blocks ? cdiv(n, 8) : n);
+  const int64_t per = (int64_t)align_up((size_t)cdiv(ncand, kSelCluster), kSelItems);
+  const int64_t lo = min(ncand, rank * per), hi = min(ncand, lo + per);
+  // candidates per thread: a power of two >= 4 covering the slice (the launch
+  // sized the shared buffer for the largest slice, n = n_max)
+  int kper = 4;
+  while ((int64_t)kper * NT < per) kper *= 2;
+  const int nslot = kper / 4;
+  const int64_t t0 = lo + (int64_t)tid * kper;
+  const bool vec_ok = (a.key_stride % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.keys) & 15) == 0);
+  int32_t* out = a.out + (int64_t)b * a.out_stride;
+  unsigned* myhist = whist[wid];
+  uint4* myslots = keys_s + (int64_t)tid * nslot;
+  const int swz = tid & (nslot - 1);
+
+  if (tid == 0) {
+    cvalid = 0;
+    s_prefix = 0;
+    s_mask = 0;
+  }
+  // load the run once, up to 16 slots in flight per thread
+  unsigned myvalid = 0;
+  for (int v0 = 0; v0 < nslot; v0 += 16) {
+    uint4 k4[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int64_t c0 = t0 + 4 * (v0 + u);
+      k4[u] = (v0 + u < nslot && c0 < hi) ? load_keys4(a, b, n, hi, c0, vec_ok) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      if (v0 + u < nslot) {
+        myslots[(v0 + u) ^ swz] = k4[u];
+        myvalid += (k4[u].x != 0u) + (k4[u].y != 0u) + (k4[u].z != 0u) + (k4[u].w != 0u);
+      }
+    }
+  }
+  myvalid = __reduce_add_sync(0xffffffffu, myvalid);
+  __syncthreads();
+  if (lane == 0) atomicAdd(&cvalid, myvalid);
+
+  int need_total = 0;
+  int pass = 0;
+  for (int shift = 24; shift >= 0; shift -= 8, ++pass) {
+    for (int d = lane; d < kBins; d += 32) myhist[d] = 0;
+    __syncthreads();
+    const uint32_t prefix = s_prefix, mask = s_mask;
+    uint32_t last = 0xFFFFFFFFu;
+    unsigned run = 0;
+    for (int v = 0; v < nslot; ++v) {
+      const uint4 k4 = myslots[v ^ swz];
+      const uint32_t kk4[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t kk = kk4[i];
+        if (kk != 0u && (kk & mask) == prefix) {
+          const uint32_t d = (kk >> shift) & 255u;
+          if (d == last) {
+            ++run;
+          } else {
+            if (run) atomicAdd(&myhist[last], run);
+            last = d;
+            run = 1;
+          }
+        }
+      }
+    }
+    if (run) atomicAdd(&myhist[last], run);
+    __syncthreads();
+    unsigned* ch = chist[pass & 1];
+    {  // this CTA's bin totals (thread t <-> bin 255 - t)
+      unsigned h = 0;
+      const int bin = kBins - 1 - tid;
+#pragma unroll
+      for (int w = 0; w < kWarpsSel; ++w) h += whist[w][bin];
+      ch[bin] = h;
+    }
+    // one barrier per pass: the other buffer is rewritten two passes later,
+    // after every CTA passed the next pass's barrier (and so finished reading)
+    cluster.sync();
+    if (pass == 0) {
+      if (tid == 0) {
+        unsigned tv = 0;
+        for (int r = 0; r < kSelCluster; ++r) tv += *cluster.map_shared_rank(&cvalid, r);
+        s_need = (int)min((int64_t)a.k, (int64_t)tv);
+      }
+      __syncthreads();
+      need_total = s_need;
+      if (need_total == 0) break;  // uniform across the cluster
+    }
+    const int need = s_need;
+    const int bin = kBins - 1 - tid;
+    unsigned hr[kSelCluster];
+#pragma unroll
+    for (int r = 0; r < kSelCluster; ++r) hr[r] = *cluster.map_shared_rank(&ch[bin], r);
+    unsigned h = 0;
+#pragma unroll
+    for (int r = 0; r < kSelCluster; ++r) h += hr[r];
+    int cum = (int)h;
+    ScanI(scan_tmp).InclusiveSum(cum, cum);
+    __syncthreads();  // s_need read above before it is rewritten
+    if (cum >= need && cum - (int)h < need) {
+      s_prefix = prefix | ((uint32_t)bin << shift);
+      s_mask = mask | (255u << shift);
+      s_need = need - (cum - (int)h);
+    }
+    __syncthreads();
+  }
+  const uint32_t T = s_prefix;
+  const int take_eq = s_need;  // candidates equal to T to take (lowest indices first)
+
+  if (need_total > 0) {
+    int gt = 0, eq = 0;
+    for (int v = 0; v < nslot; ++v) {
+      const uint4 k4 = myslots[v ^ swz];
+      const uint32_t kk4[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        gt += kk4[i] != 0u && kk4[i] > T;
+        eq += kk4[i] != 0u && kk4[i] == T;
+      }
+    }
+    const int wgt = (int)__reduce_add_sync(0xffffffffu, (unsigned)gt);
+    const int weq = (int)__reduce_add_sync(0xffffffffu, (unsigned)eq);
+    if (tid == 0) ccount[0] = ccount[1] = 0;
+    __syncthreads();
+    if (lane == 0) {
+      atomicAdd(&ccount[0], wgt);
+      atomicAdd(&ccount[1], weq);
+    }
+    cluster.sync();
+    if (tid == 0) {
+      int eq_before = 0, out_before = 0;
+      for (int r = 0; r < rank; ++r) {
+        const int* cc = cluster.map_shared_rank(ccount, r);
+        const int g_r = cc[0], e_r = cc[1];
+        out_before += g_r + max(0, min(e_r, take_eq - eq_before));
+        eq_before += e_r;
+      }
+      s_base_eq = eq_before;
+      s_base_out = out_before;
+    }
+    __syncthreads();
+    int eq_rank;
+    ScanI(scan_tmp).ExclusiveSum(eq, eq_rank);
+    __syncthreads();
+    const int eq_start = s_base_eq + eq_rank;  // cluster-wide rank of my first key equal to T
+    const int eq_take = max(0, min(eq, take_eq - eq_start));
+    int pos;
+    ScanI(scan_tmp).ExclusiveSum(gt + eq_take, pos);
+    pos += s_base_out;
+    int eq_left = eq_take;
+    for (int v = 0; v < nslot; ++v) {
+      const uint4 k4 = myslots[v ^ swz];
+      const uint32_t kk4[4] = {k4.x, k4.y, k4.z, k4.w};
+      const int64_t c0 = t0 + 4 * v;
+      int pb = 0;
+      if (a.pool) pb = c0 < hi ? a.pool[(int64_t)b * a.keep + c0 / 8] : -1;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t kk = kk4[i];
+        bool take = kk != 0u && kk > T;
+        if (kk != 0u && kk == T && eq_left > 0) {
+          take = true;
+          --eq_left;
+        }
+        if (take) out[pos++] = a.pool ? (int32_t)((int64_t)pb * 8 + (c0 + i) % 8) : (int32_t)(c0 + i);
+      }
+    }
+  }
+  if (rank == kSelCluster - 1) {  // padding after the last selected id
+    const int taken = need_total > 0 ? need_total : 0;
+    for (int i = taken + tid; i < a.k; i += NT) out[i] = -1;
+  }
+  cluster.sync();  // no CTA leaves while another may still read its shared memory
+}
+
 void launch_select(const SelectArgs& a, int B, cudaStream_t st) {
-  k_select<<<B * kSelCluster, kSelThreads, 0, st>>>(a);
+  // slice per CTA: the pool candidates, the blocks, or up to n_max entries
+  const int64_t ncand_max = a.pool ? a.ncand_fixed : (a.count_blocks ? cdiv(a.n_max, 8) : a.n_max);
+  const int64_t per = (int64_t)align_up((size_t)cdiv(ncand_max, kSelCluster), kSelItems);
+  if (per <= kResCap) {
+    int kper = 4;
+    while ((int64_t)kper * kResThreads < per) kper *= 2;
+    const int smem = kResThreads * kper * 4;
+    // a failure here surfaces as the launch error that launch_status() reports
+    cudaFuncSetAttribute(k_select_res, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kResCap * 4));
+    k_select_res<<<B * kSelCluster, kResThreads, smem, st>>>(a);
+  } else
+    k_select<<<B * kSelCluster, kSelThreads, 0, st>>>(a);
 }
 
 // ------------------------------------------------------------------ workspace

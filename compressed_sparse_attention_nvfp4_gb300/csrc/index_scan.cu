@@ -434,7 +434,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         const bool full_tile = !pooled && (t + 1) * kTile <= n;
         const bool valid = full_tile || row_info(p, b, n, t, r, scale_bulk).valid;
         const float score = valid ? sum : -INFINITY;
-        if (score_row && c < ncand) score_row[c] = score;
+        // evict-first: 4 B per entry that only the pool entries are read back from,
+        // which must not push the block maxima (read next) out of L2
+        if (score_row && c < ncand) __stcs(score_row + c, score);
         if (bmax_row) {
           float m = score;
           m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
