@@ -83,33 +83,36 @@ __global__ void __launch_bounds__(kAT, 1) k_attn_tc(
   {
     const int h = tid / 2, half = tid % 2;
     const uint4* src = reinterpret_cast<const uint4*>(qg + ((int64_t)b * kHAtt + h) * kDMain + half * 256);
+    uint4 raw[32];  // all of this thread's 256 channels in flight at once
+#pragma unroll
+    for (int i = 0; i < 32; ++i) raw[i] = src[i];
     float mx = 0.0f;
-#pragma unroll 8
+#pragma unroll
     for (int i = 0; i < 32; ++i) {
-      const uint4 raw = src[i];
-      const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+      const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w4[j] << 16)), fabsf(__uint_as_float(w4[j] & 0xFFFF0000u))));
     }
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    const int sig = mx > 0.0f ? floor_log2_f32(mx) - 14 : 0;
-#pragma unroll 8
-    for (int i = 0; i < 32; ++i) {  // 8 channels per uint4 -> one 16-byte chunk of q' (second read hits cache)
-      const uint4 raw = src[i];
-      const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+    // 2^sig brings the head's largest |q| to [2^14, 2^15); clamped so that both
+    // 2^sig and 2^-sig are normal fp32 values (bf16 q keeps q' inside f16 range)
+    const int sig = mx > 0.0f ? min(max(floor_log2_f32(mx) - 14, -126), 126) : 0;
+    const float inv = exp2i_f32(-sig);  // exact power of two: q * 2^-sig rounds only in the f16 conversion
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {  // 8 channels per uint4 -> one 16-byte chunk of q'
+      const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
       uint32_t o[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const __half lo = __float2half_rn(ldexpf(__uint_as_float(w4[j] << 16), -sig));
-        const __half hi = __float2half_rn(ldexpf(__uint_as_float(w4[j] & 0xFFFF0000u), -sig));
-        o[j] = (uint32_t)*reinterpret_cast<const uint16_t*>(&lo) |
-               ((uint32_t)*reinterpret_cast<const uint16_t*>(&hi) << 16);
+        const __half2 h2 = __floats2half2_rn(__uint_as_float(w4[j] << 16) * inv,
+                                             __uint_as_float(w4[j] & 0xFFFF0000u) * inv);
+        o[j] = *reinterpret_cast<const uint32_t*>(&h2);
       }
       const int cc = half * 32 + i;  // channel chunk c/8
       *reinterpret_cast<uint4*>(&S.u.q[cc][h * 8]) = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    if (half == 0) S.colscale[h] = ldexpf(scale, sig);
+    if (half == 0) S.colscale[h] = scale * exp2i_f32(sig);
   }
 
   // ---- rows -> f16 X (thread r owns row r of the chunk)
@@ -149,9 +152,12 @@ __global__ void __launch_bounds__(kAT, 1) k_attn_tc(
     } else if (gr - k < n_swa) {
       ok = true;
       const uint4* src = reinterpret_cast<const uint4*>(swa + ((int64_t)b * n_swa + (gr - k)) * kDMain);
-#pragma unroll 4
+      uint4 row[32];  // the whole 512-byte row in flight at once
+#pragma unroll
+      for (int i = 0; i < 32; ++i) row[i] = src[i];
+#pragma unroll
       for (int i = 0; i < 32; ++i) {  // 16 channels per uint4 -> two chunks
-        const uint4 v = src[i];
+        const uint4 v = row[i];
         *reinterpret_cast<uint4*>(&S.X[2 * i][r * 8]) =
             make_uint4(e4m3x2_to_f16x2(v.x), e4m3x2_to_f16x2(v.x >> 16), e4m3x2_to_f16x2(v.y),
                        e4m3x2_to_f16x2(v.y >> 16));
@@ -227,7 +233,7 @@ __global__ void __launch_bounds__(kAT, 1) k_attn_tc(
       for (int t = 0; t < 2; ++t) {
         const int h = hc * 8 + 2 * j + t;
         const float mh = S.m[h];
-        const float p = (sv[h] == -INFINITY || mh == -INFINITY) ? 0.0f : expf(sv[h] - mh);
+        const float p = (sv[h] == -INFINITY || mh == -INFINITY) ? 0.0f : __expf(sv[h] - mh);
         const __half ph = __float2half_rn(p);
         pv[t] = __half2float(ph);
         S.u.S[r][h] = pv[t];

@@ -306,10 +306,11 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
 // the cluster's earlier CTAs, place every chosen id in candidate order.
 // Histogram updates are run-length coded per thread (one shared atomic per run
 // of equal digits), and the per-CTA histograms alternate between two buffers so
-// that one cluster barrier per pass suffices.
-constexpr int kResThreads = 256;
+// that one cluster barrier per pass suffices.  (A single 1024-thread CTA per
+// query for the pool's 16,384 entries measured slower than eight CTAs: the
+// load latency of one query's gather is then hidden by nothing.)
 constexpr int kResMaxPer = 64;  // candidates per thread
-constexpr int64_t kResCap = (int64_t)kResThreads * kResMaxPer;
+constexpr int64_t kResCap = 256 * kResMaxPer;  // candidates per CTA: 64 KB of keys
 
 // keys of candidates c0..c0+3 (c0 a multiple of 4; 0 = not a candidate)
 __device__ __forceinline__ uint4 load_keys4(const SelectArgs& a, int b, int64_t n, int64_t ncand, int64_t c0,
@@ -345,9 +346,8 @@ __device__ __forceinline__ uint4 load_keys4(const SelectArgs& a, int b, int64_t 
   return make_uint4(k[0], k[1], k[2], k[3]);
 }
 
-__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kResThreads)
-    k_select_res(SelectArgs a) {
-  constexpr int NT = kResThreads;
+template <int NT>
+__global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
   constexpr int kBins = 256;
   constexpr int kWarpsSel = NT / 32;
   using ScanI = cub::BlockScan<int, NT>;
@@ -362,12 +362,13 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kResThread
   __shared__ int s_base_eq, s_base_out;
 
   cg::cluster_group cluster = cg::this_cluster();
+  const int ncl = (int)cluster.num_blocks();
   const int rank = (int)cluster.block_rank();
-  const int b = blockIdx.x / kSelCluster;
+  const int b = blockIdx.x / ncl;
   const int tid = threadIdx.x, lane = threadIdx.x % 32, wid = threadIdx.x / 32;
   const int64_t n = max((int64_t)0, min((int64_t)a.n_entries[b], a.n_max));
   const int64_t ncand = a.pool ? a.ncand_fixed : (a.count_blocks ? cdiv(n, 8) : n);
-  const int64_t per = (int64_t)align_up((size_t)cdiv(ncand, kSelCluster), kSelItems);
+  const int64_t per = (int64_t)align_up((size_t)cdiv(ncand, ncl), kSelItems);
   const int64_t lo = min(ncand, rank * per), hi = min(ncand, lo + per);
   // candidates per thread: a power of two >= 4 covering the slice (the launch
   // sized the shared buffer for the largest slice, n = n_max)
@@ -386,17 +387,18 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kResThread
     s_prefix = 0;
     s_mask = 0;
   }
-  // load the run once, up to 16 slots in flight per thread
+  // load the run once, up to kLoadBatch slots in flight per thread
+  constexpr int kLoadBatch = NT >= 1024 ? 4 : 16;  // within the register budget of NT threads
   unsigned myvalid = 0;
-  for (int v0 = 0; v0 < nslot; v0 += 16) {
-    uint4 k4[16];
+  for (int v0 = 0; v0 < nslot; v0 += kLoadBatch) {
+    uint4 k4[kLoadBatch];
 #pragma unroll
-    for (int u = 0; u < 16; ++u) {
+    for (int u = 0; u < kLoadBatch; ++u) {
       const int64_t c0 = t0 + 4 * (v0 + u);
       k4[u] = (v0 + u < nslot && c0 < hi) ? load_keys4(a, b, n, hi, c0, vec_ok) : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
-    for (int u = 0; u < 16; ++u) {
+    for (int u = 0; u < kLoadBatch; ++u) {
       if (v0 + u < nslot) {
         myslots[(v0 + u) ^ swz] = k4[u];
         myvalid += (k4[u].x != 0u) + (k4[u].y != 0u) + (k4[u].z != 0u) + (k4[u].w != 0u);
@@ -436,10 +438,10 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kResThread
     if (run) atomicAdd(&myhist[last], run);
     __syncthreads();
     unsigned* ch = chist[pass & 1];
-    {  // this CTA's bin totals (thread t <-> bin 255 - t)
+    if (tid < kBins) {  // this CTA's bin totals (thread t <-> bin 255 - t)
       unsigned h = 0;
       const int bin = kBins - 1 - tid;
-#pragma unroll
+#pragma unroll 8
       for (int w = 0; w < kWarpsSel; ++w) h += whist[w][bin];
       ch[bin] = h;
     }
@@ -449,7 +451,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kResThread
     if (pass == 0) {
       if (tid == 0) {
         unsigned tv = 0;
-        for (int r = 0; r < kSelCluster; ++r) tv += *cluster.map_shared_rank(&cvalid, r);
+        for (int r = 0; r < ncl; ++r) tv += *cluster.map_shared_rank(&cvalid, r);
         s_need = (int)min((int64_t)a.k, (int64_t)tv);
       }
       __syncthreads();
@@ -457,17 +459,19 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kResThread
       if (need_total == 0) break;  // uniform across the cluster
     }
     const int need = s_need;
-    const int bin = kBins - 1 - tid;
-    unsigned hr[kSelCluster];
-#pragma unroll
-    for (int r = 0; r < kSelCluster; ++r) hr[r] = *cluster.map_shared_rank(&ch[bin], r);
+    const int bin = kBins - 1 - tid;  // negative for threads beyond the 256 bins
     unsigned h = 0;
+    if (bin >= 0) {
+      unsigned hr[kSelCluster];
 #pragma unroll
-    for (int r = 0; r < kSelCluster; ++r) h += hr[r];
+      for (int r = 0; r < kSelCluster; ++r) hr[r] = r < ncl ? *cluster.map_shared_rank(&ch[bin], r) : 0u;
+#pragma unroll
+      for (int r = 0; r < kSelCluster; ++r) h += hr[r];
+    }
     int cum = (int)h;
     ScanI(scan_tmp).InclusiveSum(cum, cum);
     __syncthreads();  // s_need read above before it is rewritten
-    if (cum >= need && cum - (int)h < need) {
+    if (bin >= 0 && cum >= need && cum - (int)h < need) {
       s_prefix = prefix | ((uint32_t)bin << shift);
       s_mask = mask | (255u << shift);
       s_need = need - (cum - (int)h);
@@ -536,11 +540,33 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kResThread
       }
     }
   }
-  if (rank == kSelCluster - 1) {  // padding after the last selected id
+  if (rank == ncl - 1) {  // padding after the last selected id
     const int taken = need_total > 0 ? need_total : 0;
     for (int i = taken + tid; i < a.k; i += NT) out[i] = -1;
   }
   cluster.sync();  // no CTA leaves while another may still read its shared memory
+}
+
+template <int NT>
+void launch_select_res(const SelectArgs& a, int B, int ncl, int64_t per, cudaStream_t st) {
+  int kper = 4;
+  while ((int64_t)kper * NT < per) kper *= 2;
+  const int smem = NT * kper * 4;
+  // a failure here surfaces as the launch error that launch_status() reports
+  cudaFuncSetAttribute(k_select_res<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kResCap * 4));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(B * ncl));
+  cfg.blockDim = dim3(NT);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)ncl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, k_select_res<NT>, a);
 }
 
 void launch_select(const SelectArgs& a, int B, cudaStream_t st) {
@@ -548,12 +574,7 @@ void launch_select(const SelectArgs& a, int B, cudaStream_t st) {
   const int64_t ncand_max = a.pool ? a.ncand_fixed : (a.count_blocks ? cdiv(a.n_max, 8) : a.n_max);
   const int64_t per = (int64_t)align_up((size_t)cdiv(ncand_max, kSelCluster), kSelItems);
   if (per <= kResCap) {
-    int kper = 4;
-    while ((int64_t)kper * kResThreads < per) kper *= 2;
-    const int smem = kResThreads * kper * 4;
-    // a failure here surfaces as the launch error that launch_status() reports
-    cudaFuncSetAttribute(k_select_res, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kResCap * 4));
-    k_select_res<<<B * kSelCluster, kResThreads, smem, st>>>(a);
+    launch_select_res<256>(a, B, kSelCluster, per, st);
   } else
     k_select<<<B * kSelCluster, kSelThreads, 0, st>>>(a);
 }
