@@ -40,6 +40,10 @@ class KVPlanes(ctypes.Structure):
                 ("seq_stride", ctypes.c_int64)]
 
 
+class KernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("launches", ctypes.c_int64), ("total_ms", ctypes.c_double)]
+
+
 _lib = None
 
 
@@ -70,6 +74,8 @@ def lib() -> ctypes.CDLL:
             "csa2_v41_layer_table": ([i32, vp, vp, vp, vp, vp], ctypes.c_int),
             "csa2_check": ([vp, vp, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
             "csa2_status_string": ([ctypes.c_int], ctypes.c_char_p),
+            "csa2_timing_enable": ([i32], ctypes.c_int),
+            "csa2_kernel_times": ([ctypes.POINTER(KernelTime), i32], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -209,6 +215,23 @@ def check(ws, stream=None) -> tuple[int, int]:
     d = ctypes.c_int64(0)
     rc = lib().csa2_check(_ptr(ws), _stream(stream), ctypes.byref(d))
     return rc, d.value
+
+
+def timing_enable(on: bool) -> None:
+    """Switches per-kernel event timing on or off; discards the totals so far."""
+    _ok(lib().csa2_timing_enable(1 if on else 0), "csa2_timing_enable")
+
+
+def kernel_times() -> dict[str, tuple[int, float]]:
+    """{kernel name: (launches, summed device ms)} since the last timing_enable (waits for them)."""
+    n = lib().csa2_kernel_times(None, 0)
+    if n < 0:
+        raise Csa2Error(4, "csa2_kernel_times")
+    arr = (KernelTime * max(n, 1))()
+    n = lib().csa2_kernel_times(arr, n)
+    if n < 0:
+        raise Csa2Error(4, "csa2_kernel_times")
+    return {arr[i].name.decode(): (int(arr[i].launches), float(arr[i].total_ms)) for i in range(n)}
 
 
 def status_string(s: int) -> str:

@@ -15,7 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcsa2.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["capi.cu", "codec.cu", "index.cu", "index_scan.cu", "attn.cu", "cache_write.cu"]
+SOURCES = ["capi.cu", "codec.cu", "index.cu", "index_scan.cu", "attn.cu", "cache_write.cu", "timing.cu"]
 
 
 def nvcc_flags(extra: list[str] | None = None) -> list[str]:

@@ -16,6 +16,7 @@
 //      with (m, l) per head; a merge kernel combines the chunks by log-sum-exp.
 #include "codec.cuh"
 #include "ptx.cuh"
+#include "timing.cuh"
 
 namespace csa2 {
 
@@ -378,9 +379,15 @@ extern "C" csa2_status csa2_sparse_attn_decode(const csa2_kv_planes* kv, int32_t
   const int smem = (int)sizeof(AttnSmem);
   if (cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return CSA2_ERR_CUDA;
-  k_attn_tc<<<dim3(nchunks, B), kAT, smem, st>>>(kv->kv_codes, kv->kv_scales, kv->seq_stride, topk, k,
-                                                 swa_e4m3, n_swa, (const uint16_t*)q_bf16, softmax_scale,
-                                                 nchunks, L.part_o, L.part_ml, ws);
-  k_attn_merge<<<B * kHAtt, 128, 0, st>>>(L.part_o, L.part_ml, nchunks, out, lse_out);
+  {
+    KernelTimer timer("k_attn_tc", st);
+    k_attn_tc<<<dim3(nchunks, B), kAT, smem, st>>>(kv->kv_codes, kv->kv_scales, kv->seq_stride, topk, k,
+                                                   swa_e4m3, n_swa, (const uint16_t*)q_bf16, softmax_scale,
+                                                   nchunks, L.part_o, L.part_ml, ws);
+  }
+  {
+    KernelTimer timer("k_attn_merge", st);
+    k_attn_merge<<<B * kHAtt, 128, 0, st>>>(L.part_o, L.part_ml, nchunks, out, lse_out);
+  }
   return launch_status();
 }

@@ -8,6 +8,7 @@
 // Cbar (fp32) to the workspace; a second kernel projects K^I in fp32; the codec
 // kernels quantize both into the planes.
 #include "codec.cuh"
+#include "timing.cuh"
 
 namespace csa2 {
 
@@ -200,9 +201,15 @@ extern "C" csa2_status csa2_cache_write(const void* H_bf16, int64_t T, int32_t d
   if (cudaFuncSetAttribute(k_cw_gemm_pool, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
     return CSA2_ERR_CUDA;
-  k_cw_gemm_pool<<<dim3((unsigned)cdiv(T, kTM), kDMain / kTN), kCT, smem, st>>>(
-      (const uint16_t*)H_bf16, T, d_model, (const uint16_t*)Wkv_bf16, (const uint16_t*)Wz_bf16, m, L.cbar);
-  k_cw_ki<<<(unsigned)cdiv(n, 64), 256, 0, st>>>(L.cbar, (const uint16_t*)Wik_bf16, n, L.ki);
+  {
+    KernelTimer timer("k_cw_gemm_pool", st);
+    k_cw_gemm_pool<<<dim3((unsigned)cdiv(T, kTM), kDMain / kTN), kCT, smem, st>>>(
+        (const uint16_t*)H_bf16, T, d_model, (const uint16_t*)Wkv_bf16, (const uint16_t*)Wz_bf16, m, L.cbar);
+  }
+  {
+    KernelTimer timer("k_cw_ki", st);
+    k_cw_ki<<<(unsigned)cdiv(n, 64), 256, 0, st>>>(L.cbar, (const uint16_t*)Wik_bf16, n, L.ki);
+  }
   launch_quantize(L.cbar, L.ki, n, dst, (int64_t)seq * dst->seq_stride + entry_offset, st);
   return launch_status();
 }

@@ -3,6 +3,7 @@
 // cache compression", section 5 (s_g = E4M3(max|x|/6), xhat = s_g E2M1(x/s_g));
 // "DeepSeek-V4.1-Flash course, 02 Architecture", 2.4.4 (OCP MXFP4 indexer key).
 #include "codec.cuh"
+#include "timing.cuh"
 
 namespace csa2 {
 
@@ -25,11 +26,13 @@ void launch_quantize(const float* Cbar, const float* KI, int64_t n, const csa2_k
   if (n <= 0) return;
   if (Cbar) {
     int64_t threads = n * 32;
+    KernelTimer timer("k_quantize_main", st);
     k_quantize_main<<<(unsigned)cdiv(threads, 256), 256, 0, st>>>(
         Cbar, n, dst->kv_codes + e0 * 256, dst->kv_scales + e0 * 32);
   }
   if (KI) {
     int64_t threads = n * 4;
+    KernelTimer timer("k_quantize_index", st);
     k_quantize_index<<<(unsigned)cdiv(threads, 256), 256, 0, st>>>(
         KI, n, dst->ix_codes + e0 * 64, dst->ix_scales + e0 * 4);
   }

@@ -10,6 +10,7 @@
 
 #include "common.cuh"
 #include "index_scan.cuh"
+#include "timing.cuh"
 
 namespace csa2 {
 
@@ -566,6 +567,7 @@ void launch_select_res(const SelectArgs& a, int B, int ncl, int64_t per, cudaStr
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  KernelTimer timer("k_select_res", st);
   cudaLaunchKernelEx(&cfg, k_select_res<NT>, a);
 }
 
@@ -575,8 +577,10 @@ void launch_select(const SelectArgs& a, int B, cudaStream_t st) {
   const int64_t per = (int64_t)align_up((size_t)cdiv(ncand_max, kSelCluster), kSelItems);
   if (per <= kResCap) {
     launch_select_res<256>(a, B, kSelCluster, per, st);
-  } else
+  } else {
+    KernelTimer timer("k_select", st);
     k_select<<<B * kSelCluster, kSelThreads, 0, st>>>(a);
+  }
 }
 
 // ------------------------------------------------------------------ workspace

@@ -48,6 +48,7 @@
 #include "index_scan.cuh"
 #include "codec.cuh"
 #include "ptx.cuh"
+#include "timing.cuh"
 
 namespace csa2 {
 
@@ -524,6 +525,7 @@ csa2_status launch_scan(const csa2_kv_planes* kv, int32_t B, const int32_t* n_en
   const int S = choose_ctas_per_query(tiles, B, 2 * sms);
   ScanParams p{kv->ix_codes, kv->ix_scales, kv->seq_stride, n_entries, n_max, q, w, pool, keep,
                ncand_max, S, scores, score_stride, bmax, bmax_stride, ws};
+  KernelTimer timer("k_scan_tc", st);
   k_scan_tc<<<dim3((unsigned)S, (unsigned)B), kThreads, smem, st>>>(p, map_tile, map_block);
   return cudaGetLastError() == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
 }

@@ -225,6 +225,27 @@ typedef enum { CSA2_LAYER_SWA = 0, CSA2_LAYER_FULL = 1, CSA2_LAYER_REINDEX = 2,
 csa2_status csa2_v41_layer_table(int32_t n_layers, int32_t* mode, int32_t* m, int32_t* kv_src,
                                  int32_t* topk_src, int32_t* pool_src);
 
+/* ------------------------------------------------------------ kernel timing */
+
+/* Device time per library kernel (instrumentation for users and benchmarks; the
+ * design pages have no counterpart).  While enabled, every kernel the library
+ * launches is bracketed by two CUDA events recorded on its launch stream (two
+ * event records per launch; do not enable it around a stream capture).
+ * csa2_timing_enable(on) first folds and then discards every total, and
+ * switches recording on (on != 0) or off.  Off by default. */
+typedef struct csa2_kernel_time {
+  const char* name;  /* kernel name; valid until the next csa2_timing_enable */
+  int64_t launches;  /* launches recorded since the last csa2_timing_enable    */
+  double total_ms;   /* their summed device time                             */
+} csa2_kernel_time;
+
+csa2_status csa2_timing_enable(int32_t on);
+
+/* Waits for the recorded launches, writes up to `max` totals (sorted by name)
+ * to `out` (host; may be NULL to count) and returns how many kernels have
+ * totals, or -1 if a CUDA event query failed. */
+int32_t csa2_kernel_times(csa2_kernel_time* out, int32_t max);
+
 /* ------------------------------------------------------------------ errors */
 
 /* Synchronises `stream`, returns the first device-side error recorded in the

@@ -135,3 +135,12 @@ def test_workspace_queries(L):
     assert csa2.index_topk_workspace_size(32, 1 << 20, 512, 8, 2048) >= 32 * (1 << 20) * 4
     assert csa2.sparse_attn_workspace_size(32, 512, 128) > 0
     assert csa2.cache_write_workspace_size(131072, 2) >= 65536 * 640 * 4
+
+
+def test_kernel_timing_switch_without_gpu(L):
+    """Switching timing on and off and reading totals touch no device when
+    nothing was launched: no totals, status ok."""
+    csa2.timing_enable(True)
+    assert csa2.kernel_times() == {}
+    csa2.timing_enable(False)
+    assert csa2.kernel_times() == {}
