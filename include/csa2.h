@@ -71,7 +71,9 @@ typedef void* csa2_stream; /* a cudaStream_t */
  *   ix_codes  [e][64]   E2M1 codes of the 128-d indexer key, same nibble order.
  *   ix_scales [e][4]    E8M0 scale (2^(b-127)) of elements 32g..32g+31 in byte g.
  * ("DeepSeek-V4.1-Flash: pushing the limits of KV cache compression", section 2:
- *  288 + 68 = 356 bytes per entry.)  Base pointers must be 16-byte aligned. */
+ *  288 + 68 = 356 bytes per entry.)  Base pointers must be 16-byte aligned, and
+ *  ix_codes 32-byte aligned (the indexer reads it with packed 4-bit tensor
+ *  loads; csa2_index_topk returns CSA2_ERR_INVALID_ARG otherwise). */
 typedef struct {
   uint8_t* kv_codes;
   uint8_t* kv_scales;
