@@ -171,6 +171,80 @@ def oracle_sample(n_queries: int, steps: int):
 
 # ----------------------------------------------------------------------------- GPU arm
 
+CW_T, CW_D, CW_M, CW_SEED = 131072, 5120, 2, 3
+CW_WORKLOAD = ("prefill cache write: T=131,072 tokens x d_model 5120, m=2 -> 65,536 entries "
+               "(C,Z = H[W_KV|W_Z], softmax pooling, K^I = Cbar W_IK, codec; 23.3 MB of cache)")
+
+
+def run_cache_write(dev, st, calls: int, warmup: int):
+    """The prefill cache write (one csa2_cache_write call per step) on seeded device inputs:
+    ms per call, whole-call TFLOP/s, and k_cw_tc's own TFLOP/s against the measured bf16 peak."""
+    import torch
+
+    import compressed_sparse_attention_nvfp4_gb300 as csa2
+    import synth
+    from synth import workloads as W
+
+    T, d, m = CW_T, CW_D, CW_M
+    n = T // m
+    H = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    Wkv = torch.empty((d, 512), dtype=torch.bfloat16, device=dev)
+    Wz = torch.empty((d, 512), dtype=torch.bfloat16, device=dev)
+    Wik = torch.empty((512, 128), dtype=torch.bfloat16, device=dev)
+    ss = st.cuda_stream
+    synth.dev_normal_bf16(CW_SEED, W.TID_H, T * d, H.data_ptr(), ss)
+    synth.dev_normal_bf16(CW_SEED, W.TID_WKV, d * 512, Wkv.data_ptr(), ss, scale=1.0 / math.sqrt(d))
+    synth.dev_normal_bf16(CW_SEED, W.TID_WZ, d * 512, Wz.data_ptr(), ss, scale=1.0 / math.sqrt(d))
+    synth.dev_normal_bf16(CW_SEED, W.TID_WIK, 512 * 128, Wik.data_ptr(), ss, scale=1.0 / math.sqrt(512))
+    P = csa2.Planes.empty(1, n, dev)
+    ws = csa2.workspace(csa2.cache_write_workspace_size(T, d, m), dev)
+    torch.cuda.synchronize()
+
+    def call():
+        csa2.cache_write(H, T, d, Wkv, Wz, Wik, m, P, 0, 0, ws, stream=st)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    assert csa2.check(ws, st)[0] == 0
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for _ in range(calls):
+        call()
+    b.record(st)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / calls
+    csa2.timing_enable(True)
+    for _ in range(calls):
+        call()
+    torch.cuda.synchronize()
+    kt = csa2.kernel_times()
+    csa2.timing_enable(False)
+    assert csa2.check(ws, st)[0] == 0
+    gemm_flop = 2.0 * T * d * 2 * 512
+    all_flop = gemm_flop + 2.0 * n * 512 * 128
+    tc_n, tc_ms = kt.get("k_cw_tc", (0, 0.0))
+    tc_avg = tc_ms / max(tc_n, 1)
+    achieved = gemm_flop / (tc_avg * 1e-3) / 1e12 if tc_n else 0.0
+    peak, kind = tensor_peak()
+    return {
+        "workload": CW_WORKLOAD, "calls": calls, "ms_per_call": round(ms, 4),
+        "tflops_per_call": round(all_flop / (ms * 1e-3) / 1e12, 1),
+        "kernels_ms_per_launch": {k: round(t / max(c, 1), 4) for k, (c, t) in sorted(kt.items())},
+        "roofline": {"kernel": "k_cw_tc (bf16 tcgen05 GEMM + pooling)", "bound": "tensor",
+                     "achieved": round(achieved, 1), "peak": peak, "peak_kind": kind, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4) if peak else None,
+                     "algorithmic_flop_per_launch": gemm_flop, "launch_ms": round(tc_avg, 4)},
+    }
+
+
+def tensor_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return float(json.load(open(p))["bf16_tflops"]), "measured bf16 (burst)"
+    return 1900.0, "fallback bf16 (burst)"
+
+
 def run_ours(args, rank, world, local_rank):
     import numpy as np
     import torch
@@ -328,6 +402,8 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": launches,
         "clocks": clocks,
     }
+    if not args.no_cache_write:
+        line["cache_write"] = run_cache_write(dev, st, 5, 2)
     return line
 
 
@@ -338,6 +414,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cache-write", action="store_true",
+                    help="skip the prefill cache-write measurement (its own object in the line)")
+    ap.add_argument("--cache-write-only", action="store_true",
+                    help="profiling case: only the prefill cache write, printed as its own line")
     ap.add_argument("--batch", type=int, default=32,
                     help="queries per step; values other than 32 are for small profiling cases, "
                          "not for the reported metric")
@@ -375,6 +455,19 @@ def main():
 
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
+    if args.cache_write_only:
+        import torch
+
+        torch.cuda.set_device(local_rank)
+        import compressed_sparse_attention_nvfp4_gb300 as csa2
+
+        csa2.lib()
+        dev = torch.device("cuda", local_rank)
+        st = torch.cuda.Stream(device=dev)
+        if rank == 0:
+            print(json.dumps({"cache_write": run_cache_write(dev, st, max(1, min(args.steps, 20)),
+                                                             max(1, args.warmup))}), flush=True)
+        return
     line = run_ours(args, rank, world, local_rank)
     if line is not None:
         if world == 1 and not args.no_cpu_baseline:

@@ -62,7 +62,7 @@ def lib() -> ctypes.CDLL:
             "csa2_quantize_entries": ([vp, vp, i64, pl, i64, vp], ctypes.c_int),
             "csa2_cache_write": ([vp, i64, i32, vp, vp, vp, i32, pl, i32, i64, vp, sz, vp],
                                  ctypes.c_int),
-            "csa2_cache_write_workspace_size": ([i64, i32], sz),
+            "csa2_cache_write_workspace_size": ([i64, i32, i32], sz),
             "csa2_index_topk": ([pl, i32, vp, i64, vp, vp, i32, ctypes.c_int, i32, i32, vp, vp, vp,
                                  vp, vp, sz, vp], ctypes.c_int),
             "csa2_index_topk_workspace_size": ([i32, i64, i32, i32, i32], sz),
@@ -160,8 +160,8 @@ def quantize_entries(planes: Planes, Cbar, KI, n: int, e0: int = 0, stream=None)
                                     _stream(stream)), "csa2_quantize_entries")
 
 
-def cache_write_workspace_size(T: int, m: int) -> int:
-    return lib().csa2_cache_write_workspace_size(T, m)
+def cache_write_workspace_size(T: int, d_model: int, m: int) -> int:
+    return lib().csa2_cache_write_workspace_size(T, d_model, m)
 
 
 def cache_write(H, T: int, d_model: int, Wkv, Wz, Wik, m: int, planes: Planes, seq: int,

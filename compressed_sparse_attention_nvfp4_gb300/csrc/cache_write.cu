@@ -3,11 +3,28 @@
 // tokens and the indexer key K^I = Cbar W_IK ("DeepSeek-V4.1-Flash: pushing the
 // limits of KV cache compression", 4.1), then the cache codec (section 5).
 //
-// First version on the CUDA cores: a 64-token x 64-channel fp32 tile GEMM that
-// computes C and Z of the same channels, pools them in its epilogue and writes
-// Cbar (fp32) to the workspace; a second kernel projects K^I in fp32; the codec
-// kernels quantize both into the planes.
+// The projection runs on the 5th-generation tensor cores (k_cw_tc): a
+// persistent bf16 GEMM whose 128-token x 256-column tiles hold C and Z of the
+// same 128 channels, so that the epilogue can pool them without another pass.
+// Both operands are K-major with 128-byte swizzle: H as given, the weights
+// through a per-call transposed copy Wt[channel block j][C rows | Z rows][d]
+// (k_cw_wt, 2 x d x 512 bf16).  Warp roles: warp 0 loads the A (16 KB) and B
+// (32 KB) tiles of each 64-wide K step with TMA into a 4-stage ring; warp 1
+// allocates tensor memory and issues 4 MMAs (M128 N256 K16, kind::f16, bf16
+// operands, fp32 accumulate) per stage into one of two 256-column accumulators;
+// warps 2-5 read the finished accumulator (thread = token), pool each group of
+// m adjacent tokens with a max-subtracted per-channel softmax through lane
+// shuffles, and write Cbar (fp32).  K^I = Cbar W_IK (fp32 FMA, k_cw_ki) and the
+// codec follow.  A group of 64 tokens spans two lane quarters; m = 64 keeps the
+// CUDA-core kernel k_cw_gemm_pool, which computes the same quantities.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
 #include "codec.cuh"
+#include "index_scan.cuh"
+#include "ptx.cuh"
 #include "timing.cuh"
 
 namespace csa2 {
@@ -149,13 +166,219 @@ __global__ void __launch_bounds__(256) k_cw_ki(const float* __restrict__ cbar,
   }
 }
 
+// ------------------------------------------------------------ tensor-core path
+constexpr int kTcM = 128;         // tokens per tile
+constexpr int kTcN = 256;         // C and Z columns of 128 channels
+constexpr int kTcBK = 64;         // K elements per stage (one 128-byte swizzle row)
+constexpr int kTcStages = 4;
+constexpr int kTcThreads = 192;   // producer, MMA, 4 epilogue warps
+constexpr uint32_t kTcTmemCols = 512;
+constexpr long long kTcWaitBudget = 1LL << 32;
+
+struct __align__(1024) TcSmem {
+  uint8_t A[kTcStages][kTcM * 128];  // H tile, K-major, 128-byte swizzle
+  uint8_t B[kTcStages][kTcN * 128];  // Wt tile, K-major, 128-byte swizzle
+  uint64_t full[kTcStages], empty[kTcStages];
+  uint64_t acc_full[2], acc_free[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// Wt[j][r][k] (j = 128-channel block, r < 128: W_KV column 128j + r, r >= 128:
+// W_Z column 128j + r - 128), 32 x 32 tiles through shared memory
+__global__ void __launch_bounds__(256) k_cw_wt(const uint16_t* __restrict__ Wkv,
+                                               const uint16_t* __restrict__ Wz, int d,
+                                               uint16_t* __restrict__ Wt) {
+  __shared__ uint16_t tile[32][33];
+  const int k0 = blockIdx.x * 32;    // K rows of W
+  const int row0 = blockIdx.y * 32;  // Wt rows (0 .. 1023)
+  const int j = row0 / 256, rr = row0 % 256;
+  const uint16_t* src = rr < 128 ? Wkv : Wz;
+  const int c0 = 128 * j + (rr % 128);
+  const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
+  for (int i = ty; i < 32; i += 8) tile[i][tx] = src[(int64_t)(k0 + i) * kDMain + c0 + tx];
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) Wt[(int64_t)(row0 + i) * d + k0 + tx] = tile[tx][i];
+}
+
+__device__ __forceinline__ void tc_abort(TcSmem& S, void* ws, int where) {
+  *reinterpret_cast<volatile int*>(&S.abort_flag) = 1;
+  report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, where);
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    k_cw_tc(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w, int64_t T,
+            int d, int m, float* __restrict__ cbar, void* ws) {
+  extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
+  TcSmem& S = *reinterpret_cast<TcSmem*>(tc_smem_raw);
+  volatile int* abort_flag = &S.abort_flag;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t token_tiles = cdiv(T, kTcM);
+  const int64_t ntiles = token_tiles * (kDMain / 128);
+  const int nk = d / kTcBK;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      ptx::mbar_init(&S.full[s], 1);
+      ptx::mbar_init(&S.empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&S.acc_full[a], 1);
+      ptx::mbar_init(&S.acc_free[a], 4);
+    }
+    S.abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) ptx::tmem_alloc(&S.tmem_base, kTcTmemCols);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const int t0 = (int)((tile / 4) * kTcM), j = (int)(tile % 4);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!ptx::mbar_wait(&S.empty[s], ph ^ 1u, abort_flag, kTcWaitBudget)) {
+            tc_abort(S, ws, 31);
+            goto producer_done;
+          }
+          ptx::mbar_arrive_expect_tx(&S.full[s], (kTcM + kTcN) * 128);
+          ptx::tma_load_2d(S.A[s], &map_h, kb * kTcBK, t0, &S.full[s]);
+          ptx::tma_load_2d(S.B[s], &map_w, kb * kTcBK, j * kTcN, &S.full[s]);
+          if (++s == kTcStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+    }
+  producer_done:;
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idesc = ptx::idesc_f16(kTcM, kTcN, 1);
+      int s = 0, local = 0;
+      uint32_t ph = 0;
+      for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
+        const int a = local & 1;
+        const uint32_t u = (uint32_t)(local >> 1) & 1u;
+        if (!ptx::mbar_wait(&S.acc_free[a], u ^ 1u, abort_flag, kTcWaitBudget)) {
+          tc_abort(S, ws, 32);
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_t = tmem + (uint32_t)a * kTcN;
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!ptx::mbar_wait(&S.full[s], ph, abort_flag, kTcWaitBudget)) {
+            tc_abort(S, ws, 33);
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint64_t ad = ptx::smem_desc_sw128(S.A[s], 1024);
+          const uint64_t bd = ptx::smem_desc_sw128(S.B[s], 1024);
+#pragma unroll
+          for (int kk = 0; kk < kTcBK / 16; ++kk)  // 16 bf16 = 32 bytes per K step
+            ptx::mma_f16_ss(d_t, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc,
+                            (kb | kk) ? 1u : 0u);
+          ptx::mma_commit(&S.empty[s]);  // the stage is free once these MMAs have read it
+          if (++s == kTcStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(&S.acc_full[a]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int sub = warp % 4;  // lane quarter: tokens 32 sub .. 32 sub + 31 of the tile
+    const uint32_t lane_addr = tmem + ((uint32_t)(sub * 32) << 16);
+    const int64_t n = T / m;
+    int local = 0;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
+      const int a = local & 1;
+      const uint32_t u = (uint32_t)(local >> 1) & 1u;
+      if (!ptx::mbar_wait_warp(&S.acc_full[a], u, abort_flag, kTcWaitBudget)) {
+        tc_abort(S, ws, 34);
+        break;
+      }
+      ptx::tc_fence_after();
+      const int64_t t = (tile / 4) * kTcM + sub * 32 + lane;  // this thread's token
+      const int ch0 = (int)(tile % 4) * 128;
+      const int64_t e = t / m;                               // its entry
+      const bool writer = (lane % m) == 0 && e < n;           // first token of its group
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t cr[32], zr[32];
+        const uint32_t base = lane_addr + (uint32_t)a * kTcN + (uint32_t)cb * 32u;
+        ptx::tmem_ld_32x32b_x32(base, cr);
+        ptx::tmem_ld_32x32b_x32(base + 128u, zr);
+        ptx::tmem_wait_ld();
+        float v[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float cv = __uint_as_float(cr[c]), zv = __uint_as_float(zr[c]);
+          if (m == 1) {
+            v[c] = cv;  // the softmax over one token is exactly 1
+          } else {
+            float zmax = zv;
+            for (int o = 1; o < m; o <<= 1) zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, o));
+            const float ez = expf(zv - zmax);
+            float num = ez * cv, den = ez;
+            for (int o = 1; o < m; o <<= 1) {
+              num += __shfl_xor_sync(0xffffffffu, num, o);
+              den += __shfl_xor_sync(0xffffffffu, den, o);
+            }
+            v[c] = __fdiv_rn(num, den);
+          }
+        }
+        if (writer) {
+          float4* dst = reinterpret_cast<float4*>(cbar + e * kDMain + ch0 + cb * 32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&S.acc_free[a]);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTcTmemCols);
+  }
+}
+
+bool make_bf16_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kTcBK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct CwWs {
   float* cbar;
   float* ki;
+  uint16_t* wt;
   size_t bytes;
 };
 
-CwWs cw_ws_layout(void* ws, int64_t n) {
+CwWs cw_ws_layout(void* ws, int64_t n, int64_t d_model) {
   CwWs L;
   char* base = (char*)ws;
   size_t off = kWsHeader;
@@ -163,6 +386,8 @@ CwWs cw_ws_layout(void* ws, int64_t n) {
   off += align_up((size_t)n * kDMain * 4, 256);
   L.ki = (float*)(base ? base + off : nullptr);
   off += align_up((size_t)n * kDIdx * 4, 256);
+  L.wt = (uint16_t*)(base ? base + off : nullptr);
+  off += align_up((size_t)2 * kDMain * d_model * 2, 256);
   L.bytes = off;
   return L;
 }
@@ -171,9 +396,9 @@ CwWs cw_ws_layout(void* ws, int64_t n) {
 
 }  // namespace csa2
 
-extern "C" size_t csa2_cache_write_workspace_size(int64_t T, int32_t m) {
-  if (T < 0 || m < 1) return 0;
-  return csa2::cw_ws_layout(nullptr, T / m).bytes;
+extern "C" size_t csa2_cache_write_workspace_size(int64_t T, int32_t d_model, int32_t m) {
+  if (T < 0 || m < 1 || d_model < 0) return 0;
+  return csa2::cw_ws_layout(nullptr, T / m, d_model).bytes;
 }
 
 extern "C" csa2_status csa2_cache_write(const void* H_bf16, int64_t T, int32_t d_model,
@@ -193,15 +418,35 @@ extern "C" csa2_status csa2_cache_write(const void* H_bf16, int64_t T, int32_t d
   const int64_t n = T / m;
   if (entry_offset + n > dst->seq_stride) return CSA2_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, 256)) return CSA2_ERR_WORKSPACE;
-  CwWs L = cw_ws_layout(ws, n);
+  CwWs L = cw_ws_layout(ws, n, d_model);
   if (ws_bytes < L.bytes) return CSA2_ERR_WORKSPACE;
   if (reset_error(ws, st) != CSA2_OK) return CSA2_ERR_CUDA;
   if (T == 0) return CSA2_OK;
-  const int smem = (int)sizeof(GemmSmem);
-  if (cudaFuncSetAttribute(k_cw_gemm_pool, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-      cudaSuccess)
-    return CSA2_ERR_CUDA;
-  {
+  if (m <= 32 && T < ((int64_t)1 << 31)) {
+    // tensor cores: transposed weights, then the persistent GEMM + pooling
+    {
+      KernelTimer timer("k_cw_wt", st);
+      k_cw_wt<<<dim3((unsigned)(d_model / 32), 2 * kDMain / 32), 256, 0, st>>>(
+          (const uint16_t*)Wkv_bf16, (const uint16_t*)Wz_bf16, d_model, L.wt);
+    }
+    CUtensorMap map_h, map_w;
+    if (!make_bf16_map(&map_h, H_bf16, T, d_model, kTcM) || !make_bf16_map(&map_w, L.wt, 2 * kDMain, d_model, kTcN))
+      return CSA2_ERR_CUDA;
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CSA2_ERR_CUDA;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int smem = (int)sizeof(TcSmem);
+    if (cudaFuncSetAttribute(k_cw_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return CSA2_ERR_CUDA;
+    const int64_t ntiles = cdiv(T, kTcM) * (kDMain / 128);
+    const int grid = (int)std::min<int64_t>(ntiles, sms);
+    KernelTimer timer("k_cw_tc", st);
+    k_cw_tc<<<grid, kTcThreads, smem, st>>>(map_h, map_w, T, d_model, m, L.cbar, ws);
+  } else {
+    const int smem = (int)sizeof(GemmSmem);
+    if (cudaFuncSetAttribute(k_cw_gemm_pool, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return CSA2_ERR_CUDA;
     KernelTimer timer("k_cw_gemm_pool", st);
     k_cw_gemm_pool<<<dim3((unsigned)cdiv(T, kTM), kDMain / kTN), kCT, smem, st>>>(
         (const uint16_t*)H_bf16, T, d_model, (const uint16_t*)Wkv_bf16, (const uint16_t*)Wz_bf16, m, L.cbar);

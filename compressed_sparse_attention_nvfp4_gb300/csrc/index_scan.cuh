@@ -2,9 +2,16 @@
 // hierarchical build, the max of every 8-entry block.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 
 namespace csa2 {
+
+// cuTensorMapEncodeTiled from the driver (null if unavailable); shared by the
+// kernels that build tensor maps.
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn();
 
 // Scores the candidates of B queries (query b reads sequence slot b).
 // ncand_max: entries (pool == nullptr; n_entries[b] <= n_max are visible) or

@@ -118,12 +118,15 @@ csa2_status csa2_quantize_entries(const float* Cbar, const float* KI, int64_t n,
  * ("DeepSeek-V4.1-Flash course, 02 Architecture", 2.2 Eq. (1) and 2.3;
  *  "DeepSeek-V4.1-Flash: pushing the limits of KV cache compression", 4.1.)
  *   H [T][d_model] bf16; W_KV, W_Z [d_model][512] bf16; W_IK [512][128] bf16.
- * Requires T % m == 0, 1 <= m <= 64 with 64 % m == 0, d_model % 64 == 0. */
+ * Requires T % m == 0, 1 <= m <= 64 with 64 % m == 0, d_model % 64 == 0.
+ * The projection runs on the tensor cores (bf16 operands, fp32 accumulation)
+ * for m <= 32 and on the CUDA cores (fp32) for m = 64; the workspace also holds
+ * a transposed copy of W_KV and W_Z (2 * d_model * 512 bf16). */
 csa2_status csa2_cache_write(const void* H_bf16, int64_t T, int32_t d_model, const void* Wkv_bf16,
                              const void* Wz_bf16, const void* Wik_bf16, int32_t m,
                              const csa2_kv_planes* dst, int32_t seq, int64_t entry_offset,
                              void* ws, size_t ws_bytes, csa2_stream stream);
-size_t csa2_cache_write_workspace_size(int64_t T, int32_t m);
+size_t csa2_cache_write_workspace_size(int64_t T, int32_t d_model, int32_t m);
 
 /* ---------------------------------------------------------- indexer + top-k */
 

@@ -4,8 +4,10 @@ Top-k: the GPU set must hold every entry whose oracle score exceeds the
 oracle's k-th score tau by more than 1e-3 relative, and no entry below tau by
 more than that; it has exactly min(k, valid) distinct entries, ascending, -1
 padded.  Attention: max |gpu - oracle| <= 1e-2 * RMS(oracle) per query.
-Cache bytes: identical wherever the oracle's pre-quantization values are more
-than 1e-5 (relative) from every rounding decision point.
+Cache bytes: identical for the codec on identical fp32 inputs; for the cache
+write, identical in every group whose rounding decisions lie farther from the
+oracle's pre-quantization values than the error bound of the GPU's fp32
+accumulation (test_gpu_cache_write.py states the bound).
 """
 from __future__ import annotations
 

@@ -1,5 +1,22 @@
 """csa2_cache_write against the oracle: 100% identical bytes on dyadic inputs
-(every sum exact), and banded identity on Gaussian inputs at m = 2."""
+(every sum exact), and on Gaussian inputs identical bytes in every quantization
+group whose decisions are fixed by the mathematics, i.e. farther from every
+rounding boundary than the error bound of the GPU's fp32 accumulation.
+
+Error model.  C = H W_KV and Z = H W_Z are d-term sums of exact bf16 x bf16
+products accumulated in fp32 (in any order, on the tensor cores), so each is
+within KAPPA * u * sum_k |h_k w_k| of the exact value, u = 2^-24; KAPPA = 32 is
+three times the worst case measured over 262,144 outputs at d = 5120 (10.2 u)
+and far below the d * u of the worst-case bound.  Pooling a group of m tokens
+with softmax weights p_i moves Cbar = sum_i p_i C_i by at most max eps_C plus,
+to first order in the Z errors (dp_i = p_i (dz_i - sum_j p_j dz_j)),
+max eps_Z * sum_i p_i |C_i - Cbar|, plus a few roundings of the fp32 exp and
+division;
+K^I = Cbar W_IK (512-term fp32 sum) inherits the channels' errors, which are
+independent roundings of independent accumulations, so their effect is bounded
+by the root-sum-square sqrt(sum_c (eps_Cbar_c W_IK_c)^2) of the per-channel
+bounds (each ~16 standard deviations), plus its own KAPPA * u * sum_c |Cbar_c
+W_IK|."""
 import numpy as np
 import pytest
 
@@ -7,7 +24,9 @@ from gpu_common import csa2, require_gpu, to_dev, torch
 from synth import workloads as W
 
 pytestmark = pytest.mark.gpu
-DELTA = 1e-5
+U = 2.0 ** -24
+KAPPA = 32.0
+MID = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -28,7 +47,7 @@ def _gpu_write(H, Wkv, Wz, Wik, m, seq=1, offset=5, stride=None):
     P = csa2.Planes.empty(seq + 1, stride)
     for t in (P.kv_codes, P.kv_scales, P.ix_codes, P.ix_scales):
         t.fill_(0xA5)
-    ws = csa2.workspace(csa2.cache_write_workspace_size(T, m))
+    ws = csa2.workspace(csa2.cache_write_workspace_size(T, d, m))
     csa2.cache_write(to_dev(H.view(np.int16)), T, d, to_dev(Wkv.view(np.int16)),
                      to_dev(Wz.view(np.int16)), to_dev(Wik.view(np.int16)), m, P, seq, offset, ws)
     assert csa2.check(ws)[0] == 0
@@ -53,29 +72,88 @@ def test_dyadic_bytes_exact(oracle_mod, T, d):
         assert np.array_equal(g, r), name
 
 
-def _group_bytes_ok(got_codes, got_scales, ref_codes, ref_scales, margins, group_bytes):
-    """Groups far from a decision point must match exactly; returns (#exact-checked, #banded)."""
+def _f64(bf16):
+    return (np.asarray(bf16).view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _error_bounds(H, Wkv, Wz, Wik, m, cb):
+    """Absolute error bounds of the GPU's Cbar [n,512] and K^I [n,128] (module docstring)."""
+    Hf, Cw, Zw, Iw = _f64(H), _f64(Wkv), _f64(Wz), _f64(Wik)
+    C, Z = Hf @ Cw, Hf @ Zw
+    eC = KAPPA * U * (np.abs(Hf) @ np.abs(Cw))
+    eZ = KAPPA * U * (np.abs(Hf) @ np.abs(Zw))
+    n = C.shape[0] // m
+    g = lambda a: a.reshape(n, m, -1)
+    zg = g(Z)
+    p = np.exp(zg - zg.max(1, keepdims=True))
+    p /= p.sum(1, keepdims=True)
+    spread = (p * np.abs(g(C) - cb[:, None, :])).sum(1)
+    eCb = g(eC).max(1) + g(eZ).max(1) * spread + 8.0 * U * np.abs(cb)
+    eKI = np.sqrt((eCb ** 2) @ (Iw ** 2)) + KAPPA * U * (np.abs(cb) @ np.abs(Iw))
+    return eCb, eKI
+
+
+def _decided_main(x, e, e4m3_mids, oracle_mod):
+    """Groups of 16 whose E4M3 scale and E2M1 codes (with signs) are fixed within the bounds."""
+    n = x.shape[0]
+    xg, eg = x.reshape(n, -1, 16), e.reshape(n, -1, 16)
+    amax = np.abs(xg).max(-1)
+    emax = eg.max(-1)
+    t = amax / 6.0
+    d_scale = np.abs(t[..., None] - e4m3_mids).min(-1)
+    ok = d_scale > emax / 6.0
+    s = np.vectorize(lambda v: oracle_mod.e4m3_value(oracle_mod.e4m3_encode(float(v))))(t)
+    s = np.where(s > 0, s, np.inf)
+    y = np.abs(xg) / s[..., None]
+    d_el = np.minimum(np.abs(y[..., None] - MID).min(-1), y) * s[..., None]  # y itself: the sign of a zero
+    return ok & (d_el > eg).all(-1)
+
+
+def _decided_index(x, e):
+    """Groups of 32 whose E8M0 scale and E2M1 codes (with signs) are fixed within the bounds."""
+    n = x.shape[0]
+    xg, eg = x.reshape(n, -1, 32), e.reshape(n, -1, 32)
+    amax = np.abs(xg).max(-1)
+    emax = eg.max(-1)
+    ex = np.floor(np.log2(np.where(amax > 0, amax, 1.0)))
+    lo, hi = 2.0 ** ex, 2.0 ** (ex + 1)
+    ok = np.minimum(amax - lo, hi - amax) > emax
+    X = 2.0 ** np.maximum(ex - 2, -127)
+    y = np.abs(xg) / X[..., None]
+    d_el = np.minimum(np.abs(y[..., None] - MID).min(-1), y) * X[..., None]
+    return ok & (d_el > eg).all(-1)
+
+
+def _group_bytes_ok(got_codes, got_scales, ref_codes, ref_scales, decided, group_bytes):
+    """Decided groups must match exactly; the others may move the scale by one code."""
     n, ng = ref_scales.shape
     gc = got_codes.reshape(n, ng, group_bytes)
     rc = ref_codes.reshape(n, ng, group_bytes)
-    far = margins.reshape(n, ng) > DELTA
     same = (gc == rc).all(-1) & (got_scales == ref_scales)
-    bad = far & ~same
-    assert not bad.any(), f"{bad.sum()} far-from-boundary groups differ, first {np.argwhere(bad)[:3]}"
-    near = ~far
-    # groups inside the band: the scale byte may move by at most one code
+    bad = decided & ~same
+    assert not bad.any(), f"{bad.sum()} decided groups differ, first {np.argwhere(bad)[:3]}"
     ds = np.abs(got_scales.astype(int) - ref_scales.astype(int))
-    assert np.all(ds[near] <= 1)
-    return int(far.sum()), int(near.sum())
+    assert np.all(ds[~decided] <= 1)
+    return int(decided.sum()), int((~decided).sum())
 
 
-def test_gaussian_m2_banded(oracle_mod):
-    T, d = 512, 5120
+@pytest.mark.parametrize("T,d,m", [
+    (512, 5120, 2),   # the model's d_model, several token tiles
+    (200, 1024, 2),   # a partial last token tile
+    (256, 1024, 4),   # pooling over 4 lanes
+    (1024, 1024, 32),  # a whole lane quarter per group
+    (1536, 1024, 64),  # groups across lane quarters: the CUDA-core kernel
+])
+def test_gaussian_banded(oracle_mod, T, d, m):
     H, Wkv, Wz, Wik = W.cache_write_inputs(3, T, d)
-    got = _gpu_write(H, Wkv, Wz, Wik, 2)
-    kvc, kvs, ixc, ixs, cb, ki = oracle_mod.cache_write(H, Wkv, Wz, Wik, 2, return_prequant=True)
-    mm = oracle_mod.main_group_margins(cb.astype(np.float32).astype(np.float64))
-    mi = oracle_mod.index_group_margins(ki.astype(np.float32).astype(np.float64))
-    f1, b1 = _group_bytes_ok(got[0], got[1], kvc, kvs, mm, 8)
-    f2, b2 = _group_bytes_ok(got[2], got[3], ixc, ixs, mi, 16)
-    assert f1 > 0.99 * (f1 + b1) and f2 > 0.99 * (f2 + b2)
+    got = _gpu_write(H, Wkv, Wz, Wik, m)
+    kvc, kvs, ixc, ixs, cb, ki = oracle_mod.cache_write(H, Wkv, Wz, Wik, m, return_prequant=True)
+    eCb, eKI = _error_bounds(H, Wkv, Wz, Wik, m, cb)
+    e4m3_mids = np.array([0.5 * (oracle_mod.e4m3_value(c) + oracle_mod.e4m3_value(c + 1)) for c in range(126)])
+    # the oracle quantizes fp32(Cbar) and fp32(K^I): decisions are taken on those values
+    cb32 = cb.astype(np.float32).astype(np.float64)
+    ki32 = ki.astype(np.float32).astype(np.float64)
+    f1, b1 = _group_bytes_ok(got[0], got[1], kvc, kvs, _decided_main(cb32, eCb, e4m3_mids, oracle_mod), 8)
+    f2, b2 = _group_bytes_ok(got[2], got[3], ixc, ixs, _decided_index(ki32, eKI), 16)
+    # the bounds leave the test its teeth: most groups are decided
+    assert f1 > 0.8 * (f1 + b1) and f2 > 0.8 * (f2 + b2), (f1, b1, f2, b2)

@@ -72,6 +72,9 @@ def adversarial_index(rng, n):
 
 def _run_codec(x_main, x_idx):
     n = max(x_main.shape[0], x_idx.shape[0])
+    # both inputs must hold n rows: the entry point reads n rows of each
+    x_main = np.concatenate([x_main, np.zeros((n - x_main.shape[0], 512), np.float32)])
+    x_idx = np.concatenate([x_idx, np.zeros((n - x_idx.shape[0], 128), np.float32)])
     P = csa2.Planes.empty(1, n)
     csa2.quantize_entries(P, to_dev(x_main), to_dev(x_idx), n, 0)
     torch.cuda.synchronize()
