@@ -127,42 +127,69 @@ __global__ void __launch_bounds__(kCT) k_cw_gemm_pool(const uint16_t* __restrict
   }
 }
 
-// K^I[n][128] = Cbar[n][512] W_IK[512][128] in fp32; one CTA per 64 entries.
+// K^I[n][128] = Cbar[n][512] W_IK[512][128] in fp32 FMA (sequential over the 512
+// channels).  One CTA per 128 entries x 128 outputs; thread (ty, tx) accumulates an
+// 8 x 8 block (entries 8ty.., outputs 8tx..) from k-major shared tiles: per channel
+// two 16-byte loads of Cbar and two of W_IK feed 64 FMAs.
+constexpr int kKiE = 128, kKiK = 16;
+
 __global__ void __launch_bounds__(256) k_cw_ki(const float* __restrict__ cbar,
                                                const uint16_t* __restrict__ Wik, int64_t n,
                                                float* __restrict__ ki) {
-  __shared__ float Ws[32][kDIdx];
-  __shared__ float Cs[64][33];
-  const int64_t e0 = (int64_t)blockIdx.x * 64;
-  const int ty = threadIdx.x / 32, tx = threadIdx.x % 32;  // rows ty*8.., cols tx*4..
-  float acc[8][4] = {};
-  for (int k0 = 0; k0 < kDMain; k0 += 32) {
-    for (int i = threadIdx.x; i < 32 * kDIdx; i += 256)
-      Ws[i / kDIdx][i % kDIdx] = bf16_bits_to_float(Wik[(int64_t)(k0 + i / kDIdx) * kDIdx + i % kDIdx]);
-    for (int i = threadIdx.x; i < 64 * 32; i += 256) {
-      const int64_t e = e0 + i / 32;
-      Cs[i / 32][i % 32] = e < n ? cbar[e * kDMain + k0 + i % 32] : 0.0f;
+  __shared__ __align__(16) float Cs[kKiK][kKiE];   // Cs[k][entry]
+  __shared__ __align__(16) float Ws[kKiK][kDIdx];  // Ws[k][output]
+  const int64_t e0 = (int64_t)blockIdx.x * kKiE;
+  const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
+  float acc[8][8] = {};
+  for (int k0 = 0; k0 < kDMain; k0 += kKiK) {
+    {  // Cbar tile: 128 entries x 16 channels (one float4 of 4 channels per thread, twice)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int idx = threadIdx.x + 256 * r;  // 0..511
+        const int ent = idx / 4, c4 = (idx % 4) * 4;
+        const int64_t e = e0 + ent;
+        const float4 v = e < n ? *reinterpret_cast<const float4*>(cbar + e * kDMain + k0 + c4)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        Cs[c4][ent] = v.x;
+        Cs[c4 + 1][ent] = v.y;
+        Cs[c4 + 2][ent] = v.z;
+        Cs[c4 + 3][ent] = v.w;
+      }
+    }
+    {  // W_IK tile: 16 channels x 128 outputs (8 bf16 per thread)
+      const int kk = threadIdx.x / 16, o8 = (threadIdx.x % 16) * 8;
+      const uint4 raw = *reinterpret_cast<const uint4*>(Wik + (int64_t)(k0 + kk) * kDIdx + o8);
+      const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        Ws[kk][o8 + 2 * i] = __uint_as_float(w4[i] << 16);
+        Ws[kk][o8 + 2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
+      }
     }
     __syncthreads();
-    for (int kk = 0; kk < 32; ++kk) {
-      const float4 wv = *reinterpret_cast<const float4*>(&Ws[kk][tx * 4]);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float c = Cs[ty * 8 + i][kk];
-        acc[i][0] = fmaf(c, wv.x, acc[i][0]);
-        acc[i][1] = fmaf(c, wv.y, acc[i][1]);
-        acc[i][2] = fmaf(c, wv.z, acc[i][2]);
-        acc[i][3] = fmaf(c, wv.w, acc[i][3]);
-      }
+    for (int kk = 0; kk < kKiK; ++kk) {
+      const float4 a0 = *reinterpret_cast<const float4*>(&Cs[kk][ty * 8]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&Cs[kk][ty * 8 + 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&Ws[kk][tx * 8]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Ws[kk][tx * 8 + 4]);
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
     }
     __syncthreads();
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int64_t e = e0 + ty * 8 + i;
-    if (e < n)
-      *reinterpret_cast<float4*>(ki + e * kDIdx + tx * 4) =
-          make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    if (e < n) {
+      float4* dst = reinterpret_cast<float4*>(ki + e * kDIdx + tx * 8);
+      dst[0] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      dst[1] = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+    }
   }
 }
 
@@ -453,7 +480,7 @@ extern "C" csa2_status csa2_cache_write(const void* H_bf16, int64_t T, int32_t d
   }
   {
     KernelTimer timer("k_cw_ki", st);
-    k_cw_ki<<<(unsigned)cdiv(n, 64), 256, 0, st>>>(L.cbar, (const uint16_t*)Wik_bf16, n, L.ki);
+    k_cw_ki<<<(unsigned)cdiv(n, kKiE), 256, 0, st>>>(L.cbar, (const uint16_t*)Wik_bf16, n, L.ki);
   }
   launch_quantize(L.cbar, L.ki, n, dst, (int64_t)seq * dst->seq_stride + entry_offset, st);
   return launch_status();
