@@ -14,8 +14,9 @@
 // operands, fp32 accumulate) per stage into one of two 256-column accumulators;
 // warps 2-5 read the finished accumulator (thread = token), pool each group of
 // m adjacent tokens with a max-subtracted per-channel softmax through lane
-// shuffles, and write Cbar (fp32).  K^I = Cbar W_IK (fp32 FMA, k_cw_ki) and the
-// codec follow.  A group of 64 tokens spans two lane quarters; m = 64 keeps the
+// shuffles, and write Cbar (fp32).  K^I = Cbar W_IK follows on the tensor cores
+// with every product exact (k_cw_ki_tc: Cbar split into three bf16 terms), then
+// the codec.  A group of 64 tokens spans two lane quarters; m = 64 keeps the
 // CUDA-core kernel k_cw_gemm_pool, which computes the same quantities.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -124,72 +125,6 @@ __global__ void __launch_bounds__(kCT) k_cw_gemm_pool(const uint16_t* __restrict
       v = __fdiv_rn(num, den);
     }
     cbar[(t0 / m + g) * kDMain + ch0 + c] = v;
-  }
-}
-
-// K^I[n][128] = Cbar[n][512] W_IK[512][128] in fp32 FMA (sequential over the 512
-// channels).  One CTA per 128 entries x 128 outputs; thread (ty, tx) accumulates an
-// 8 x 8 block (entries 8ty.., outputs 8tx..) from k-major shared tiles: per channel
-// two 16-byte loads of Cbar and two of W_IK feed 64 FMAs.
-constexpr int kKiE = 128, kKiK = 16;
-
-__global__ void __launch_bounds__(256) k_cw_ki(const float* __restrict__ cbar,
-                                               const uint16_t* __restrict__ Wik, int64_t n,
-                                               float* __restrict__ ki) {
-  __shared__ __align__(16) float Cs[kKiK][kKiE];   // Cs[k][entry]
-  __shared__ __align__(16) float Ws[kKiK][kDIdx];  // Ws[k][output]
-  const int64_t e0 = (int64_t)blockIdx.x * kKiE;
-  const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
-  float acc[8][8] = {};
-  for (int k0 = 0; k0 < kDMain; k0 += kKiK) {
-    {  // Cbar tile: 128 entries x 16 channels (one float4 of 4 channels per thread, twice)
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int idx = threadIdx.x + 256 * r;  // 0..511
-        const int ent = idx / 4, c4 = (idx % 4) * 4;
-        const int64_t e = e0 + ent;
-        const float4 v = e < n ? *reinterpret_cast<const float4*>(cbar + e * kDMain + k0 + c4)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-        Cs[c4][ent] = v.x;
-        Cs[c4 + 1][ent] = v.y;
-        Cs[c4 + 2][ent] = v.z;
-        Cs[c4 + 3][ent] = v.w;
-      }
-    }
-    {  // W_IK tile: 16 channels x 128 outputs (8 bf16 per thread)
-      const int kk = threadIdx.x / 16, o8 = (threadIdx.x % 16) * 8;
-      const uint4 raw = *reinterpret_cast<const uint4*>(Wik + (int64_t)(k0 + kk) * kDIdx + o8);
-      const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        Ws[kk][o8 + 2 * i] = __uint_as_float(w4[i] << 16);
-        Ws[kk][o8 + 2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int kk = 0; kk < kKiK; ++kk) {
-      const float4 a0 = *reinterpret_cast<const float4*>(&Cs[kk][ty * 8]);
-      const float4 a1 = *reinterpret_cast<const float4*>(&Cs[kk][ty * 8 + 4]);
-      const float4 b0 = *reinterpret_cast<const float4*>(&Ws[kk][tx * 8]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&Ws[kk][tx * 8 + 4]);
-      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int64_t e = e0 + ty * 8 + i;
-    if (e < n) {
-      float4* dst = reinterpret_cast<float4*>(ki + e * kDIdx + tx * 8);
-      dst[0] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-      dst[1] = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
-    }
   }
 }
 
@@ -386,6 +321,179 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
+// K^I = Cbar W_IK on the tensor cores, exactly in every product: each fp32
+// Cbar value splits into three bf16 terms, hi = its top 8 significant bits
+// (truncated), mid = the next 8 of the remainder, lo = the rest (at most 8
+// bits), so Cbar = hi + mid + lo exactly, and W_IK is bf16 already.  The three
+// terms are three MMA sets into one fp32 accumulator; only the order of the
+// fp32 additions differs from a sequential sum.  One CTA per 128 entries: all
+// of W_IK^T (128 outputs x 512, K-major, 128-byte swizzle) stays in shared
+// memory; threads stream Cbar 64 channels at a time, split it and store the
+// three 128 x 64 operand tiles (two buffers); one thread issues 3 x 4 MMAs
+// (M128 N128 K16) per chunk.
+constexpr int kKtThreads = 256;
+constexpr long long kKtWaitBudget = 1LL << 32;
+
+struct __align__(1024) KtSmem {
+  uint8_t B[8][128 * 128];         // W_IK^T chunk j: 128 outputs x 64 channels
+  uint8_t A[2][3][128 * 128];      // [buffer][hi, mid, lo]: 128 entries x 64 channels
+  uint64_t b_full, a_free[2], done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__global__ void __launch_bounds__(kKtThreads, 1)
+    k_cw_ki_tc(const __grid_constant__ CUtensorMap map_wt, const float* __restrict__ cbar, int64_t n,
+               float* __restrict__ ki, void* ws) {
+  extern __shared__ __align__(1024) unsigned char kt_smem_raw[];
+  KtSmem& S = *reinterpret_cast<KtSmem*>(kt_smem_raw);
+  volatile int* abort_flag = &S.abort_flag;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int64_t e0 = (int64_t)blockIdx.x * 128;
+  if (tid == 0) {
+    ptx::mbar_init(&S.b_full, 1);
+    ptx::mbar_init(&S.a_free[0], 1);
+    ptx::mbar_init(&S.a_free[1], 1);
+    ptx::mbar_init(&S.done, 1);
+    S.abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0) ptx::tmem_alloc(&S.tmem_base, 128);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+  if (tid == 0) {
+    ptx::mbar_arrive_expect_tx(&S.b_full, 8 * 128 * 128);
+    for (int j = 0; j < 8; ++j) ptx::tma_load_2d(S.B[j], &map_wt, 64 * j, 0, &S.b_full);
+  }
+  // thread -> (entry r = tid / 2 .. in two passes, 32 channels = 4 chunks of 8)
+  bool ok = true;
+  for (int j = 0; j < 8; ++j) {
+    const int buf = j & 1;
+    // buffer `buf` is free once the MMAs of chunk j - 2 completed
+    if (j >= 2 && !ptx::mbar_wait(&S.a_free[buf], (uint32_t)((j - 2) >> 1) & 1u, abort_flag, kKtWaitBudget)) {
+      ok = false;
+      report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 43);
+    }
+    if (ok) {
+#pragma unroll
+      for (int pass = 0; pass < 2; ++pass) {
+        const int r = pass * 64 + tid / 4;  // entry row of the tile
+        const int c0 = (tid % 4) * 16;      // 16 channels: two 8-element chunks
+        const int64_t e = e0 + r;
+        float x[16];
+        if (e < n) {
+          const float4* src = reinterpret_cast<const float4*>(cbar + e * kDMain + 64 * j + c0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 v = src[q];
+            x[4 * q] = v.x;
+            x[4 * q + 1] = v.y;
+            x[4 * q + 2] = v.z;
+            x[4 * q + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 16; ++q) x[q] = 0.0f;
+        }
+        uint32_t t3[3][8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          uint32_t h[2], md[2], lw[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const float v = x[2 * q + u];
+            const uint32_t hb = __float_as_uint(v) & 0xFFFF0000u;      // top 8 significant bits
+            const float r1 = v - __uint_as_float(hb);                   // exact
+            const uint32_t mb = __float_as_uint(r1) & 0xFFFF0000u;
+            const float r2 = r1 - __uint_as_float(mb);                  // exact, <= 8 bits left
+            h[u] = hb >> 16;
+            md[u] = mb >> 16;
+            lw[u] = __float_as_uint(r2) >> 16;                          // exact: low half is zero
+          }
+          t3[0][q] = h[0] | (h[1] << 16);
+          t3[1][q] = md[0] | (md[1] << 16);
+          t3[2][q] = lw[0] | (lw[1] << 16);
+        }
+#pragma unroll
+        for (int t = 0; t < 3; ++t)
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int chunk = (c0 / 8) + cc;  // 16-byte chunk of the 128-byte row
+            uint8_t* dst = S.A[buf][t] + r * 128 + ((chunk ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4*>(dst) =
+                make_uint4(t3[t][4 * cc], t3[t][4 * cc + 1], t3[t][4 * cc + 2], t3[t][4 * cc + 3]);
+          }
+      }
+    }
+    ptx::fence_proxy_async_smem();
+    ok = __syncthreads_and(ok) != 0;
+    if (!ok) break;
+    if (tid == 0) {
+      if (j == 0 && !ptx::mbar_wait(&S.b_full, 0, abort_flag, kKtWaitBudget)) {
+        *abort_flag = 1;
+        report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 41);
+      } else {
+        ptx::tc_fence_after();
+        constexpr uint32_t idesc = ptx::idesc_f16(128, 128, 1);
+        const uint64_t bd = ptx::smem_desc_sw128(S.B[j], 1024);
+#pragma unroll
+        for (int t = 0; t < 3; ++t) {
+          const uint64_t ad = ptx::smem_desc_sw128(S.A[buf][t], 1024);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            ptx::mma_f16_ss(tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc,
+                            (j | t | kk) ? 1u : 0u);
+        }
+        ptx::mma_commit(j == 7 ? &S.done : &S.a_free[buf]);
+      }
+    }
+  }
+  // after a wait gave up: one commit tracks every MMA already issued, so the
+  // tensor memory is released only once they are done
+  if (!ok && tid == 0) ptx::mma_commit(&S.done);
+  // epilogue: thread = entry row (warps 0-3 own the four lane quarters)
+  if (warp < 4) {
+    const bool landed = ptx::mbar_wait_warp(&S.done, 0, abort_flag, kKtWaitBudget);
+    const bool fin = ok && landed;
+    if (!landed && lane == 0) report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 42);
+    ptx::tc_fence_after();
+    const int64_t e = e0 + warp * 32 + lane;
+    if (fin) {
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)cb * 32u, v);
+        ptx::tmem_wait_ld();
+        if (e < n) {
+          float4* dst = reinterpret_cast<float4*>(ki + e * kDIdx + cb * 32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                 __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        }
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 128);
+  }
+}
+
+// W_IK^T [128][512] bf16 (K-major) from W_IK [512][128]
+__global__ void __launch_bounds__(256) k_cw_wik_t(const uint16_t* __restrict__ Wik, uint16_t* __restrict__ Wt) {
+  __shared__ uint16_t tile[32][33];
+  const int k0 = blockIdx.x * 32, o0 = blockIdx.y * 32;
+  const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
+  for (int i = ty; i < 32; i += 8) tile[i][tx] = Wik[(int64_t)(k0 + i) * kDIdx + o0 + tx];
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) Wt[(int64_t)(o0 + i) * kDMain + k0 + tx] = tile[tx][i];
+}
+
 bool make_bf16_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
@@ -402,6 +510,7 @@ struct CwWs {
   float* cbar;
   float* ki;
   uint16_t* wt;
+  uint16_t* wikt;
   size_t bytes;
 };
 
@@ -415,6 +524,8 @@ CwWs cw_ws_layout(void* ws, int64_t n, int64_t d_model) {
   off += align_up((size_t)n * kDIdx * 4, 256);
   L.wt = (uint16_t*)(base ? base + off : nullptr);
   off += align_up((size_t)2 * kDMain * d_model * 2, 256);
+  L.wikt = (uint16_t*)(base ? base + off : nullptr);
+  off += align_up((size_t)kDIdx * kDMain * 2, 256);
   L.bytes = off;
   return L;
 }
@@ -479,8 +590,18 @@ extern "C" csa2_status csa2_cache_write(const void* H_bf16, int64_t T, int32_t d
         (const uint16_t*)H_bf16, T, d_model, (const uint16_t*)Wkv_bf16, (const uint16_t*)Wz_bf16, m, L.cbar);
   }
   {
-    KernelTimer timer("k_cw_ki", st);
-    k_cw_ki<<<(unsigned)cdiv(n, kKiE), 256, 0, st>>>(L.cbar, (const uint16_t*)Wik_bf16, n, L.ki);
+    // K^I on the tensor cores (exact three-way bf16 split of Cbar)
+    {
+      KernelTimer timer("k_cw_wik_t", st);
+      k_cw_wik_t<<<dim3(kDMain / 32, kDIdx / 32), 256, 0, st>>>((const uint16_t*)Wik_bf16, L.wikt);
+    }
+    CUtensorMap map_wikt;
+    if (!make_bf16_map(&map_wikt, L.wikt, kDIdx, kDMain, kDIdx)) return CSA2_ERR_CUDA;
+    const int smem = (int)sizeof(KtSmem);
+    if (cudaFuncSetAttribute(k_cw_ki_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return CSA2_ERR_CUDA;
+    KernelTimer timer("k_cw_ki_tc", st);
+    k_cw_ki_tc<<<(unsigned)cdiv(n, 128), kKtThreads, smem, st>>>(map_wikt, L.cbar, n, L.ki, ws);
   }
   launch_quantize(L.cbar, L.ki, n, dst, (int64_t)seq * dst->seq_stride + entry_offset, st);
   return launch_status();
