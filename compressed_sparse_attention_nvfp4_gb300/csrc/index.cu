@@ -588,6 +588,8 @@ struct IndexWs {
   float* scores;
   float* bmax;
   int32_t* pool;
+  uint8_t* stage_codes;   // POOL mode: the pool blocks' keys gathered contiguously
+  uint8_t* stage_scales;  // [B][keep * block] entries of 64 + 4 bytes
   int64_t score_cols, bmax_cols;
   size_t bytes;
 };
@@ -607,8 +609,39 @@ static IndexWs index_ws_layout(void* ws, int32_t B, int64_t n_max, int32_t block
   off += align_up(b_bytes, 256);
   L.pool = (int32_t*)(base ? base + off : nullptr);
   off += p_bytes;
+  const size_t stage_rows = (size_t)B * keep * block;
+  L.stage_codes = (uint8_t*)(base ? base + off : nullptr);
+  off += align_up(stage_rows * 64, 256);
+  L.stage_scales = (uint8_t*)(base ? base + off : nullptr);
+  off += align_up(stage_rows * 4, 256);
   L.bytes = off;
   return L;
+}
+
+// POOL mode gather: block u of query b's pool -> staged entries (b*keep + u)*8 ..+7
+// (codes 512 B, scales 32 B); one warp per block, 16-byte copies.  Blocks that
+// are padding (-1) or start at or beyond n are left as they are: the selector
+// masks their candidates by the pool ids.
+__global__ void __launch_bounds__(256) k_pool_gather(const uint8_t* __restrict__ ix_codes,
+                                                     const uint8_t* __restrict__ ix_scales, int64_t seq_stride,
+                                                     const int32_t* __restrict__ n_entries, int64_t n_max,
+                                                     const int32_t* __restrict__ pool, int keep, int B,
+                                                     uint8_t* __restrict__ st_codes, uint8_t* __restrict__ st_scales) {
+  const int64_t wg = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32;
+  const int lane = threadIdx.x % 32;
+  if (wg >= (int64_t)B * keep) return;
+  const int b = (int)(wg / keep);
+  const int64_t n = max((int64_t)0, min((int64_t)n_entries[b], n_max));
+  const int pb = pool[wg];
+  if (pb < 0 || (int64_t)pb * 8 >= n) return;
+  const int rows = (int)min((int64_t)8, seq_stride - (int64_t)pb * 8);  // rows inside the slot
+  const int64_t src = (int64_t)b * seq_stride + (int64_t)pb * 8;  // first entry of the block
+  if (lane / 4 < rows)  // a quarter of a 64-byte row per lane
+    reinterpret_cast<uint4*>(st_codes + wg * 8 * 64)[lane] =
+        reinterpret_cast<const uint4*>(ix_codes + src * 64)[lane];
+  if (lane < rows)
+    reinterpret_cast<uint32_t*>(st_scales + wg * 8 * 4)[lane] =
+        reinterpret_cast<const uint32_t*>(ix_scales + src * 4)[lane];
 }
 
 }  // namespace csa2
@@ -653,8 +686,22 @@ extern "C" csa2_status csa2_index_topk(const csa2_kv_planes* kv, int32_t B, cons
   if (mode == CSA2_TOPK_POOL) {
     float* sc = scores_out ? scores_out : L.scores;
     int64_t sc_stride = scores_out ? keep_c : L.score_cols;
-    csa2_status rs = launch_scan(kv, B, n_entries, n_max, keep_c, q, w, pool_in, n_blocks_keep, sc,
-                                 sc_stride, nullptr, 0, ws, st);
+    // gather the pool's blocks into contiguous staged entries, then scan those
+    // as flat slots of keep_c entries (one tensor load per 128 entries instead
+    // of one per 8-entry block)
+    {
+      KernelTimer timer("k_pool_gather", st);
+      const int64_t warps = (int64_t)B * n_blocks_keep;
+      k_pool_gather<<<(unsigned)cdiv(warps * 32, 256), 256, 0, st>>>(
+          kv->ix_codes, kv->ix_scales, kv->seq_stride, n_entries, n_max, pool_in, n_blocks_keep, B,
+          L.stage_codes, L.stage_scales);
+    }
+    csa2_kv_planes staged = *kv;
+    staged.ix_codes = L.stage_codes;
+    staged.ix_scales = L.stage_scales;
+    staged.seq_stride = keep_c;
+    csa2_status rs = launch_scan(&staged, B, nullptr, keep_c, keep_c, q, w, nullptr, 0, sc, sc_stride,
+                                 nullptr, 0, ws, st);
     if (rs != CSA2_OK) return rs;
     SelectArgs a{sc, sc_stride, n_entries, pool_in, n_blocks_keep, 0, keep_c, k, topk_out, k, n_max};
     launch_select(a, B, st);

@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int b = blockIdx.y;
 
-  int64_t n = p.n_entries[b];
+  int64_t n = p.n_entries ? p.n_entries[b] : p.n_max;  // no counts: every slot holds n_max
   if (n > p.n_max) {
     if (threadIdx.x == 0 && blockIdx.x == 0) report_error(p.ws, CSA2_ERR_INDEX_RANGE, n);
     n = p.n_max;
