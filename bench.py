@@ -238,6 +238,77 @@ def run_cache_write(dev, st, calls: int, warmup: int):
     }
 
 
+ST_B, ST_CTX, ST_SEED = 128, 262144, 4
+ST_WORKLOAD = ("40-layer V4.1 decode step: batch 128 at a 262,144-token context; layers 0-1 SWA only, "
+               "encoder 3 x (Full + 5 Reuse) at m=2 (131,072 entries), decoder (Full + 3 Reuse) + "
+               "4 x (Reindex + 3 Reuse) at m=1 (262,144 entries, 2,048-block pool), top-512 + 128-row "
+               "FP8 window in every layer")
+
+
+def run_step40(dev, st, steps: int, warmup: int):
+    """One decode step over the 40-layer schedule (schedule.run_step) on seeded device inputs."""
+    import torch
+
+    import compressed_sparse_attention_nvfp4_gb300 as csa2
+    from compressed_sparse_attention_nvfp4_gb300 import schedule as SCH
+    from compressed_sparse_attention_nvfp4_gb300 import workload as WL
+
+    B, T = ST_B, ST_CTX
+    t = csa2.v41_layer_table()
+    full = [l for l in range(40) if t["mode"][l] == csa2.LAYER_FULL]
+    n_of = {f: T // t["m"][f] for f in full}
+    with torch.cuda.stream(st):
+        kv, ne, nm = {}, {}, {}
+        for f in full:
+            kv[f] = csa2.Planes.empty(B, n_of[f], dev)
+            WL.fill_planes(kv[f], ST_SEED, f, B, n_of[f], stream=st)
+            ne[f] = torch.full((B,), n_of[f], dtype=torch.int32, device=dev)
+            nm[f] = n_of[f]
+        qidx, w, q, swa, out = {}, {}, {}, {}, {}
+        for l in range(40):
+            if t["mode"][l] in (csa2.LAYER_FULL, csa2.LAYER_REINDEX):
+                qidx[l], w[l], _, _ = WL.index_query_dev(ST_SEED, l, B, dev)
+            q[l], _ = WL.attn_query_dev(ST_SEED, l, B, dev)
+            swa[l] = WL.swa_dev(ST_SEED, l, B, NSWA, dev, stream=st)
+            out[l] = torch.empty((B, 64, 512), dtype=torch.float32, device=dev)
+        buf = SCH.StepBuffers(B=B, kv=kv, n_entries=ne, n_max=nm, qidx=qidx, w=w, q=q, swa=swa, out=out,
+                              k=K_TOP, n_blocks_keep=KEEP)
+        SCH.allocate_scratch(buf, dev)
+    torch.cuda.synchronize()
+    for _ in range(warmup):
+        SCH.run_step(buf, stream=st)
+    torch.cuda.synchronize()
+    assert csa2.check(buf.ws_index, st)[0] == 0 and csa2.check(buf.ws_attn, st)[0] == 0
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for _ in range(steps):
+        calls = SCH.run_step(buf, stream=st)
+    b.record(st)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    csa2.timing_enable(True)
+    SCH.run_step(buf, stream=st)
+    torch.cuda.synchronize()
+    kt = csa2.kernel_times()
+    csa2.timing_enable(False)
+    assert csa2.check(buf.ws_index, st)[0] == 0 and csa2.check(buf.ws_attn, st)[0] == 0
+    # algorithmic bytes: every Full layer's keys once, each Reindex layer's pool, and
+    # every attention layer's selected entries and window rows
+    n_reindex = sum(1 for l in range(40) if t["mode"][l] == csa2.LAYER_REINDEX)
+    n_attn_sel = sum(1 for l in range(40) if t["mode"][l] != csa2.LAYER_SWA)
+    step_bytes = B * (sum(n_of.values()) * IDX_BYTES + n_reindex * KEEP * BLOCK * IDX_BYTES
+                      + n_attn_sel * K_TOP * MAIN_BYTES + 40 * NSWA * SWA_ROW)
+    hbm, kind = peaks()
+    achieved = step_bytes / (ms * 1e-3) / 1e9
+    return {
+        "workload": ST_WORKLOAD, "steps": steps, "library_calls_per_step": calls,
+        "ms_per_step": round(ms, 4), "queries_per_s": round(B / (ms * 1e-3), 1),
+        "kernels_ms_per_step": {k: round(tm, 4) for k, (n, tm) in sorted(kt.items())},
+        "hbm": {"algorithmic_bytes": step_bytes, "achieved_gbs": round(achieved, 1), "peak": hbm,
+                "peak_kind": kind, "frac": round(achieved / hbm, 4)},
+    }
+
+
 def tensor_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -404,6 +475,10 @@ def run_ours(args, rank, world, local_rank):
     }
     if not args.no_cache_write:
         line["cache_write"] = run_cache_write(dev, st, 5, 2)
+    if not args.no_step40:
+        del planes, ws_i, ws_a
+        torch.cuda.empty_cache()
+        line["step_40_layers"] = run_step40(dev, st, 5, 2)
     return line
 
 
@@ -416,6 +491,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-cache-write", action="store_true",
                     help="skip the prefill cache-write measurement (its own object in the line)")
+    ap.add_argument("--no-step40", action="store_true",
+                    help="skip the 40-layer step measurement (its own object in the line)")
+    ap.add_argument("--step40-only", action="store_true",
+                    help="profiling case: only the 40-layer step, printed as its own line")
     ap.add_argument("--cache-write-only", action="store_true",
                     help="profiling case: only the prefill cache write, printed as its own line")
     ap.add_argument("--batch", type=int, default=32,
@@ -455,6 +534,19 @@ def main():
 
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
+    if args.step40_only:
+        import torch
+
+        torch.cuda.set_device(local_rank)
+        import compressed_sparse_attention_nvfp4_gb300 as csa2
+
+        csa2.lib()
+        dev = torch.device("cuda", local_rank)
+        st = torch.cuda.Stream(device=dev)
+        if rank == 0:
+            print(json.dumps({"step_40_layers": run_step40(dev, st, max(1, min(args.steps, 20)),
+                                                           max(1, args.warmup))}), flush=True)
+        return
     if args.cache_write_only:
         import torch
 

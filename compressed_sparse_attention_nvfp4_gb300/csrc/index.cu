@@ -619,29 +619,44 @@ static IndexWs index_ws_layout(void* ws, int32_t B, int64_t n_max, int32_t block
 }
 
 // POOL mode gather: block u of query b's pool -> staged entries (b*keep + u)*8 ..+7
-// (codes 512 B, scales 32 B); one warp per block, 16-byte copies.  Blocks that
-// are padding (-1) or start at or beyond n are left as they are: the selector
-// masks their candidates by the pool ids.
+// (codes 512 B, scales 32 B); a warp copies kGatherBlocks blocks with all their
+// 16-byte loads in flight.  Blocks that are padding (-1) or start at or beyond n
+// are left as they are: the selector masks their candidates by the pool ids.
+constexpr int kGatherBlocks = 4;
+
 __global__ void __launch_bounds__(256) k_pool_gather(const uint8_t* __restrict__ ix_codes,
                                                      const uint8_t* __restrict__ ix_scales, int64_t seq_stride,
                                                      const int32_t* __restrict__ n_entries, int64_t n_max,
                                                      const int32_t* __restrict__ pool, int keep, int B,
                                                      uint8_t* __restrict__ st_codes, uint8_t* __restrict__ st_scales) {
-  const int64_t wg = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32;
+  const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32 * kGatherBlocks;
   const int lane = threadIdx.x % 32;
-  if (wg >= (int64_t)B * keep) return;
-  const int b = (int)(wg / keep);
-  const int64_t n = max((int64_t)0, min((int64_t)n_entries[b], n_max));
-  const int pb = pool[wg];
-  if (pb < 0 || (int64_t)pb * 8 >= n) return;
-  const int rows = (int)min((int64_t)8, seq_stride - (int64_t)pb * 8);  // rows inside the slot
-  const int64_t src = (int64_t)b * seq_stride + (int64_t)pb * 8;  // first entry of the block
-  if (lane / 4 < rows)  // a quarter of a 64-byte row per lane
-    reinterpret_cast<uint4*>(st_codes + wg * 8 * 64)[lane] =
-        reinterpret_cast<const uint4*>(ix_codes + src * 64)[lane];
-  if (lane < rows)
-    reinterpret_cast<uint32_t*>(st_scales + wg * 8 * 4)[lane] =
-        reinterpret_cast<const uint32_t*>(ix_scales + src * 4)[lane];
+  const int64_t total = (int64_t)B * keep;
+  uint4 code[kGatherBlocks];
+  uint32_t scale[kGatherBlocks];
+  bool cp_code[kGatherBlocks], cp_scale[kGatherBlocks];
+#pragma unroll
+  for (int g = 0; g < kGatherBlocks; ++g) {
+    const int64_t wg = w0 + g;
+    cp_code[g] = cp_scale[g] = false;
+    if (wg >= total) continue;
+    const int b = (int)(wg / keep);
+    const int64_t n = max((int64_t)0, min((int64_t)n_entries[b], n_max));
+    const int pb = pool[wg];
+    if (pb < 0 || (int64_t)pb * 8 >= n) continue;
+    const int rows = (int)min((int64_t)8, seq_stride - (int64_t)pb * 8);  // rows inside the slot
+    const int64_t src = (int64_t)b * seq_stride + (int64_t)pb * 8;       // first entry of the block
+    cp_code[g] = lane / 4 < rows;  // a quarter of a 64-byte row per lane
+    cp_scale[g] = lane < rows;
+    if (cp_code[g]) code[g] = reinterpret_cast<const uint4*>(ix_codes + src * 64)[lane];
+    if (cp_scale[g]) scale[g] = reinterpret_cast<const uint32_t*>(ix_scales + src * 4)[lane];
+  }
+#pragma unroll
+  for (int g = 0; g < kGatherBlocks; ++g) {
+    const int64_t wg = w0 + g;
+    if (cp_code[g]) reinterpret_cast<uint4*>(st_codes + wg * 8 * 64)[lane] = code[g];
+    if (cp_scale[g]) reinterpret_cast<uint32_t*>(st_scales + wg * 8 * 4)[lane] = scale[g];
+  }
 }
 
 }  // namespace csa2
@@ -691,7 +706,7 @@ extern "C" csa2_status csa2_index_topk(const csa2_kv_planes* kv, int32_t B, cons
     // of one per 8-entry block)
     {
       KernelTimer timer("k_pool_gather", st);
-      const int64_t warps = (int64_t)B * n_blocks_keep;
+      const int64_t warps = cdiv((int64_t)B * n_blocks_keep, kGatherBlocks);
       k_pool_gather<<<(unsigned)cdiv(warps * 32, 256), 256, 0, st>>>(
           kv->ix_codes, kv->ix_scales, kv->seq_stride, n_entries, n_max, pool_in, n_blocks_keep, B,
           L.stage_codes, L.stage_scales);
