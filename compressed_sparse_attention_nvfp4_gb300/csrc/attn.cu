@@ -4,32 +4,23 @@
 // sliding-window branch; "DeepSeek-V4.1-Flash: pushing the limits of KV cache
 // compression", 4.1).  K = V = the 512-channel latent; 64 heads share it.
 //
-// k_attn_qprep stages q once per query: q' = q 2^-s_h in f16 with a
-// power-of-two prescale per head (exact for bf16 q), already in the byte image
-// of the S MMA's B operand.  Then each CTA of k_attn takes a chunk of 128 rows
-// of one query and runs it on the tensor cores (tcgen05, kind::f16, fp32
-// accumulation in tensor memory):
-//   1. copies q' in with one bulk copy while its threads gather and dequantize
-//      the rows into shared memory as f16 (exact: E2M1 x E4M3 has at most 6
-//      significant bits), interleaved X[c/8][row][c%8]: K-major for S,
-//      M-major for O;
-//   2. S^T[128 rows x 64 heads] = X q'^T (one thread issues 32 MMAs);
-//   3. per head, the maximum logit: over the chunk, then over the query;
-//   4. P = exp(S - max) rounded to f16, with its column sums l;
-//   5. O^T[512 x 64] = X^T P^T (four 128-channel M tiles).
-// When a query's chunks fit one thread-block cluster (at most 8 chunks, 1024
-// rows) the cluster exchanges the chunk maxima before step 4, so that every
-// chunk's probabilities share one reference, and sums the chunks' O and l
-// through distributed shared memory into the normalised output.  Longer
-// selections write each chunk's unnormalised O with its (max, l) and a merge
-// kernel combines the chunks by log-sum-exp.
-#include <cooperative_groups.h>
-
+// k_attn stages q in shared memory as q' = q 2^-s_h in f16 with a power-of-two
+// prescale per head (exact for bf16 q), then runs the query's rows (selected
+// entries, then window rows) in chunks of 128 on the tensor cores (tcgen05,
+// kind::f16, fp32 accumulation in tensor memory):
+//   1. the chunk's rows are dequantized into shared memory as f16 (exact:
+//      E2M1 x E4M3 has at most 6 significant bits), interleaved
+//      X[c/8][row][c%8]: K-major for S, M-major for O;
+//   2. S^T[128 rows x 64 heads] = X q'^T;
+//   3. online softmax per head, P rounded to f16 once, l = sums of the rounded P;
+//   4. O^T[512 x 64] += X^T P^T (four 128-channel M tiles).
+// One CTA per query keeps O in tensor memory across all its chunks, so no
+// partial result leaves the SM.  When the batch is too small to fill the GPU
+// a query's chunks are split over a few CTAs, which write (max, l, O) partials
+// that a merge kernel combines by log-sum-exp.
 #include "codec.cuh"
 #include "ptx.cuh"
 #include "timing.cuh"
-
-namespace cg = cooperative_groups;
 
 namespace csa2 {
 
@@ -38,29 +29,35 @@ namespace {
 constexpr int kRows = 128;  // rows per CTA: the M of the S MMA
 constexpr int kAT = 288;    // warps 0-7: two threads per row in the gather, the epilogues; warp 8: control
 constexpr int kCtlWarp = 8;
-constexpr int kMaxCluster = 8;
-constexpr uint32_t kAttnTmemCols = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+// the softmax reference (log2 units) moves only when a chunk exceeds it by
+// more than 8 nats, so probabilities stay below e^8 (inside f16)
+constexpr float kTau2 = 8.0f * kLog2e;
+// q' plane stride: 64 heads x 16 bytes plus 16 bytes of padding, so that the
+// 16-byte stores of consecutive channel chunks fall in different banks
+constexpr int kQPlane = kHAtt * 8 + 8;  // in f16 elements (1040 bytes)
+constexpr uint32_t kAttnTmemCols = 512;  // O^T 256 columns, S^T 64
 constexpr long long kAttnWaitBudget = 1LL << 32;
-constexpr uint32_t kQBytes = kDMain * kHAtt * 2;  // staged q' image per query
 
 struct __align__(1024) AttnSmem {
-  // f16 rows [c/8][row][c%8]; once the O MMA has completed, this CTA's O^T as
-  // fp32 [head][channel] for the cluster's reduction
-  uint16_t X[kDMain / 8][kRows * 8];
-  uint16_t q[kDMain / 8][kHAtt * 8];  // f16 q' [c/8][head][c%8]
+  uint16_t X[kDMain / 8][kRows * 8];  // f16 rows [c/8][row][c%8]; planes 0-31 / 32-63 = channel halves
+  uint16_t q[kDMain / 8][kQPlane];    // f16 q' [c/8][head][c%8], planes padded
   uint16_t P[kHAtt / 8][kRows * 8];   // f16 probabilities [h/8][row][h%8]
-  float colscale[kHAtt];              // softmax_scale * 2^s_h
-  float red[4][kHAtt];                // per lane quarter partial column reductions
-  float mloc[kHAtt];                  // chunk maximum (read by the cluster)
-  float M[kHAtt];                     // reference maximum of this chunk's probabilities
-  float lloc[kHAtt];                  // chunk sum of the rounded probabilities (read by the cluster)
-  float invL[kHAtt];
+  float c2[kHAtt];                    // log2(e) * softmax_scale * 2^s_h: logit (log2 units) per raw S
+  float m2w[8][32];                   // per warp: the reference of its 32 heads (0 while none)
+  float red[4][kHAtt];                // per lane quarter column maxima of the chunk
+  float red2[4][kHAtt];               // per lane quarter column sums of the chunk's P
   int valid[kRows];
-  uint64_t qbar, bar;
+  uint64_t q_full;                    // q' and colscale written (8 warps)
+  uint64_t x_full[2];                 // channel half of X written (4 warps each)
+  uint64_t s_full;                    // S^T MMAs complete
+  uint64_t red_full;                  // chunk maxima posted (8 warps)
+  uint64_t p_full;                    // P written, O rescaled, sums posted (8 warps)
+  uint64_t x_free[2];                 // O MMAs reading that channel half of X (and P) complete
+  uint64_t drained;                   // every MMA issued complete
   uint32_t tmem_base;
   int abort_flag;
 };
-static_assert(sizeof(float) * kHAtt * kDMain == sizeof(uint16_t) * kDMain * kRows, "O^T fits the rows");
 
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   uint32_t r;
@@ -108,340 +105,404 @@ __device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane,
 
 // q' = q_h 2^-s_h in f16 with 2^s_h bringing the head's largest |q| to
 // [2^14, 2^15), clamped so that both 2^s_h and 2^-s_h are normal fp32 values;
-// bf16 q keeps q' exact and inside the f16 range.  One warp per head: lane l
-// converts channels 8l..8l+7 and 256+8l..256+8l+7, i.e. 16-byte chunks l and
-// 32+l of the [c/8][head][c%8] image.
-__global__ void __launch_bounds__(256) k_attn_qprep(const uint16_t* __restrict__ qg, float scale,
-                                                    uint16_t* __restrict__ qs, float* __restrict__ colscale) {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int b = blockIdx.y;
-  const int h = blockIdx.x * 8 + threadIdx.x / 32, lane = threadIdx.x % 32;
-  const uint4* src = reinterpret_cast<const uint4*>(qg + ((int64_t)b * kHAtt + h) * kDMain);
-  const uint4 raw[2] = {src[lane], src[32 + lane]};
-  float mx = 0.0f;
+// bf16 q keeps q' exact and inside the f16 range.  Warp w converts heads
+// 8w..8w+7: lane l holds channels 8l..8l+7 and 256+8l..256+8l+7 of each, i.e.
+// chunks l and 32+l of the [c/8][head][c%8] image.
+struct QFetch {
+  uint4 raw[8][2];
+};
+__device__ __forceinline__ void fetch_q(QFetch& f, const uint16_t* __restrict__ qg, int b, int warp, int lane) {
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w4[j] << 16)), fabsf(__uint_as_float(w4[j] & 0xFFFF0000u))));
+  for (int u = 0; u < 8; ++u) {
+    const uint4* src = reinterpret_cast<const uint4*>(qg + ((int64_t)b * kHAtt + warp * 8 + u) * kDMain);
+    f.raw[u][0] = src[lane];
+    f.raw[u][1] = src[32 + lane];
   }
+}
+__device__ __forceinline__ void stage_q(AttnSmem& S, const QFetch& f, float scale, int warp, int lane) {
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  const int sig = mx > 0.0f ? min(max(floor_log2_f32(mx) - 14, -126), 126) : 0;
-  const float inv = exp2i_f32(-sig);  // exact power of two: q 2^-sig rounds only in the f16 conversion
-  uint16_t* dst = qs + (int64_t)b * (kQBytes / 2);
+  for (int u = 0; u < 8; ++u) {
+    float mx = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-    uint32_t o[4];
+    for (int i = 0; i < 2; ++i) {
+      const uint32_t w4[4] = {f.raw[u][i].x, f.raw[u][i].y, f.raw[u][i].z, f.raw[u][i].w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const __half2 h2 = __floats2half2_rn(__uint_as_float(w4[j] << 16) * inv,
-                                           __uint_as_float(w4[j] & 0xFFFF0000u) * inv);
-      o[j] = *reinterpret_cast<const uint32_t*>(&h2);
+      for (int j = 0; j < 4; ++j)
+        mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w4[j] << 16)), fabsf(__uint_as_float(w4[j] & 0xFFFF0000u))));
     }
-    const int cc = i * 32 + lane;
-    *reinterpret_cast<uint4*>(dst + ((int64_t)cc * kHAtt + h) * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const int sig = mx > 0.0f ? min(max(floor_log2_f32(mx) - 14, -126), 126) : 0;
+    const float inv = exp2i_f32(-sig);  // exact power of two: q 2^-sig rounds only in the f16 conversion
+    const int h = warp * 8 + u;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint32_t w4[4] = {f.raw[u][i].x, f.raw[u][i].y, f.raw[u][i].z, f.raw[u][i].w};
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const __half2 h2 = __floats2half2_rn(__uint_as_float(w4[j] << 16) * inv,
+                                             __uint_as_float(w4[j] & 0xFFFF0000u) * inv);
+        o[j] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      *reinterpret_cast<uint4*>(&S.q[i * 32 + lane][h * 8]) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (lane == 0) S.c2[h] = kLog2e * scale * exp2i_f32(sig);
   }
-  if (lane == 0) colscale[b * kHAtt + h] = scale * exp2i_f32(sig);
 }
 
-// Gathers and dequantizes half a row: channels [256 half, 256 half + 256).
-__device__ __forceinline__ bool gather_half_row(AttnSmem& S, const uint8_t* __restrict__ kv_codes,
-                                                const uint8_t* __restrict__ kv_scales, int64_t seq_stride,
-                                                const int32_t* __restrict__ topk, int k,
-                                                const uint8_t* __restrict__ swa, int n_swa, int b, int gr,
-                                                int r, int half, void* ws) {
+// One thread's half row of a chunk, fetched ahead of its dequantization.
+struct RowFetch {
+  uint4 raw[16];  // main entry: 8 x 16 code bytes + 16 scale bytes; window row: 256 bytes
+  int kind;       // 0 = no row, 1 = main entry, 2 = window row
+};
+
+// topk entry of chunk row gr (rows gr >= k are window rows or padding)
+__device__ __forceinline__ int64_t fetch_index(const int32_t* __restrict__ topk, int k, int b, int gr) {
+  return gr < k ? (int64_t)topk[(int64_t)b * k + gr] : -1;
+}
+
+// Starts the loads of half a row: a selected entry (gr < k, index idx), a
+// window row (k <= gr < k + n_swa) or nothing.
+__device__ __forceinline__ void issue_row(RowFetch& f, int64_t idx, const uint8_t* __restrict__ kv_codes,
+                                          const uint8_t* __restrict__ kv_scales, int64_t seq_stride,
+                                          const uint8_t* __restrict__ swa, int n_swa, int k, int b, int gr,
+                                          int half, void* ws) {
+  f.kind = 0;
   if (gr < k) {
-    const int64_t idx = topk[(int64_t)b * k + gr];
     if (idx >= 0 && idx < seq_stride) {
       const int64_t e = (int64_t)b * seq_stride + idx;
       const uint4* cs = reinterpret_cast<const uint4*>(kv_codes + e * 256 + half * 128);
-      uint4 c8[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) c8[i] = cs[i];
-      const uint4 s4 = reinterpret_cast<const uint4*>(kv_scales + e * 32)[half];
-      const uint32_t sw[4] = {s4.x, s4.y, s4.z, s4.w};
+      for (int i = 0; i < 8; ++i) f.raw[i] = cs[i];
+      f.raw[8] = reinterpret_cast<const uint4*>(kv_scales + e * 32)[half];
+      f.kind = 1;
+    } else if (idx != -1 && half == 0) {
+      report_error(ws, CSA2_ERR_INDEX_RANGE, idx);
+    }
+  } else if (gr - k < n_swa) {
+    const uint4* src = reinterpret_cast<const uint4*>(swa + ((int64_t)b * n_swa + (gr - k)) * kDMain + half * 256);
 #pragma unroll
-      for (int g = 0; g < 16; ++g) {  // 16 channels: 8 code bytes, one E4M3 scale
-        const uint32_t sb = (sw[g / 4] >> (8 * (g % 4))) & 0xFFu;
+    for (int i = 0; i < 16; ++i) f.raw[i] = src[i];
+    f.kind = 2;
+  }
+}
+
+// Writes the half row [256 half, 256 half + 256) of row r to X as f16 (zeros
+// when there is no row), 64 channels at a time; returns whether the row exists.
+__device__ __forceinline__ bool dequant_half_row(AttnSmem& S, const RowFetch& f, int r, int half) {
+#pragma unroll
+  for (int blk = 0; blk < 4; ++blk) {
+    uint32_t w[32];  // channels 64 blk + 2j, 2j + 1 in w[j]
+    if (f.kind == 1) {
+      const uint32_t sw = blk == 0 ? f.raw[8].x : blk == 1 ? f.raw[8].y : blk == 2 ? f.raw[8].z : f.raw[8].w;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {  // 16 channels: 8 code bytes, one E4M3 scale
+        const int G = blk * 4 + g;
+        const uint32_t sb = (sw >> (8 * g)) & 0xFFu;
         const uint32_t s2 = e4m3x2_to_f16x2(sb | (sb << 8));
-        const uint4 cw = c8[g / 2];
-        const uint32_t w0 = (g & 1) ? cw.z : cw.x, w1 = (g & 1) ? cw.w : cw.y;
+        const uint4 cw = f.raw[G / 2];
+        const uint32_t w0 = (G & 1) ? cw.z : cw.x, w1 = (G & 1) ? cw.w : cw.y;
         uint32_t h0[4], h1[4];
         e2m1x8_to_f16(w0, h0);
         e2m1x8_to_f16(w1, h1);
-        const int cc = half * 32 + 2 * g;
-        *reinterpret_cast<uint4*>(&S.X[cc][r * 8]) =
-            make_uint4(hmul2_u32(h0[0], s2), hmul2_u32(h0[1], s2), hmul2_u32(h0[2], s2), hmul2_u32(h0[3], s2));
-        *reinterpret_cast<uint4*>(&S.X[cc + 1][r * 8]) =
-            make_uint4(hmul2_u32(h1[0], s2), hmul2_u32(h1[1], s2), hmul2_u32(h1[2], s2), hmul2_u32(h1[3], s2));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          w[8 * g + j] = hmul2_u32(h0[j], s2);
+          w[8 * g + 4 + j] = hmul2_u32(h1[j], s2);
+        }
       }
-      return true;
-    }
-    if (idx != -1 && half == 0) report_error(ws, CSA2_ERR_INDEX_RANGE, idx);
-    return false;
-  }
-  if (gr - k < n_swa) {
-    const uint4* src = reinterpret_cast<const uint4*>(swa + ((int64_t)b * n_swa + (gr - k)) * kDMain + half * 256);
-    uint4 row[16];
+    } else if (f.kind == 2) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) row[i] = src[i];
+      for (int u = 0; u < 4; ++u) {  // 16 channels per uint4
+        const uint4 v = f.raw[blk * 4 + u];
+        w[8 * u + 0] = e4m3x2_to_f16x2(v.x);
+        w[8 * u + 1] = e4m3x2_to_f16x2(v.x >> 16);
+        w[8 * u + 2] = e4m3x2_to_f16x2(v.y);
+        w[8 * u + 3] = e4m3x2_to_f16x2(v.y >> 16);
+        w[8 * u + 4] = e4m3x2_to_f16x2(v.z);
+        w[8 * u + 5] = e4m3x2_to_f16x2(v.z >> 16);
+        w[8 * u + 6] = e4m3x2_to_f16x2(v.w);
+        w[8 * u + 7] = e4m3x2_to_f16x2(v.w >> 16);
+      }
+    } else {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {  // 16 channels per uint4 -> two chunks
-      const uint4 v = row[i];
-      const int cc = half * 32 + 2 * i;
-      *reinterpret_cast<uint4*>(&S.X[cc][r * 8]) = make_uint4(
-          e4m3x2_to_f16x2(v.x), e4m3x2_to_f16x2(v.x >> 16), e4m3x2_to_f16x2(v.y), e4m3x2_to_f16x2(v.y >> 16));
-      *reinterpret_cast<uint4*>(&S.X[cc + 1][r * 8]) = make_uint4(
-          e4m3x2_to_f16x2(v.z), e4m3x2_to_f16x2(v.z >> 16), e4m3x2_to_f16x2(v.w), e4m3x2_to_f16x2(v.w >> 16));
+      for (int j = 0; j < 32; ++j) w[j] = 0u;
     }
-    return true;
+#pragma unroll
+    for (int pl = 0; pl < 8; ++pl)
+      *reinterpret_cast<uint4*>(&S.X[half * 32 + blk * 8 + pl][r * 8]) =
+          make_uint4(w[4 * pl], w[4 * pl + 1], w[4 * pl + 2], w[4 * pl + 3]);
   }
-  return false;
+  return f.kind != 0;
 }
 
-// kMerge: the grid's x dimension (the query's chunks) is one cluster and the
-// kernel writes the normalised output; otherwise it writes per-chunk partials.
-// Warps 0-7 gather the rows and run the epilogues (warp w reads tensor-memory
-// lane quarter w % 4); warp 8 owns the barriers, the tensor memory, the q'
-// copy and the MMA issue.
-template <bool kMerge>
+// One CTA runs chunks [c0, c1) of query b's rows with an online softmax; the
+// output accumulates in tensor memory across the chunks.
+//   warps 0-3 / 4-7: dequantize channels 0-255 / 256-511 of each chunk into X,
+//     fetching the next chunk's rows while the current one is on the tensor
+//     cores; then all eight run the chunk's softmax (warp w reads tensor-memory
+//     lane quarter w % 4, heads 32 (w / 4) .. +31);
+//   warp 8: barriers, tensor memory, the q' copy and the MMA issue.
+// Per chunk the MMA thread issues S over the first channel half as soon as it
+// is written, then the second; after the softmax, O over the first channel
+// half, whose completion frees that half of X for the next chunk, then the
+// second.  The softmax keeps, per head, a reference m (the running maximum,
+// raised only when a chunk exceeds it by more than kTau2, which then rescales
+// O and l in place), so probabilities stay below e^8.  The softmax runs in
+// log2 units: p = 2^(raw S * c2_h - m2_h).
+// kPartial: write the unnormalised O with (m, l) for the merge kernel instead
+// of the normalised output.
+template <bool kPartial>
 __global__ void __launch_bounds__(kAT, 1) k_attn(
     const uint8_t* __restrict__ kv_codes, const uint8_t* __restrict__ kv_scales, int64_t seq_stride,
     const int32_t* __restrict__ topk, int k, const uint8_t* __restrict__ swa, int n_swa,
-    const uint16_t* __restrict__ qs, const float* __restrict__ qscale, int nchunks,
+    const uint16_t* __restrict__ qg, float scale, int nchunks, int cps,
     float* __restrict__ out, float* __restrict__ lse, float* __restrict__ part_o,
     float2* __restrict__ part_ml, void* ws) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   AttnSmem& S = *reinterpret_cast<AttnSmem*>(smem_raw);
   volatile int* abort_flag = &S.abort_flag;
-  const int b = blockIdx.y, chunk = blockIdx.x;
+  const int b = blockIdx.y, split = blockIdx.x;
+  const int c0 = split * cps, nc = min(nchunks, c0 + cps) - c0;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const bool ctl = warp == kCtlWarp;
 
-  if (ctl) {
+  if (warp == kCtlWarp) {
     if (lane == 0) {
-      ptx::mbar_init(&S.qbar, 1);
-      ptx::mbar_init(&S.bar, 1);
+      ptx::mbar_init(&S.q_full, 8);
+      ptx::mbar_init(&S.x_full[0], 4);
+      ptx::mbar_init(&S.x_full[1], 4);
+      ptx::mbar_init(&S.s_full, 1);
+      ptx::mbar_init(&S.red_full, 8);
+      ptx::mbar_init(&S.p_full, 8);
+      ptx::mbar_init(&S.x_free[0], 1);
+      ptx::mbar_init(&S.x_free[1], 1);
+      ptx::mbar_init(&S.drained, 1);
       S.abort_flag = 0;
       ptx::fence_mbar_init();
-      // q' is written by the preceding staging kernel, which lets this grid
-      // start early: wait for it here, then copy q' and its column scales in
-      // while the other warps gather
-      asm volatile("griddepcontrol.wait;" ::: "memory");
-      ptx::mbar_arrive_expect_tx(&S.qbar, kQBytes + kHAtt * 4);
-      ptx::bulk_g2s(&S.q[0][0], qs + (int64_t)b * (kQBytes / 2), kQBytes, &S.qbar);
-      ptx::bulk_g2s(S.colscale, qscale + (int64_t)b * kHAtt, kHAtt * 4, &S.qbar);
     }
     __syncwarp();
     ptx::tmem_alloc(&S.tmem_base, kAttnTmemCols);
-  } else {
-    // ---- rows -> f16 X (threads r and r + 128 own the two halves of row r)
-    const int r = tid % kRows, half = tid / kRows;
-    const bool ok = gather_half_row(S, kv_codes, kv_scales, seq_stride, topk, k, swa, n_swa, b,
-                                    chunk * kRows + r, r, half, ws);
-    if (!ok)
-#pragma unroll 8
-      for (int cc = half * 32; cc < half * 32 + 32; ++cc)
-        *reinterpret_cast<uint4*>(&S.X[cc][r * 8]) = make_uint4(0, 0, 0, 0);
-    if (half == 0) S.valid[r] = ok ? 1 : 0;
+  }
+  // q and the first chunk's indices load together; q is converted while the
+  // indices arrive, then the rows are requested
+  const int r = tid % kRows, half = (tid / kRows) & 1;
+  RowFetch rf;
+  if (warp < kCtlWarp) {
+    const int gr = c0 * kRows + r;
+    QFetch qf;
+    fetch_q(qf, qg, b, warp, lane);
+    const int64_t idx0 = fetch_index(topk, k, b, gr);
+    stage_q(S, qf, scale, warp, lane);
     ptx::fence_proxy_async_smem();
+    issue_row(rf, idx0, kv_codes, kv_scales, seq_stride, swa, n_swa, k, b, gr, half, ws);
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  __syncthreads();  // barriers initialised, tensor memory allocated
   ptx::tc_fence_after();
   const uint32_t tmem = S.tmem_base;
+  const uint32_t tS = tmem + 256u;  // S^T: 64 columns after the 256 of O^T
 
-  // ---- S^T = X q'^T : M = 128 rows, N = 64 heads, K = 512
-  if (ctl && lane == 0) {
-    if (ptx::mbar_wait(&S.qbar, 0, abort_flag, kAttnWaitBudget)) {
-      constexpr uint32_t idesc = ptx::idesc_f16(128, 64, 0);
+  if (warp == kCtlWarp) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA issue
+      bool good = ptx::mbar_wait(&S.q_full, 0, abort_flag, kAttnWaitBudget);
+      constexpr uint32_t idesc_s = ptx::idesc_f16(128, 64, 0);
+      constexpr uint32_t idesc_o = ptx::idesc_f16(128, 64, 0) | (1u << 15) | (1u << 16);  // M/N-major
+      for (int i = 0; i < nc && good; ++i) {
+        const uint32_t par = (uint32_t)(i & 1);
+        // S^T = X q'^T : M = 128 rows, N = 64 heads, K = 512 in two channel halves
+        for (int h2 = 0; h2 < 2 && good; ++h2) {
+          good = ptx::mbar_wait(&S.x_full[h2], par, abort_flag, kAttnWaitBudget);
+          if (!good) break;
+          ptx::tc_fence_after();
 #pragma unroll 4
-      for (int ks = 0; ks < kDMain / 16; ++ks) {
-        const uint64_t ad = ptx::smem_desc_noswizzle(&S.X[2 * ks][0], kRows * 16, 128);
-        const uint64_t bd = ptx::smem_desc_noswizzle(&S.q[2 * ks][0], kHAtt * 16, 128);
-        ptx::mma_f16_ss(tmem, ad, bd, idesc, ks > 0 ? 1u : 0u);
-      }
-      ptx::mma_commit(&S.bar);
-    } else {
-      *abort_flag = 1;
-      report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 20);
-    }
-  }
-  bool ok = true;
-  const int q4 = warp & 3, hh = (warp >> 2) & 1;
-  const int r = q4 * 32 + lane;
-  const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16);
-  float sv[32];
-  if (!ctl) {
-    ok = ptx::mbar_wait_warp(&S.bar, 0, abort_flag, kAttnWaitBudget);
-    if (!ok && lane == 0 && !*abort_flag) {
-      *abort_flag = 1;
-      report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 21);
-    }
-    ok = ok && ptx::mbar_wait_warp(&S.qbar, 0, abort_flag, kAttnWaitBudget);  // colscale landed (acquire)
-    ptx::tc_fence_after();
-    uint32_t a[32];
-    ptx::tmem_ld_32x32b_x32(taddr + (uint32_t)hh * 32u, a);
-    ptx::tmem_wait_ld();
-    const bool v = ok && S.valid[r] != 0;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) sv[j] = v ? __uint_as_float(a[j]) * S.colscale[hh * 32 + j] : -INFINITY;
-    float t[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) t[j] = sv[j];
-    S.red[q4][hh * 32 + lane] = warp_reduce_scatter32(t, lane, MaxOp());
-  }
-  ptx::tc_fence_before();
-  __syncthreads();
-  if (tid < kHAtt) {
-    const float m = fmaxf(fmaxf(S.red[0][tid], S.red[1][tid]), fmaxf(S.red[2][tid], S.red[3][tid]));
-    S.mloc[tid] = m;
-    if (!kMerge) S.M[tid] = m;
-  }
-  if constexpr (kMerge) {
-    cg::cluster_group cluster = cg::this_cluster();
-    cluster.sync();  // chunk maxima visible to the cluster
-    if (tid < kHAtt) {
-      float m = -INFINITY;
-      for (int rr = 0; rr < nchunks; ++rr) m = fmaxf(m, cluster.map_shared_rank(S.mloc, rr)[tid]);
-      S.M[tid] = m;
-    }
-  }
-  __syncthreads();
-
-  // ---- P = exp(S - M) rounded to f16 once; l = column sums of the rounded values
-  if (!ctl) {
-    float pr[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float mh = S.M[hh * 32 + j];
-      const float p = (sv[j] == -INFINITY || mh == -INFINITY) ? 0.0f : __expf(sv[j] - mh);
-      pr[j] = __half2float(__float2half_rn(p));
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint32_t o[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const __half2 h2 = __floats2half2_rn(pr[8 * i + 2 * j], pr[8 * i + 2 * j + 1]);
-        o[j] = *reinterpret_cast<const uint32_t*>(&h2);
-      }
-      *reinterpret_cast<uint4*>(&S.P[hh * 4 + i][r * 8]) = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-    S.red[q4][hh * 32 + lane] = warp_reduce_scatter32(pr, lane, AddOp());
-    ptx::fence_proxy_async_smem();
-  }
-  __syncthreads();
-  ptx::tc_fence_after();
-  if (tid < kHAtt) S.lloc[tid] = ((S.red[0][tid] + S.red[1][tid]) + S.red[2][tid]) + S.red[3][tid];
-
-  // ---- O^T = X^T P^T : four M tiles of 128 channels, N = 64 heads, K = 128 rows
-  if (ctl && lane == 0 && !*abort_flag) {
-    constexpr uint32_t idesc = ptx::idesc_f16(128, 64, 0) | (1u << 15) | (1u << 16);  // both M/N-major
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-      for (int ks = 0; ks < kRows / 16; ++ks) {
-        const uint64_t ad = ptx::smem_desc_noswizzle(&S.X[mt * 16][ks * 16 * 8], 128, kRows * 16);
-        const uint64_t bd = ptx::smem_desc_noswizzle(&S.P[0][ks * 16 * 8], 128, kRows * 16);
-        ptx::mma_f16_ss(tmem + (uint32_t)mt * 64u, ad, bd, idesc, ks > 0 ? 1u : 0u);
-      }
-    ptx::mma_commit(&S.bar);
-  }
-  const int64_t pc = ((int64_t)b * nchunks + chunk) * kHAtt;
-  float* obuf = reinterpret_cast<float*>(&S.X[0][0]);  // O^T as [head][channel]
-  if (!ctl) {
-    ok = ok && ptx::mbar_wait_warp(&S.bar, 1, abort_flag, kAttnWaitBudget);
-    if (!ok && lane == 0 && !*abort_flag) {
-      *abort_flag = 1;
-      report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 22);
-    }
-    ptx::tc_fence_after();
-    ptx::fence_proxy_async_smem();  // the MMAs' reads of X precede the writes below
-#pragma unroll 1
-    for (int mt = 0; mt < 4; mt += 2) {
-      uint32_t a0[32], a1[32];
-      ptx::tmem_ld_32x32b_x32(taddr + (uint32_t)mt * 64u + (uint32_t)hh * 32u, a0);
-      ptx::tmem_ld_32x32b_x32(taddr + (uint32_t)(mt + 1) * 64u + (uint32_t)hh * 32u, a1);
-      ptx::tmem_wait_ld();
-      const int c0 = mt * kRows + r, c1 = c0 + kRows;  // channels
-      if constexpr (kMerge) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          obuf[(hh * 32 + j) * kDMain + c0] = ok ? __uint_as_float(a0[j]) : 0.0f;
-          obuf[(hh * 32 + j) * kDMain + c1] = ok ? __uint_as_float(a1[j]) : 0.0f;
+          for (int ks = h2 * 16; ks < h2 * 16 + 16; ++ks) {
+            const uint64_t ad = ptx::smem_desc_noswizzle(&S.X[2 * ks][0], kRows * 16, 128);
+            const uint64_t bd = ptx::smem_desc_noswizzle(&S.q[2 * ks][0], kQPlane * 2, 128);
+            ptx::mma_f16_ss(tS, ad, bd, idesc_s, ks > 0 ? 1u : 0u);
+          }
         }
-      } else if (ok) {
+        if (!good) break;
+        ptx::mma_commit(&S.s_full);
+        // O^T += X^T P^T : four 128-channel M tiles, N = 64 heads, K = 128 rows
+        good = ptx::mbar_wait(&S.p_full, par, abort_flag, kAttnWaitBudget);
+        if (!good) break;
+        ptx::tc_fence_after();
+        for (int h2 = 0; h2 < 2; ++h2) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          part_o[(pc + hh * 32 + j) * kDMain + c0] = __uint_as_float(a0[j]);
-          part_o[(pc + hh * 32 + j) * kDMain + c1] = __uint_as_float(a1[j]);
-        }
-      }
-    }
-  }
-
-  if constexpr (kMerge) {
-    cg::cluster_group cluster = cg::this_cluster();
-    const int rank = (int)cluster.block_rank();
-    cluster.sync();  // every chunk's O^T and l visible to the cluster
-    if (tid < kHAtt) {
-      float L = 0.0f;
-      for (int rr = 0; rr < nchunks; ++rr) L += cluster.map_shared_rank(S.lloc, rr)[tid];
-      S.invL[tid] = L > 0.0f ? 1.0f / L : 0.0f;
-      if (lse && rank == 0) lse[b * kHAtt + tid] = L > 0.0f ? S.M[tid] + logf(L) : -INFINITY;
-    }
-    __syncthreads();
-    // this CTA's share of the output: float4 slots [lo, hi) of the [64][512]
-    // result, summed over the chunks in rank order with every load of a batch
-    // in flight at once
-    uint32_t peer[kMaxCluster];  // shared::cluster addresses of the chunks' O^T
+          for (int mt = 2 * h2; mt < 2 * h2 + 2; ++mt)
 #pragma unroll
-    for (int rr = 0; rr < kMaxCluster; ++rr) peer[rr] = ptx::mapa_cluster(ptx::smem_u32(obuf), rr < nchunks ? rr : 0);
-    constexpr int kF4 = kHAtt * kDMain / 4;
-    constexpr int kU = 3;
-    const int per = (kF4 + nchunks - 1) / nchunks;
-    const int lo = rank * per, hi = min(kF4, lo + per);
-    float4* ob = reinterpret_cast<float4*>(out + (int64_t)b * kHAtt * kDMain);
-    for (int f0 = lo + tid; f0 < hi; f0 += kU * kAT) {
-      float4 v[kMaxCluster][kU];
-#pragma unroll
-      for (int rr = 0; rr < kMaxCluster; ++rr)
-#pragma unroll
-        for (int u = 0; u < kU; ++u)
-          if (rr < nchunks && f0 + u * kAT < hi) v[rr][u] = ptx::ld_cluster_f4(peer[rr] + (uint32_t)(f0 + u * kAT) * 16u);
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int f = f0 + u * kAT;
-        if (f < hi) {
-          float4 acc = v[0][u];
-#pragma unroll
-          for (int rr = 1; rr < kMaxCluster; ++rr)
-            if (rr < nchunks) {
-              acc.x += v[rr][u].x;
-              acc.y += v[rr][u].y;
-              acc.z += v[rr][u].z;
-              acc.w += v[rr][u].w;
+            for (int ks = 0; ks < kRows / 16; ++ks) {
+              const uint64_t ad = ptx::smem_desc_noswizzle(&S.X[mt * 16][ks * 16 * 8], 128, kRows * 16);
+              const uint64_t bd = ptx::smem_desc_noswizzle(&S.P[0][ks * 16 * 8], 128, kRows * 16);
+              ptx::mma_f16_ss(tmem + (uint32_t)mt * 64u, ad, bd, idesc_o, (i > 0 || ks > 0) ? 1u : 0u);
             }
-          const float il = S.invL[f / (kDMain / 4)];
-          ob[f] = make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
+          ptx::mma_commit(&S.x_free[h2]);  // that channel half of X is no longer read
         }
       }
+      if (!good && !*abort_flag) {
+        *abort_flag = 1;
+        report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 23);
+      }
+      // every MMA issued so far has completed before tensor memory is freed
+      ptx::mma_commit(&S.drained);
+      volatile int keep_waiting = 0;
+      ptx::mbar_wait(&S.drained, 0, &keep_waiting, kAttnWaitBudget);
     }
-    cluster.sync();  // no CTA leaves while another may still read its shared memory
   } else {
-    if (tid < kHAtt) part_ml[pc + tid] = ok ? make_float2(S.M[tid], S.lloc[tid]) : make_float2(-INFINITY, 0.0f);
-  }
-  if (ctl && lane == 0 && *abort_flag) {  // after a timeout: let the q' copy land before the CTA's memory is freed
-    volatile int keep_waiting = 0;
-    ptx::mbar_wait(&S.qbar, 0, &keep_waiting, kAttnWaitBudget);
+    // ------------------------------------------------------ rows and softmax
+    const int q4 = warp & 3, hh = warp >> 2;
+    const int rr = q4 * 32 + lane;  // row of this thread in the softmax (tensor-memory lane)
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    float m2 = -INFINITY, l_run = 0.0f;  // this lane's head hh * 32 + lane: reference (log2 units), sum
+    S.m2w[warp][lane] = 0.0f;
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&S.q_full);
+    bool good = true;
+    for (int i = 0; i < nc && good; ++i) {
+      const uint32_t par = (uint32_t)(i & 1);
+      // the next chunk's index, in flight during the wait and the dequantization
+      const int gr_next = (c0 + i + 1) * kRows + r;
+      const int64_t idx_next = i + 1 < nc ? fetch_index(topk, k, b, gr_next) : -1;
+      if (i > 0) {
+        good = ptx::mbar_wait_warp(&S.x_free[half], par ^ 1u, abort_flag, kAttnWaitBudget);
+        if (!good) break;
+      }
+      const bool valid = dequant_half_row(S, rf, r, half);
+      if (half == 0) S.valid[r] = valid ? 1 : 0;
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&S.x_full[half]);
+      if (i + 1 < nc)
+        issue_row(rf, idx_next, kv_codes, kv_scales, seq_stride, swa, n_swa, k, b, gr_next, half, ws);
+
+      // ---- chunk softmax
+      good = ptx::mbar_wait_warp(&S.s_full, par, abort_flag, kAttnWaitBudget) &&
+             ptx::mbar_wait_warp(&S.x_full[0], par, abort_flag, kAttnWaitBudget) &&  // valid[] (acquire)
+             ptx::mbar_wait_warp(&S.q_full, 0, abort_flag, kAttnWaitBudget);         // c2 (acquire)
+      if (!good) break;
+      ptx::tc_fence_after();
+      float sv[32];
+      {
+        uint32_t a[32];
+        ptx::tmem_ld_32x32b_x32(tS + lane_base + (uint32_t)hh * 32u, a);
+        ptx::tmem_wait_ld();
+        const bool v = S.valid[rr] != 0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sv[j] = v ? __uint_as_float(a[j]) : -INFINITY;  // raw S
+        float t[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) t[j] = sv[j];
+        S.red[q4][hh * 32 + lane] = warp_reduce_scatter32(t, lane, MaxOp());
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&S.red_full);
+      good = ptx::mbar_wait_warp(&S.red_full, par, abort_flag, kAttnWaitBudget);
+      if (!good) break;
+      const int h = hh * 32 + lane;
+      const float cm = fmaxf(fmaxf(S.red[0][h], S.red[1][h]), fmaxf(S.red[2][h], S.red[3][h])) * S.c2[h];
+      float alpha = 1.0f;
+      if (cm > m2 + kTau2) {  // also the first chunk with a row of this head
+        alpha = m2 == -INFINITY ? 0.0f : ptx::ex2(m2 - cm);
+        m2 = cm;
+      }
+      const bool moved = __any_sync(0xffffffffu, alpha != 1.0f);
+      const bool rescale = i > 0 && moved;
+      if (moved) {  // this warp's copy of its heads' references
+        S.m2w[warp][lane] = m2 == -INFINITY ? 0.0f : m2;
+        __syncwarp();
+      }
+      if (i > 0) {  // P and O of the previous chunk are no longer read
+        good = ptx::mbar_wait_warp(&S.x_free[1], par ^ 1u, abort_flag, kAttnWaitBudget);
+        if (!good) break;
+        ptx::tc_fence_after();
+      }
+      {
+        float pr[32];  // the probabilities as rounded to f16, for the sums
+        uint32_t ph[16];
+        const float4* m2v = reinterpret_cast<const float4*>(S.m2w[warp]);
+        const float4* c2v = reinterpret_cast<const float4*>(&S.c2[hh * 32]);
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          const float4 mq = m2v[j / 4], cq = c2v[j / 4];
+          const float mm[4] = {mq.x, mq.y, mq.z, mq.w}, cc4[4] = {cq.x, cq.y, cq.z, cq.w};
+#pragma unroll
+          for (int t = 0; t < 4; ++t) pr[j + t] = ptx::ex2(fmaf(sv[j + t], cc4[t], -mm[t]));  // -inf rows -> 0
+        }
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const __half2 h2 = __floats2half2_rn(pr[j], pr[j + 1]);
+          ph[j / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+          const float2 back = __half22float2(h2);
+          pr[j] = back.x;
+          pr[j + 1] = back.y;
+        }
+#pragma unroll
+        for (int i4 = 0; i4 < 4; ++i4)
+          *reinterpret_cast<uint4*>(&S.P[hh * 4 + i4][rr * 8]) =
+              make_uint4(ph[4 * i4], ph[4 * i4 + 1], ph[4 * i4 + 2], ph[4 * i4 + 3]);
+        S.red2[q4][h] = warp_reduce_scatter32(pr, lane, AddOp());
+      }
+      if (rescale) {  // O^T columns of this warp's heads, its lane quarter, all four M tiles
+#pragma unroll 1
+        for (int mt = 0; mt < 4; ++mt) {
+          uint32_t a[32];
+          const uint32_t ta = tmem + lane_base + (uint32_t)mt * 64u + (uint32_t)hh * 32u;
+          ptx::tmem_ld_32x32b_x32(ta, a);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            a[j] = __float_as_uint(__uint_as_float(a[j]) * __shfl_sync(0xffffffffu, alpha, j));
+          ptx::tmem_st_32x32b_x32(ta, a);
+        }
+        ptx::tmem_wait_st();
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&S.p_full);
+      good = ptx::mbar_wait_warp(&S.p_full, par, abort_flag, kAttnWaitBudget);
+      if (!good) break;
+      l_run = fmaf(alpha, l_run, ((S.red2[0][h] + S.red2[1][h]) + S.red2[2][h]) + S.red2[3][h]);
+    }
+    if (good)
+      good = ptx::mbar_wait_warp(&S.x_free[1], (uint32_t)((nc - 1) & 1), abort_flag, kAttnWaitBudget);
+    if (!good && lane == 0 && !*abort_flag) {
+      *abort_flag = 1;
+      report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 24);
+    }
+    // ---- epilogue: O^T rows = channels of this lane quarter, 32 heads per warp;
+    // for each head the warp stores 32 consecutive channels
+    if (good) {
+      ptx::tc_fence_after();
+      const int h = hh * 32 + lane;
+      const float inv = kPartial ? 1.0f : (l_run > 0.0f ? 1.0f / l_run : 0.0f);
+      const float m_nat = m2 / kLog2e;  // reference in natural units
+      if (q4 == 0) {
+        if (kPartial)
+          part_ml[((int64_t)b * gridDim.x + split) * kHAtt + h] = make_float2(m_nat, l_run);
+        else if (lse)
+          lse[b * kHAtt + h] = l_run > 0.0f ? m_nat + logf(l_run) : -INFINITY;
+      }
+      float* ob = kPartial ? part_o + ((int64_t)b * gridDim.x + split) * kHAtt * kDMain
+                           : out + (int64_t)b * kHAtt * kDMain;
+#pragma unroll 1
+      for (int mt = 0; mt < 4; ++mt) {
+        uint32_t a[32];
+        ptx::tmem_ld_32x32b_x32(tmem + lane_base + (uint32_t)mt * 64u + (uint32_t)hh * 32u, a);
+        ptx::tmem_wait_ld();
+        const int c = mt * kRows + rr;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          ob[(hh * 32 + j) * kDMain + c] = __uint_as_float(a[j]) * __shfl_sync(0xffffffffu, inv, j);
+      }
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
-  if (ctl) {
+  if (warp == kCtlWarp) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kAttnTmemCols);
   }
@@ -475,34 +536,42 @@ __global__ void __launch_bounds__(128) k_attn_merge(const float* __restrict__ pa
 }
 
 struct AttnWs {
-  uint16_t* qs;     // [B] staged q' images
-  float* qscale;    // [B][64]
-  float* part_o;    // [B][nchunks][64][512] (partials path only)
-  float2* part_ml;  // [B][nchunks][64]
+  float* part_o;    // [B][nsplit][64][512] (split queries only)
+  float2* part_ml;  // [B][nsplit][64]
   size_t bytes;
 };
 
-AttnWs attn_ws_layout(void* ws, int32_t B, int nchunks) {
+// Chunks per CTA and CTAs per query: one CTA per query once the batch fills the
+// GPU; below that a query's chunks are spread over up to kFillCtas / B CTAs
+// (then evened out) at the cost of a merge.  Depends only on the shapes, so the
+// workspace size does too.
+constexpr int kFillCtas = 148;
+struct AttnPlan {
+  int nchunks, cps, nsplit;
+};
+AttnPlan attn_plan(int32_t B, int32_t k, int32_t n_swa) {
+  AttnPlan p;
+  p.nchunks = (int)cdiv(k + n_swa, kRows);
+  if (p.nchunks < 1) p.nchunks = 1;
+  int want = B >= kFillCtas ? 1 : kFillCtas / B;
+  want = want < 1 ? 1 : (want > p.nchunks ? p.nchunks : want);
+  p.cps = (int)cdiv(p.nchunks, want);
+  p.nsplit = (int)cdiv(p.nchunks, p.cps);
+  return p;
+}
+
+AttnWs attn_ws_layout(void* ws, int32_t B, const AttnPlan& plan) {
   AttnWs L{};
   size_t off = kWsHeader;
   char* base = (char*)ws;
-  L.qs = (uint16_t*)(base ? base + off : nullptr);
-  off += align_up((size_t)B * kQBytes, 256);
-  L.qscale = (float*)(base ? base + off : nullptr);
-  off += align_up((size_t)B * kHAtt * 4, 256);
-  if (nchunks > kMaxCluster) {
+  if (plan.nsplit > 1) {
     L.part_o = (float*)(base ? base + off : nullptr);
-    off += align_up((size_t)B * nchunks * kHAtt * kDMain * 4, 256);
+    off += align_up((size_t)B * plan.nsplit * kHAtt * kDMain * 4, 256);
     L.part_ml = (float2*)(base ? base + off : nullptr);
-    off += align_up((size_t)B * nchunks * kHAtt * 8, 256);
+    off += align_up((size_t)B * plan.nsplit * kHAtt * 8, 256);
   }
   L.bytes = off;
   return L;
-}
-
-int attn_chunks(int32_t k, int32_t n_swa) {
-  const int n = (int)cdiv(k + n_swa, kRows);
-  return n < 1 ? 1 : n;
 }
 
 }  // namespace
@@ -511,7 +580,7 @@ int attn_chunks(int32_t k, int32_t n_swa) {
 
 extern "C" size_t csa2_sparse_attn_workspace_size(int32_t B, int32_t k, int32_t n_swa) {
   if (B <= 0 || k < 0 || n_swa < 0) return 0;
-  return csa2::attn_ws_layout(nullptr, B, csa2::attn_chunks(k, n_swa)).bytes;
+  return csa2::attn_ws_layout(nullptr, B, csa2::attn_plan(B, k, n_swa)).bytes;
 }
 
 extern "C" csa2_status csa2_sparse_attn_decode(const csa2_kv_planes* kv, int32_t B, const int32_t* topk,
@@ -524,51 +593,28 @@ extern "C" csa2_status csa2_sparse_attn_decode(const csa2_kv_planes* kv, int32_t
   if (!planes_ok(kv) || B <= 0 || B > 65535 || k < 0 || k > CSA2_MAX_TOPK || n_swa < 0 || n_swa > CSA2_MAX_SWA)
     return CSA2_ERR_INVALID_ARG;
   if ((k > 0 && !topk) || (n_swa > 0 && !swa_e4m3) || !q_bf16 || !out) return CSA2_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.0f) || softmax_scale > 3.0e38f) return CSA2_ERR_INVALID_ARG;  // positive, finite
   if (!aligned(q_bf16, 16) || !aligned(out, 16) || (swa_e4m3 && !aligned(swa_e4m3, 16)))
     return CSA2_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, 256)) return CSA2_ERR_WORKSPACE;
-  const int nchunks = attn_chunks(k, n_swa);
-  AttnWs L = attn_ws_layout(ws, B, nchunks);
+  const AttnPlan plan = attn_plan(B, k, n_swa);
+  AttnWs L = attn_ws_layout(ws, B, plan);
   if (ws_bytes < L.bytes) return CSA2_ERR_WORKSPACE;
   if (reset_error(ws, st) != CSA2_OK) return CSA2_ERR_CUDA;
-  {
-    KernelTimer timer("k_attn_qprep", st);
-    k_attn_qprep<<<dim3(kHAtt / 8, B), 256, 0, st>>>((const uint16_t*)q_bf16, softmax_scale, L.qs, L.qscale);
-  }
   const int smem = (int)sizeof(AttnSmem);
-  if (nchunks <= kMaxCluster) {
-    if (cudaFuncSetAttribute(k_attn<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return CSA2_ERR_CUDA;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(nchunks, B);
-    cfg.blockDim = dim3(kAT);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)nchunks;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlap the q' staging kernel
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    KernelTimer timer("k_attn", st);
-    if (cudaLaunchKernelEx(&cfg, k_attn<true>, kv->kv_codes, kv->kv_scales, kv->seq_stride, topk, k, swa_e4m3,
-                           n_swa, (const uint16_t*)L.qs, (const float*)L.qscale, nchunks, out, lse_out,
-                           (float*)nullptr, (float2*)nullptr, ws) != cudaSuccess)
-      return CSA2_ERR_CUDA;
-  } else {
-    if (cudaFuncSetAttribute(k_attn<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return CSA2_ERR_CUDA;
-    {
-      KernelTimer timer("k_attn_part", st);
-      k_attn<false><<<dim3(nchunks, B), kAT, smem, st>>>(kv->kv_codes, kv->kv_scales, kv->seq_stride, topk, k,
-                                                          swa_e4m3, n_swa, L.qs, L.qscale, nchunks, out,
-                                                          lse_out, L.part_o, L.part_ml, ws);
-    }
+  const bool partial = plan.nsplit > 1;
+  auto kern = partial ? k_attn<true> : k_attn<false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return CSA2_ERR_CUDA;
+  {
+    KernelTimer timer(partial ? "k_attn_part" : "k_attn", st);
+    kern<<<dim3(plan.nsplit, B), kAT, smem, st>>>(kv->kv_codes, kv->kv_scales, kv->seq_stride, topk, k, swa_e4m3,
+                                                   n_swa, (const uint16_t*)q_bf16, softmax_scale, plan.nchunks,
+                                                   plan.cps, out, lse_out, L.part_o, L.part_ml, ws);
+  }
+  if (partial) {
     KernelTimer timer("k_attn_merge", st);
-    k_attn_merge<<<B * kHAtt, 128, 0, st>>>(L.part_o, L.part_ml, nchunks, out, lse_out);
+    k_attn_merge<<<B * kHAtt, 128, 0, st>>>(L.part_o, L.part_ml, plan.nsplit, out, lse_out);
   }
   return launch_status();
 }

@@ -109,6 +109,18 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Waits until the grids this one depends on (programmatic dependent launch)
+// have completed and their memory is visible; a no-op without such a launch.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// 2^x by the hardware approximation (ex2.approx: relative error about 2^-22;
+// 2^-inf = 0)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ------------------------------------------------------------------ cluster
 // address of the same shared-memory variable in CTA `rank` of the cluster
 __device__ __forceinline__ uint32_t mapa_cluster(uint32_t smem_addr, int rank) {

@@ -204,6 +204,7 @@ csa2_status csa2_index_topk_noalloc(const csa2_kv_planes* kv, int32_t B, const i
  *   topk      [B][k] int32 entry indices of slot b (-1 = skip)
  *   swa_e4m3  [B][n_swa][512] FP8 E4M3 bytes (no scale), 0 <= n_swa <= 128
  *   q_bf16    [B][64][512] bf16 (unscaled);  out [B][64][512] fp32;  lse_out [B][64] or NULL
+ *   softmax_scale  positive and finite (CSA2_ERR_INVALID_ARG otherwise)
  * An index outside [0, seq_stride) is skipped and reported as CSA2_ERR_INDEX_RANGE
  * through the workspace error word.  With no rows, out = 0 and lse = -inf. */
 csa2_status csa2_sparse_attn_decode(const csa2_kv_planes* kv, int32_t B, const int32_t* topk,

@@ -129,6 +129,9 @@ def test_host_validation_without_gpu(L):
                               None) == 2  # m = 3
     assert L.csa2_sparse_attn_decode(ctypes.byref(fake), 1, 16, 512, 16, 129, 16, 1.0, 16, None, 256,
                                      1 << 30, None) == 1  # n_swa > 128
+    for bad_scale in (0.0, -0.04, float("inf"), float("nan")):  # the softmax scale must be positive, finite
+        assert L.csa2_sparse_attn_decode(ctypes.byref(fake), 1, 16, 512, 16, 128, 16, bad_scale, 16, None,
+                                         256, 1 << 30, None) == 1
 
 
 def test_workspace_queries(L):
