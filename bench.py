@@ -309,6 +309,72 @@ def run_step40(dev, st, steps: int, warmup: int):
     }
 
 
+AT_B, AT_N, AT_SEED = 128, 65536, 5
+AT_WORKLOAD = ("sparse MQA decode attention alone: batch 128, 64 heads x 512 channels, top-512 "
+               "FP4 entries of a 65,536-entry cache + 128 FP8 window rows per query")
+
+
+def run_attention(dev, st, steps: int, warmup: int):
+    """csa2_sparse_attn_decode alone at the 40-layer step's batch (one CTA per query)."""
+    import numpy as np
+    import torch
+
+    import compressed_sparse_attention_nvfp4_gb300 as csa2
+    from compressed_sparse_attention_nvfp4_gb300 import workload as WL
+
+    B, Nn = AT_B, AT_N
+    rng = np.random.default_rng(AT_SEED)
+    sel = np.sort(np.stack([rng.choice(Nn, K_TOP, replace=False) for _ in range(B)]), axis=1)
+    with torch.cuda.stream(st):
+        planes = csa2.Planes.empty(B, Nn, dev)
+        WL.fill_planes(planes, AT_SEED, 0, B, Nn, stream=st)
+        q, _ = WL.attn_query_dev(AT_SEED, 0, B, dev)
+        swa = WL.swa_dev(AT_SEED, 0, B, NSWA, dev, stream=st)
+        topk = torch.from_numpy(sel.astype(np.int32)).to(dev)
+        out = torch.empty((B, 64, 512), dtype=torch.float32, device=dev)
+        lse = torch.empty((B, 64), dtype=torch.float32, device=dev)
+        ws = csa2.workspace(csa2.sparse_attn_workspace_size(B, K_TOP, NSWA), dev)
+    torch.cuda.synchronize()
+    scale = 1.0 / math.sqrt(512)
+
+    def call():
+        csa2.sparse_attn_decode(planes, B, topk, K_TOP, swa, NSWA, q, scale, out, ws, lse_out=lse, stream=st)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    assert csa2.check(ws, st)[0] == 0
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for _ in range(steps):
+        call()
+    b.record(st)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    csa2.timing_enable(True)
+    for _ in range(min(steps, 20)):
+        call()
+    torch.cuda.synchronize()
+    kt = csa2.kernel_times()
+    csa2.timing_enable(False)
+    n_k, t_k = kt["k_attn"]
+    k_ms = t_k / n_k
+    # algorithmic bytes: selected entries, window rows, q in, output out; flops: S and O
+    rows = K_TOP + NSWA
+    call_bytes = B * (K_TOP * MAIN_BYTES + NSWA * SWA_ROW + 64 * 512 * 2 + 64 * 512 * 4)
+    call_flop = B * rows * 64 * 512 * 2 * 2
+    hbm, kind = peaks()
+    tp, tkind = tensor_peak()
+    return {
+        "workload": AT_WORKLOAD, "calls": steps, "ms_per_call": round(ms, 4),
+        "kernels_ms_per_launch": {k: round(tm / n, 4) for k, (n, tm) in sorted(kt.items())},
+        "k_attn": {"algorithmic_bytes": call_bytes, "hbm_gbs": round(call_bytes / (k_ms * 1e-3) / 1e9, 1),
+                   "hbm_frac": round(call_bytes / (k_ms * 1e-3) / 1e9 / hbm, 4), "hbm_peak_kind": kind,
+                   "flop": call_flop, "tflops": round(call_flop / (k_ms * 1e-3) / 1e12, 1),
+                   "tensor_frac": round(call_flop / (k_ms * 1e-3) / 1e12 / tp, 4), "tensor_peak_kind": tkind},
+    }
+
+
 def tensor_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -473,6 +539,8 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": launches,
         "clocks": clocks,
     }
+    if not args.no_attn:
+        line["attention_b128"] = run_attention(dev, st, 50, 3)
     if not args.no_cache_write:
         line["cache_write"] = run_cache_write(dev, st, 5, 2)
     if not args.no_step40:
@@ -493,6 +561,10 @@ def main():
                     help="skip the prefill cache-write measurement (its own object in the line)")
     ap.add_argument("--no-step40", action="store_true",
                     help="skip the 40-layer step measurement (its own object in the line)")
+    ap.add_argument("--no-attn", action="store_true",
+                    help="skip the batch-128 attention measurement (its own object in the line)")
+    ap.add_argument("--attn-only", action="store_true",
+                    help="profiling case: only the batch-128 attention, printed as its own line")
     ap.add_argument("--step40-only", action="store_true",
                     help="profiling case: only the 40-layer step, printed as its own line")
     ap.add_argument("--cache-write-only", action="store_true",
@@ -534,6 +606,19 @@ def main():
 
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
+    if args.attn_only:
+        import torch
+
+        torch.cuda.set_device(local_rank)
+        import compressed_sparse_attention_nvfp4_gb300 as csa2
+
+        csa2.lib()
+        dev = torch.device("cuda", local_rank)
+        st = torch.cuda.Stream(device=dev)
+        if rank == 0:
+            print(json.dumps({"attention_b128": run_attention(dev, st, max(1, min(args.steps, 200)),
+                                                              max(1, args.warmup))}), flush=True)
+        return
     if args.step40_only:
         import torch
 
