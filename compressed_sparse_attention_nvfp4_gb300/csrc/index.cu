@@ -450,10 +450,10 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
     // after every CTA passed the next pass's barrier (and so finished reading)
     cluster.sync();
     if (pass == 0) {
-      if (tid == 0) {
-        unsigned tv = 0;
-        for (int r = 0; r < ncl; ++r) tv += *cluster.map_shared_rank(&cvalid, r);
-        s_need = (int)min((int64_t)a.k, (int64_t)tv);
+      if (wid == 0) {  // lane r reads CTA r's count: one round trip instead of ncl
+        unsigned tv = lane < ncl ? *cluster.map_shared_rank(&cvalid, lane) : 0u;
+        tv = __reduce_add_sync(0xffffffffu, tv);
+        if (lane == 0) s_need = (int)min((int64_t)a.k, (int64_t)tv);
       }
       __syncthreads();
       need_total = s_need;
@@ -502,16 +502,23 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
       atomicAdd(&ccount[1], weq);
     }
     cluster.sync();
-    if (tid == 0) {
+    if (wid == 0) {  // lane r reads CTA r's counts at once, then lane 0 combines them in rank order
+      int g_r = 0, e_r = 0;
+      if (lane < rank) {
+        const int* cc = cluster.map_shared_rank(ccount, lane);
+        g_r = cc[0];
+        e_r = cc[1];
+      }
       int eq_before = 0, out_before = 0;
       for (int r = 0; r < rank; ++r) {
-        const int* cc = cluster.map_shared_rank(ccount, r);
-        const int g_r = cc[0], e_r = cc[1];
-        out_before += g_r + max(0, min(e_r, take_eq - eq_before));
-        eq_before += e_r;
+        const int gr = __shfl_sync(0xffffffffu, g_r, r), er = __shfl_sync(0xffffffffu, e_r, r);
+        out_before += gr + max(0, min(er, take_eq - eq_before));
+        eq_before += er;
       }
-      s_base_eq = eq_before;
-      s_base_out = out_before;
+      if (lane == 0) {
+        s_base_eq = eq_before;
+        s_base_out = out_before;
+      }
     }
     __syncthreads();
     int eq_rank;

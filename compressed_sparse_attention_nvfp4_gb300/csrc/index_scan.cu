@@ -262,6 +262,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (warp == 0) {
       // ------------------------------------------------------------ producer
       if (lane == 0) {
+        // the keys are read once: keep them from evicting the block maxima and
+        // pool the selection kernels read back
+        const uint64_t pol = ptx::policy_evict_first();
         Ring<kStages> st(0);
         for (int i = 0; i < my_tiles; ++i, st.step(1)) {
           const int s = st.slot;
@@ -278,9 +281,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             const uint32_t cnt4 = scale_bulk ? (cnt & ~3u) : 0u;
             // scales first, on their own barrier, so that their reorder overlaps the codes' arrival
             ptx::mbar_arrive_expect_tx(&S.sfull[s], cnt4 * 4u);
-            if (cnt4) ptx::bulk_g2s(S.scales[s], scales_b + j0 * 4, cnt4 * 4u, &S.sfull[s]);
+            if (cnt4) ptx::bulk_g2s_hint(S.scales[s], scales_b + j0 * 4, cnt4 * 4u, &S.sfull[s], pol);
             ptx::mbar_arrive_expect_tx(&S.full[s], kCodeBytes);
-            ptx::tma_load_2d(S.codes[s], &map_tile, 0, (int)(b * p.seq_stride + j0), &S.full[s]);
+            ptx::tma_load_2d_hint(S.codes[s], &map_tile, 0, (int)(b * p.seq_stride + j0), &S.full[s], pol);
           } else {
             int pbv[16];
             uint32_t cnt[16];
