@@ -356,10 +356,10 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
   extern __shared__ uint4 keys_s[];  // thread t: 4-key slots t*S .. t*S+S-1, swizzled
   __shared__ unsigned whist[kWarpsSel][kBins];
   __shared__ unsigned chist[2][kBins];  // this CTA's histogram of pass p in chist[p & 1]
-  __shared__ unsigned cvalid;
+  __shared__ unsigned cvalid, ckmin, ckmax;  // this CTA's valid count and key range, read by the cluster
   __shared__ int ccount[2];
   __shared__ uint32_t s_prefix, s_mask;
-  __shared__ int s_need;
+  __shared__ int s_need, s_shift0;
   __shared__ int s_base_eq, s_base_out;
 
   cg::cluster_group cluster = cg::this_cluster();
@@ -385,12 +385,13 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
 
   if (tid == 0) {
     cvalid = 0;
-    s_prefix = 0;
-    s_mask = 0;
+    ckmin = 0xFFFFFFFFu;
+    ckmax = 0;
   }
   // load the run once, up to kLoadBatch slots in flight per thread
   constexpr int kLoadBatch = NT >= 1024 ? 4 : 16;  // within the register budget of NT threads
   unsigned myvalid = 0;
+  uint32_t mykmin = 0xFFFFFFFFu, mykmax = 0;
   for (int v0 = 0; v0 < nslot; v0 += kLoadBatch) {
     uint4 k4[kLoadBatch];
 #pragma unroll
@@ -402,22 +403,61 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
     for (int u = 0; u < kLoadBatch; ++u) {
       if (v0 + u < nslot) {
         myslots[(v0 + u) ^ swz] = k4[u];
-        myvalid += (k4[u].x != 0u) + (k4[u].y != 0u) + (k4[u].z != 0u) + (k4[u].w != 0u);
+        const uint32_t kv[4] = {k4[u].x, k4[u].y, k4[u].z, k4[u].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (kv[i] != 0u) {
+            ++myvalid;
+            mykmin = min(mykmin, kv[i]);
+            mykmax = max(mykmax, kv[i]);
+          }
       }
     }
   }
   myvalid = __reduce_add_sync(0xffffffffu, myvalid);
+  mykmin = __reduce_min_sync(0xffffffffu, mykmin);
+  mykmax = __reduce_max_sync(0xffffffffu, mykmax);
   __syncthreads();
-  if (lane == 0) atomicAdd(&cvalid, myvalid);
+  if (lane == 0) {
+    atomicAdd(&cvalid, myvalid);
+    atomicMin(&ckmin, mykmin);
+    atomicMax(&ckmax, mykmax);
+  }
+  // the cluster's valid count and key range: the bits above the highest bit
+  // where the smallest and largest keys differ are common to every key, so the
+  // digits start below them (the first digit then splits the keys)
+  cluster.sync();
+  if (wid == 0) {  // lane r reads CTA r's values: one round trip
+    unsigned tv = 0, kmn = 0xFFFFFFFFu, kmx = 0;
+    if (lane < ncl) {
+      tv = *cluster.map_shared_rank(&cvalid, lane);
+      kmn = *cluster.map_shared_rank(&ckmin, lane);
+      kmx = *cluster.map_shared_rank(&ckmax, lane);
+    }
+    tv = __reduce_add_sync(0xffffffffu, tv);
+    kmn = __reduce_min_sync(0xffffffffu, kmn);
+    kmx = __reduce_max_sync(0xffffffffu, kmx);
+    if (lane == 0) {
+      s_need = (int)min((int64_t)a.k, (int64_t)tv);
+      const int top = kmn < kmx ? 31 - __clz((int)(kmn ^ kmx)) : 7;  // highest differing bit
+      s_shift0 = max(top - 7, 0);
+      s_mask = top >= 31 ? 0u : (0xFFFFFFFFu << (top + 1));  // bits shared by every valid key
+      s_prefix = tv ? (kmn & s_mask) : 0u;
+    }
+  }
+  __syncthreads();
+  const int need_total = s_need;
+  const int shift0 = s_shift0;
 
-  int need_total = 0;
   int pass = 0;
-  for (int shift = 24; shift >= 0; shift -= 8, ++pass) {
+  // digit of pass p: bits [shift + 7, shift] (the last pass may reach below bit 0)
+  for (int shift = shift0; need_total > 0 && shift > -8; shift -= 8, ++pass) {
     for (int d = lane; d < kBins; d += 32) myhist[d] = 0;
     __syncthreads();
     const uint32_t prefix = s_prefix, mask = s_mask;
-    uint32_t last = 0xFFFFFFFFu;
-    unsigned run = 0;
+    // four independent run-length counters (one per key of a slot) for ILP
+    uint32_t last[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
+    unsigned run[4] = {0, 0, 0, 0};
     for (int v = 0; v < nslot; ++v) {
       const uint4 k4 = myslots[v ^ swz];
       const uint32_t kk4[4] = {k4.x, k4.y, k4.z, k4.w};
@@ -425,18 +465,20 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
       for (int i = 0; i < 4; ++i) {
         const uint32_t kk = kk4[i];
         if (kk != 0u && (kk & mask) == prefix) {
-          const uint32_t d = (kk >> shift) & 255u;
-          if (d == last) {
-            ++run;
+          const uint32_t d = (shift >= 0 ? kk >> shift : kk << -shift) & 255u;
+          if (d == last[i]) {
+            ++run[i];
           } else {
-            if (run) atomicAdd(&myhist[last], run);
-            last = d;
-            run = 1;
+            if (run[i]) atomicAdd(&myhist[last[i]], run[i]);
+            last[i] = d;
+            run[i] = 1;
           }
         }
       }
     }
-    if (run) atomicAdd(&myhist[last], run);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (run[i]) atomicAdd(&myhist[last[i]], run[i]);
     __syncthreads();
     unsigned* ch = chist[pass & 1];
     if (tid < kBins) {  // this CTA's bin totals (thread t <-> bin 255 - t)
@@ -449,16 +491,6 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
     // one barrier per pass: the other buffer is rewritten two passes later,
     // after every CTA passed the next pass's barrier (and so finished reading)
     cluster.sync();
-    if (pass == 0) {
-      if (wid == 0) {  // lane r reads CTA r's count: one round trip instead of ncl
-        unsigned tv = lane < ncl ? *cluster.map_shared_rank(&cvalid, lane) : 0u;
-        tv = __reduce_add_sync(0xffffffffu, tv);
-        if (lane == 0) s_need = (int)min((int64_t)a.k, (int64_t)tv);
-      }
-      __syncthreads();
-      need_total = s_need;
-      if (need_total == 0) break;  // uniform across the cluster
-    }
     const int need = s_need;
     const int bin = kBins - 1 - tid;  // negative for threads beyond the 256 bins
     unsigned h = 0;
@@ -473,8 +505,8 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
     ScanI(scan_tmp).InclusiveSum(cum, cum);
     __syncthreads();  // s_need read above before it is rewritten
     if (bin >= 0 && cum >= need && cum - (int)h < need) {
-      s_prefix = prefix | ((uint32_t)bin << shift);
-      s_mask = mask | (255u << shift);
+      s_prefix = prefix | (shift >= 0 ? (uint32_t)bin << shift : (uint32_t)bin >> -shift);
+      s_mask = mask | (shift >= 0 ? 255u << shift : 255u >> -shift);
       s_need = need - (cum - (int)h);
     }
     __syncthreads();
