@@ -382,6 +382,30 @@ def tensor_peak():
     return 1900.0, "fallback bf16 (burst)"
 
 
+def replica_seed(base: int, rank: int) -> int:
+    """Seed of rank `rank`'s replica: rank 0 keeps the workload's seed, the others get
+    distinct synthetic problems of the same shape (weak scaling: one batch per GPU)."""
+    return base + 1000 * rank
+
+
+def max_over_ranks(times, world: int, device="cpu"):
+    """Each timing replaced by its maximum over the ranks: the slowest replica sets the
+    job's pace.  Collective over the default process group when world > 1."""
+    if world <= 1:
+        return [float(t) for t in times]
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x) for x in times], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_rate(world: int, per_rank_units: int, steps: int, ms: float) -> float:
+    """Whole-job units per second: every rank processed per_rank_units per step."""
+    return world * per_rank_units * steps / (ms * 1e-3)
+
+
 def run_ours(args, rank, world, local_rank):
     import numpy as np
     import torch
@@ -394,13 +418,14 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     csa2.lib()
     st = torch.cuda.Stream(device=dev)
+    seed = replica_seed(SEED, rank)
     with torch.cuda.stream(st):
         planes = csa2.Planes.empty(B, N, dev)
-        qd, wd, q_h, w_h = WL.index_query_dev(SEED, 0, B, dev)
+        qd, wd, q_h, w_h = WL.index_query_dev(seed, 0, B, dev)
         hv = W.hot_vectors(q_h, w_h, 3.0)
-        WL.fill_planes(planes, SEED, 0, B, N, hot_prob=0.02, hotvecs=hv, stream=st)
-        qa_d, qa_h = WL.attn_query_dev(SEED, 0, B, dev)
-        swa_d = WL.swa_dev(SEED, 0, B, NSWA, dev, stream=st)
+        WL.fill_planes(planes, seed, 0, B, N, hot_prob=0.02, hotvecs=hv, stream=st)
+        qa_d, qa_h = WL.attn_query_dev(seed, 0, B, dev)
+        swa_d = WL.swa_dev(seed, 0, B, NSWA, dev, stream=st)
         ne = torch.full((B,), N, dtype=torch.int32, device=dev)
         topk = torch.empty((B, K_TOP), dtype=torch.int32, device=dev)
         pool = torch.empty((B, KEEP), dtype=torch.int32, device=dev)
@@ -494,12 +519,7 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = e_start.elapsed_time(e_stop)
     assert csa2.check(ws_i, st)[0] == 0 and csa2.check(ws_a, st)[0] == 0
 
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([elapsed_ms, e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms, e2e_ms = t.tolist()
+    elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], world, dev)
     if rank != 0:
         return None
     hbm, peak_kind = peaks()
@@ -512,7 +532,7 @@ def run_ours(args, rank, world, local_rank):
     traffic = recorded_traffic(fp)
     # kernel launches of the K timed steps: the library's count per instrumented step x K
     launches = round(sum(n for n, _ in ktimes.values()) * args.steps / n_instr)
-    value = world * B * args.steps / (elapsed_ms * 1e-3)
+    value = job_rate(world, B, args.steps, elapsed_ms)
     step_bytes = B * (N * IDX_BYTES + K_TOP * MAIN_BYTES + NSWA * SWA_ROW)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -520,7 +540,7 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": args.dtype_label, "data": "synthetic (seeded counter-based generator)",
         "config": {"workload": WORKLOAD, "B": B, "N_entries": N, "k": K_TOP, "block": BLOCK,
-                   "n_blocks_keep": KEEP, "n_swa": NSWA, "seed": SEED,
+                   "n_blocks_keep": KEEP, "n_swa": NSWA, "seed": SEED if world == 1 else f"{SEED} + 1000 x rank",
                    "l2": "inputs larger than L2 (11.95 GB cache resident in HBM); no flush",
                    "parallelism": f"replicas x{world}"},
         "step_breakdown_ms": {"index_topk": round(idx_ms, 4), "sparse_attn": round(att_ms, 4)},
@@ -534,7 +554,7 @@ def run_ours(args, rank, world, local_rank):
                      "launch_ms": round(scan_avg_ms, 4), "sources": fp,
                      "index_call": {"achieved": round(idx_achieved, 1),
                                     "frac": round(idx_achieved / hbm, 4)}},
-        "e2e": {"value": round(world * B * args.steps / (e2e_ms * 1e-3), 2), "unit": UNIT,
+        "e2e": {"value": round(job_rate(world, B, args.steps, e2e_ms), 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clocks,
