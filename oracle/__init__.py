@@ -51,7 +51,7 @@ def _load():
         lib.o_index_group_margin.argtypes = [vp]
         lib.o_index_group_margin.restype = f64
         lib.o_cache_write.argtypes = [vp, i64, ctypes.c_int, vp, vp, vp, ctypes.c_int, vp, vp, vp,
-                                      vp, vp, vp, ctypes.c_int]
+                                      vp, vp, vp, ctypes.c_int, vp, f64, ctypes.c_int, f64, f64, f64, vp]
         lib.o_cache_write.restype = ctypes.c_int
         lib.o_pool.argtypes = [vp, vp, i64, ctypes.c_int, ctypes.c_int, vp]
         lib.o_pool.restype = None
@@ -69,6 +69,16 @@ def _load():
         lib.o_pool_topk.restype = ctypes.c_int
         lib.o_attention.argtypes = [vp, vp, vp, ctypes.c_int, vp, ctypes.c_int, vp, f64, vp, vp]
         lib.o_attention.restype = None
+        lib.o_attention_ex.argtypes = [vp, vp, vp, ctypes.c_int, vp, ctypes.c_int, vp, f64, vp, f64,
+                                       ctypes.c_int, f64, f64, vp, vp, vp]
+        lib.o_attention_ex.restype = None
+        lib.o_attention_rows.argtypes = [vp, ctypes.c_int, vp, f64, vp, f64, ctypes.c_int, f64, f64,
+                                         vp, vp, vp]
+        lib.o_attention_rows.restype = None
+        lib.o_rmsnorm.argtypes = [vp, ctypes.c_int, vp, f64, vp]
+        lib.o_rmsnorm.restype = None
+        lib.o_rope.argtypes = [vp, f64, f64]
+        lib.o_rope.restype = None
         lib.o_e2m1_encode_array.argtypes = [vp, i64, vp]
         lib.o_e2m1_encode_array.restype = None
         lib.o_e4m3_encode_array.argtypes = [vp, i64, vp]
@@ -180,11 +190,16 @@ def index_group_margins(x: np.ndarray) -> np.ndarray:
 # ----------------------------------------------------------------------------- cache write
 
 def cache_write(H: np.ndarray, Wkv: np.ndarray, Wz: np.ndarray, Wik: np.ndarray, m: int,
-                return_prequant: bool = False):
+                return_prequant: bool = False, norm_weight=None, eps: float = 1e-6,
+                rope: bool = False, rope_base: float = 10000.0, pos_first: float = 0.0,
+                pos_step: float | None = None):
     """H bf16 bits [T,d]; W_KV, W_Z bf16 bits [d,512]; W_IK bf16 bits [512,128].
 
     Returns (kv_codes, kv_scales, ix_codes, ix_scales) for T/m entries and, if
-    asked, the fp64 pooled latents Cbar [T/m,512] and indexer keys K^I [T/m,128].
+    asked, the fp64 pooled latents Cbar [T/m,512] and indexer keys K^I [T/m,128],
+    and the values the main quantizer saw [T/m,512].  norm_weight (fp32 [512] or
+    None) and rope: RMSNorm / RoPE of the main-KV copy, entry j at position
+    pos_first + j * pos_step (pos_step defaults to m).
     """
     H = np.ascontiguousarray(H, np.uint16)
     T, d = H.shape
@@ -195,14 +210,18 @@ def cache_write(H: np.ndarray, Wkv: np.ndarray, Wz: np.ndarray, Wik: np.ndarray,
     ixs = np.zeros((n, 4), np.uint8)
     cb = np.zeros((n, D_MAIN), np.float64) if return_prequant else None
     ki = np.zeros((n, D_IDX), np.float64) if return_prequant else None
+    att = np.zeros((n, D_MAIN), np.float64) if return_prequant else None
+    nw = None if norm_weight is None else np.ascontiguousarray(norm_weight, np.float32)
     rc = _load().o_cache_write(_p(H), T, d, _p(np.ascontiguousarray(Wkv, np.uint16)),
                                _p(np.ascontiguousarray(Wz, np.uint16)),
                                _p(np.ascontiguousarray(Wik, np.uint16)), m, _p(kvc), _p(kvs),
-                               _p(ixc), _p(ixs), _p(cb), _p(ki), _threads())
+                               _p(ixc), _p(ixs), _p(cb), _p(ki), _threads(), _p(nw), float(eps),
+                               int(bool(rope)), float(rope_base), float(pos_first),
+                               float(m if pos_step is None else pos_step), _p(att))
     if rc != 0:
         raise ValueError("oracle cache_write: bad arguments")
     if return_prequant:
-        return kvc, kvs, ixc, ixs, cb, ki
+        return kvc, kvs, ixc, ixs, cb, ki, att
     return kvc, kvs, ixc, ixs
 
 
@@ -275,15 +294,61 @@ def pool_topk(scores: np.ndarray, pool_blocks: np.ndarray, blk: int, k: int,
 
 # ----------------------------------------------------------------------------- attention
 
-def attention(kv_codes, kv_scales, topk_idx, swa, q_bits, scale):
-    """One query: returns (out fp64 [64,512], lse fp64 [64])."""
+def attention(kv_codes, kv_scales, topk_idx, swa, q_bits, scale, q_norm_weight=None,
+              eps: float = 1e-6, qpos=None, rope_base: float = 10000.0, sink=None):
+    """One query: returns (out fp64 [64,512], lse fp64 [64]).
+
+    q_norm_weight (fp32 [512]): RMSNorm of each query head; qpos: RoPE of the
+    query at qpos and of the output at -qpos; sink (fp32 [64]): per-head sink
+    logits in the softmax denominator.  Each is off when None.
+    """
     topk_idx = np.ascontiguousarray(topk_idx, np.int32)
     swa = np.ascontiguousarray(swa, np.uint8).reshape(-1, D_MAIN)
     out = np.empty((H_ATT, D_MAIN), np.float64)
     lse = np.empty(H_ATT, np.float64)
-    _load().o_attention(_p(np.ascontiguousarray(kv_codes, np.uint8)),
-                        _p(np.ascontiguousarray(kv_scales, np.uint8)), _p(topk_idx),
-                        topk_idx.shape[0], _p(swa) if swa.size else None, swa.shape[0],
-                        _p(np.ascontiguousarray(q_bits, np.uint16)), float(scale), _p(out),
-                        _p(lse))
+    nw = None if q_norm_weight is None else np.ascontiguousarray(q_norm_weight, np.float32)
+    sk = None if sink is None else np.ascontiguousarray(sink, np.float32)
+    _load().o_attention_ex(_p(np.ascontiguousarray(kv_codes, np.uint8)),
+                           _p(np.ascontiguousarray(kv_scales, np.uint8)), _p(topk_idx),
+                           topk_idx.shape[0], _p(swa) if swa.size else None, swa.shape[0],
+                           _p(np.ascontiguousarray(q_bits, np.uint16)), float(scale), _p(nw),
+                           float(eps), int(qpos is not None), float(rope_base),
+                           float(0.0 if qpos is None else qpos), _p(sk), _p(out), _p(lse))
     return out, lse
+
+
+def attention_rows(X, q_bits, scale, q_norm_weight=None, eps: float = 1e-6, qpos=None,
+                   rope_base: float = 10000.0, sink=None):
+    """attention() over given fp64 rows X [rows,512] instead of cache entries."""
+    X = np.ascontiguousarray(X, np.float64).reshape(-1, D_MAIN)
+    out = np.empty((H_ATT, D_MAIN), np.float64)
+    lse = np.empty(H_ATT, np.float64)
+    nw = None if q_norm_weight is None else np.ascontiguousarray(q_norm_weight, np.float32)
+    sk = None if sink is None else np.ascontiguousarray(sink, np.float32)
+    _load().o_attention_rows(_p(X) if X.size else None, X.shape[0],
+                             _p(np.ascontiguousarray(q_bits, np.uint16)), float(scale), _p(nw),
+                             float(eps), int(qpos is not None), float(rope_base),
+                             float(0.0 if qpos is None else qpos), _p(sk), _p(out), _p(lse))
+    return out, lse
+
+
+def rmsnorm(x, weight=None, eps: float = 1e-6) -> np.ndarray:
+    """RMSNorm of each row of x (fp64) over its channels."""
+    x = np.ascontiguousarray(x, np.float64)
+    rows = x.reshape(-1, x.shape[-1])
+    out = np.empty_like(rows)
+    w = None if weight is None else np.ascontiguousarray(weight, np.float32)
+    for i in range(rows.shape[0]):
+        _load().o_rmsnorm(_p(np.ascontiguousarray(rows[i])), rows.shape[1], _p(w), float(eps),
+                          _p(out[i:i + 1]))
+    return out.reshape(x.shape)
+
+
+def rope(x, pos: float, base: float = 10000.0) -> np.ndarray:
+    """RoPE of the last 64 channels of each 512-channel row of x at position pos."""
+    out = np.array(x, np.float64, copy=True).reshape(-1, D_MAIN)
+    for i in range(out.shape[0]):
+        row = np.ascontiguousarray(out[i])
+        _load().o_rope(_p(row), float(pos), float(base))
+        out[i] = row
+    return out.reshape(np.shape(x))

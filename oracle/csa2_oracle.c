@@ -264,6 +264,36 @@ double o_index_group_margin(const double* x) {
 }
 
 /* ========================================================================== */
+/* Q/KV RMSNorm and partial RoPE ([V4] CSA, "other details": RMSNorm of every  */
+/* query head and of each compressed entry before the core attention; RoPE on */
+/* the last 64 channels of query, KV and output)                              */
+/* ========================================================================== */
+
+#define ROPE_DIMS 64
+#define ROPE_FIRST (D_MAIN - ROPE_DIMS)
+
+/* y = w * x / sqrt(mean(x^2) + eps) over n channels (w = NULL: all ones) */
+void o_rmsnorm(const double* x, int n, const float* w, double eps, double* y) {
+  double ss = 0.0;
+  for (int c = 0; c < n; ++c) ss += x[c] * x[c];
+  const double inv = 1.0 / sqrt(ss / n + eps);
+  for (int c = 0; c < n; ++c) y[c] = (w ? (double)w[c] : 1.0) * x[c] * inv;
+}
+
+/* Rotates the last 64 channels of a 512-vector in place by position pos: pair
+ * i, channels (448 + 2i, 449 + 2i), turns by the angle pos * base^(-2i/64). */
+void o_rope(double* x, double pos, double base) {
+  for (int i = 0; i < ROPE_DIMS / 2; ++i) {
+    const double theta = pos * pow(base, -2.0 * i / ROPE_DIMS);
+    const double c = cos(theta), s = sin(theta);
+    double* v = x + ROPE_FIRST + 2 * i;
+    const double a = v[0], b = v[1];
+    v[0] = a * c - b * s;
+    v[1] = a * s + b * c;
+  }
+}
+
+/* ========================================================================== */
 /* Compressor / cache write ([CRS] Eq. (1) and 2.3; [V41] 4.1)                */
 /* ========================================================================== */
 
@@ -282,7 +312,11 @@ typedef struct {
   int64_t T;
   int d, m;
   uint8_t *kvc, *kvs, *ixc, *ixs;
-  double *cbar_out, *ki_out;
+  double *cbar_out, *ki_out, *att_out;
+  const float* norm_w; /* RMSNorm weight of the attention copy, or NULL: no RMSNorm */
+  double eps;
+  int rope;
+  double rope_base, pos_first, pos_step;
   int64_t j_lo, j_hi;
 } cw_job;
 
@@ -292,7 +326,7 @@ static void cache_write_range(const cw_job* jb) {
   double* Z = (double*)malloc(sizeof(double) * (size_t)m * D_MAIN);
   double* Wkv = (double*)malloc(sizeof(double) * (size_t)d * D_MAIN);
   double* Wz = (double*)malloc(sizeof(double) * (size_t)d * D_MAIN);
-  double cbar[D_MAIN], ki[D_IDX];
+  double cbar[D_MAIN], ki[D_IDX], att[D_MAIN];
   float cbar32[D_MAIN], ki32[D_IDX];
   for (int64_t i = 0; i < (int64_t)d * D_MAIN; ++i) {
     Wkv[i] = bf16_value(jb->Wkv[i]);
@@ -332,12 +366,21 @@ static void cache_write_range(const cw_job* jb) {
       for (int c = 0; c < D_MAIN; ++c) s += cbar[c] * bf16_value(jb->Wik[(size_t)c * D_IDX + o]);
       ki[o] = s;
     }
-    for (int c = 0; c < D_MAIN; ++c) cbar32[c] = (float)cbar[c];
+    /* the attention copy: RMSNorm, then RoPE at the entry's position, then the
+     * FP4 quantization ([V41] 2.4.4: the cache is quantized after RoPE); the
+     * indexer key keeps the pooled latent */
+    if (jb->norm_w)
+      o_rmsnorm(cbar, D_MAIN, jb->norm_w, jb->eps, att);
+    else
+      memcpy(att, cbar, sizeof(att));
+    if (jb->rope) o_rope(att, jb->pos_first + (double)j * jb->pos_step, jb->rope_base);
+    for (int c = 0; c < D_MAIN; ++c) cbar32[c] = (float)att[c];
     for (int o = 0; o < D_IDX; ++o) ki32[o] = (float)ki[o];
     o_quantize_main(cbar32, 1, jb->kvc + j * 256, jb->kvs + j * 32);
     o_quantize_index(ki32, 1, jb->ixc + j * 64, jb->ixs + j * 4);
     if (jb->cbar_out) memcpy(jb->cbar_out + j * D_MAIN, cbar, sizeof(cbar));
     if (jb->ki_out) memcpy(jb->ki_out + j * D_IDX, ki, sizeof(ki));
+    if (jb->att_out) memcpy(jb->att_out + j * D_MAIN, att, sizeof(att));
   }
   free(C);
   free(Z);
@@ -350,11 +393,15 @@ static void* cache_write_worker(void* p) {
   return NULL;
 }
 
-/* Writes entries 0 .. T/m - 1 into the four planes (T must be a multiple of m). */
+/* Writes entries 0 .. T/m - 1 into the four planes (T must be a multiple of m).
+ * norm_w (or NULL), eps, rope, rope_base: RMSNorm and RoPE of the main-KV copy;
+ * entry j sits at position pos_first + j * pos_step.  att_out (or NULL) gets
+ * the values the main quantizer saw. */
 int o_cache_write(const uint16_t* H, int64_t T, int d, const uint16_t* Wkv, const uint16_t* Wz,
                   const uint16_t* Wik, int m, uint8_t* kv_codes, uint8_t* kv_scales,
                   uint8_t* ix_codes, uint8_t* ix_scales, double* cbar_out, double* ki_out,
-                  int nthreads) {
+                  int nthreads, const float* norm_w, double eps, int rope, double rope_base,
+                  double pos_first, double pos_step, double* att_out) {
   if (m < 1 || T % m != 0 || d < 1) return 1;
   int64_t n = T / m;
   if (nthreads < 1) nthreads = 1;
@@ -364,8 +411,10 @@ int o_cache_write(const uint16_t* H, int64_t T, int d, const uint16_t* Wkv, cons
   cw_job jobs[128];
   int64_t per = (n + nthreads - 1) / nthreads;
   for (int t = 0; t < nthreads; ++t) {
-    cw_job jb = {H, Wkv, Wz, Wik, T, d, m, kv_codes, kv_scales, ix_codes, ix_scales, cbar_out,
-                 ki_out, (int64_t)t * per, (int64_t)(t + 1) * per};
+    cw_job jb = {H,        Wkv,   Wz,       Wik,        T,         d,         m,
+                 kv_codes, kv_scales, ix_codes, ix_scales, cbar_out, ki_out, att_out,
+                 norm_w,   eps,   rope,     rope_base,  pos_first, pos_step,
+                 (int64_t)t * per, (int64_t)(t + 1) * per};
     if (jb.j_hi > n) jb.j_hi = n;
     jobs[t] = jb;
   }
@@ -566,10 +615,54 @@ int o_pool_topk(const double* scores, int64_t n, const int32_t* pool, int keep, 
 
 /* kv planes of one sequence; topk [k] (entries < 0 are skipped);
  * swa [n_swa,512] E4M3 bytes; q [64,512] bf16; out [64,512]; lse [64] (natural
- * log of the softmax denominator of the scaled logits, incl. the max). */
-void o_attention(const uint8_t* kv_codes, const uint8_t* kv_scales, const int32_t* topk, int k,
-                 const uint8_t* swa, int n_swa, const uint16_t* q_bf16, double scale,
-                 double* out, double* lse) {
+ * log of the softmax denominator of the scaled logits, incl. the max).
+ * Extras ([V4] CSA, "other details"), each off when NULL / 0:
+ *   q_norm_w [512]: RMSNorm of every query head (eps) before the logits;
+ *   rope: RoPE of the query's last 64 channels at position qpos (base), and of
+ *     the output at position -qpos (the cached entries carry their own);
+ *   sink [64]: per-head logit z'_h whose exp joins the softmax denominator
+ *     (and lse).
+ * o_attention_rows takes the rows X [rows,512] (fp64) directly. */
+void o_attention_rows(const double* X, int rows, const uint16_t* q_bf16, double scale,
+                      const float* q_norm_w, double eps, int rope, double rope_base, double qpos,
+                      const float* sink, double* out, double* lse) {
+  double* logit = (double*)malloc(sizeof(double) * (size_t)(rows > 0 ? rows : 1));
+  for (int h = 0; h < H_ATT; ++h) {
+    double q[D_MAIN];
+    for (int c = 0; c < D_MAIN; ++c) q[c] = bf16_value(q_bf16[h * D_MAIN + c]);
+    if (q_norm_w) o_rmsnorm(q, D_MAIN, q_norm_w, eps, q);
+    if (rope) o_rope(q, qpos, rope_base);
+    double mx = -INFINITY;
+    for (int s = 0; s < rows; ++s) {
+      double dot = 0.0;
+      for (int c = 0; c < D_MAIN; ++c) dot += q[c] * X[(size_t)s * D_MAIN + c];
+      logit[s] = scale * dot;
+      if (logit[s] > mx) mx = logit[s];
+    }
+    /* the sink joins the denominator: sum_s exp(l_s) + exp(z'_h), kept relative
+     * to the larger of the logits' maximum and z'_h */
+    const double z = sink ? (double)sink[h] : -INFINITY;
+    const double ref = (rows > 0 && mx > z) ? mx : z;
+    double den = 0.0;
+    for (int s = 0; s < rows; ++s) den += exp(logit[s] - ref);
+    if (sink) den += exp(z - ref);
+    for (int c = 0; c < D_MAIN; ++c) out[h * D_MAIN + c] = 0.0;
+    for (int s = 0; s < rows; ++s) {
+      double p = exp(logit[s] - ref) / den;
+      for (int c = 0; c < D_MAIN; ++c) out[h * D_MAIN + c] += p * X[(size_t)s * D_MAIN + c];
+    }
+    if (rope) o_rope(out + h * D_MAIN, -qpos, rope_base);
+    if (lse) lse[h] = (rows > 0 || sink) ? ref + log(den) : -INFINITY;
+  }
+  free(logit);
+}
+
+/* The same over dequantized cache rows: the selected main entries, then the
+ * window rows. */
+void o_attention_ex(const uint8_t* kv_codes, const uint8_t* kv_scales, const int32_t* topk, int k,
+                    const uint8_t* swa, int n_swa, const uint16_t* q_bf16, double scale,
+                    const float* q_norm_w, double eps, int rope, double rope_base, double qpos,
+                    const float* sink, double* out, double* lse) {
   int rows = 0;
   for (int i = 0; i < k; ++i)
     if (topk[i] >= 0) ++rows;
@@ -584,28 +677,15 @@ void o_attention(const uint8_t* kv_codes, const uint8_t* kv_scales, const int32_
   }
   for (int i = 0; i < n_swa; ++i, ++r)
     for (int c = 0; c < D_MAIN; ++c) X[(size_t)r * D_MAIN + c] = o_e4m3_value(swa[i * D_MAIN + c]);
-  double* logit = (double*)malloc(sizeof(double) * (size_t)(rows > 0 ? rows : 1));
-  for (int h = 0; h < H_ATT; ++h) {
-    double q[D_MAIN];
-    for (int c = 0; c < D_MAIN; ++c) q[c] = bf16_value(q_bf16[h * D_MAIN + c]);
-    double mx = -INFINITY;
-    for (int s = 0; s < rows; ++s) {
-      double dot = 0.0;
-      for (int c = 0; c < D_MAIN; ++c) dot += q[c] * X[(size_t)s * D_MAIN + c];
-      logit[s] = scale * dot;
-      if (logit[s] > mx) mx = logit[s];
-    }
-    double den = 0.0;
-    for (int s = 0; s < rows; ++s) den += exp(logit[s] - mx);
-    for (int c = 0; c < D_MAIN; ++c) out[h * D_MAIN + c] = 0.0;
-    for (int s = 0; s < rows; ++s) {
-      double p = exp(logit[s] - mx) / den;
-      for (int c = 0; c < D_MAIN; ++c) out[h * D_MAIN + c] += p * X[(size_t)s * D_MAIN + c];
-    }
-    if (lse) lse[h] = rows > 0 ? mx + log(den) : -INFINITY;
-  }
+  o_attention_rows(X, rows, q_bf16, scale, q_norm_w, eps, rope, rope_base, qpos, sink, out, lse);
   free(X);
-  free(logit);
+}
+
+void o_attention(const uint8_t* kv_codes, const uint8_t* kv_scales, const int32_t* topk, int k,
+                 const uint8_t* swa, int n_swa, const uint16_t* q_bf16, double scale,
+                 double* out, double* lse) {
+  o_attention_ex(kv_codes, kv_scales, topk, k, swa, n_swa, q_bf16, scale, NULL, 0.0, 0, 0.0, 0.0,
+                 NULL, out, lse);
 }
 
 /* ========================================================================== */

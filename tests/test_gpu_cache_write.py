@@ -147,7 +147,7 @@ def _group_bytes_ok(got_codes, got_scales, ref_codes, ref_scales, decided, group
 def test_gaussian_banded(oracle_mod, T, d, m):
     H, Wkv, Wz, Wik = W.cache_write_inputs(3, T, d)
     got = _gpu_write(H, Wkv, Wz, Wik, m)
-    kvc, kvs, ixc, ixs, cb, ki = oracle_mod.cache_write(H, Wkv, Wz, Wik, m, return_prequant=True)
+    kvc, kvs, ixc, ixs, cb, ki, _ = oracle_mod.cache_write(H, Wkv, Wz, Wik, m, return_prequant=True)
     eCb, eKI = _error_bounds(H, Wkv, Wz, Wik, m, cb)
     e4m3_mids = np.array([0.5 * (oracle_mod.e4m3_value(c) + oracle_mod.e4m3_value(c + 1)) for c in range(126)])
     # the oracle quantizes fp32(Cbar) and fp32(K^I): decisions are taken on those values

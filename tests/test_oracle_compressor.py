@@ -84,7 +84,7 @@ def test_cache_write_m2_matches_numpy_pipeline(oracle_mod):
     s0 = 1.0 / (1.0 + np.exp(Z[1::2] - Z[0::2]))
     Cb = s0 * C[0::2] + (1 - s0) * C[1::2]
     KI = Cb @ Wikf
-    _, _, _, _, cb, ki = oracle_mod.cache_write(H, Wkv, Wz, Wik, 2, return_prequant=True)
+    _, _, _, _, cb, ki, _ = oracle_mod.cache_write(H, Wkv, Wz, Wik, 2, return_prequant=True)
     assert np.allclose(cb, Cb, rtol=1e-12, atol=1e-12)
     assert np.allclose(ki, KI, rtol=1e-11, atol=1e-12)
 
