@@ -64,7 +64,8 @@ def test_cache_write_dyadic_exact(oracle_mod):
     KI = (H @ Wkv @ Wik) / 256.0
     out = oracle_mod.cache_write(_bf16_bits(H), _bf16_bits(Wkv / 16.0), _bf16_bits(Wz / 16.0),
                                  _bf16_bits(Wik / 16.0), 1, return_prequant=True)
-    kvc, kvs, ixc, ixs, cb, ki = out
+    kvc, kvs, ixc, ixs, cb, ki, att = out
+    assert np.array_equal(att, cb)  # no RMSNorm / RoPE: the main quantizer sees the pooled latent
     assert np.array_equal(cb, C)
     assert np.array_equal(ki, KI)
     c2, s2 = oracle_mod.quantize_main(C.astype(np.float32))
