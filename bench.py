@@ -359,6 +359,26 @@ def run_attention(dev, st, steps: int, warmup: int):
     csa2.timing_enable(False)
     n_k, t_k = kt["k_attn"]
     k_ms = t_k / n_k
+    # the same call with the in-layer extras on: query RMSNorm + RoPE (output turned
+    # back) at positions near 10^6, a sink logit per head
+    w = torch.ones(512, dtype=torch.float32, device=dev)
+    pos = torch.arange(1_000_000, 1_000_000 + B, dtype=torch.int64, device=dev)
+    sink = torch.zeros(64, dtype=torch.float32, device=dev)
+    nr = csa2.norm_rope(w, 1e-6, True, 10000.0)
+
+    def call_ex():
+        csa2.sparse_attn_decode(planes, B, topk, K_TOP, swa, NSWA, q, scale, out, ws, lse_out=lse, stream=st,
+                                q_nr=nr, q_pos=pos, sink=sink)
+
+    for _ in range(warmup):
+        call_ex()
+    a.record(st)
+    for _ in range(steps):
+        call_ex()
+    b.record(st)
+    torch.cuda.synchronize()
+    assert csa2.check(ws, st)[0] == 0
+    ms_ex = a.elapsed_time(b) / steps
     # algorithmic bytes: selected entries, window rows, q in, output out; flops: S and O
     rows = K_TOP + NSWA
     call_bytes = B * (K_TOP * MAIN_BYTES + NSWA * SWA_ROW + 64 * 512 * 2 + 64 * 512 * 4)
@@ -367,6 +387,7 @@ def run_attention(dev, st, steps: int, warmup: int):
     tp, tkind = tensor_peak()
     return {
         "workload": AT_WORKLOAD, "calls": steps, "ms_per_call": round(ms, 4),
+        "ms_per_call_with_norm_rope_sink": round(ms_ex, 4),
         "kernels_ms_per_launch": {k: round(tm / n, 4) for k, (n, tm) in sorted(kt.items())},
         "k_attn": {"algorithmic_bytes": call_bytes, "hbm_gbs": round(call_bytes / (k_ms * 1e-3) / 1e9, 1),
                    "hbm_frac": round(call_bytes / (k_ms * 1e-3) / 1e9 / hbm, 4), "hbm_peak_kind": kind,

@@ -40,6 +40,20 @@ class KVPlanes(ctypes.Structure):
                 ("seq_stride", ctypes.c_int64)]
 
 
+class NormRope(ctypes.Structure):
+    """csa2_norm_rope: RMSNorm weight (device fp32 [512] or None), eps, RoPE on/off, base."""
+    _fields_ = [("norm_weight", ctypes.c_void_p), ("norm_eps", ctypes.c_float),
+                ("rope", ctypes.c_int32), ("rope_base", ctypes.c_float)]
+
+
+def norm_rope(norm_weight=None, eps: float = 1e-6, rope: bool = False, rope_base: float = 10000.0):
+    """A csa2_norm_rope for the cache write (main-KV copy) or the attention (query heads).
+    The struct keeps a reference to norm_weight, so the device array lives as long as it."""
+    nr = NormRope(_ptr(norm_weight), float(eps), int(bool(rope)), float(rope_base))
+    nr._weight = norm_weight
+    return nr
+
+
 class KernelTime(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char_p), ("launches", ctypes.c_int64), ("total_ms", ctypes.c_double)]
 
@@ -58,9 +72,10 @@ def lib() -> ctypes.CDLL:
         vp, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
                                  ctypes.c_size_t)
         pl = ctypes.POINTER(KVPlanes)
+        nr = ctypes.POINTER(NormRope)
         sig = {
             "csa2_quantize_entries": ([vp, vp, i64, pl, i64, vp], ctypes.c_int),
-            "csa2_cache_write": ([vp, i64, i32, vp, vp, vp, i32, pl, i32, i64, vp, sz, vp],
+            "csa2_cache_write": ([vp, i64, i32, vp, vp, vp, i32, pl, i32, i64, nr, i64, vp, sz, vp],
                                  ctypes.c_int),
             "csa2_cache_write_workspace_size": ([i64, i32, i32], sz),
             "csa2_index_topk": ([pl, i32, vp, i64, vp, vp, i32, ctypes.c_int, i32, i32, vp, vp, vp,
@@ -68,8 +83,8 @@ def lib() -> ctypes.CDLL:
             "csa2_index_topk_workspace_size": ([i32, i64, i32, i32, i32], sz),
             "csa2_index_topk_noalloc": ([pl, i32, vp, i64, vp, vp, i32, ctypes.c_int, i32, i32, vp,
                                          vp, vp, vp], ctypes.c_int),
-            "csa2_sparse_attn_decode": ([pl, i32, vp, i32, vp, i32, vp, f32, vp, vp, vp, sz, vp],
-                                        ctypes.c_int),
+            "csa2_sparse_attn_decode": ([pl, i32, vp, i32, vp, i32, vp, f32, nr, vp, vp, vp, vp, vp, sz,
+                                         vp], ctypes.c_int),
             "csa2_sparse_attn_workspace_size": ([i32, i32, i32], sz),
             "csa2_v41_layer_table": ([i32, vp, vp, vp, vp, vp], ctypes.c_int),
             "csa2_check": ([vp, vp, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
@@ -165,10 +180,14 @@ def cache_write_workspace_size(T: int, d_model: int, m: int) -> int:
 
 
 def cache_write(H, T: int, d_model: int, Wkv, Wz, Wik, m: int, planes: Planes, seq: int,
-                entry_offset: int, ws, stream=None) -> None:
+                entry_offset: int, ws, stream=None, kv_nr: NormRope | None = None,
+                pos_first: int = 0) -> None:
+    """kv_nr (norm_rope(...)): RMSNorm / RoPE of the main-KV copy; entry j of the call at
+    position pos_first + j * m."""
     _ok(lib().csa2_cache_write(_ptr(H), T, d_model, _ptr(Wkv), _ptr(Wz), _ptr(Wik), m,
-                               ctypes.byref(planes.c), seq, entry_offset, _ptr(ws), _nbytes(ws),
-                               _stream(stream)), "csa2_cache_write")
+                               ctypes.byref(planes.c), seq, entry_offset,
+                               ctypes.byref(kv_nr) if kv_nr is not None else None, int(pos_first),
+                               _ptr(ws), _nbytes(ws), _stream(stream)), "csa2_cache_write")
 
 
 def index_topk_workspace_size(B: int, n_max: int, k: int, block: int = 8,
@@ -204,10 +223,15 @@ def sparse_attn_workspace_size(B: int, k: int, n_swa: int) -> int:
 
 
 def sparse_attn_decode(planes: Planes, B: int, topk, k: int, swa, n_swa: int, q,
-                       softmax_scale: float, out, ws, lse_out=None, stream=None) -> None:
+                       softmax_scale: float, out, ws, lse_out=None, stream=None,
+                       q_nr: NormRope | None = None, q_pos=None, sink=None) -> None:
+    """q_nr (norm_rope(...)): RMSNorm / RoPE of the query heads, q_pos int64 [B] (needed with
+    RoPE; the output turns back by -q_pos); sink fp32 [64] per-head sink logits."""
     _ok(lib().csa2_sparse_attn_decode(ctypes.byref(planes.c), B, _ptr(topk), k, _ptr(swa), n_swa,
-                                      _ptr(q), softmax_scale, _ptr(out), _ptr(lse_out), _ptr(ws),
-                                      _nbytes(ws), _stream(stream)), "csa2_sparse_attn_decode")
+                                      _ptr(q), softmax_scale,
+                                      ctypes.byref(q_nr) if q_nr is not None else None, _ptr(q_pos),
+                                      _ptr(sink), _ptr(out), _ptr(lse_out), _ptr(ws), _nbytes(ws),
+                                      _stream(stream)), "csa2_sparse_attn_decode")
 
 
 def check(ws, stream=None) -> tuple[int, int]:

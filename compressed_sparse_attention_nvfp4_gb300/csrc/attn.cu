@@ -39,6 +39,18 @@ constexpr int kQPlane = kHAtt * 8 + 8;  // in f16 elements (1040 bytes)
 constexpr uint32_t kAttnTmemCols = 512;  // O^T 256 columns, S^T 64
 constexpr long long kAttnWaitBudget = 1LL << 32;
 
+// In-layer extras ("DeepSeek-V4: ...", CSA, other details), each off when null /
+// zero: RMSNorm weight of the query heads, RoPE of the query at qpos[b] with the
+// output turned back by -qpos[b], per-head sink logits.
+struct AttnExtras {
+  const float* qnorm_w;
+  float eps;
+  int rope;
+  const int64_t* qpos;
+  const float* sink;
+  RopeTheta th;
+};
+
 struct __align__(1024) AttnSmem {
   uint16_t X[kDMain / 8][kRows * 8];  // f16 rows [c/8][row][c%8]; planes 0-31 / 32-63 = channel halves
   uint16_t q[kDMain / 8][kQPlane];    // f16 q' [c/8][head][c%8], planes padded
@@ -105,9 +117,10 @@ __device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane,
 
 // q' = q_h 2^-s_h in f16 with 2^s_h bringing the head's largest |q| to
 // [2^14, 2^15), clamped so that both 2^s_h and 2^-s_h are normal fp32 values;
-// bf16 q keeps q' exact and inside the f16 range.  Warp w converts heads
-// 8w..8w+7: lane l holds channels 8l..8l+7 and 256+8l..256+8l+7 of each, i.e.
-// chunks l and 32+l of the [c/8][head][c%8] image.
+// bf16 q keeps q' exact and inside the f16 range (with RMSNorm or RoPE the
+// fp32 result is rounded to f16 once).  Warp w converts heads 8w..8w+7: lane l
+// holds channels 8l..8l+7 and 256+8l..256+8l+7 of each, i.e. chunks l and 32+l
+// of the [c/8][head][c%8] image; the rotated pairs sit in lanes 24-31.
 struct QFetch {
   uint4 raw[8][2];
 };
@@ -119,17 +132,56 @@ __device__ __forceinline__ void fetch_q(QFetch& f, const uint16_t* __restrict__ 
     f.raw[u][1] = src[32 + lane];
   }
 }
-__device__ __forceinline__ void stage_q(AttnSmem& S, const QFetch& f, float scale, int warp, int lane) {
+template <bool kEx>
+__device__ __forceinline__ void stage_q(AttnSmem& S, const QFetch& f, float scale, int warp, int lane,
+                                        const AttnExtras& ex, int b) {
+  // per lane: the RMSNorm weights of its 16 channels, the cos / sin of its 4 pairs
+  float wq[16], rc[4], rs[4];
+  const bool norm = kEx && ex.qnorm_w != nullptr;
+  if (norm) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float4* wv = reinterpret_cast<const float4*>(ex.qnorm_w + i * 256 + lane * 8);
+      const float4 a = wv[0], c = wv[1];
+      wq[8 * i] = a.x, wq[8 * i + 1] = a.y, wq[8 * i + 2] = a.z, wq[8 * i + 3] = a.w;
+      wq[8 * i + 4] = c.x, wq[8 * i + 5] = c.y, wq[8 * i + 6] = c.z, wq[8 * i + 7] = c.w;
+    }
+  }
+  const bool rot = kEx && ex.rope && 256 + lane * 8 >= kRopeFirst;
+  if (rot) {
+    const double pos = (double)ex.qpos[b];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) rope_cos_sin(ex.th.t[(256 + lane * 8 - kRopeFirst) / 2 + p], pos, rc[p], rs[p]);
+  }
 #pragma unroll
   for (int u = 0; u < 8; ++u) {
-    float mx = 0.0f;
+    float v[16];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const uint32_t w4[4] = {f.raw[u][i].x, f.raw[u][i].y, f.raw[u][i].z, f.raw[u][i].w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w4[j] << 16)), fabsf(__uint_as_float(w4[j] & 0xFFFF0000u))));
+      for (int j = 0; j < 4; ++j) {
+        v[8 * i + 2 * j] = __uint_as_float(w4[j] << 16);
+        v[8 * i + 2 * j + 1] = __uint_as_float(w4[j] & 0xFFFF0000u);
+      }
     }
+    if (norm) {
+      float ss = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) ss = fmaf(v[i], v[i], ss);
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float r = 1.0f / sqrtf(ss / (float)kDMain + ex.eps);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = wq[i] * (v[i] * r);
+    }
+    if (rot) {
+#pragma unroll
+      for (int p = 0; p < 4; ++p) rope_pair(v[8 + 2 * p], v[9 + 2 * p], rc[p], rs[p]);
+    }
+    float mx = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) mx = fmaxf(mx, fabsf(v[i]));
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     const int sig = mx > 0.0f ? min(max(floor_log2_f32(mx) - 14, -126), 126) : 0;
@@ -137,12 +189,10 @@ __device__ __forceinline__ void stage_q(AttnSmem& S, const QFetch& f, float scal
     const int h = warp * 8 + u;
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      const uint32_t w4[4] = {f.raw[u][i].x, f.raw[u][i].y, f.raw[u][i].z, f.raw[u][i].w};
       uint32_t o[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const __half2 h2 = __floats2half2_rn(__uint_as_float(w4[j] << 16) * inv,
-                                             __uint_as_float(w4[j] & 0xFFFF0000u) * inv);
+        const __half2 h2 = __floats2half2_rn(v[8 * i + 2 * j] * inv, v[8 * i + 2 * j + 1] * inv);
         o[j] = *reinterpret_cast<const uint32_t*>(&h2);
       }
       *reinterpret_cast<uint4*>(&S.q[i * 32 + lane][h * 8]) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -253,11 +303,11 @@ __device__ __forceinline__ bool dequant_half_row(AttnSmem& S, const RowFetch& f,
 // log2 units: p = 2^(raw S * c2_h - m2_h).
 // kPartial: write the unnormalised O with (m, l) for the merge kernel instead
 // of the normalised output.
-template <bool kPartial>
+template <bool kPartial, bool kEx>
 __global__ void __launch_bounds__(kAT, 1) k_attn(
     const uint8_t* __restrict__ kv_codes, const uint8_t* __restrict__ kv_scales, int64_t seq_stride,
     const int32_t* __restrict__ topk, int k, const uint8_t* __restrict__ swa, int n_swa,
-    const uint16_t* __restrict__ qg, float scale, int nchunks, int cps,
+    const uint16_t* __restrict__ qg, float scale, AttnExtras ex, int nchunks, int cps,
     float* __restrict__ out, float* __restrict__ lse, float* __restrict__ part_o,
     float2* __restrict__ part_ml, void* ws) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -293,7 +343,7 @@ __global__ void __launch_bounds__(kAT, 1) k_attn(
     QFetch qf;
     fetch_q(qf, qg, b, warp, lane);
     const int64_t idx0 = fetch_index(topk, k, b, gr);
-    stage_q(S, qf, scale, warp, lane);
+    stage_q<kEx>(S, qf, scale, warp, lane, ex, b);
     ptx::fence_proxy_async_smem();
     issue_row(rf, idx0, kv_codes, kv_scales, seq_stride, swa, n_swa, k, b, gr, half, ws);
   }
@@ -474,29 +524,51 @@ __global__ void __launch_bounds__(kAT, 1) k_attn(
       report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 24);
     }
     // ---- epilogue: O^T rows = channels of this lane quarter, 32 heads per warp;
-    // for each head the warp stores 32 consecutive channels
+    // for each head the warp stores 32 consecutive channels.  The sink joins
+    // the denominator here (split queries: in the merge); with RoPE the last
+    // 64 channels turn back by -qpos (pairs are adjacent lanes; the turn is
+    // linear, so partials may take it before the merge).
     if (good) {
       ptx::tc_fence_after();
       const int h = hh * 32 + lane;
-      const float inv = kPartial ? 1.0f : (l_run > 0.0f ? 1.0f / l_run : 0.0f);
       const float m_nat = m2 / kLog2e;  // reference in natural units
+      float den = l_run;
+      if (!kPartial && kEx && ex.sink) den += ptx::ex2(ex.sink[h] * kLog2e - m2);  // 2^(z2 - m2); m2 = -inf -> inf
+      const float inv = kPartial ? 1.0f : (den > 0.0f ? 1.0f / den : 0.0f);
       if (q4 == 0) {
-        if (kPartial)
+        if (kPartial) {
           part_ml[((int64_t)b * gridDim.x + split) * kHAtt + h] = make_float2(m_nat, l_run);
-        else if (lse)
-          lse[b * kHAtt + h] = l_run > 0.0f ? m_nat + logf(l_run) : -INFINITY;
+        } else if (lse) {
+          if (kEx && ex.sink) {
+            const float z = ex.sink[h], mx = fmaxf(m_nat, z);
+            lse[b * kHAtt + h] = mx + logf(l_run * expf(m_nat - mx) + expf(z - mx));
+          } else {
+            lse[b * kHAtt + h] = l_run > 0.0f ? m_nat + logf(l_run) : -INFINITY;
+          }
+        }
       }
       float* ob = kPartial ? part_o + ((int64_t)b * gridDim.x + split) * kHAtt * kDMain
                            : out + (int64_t)b * kHAtt * kDMain;
+      float tc = 1.0f, ts = 0.0f;  // cos / sin of this lane's pair angle (channel c, c ^ 1)
+      if (kEx && ex.rope && 3 * kRows + rr >= kRopeFirst)
+        rope_cos_sin(ex.th.t[(3 * kRows + rr - kRopeFirst) / 2], (double)ex.qpos[b], tc, ts);
+      if (lane & 1) ts = -ts;  // turning back by -t: x' = x c + y s, y' = y c - x s
 #pragma unroll 1
       for (int mt = 0; mt < 4; ++mt) {
         uint32_t a[32];
         ptx::tmem_ld_32x32b_x32(tmem + lane_base + (uint32_t)mt * 64u + (uint32_t)hh * 32u, a);
         ptx::tmem_wait_ld();
         const int c = mt * kRows + rr;
+        const bool turn = kEx && ex.rope && mt == 3 && q4 >= 2;  // warp-uniform: channels 448..511
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          ob[(hh * 32 + j) * kDMain + c] = __uint_as_float(a[j]) * __shfl_sync(0xffffffffu, inv, j);
+        for (int j = 0; j < 32; ++j) {
+          float v = __uint_as_float(a[j]) * __shfl_sync(0xffffffffu, inv, j);
+          if (turn) {
+            const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
+            v = fmaf(v, tc, partner * ts);
+          }
+          ob[(hh * 32 + j) * kDMain + c] = v;
+        }
       }
     }
   }
@@ -510,18 +582,21 @@ __global__ void __launch_bounds__(kAT, 1) k_attn(
 
 __global__ void __launch_bounds__(128) k_attn_merge(const float* __restrict__ part_o,
                                                     const float2* __restrict__ part_ml, int nchunks,
-                                                    float* __restrict__ out, float* __restrict__ lse) {
+                                                    const float* __restrict__ sink, float* __restrict__ out,
+                                                    float* __restrict__ lse) {
   const int bh = blockIdx.x;  // b * 64 + h
   const int b = bh / kHAtt, h = bh % kHAtt;
   float M = -INFINITY;
   for (int c = 0; c < nchunks; ++c) M = fmaxf(M, part_ml[((int64_t)b * nchunks + c) * kHAtt + h].x);
-  float L = 0.0f;
+  const float z = sink ? sink[h] : -INFINITY;  // the sink joins the denominator once per query
+  const float ref = fmaxf(M, z);
+  float L = sink ? expf(z - ref) : 0.0f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int c = 0; c < nchunks; ++c) {
     const int64_t pc = ((int64_t)b * nchunks + c) * kHAtt + h;
     const float2 ml = part_ml[pc];
     if (ml.y <= 0.0f) continue;
-    const float f = expf(ml.x - M);
+    const float f = expf(ml.x - ref);
     L = fmaf(f, ml.y, L);
     const float4 v = reinterpret_cast<const float4*>(part_o + pc * kDMain)[threadIdx.x];
     acc.x = fmaf(f, v.x, acc.x);
@@ -532,7 +607,7 @@ __global__ void __launch_bounds__(128) k_attn_merge(const float* __restrict__ pa
   float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
   if (L > 0.0f) r = make_float4(acc.x / L, acc.y / L, acc.z / L, acc.w / L);
   reinterpret_cast<float4*>(out + (int64_t)bh * kDMain)[threadIdx.x] = r;
-  if (lse && threadIdx.x == 0) lse[bh] = L > 0.0f ? M + logf(L) : -INFINITY;
+  if (lse && threadIdx.x == 0) lse[bh] = L > 0.0f ? ref + logf(L) : -INFINITY;
 }
 
 struct AttnWs {
@@ -585,15 +660,25 @@ extern "C" size_t csa2_sparse_attn_workspace_size(int32_t B, int32_t k, int32_t 
 
 extern "C" csa2_status csa2_sparse_attn_decode(const csa2_kv_planes* kv, int32_t B, const int32_t* topk,
                                                int32_t k, const uint8_t* swa_e4m3, int32_t n_swa,
-                                               const void* q_bf16, float softmax_scale, float* out,
-                                               float* lse_out, void* ws, size_t ws_bytes,
-                                               csa2_stream stream) {
+                                               const void* q_bf16, float softmax_scale,
+                                               const csa2_norm_rope* q_nr, const int64_t* q_pos,
+                                               const float* sink, float* out, float* lse_out, void* ws,
+                                               size_t ws_bytes, csa2_stream stream) {
   using namespace csa2;
   cudaStream_t st = (cudaStream_t)stream;
   if (!planes_ok(kv) || B <= 0 || B > 65535 || k < 0 || k > CSA2_MAX_TOPK || n_swa < 0 || n_swa > CSA2_MAX_SWA)
     return CSA2_ERR_INVALID_ARG;
   if ((k > 0 && !topk) || (n_swa > 0 && !swa_e4m3) || !q_bf16 || !out) return CSA2_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.0f) || softmax_scale > 3.0e38f) return CSA2_ERR_INVALID_ARG;  // positive, finite
+  if (q_nr && (!norm_rope_ok(q_nr) || (q_nr->rope && !q_pos))) return CSA2_ERR_INVALID_ARG;
+  if ((q_pos && !aligned(q_pos, 8)) || (sink && !aligned(sink, 4))) return CSA2_ERR_INVALID_ARG;
+  AttnExtras ex{};
+  ex.qnorm_w = q_nr ? q_nr->norm_weight : nullptr;
+  ex.eps = q_nr ? q_nr->norm_eps : 0.0f;
+  ex.rope = q_nr ? q_nr->rope : 0;
+  ex.qpos = ex.rope ? q_pos : nullptr;
+  ex.sink = sink;
+  if (ex.rope) ex.th = make_rope_theta(q_nr->rope_base);
   if (!aligned(q_bf16, 16) || !aligned(out, 16) || (swa_e4m3 && !aligned(swa_e4m3, 16)))
     return CSA2_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, 256)) return CSA2_ERR_WORKSPACE;
@@ -603,18 +688,20 @@ extern "C" csa2_status csa2_sparse_attn_decode(const csa2_kv_planes* kv, int32_t
   if (reset_error(ws, st) != CSA2_OK) return CSA2_ERR_CUDA;
   const int smem = (int)sizeof(AttnSmem);
   const bool partial = plan.nsplit > 1;
-  auto kern = partial ? k_attn<true> : k_attn<false>;
+  const bool extras = ex.qnorm_w || ex.rope || ex.sink;
+  auto kern = partial ? (extras ? k_attn<true, true> : k_attn<true, false>)
+                      : (extras ? k_attn<false, true> : k_attn<false, false>);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return CSA2_ERR_CUDA;
   {
     KernelTimer timer(partial ? "k_attn_part" : "k_attn", st);
     kern<<<dim3(plan.nsplit, B), kAT, smem, st>>>(kv->kv_codes, kv->kv_scales, kv->seq_stride, topk, k, swa_e4m3,
-                                                   n_swa, (const uint16_t*)q_bf16, softmax_scale, plan.nchunks,
+                                                   n_swa, (const uint16_t*)q_bf16, softmax_scale, ex, plan.nchunks,
                                                    plan.cps, out, lse_out, L.part_o, L.part_ml, ws);
   }
   if (partial) {
     KernelTimer timer("k_attn_merge", st);
-    k_attn_merge<<<B * kHAtt, 128, 0, st>>>(L.part_o, L.part_ml, plan.nsplit, out, lse_out);
+    k_attn_merge<<<B * kHAtt, 128, 0, st>>>(L.part_o, L.part_ml, plan.nsplit, sink, out, lse_out);
   }
   return launch_status();
 }

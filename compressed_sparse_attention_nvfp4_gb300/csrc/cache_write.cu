@@ -542,8 +542,8 @@ extern "C" size_t csa2_cache_write_workspace_size(int64_t T, int32_t d_model, in
 extern "C" csa2_status csa2_cache_write(const void* H_bf16, int64_t T, int32_t d_model,
                                         const void* Wkv_bf16, const void* Wz_bf16, const void* Wik_bf16,
                                         int32_t m, const csa2_kv_planes* dst, int32_t seq,
-                                        int64_t entry_offset, void* ws, size_t ws_bytes,
-                                        csa2_stream stream) {
+                                        int64_t entry_offset, const csa2_norm_rope* kv_nr,
+                                        int64_t pos_first, void* ws, size_t ws_bytes, csa2_stream stream) {
   using namespace csa2;
   cudaStream_t st = (cudaStream_t)stream;
   if (!planes_ok(dst) || !H_bf16 || !Wkv_bf16 || !Wz_bf16 || !Wik_bf16 || T < 0 || seq < 0 ||
@@ -553,6 +553,7 @@ extern "C" csa2_status csa2_cache_write(const void* H_bf16, int64_t T, int32_t d
   if (d_model < kTK || d_model % 64 != 0) return CSA2_ERR_UNSUPPORTED;
   if (!aligned(H_bf16, 16) || !aligned(Wkv_bf16, 16) || !aligned(Wz_bf16, 16) || !aligned(Wik_bf16, 16))
     return CSA2_ERR_INVALID_ARG;
+  if (kv_nr && !norm_rope_ok(kv_nr)) return CSA2_ERR_INVALID_ARG;
   const int64_t n = T / m;
   if (entry_offset + n > dst->seq_stride) return CSA2_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, 256)) return CSA2_ERR_WORKSPACE;
@@ -603,6 +604,6 @@ extern "C" csa2_status csa2_cache_write(const void* H_bf16, int64_t T, int32_t d
     KernelTimer timer("k_cw_ki_tc", st);
     k_cw_ki_tc<<<(unsigned)cdiv(n, 128), kKtThreads, smem, st>>>(map_wikt, L.cbar, n, L.ki, ws);
   }
-  launch_quantize(L.cbar, L.ki, n, dst, (int64_t)seq * dst->seq_stride + entry_offset, st);
+  launch_quantize(L.cbar, L.ki, n, dst, (int64_t)seq * dst->seq_stride + entry_offset, st, kv_nr, pos_first, m);
   return launch_status();
 }

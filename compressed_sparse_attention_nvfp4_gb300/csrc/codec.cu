@@ -21,10 +21,65 @@ __global__ void k_quantize_index(const float* __restrict__ x, int64_t n, uint8_t
   quantize_index_group(x + t * 32, codes + t * 16, scales + t);
 }
 
+// The main-KV quantizer with RMSNorm and RoPE first ("DeepSeek-V4: ...", CSA,
+// other details; "DeepSeek-V4.1-Flash course, 02 Architecture", 2.4.4: the
+// cache is quantized after RoPE): one warp per entry, lane l holds channels
+// 16l .. 16l + 15 (its quantization group), the rotated pairs sit in lanes 28-31.
+__global__ void k_quantize_main_nr(const float* __restrict__ x, int64_t n, const float* __restrict__ w,
+                                   float eps, int rope, RopeTheta th, int64_t pos_first, int64_t pos_step,
+                                   uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  const int64_t e = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32;
+  const int lane = threadIdx.x % 32;
+  if (e >= n) return;  // whole warps leave together
+  float v[16];
+  const float4* src = reinterpret_cast<const float4*>(x + e * kDMain + lane * 16);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 f = src[i];
+    v[4 * i] = f.x;
+    v[4 * i + 1] = f.y;
+    v[4 * i + 2] = f.z;
+    v[4 * i + 3] = f.w;
+  }
+  if (w) {
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ss = fmaf(v[i], v[i], ss);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float inv = 1.0f / sqrtf(ss / (float)kDMain + eps);
+    const float4* wv = reinterpret_cast<const float4*>(w + lane * 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 g = wv[i];
+      v[4 * i] = g.x * (v[4 * i] * inv);
+      v[4 * i + 1] = g.y * (v[4 * i + 1] * inv);
+      v[4 * i + 2] = g.z * (v[4 * i + 2] * inv);
+      v[4 * i + 3] = g.w * (v[4 * i + 3] * inv);
+    }
+  }
+  if (rope && lane * 16 >= kRopeFirst) {
+    const double pos = (double)(pos_first + e * pos_step);
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      float c, s;
+      rope_cos_sin(th.t[(lane * 16 - kRopeFirst) / 2 + p], pos, c, s);
+      rope_pair(v[2 * p], v[2 * p + 1], c, s);
+    }
+  }
+  quantize_main_group_vals(v, codes + e * 256 + lane * 8, scales + e * 32 + lane);
+}
+
 void launch_quantize(const float* Cbar, const float* KI, int64_t n, const csa2_kv_planes* dst,
-                     int64_t e0, cudaStream_t st) {
+                     int64_t e0, cudaStream_t st, const csa2_norm_rope* nr, int64_t pos_first,
+                     int64_t pos_step) {
   if (n <= 0) return;
-  if (Cbar) {
+  if (Cbar && nr && (nr->norm_weight || nr->rope)) {
+    KernelTimer timer("k_quantize_main_nr", st);
+    k_quantize_main_nr<<<(unsigned)cdiv(n * 32, 256), 256, 0, st>>>(
+        Cbar, n, nr->norm_weight, nr->norm_eps, nr->rope, nr->rope ? make_rope_theta(nr->rope_base) : RopeTheta{},
+        pos_first, pos_step, dst->kv_codes + e0 * 256, dst->kv_scales + e0 * 32);
+  } else if (Cbar) {
     int64_t threads = n * 32;
     KernelTimer timer("k_quantize_main", st);
     k_quantize_main<<<(unsigned)cdiv(threads, 256), 256, 0, st>>>(

@@ -43,6 +43,33 @@ __device__ __forceinline__ void quantize_main_group(const float* __restrict__ x1
   quantize_main_group_vals(v, codes8, scale1);
 }
 
+// ---------------------------------------------------------------- RMSNorm / RoPE
+// Partial RoPE of a 512-channel vector: pair i (channels 448 + 2i, 449 + 2i,
+// i < 32) turns by pos * theta_i, theta_i = base^(-i/32).  The angles are
+// formed and reduced modulo 2 pi in fp64 (positions reach millions), then
+// sin / cos in fp32.
+constexpr int kRopeFirst = kDMain - 64;
+struct RopeTheta {
+  double t[32];
+};
+inline RopeTheta make_rope_theta(double base) {
+  RopeTheta r;
+  for (int i = 0; i < 32; ++i) r.t[i] = pow(base, -2.0 * i / 64.0);
+  return r;
+}
+__device__ __forceinline__ void rope_cos_sin(double theta, double pos, float& c, float& s) {
+  constexpr double kTwoPi = 6.283185307179586476925286766559;
+  const double a = pos * theta;
+  const double red = fma(-kTwoPi, rint(a / kTwoPi), a);  // in [-pi, pi]
+  sincosf((float)red, &s, &c);
+}
+// (x, y) turned counter-clockwise by the angle with cosine c, sine s
+__device__ __forceinline__ void rope_pair(float& x, float& y, float c, float s) {
+  const float nx = x * c - y * s, ny = x * s + y * c;
+  x = nx;
+  y = ny;
+}
+
 // floor(log2 a) of a finite fp32 a > 0 (normal or subnormal), exactly
 __device__ __forceinline__ int floor_log2_f32(float a) {
   uint32_t u = __float_as_uint(a);
@@ -94,6 +121,7 @@ __device__ __forceinline__ void quantize_index_group(const float* __restrict__ x
 }
 
 void launch_quantize(const float* Cbar, const float* KI, int64_t n, const csa2_kv_planes* dst,
-                     int64_t e0, cudaStream_t st);
+                     int64_t e0, cudaStream_t st, const csa2_norm_rope* nr = nullptr, int64_t pos_first = 0,
+                     int64_t pos_step = 1);
 
 }  // namespace csa2

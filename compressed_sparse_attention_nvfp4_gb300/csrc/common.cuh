@@ -106,6 +106,13 @@ inline bool planes_ok(const csa2_kv_planes* kv) {
          kv->seq_stride > 0 && aligned(kv->kv_codes, 16) && aligned(kv->kv_scales, 16) &&
          aligned(kv->ix_codes, 16) && aligned(kv->ix_scales, 16);
 }
+// RMSNorm / RoPE parameters: weight 16-byte aligned, eps >= 0, base > 1
+inline bool norm_rope_ok(const csa2_norm_rope* nr) {
+  if (nr->norm_weight && !aligned(nr->norm_weight, 16)) return false;
+  if (!(nr->norm_eps >= 0.0f) || nr->norm_eps > 1.0e30f) return false;
+  if (nr->rope && (!(nr->rope_base > 1.0f) || nr->rope_base > 1.0e30f)) return false;
+  return true;
+}
 // clears the error word at the start of a call
 inline csa2_status reset_error(void* ws, cudaStream_t st) {
   return cudaMemsetAsync(ws, 0, sizeof(ErrWord), st) == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;

@@ -106,6 +106,23 @@ typedef enum {
 csa2_status csa2_quantize_entries(const float* Cbar, const float* KI, int64_t n,
                                   const csa2_kv_planes* dst, int64_t e0, csa2_stream stream);
 
+/* ----------------------------------------------------- in-layer RMSNorm/RoPE */
+
+/* RMSNorm and partial RoPE of a 512-channel vector ("DeepSeek-V4: Towards Highly
+ * Efficient Million-Token Context Intelligence", CSA, other details: RMSNorm of
+ * every query head and compressed entry before the core attention; RoPE on the
+ * last 64 channels of query, KV and output):
+ *   y = norm_weight[c] * x[c] / sqrt(mean(x^2) + norm_eps)     when norm_weight != NULL;
+ *   channels 448 + 2i, 449 + 2i (i < 32) turned counter-clockwise by
+ *   pos * rope_base^(-i/32)                                    when rope != 0.
+ * norm_weight is a device array of 512 fp32.  rope_base > 1, norm_eps >= 0. */
+typedef struct {
+  const float* norm_weight;
+  float norm_eps;
+  int32_t rope;
+  float rope_base;
+} csa2_norm_rope;
+
 /* -------------------------------------------------------------- cache write */
 
 /* Prefill cache write of one sequence slot (CED Eq. (1) and the CSA2 compressor):
@@ -121,11 +138,16 @@ csa2_status csa2_quantize_entries(const float* Cbar, const float* KI, int64_t n,
  * Requires T % m == 0, 1 <= m <= 64 with 64 % m == 0, d_model % 64 == 0.
  * The projection runs on the tensor cores (bf16 operands, fp32 accumulation)
  * for m <= 32 and on the CUDA cores (fp32) for m = 64; the workspace also holds
- * a transposed copy of W_KV and W_Z (2 * d_model * 512 bf16). */
+ * a transposed copy of W_KV and W_Z (2 * d_model * 512 bf16).
+ * kv_nr (or NULL): RMSNorm / RoPE of the main-KV copy before its quantization
+ * ("DeepSeek-V4.1-Flash course, 02 Architecture", 2.4.4: quantized after RoPE);
+ * entry j of the call sits at position pos_first + j * m.  The indexer key
+ * keeps the pooled latent. */
 csa2_status csa2_cache_write(const void* H_bf16, int64_t T, int32_t d_model, const void* Wkv_bf16,
                              const void* Wz_bf16, const void* Wik_bf16, int32_t m,
                              const csa2_kv_planes* dst, int32_t seq, int64_t entry_offset,
-                             void* ws, size_t ws_bytes, csa2_stream stream);
+                             const csa2_norm_rope* kv_nr, int64_t pos_first, void* ws,
+                             size_t ws_bytes, csa2_stream stream);
 size_t csa2_cache_write_workspace_size(int64_t T, int32_t d_model, int32_t m);
 
 /* ---------------------------------------------------------- indexer + top-k */
@@ -206,11 +228,21 @@ csa2_status csa2_index_topk_noalloc(const csa2_kv_planes* kv, int32_t B, const i
  *   q_bf16    [B][64][512] bf16 (unscaled);  out [B][64][512] fp32;  lse_out [B][64] or NULL
  *   softmax_scale  positive and finite (CSA2_ERR_INVALID_ARG otherwise)
  * An index outside [0, seq_stride) is skipped and reported as CSA2_ERR_INDEX_RANGE
- * through the workspace error word.  With no rows, out = 0 and lse = -inf. */
+ * through the workspace error word.  With no rows, out = 0 and lse = -inf.
+ * In-layer extras ("DeepSeek-V4 ...", CSA, other details), each off when NULL:
+ *   q_nr      RMSNorm of every query head and/or RoPE of its last 64 channels at
+ *             q_pos[b]; with RoPE the output's last 64 channels are turned back
+ *             by -q_pos[b] (the cached entries and window rows carry their own);
+ *   q_pos     [B] int64 query positions (required when q_nr->rope);
+ *   sink      [64] fp32 per-head logits z'_h: exp(z'_h) joins every softmax
+ *             denominator (and lse); with no rows out = 0 and lse = z'_h.
+ * The normalised / rotated q is rounded to f16 for the tensor cores. */
 csa2_status csa2_sparse_attn_decode(const csa2_kv_planes* kv, int32_t B, const int32_t* topk,
                                     int32_t k, const uint8_t* swa_e4m3, int32_t n_swa,
-                                    const void* q_bf16, float softmax_scale, float* out,
-                                    float* lse_out, void* ws, size_t ws_bytes, csa2_stream stream);
+                                    const void* q_bf16, float softmax_scale,
+                                    const csa2_norm_rope* q_nr, const int64_t* q_pos,
+                                    const float* sink, float* out, float* lse_out, void* ws,
+                                    size_t ws_bytes, csa2_stream stream);
 size_t csa2_sparse_attn_workspace_size(int32_t B, int32_t k, int32_t n_swa);
 
 /* ---------------------------------------------------------------- schedule */

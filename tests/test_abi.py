@@ -109,9 +109,10 @@ def test_host_validation_without_gpu(L):
                            None, None, 0, None)
     assert rc == 1
     rc = L.csa2_sparse_attn_decode(ctypes.byref(P), 1, None, 512, None, 0, None, 1.0, None, None,
-                                   None, 0, None)
+                                   None, None, None, None, 0, None)
     assert rc == 1
-    rc = L.csa2_cache_write(None, 64, 5120, None, None, None, 2, ctypes.byref(P), 0, 0, None, 0, None)
+    rc = L.csa2_cache_write(None, 64, 5120, None, None, None, 2, ctypes.byref(P), 0, 0, None, 0, None, 0,
+                            None)
     assert rc == 1
     fake = csa2.KVPlanes(16, 16, 16, 16, 100)  # aligned non-null pointers, never dereferenced
     # k out of range, bad mode, workspace missing
@@ -125,13 +126,23 @@ def test_host_validation_without_gpu(L):
                              256, 1 << 20, None) == 1  # POOL without pool_in
     assert L.csa2_index_topk(ctypes.byref(fake), 1, 16, 10, 16, 16, 8, 1, 4, 16, None, 16, None, None,
                              256, 1 << 20, None) == 2  # block != 8
-    assert L.csa2_cache_write(16, 64, 5120, 16, 16, 16, 3, ctypes.byref(fake), 0, 0, 256, 1 << 30,
-                              None) == 2  # m = 3
-    assert L.csa2_sparse_attn_decode(ctypes.byref(fake), 1, 16, 512, 16, 129, 16, 1.0, 16, None, 256,
-                                     1 << 30, None) == 1  # n_swa > 128
+    assert L.csa2_cache_write(16, 64, 5120, 16, 16, 16, 3, ctypes.byref(fake), 0, 0, None, 0, 256,
+                              1 << 30, None) == 2  # m = 3
+    assert L.csa2_sparse_attn_decode(ctypes.byref(fake), 1, 16, 512, 16, 129, 16, 1.0, None, None, None,
+                                     16, None, 256, 1 << 30, None) == 1  # n_swa > 128
     for bad_scale in (0.0, -0.04, float("inf"), float("nan")):  # the softmax scale must be positive, finite
-        assert L.csa2_sparse_attn_decode(ctypes.byref(fake), 1, 16, 512, 16, 128, 16, bad_scale, 16, None,
-                                         256, 1 << 30, None) == 1
+        assert L.csa2_sparse_attn_decode(ctypes.byref(fake), 1, 16, 512, 16, 128, 16, bad_scale, None, None,
+                                         None, 16, None, 256, 1 << 30, None) == 1
+    # RoPE of the query needs the positions; a base <= 1 and a negative eps are rejected
+    nr = csa2.NormRope(None, 1e-6, 1, 10000.0)
+    assert L.csa2_sparse_attn_decode(ctypes.byref(fake), 1, 16, 512, 16, 128, 16, 0.04, ctypes.byref(nr),
+                                     None, None, 16, None, 256, 1 << 30, None) == 1
+    for bad in (csa2.NormRope(None, 1e-6, 1, 1.0), csa2.NormRope(None, -1.0, 0, 10000.0),
+                csa2.NormRope(4, 1e-6, 0, 10000.0)):  # misaligned weight
+        assert L.csa2_sparse_attn_decode(ctypes.byref(fake), 1, 16, 512, 16, 128, 16, 0.04, ctypes.byref(bad),
+                                         16, None, 16, None, 256, 1 << 30, None) == 1
+        assert L.csa2_cache_write(16, 64, 5120, 16, 16, 16, 2, ctypes.byref(fake), 0, 0, ctypes.byref(bad), 0,
+                                  256, 1 << 30, None) == 1
 
 
 def test_workspace_queries(L):

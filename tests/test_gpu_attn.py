@@ -105,3 +105,77 @@ def test_out_of_range_index_reported(cache):
     topk[1, 7] = 3072 + 5  # beyond the slot
     _, _, st, det = _attn(c, topk, swa, q, 512, 128)
     assert st == 6 and det == 3077
+
+
+def _extras(B, seed):
+    rng = np.random.default_rng(seed)
+    w = (1.0 + 0.3 * rng.standard_normal(512)).astype(np.float32)
+    pos = (1_000_003 + 37 * np.arange(B)).astype(np.int64)  # millions: the fp64 angle path
+    sink = (2.0 * rng.standard_normal(64)).astype(np.float32)
+    return w, pos, sink
+
+
+def _lse_bound(oracle_mod, c, topk, swa, q, n_swa, w, pos):
+    """Each logit moves by at most scale * 2^-11 * sum_c |q'_c x_c| when q' (normalised and
+    rotated in fp32) is rounded to f16 (2^-12 relative) plus its fp32 arithmetic (2^-12,
+    generously); lse moves by at most the largest logit change of its query."""
+    import synth
+
+    bounds = []
+    for b in range(topk.shape[0]):
+        kvc, kvs, _, _ = c.oracle_slot(b)
+        idx = topk[b][topk[b] >= 0]
+        X = np.concatenate([oracle_mod.dequant_main(kvc[idx], kvs[idx]),
+                            _e4m3_rows(swa[b][:n_swa])]) if n_swa else oracle_mod.dequant_main(kvc[idx], kvs[idx])
+        qf = synth.bf16_to_f32(q[b]).astype(np.float64)
+        qn = oracle_mod.rope(oracle_mod.rmsnorm(qf, w, 1e-6), float(pos[b]))
+        bounds.append(SCALE * 2.0 ** -11 * (np.abs(qn) @ np.abs(X).T).max(1))
+    return np.stack(bounds)
+
+
+def _e4m3_rows(b):
+    return torch.from_numpy(np.ascontiguousarray(b)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+@pytest.mark.parametrize("B", [2, 80])
+def test_attention_with_norm_rope_sink(oracle_mod, B):
+    """Query RMSNorm + RoPE at positions near 10^6, the output turned back, a sink per head:
+    batch 2 splits each query over several CTAs (the merge adds the sink), batch 80 runs a
+    query in one CTA."""
+    n = 700
+    c = SmallCache(oracle_mod, 6, B, n)
+    k, n_swa = 512, 128
+    rng = np.random.default_rng(B)
+    topk = np.sort(np.stack([rng.choice(n, k, replace=False) for _ in range(B)]), 1).astype(np.int32)
+    topk[:, 5] = -1
+    q = W.attn_query(6, 1, B)
+    swa = W.swa_rows(6, 1, B, 128)
+    w, pos, sink = _extras(B, B + 1)
+    out = torch.empty((B, 64, 512), dtype=torch.float32, device="cuda")
+    lse = torch.empty((B, 64), dtype=torch.float32, device="cuda")
+    ws = csa2.workspace(csa2.sparse_attn_workspace_size(B, k, n_swa))
+    w_d = to_dev(w)
+    csa2.sparse_attn_decode(c.planes, B, to_dev(topk), k, to_dev(np.ascontiguousarray(swa)), n_swa,
+                            to_dev(q.view(np.int16)), SCALE, out, ws, lse_out=lse,
+                            q_nr=csa2.norm_rope(w_d, 1e-6, True, 10000.0), q_pos=to_dev(pos),
+                            sink=to_dev(sink))
+    assert csa2.check(ws)[0] == 0
+    got, glse = out.cpu().numpy(), lse.cpu().numpy()
+    ref, rlse = [], []
+    for b in range(B):
+        kvc, kvs, _, _ = c.oracle_slot(b)
+        o, l_ = oracle_mod.attention(kvc, kvs, topk[b], swa[b], q[b], SCALE, q_norm_weight=w, eps=1e-6,
+                                     qpos=float(pos[b]), sink=sink)
+        ref.append(o)
+        rlse.append(l_)
+    ref, rlse = np.stack(ref), np.stack(rlse)
+    check_attention(got, ref)
+    bound = _lse_bound(oracle_mod, c, topk, swa, q, n_swa, w, pos)
+    assert np.all(np.abs(glse - rlse) <= bound + 1e-5 * np.abs(rlse) + 1e-5)
+    # the sink takes weight: a sink far above every logit drives the output to zero
+    csa2.sparse_attn_decode(c.planes, B, to_dev(topk), k, to_dev(np.ascontiguousarray(swa)), n_swa,
+                            to_dev(q.view(np.int16)), SCALE, out, ws, lse_out=lse,
+                            q_nr=csa2.norm_rope(w_d, 1e-6, True, 10000.0), q_pos=to_dev(pos),
+                            sink=to_dev(np.full(64, 1e4, np.float32)))
+    assert np.abs(out.cpu().numpy()).max() < 1e-30
+    assert np.allclose(lse.cpu().numpy(), 1e4, rtol=1e-6)

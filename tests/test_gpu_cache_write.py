@@ -40,7 +40,7 @@ def _bits(x):
     return (b >> 16).astype(np.uint16)
 
 
-def _gpu_write(H, Wkv, Wz, Wik, m, seq=1, offset=5, stride=None):
+def _gpu_write(H, Wkv, Wz, Wik, m, seq=1, offset=5, stride=None, kv_nr=None, pos_first=0):
     T, d = H.shape
     n = T // m
     stride = stride or (offset + n + 3)
@@ -49,7 +49,8 @@ def _gpu_write(H, Wkv, Wz, Wik, m, seq=1, offset=5, stride=None):
         t.fill_(0xA5)
     ws = csa2.workspace(csa2.cache_write_workspace_size(T, d, m))
     csa2.cache_write(to_dev(H.view(np.int16)), T, d, to_dev(Wkv.view(np.int16)),
-                     to_dev(Wz.view(np.int16)), to_dev(Wik.view(np.int16)), m, P, seq, offset, ws)
+                     to_dev(Wz.view(np.int16)), to_dev(Wik.view(np.int16)), m, P, seq, offset, ws,
+                     kv_nr=kv_nr, pos_first=pos_first)
     assert csa2.check(ws)[0] == 0
     e0 = seq * stride + offset
     out = [t[e0:e0 + n].cpu().numpy() for t in (P.kv_codes, P.kv_scales, P.ix_codes, P.ix_scales)]
@@ -156,4 +157,47 @@ def test_gaussian_banded(oracle_mod, T, d, m):
     f1, b1 = _group_bytes_ok(got[0], got[1], kvc, kvs, _decided_main(cb32, eCb, e4m3_mids, oracle_mod), 8)
     f2, b2 = _group_bytes_ok(got[2], got[3], ixc, ixs, _decided_index(ki32, eKI), 16)
     # the bounds leave the test its teeth: most groups are decided
+    assert f1 > 0.8 * (f1 + b1) and f2 > 0.8 * (f2 + b2), (f1, b1, f2, b2)
+
+
+def _norm_rope_bounds(cb, att, eCb, w, eps):
+    """Error bounds of the GPU's normalised, rotated copy from those of its Cbar.
+    RMSNorm y_c = w_c x_c / r with r = sqrt(mean(x^2) + eps): an input error dx moves r
+    by at most rms(dx) (Cauchy-Schwarz), so y_c by |w_c| (dx_c + |x_c| rms(dx) / r) / r,
+    plus the fp32 evaluation (a warp tree of 512 squares, a square root, a division:
+    32 u of |y| covers it).  RoPE of a pair (x, y): each output moves by at most the two
+    inputs' bounds plus the angle error (fp64 reduction, fp32 angle and sincos: 3e-7 rad)
+    and four fp32 roundings, times |x| + |y|."""
+    r = np.sqrt((cb ** 2).mean(1, keepdims=True) + eps)
+    rms_e = np.sqrt((eCb ** 2).mean(1, keepdims=True))
+    y = w[None, :].astype(np.float64) * cb / r
+    e = np.abs(w)[None, :] * (eCb + np.abs(cb) * rms_e / r) / r + 32.0 * U * np.abs(y)
+    e_out = e.copy()
+    ex, ey = e[:, 448::2], e[:, 449::2]
+    mag = np.abs(y[:, 448::2]) + np.abs(y[:, 449::2])
+    e_pair = ex + ey + (3e-7 + 4.0 * U) * mag
+    e_out[:, 448::2] = e_pair
+    e_out[:, 449::2] = e_pair
+    return e_out
+
+
+@pytest.mark.parametrize("T,d,m", [(512, 5120, 2), (1536, 1024, 64)])
+def test_gaussian_banded_norm_rope(oracle_mod, T, d, m):
+    """The main-KV copy normalised by RMSNorm and turned by RoPE at positions near 10^6
+    before its quantization; the indexer planes as without."""
+    H, Wkv, Wz, Wik = W.cache_write_inputs(3, T, d)
+    w = (1.0 + 0.3 * np.random.default_rng(T).standard_normal(512)).astype(np.float32)
+    pos_first = 1_000_001
+    got = _gpu_write(H, Wkv, Wz, Wik, m, kv_nr=csa2.norm_rope(to_dev(w), 1e-6, True, 10000.0),
+                     pos_first=pos_first)
+    kvc, kvs, ixc, ixs, cb, ki, att = oracle_mod.cache_write(
+        H, Wkv, Wz, Wik, m, return_prequant=True, norm_weight=w, eps=1e-6, rope=True,
+        pos_first=float(pos_first), pos_step=float(m))
+    eCb, eKI = _error_bounds(H, Wkv, Wz, Wik, m, cb)
+    eAtt = _norm_rope_bounds(cb, att, eCb, w, 1e-6)
+    e4m3_mids = np.array([0.5 * (oracle_mod.e4m3_value(c) + oracle_mod.e4m3_value(c + 1)) for c in range(126)])
+    att32 = att.astype(np.float32).astype(np.float64)
+    ki32 = ki.astype(np.float32).astype(np.float64)
+    f1, b1 = _group_bytes_ok(got[0], got[1], kvc, kvs, _decided_main(att32, eAtt, e4m3_mids, oracle_mod), 8)
+    f2, b2 = _group_bytes_ok(got[2], got[3], ixc, ixs, _decided_index(ki32, eKI), 16)
     assert f1 > 0.8 * (f1 + b1) and f2 > 0.8 * (f2 + b2), (f1, b1, f2, b2)
