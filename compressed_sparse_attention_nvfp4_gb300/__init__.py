@@ -78,6 +78,7 @@ def lib() -> ctypes.CDLL:
             "csa2_cache_write": ([vp, i64, i32, vp, vp, vp, i32, pl, i32, i64, nr, i64, vp, sz, vp],
                                  ctypes.c_int),
             "csa2_cache_write_workspace_size": ([i64, i32, i32], sz),
+            "csa2_quantize_index_query": ([vp, i64, vp, vp], ctypes.c_int),
             "csa2_index_topk": ([pl, i32, vp, i64, vp, vp, i32, ctypes.c_int, i32, i32, vp, vp, vp,
                                  vp, vp, sz, vp], ctypes.c_int),
             "csa2_index_topk_workspace_size": ([i32, i64, i32, i32, i32], sz),
@@ -173,6 +174,13 @@ def workspace(nbytes: int, device="cuda"):
 def quantize_entries(planes: Planes, Cbar, KI, n: int, e0: int = 0, stream=None) -> None:
     _ok(lib().csa2_quantize_entries(_ptr(Cbar), _ptr(KI), n, ctypes.byref(planes.c), e0,
                                     _stream(stream)), "csa2_quantize_entries")
+
+
+def quantize_index_query(q, n_rows: int, out, stream=None) -> None:
+    """MXFP4 indexer query: q bf16 [n_rows][128] -> out bf16 (may be q) holding the values of
+    its E2M1 codes under one E8M0 scale per 32 channels."""
+    _ok(lib().csa2_quantize_index_query(_ptr(q), n_rows, _ptr(out), _stream(stream)),
+        "csa2_quantize_index_query")
 
 
 def cache_write_workspace_size(T: int, d_model: int, m: int) -> int:

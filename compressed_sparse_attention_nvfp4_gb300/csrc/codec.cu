@@ -93,7 +93,56 @@ void launch_quantize(const float* Cbar, const float* KI, int64_t n, const csa2_k
   }
 }
 
+// MXFP4 indexer query: one thread per group of 32 consecutive channels, quantized
+// by the indexer-key rule and written back as the bf16 values the codes decode to
+// (E2M1 times a power of two: exact in bf16, subnormal scales included).
+__global__ void k_quantize_query_mxfp4(const uint16_t* __restrict__ q, int64_t ngroups, uint16_t* __restrict__ out) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= ngroups) return;
+  const uint4* src = reinterpret_cast<const uint4*>(q + t * 32);
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 r = src[i];
+    const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[8 * i + 2 * j] = __uint_as_float(w4[j] << 16);
+      v[8 * i + 2 * j + 1] = __uint_as_float(w4[j] & 0xFFFF0000u);
+    }
+  }
+  __align__(16) uint8_t codes[16];
+  uint8_t sb;
+  quantize_index_group_vals(v, codes, &sb);
+  const float X = e8m0_to_float(sb);
+  uint32_t o[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {  // byte i: elements 2i (low nibble), 2i + 1
+    const float2 e = e2m1x2_to_float2(codes[i]);
+    const uint32_t lo = __float_as_uint(e.x * X) >> 16, hi = __float_as_uint(e.y * X) >> 16;
+    o[i] = lo | (hi << 16);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(out + t * 32);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+}
+
 }  // namespace csa2
+
+extern "C" csa2_status csa2_quantize_index_query(const void* q_bf16, int64_t n_rows, void* q_out_bf16,
+                                                 csa2_stream stream) {
+  using namespace csa2;
+  if (n_rows < 0 || (n_rows > 0 && (!q_bf16 || !q_out_bf16))) return CSA2_ERR_INVALID_ARG;
+  if ((q_bf16 && !aligned(q_bf16, 16)) || (q_out_bf16 && !aligned(q_out_bf16, 16))) return CSA2_ERR_INVALID_ARG;
+  if (n_rows == 0) return CSA2_OK;
+  if (n_rows > (int64_t)1 << 34) return CSA2_ERR_UNSUPPORTED;
+  const int64_t ngroups = n_rows * (kDIdx / 32);
+  cudaStream_t st = (cudaStream_t)stream;
+  KernelTimer timer("k_quantize_query_mxfp4", st);
+  k_quantize_query_mxfp4<<<(unsigned)cdiv(ngroups, 256), 256, 0, st>>>((const uint16_t*)q_bf16, ngroups,
+                                                                     (uint16_t*)q_out_bf16);
+  return launch_status();
+}
 
 extern "C" csa2_status csa2_quantize_entries(const float* Cbar, const float* KI, int64_t n,
                                              const csa2_kv_planes* dst, int64_t e0,

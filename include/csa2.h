@@ -106,6 +106,16 @@ typedef enum {
 csa2_status csa2_quantize_entries(const float* Cbar, const float* KI, int64_t n,
                                   const csa2_kv_planes* dst, int64_t e0, csa2_stream stream);
 
+/* MXFP4 indexer query ("DeepSeek-V4: Towards Highly Efficient Million-Token Context
+ * Intelligence", lightning indexer: the indexer query is quantized to FP4 like its keys):
+ * every group of 32 consecutive channels of q_bf16 [n_rows][128] (n_rows = B x 32 heads)
+ * becomes E2M1 codes under one E8M0 scale by the indexer-key rule above, and q_out_bf16
+ * receives the bf16 values the codes decode to (exact: two significant bits times a power
+ * of two).  csa2_index_topk takes the result as its query.  q_out_bf16 may equal q_bf16;
+ * both 16-byte aligned. */
+csa2_status csa2_quantize_index_query(const void* q_bf16, int64_t n_rows, void* q_out_bf16,
+                                      csa2_stream stream);
+
 /* ----------------------------------------------------- in-layer RMSNorm/RoPE */
 
 /* RMSNorm and partial RoPE of a 512-channel vector ("DeepSeek-V4: Towards Highly

@@ -111,6 +111,10 @@ def test_host_validation_without_gpu(L):
     rc = L.csa2_sparse_attn_decode(ctypes.byref(P), 1, None, 512, None, 0, None, 1.0, None, None,
                                    None, None, None, None, 0, None)
     assert rc == 1
+    assert L.csa2_quantize_index_query(None, -1, None, None) == 1
+    assert L.csa2_quantize_index_query(16, 4, None, None) == 1      # no output
+    assert L.csa2_quantize_index_query(8, 4, 16, None) == 1         # misaligned input
+    assert L.csa2_quantize_index_query(None, 0, None, None) == 0    # nothing to do
     rc = L.csa2_cache_write(None, 64, 5120, None, None, None, 2, ctypes.byref(P), 0, 0, None, 0, None, 0,
                             None)
     assert rc == 1

@@ -134,3 +134,35 @@ def test_negative_weights_general_sign(cache, oracle_mod):
         _, _, ixc, ixs = c.oracle_slot(b)
         s = oracle_mod.index_scores(ixc, ixs, q[b], wn[b], n=n)
         check_topk(topk[b], s, 256, what=f"signed[{b}]")
+
+
+def test_mxfp4_query(cache, oracle_mod):
+    """The MXFP4 indexer query: bytes identical to the oracle's quantize-then-decode of q (the
+    key rule on groups of 32), tiny and all-zero groups included; the index over the quantized
+    query matches the oracle's scores of the same quantized query."""
+    import synth
+
+    c, q, w = cache
+    q = q.copy()
+    q[0, 0, :32] = 0                                      # an all-zero group
+    q[1, 3, 32:64] = (q[1, 3, 32:64].astype(np.uint32) & 0x807F).astype(np.uint16)  # subnormal-range group
+    n_rows = q.shape[0] * q.shape[1]
+    qd = to_dev(q.view(np.int16))
+    out = torch.empty_like(qd)
+    csa2.quantize_index_query(qd, n_rows, out)
+    got = out.cpu().numpy().view(np.uint16).reshape(q.shape)
+    codes, scales = oracle_mod.quantize_index(synth.bf16_to_f32(q).reshape(n_rows, 128))
+    vals = oracle_mod.dequant_index(codes, scales).astype(np.float32)
+    ref = (vals.view(np.uint32) >> 16).astype(np.uint16).reshape(q.shape)
+    assert np.array_equal(vals.view(np.uint32) & 0xFFFF, np.zeros_like(vals.view(np.uint32)))  # exact in bf16
+    assert np.array_equal(got, ref)
+    # in place, and through the index
+    csa2.quantize_index_query(qd, n_rows, qd)
+    assert np.array_equal(qd.cpu().numpy().view(np.uint16).reshape(q.shape), ref)
+    n_entries = [4133, 4096, 700]
+    topk, _, scores = _run(c, got, w, n_entries, 512, csa2.TOPK_FLAT)
+    for b, n in enumerate(n_entries):
+        _, _, ixc, ixs = c.oracle_slot(b)
+        s = oracle_mod.index_scores(ixc, ixs, got[b], w[b], n=n)
+        assert np.allclose(scores[b, :n], s, rtol=2e-5, atol=2e-5 * np.abs(s).max())
+        check_topk(topk[b], s, 512, what=f"mxfp4-q[{b}]")
