@@ -396,6 +396,68 @@ def run_attention(dev, st, steps: int, warmup: int):
     }
 
 
+def run_append(dev, st, calls: int, warmup: int):
+    """Per-step decode writes at batch 128: the decoder layer's append (one entry per query,
+    m = 1, d_model 5120, RMSNorm + RoPE) and one window row per query."""
+    import numpy as np
+    import torch
+
+    import compressed_sparse_attention_nvfp4_gb300 as csa2
+    import synth
+    from synth import workloads as W
+
+    G, d, m, stride = AT_B, CW_D, 1, 4096
+    ss = torch.cuda.current_stream(dev).cuda_stream
+    with torch.cuda.stream(st):
+        H = torch.empty((G, d), dtype=torch.int16, device=dev)
+        Wkv = torch.empty((d, 512), dtype=torch.int16, device=dev)
+        Wz = torch.empty((d, 512), dtype=torch.int16, device=dev)
+        Wik = torch.empty((512, 128), dtype=torch.int16, device=dev)
+    synth.dev_normal_bf16(CW_SEED, W.TID_H, G * d, H.data_ptr(), ss)
+    synth.dev_normal_bf16(CW_SEED, W.TID_WKV, d * 512, Wkv.data_ptr(), ss, scale=1.0 / math.sqrt(d))
+    synth.dev_normal_bf16(CW_SEED, W.TID_WZ, d * 512, Wz.data_ptr(), ss, scale=1.0 / math.sqrt(d))
+    synth.dev_normal_bf16(CW_SEED, W.TID_WIK, 512 * 128, Wik.data_ptr(), ss, scale=1.0 / math.sqrt(512))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(st):
+        P = csa2.Planes.empty(G, stride, dev)
+        slot = torch.arange(G, dtype=torch.int32, device=dev)
+        entry = torch.full((G,), 4000, dtype=torch.int64, device=dev)
+        pos = entry + 0
+        w = torch.ones(512, dtype=torch.float32, device=dev)
+        ws = csa2.workspace(csa2.cache_append_workspace_size(G, d, m), dev)
+        x = torch.randn((G, 512), dtype=torch.float32, device=dev)
+        ring = torch.zeros((G, NSWA, 512), dtype=torch.uint8, device=dev)
+    nr = csa2.norm_rope(w, 1e-6, True, 10000.0)
+
+    def append():
+        csa2.cache_append(H, G, d, Wkv, Wz, Wik, m, P, G, slot, entry, ws, kv_nr=nr, pos=pos, stream=st)
+
+    def window():
+        csa2.swa_append(x, G, pos, G, ring, NSWA, nr=nr, stream=st)
+
+    out = {"workload": f"decode-time writes, batch {G}: one cache entry per query (m = 1, d_model {d}, "
+                       "RMSNorm + RoPE, E2M1/E4M3 + MXFP4 planes) and one E4M3 window row per query"}
+    for name, fn in (("cache_append", append), ("swa_append", window)):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for _ in range(calls):
+            fn()
+        b.record(st)
+        torch.cuda.synchronize()
+        out[name + "_ms_per_call"] = round(a.elapsed_time(b) / calls, 4)
+    assert csa2.check(ws, st)[0] == 0
+    csa2.timing_enable(True)
+    append()
+    window()
+    torch.cuda.synchronize()
+    out["kernels_ms_per_launch"] = {k: round(t / n, 4) for k, (n, t) in sorted(csa2.kernel_times().items())}
+    csa2.timing_enable(False)
+    return out
+
+
 def tensor_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -584,6 +646,7 @@ def run_ours(args, rank, world, local_rank):
         line["attention_b128"] = run_attention(dev, st, 50, 3)
     if not args.no_cache_write:
         line["cache_write"] = run_cache_write(dev, st, 5, 2)
+        line["decode_append"] = run_append(dev, st, 20, 3)
     if not args.no_step40:
         del planes, ws_i, ws_a
         torch.cuda.empty_cache()
@@ -606,6 +669,8 @@ def main():
                     help="skip the batch-128 attention measurement (its own object in the line)")
     ap.add_argument("--attn-only", action="store_true",
                     help="profiling case: only the batch-128 attention, printed as its own line")
+    ap.add_argument("--append-only", action="store_true",
+                    help="profiling case: only the decode-time cache append and window write")
     ap.add_argument("--step40-only", action="store_true",
                     help="profiling case: only the 40-layer step, printed as its own line")
     ap.add_argument("--cache-write-only", action="store_true",
@@ -672,6 +737,19 @@ def main():
         if rank == 0:
             print(json.dumps({"step_40_layers": run_step40(dev, st, max(1, min(args.steps, 20)),
                                                            max(1, args.warmup))}), flush=True)
+        return
+    if args.append_only:
+        import torch
+
+        torch.cuda.set_device(local_rank)
+        import compressed_sparse_attention_nvfp4_gb300 as csa2
+
+        csa2.lib()
+        dev = torch.device("cuda", local_rank)
+        st = torch.cuda.Stream(device=dev)
+        if rank == 0:
+            print(json.dumps({"decode_append": run_append(dev, st, max(1, min(args.steps, 50)),
+                                                          max(1, args.warmup))}), flush=True)
         return
     if args.cache_write_only:
         import torch

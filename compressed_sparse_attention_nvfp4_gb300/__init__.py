@@ -79,6 +79,10 @@ def lib() -> ctypes.CDLL:
                                  ctypes.c_int),
             "csa2_cache_write_workspace_size": ([i64, i32, i32], sz),
             "csa2_quantize_index_query": ([vp, i64, vp, vp], ctypes.c_int),
+            "csa2_cache_append": ([vp, i32, i32, vp, vp, vp, i32, pl, i32, vp, vp, nr, vp, vp, sz, vp],
+                                  ctypes.c_int),
+            "csa2_cache_append_workspace_size": ([i32, i32, i32], sz),
+            "csa2_swa_append": ([vp, i32, vp, vp, i32, nr, vp, i32, vp], ctypes.c_int),
             "csa2_index_topk": ([pl, i32, vp, i64, vp, vp, i32, ctypes.c_int, i32, i32, vp, vp, vp,
                                  vp, vp, sz, vp], ctypes.c_int),
             "csa2_index_topk_workspace_size": ([i32, i64, i32, i32, i32], sz),
@@ -196,6 +200,28 @@ def cache_write(H, T: int, d_model: int, Wkv, Wz, Wik, m: int, planes: Planes, s
                                ctypes.byref(planes.c), seq, entry_offset,
                                ctypes.byref(kv_nr) if kv_nr is not None else None, int(pos_first),
                                _ptr(ws), _nbytes(ws), _stream(stream)), "csa2_cache_write")
+
+
+def cache_append_workspace_size(G: int, d_model: int, m: int) -> int:
+    return lib().csa2_cache_append_workspace_size(G, d_model, m)
+
+
+def cache_append(H, G: int, d_model: int, Wkv, Wz, Wik, m: int, planes: Planes, n_slots: int, slot, entry,
+                 ws, kv_nr: NormRope | None = None, pos=None, stream=None) -> None:
+    """Decode-time append: G groups of m tokens (H bf16 [G][m][d_model]); entry g goes to slot
+    slot[g], index entry[g] (device int32 / int64 arrays), at position pos[g] with RoPE."""
+    _ok(lib().csa2_cache_append(_ptr(H), G, d_model, _ptr(Wkv), _ptr(Wz), _ptr(Wik), m,
+                                ctypes.byref(planes.c), n_slots, _ptr(slot), _ptr(entry),
+                                ctypes.byref(kv_nr) if kv_nr is not None else None, _ptr(pos), _ptr(ws),
+                                _nbytes(ws), _stream(stream)), "csa2_cache_append")
+
+
+def swa_append(x, R: int, pos, n_queries: int, ring, n_win: int, query=None, nr: NormRope | None = None,
+               stream=None) -> None:
+    """Window ring write: row r of x (fp32 [R][512]) -> E4M3 into ring[query[r] or r][pos[r] % n_win]."""
+    _ok(lib().csa2_swa_append(_ptr(x), R, _ptr(query), _ptr(pos), n_queries,
+                              ctypes.byref(nr) if nr is not None else None, _ptr(ring), n_win,
+                              _stream(stream)), "csa2_swa_append")
 
 
 def index_topk_workspace_size(B: int, n_max: int, k: int, block: int = 8,

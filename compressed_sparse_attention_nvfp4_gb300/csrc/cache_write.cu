@@ -539,28 +539,17 @@ extern "C" size_t csa2_cache_write_workspace_size(int64_t T, int32_t d_model, in
   return csa2::cw_ws_layout(nullptr, T / m, d_model).bytes;
 }
 
-extern "C" csa2_status csa2_cache_write(const void* H_bf16, int64_t T, int32_t d_model,
-                                        const void* Wkv_bf16, const void* Wz_bf16, const void* Wik_bf16,
-                                        int32_t m, const csa2_kv_planes* dst, int32_t seq,
-                                        int64_t entry_offset, const csa2_norm_rope* kv_nr,
-                                        int64_t pos_first, void* ws, size_t ws_bytes, csa2_stream stream) {
-  using namespace csa2;
-  cudaStream_t st = (cudaStream_t)stream;
-  if (!planes_ok(dst) || !H_bf16 || !Wkv_bf16 || !Wz_bf16 || !Wik_bf16 || T < 0 || seq < 0 ||
-      entry_offset < 0)
-    return CSA2_ERR_INVALID_ARG;
-  if (m < 1 || m > 64 || 64 % m != 0 || T % m != 0) return CSA2_ERR_UNSUPPORTED;
-  if (d_model < kTK || d_model % 64 != 0) return CSA2_ERR_UNSUPPORTED;
-  if (!aligned(H_bf16, 16) || !aligned(Wkv_bf16, 16) || !aligned(Wz_bf16, 16) || !aligned(Wik_bf16, 16))
-    return CSA2_ERR_INVALID_ARG;
-  if (kv_nr && !norm_rope_ok(kv_nr)) return CSA2_ERR_INVALID_ARG;
+namespace csa2 {
+namespace {
+
+// C = H W_KV, Z = H W_Z (bf16 operands, fp32 accumulation), softmax pooling over
+// groups of m consecutive rows of H into L.cbar, then K^I = Cbar W_IK into L.ki:
+// T / m entries.  Shared by the prefill write (one slot, contiguous entries) and
+// the decode-time append (one group per slot).
+csa2_status cw_compute(const void* H_bf16, int64_t T, int32_t d_model, const void* Wkv_bf16,
+                       const void* Wz_bf16, const void* Wik_bf16, int32_t m, const CwWs& L, void* ws,
+                       cudaStream_t st) {
   const int64_t n = T / m;
-  if (entry_offset + n > dst->seq_stride) return CSA2_ERR_INVALID_ARG;
-  if (!ws || !aligned(ws, 256)) return CSA2_ERR_WORKSPACE;
-  CwWs L = cw_ws_layout(ws, n, d_model);
-  if (ws_bytes < L.bytes) return CSA2_ERR_WORKSPACE;
-  if (reset_error(ws, st) != CSA2_OK) return CSA2_ERR_CUDA;
-  if (T == 0) return CSA2_OK;
   if (m <= 32 && T < ((int64_t)1 << 31)) {
     // tensor cores: transposed weights, then the persistent GEMM + pooling
     {
@@ -604,6 +593,78 @@ extern "C" csa2_status csa2_cache_write(const void* H_bf16, int64_t T, int32_t d
     KernelTimer timer("k_cw_ki_tc", st);
     k_cw_ki_tc<<<(unsigned)cdiv(n, 128), kKtThreads, smem, st>>>(map_wikt, L.cbar, n, L.ki, ws);
   }
-  launch_quantize(L.cbar, L.ki, n, dst, (int64_t)seq * dst->seq_stride + entry_offset, st, kv_nr, pos_first, m);
+  return CSA2_OK;
+}
+
+}  // namespace
+}  // namespace csa2
+
+extern "C" csa2_status csa2_cache_write(const void* H_bf16, int64_t T, int32_t d_model,
+                                        const void* Wkv_bf16, const void* Wz_bf16, const void* Wik_bf16,
+                                        int32_t m, const csa2_kv_planes* dst, int32_t seq,
+                                        int64_t entry_offset, const csa2_norm_rope* kv_nr,
+                                        int64_t pos_first, void* ws, size_t ws_bytes, csa2_stream stream) {
+  using namespace csa2;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (!planes_ok(dst) || !H_bf16 || !Wkv_bf16 || !Wz_bf16 || !Wik_bf16 || T < 0 || seq < 0 ||
+      entry_offset < 0)
+    return CSA2_ERR_INVALID_ARG;
+  if (m < 1 || m > 64 || 64 % m != 0 || T % m != 0) return CSA2_ERR_UNSUPPORTED;
+  if (d_model < kTK || d_model % 64 != 0) return CSA2_ERR_UNSUPPORTED;
+  if (!aligned(H_bf16, 16) || !aligned(Wkv_bf16, 16) || !aligned(Wz_bf16, 16) || !aligned(Wik_bf16, 16))
+    return CSA2_ERR_INVALID_ARG;
+  if (kv_nr && !norm_rope_ok(kv_nr)) return CSA2_ERR_INVALID_ARG;
+  const int64_t n = T / m;
+  if (entry_offset + n > dst->seq_stride) return CSA2_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256)) return CSA2_ERR_WORKSPACE;
+  CwWs L = cw_ws_layout(ws, n, d_model);
+  if (ws_bytes < L.bytes) return CSA2_ERR_WORKSPACE;
+  if (reset_error(ws, st) != CSA2_OK) return CSA2_ERR_CUDA;
+  if (T == 0) return CSA2_OK;
+  const csa2_status rc = cw_compute(H_bf16, T, d_model, Wkv_bf16, Wz_bf16, Wik_bf16, m, L, ws, st);
+  if (rc != CSA2_OK) return rc;
+  QDest d{};
+  d.e0 = (int64_t)seq * dst->seq_stride + entry_offset;
+  d.pos_first = pos_first;
+  d.pos_step = m;
+  launch_quantize(L.cbar, L.ki, n, dst, d, st, kv_nr);
+  return launch_status();
+}
+
+extern "C" size_t csa2_cache_append_workspace_size(int32_t G, int32_t d_model, int32_t m) {
+  if (G < 0 || d_model <= 0 || m < 1) return 0;
+  return csa2::cw_ws_layout(nullptr, G, d_model).bytes;
+}
+
+extern "C" csa2_status csa2_cache_append(const void* H_bf16, int32_t G, int32_t d_model, const void* Wkv_bf16,
+                                         const void* Wz_bf16, const void* Wik_bf16, int32_t m,
+                                         const csa2_kv_planes* dst, int32_t n_slots, const int32_t* slot,
+                                         const int64_t* entry, const csa2_norm_rope* kv_nr, const int64_t* pos,
+                                         void* ws, size_t ws_bytes, csa2_stream stream) {
+  using namespace csa2;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (!planes_ok(dst) || !H_bf16 || !Wkv_bf16 || !Wz_bf16 || !Wik_bf16 || G < 0 || n_slots <= 0)
+    return CSA2_ERR_INVALID_ARG;
+  if (G > 0 && (!slot || !entry || !aligned(entry, 8) || !aligned(slot, 4))) return CSA2_ERR_INVALID_ARG;
+  if (m < 1 || m > 64 || 64 % m != 0) return CSA2_ERR_UNSUPPORTED;
+  if (d_model < kTK || d_model % 64 != 0) return CSA2_ERR_UNSUPPORTED;
+  if (!aligned(H_bf16, 16) || !aligned(Wkv_bf16, 16) || !aligned(Wz_bf16, 16) || !aligned(Wik_bf16, 16))
+    return CSA2_ERR_INVALID_ARG;
+  if (kv_nr && (!norm_rope_ok(kv_nr) || (kv_nr->rope && (!pos || !aligned(pos, 8))))) return CSA2_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256)) return CSA2_ERR_WORKSPACE;
+  CwWs L = cw_ws_layout(ws, G, d_model);
+  if (ws_bytes < L.bytes) return CSA2_ERR_WORKSPACE;
+  if (reset_error(ws, st) != CSA2_OK) return CSA2_ERR_CUDA;
+  if (G == 0) return CSA2_OK;
+  const csa2_status rc = cw_compute(H_bf16, (int64_t)G * m, d_model, Wkv_bf16, Wz_bf16, Wik_bf16, m, L, ws, st);
+  if (rc != CSA2_OK) return rc;
+  QDest d{};
+  d.slot = slot;
+  d.entry = entry;
+  d.stride = dst->seq_stride;
+  d.n_slots = n_slots;
+  d.pos = pos;
+  d.ws = ws;
+  launch_quantize(L.cbar, L.ki, G, dst, d, st, kv_nr);
   return launch_status();
 }

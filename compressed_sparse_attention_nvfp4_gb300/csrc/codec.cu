@@ -7,18 +7,39 @@
 
 namespace csa2 {
 
+// Entry e of a quantize launch goes to plane row dest_row(d, e): contiguous rows
+// e0 + e, or (scattered) slot[e] * stride + entry[e], skipped and reported when
+// outside the planes.
+__device__ __forceinline__ int64_t dest_row(const QDest& d, int64_t e) {
+  if (!d.slot) return d.e0 + e;
+  const int32_t sl = d.slot[e];
+  const int64_t en = d.entry[e];
+  if (sl < 0 || sl >= d.n_slots || en < 0 || en >= d.stride) {
+    if (d.ws) report_error(d.ws, CSA2_ERR_INDEX_RANGE, sl < 0 || sl >= d.n_slots ? (long long)sl : en);
+    return -1;
+  }
+  return (int64_t)sl * d.stride + en;
+}
+__device__ __forceinline__ int64_t dest_pos(const QDest& d, int64_t e) {
+  return d.pos ? d.pos[e] : d.pos_first + e * d.pos_step;
+}
+
 __global__ void k_quantize_main(const float* __restrict__ x, int64_t n, uint8_t* __restrict__ codes,
-                                uint8_t* __restrict__ scales) {
+                                uint8_t* __restrict__ scales, QDest d) {
   int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= n * 32) return;
-  quantize_main_group(x + t * 16, codes + t * 8, scales + t);
+  const int64_t row = dest_row(d, t / 32);
+  if (row < 0) return;
+  quantize_main_group(x + t * 16, codes + row * 256 + (t % 32) * 8, scales + row * 32 + t % 32);
 }
 
 __global__ void k_quantize_index(const float* __restrict__ x, int64_t n, uint8_t* __restrict__ codes,
-                                 uint8_t* __restrict__ scales) {
+                                 uint8_t* __restrict__ scales, QDest d) {
   int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= n * 4) return;
-  quantize_index_group(x + t * 32, codes + t * 16, scales + t);
+  const int64_t row = dest_row(d, t / 4);
+  if (row < 0) return;
+  quantize_index_group(x + t * 32, codes + row * 64 + (t % 4) * 16, scales + row * 4 + t % 4);
 }
 
 // The main-KV quantizer with RMSNorm and RoPE first ("DeepSeek-V4: ...", CSA,
@@ -26,11 +47,13 @@ __global__ void k_quantize_index(const float* __restrict__ x, int64_t n, uint8_t
 // cache is quantized after RoPE): one warp per entry, lane l holds channels
 // 16l .. 16l + 15 (its quantization group), the rotated pairs sit in lanes 28-31.
 __global__ void k_quantize_main_nr(const float* __restrict__ x, int64_t n, const float* __restrict__ w,
-                                   float eps, int rope, RopeTheta th, int64_t pos_first, int64_t pos_step,
-                                   uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+                                   float eps, int rope, RopeTheta th, uint8_t* __restrict__ codes,
+                                   uint8_t* __restrict__ scales, QDest d) {
   const int64_t e = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;
   if (e >= n) return;  // whole warps leave together
+  const int64_t row = dest_row(d, e);
+  if (row < 0) return;  // the same for the whole warp
   float v[16];
   const float4* src = reinterpret_cast<const float4*>(x + e * kDMain + lane * 16);
 #pragma unroll
@@ -59,7 +82,7 @@ __global__ void k_quantize_main_nr(const float* __restrict__ x, int64_t n, const
     }
   }
   if (rope && lane * 16 >= kRopeFirst) {
-    const double pos = (double)(pos_first + e * pos_step);
+    const double pos = (double)dest_pos(d, e);
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
       float c, s;
@@ -67,29 +90,26 @@ __global__ void k_quantize_main_nr(const float* __restrict__ x, int64_t n, const
       rope_pair(v[2 * p], v[2 * p + 1], c, s);
     }
   }
-  quantize_main_group_vals(v, codes + e * 256 + lane * 8, scales + e * 32 + lane);
+  quantize_main_group_vals(v, codes + row * 256 + lane * 8, scales + row * 32 + lane);
 }
 
-void launch_quantize(const float* Cbar, const float* KI, int64_t n, const csa2_kv_planes* dst,
-                     int64_t e0, cudaStream_t st, const csa2_norm_rope* nr, int64_t pos_first,
-                     int64_t pos_step) {
+void launch_quantize(const float* Cbar, const float* KI, int64_t n, const csa2_kv_planes* dst, const QDest& d,
+                     cudaStream_t st, const csa2_norm_rope* nr) {
   if (n <= 0) return;
   if (Cbar && nr && (nr->norm_weight || nr->rope)) {
     KernelTimer timer("k_quantize_main_nr", st);
     k_quantize_main_nr<<<(unsigned)cdiv(n * 32, 256), 256, 0, st>>>(
         Cbar, n, nr->norm_weight, nr->norm_eps, nr->rope, nr->rope ? make_rope_theta(nr->rope_base) : RopeTheta{},
-        pos_first, pos_step, dst->kv_codes + e0 * 256, dst->kv_scales + e0 * 32);
+        dst->kv_codes, dst->kv_scales, d);
   } else if (Cbar) {
     int64_t threads = n * 32;
     KernelTimer timer("k_quantize_main", st);
-    k_quantize_main<<<(unsigned)cdiv(threads, 256), 256, 0, st>>>(
-        Cbar, n, dst->kv_codes + e0 * 256, dst->kv_scales + e0 * 32);
+    k_quantize_main<<<(unsigned)cdiv(threads, 256), 256, 0, st>>>(Cbar, n, dst->kv_codes, dst->kv_scales, d);
   }
   if (KI) {
     int64_t threads = n * 4;
     KernelTimer timer("k_quantize_index", st);
-    k_quantize_index<<<(unsigned)cdiv(threads, 256), 256, 0, st>>>(
-        KI, n, dst->ix_codes + e0 * 64, dst->ix_scales + e0 * 4);
+    k_quantize_index<<<(unsigned)cdiv(threads, 256), 256, 0, st>>>(KI, n, dst->ix_codes, dst->ix_scales, d);
   }
 }
 
@@ -127,7 +147,83 @@ __global__ void k_quantize_query_mxfp4(const uint16_t* __restrict__ q, int64_t n
   for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
 }
 
+// Window ring write: one warp per row; lane l holds channels 16l .. 16l + 15,
+// optional RMSNorm and RoPE (pairs in lanes 28-31), then E4M3 (nearest even,
+// saturating, no scale) into ring[query][pos mod n_win].  Rows with a negative
+// position or a query outside [0, n_queries) are skipped.
+__global__ void k_swa_append(const float* __restrict__ x, int32_t R, const int32_t* __restrict__ query,
+                             const int64_t* __restrict__ pos, int32_t n_queries, const float* __restrict__ w,
+                             float eps, int rope, RopeTheta th, uint8_t* __restrict__ ring, int32_t n_win) {
+  const int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32;
+  const int lane = threadIdx.x % 32;
+  if (r >= R) return;
+  const int64_t p = pos[r];
+  const int32_t b = query ? query[r] : (int32_t)r;
+  if (p < 0 || b < 0 || b >= n_queries) return;  // the same for the whole warp
+  float v[16];
+  const float4* src = reinterpret_cast<const float4*>(x + r * kDMain + lane * 16);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 f = src[i];
+    v[4 * i] = f.x;
+    v[4 * i + 1] = f.y;
+    v[4 * i + 2] = f.z;
+    v[4 * i + 3] = f.w;
+  }
+  if (w) {
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ss = fmaf(v[i], v[i], ss);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float inv = 1.0f / sqrtf(ss / (float)kDMain + eps);
+    const float4* wv = reinterpret_cast<const float4*>(w + lane * 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 g = wv[i];
+      v[4 * i] = g.x * (v[4 * i] * inv);
+      v[4 * i + 1] = g.y * (v[4 * i + 1] * inv);
+      v[4 * i + 2] = g.z * (v[4 * i + 2] * inv);
+      v[4 * i + 3] = g.w * (v[4 * i + 3] * inv);
+    }
+  }
+  if (rope && lane * 16 >= kRopeFirst) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      float c, sn;
+      rope_cos_sin(th.t[(lane * 16 - kRopeFirst) / 2 + q], (double)p, c, sn);
+      rope_pair(v[2 * q], v[2 * q + 1], c, sn);
+    }
+  }
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    o[i] = float_to_e4m3(v[4 * i]) | (float_to_e4m3(v[4 * i + 1]) << 8) | (float_to_e4m3(v[4 * i + 2]) << 16) |
+           (float_to_e4m3(v[4 * i + 3]) << 24);
+  uint8_t* dst = ring + ((int64_t)b * n_win + p % n_win) * kDMain + lane * 16;
+  *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 }  // namespace csa2
+
+extern "C" csa2_status csa2_swa_append(const float* x, int32_t R, const int32_t* query, const int64_t* pos,
+                                       int32_t n_queries, const csa2_norm_rope* nr, uint8_t* ring, int32_t n_win,
+                                       csa2_stream stream) {
+  using namespace csa2;
+  if (R < 0 || n_queries <= 0 || n_win <= 0) return CSA2_ERR_INVALID_ARG;
+  if (R > 0 && (!x || !pos || !ring || !aligned(x, 16) || !aligned(pos, 8) || !aligned(ring, 16) ||
+                (query && !aligned(query, 4))))
+    return CSA2_ERR_INVALID_ARG;
+  if (nr && !norm_rope_ok(nr)) return CSA2_ERR_INVALID_ARG;
+  if (R == 0) return CSA2_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  const bool rope = nr && nr->rope;
+  KernelTimer timer("k_swa_append", st);
+  k_swa_append<<<(unsigned)cdiv((int64_t)R * 32, 256), 256, 0, st>>>(
+      x, R, query, pos, n_queries, nr ? nr->norm_weight : nullptr, nr ? nr->norm_eps : 0.0f, rope ? 1 : 0,
+      rope ? make_rope_theta(nr->rope_base) : RopeTheta{}, ring, n_win);
+  return launch_status();
+}
 
 extern "C" csa2_status csa2_quantize_index_query(const void* q_bf16, int64_t n_rows, void* q_out_bf16,
                                                  csa2_stream stream) {
@@ -152,6 +248,8 @@ extern "C" csa2_status csa2_quantize_entries(const float* Cbar, const float* KI,
   if ((Cbar && !aligned(Cbar, 16)) || (KI && !aligned(KI, 16))) return CSA2_ERR_INVALID_ARG;
   if (n == 0) return CSA2_OK;
   if (n > (int64_t)1 << 36) return CSA2_ERR_UNSUPPORTED;
-  launch_quantize(Cbar, KI, n, dst, e0, (cudaStream_t)stream);
+  QDest d{};
+  d.e0 = e0;
+  launch_quantize(Cbar, KI, n, dst, d, (cudaStream_t)stream, nullptr);
   return launch_status();
 }

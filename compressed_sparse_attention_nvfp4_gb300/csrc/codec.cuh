@@ -59,8 +59,12 @@ inline RopeTheta make_rope_theta(double base) {
 }
 __device__ __forceinline__ void rope_cos_sin(double theta, double pos, float& c, float& s) {
   constexpr double kTwoPi = 6.283185307179586476925286766559;
+  constexpr double kInvTwoPi = 0.15915494309189533576888376337251;
   const double a = pos * theta;
-  const double red = fma(-kTwoPi, rint(a / kTwoPi), a);  // in [-pi, pi]
+  // a - 2 pi n with n the nearest integer to a / 2 pi (a product, not an fp64
+  // division): |red| <= pi up to a last-bit slip near a half turn, which sincosf
+  // takes as it is
+  const double red = fma(-kTwoPi, rint(a * kInvTwoPi), a);
   sincosf((float)red, &s, &c);
 }
 // (x, y) turned counter-clockwise by the angle with cosine c, sine s
@@ -120,8 +124,18 @@ __device__ __forceinline__ void quantize_index_group(const float* __restrict__ x
   quantize_index_group_vals(v, codes16, scale1);
 }
 
-void launch_quantize(const float* Cbar, const float* KI, int64_t n, const csa2_kv_planes* dst,
-                     int64_t e0, cudaStream_t st, const csa2_norm_rope* nr = nullptr, int64_t pos_first = 0,
-                     int64_t pos_step = 1);
+// Where the entries of a quantize launch go (and, for RoPE, their positions).
+struct QDest {
+  int64_t e0;             // contiguous: entry e -> plane row e0 + e
+  const int32_t* slot;    // or scattered: entry e -> row slot[e] * stride + entry[e]
+  const int64_t* entry;
+  int64_t stride;
+  int32_t n_slots;
+  const int64_t* pos;     // positions of the entries, or pos_first + e * pos_step
+  int64_t pos_first, pos_step;
+  void* ws;               // error word for destinations outside the planes
+};
+void launch_quantize(const float* Cbar, const float* KI, int64_t n, const csa2_kv_planes* dst, const QDest& d,
+                     cudaStream_t st, const csa2_norm_rope* nr);
 
 }  // namespace csa2

@@ -160,6 +160,37 @@ csa2_status csa2_cache_write(const void* H_bf16, int64_t T, int32_t d_model, con
                              size_t ws_bytes, csa2_stream stream);
 size_t csa2_cache_write_workspace_size(int64_t T, int32_t d_model, int32_t m);
 
+/* Decode-time cache append: G groups of m consecutive tokens, each completing one
+ * entry of its own sequence slot ("DeepSeek-V4.1-Flash course, 02 Architecture",
+ * 3.1: during decode every new token projects its hidden state into a new global KV
+ * entry; m = 1 in the decoder, a group completes every m-th token elsewhere).  Each
+ * entry is computed exactly as csa2_cache_write computes one:
+ *   H [G][m][d_model] bf16, the group's tokens in order;
+ *   entry g goes to slot slot[g] (< n_slots), entry index entry[g] (< seq_stride) --
+ *   a destination outside the planes is skipped and reported as CSA2_ERR_INDEX_RANGE
+ *   through the workspace error word;
+ *   kv_nr (or NULL) as in csa2_cache_write, entry g at position pos[g] (required with
+ *   RoPE).  slot, entry, pos are device arrays. */
+csa2_status csa2_cache_append(const void* H_bf16, int32_t G, int32_t d_model, const void* Wkv_bf16,
+                              const void* Wz_bf16, const void* Wik_bf16, int32_t m,
+                              const csa2_kv_planes* dst, int32_t n_slots, const int32_t* slot,
+                              const int64_t* entry, const csa2_norm_rope* kv_nr, const int64_t* pos,
+                              void* ws, size_t ws_bytes, csa2_stream stream);
+size_t csa2_cache_append_workspace_size(int32_t G, int32_t d_model, int32_t m);
+
+/* Sliding-window ring write ("DeepSeek-V4 ...", sliding-window branch: every query keeps
+ * its last n_win uncompressed rows; "DeepSeek-V4.1-Flash course, 02 Architecture", 2.4.4:
+ * they stay FP8): row r, the latent x [R][512] fp32 of a token at position pos[r] of
+ * query query[r] (query == NULL: query r), optionally normalised / rotated by nr at
+ * pos[r], is encoded as E4M3 (nearest even, saturating at +-448, no scale) into
+ * ring[query][pos mod n_win][512] (ring: [n_queries][n_win][512] bytes).  Rows with a
+ * negative position or a query outside [0, n_queries) are skipped.  The ring is the
+ * swa_e4m3 input of csa2_sparse_attn_decode (n_swa = the rows written so far, at most
+ * n_win): the attention does not depend on the order of its rows. */
+csa2_status csa2_swa_append(const float* x, int32_t R, const int32_t* query, const int64_t* pos,
+                            int32_t n_queries, const csa2_norm_rope* nr, uint8_t* ring, int32_t n_win,
+                            csa2_stream stream);
+
 /* ---------------------------------------------------------- indexer + top-k */
 
 /* Lightning-indexer scores and top-k selection for B decode queries; query b

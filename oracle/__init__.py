@@ -79,6 +79,8 @@ def _load():
         lib.o_rmsnorm.restype = None
         lib.o_rope.argtypes = [vp, f64, f64]
         lib.o_rope.restype = None
+        lib.o_swa_row.argtypes = [vp, vp, f64, ctypes.c_int, f64, f64, vp, vp]
+        lib.o_swa_row.restype = None
         lib.o_e2m1_encode_array.argtypes = [vp, i64, vp]
         lib.o_e2m1_encode_array.restype = None
         lib.o_e4m3_encode_array.argtypes = [vp, i64, vp]
@@ -352,3 +354,14 @@ def rope(x, pos: float, base: float = 10000.0) -> np.ndarray:
         _load().o_rope(_p(row), float(pos), float(base))
         out[i] = row
     return out.reshape(np.shape(x))
+
+
+def swa_row(x, norm_weight=None, eps: float = 1e-6, pos=None, rope_base: float = 10000.0):
+    """One window row: (E4M3 bytes [512], the fp64 values before the encoding)."""
+    x = np.ascontiguousarray(x, np.float64).reshape(D_MAIN)
+    out = np.empty(D_MAIN, np.uint8)
+    pre = np.empty(D_MAIN, np.float64)
+    w = None if norm_weight is None else np.ascontiguousarray(norm_weight, np.float32)
+    _load().o_swa_row(_p(x), _p(w), float(eps), int(pos is not None), float(rope_base),
+                      float(0.0 if pos is None else pos), _p(out), _p(pre))
+    return out, pre

@@ -293,6 +293,22 @@ void o_rope(double* x, double pos, double base) {
   }
 }
 
+/* One sliding-window row ([V4] sliding-window branch; [CRS] 2.4.4: the window
+ * stays FP8): RMSNorm (w, or none when NULL), RoPE at pos (rope), then E4M3 of
+ * the value rounded to fp32 (nearest even, saturating at 448, no scale).
+ * pre (or NULL) gets the values before the encoding. */
+void o_swa_row(const double* x, const float* w, double eps, int rope, double base, double pos,
+               uint8_t* out, double* pre) {
+  double y[D_MAIN];
+  if (w)
+    o_rmsnorm(x, D_MAIN, w, eps, y);
+  else
+    memcpy(y, x, sizeof(y));
+  if (rope) o_rope(y, pos, base);
+  for (int c = 0; c < D_MAIN; ++c) out[c] = (uint8_t)o_e4m3_encode((float)y[c]);
+  if (pre) memcpy(pre, y, sizeof(y));
+}
+
 /* ========================================================================== */
 /* Compressor / cache write ([CRS] Eq. (1) and 2.3; [V41] 4.1)                */
 /* ========================================================================== */

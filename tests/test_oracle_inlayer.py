@@ -160,3 +160,18 @@ def test_cache_write_quantizes_the_normalised_rotated_copy(oracle_mod):
     assert np.allclose((oracle_mod.rmsnorm(cb, None, 0.0) ** 2).mean(1), 1.0, atol=1e-12)
     kc, ks = oracle_mod.quantize_main(att.astype(np.float32))
     assert np.array_equal(got[0], kc) and np.array_equal(got[1], ks)
+
+
+def test_swa_row_encodes_the_normalised_rotated_value(oracle_mod):
+    x = _rows(1, 11)[0] * 3.0
+    plain, pre = oracle_mod.swa_row(x)
+    assert np.array_equal(pre, x)
+    assert np.array_equal(plain, oracle_mod.e4m3_encode_array(x.astype(np.float32)))
+    w = np.linspace(0.5, 1.5, D).astype(np.float32)
+    out, pre = oracle_mod.swa_row(x, w, 1e-6, pos=4321.0)
+    assert np.allclose(oracle_mod.rope(pre, -4321.0), oracle_mod.rmsnorm(x, w, 1e-6), rtol=1e-12, atol=1e-12)
+    assert np.array_equal(out, oracle_mod.e4m3_encode_array(pre.astype(np.float32)))
+    # E4M3 keeps 3 mantissa bits: the decoded row is within 2^-4 relative of the value (or saturated)
+    dec = np.array([oracle_mod.e4m3_value(int(v)) for v in out])
+    ok = np.abs(pre) < 448
+    assert np.all(np.abs(dec[ok] - pre[ok]) <= 2.0 ** -4 * np.abs(pre[ok]) + 2.0 ** -10)
