@@ -458,6 +458,61 @@ def run_append(dev, st, calls: int, warmup: int):
     return out
 
 
+PF_N, PF_Q, PF_SEED = 131072, 2048, 6
+PF_WORKLOAD = ("prefill indexer of an encoder Full layer: 2,048 queries of one 262,144-token sequence "
+               "(131,072 entries at m = 2), query i sees the entries of the 128 (i + 1) tokens before it, "
+               "top-512 each")
+
+
+def run_prefill_index(dev, st, calls: int, warmup: int):
+    """csa2_index_topk_prefill: every query scores the visible prefix of one shared slot."""
+    import numpy as np
+    import torch
+
+    import compressed_sparse_attention_nvfp4_gb300 as csa2
+    from compressed_sparse_attention_nvfp4_gb300 import workload as WL
+
+    N, Q = PF_N, PF_Q
+    n_vis = ((np.arange(Q, dtype=np.int64) + 1) * (2 * N // Q) // 2).astype(np.int32)  # token 128 (i + 1), m = 2
+    with torch.cuda.stream(st):
+        planes = csa2.Planes.empty(1, N, dev)
+        WL.fill_planes(planes, PF_SEED, 0, 1, N, stream=st)
+        q, w, _, _ = WL.index_query_dev(PF_SEED, 0, Q, dev)
+        nv = torch.from_numpy(n_vis).to(dev)
+        topk = torch.empty((Q, K_TOP), dtype=torch.int32, device=dev)
+        ws = csa2.workspace(csa2.index_topk_prefill_workspace_size(Q, N, K_TOP), dev)
+    torch.cuda.synchronize()
+
+    def call():
+        csa2.index_topk_prefill(planes, 0, Q, nv, N, q, w, K_TOP, topk, ws, stream=st)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    assert csa2.check(ws, st)[0] == 0
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for _ in range(calls):
+        call()
+    b.record(st)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / calls
+    csa2.timing_enable(True)
+    call()
+    torch.cuda.synchronize()
+    kt = csa2.kernel_times()
+    csa2.timing_enable(False)
+    scored = int(n_vis.astype(np.int64).sum())
+    flop = scored * 32 * 128 * 2  # q_h . K_j for 32 heads of 128
+    return {
+        "workload": PF_WORKLOAD, "calls": calls, "ms_per_call": round(ms, 4),
+        "queries_per_s": round(Q / (ms * 1e-3), 1), "entries_scored_per_call": scored,
+        "entries_scored_per_s": round(scored / (ms * 1e-3), 1),
+        "score_tflops": round(flop / (ms * 1e-3) / 1e12, 1),
+        "kernels_ms_per_launch": {k: round(t / n, 4) for k, (n, t) in sorted(kt.items())},
+    }
+
+
 def tensor_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -647,6 +702,7 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_cache_write:
         line["cache_write"] = run_cache_write(dev, st, 5, 2)
         line["decode_append"] = run_append(dev, st, 20, 3)
+        line["prefill_indexer"] = run_prefill_index(dev, st, 5, 2)
     if not args.no_step40:
         del planes, ws_i, ws_a
         torch.cuda.empty_cache()
@@ -669,6 +725,8 @@ def main():
                     help="skip the batch-128 attention measurement (its own object in the line)")
     ap.add_argument("--attn-only", action="store_true",
                     help="profiling case: only the batch-128 attention, printed as its own line")
+    ap.add_argument("--prefill-index-only", action="store_true",
+                    help="profiling case: only the prefill indexer")
     ap.add_argument("--append-only", action="store_true",
                     help="profiling case: only the decode-time cache append and window write")
     ap.add_argument("--step40-only", action="store_true",
@@ -737,6 +795,19 @@ def main():
         if rank == 0:
             print(json.dumps({"step_40_layers": run_step40(dev, st, max(1, min(args.steps, 20)),
                                                            max(1, args.warmup))}), flush=True)
+        return
+    if args.prefill_index_only:
+        import torch
+
+        torch.cuda.set_device(local_rank)
+        import compressed_sparse_attention_nvfp4_gb300 as csa2
+
+        csa2.lib()
+        dev = torch.device("cuda", local_rank)
+        st = torch.cuda.Stream(device=dev)
+        if rank == 0:
+            print(json.dumps({"prefill_indexer": run_prefill_index(dev, st, max(1, min(args.steps, 20)),
+                                                                   max(1, args.warmup))}), flush=True)
         return
     if args.append_only:
         import torch

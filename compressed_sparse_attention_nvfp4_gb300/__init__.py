@@ -86,6 +86,8 @@ def lib() -> ctypes.CDLL:
             "csa2_index_topk": ([pl, i32, vp, i64, vp, vp, i32, ctypes.c_int, i32, i32, vp, vp, vp,
                                  vp, vp, sz, vp], ctypes.c_int),
             "csa2_index_topk_workspace_size": ([i32, i64, i32, i32, i32], sz),
+            "csa2_index_topk_prefill": ([pl, i32, i32, vp, i64, vp, vp, i32, vp, vp, sz, vp], ctypes.c_int),
+            "csa2_index_topk_prefill_workspace_size": ([i32, i64, i32], sz),
             "csa2_index_topk_noalloc": ([pl, i32, vp, i64, vp, vp, i32, ctypes.c_int, i32, i32, vp,
                                          vp, vp, vp], ctypes.c_int),
             "csa2_sparse_attn_decode": ([pl, i32, vp, i32, vp, i32, vp, f32, nr, vp, vp, vp, vp, vp, sz,
@@ -236,6 +238,18 @@ def index_topk(planes: Planes, B: int, n_entries, n_max: int, qidx, w, k: int, m
                               k, mode, block, n_blocks_keep, _ptr(pool_in), _ptr(topk_out),
                               _ptr(pool_out), _ptr(scores_out), _ptr(ws), _nbytes(ws),
                               _stream(stream)), "csa2_index_topk")
+
+
+def index_topk_prefill_workspace_size(Q: int, n_max: int, k: int) -> int:
+    return lib().csa2_index_topk_prefill_workspace_size(Q, n_max, k)
+
+
+def index_topk_prefill(planes: Planes, seq: int, Q: int, n_visible, n_max: int, qidx, w, k: int, topk_out,
+                       ws, stream=None) -> None:
+    """Prefill indexer: Q queries of slot `seq`, query q sees entries [0, n_visible[q])."""
+    _ok(lib().csa2_index_topk_prefill(ctypes.byref(planes.c), seq, Q, _ptr(n_visible), n_max, _ptr(qidx),
+                                      _ptr(w), k, _ptr(topk_out), _ptr(ws), _nbytes(ws), _stream(stream)),
+        "csa2_index_topk_prefill")
 
 
 NOALLOC_SCRATCH_BYTES = 32 << 20

@@ -700,6 +700,57 @@ __global__ void __launch_bounds__(256) k_pool_gather(const uint8_t* __restrict__
 
 }  // namespace csa2
 
+namespace csa2 {
+namespace {
+// Prefill indexer: queries per scan launch, so that their fp32 scores fit in
+// about 1 GB of workspace (at least one query, at most all of them).
+constexpr int64_t kPrefillScoreBytes = (int64_t)1 << 30;
+int64_t prefill_batch(int32_t Q, int64_t n_max) {
+  const int64_t cols = (int64_t)align_up((size_t)std::max<int64_t>(n_max, 1), 64);
+  return std::max<int64_t>(1, std::min<int64_t>(Q, kPrefillScoreBytes / (cols * 4)));
+}
+size_t prefill_ws_bytes(int32_t Q, int64_t n_max) {
+  const int64_t cols = (int64_t)align_up((size_t)std::max<int64_t>(n_max, 1), 64);
+  return kWsHeader + align_up((size_t)prefill_batch(Q, n_max) * cols * 4, 256);
+}
+}  // namespace
+}  // namespace csa2
+
+extern "C" size_t csa2_index_topk_prefill_workspace_size(int32_t Q, int64_t n_max, int32_t k) {
+  (void)k;
+  if (Q <= 0 || n_max < 0) return 0;
+  return csa2::prefill_ws_bytes(Q, n_max);
+}
+
+extern "C" csa2_status csa2_index_topk_prefill(const csa2_kv_planes* kv, int32_t seq, int32_t Q,
+                                               const int32_t* n_visible, int64_t n_max, const void* qidx_bf16,
+                                               const float* w, int32_t k, int32_t* topk_out, void* ws,
+                                               size_t ws_bytes, csa2_stream stream) {
+  using namespace csa2;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (!planes_ok(kv) || seq < 0 || Q <= 0 || !n_visible || !qidx_bf16 || !w || !topk_out)
+    return CSA2_ERR_INVALID_ARG;
+  if (k < 1 || k > CSA2_MAX_TOPK || n_max < 0 || n_max > kv->seq_stride || n_max >= ((int64_t)1 << 31))
+    return CSA2_ERR_INVALID_ARG;
+  if (!aligned(qidx_bf16, 16) || !aligned(w, 16)) return CSA2_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256)) return CSA2_ERR_WORKSPACE;
+  if (ws_bytes < prefill_ws_bytes(Q, n_max)) return CSA2_ERR_WORKSPACE;
+  if (reset_error(ws, st) != CSA2_OK) return CSA2_ERR_CUDA;
+  const int64_t qb = prefill_batch(Q, n_max);
+  const int64_t cols = (int64_t)align_up((size_t)std::max<int64_t>(n_max, 1), 64);
+  float* scores = (float*)((char*)ws + kWsHeader);
+  const uint16_t* q = (const uint16_t*)qidx_bf16;
+  for (int64_t q0 = 0; q0 < Q; q0 += qb) {
+    const int32_t nb = (int32_t)std::min<int64_t>(qb, Q - q0);
+    csa2_status rs = launch_scan(kv, nb, n_visible + q0, n_max, n_max, q + q0 * kHIdx * kDIdx, w + q0 * kHIdx,
+                                 nullptr, 0, scores, cols, nullptr, 0, ws, st, seq);
+    if (rs != CSA2_OK) return rs;
+    SelectArgs a{scores, cols, n_visible + q0, nullptr, 0, 0, 0, k, topk_out + q0 * k, k, n_max};
+    launch_select(a, nb, st);
+  }
+  return launch_status();
+}
+
 extern "C" size_t csa2_index_topk_workspace_size(int32_t B, int64_t n_max, int32_t k, int32_t block,
                                                  int32_t n_blocks_keep) {
   (void)k;

@@ -108,6 +108,7 @@ struct ScanParams {
   float* bmax;
   int64_t bmax_stride;
   void* ws;
+  int shared_slot;  // >= 0: every query reads this sequence slot (prefill); else query b reads slot b
 };
 
 __device__ __forceinline__ void scan_abort(ScanSmem& S, void* ws, int where) {
@@ -198,8 +199,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int64_t t_begin = ntiles * blockIdx.x / p.ctas_per_query;
   const int64_t t_end = ntiles * (blockIdx.x + 1) / p.ctas_per_query;
   const int my_tiles = (int)(t_end - t_begin);
-  const bool scale_bulk = ((b * p.seq_stride) & 3) == 0;  // 16-byte aligned scale rows
-  const uint8_t* scales_b = p.ix_scales + (int64_t)b * p.seq_stride * 4;
+  const int64_t srow = (int64_t)(p.shared_slot >= 0 ? p.shared_slot : b) * p.seq_stride;  // slot's first row
+  const bool scale_bulk = (srow & 3) == 0;  // 16-byte aligned scale rows
+  const uint8_t* scales_b = p.ix_scales + srow * 4;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -283,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             ptx::mbar_arrive_expect_tx(&S.sfull[s], cnt4 * 4u);
             if (cnt4) ptx::bulk_g2s_hint(S.scales[s], scales_b + j0 * 4, cnt4 * 4u, &S.sfull[s], pol);
             ptx::mbar_arrive_expect_tx(&S.full[s], kCodeBytes);
-            ptx::tma_load_2d_hint(S.codes[s], &map_tile, 0, (int)(b * p.seq_stride + j0), &S.full[s], pol);
+            ptx::tma_load_2d_hint(S.codes[s], &map_tile, 0, (int)(srow + j0), &S.full[s], pol);
           } else {
             int pbv[16];
             uint32_t cnt[16];
@@ -308,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int u = 0; u < 16; ++u) {
               if (!cnt[u]) continue;
               const int64_t base = (int64_t)pbv[u] * 8;
-              ptx::tma_load_2d(S.codes[s] + u * 1024, &map_block, 0, (int)(b * p.seq_stride + base),
+              ptx::tma_load_2d(S.codes[s] + u * 1024, &map_block, 0, (int)(srow + base),
                                &S.full[s]);
             }
           }
@@ -509,9 +511,9 @@ bool make_code_map(CUtensorMap* map, const uint8_t* codes, int64_t rows, uint32_
 csa2_status launch_scan(const csa2_kv_planes* kv, int32_t B, const int32_t* n_entries, int64_t n_max,
                         int64_t ncand_max, const uint16_t* q, const float* w, const int32_t* pool,
                         int keep, float* scores, int64_t score_stride, float* bmax, int64_t bmax_stride,
-                        void* ws, cudaStream_t st) {
+                        void* ws, cudaStream_t st, int shared_slot) {
   if (ncand_max <= 0) return CSA2_OK;
-  const int64_t rows = (int64_t)B * kv->seq_stride;
+  const int64_t rows = (int64_t)(shared_slot >= 0 ? shared_slot + 1 : B) * kv->seq_stride;
   if (rows >= ((int64_t)1 << 31)) return CSA2_ERR_UNSUPPORTED;
   if (!aligned(kv->ix_codes, 32)) return CSA2_ERR_INVALID_ARG;  // packed 4-bit tensor loads
   CUtensorMap map_tile, map_block;
@@ -527,7 +529,7 @@ csa2_status launch_scan(const csa2_kv_planes* kv, int32_t B, const int32_t* n_en
   const int64_t tiles = cdiv(ncand_max, kTile);
   const int S = choose_ctas_per_query(tiles, B, 2 * sms);
   ScanParams p{kv->ix_codes, kv->ix_scales, kv->seq_stride, n_entries, n_max, q, w, pool, keep,
-               ncand_max, S, scores, score_stride, bmax, bmax_stride, ws};
+               ncand_max, S, scores, score_stride, bmax, bmax_stride, ws, shared_slot};
   KernelTimer timer("k_scan_tc", st);
   k_scan_tc<<<dim3((unsigned)S, (unsigned)B), kThreads, smem, st>>>(p, map_tile, map_block);
   return cudaGetLastError() == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;

@@ -22,6 +22,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn();
 csa2_status launch_scan(const csa2_kv_planes* kv, int32_t B, const int32_t* n_entries, int64_t n_max,
                         int64_t ncand_max, const uint16_t* q, const float* w, const int32_t* pool,
                         int keep, float* scores, int64_t score_stride, float* bmax, int64_t bmax_stride,
-                        void* ws, cudaStream_t st);
+                        void* ws, cudaStream_t st, int shared_slot = -1);
 
 }  // namespace csa2

@@ -248,6 +248,23 @@ size_t csa2_index_topk_workspace_size(int32_t B, int64_t n_max, int32_t k, int32
  *  - Device-side error reports go to the array's error word and are not
  *    readable through csa2_check; results equal csa2_index_topk's. */
 #define CSA2_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* Prefill (encoder) indexer: Q queries of one sequence slot `seq` score its entries
+ * with the same score and selection rules, query q seeing entries [0, n_visible[q])
+ * (its causal bound: the caller counts the entries whose m tokens all precede it),
+ * and each keeps its top-k ids (ascending, -1 padded).  This is the O(N^2) indexer
+ * work of prefill ("DeepSeek-V4.1-Flash course, 04", decode-cost discussion: the
+ * encoder's prefill indexer stays O(N^2), about 3072 N^2 multiply-adds over 3 Full
+ * layers).  Every query streams the slot's keys (68 bytes per entry; after the
+ * first query they come from L2 when the slot fits).  Queries run in batches whose
+ * fp32 scores take about 1 GB of workspace.
+ *   qidx [Q][32][128] bf16; w [Q][32] fp32; n_visible [Q] int32 (device);
+ *   topk_out [Q][k] int32. */
+csa2_status csa2_index_topk_prefill(const csa2_kv_planes* kv, int32_t seq, int32_t Q,
+                                    const int32_t* n_visible, int64_t n_max, const void* qidx_bf16,
+                                    const float* w, int32_t k, int32_t* topk_out, void* ws,
+                                    size_t ws_bytes, csa2_stream stream);
+size_t csa2_index_topk_prefill_workspace_size(int32_t Q, int64_t n_max, int32_t k);
 csa2_status csa2_index_topk_noalloc(const csa2_kv_planes* kv, int32_t B, const int32_t* n_entries,
                                     int64_t n_max, const void* qidx_bf16, const float* w, int32_t k,
                                     csa2_topk_mode mode, int32_t block, int32_t n_blocks_keep,

@@ -166,3 +166,46 @@ def test_mxfp4_query(cache, oracle_mod):
         s = oracle_mod.index_scores(ixc, ixs, got[b], w[b], n=n)
         assert np.allclose(scores[b, :n], s, rtol=2e-5, atol=2e-5 * np.abs(s).max())
         check_topk(topk[b], s, 512, what=f"mxfp4-q[{b}]")
+
+
+def _prefill(planes, seq, q, w, n_vis, n_max, k=512):
+    Q = q.shape[0]
+    topk = torch.empty((Q, k), dtype=torch.int32, device="cuda")
+    ws = csa2.workspace(csa2.index_topk_prefill_workspace_size(Q, n_max, k))
+    csa2.index_topk_prefill(planes, seq, Q, to_dev(n_vis), n_max, to_dev(q.view(np.int16)), to_dev(w), k, topk, ws)
+    assert csa2.check(ws)[0] == 0
+    return topk.cpu().numpy()
+
+
+def test_prefill_indexer_shared_slot(cache, oracle_mod):
+    """Q queries of one slot, each with its own causal bound: every query's top-512 is the
+    oracle's top-512 of that query over entries [0, n_visible)."""
+    c, _, _ = cache
+    Q, seq = 40, 1
+    q, w = W.index_query(4, 0, Q)
+    rng = np.random.default_rng(2)
+    n_vis = np.concatenate([[0, 1, 7, 513, 4133], rng.integers(0, 4134, Q - 5)]).astype(np.int32)
+    topk = _prefill(c.planes, seq, q, w, n_vis, c.n_max)
+    _, _, ixc, ixs = c.oracle_slot(seq)
+    for i in range(Q):
+        s = oracle_mod.index_scores(ixc, ixs, q[i], w[i], n=int(n_vis[i])) if n_vis[i] else np.zeros(0)
+        check_topk(topk[i], s, 512, what=f"prefill[{i}]")
+
+
+def test_prefill_indexer_batches(cache, oracle_mod):
+    """A 2^24-entry bound makes the scores of only 16 queries fit the workspace's 1 GB, so
+    40 queries run in three launches (the visible entries are the cache's first 4,133)."""
+    c, _, _ = cache
+    Q, stride = 40, 1 << 24
+    big = csa2.Planes.empty(1, stride)
+    src = c.gpu_slot(0)
+    for t, a in zip((big.kv_codes, big.kv_scales, big.ix_codes, big.ix_scales), src):
+        t[:a.shape[0]] = torch.from_numpy(a).to(t.device)
+    q, w = W.index_query(5, 0, Q)
+    n_vis = np.random.default_rng(3).integers(1, 4134, Q).astype(np.int32)
+    assert csa2.index_topk_prefill_workspace_size(Q, stride, 512) < 2 * (1 << 30)
+    topk = _prefill(big, 0, q, w, n_vis, stride)
+    _, _, ixc, ixs = c.oracle_slot(0)
+    for i in range(Q):
+        s = oracle_mod.index_scores(ixc, ixs, q[i], w[i], n=int(n_vis[i]))
+        check_topk(topk[i], s, 512, what=f"prefill-batched[{i}]")
