@@ -25,7 +25,8 @@ D_MAIN, D_IDX, H_IDX, H_ATT = 512, 128, 32, 64
 def _load():
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB):
+        src = os.path.join(os.path.dirname(LIB), "csa2_oracle.c")
+        if not os.path.exists(LIB) or os.path.getmtime(LIB) < os.path.getmtime(src):
             from . import build as _b
 
             _b.build()
@@ -81,6 +82,17 @@ def _load():
         lib.o_rope.restype = None
         lib.o_swa_row.argtypes = [vp, vp, f64, ctypes.c_int, f64, f64, vp, vp]
         lib.o_swa_row.restype = None
+        lib.o_project.argtypes = [vp, i64, ctypes.c_int, vp, vp, ctypes.c_int]
+        lib.o_project.restype = None
+        lib.o_pool_overlap.argtypes = [vp, vp, vp, vp, vp, vp, i64, ctypes.c_int, ctypes.c_int, vp]
+        lib.o_pool_overlap.restype = None
+        lib.o_pool_bias.argtypes = [vp, vp, vp, i64, ctypes.c_int, ctypes.c_int, vp]
+        lib.o_pool_bias.restype = None
+        lib.o_compress_overlap.argtypes = [vp, i64, ctypes.c_int, vp, vp, vp, vp, vp, vp, ctypes.c_int, vp,
+                                           ctypes.c_int]
+        lib.o_compress_overlap.restype = ctypes.c_int
+        lib.o_compress_hca.argtypes = [vp, i64, ctypes.c_int, vp, vp, vp, ctypes.c_int, vp, ctypes.c_int]
+        lib.o_compress_hca.restype = ctypes.c_int
         lib.o_e2m1_encode_array.argtypes = [vp, i64, vp]
         lib.o_e2m1_encode_array.restype = None
         lib.o_e4m3_encode_array.argtypes = [vp, i64, vp]
@@ -233,6 +245,74 @@ def pool(C: np.ndarray, Z: np.ndarray, m: int) -> np.ndarray:
     T, width = C.shape
     out = np.empty((T // m, width), np.float64)
     _load().o_pool(_p(C), _p(Z), T, width, m, _p(out))
+    return out
+
+
+# ----------------------------------------------------------------------------- V4 compressors
+
+def _u16(a):
+    return np.ascontiguousarray(a, np.uint16)
+
+
+def _f32(a):
+    return np.ascontiguousarray(a, np.float32)
+
+
+def project(H: np.ndarray, W: np.ndarray) -> np.ndarray:
+    """H bf16 bits [T,d] times W bf16 bits [d,512], fp64 sums: [T,512]."""
+    H = _u16(H)
+    T, d = H.shape
+    out = np.empty((T, D_MAIN), np.float64)
+    _load().o_project(_p(H), T, d, _p(_u16(W)), _p(out), _threads())
+    return out
+
+
+def pool_overlap(Ca, Za, Cb, Zb, Ba, Bb, m: int) -> np.ndarray:
+    """Two-path overlapping pool ("DeepSeek-V4 ...", CSA step 1): entry i takes
+    rows [m i, m i + m) of (Ca, Za + Ba) and rows [m (i-1), m i) of (Cb, Zb + Bb),
+    one per-channel softmax over the 2m scores; entry 0 only the first part.
+    C*, Z* fp64 [T,width]; B* fp32 [m,width]."""
+    Ca, Za, Cb, Zb = (np.ascontiguousarray(a, np.float64) for a in (Ca, Za, Cb, Zb))
+    T, width = Ca.shape
+    Ba, Bb = _f32(Ba), _f32(Bb)
+    assert Ba.shape == (m, width) and Bb.shape == (m, width) and T % m == 0
+    out = np.empty((T // m, width), np.float64)
+    _load().o_pool_overlap(_p(Ca), _p(Za), _p(Cb), _p(Zb), _p(Ba), _p(Bb), T, width, m, _p(out))
+    return out
+
+
+def pool_bias(C, Z, Bp, m: int) -> np.ndarray:
+    """HCA pool: entry i = per-channel softmax over rows [m i, m i + m) of Z + B."""
+    C, Z = (np.ascontiguousarray(a, np.float64) for a in (C, Z))
+    T, width = C.shape
+    Bp = _f32(Bp)
+    assert Bp.shape == (m, width) and T % m == 0
+    out = np.empty((T // m, width), np.float64)
+    _load().o_pool_bias(_p(C), _p(Z), _p(Bp), T, width, m, _p(out))
+    return out
+
+
+def compress_overlap(H, Wa_kv, Wb_kv, Wa_z, Wb_z, Ba, Bb, m: int) -> np.ndarray:
+    """CSA step 1 end to end: [T/m, 512] fp64 compressed entries of H."""
+    H = _u16(H)
+    T, d = H.shape
+    out = np.empty((T // m if m > 0 else 0, D_MAIN), np.float64)
+    rc = _load().o_compress_overlap(_p(H), T, d, _p(_u16(Wa_kv)), _p(_u16(Wb_kv)), _p(_u16(Wa_z)),
+                                    _p(_u16(Wb_z)), _p(_f32(Ba)), _p(_f32(Bb)), m, _p(out), _threads())
+    if rc != 0:
+        raise ValueError("oracle compress_overlap: bad arguments")
+    return out
+
+
+def compress_hca(H, Wkv, Wz, Bp, m: int) -> np.ndarray:
+    """HCA compressor end to end: [T/m, 512] fp64 compressed entries of H."""
+    H = _u16(H)
+    T, d = H.shape
+    out = np.empty((T // m if m > 0 else 0, D_MAIN), np.float64)
+    rc = _load().o_compress_hca(_p(H), T, d, _p(_u16(Wkv)), _p(_u16(Wz)), _p(_f32(Bp)), m, _p(out),
+                                _threads())
+    if rc != 0:
+        raise ValueError("oracle compress_hca: bad arguments")
     return out
 
 

@@ -10,8 +10,9 @@
  *   [CRS]  "DeepSeek-V4.1-Flash course, 02 Architecture", section 2.2 Eq. (1),
  *          2.3 CSA2, 2.3.1, 2.3.2 (Fig. 5), 2.4.4 FP4 main KV cache.
  *   [V4]   "DeepSeek-V4: Towards Highly Efficient Million-Token Context
- *          Intelligence", CSA step 2 (lightning indexer, top-k) and step 3
- *          (shared-KV MQA), sliding-window branch.
+ *          Intelligence", CSA step 1 (two-path overlapping compressor), step 2
+ *          (lightning indexer, top-k) and step 3 (shared-KV MQA), the
+ *          sliding-window branch, and HCA (m' tokens per entry, dense).
  *
  * Only the tests, the smoke check and the benchmark's CPU-baseline leg may load
  * this library.  It shares no code with the CUDA library: nothing here is
@@ -454,6 +455,158 @@ void o_pool(const double* C, const double* Z, int64_t T, int width, int m, doubl
       }
       out[j * width + c] = num / den;
     }
+}
+
+/* ========================================================================== */
+/* V4 compressors ([V4] CSA step 1: two paths with overlapping blocks; HCA:   */
+/* one path, m' tokens per entry).  Position biases B join the scores before  */
+/* the per-channel softmax over the rows an entry draws from.                */
+/* ========================================================================== */
+
+typedef struct {
+  const uint16_t *H, *W;
+  int64_t r_lo, r_hi;
+  int d;
+  double* out;
+} proj_job;
+
+static void* project_worker(void* p) {
+  const proj_job* jb = (const proj_job*)p;
+  int d = jb->d;
+  double* W = (double*)malloc(sizeof(double) * (size_t)d * D_MAIN);
+  for (int64_t i = 0; i < (int64_t)d * D_MAIN; ++i) W[i] = bf16_value(jb->W[i]);
+  for (int64_t r = jb->r_lo; r < jb->r_hi; ++r) {
+    double* o = jb->out + r * D_MAIN;
+    for (int c = 0; c < D_MAIN; ++c) o[c] = 0.0;
+    for (int k = 0; k < d; ++k) {
+      double hv = bf16_value(jb->H[r * d + k]);
+      if (hv == 0.0) continue;
+      const double* wk = W + (size_t)k * D_MAIN;
+      for (int c = 0; c < D_MAIN; ++c) o[c] += hv * wk[c];
+    }
+  }
+  free(W);
+  return NULL;
+}
+
+/* out [T][512] = H [T][d] W [d][512], bf16 operands, fp64 sums */
+void o_project(const uint16_t* H, int64_t T, int d, const uint16_t* W, double* out, int nthreads) {
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 128) nthreads = 128;
+  if (nthreads > T) nthreads = (int)(T > 0 ? T : 1);
+  pthread_t th[128];
+  proj_job jobs[128];
+  int64_t per = (T + nthreads - 1) / nthreads;
+  for (int t = 0; t < nthreads; ++t) {
+    proj_job jb = {H, W, (int64_t)t * per, (int64_t)(t + 1) * per, d, out};
+    if (jb.r_hi > T) jb.r_hi = T;
+    if (jb.r_lo > T) jb.r_lo = T;
+    jobs[t] = jb;
+  }
+  for (int t = 0; t < nthreads; ++t) pthread_create(&th[t], NULL, project_worker, &jobs[t]);
+  for (int t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+}
+
+/* Overlapping pool.  Entry i draws from rows m i .. m i + m - 1 of path a
+ * (scores Za + Ba[r]) and rows m (i - 1) .. m i - 1 of path b (scores
+ * Zb + Bb[r]); per channel the 2m scores go through one softmax and weight
+ * their rows of Ca / Cb.  Entry 0 has no previous block: its path-b rows count
+ * as score -inf and value 0, i.e. they drop out.  C*, Z* fp64 [T][width];
+ * B* fp32 [m][width]; out [T/m][width]. */
+void o_pool_overlap(const double* Ca, const double* Za, const double* Cb, const double* Zb,
+                    const float* Ba, const float* Bb, int64_t T, int width, int m, double* out) {
+  for (int64_t i = 0; i < T / m; ++i)
+    for (int c = 0; c < width; ++c) {
+      double zmax = -INFINITY;
+      for (int r = 0; r < m; ++r) {
+        double z = Za[(i * m + r) * width + c] + (double)Ba[r * width + c];
+        if (z > zmax) zmax = z;
+      }
+      if (i > 0)
+        for (int r = 0; r < m; ++r) {
+          double z = Zb[((i - 1) * m + r) * width + c] + (double)Bb[r * width + c];
+          if (z > zmax) zmax = z;
+        }
+      double num = 0.0, den = 0.0;
+      for (int r = 0; r < m; ++r) {
+        int64_t row = (i * m + r) * width + c;
+        double e = exp(Za[row] + (double)Ba[r * width + c] - zmax);
+        num += e * Ca[row];
+        den += e;
+      }
+      if (i > 0)
+        for (int r = 0; r < m; ++r) {
+          int64_t row = ((i - 1) * m + r) * width + c;
+          double e = exp(Zb[row] + (double)Bb[r * width + c] - zmax);
+          num += e * Cb[row];
+          den += e;
+        }
+      out[i * width + c] = num / den;
+    }
+}
+
+/* HCA pool: entry i = per-channel softmax over rows m i .. m i + m - 1 of
+ * Z + B[r], weighting the same rows of C. */
+void o_pool_bias(const double* C, const double* Z, const float* Bp, int64_t T, int width, int m,
+                 double* out) {
+  for (int64_t i = 0; i < T / m; ++i)
+    for (int c = 0; c < width; ++c) {
+      double zmax = -INFINITY;
+      for (int r = 0; r < m; ++r) {
+        double z = Z[(i * m + r) * width + c] + (double)Bp[r * width + c];
+        if (z > zmax) zmax = z;
+      }
+      double num = 0.0, den = 0.0;
+      for (int r = 0; r < m; ++r) {
+        int64_t row = (i * m + r) * width + c;
+        double e = exp(Z[row] + (double)Bp[r * width + c] - zmax);
+        num += e * C[row];
+        den += e;
+      }
+      out[i * width + c] = num / den;
+    }
+}
+
+/* The two compressors end to end: projections of H, then the pool.  Returns 1
+ * when T is not a multiple of m (or an allocation fails). */
+int o_compress_overlap(const uint16_t* H, int64_t T, int d, const uint16_t* Wa_kv, const uint16_t* Wb_kv,
+                       const uint16_t* Wa_z, const uint16_t* Wb_z, const float* Ba, const float* Bb, int m,
+                       double* out, int nthreads) {
+  if (m < 1 || d < 1 || T < 0 || T % m != 0) return 1;
+  size_t sz = sizeof(double) * (size_t)(T > 0 ? T : 1) * D_MAIN;
+  double *Ca = (double*)malloc(sz), *Za = (double*)malloc(sz), *Cb = (double*)malloc(sz),
+         *Zb = (double*)malloc(sz);
+  int rc = 1;
+  if (Ca && Za && Cb && Zb) {
+    o_project(H, T, d, Wa_kv, Ca, nthreads);
+    o_project(H, T, d, Wa_z, Za, nthreads);
+    o_project(H, T, d, Wb_kv, Cb, nthreads);
+    o_project(H, T, d, Wb_z, Zb, nthreads);
+    o_pool_overlap(Ca, Za, Cb, Zb, Ba, Bb, T, D_MAIN, m, out);
+    rc = 0;
+  }
+  free(Ca);
+  free(Za);
+  free(Cb);
+  free(Zb);
+  return rc;
+}
+
+int o_compress_hca(const uint16_t* H, int64_t T, int d, const uint16_t* Wkv, const uint16_t* Wz,
+                   const float* Bp, int m, double* out, int nthreads) {
+  if (m < 1 || d < 1 || T < 0 || T % m != 0) return 1;
+  size_t sz = sizeof(double) * (size_t)(T > 0 ? T : 1) * D_MAIN;
+  double *C = (double*)malloc(sz), *Z = (double*)malloc(sz);
+  int rc = 1;
+  if (C && Z) {
+    o_project(H, T, d, Wkv, C, nthreads);
+    o_project(H, T, d, Wz, Z, nthreads);
+    o_pool_bias(C, Z, Bp, T, D_MAIN, m, out);
+    rc = 0;
+  }
+  free(C);
+  free(Z);
+  return rc;
 }
 
 /* ========================================================================== */

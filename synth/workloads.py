@@ -15,6 +15,8 @@ Tensor ids (the generator's stream id per role):
     attention query q of layer l ..................... 6 + 64*l
     sliding-window rows of layer l ................... 7 + 64*l
     cache-write H, W_KV, W_Z, W_IK ................... 8, 9, 10, 11
+    V4 two-path compressor W_aKV, W_bKV, W_aZ, W_bZ .. 12, 13, 14, 15
+    V4 position biases B^a, B^b, HCA B ............... 16, 17, 18
 Seeds: workload c uses seed c.
 """
 from __future__ import annotations
@@ -160,3 +162,27 @@ def cache_write_inputs(seed: int, T: int, d_model: int, t0: int = 0):
     sk = np.float32(1.0 / math.sqrt(D_MAIN))
     Wik = normal_bf16(seed, TID_WIK, D_MAIN * D_IDX, scale=float(sk)).reshape(D_MAIN, D_IDX)
     return H, Wkv, Wz, Wik
+
+
+TID_WA_KV, TID_WB_KV, TID_WA_Z, TID_WB_Z = 12, 13, 14, 15
+TID_BA, TID_BB, TID_BHCA = 16, 17, 18
+BIAS_SD = 0.5     # position-bias draw N(0, 0.5^2)
+
+
+def overlap_compressor_inputs(seed: int, T: int, d_model: int, m: int, t0: int = 0):
+    """H bf16 [T,d] ~ N(0,1); W_aKV, W_bKV, W_aZ, W_bZ bf16 [d,512] ~ N(0,1/d);
+    B^a, B^b fp32 [m,512] ~ N(0, 0.5^2)."""
+    H = normal_bf16(seed, TID_H, T * d_model, offset=t0 * d_model).reshape(T, d_model)
+    sd = float(np.float32(1.0 / math.sqrt(d_model)))
+    Ws = [normal_bf16(seed, t, d_model * D_MAIN, scale=sd).reshape(d_model, D_MAIN)
+          for t in (TID_WA_KV, TID_WB_KV, TID_WA_Z, TID_WB_Z)]
+    Ba = normal_f32(seed, TID_BA, m * D_MAIN, scale=BIAS_SD).reshape(m, D_MAIN)
+    Bb = normal_f32(seed, TID_BB, m * D_MAIN, scale=BIAS_SD).reshape(m, D_MAIN)
+    return (H, *Ws, Ba, Bb)
+
+
+def hca_compressor_inputs(seed: int, T: int, d_model: int, m: int, t0: int = 0):
+    """H bf16 [T,d] ~ N(0,1); W_KV, W_Z bf16 [d,512] ~ N(0,1/d); B fp32 [m,512] ~ N(0, 0.5^2)."""
+    H, Wkv, Wz, _ = cache_write_inputs(seed, T, d_model, t0)
+    Bp = normal_f32(seed, TID_BHCA, m * D_MAIN, scale=BIAS_SD).reshape(m, D_MAIN)
+    return H, Wkv, Wz, Bp
