@@ -513,6 +513,129 @@ def run_prefill_index(dev, st, calls: int, warmup: int):
     }
 
 
+V4_T, V4_D, V4_M, V4_MH, V4_SEED = 65536, 4096, 4, 128, 7
+V4_B, V4_N = 32, 8192
+V4_WORKLOAD = ("V4 compressors on a prefill chunk of T=65,536 tokens x d_model 4096: the two-path "
+               "overlapping CSA compressor at m=4 (16,384 entries) and the HCA compressor at m'=128 "
+               "(512 entries); HCA dense decode attention: batch 32, every one of 8,192 entries "
+               "(a 1,048,576-token context at m'=128) + 128 window rows")
+
+
+def run_v4(dev, st, calls: int, warmup: int):
+    """The V4 compressor variants (csa2_compress_overlap, csa2_compress_hca) and the HCA
+    dense attention (csa2_dense_attn_decode) on seeded device inputs."""
+    import torch
+
+    import compressed_sparse_attention_nvfp4_gb300 as csa2
+    import synth
+    from compressed_sparse_attention_nvfp4_gb300 import workload as WL
+    from synth import workloads as W
+
+    T, d, m, mh = V4_T, V4_D, V4_M, V4_MH
+    ss = st.cuda_stream
+    sd = 1.0 / math.sqrt(d)
+    H = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    synth.dev_normal_bf16(V4_SEED, W.TID_H, T * d, H.data_ptr(), ss)
+    Ws = {}
+    for name, tid in (("a_kv", W.TID_WA_KV), ("b_kv", W.TID_WB_KV), ("a_z", W.TID_WA_Z), ("b_z", W.TID_WB_Z),
+                      ("kv", W.TID_WKV), ("z", W.TID_WZ)):
+        Ws[name] = torch.empty((d, 512), dtype=torch.bfloat16, device=dev)
+        synth.dev_normal_bf16(V4_SEED, tid, d * 512, Ws[name].data_ptr(), ss, scale=sd)
+    Bs = {}
+    for name, tid, rows in (("a", W.TID_BA, m), ("b", W.TID_BB, m), ("h", W.TID_BHCA, mh)):
+        Bs[name] = torch.empty((rows, 512), dtype=torch.float32, device=dev)
+        synth.dev_normal_f32(V4_SEED, tid, rows * 512, Bs[name].data_ptr(), ss, scale=W.BIAS_SD)
+    out_o = torch.empty((T // m, 512), dtype=torch.float32, device=dev)
+    out_h = torch.empty((T // mh, 512), dtype=torch.float32, device=dev)
+    ws = csa2.workspace(csa2.compress_workspace_size(T, d), dev)
+    torch.cuda.synchronize()
+
+    def overlap():
+        csa2.compress_overlap(H, T, d, Ws["a_kv"], Ws["b_kv"], Ws["a_z"], Ws["b_z"], Bs["a"], Bs["b"], m, out_o,
+                              ws, stream=st)
+
+    def hca():
+        csa2.compress_hca(H, T, d, Ws["kv"], Ws["z"], Bs["h"], mh, out_h, ws, stream=st)
+
+    def timed(fn, n):
+        for _ in range(warmup):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(st)
+        for _ in range(n):
+            fn()
+        b.record(st)
+        torch.cuda.synchronize()
+        csa2.timing_enable(True)
+        fn()
+        torch.cuda.synchronize()
+        kt = csa2.kernel_times()
+        csa2.timing_enable(False)
+        return a.elapsed_time(b) / n, kt
+
+    peak, kind = tensor_peak()
+    hbm, hkind = peaks()
+    res = {"workload": V4_WORKLOAD}
+    for name, fn, paths, pool_kernel, mm in (("compress_overlap", overlap, 2, "k_pool_overlap", m),
+                                            ("compress_hca", hca, 1, "k_pool_bias", mh)):
+        ms, kt = timed(fn, calls)
+        assert csa2.check(ws, st)[0] == 0
+        gemm_flop = 2.0 * T * d * 2 * 512  # one path: C and Z
+        tc_n, tc_ms = kt.get("k_cw_tc", (0, 0.0))
+        tc_avg = tc_ms / max(tc_n, 1)
+        p_n, p_ms = kt.get(pool_kernel, (0, 0.0))
+        pool_bytes = paths * 2 * T * 512 * 4 + (T // mm) * 512 * 4  # unpooled C, Z in; entries out
+        achieved = gemm_flop / (tc_avg * 1e-3) / 1e12 if tc_n else 0.0
+        res[name] = {
+            "ms_per_call": round(ms, 4), "tokens_per_s": round(T / (ms * 1e-3), 1),
+            "tflops_per_call": round(paths * gemm_flop / (ms * 1e-3) / 1e12, 1),
+            "kernels_ms_per_launch": {k: round(t / max(c, 1), 4) for k, (c, t) in sorted(kt.items())},
+            "roofline": {"kernel": "k_cw_tc (bf16 tcgen05 GEMM, unpooled C and Z out)", "bound": "tensor",
+                         "achieved": round(achieved, 1), "peak": peak, "peak_kind": kind, "unit": "TFLOP/s",
+                         "frac": round(achieved / peak, 4) if peak else None,
+                         "algorithmic_flop_per_launch": gemm_flop, "launch_ms": round(tc_avg, 4)},
+            "pool": {"kernel": pool_kernel, "algorithmic_bytes": pool_bytes,
+                     "hbm_gbs": round(pool_bytes / (p_ms / max(p_n, 1) * 1e-3) / 1e9, 1) if p_n else None,
+                     "hbm_peak": hbm, "hbm_peak_kind": hkind},
+        }
+    del H, ws, out_o, out_h, Ws
+    torch.cuda.empty_cache()
+    # HCA dense attention: every compressed entry of a 1M-token context
+    B, Nn = V4_B, V4_N
+    with torch.cuda.stream(st):
+        planes = csa2.Planes.empty(B, Nn, dev)
+        WL.fill_planes(planes, V4_SEED, 0, B, Nn, stream=st)
+        q, _ = WL.attn_query_dev(V4_SEED, 0, B, dev)
+        swa = WL.swa_dev(V4_SEED, 0, B, NSWA, dev, stream=st)
+        n_ent = torch.full((B,), Nn, dtype=torch.int32, device=dev)
+        out = torch.empty((B, 64, 512), dtype=torch.float32, device=dev)
+        lse = torch.empty((B, 64), dtype=torch.float32, device=dev)
+        wsa = csa2.workspace(csa2.dense_attn_workspace_size(B, Nn, NSWA), dev)
+    torch.cuda.synchronize()
+    scale = 1.0 / math.sqrt(512)
+
+    def dense():
+        csa2.dense_attn_decode(planes, B, n_ent, Nn, swa, NSWA, q, scale, out, wsa, lse_out=lse, stream=st)
+
+    ms, kt = timed(dense, max(calls, 20))
+    assert csa2.check(wsa, st)[0] == 0
+    att_n, att_ms = kt.get("k_attn_part", kt.get("k_attn", (0, 0.0)))
+    att_avg = att_ms / max(att_n, 1)
+    call_bytes = B * (Nn * MAIN_BYTES + NSWA * SWA_ROW + 64 * 512 * 2)
+    call_flop = B * (Nn + NSWA) * 64 * 512 * 2 * 2
+    res["hca_dense_attention"] = {
+        "ms_per_call": round(ms, 4), "queries_per_s": round(B / (ms * 1e-3), 1),
+        "kernels_ms_per_launch": {k: round(t / max(c, 1), 4) for k, (c, t) in sorted(kt.items())},
+        "k_attn": {"algorithmic_bytes": call_bytes, "flop": call_flop,
+                   "hbm_gbs": round(call_bytes / (att_avg * 1e-3) / 1e9, 1) if att_n else None,
+                   "tflops": round(call_flop / (att_avg * 1e-3) / 1e12, 1) if att_n else None,
+                   "tensor_frac": round(call_flop / (att_avg * 1e-3) / 1e12 / peak, 4) if att_n else None,
+                   "tensor_peak_kind": kind},
+    }
+    return res
+
+
 def tensor_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -703,6 +826,7 @@ def run_ours(args, rank, world, local_rank):
         line["cache_write"] = run_cache_write(dev, st, 5, 2)
         line["decode_append"] = run_append(dev, st, 20, 3)
         line["prefill_indexer"] = run_prefill_index(dev, st, 5, 2)
+        line["v4_variants"] = run_v4(dev, st, 5, 2)
     if not args.no_step40:
         del planes, ws_i, ws_a
         torch.cuda.empty_cache()
@@ -729,6 +853,8 @@ def main():
                     help="profiling case: only the prefill indexer")
     ap.add_argument("--append-only", action="store_true",
                     help="profiling case: only the decode-time cache append and window write")
+    ap.add_argument("--v4-only", action="store_true",
+                    help="profiling case: only the V4 compressors and the HCA dense attention")
     ap.add_argument("--step40-only", action="store_true",
                     help="profiling case: only the 40-layer step, printed as its own line")
     ap.add_argument("--cache-write-only", action="store_true",
@@ -821,6 +947,19 @@ def main():
         if rank == 0:
             print(json.dumps({"decode_append": run_append(dev, st, max(1, min(args.steps, 50)),
                                                           max(1, args.warmup))}), flush=True)
+        return
+    if args.v4_only:
+        import torch
+
+        torch.cuda.set_device(local_rank)
+        import compressed_sparse_attention_nvfp4_gb300 as csa2
+
+        csa2.lib()
+        dev = torch.device("cuda", local_rank)
+        st = torch.cuda.Stream(device=dev)
+        if rank == 0:
+            print(json.dumps({"v4_variants": run_v4(dev, st, max(1, min(args.steps, 20)), max(1, args.warmup))}),
+                  flush=True)
         return
     if args.cache_write_only:
         import torch

@@ -93,6 +93,12 @@ def lib() -> ctypes.CDLL:
             "csa2_sparse_attn_decode": ([pl, i32, vp, i32, vp, i32, vp, f32, nr, vp, vp, vp, vp, vp, sz,
                                          vp], ctypes.c_int),
             "csa2_sparse_attn_workspace_size": ([i32, i32, i32], sz),
+            "csa2_dense_attn_decode": ([pl, i32, vp, i64, vp, i32, vp, f32, nr, vp, vp, vp, vp, vp, sz, vp],
+                                       ctypes.c_int),
+            "csa2_dense_attn_workspace_size": ([i32, i64, i32], sz),
+            "csa2_compress_overlap": ([vp, i64, i32, vp, vp, vp, vp, vp, vp, i32, vp, vp, sz, vp], ctypes.c_int),
+            "csa2_compress_hca": ([vp, i64, i32, vp, vp, vp, i32, vp, vp, sz, vp], ctypes.c_int),
+            "csa2_compress_workspace_size": ([i64, i32], sz),
             "csa2_v41_layer_table": ([i32, vp, vp, vp, vp, vp], ctypes.c_int),
             "csa2_check": ([vp, vp, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
             "csa2_status_string": ([ctypes.c_int], ctypes.c_char_p),
@@ -280,6 +286,39 @@ def sparse_attn_decode(planes: Planes, B: int, topk, k: int, swa, n_swa: int, q,
                                       ctypes.byref(q_nr) if q_nr is not None else None, _ptr(q_pos),
                                       _ptr(sink), _ptr(out), _ptr(lse_out), _ptr(ws), _nbytes(ws),
                                       _stream(stream)), "csa2_sparse_attn_decode")
+
+
+def dense_attn_workspace_size(B: int, n_max: int, n_swa: int) -> int:
+    return lib().csa2_dense_attn_workspace_size(B, n_max, n_swa)
+
+
+def dense_attn_decode(planes: Planes, B: int, n_entries, n_max: int, swa, n_swa: int, q,
+                      softmax_scale: float, out, ws, lse_out=None, stream=None,
+                      q_nr: NormRope | None = None, q_pos=None, sink=None) -> None:
+    """HCA attention: every entry [0, n_entries[b]) of slot b plus the window rows."""
+    _ok(lib().csa2_dense_attn_decode(ctypes.byref(planes.c), B, _ptr(n_entries), n_max, _ptr(swa), n_swa,
+                                     _ptr(q), softmax_scale,
+                                     ctypes.byref(q_nr) if q_nr is not None else None, _ptr(q_pos),
+                                     _ptr(sink), _ptr(out), _ptr(lse_out), _ptr(ws), _nbytes(ws),
+                                     _stream(stream)), "csa2_dense_attn_decode")
+
+
+def compress_workspace_size(T: int, d_model: int) -> int:
+    return lib().csa2_compress_workspace_size(T, d_model)
+
+
+def compress_overlap(H, T: int, d_model: int, Wa_kv, Wb_kv, Wa_z, Wb_z, Ba, Bb, m: int, out, ws,
+                     stream=None) -> None:
+    """Two-path overlapping compressor: out fp32 [T/m][512]."""
+    _ok(lib().csa2_compress_overlap(_ptr(H), T, d_model, _ptr(Wa_kv), _ptr(Wb_kv), _ptr(Wa_z), _ptr(Wb_z),
+                                    _ptr(Ba), _ptr(Bb), m, _ptr(out), _ptr(ws), _nbytes(ws), _stream(stream)),
+        "csa2_compress_overlap")
+
+
+def compress_hca(H, T: int, d_model: int, Wkv, Wz, Bp, m: int, out, ws, stream=None) -> None:
+    """HCA compressor: out fp32 [T/m][512]."""
+    _ok(lib().csa2_compress_hca(_ptr(H), T, d_model, _ptr(Wkv), _ptr(Wz), _ptr(Bp), m, _ptr(out), _ptr(ws),
+                                _nbytes(ws), _stream(stream)), "csa2_compress_hca")
 
 
 def check(ws, stream=None) -> tuple[int, int]:

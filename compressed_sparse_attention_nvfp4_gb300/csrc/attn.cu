@@ -207,9 +207,13 @@ struct RowFetch {
   int kind;       // 0 = no row, 1 = main entry, 2 = window row
 };
 
-// topk entry of chunk row gr (rows gr >= k are window rows or padding)
-__device__ __forceinline__ int64_t fetch_index(const int32_t* __restrict__ topk, int k, int b, int gr) {
-  return gr < k ? (int64_t)topk[(int64_t)b * k + gr] : -1;
+// entry of chunk row gr (rows gr >= k are window rows or padding): topk[b][gr],
+// or, dense, entry gr itself while gr < dense_n[b]
+__device__ __forceinline__ int64_t fetch_index(const int32_t* __restrict__ topk, const int32_t* __restrict__ dense_n,
+                                               int k, int b, int gr) {
+  if (gr >= k) return -1;
+  if (dense_n) return gr < __ldg(dense_n + b) ? gr : -1;
+  return (int64_t)topk[(int64_t)b * k + gr];
 }
 
 // Starts the loads of half a row: a selected entry (gr < k, index idx), a
@@ -306,7 +310,8 @@ __device__ __forceinline__ bool dequant_half_row(AttnSmem& S, const RowFetch& f,
 template <bool kPartial, bool kEx>
 __global__ void __launch_bounds__(kAT, 1) k_attn(
     const uint8_t* __restrict__ kv_codes, const uint8_t* __restrict__ kv_scales, int64_t seq_stride,
-    const int32_t* __restrict__ topk, int k, const uint8_t* __restrict__ swa, int n_swa,
+    const int32_t* __restrict__ topk, const int32_t* __restrict__ dense_n, int k, const uint8_t* __restrict__ swa,
+    int n_swa,
     const uint16_t* __restrict__ qg, float scale, AttnExtras ex, int nchunks, int cps,
     float* __restrict__ out, float* __restrict__ lse, float* __restrict__ part_o,
     float2* __restrict__ part_ml, void* ws) {
@@ -342,7 +347,7 @@ __global__ void __launch_bounds__(kAT, 1) k_attn(
     const int gr = c0 * kRows + r;
     QFetch qf;
     fetch_q(qf, qg, b, warp, lane);
-    const int64_t idx0 = fetch_index(topk, k, b, gr);
+    const int64_t idx0 = fetch_index(topk, dense_n, k, b, gr);
     stage_q<kEx>(S, qf, scale, warp, lane, ex, b);
     ptx::fence_proxy_async_smem();
     issue_row(rf, idx0, kv_codes, kv_scales, seq_stride, swa, n_swa, k, b, gr, half, ws);
@@ -414,7 +419,7 @@ __global__ void __launch_bounds__(kAT, 1) k_attn(
       const uint32_t par = (uint32_t)(i & 1);
       // the next chunk's index, in flight during the wait and the dequantization
       const int gr_next = (c0 + i + 1) * kRows + r;
-      const int64_t idx_next = i + 1 < nc ? fetch_index(topk, k, b, gr_next) : -1;
+      const int64_t idx_next = i + 1 < nc ? fetch_index(topk, dense_n, k, b, gr_next) : -1;
       if (i > 0) {
         good = ptx::mbar_wait_warp(&S.x_free[half], par ^ 1u, abort_flag, kAttnWaitBudget);
         if (!good) break;
@@ -658,17 +663,15 @@ extern "C" size_t csa2_sparse_attn_workspace_size(int32_t B, int32_t k, int32_t 
   return csa2::attn_ws_layout(nullptr, B, csa2::attn_plan(B, k, n_swa)).bytes;
 }
 
-extern "C" csa2_status csa2_sparse_attn_decode(const csa2_kv_planes* kv, int32_t B, const int32_t* topk,
-                                               int32_t k, const uint8_t* swa_e4m3, int32_t n_swa,
-                                               const void* q_bf16, float softmax_scale,
-                                               const csa2_norm_rope* q_nr, const int64_t* q_pos,
-                                               const float* sink, float* out, float* lse_out, void* ws,
-                                               size_t ws_bytes, csa2_stream stream) {
-  using namespace csa2;
-  cudaStream_t st = (cudaStream_t)stream;
-  if (!planes_ok(kv) || B <= 0 || B > 65535 || k < 0 || k > CSA2_MAX_TOPK || n_swa < 0 || n_swa > CSA2_MAX_SWA)
-    return CSA2_ERR_INVALID_ARG;
-  if ((k > 0 && !topk) || (n_swa > 0 && !swa_e4m3) || !q_bf16 || !out) return CSA2_ERR_INVALID_ARG;
+namespace csa2 {
+namespace {
+
+// One attention call over k rows per query named by topk (or, dense_n given,
+// entries 0 .. dense_n[b] - 1) joined with n_swa window rows.
+csa2_status attn_run(const csa2_kv_planes* kv, int32_t B, const int32_t* topk, const int32_t* dense_n, int32_t k,
+                     const uint8_t* swa_e4m3, int32_t n_swa, const void* q_bf16, float softmax_scale,
+                     const csa2_norm_rope* q_nr, const int64_t* q_pos, const float* sink, float* out,
+                     float* lse_out, void* ws, size_t ws_bytes, cudaStream_t st) {
   if (!(softmax_scale > 0.0f) || softmax_scale > 3.0e38f) return CSA2_ERR_INVALID_ARG;  // positive, finite
   if (q_nr && (!norm_rope_ok(q_nr) || (q_nr->rope && !q_pos))) return CSA2_ERR_INVALID_ARG;
   if ((q_pos && !aligned(q_pos, 8)) || (sink && !aligned(sink, 4))) return CSA2_ERR_INVALID_ARG;
@@ -695,13 +698,51 @@ extern "C" csa2_status csa2_sparse_attn_decode(const csa2_kv_planes* kv, int32_t
     return CSA2_ERR_CUDA;
   {
     KernelTimer timer(partial ? "k_attn_part" : "k_attn", st);
-    kern<<<dim3(plan.nsplit, B), kAT, smem, st>>>(kv->kv_codes, kv->kv_scales, kv->seq_stride, topk, k, swa_e4m3,
-                                                   n_swa, (const uint16_t*)q_bf16, softmax_scale, ex, plan.nchunks,
-                                                   plan.cps, out, lse_out, L.part_o, L.part_ml, ws);
+    kern<<<dim3(plan.nsplit, B), kAT, smem, st>>>(kv->kv_codes, kv->kv_scales, kv->seq_stride, topk, dense_n, k,
+                                                   swa_e4m3, n_swa, (const uint16_t*)q_bf16, softmax_scale, ex,
+                                                   plan.nchunks, plan.cps, out, lse_out, L.part_o, L.part_ml, ws);
   }
   if (partial) {
     KernelTimer timer("k_attn_merge", st);
     k_attn_merge<<<B * kHAtt, 128, 0, st>>>(L.part_o, L.part_ml, plan.nsplit, sink, out, lse_out);
   }
   return launch_status();
+}
+
+}  // namespace
+}  // namespace csa2
+
+extern "C" csa2_status csa2_sparse_attn_decode(const csa2_kv_planes* kv, int32_t B, const int32_t* topk,
+                                               int32_t k, const uint8_t* swa_e4m3, int32_t n_swa,
+                                               const void* q_bf16, float softmax_scale,
+                                               const csa2_norm_rope* q_nr, const int64_t* q_pos,
+                                               const float* sink, float* out, float* lse_out, void* ws,
+                                               size_t ws_bytes, csa2_stream stream) {
+  using namespace csa2;
+  if (!planes_ok(kv) || B <= 0 || B > 65535 || k < 0 || k > CSA2_MAX_TOPK || n_swa < 0 || n_swa > CSA2_MAX_SWA)
+    return CSA2_ERR_INVALID_ARG;
+  if ((k > 0 && !topk) || (n_swa > 0 && !swa_e4m3) || !q_bf16 || !out) return CSA2_ERR_INVALID_ARG;
+  return attn_run(kv, B, topk, nullptr, k, swa_e4m3, n_swa, q_bf16, softmax_scale, q_nr, q_pos, sink, out, lse_out,
+                  ws, ws_bytes, (cudaStream_t)stream);
+}
+
+extern "C" size_t csa2_dense_attn_workspace_size(int32_t B, int64_t n_max, int32_t n_swa) {
+  if (B <= 0 || n_max < 0 || n_max > CSA2_MAX_DENSE || n_swa < 0) return 0;
+  return csa2::attn_ws_layout(nullptr, B, csa2::attn_plan(B, (int32_t)n_max, n_swa)).bytes;
+}
+
+extern "C" csa2_status csa2_dense_attn_decode(const csa2_kv_planes* kv, int32_t B, const int32_t* n_entries,
+                                              int64_t n_max, const uint8_t* swa_e4m3, int32_t n_swa,
+                                              const void* q_bf16, float softmax_scale,
+                                              const csa2_norm_rope* q_nr, const int64_t* q_pos,
+                                              const float* sink, float* out, float* lse_out, void* ws,
+                                              size_t ws_bytes, csa2_stream stream) {
+  using namespace csa2;
+  if (!planes_ok(kv) || B <= 0 || B > 65535 || n_max < 0 || n_max > CSA2_MAX_DENSE || n_max > kv->seq_stride ||
+      n_swa < 0 || n_swa > CSA2_MAX_SWA)
+    return CSA2_ERR_INVALID_ARG;
+  if ((n_max > 0 && !n_entries) || (n_swa > 0 && !swa_e4m3) || !q_bf16 || !out) return CSA2_ERR_INVALID_ARG;
+  if (n_entries && !aligned(n_entries, 4)) return CSA2_ERR_INVALID_ARG;
+  return attn_run(kv, B, nullptr, n_entries, (int32_t)n_max, swa_e4m3, n_swa, q_bf16, softmax_scale, q_nr, q_pos,
+                  sink, out, lse_out, ws, ws_bytes, (cudaStream_t)stream);
 }

@@ -170,7 +170,7 @@ __device__ __forceinline__ void tc_abort(TcSmem& S, void* ws, int where) {
 
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_cw_tc(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w, int64_t T,
-            int d, int m, float* __restrict__ cbar, void* ws) {
+            int d, int m, float* __restrict__ cbar, float* __restrict__ zout, void* ws) {
   extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
   TcSmem& S = *reinterpret_cast<TcSmem*>(tc_smem_raw);
   volatile int* abort_flag = &S.abort_flag;
@@ -305,6 +305,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           float4* dst = reinterpret_cast<float4*>(cbar + e * kDMain + ch0 + cb * 32);
 #pragma unroll
           for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          if (zout) {  // unpooled projections (m = 1): Z next to C
+            float4* zd = reinterpret_cast<float4*>(zout + e * kDMain + ch0 + cb * 32);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              zd[q] = make_float4(__uint_as_float(zr[4 * q]), __uint_as_float(zr[4 * q + 1]),
+                                  __uint_as_float(zr[4 * q + 2]), __uint_as_float(zr[4 * q + 3]));
+          }
         }
       }
       ptx::tc_fence_before();
@@ -569,7 +576,7 @@ csa2_status cw_compute(const void* H_bf16, int64_t T, int32_t d_model, const voi
     const int64_t ntiles = cdiv(T, kTcM) * (kDMain / 128);
     const int grid = (int)std::min<int64_t>(ntiles, sms);
     KernelTimer timer("k_cw_tc", st);
-    k_cw_tc<<<grid, kTcThreads, smem, st>>>(map_h, map_w, T, d_model, m, L.cbar, ws);
+    k_cw_tc<<<grid, kTcThreads, smem, st>>>(map_h, map_w, T, d_model, m, L.cbar, nullptr, ws);
   } else {
     const int smem = (int)sizeof(GemmSmem);
     if (cudaFuncSetAttribute(k_cw_gemm_pool, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
@@ -666,5 +673,167 @@ extern "C" csa2_status csa2_cache_append(const void* H_bf16, int32_t G, int32_t 
   d.pos = pos;
   d.ws = ws;
   launch_quantize(L.cbar, L.ki, G, dst, d, st, kv_nr);
+  return launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// The V4 compressors ("DeepSeek-V4: Towards Highly Efficient Million-Token
+// Context Intelligence", CSA step 1 and HCA): the projections run unpooled on
+// the tensor cores (k_cw_tc with m = 1 writes C and Z), then a pooling kernel
+// forms each entry with per-channel softmax weights that include the learned
+// position biases.
+namespace csa2 {
+namespace {
+
+// overlapping: entry i pools rows m i .. m i + m - 1 of (Ca, Za + Ba) and rows
+// m (i - 1) .. m i - 1 of (Cb, Zb + Bb); entry 0 has only the first part.  One
+// thread per (entry, channel).
+__global__ void k_pool_overlap(const float* __restrict__ Ca, const float* __restrict__ Za,
+                               const float* __restrict__ Cb, const float* __restrict__ Zb,
+                               const float* __restrict__ Ba, const float* __restrict__ Bb, int64_t n, int m,
+                               float* __restrict__ out) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= n * kDMain) return;
+  const int64_t i = t / kDMain;
+  const int c = (int)(t % kDMain);
+  float zmax = -INFINITY;
+  for (int r = 0; r < m; ++r) zmax = fmaxf(zmax, Za[(i * m + r) * kDMain + c] + Ba[r * kDMain + c]);
+  if (i > 0)
+    for (int r = 0; r < m; ++r) zmax = fmaxf(zmax, Zb[((i - 1) * m + r) * kDMain + c] + Bb[r * kDMain + c]);
+  float num = 0.0f, den = 0.0f;
+  for (int r = 0; r < m; ++r) {
+    const int64_t row = (i * m + r) * kDMain + c;
+    const float e = expf(Za[row] + Ba[r * kDMain + c] - zmax);
+    num = fmaf(e, Ca[row], num);
+    den += e;
+  }
+  if (i > 0)
+    for (int r = 0; r < m; ++r) {
+      const int64_t row = ((i - 1) * m + r) * kDMain + c;
+      const float e = expf(Zb[row] + Bb[r * kDMain + c] - zmax);
+      num = fmaf(e, Cb[row], num);
+      den += e;
+    }
+  out[t] = __fdiv_rn(num, den);
+}
+
+// HCA: entry i pools rows m i .. m i + m - 1 of (C, Z + B).
+__global__ void k_pool_bias(const float* __restrict__ C, const float* __restrict__ Z, const float* __restrict__ Bp,
+                            int64_t n, int m, float* __restrict__ out) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= n * kDMain) return;
+  const int64_t i = t / kDMain;
+  const int c = (int)(t % kDMain);
+  float zmax = -INFINITY;
+  for (int r = 0; r < m; ++r) zmax = fmaxf(zmax, Z[(i * m + r) * kDMain + c] + Bp[r * kDMain + c]);
+  float num = 0.0f, den = 0.0f;
+  for (int r = 0; r < m; ++r) {
+    const int64_t row = (i * m + r) * kDMain + c;
+    const float e = expf(Z[row] + Bp[r * kDMain + c] - zmax);
+    num = fmaf(e, C[row], num);
+    den += e;
+  }
+  out[t] = __fdiv_rn(num, den);
+}
+
+struct CmpWs {
+  float *c0, *z0, *c1, *z1;  // [T][512] each: the unpooled projections of up to two paths
+  uint16_t* wt;              // transposed weights of one path
+  size_t bytes;
+};
+CmpWs cmp_ws_layout(void* ws, int64_t T, int64_t d_model) {
+  CmpWs L{};
+  char* base = (char*)ws;
+  size_t off = kWsHeader;
+  float** f[4] = {&L.c0, &L.z0, &L.c1, &L.z1};
+  for (int i = 0; i < 4; ++i) {
+    *f[i] = (float*)(base ? base + off : nullptr);
+    off += align_up((size_t)T * kDMain * 4, 256);
+  }
+  L.wt = (uint16_t*)(base ? base + off : nullptr);
+  off += align_up((size_t)2 * kDMain * d_model * 2, 256);
+  L.bytes = off;
+  return L;
+}
+
+// C = H Wc, Z = H Wz (unpooled, fp32) on the tensor cores
+csa2_status project_raw(const void* H, int64_t T, int32_t d_model, const void* Wc, const void* Wz, float* C,
+                        float* Z, uint16_t* wt, void* ws, cudaStream_t st) {
+  {
+    KernelTimer timer("k_cw_wt", st);
+    k_cw_wt<<<dim3((unsigned)(d_model / 32), 2 * kDMain / 32), 256, 0, st>>>((const uint16_t*)Wc,
+                                                                            (const uint16_t*)Wz, d_model, wt);
+  }
+  CUtensorMap map_h, map_w;
+  if (!make_bf16_map(&map_h, H, T, d_model, kTcM) || !make_bf16_map(&map_w, wt, 2 * kDMain, d_model, kTcN))
+    return CSA2_ERR_CUDA;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CSA2_ERR_CUDA;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int smem = (int)sizeof(TcSmem);
+  if (cudaFuncSetAttribute(k_cw_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return CSA2_ERR_CUDA;
+  const int64_t ntiles = cdiv(T, kTcM) * (kDMain / 128);
+  KernelTimer timer("k_cw_tc", st);
+  k_cw_tc<<<(int)std::min<int64_t>(ntiles, sms), kTcThreads, smem, st>>>(map_h, map_w, T, d_model, 1, C, Z, ws);
+  return CSA2_OK;
+}
+
+csa2_status compress_checks(const void* H, int64_t T, int32_t d_model, int32_t m, float* out, void* ws,
+                            size_t ws_bytes, size_t need) {
+  if ((!H && T > 0) || !out || T < 0 || m < 1 || m > 1024) return CSA2_ERR_INVALID_ARG;
+  if (T % m != 0) return CSA2_ERR_UNSUPPORTED;
+  if (d_model < kTK || d_model % 64 != 0 || T >= ((int64_t)1 << 30)) return CSA2_ERR_UNSUPPORTED;
+  if (!aligned(H, 16) || !aligned(out, 16)) return CSA2_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256)) return CSA2_ERR_WORKSPACE;
+  if (ws_bytes < need) return CSA2_ERR_WORKSPACE;
+  return CSA2_OK;
+}
+
+}  // namespace
+}  // namespace csa2
+
+extern "C" size_t csa2_compress_workspace_size(int64_t T, int32_t d_model) {
+  if (T < 0 || d_model <= 0) return 0;
+  return csa2::cmp_ws_layout(nullptr, T, d_model).bytes;
+}
+
+extern "C" csa2_status csa2_compress_overlap(const void* H_bf16, int64_t T, int32_t d_model, const void* Wa_kv,
+                                             const void* Wb_kv, const void* Wa_z, const void* Wb_z, const float* Ba,
+                                             const float* Bb, int32_t m, float* out, void* ws, size_t ws_bytes,
+                                             csa2_stream stream) {
+  using namespace csa2;
+  const CmpWs L = cmp_ws_layout(ws, T, d_model);
+  csa2_status rc = compress_checks(H_bf16, T, d_model, m, out, ws, ws_bytes, L.bytes);
+  if (rc != CSA2_OK) return rc;
+  if (!Wa_kv || !Wb_kv || !Wa_z || !Wb_z || !Ba || !Bb) return CSA2_ERR_INVALID_ARG;
+  if (!aligned(Wa_kv, 16) || !aligned(Wb_kv, 16) || !aligned(Wa_z, 16) || !aligned(Wb_z, 16))
+    return CSA2_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (reset_error(ws, st) != CSA2_OK) return CSA2_ERR_CUDA;
+  if (T == 0) return CSA2_OK;
+  if ((rc = project_raw(H_bf16, T, d_model, Wa_kv, Wa_z, L.c0, L.z0, L.wt, ws, st)) != CSA2_OK) return rc;
+  if ((rc = project_raw(H_bf16, T, d_model, Wb_kv, Wb_z, L.c1, L.z1, L.wt, ws, st)) != CSA2_OK) return rc;
+  const int64_t n = T / m;
+  KernelTimer timer("k_pool_overlap", st);
+  k_pool_overlap<<<(unsigned)cdiv(n * kDMain, 256), 256, 0, st>>>(L.c0, L.z0, L.c1, L.z1, Ba, Bb, n, m, out);
+  return launch_status();
+}
+
+extern "C" csa2_status csa2_compress_hca(const void* H_bf16, int64_t T, int32_t d_model, const void* W_kv,
+                                         const void* W_z, const float* Bp, int32_t m, float* out, void* ws,
+                                         size_t ws_bytes, csa2_stream stream) {
+  using namespace csa2;
+  const CmpWs L = cmp_ws_layout(ws, T, d_model);
+  csa2_status rc = compress_checks(H_bf16, T, d_model, m, out, ws, ws_bytes, L.bytes);
+  if (rc != CSA2_OK) return rc;
+  if (!W_kv || !W_z || !Bp || !aligned(W_kv, 16) || !aligned(W_z, 16)) return CSA2_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (reset_error(ws, st) != CSA2_OK) return CSA2_ERR_CUDA;
+  if (T == 0) return CSA2_OK;
+  if ((rc = project_raw(H_bf16, T, d_model, W_kv, W_z, L.c0, L.z0, L.wt, ws, st)) != CSA2_OK) return rc;
+  const int64_t n = T / m;
+  KernelTimer timer("k_pool_bias", st);
+  k_pool_bias<<<(unsigned)cdiv(n * kDMain, 256), 256, 0, st>>>(L.c0, L.z0, Bp, n, m, out);
   return launch_status();
 }

@@ -50,6 +50,7 @@ extern "C" {
 #define CSA2_ENTRY_BYTES 356     /* 288 main + 68 indexer                      */
 #define CSA2_MAX_TOPK 2048
 #define CSA2_MAX_SWA 128
+#define CSA2_MAX_DENSE 65536
 
 typedef enum {
   CSA2_OK = 0,
@@ -191,6 +192,38 @@ csa2_status csa2_swa_append(const float* x, int32_t R, const int32_t* query, con
                             int32_t n_queries, const csa2_norm_rope* nr, uint8_t* ring, int32_t n_win,
                             csa2_stream stream);
 
+/* ------------------------------------------------------- V4 compressors */
+
+/* The V4 compressors ("DeepSeek-V4: Towards Highly Efficient Million-Token Context
+ * Intelligence", CSA step 1 and the HCA section), each writing the T/m compressed
+ * latents as fp32 out [T/m][512] (quantize them into a cache with
+ * csa2_quantize_entries).  The projections run on the tensor cores (bf16 operands,
+ * fp32 sums); the pools take, per channel, one softmax over the scores of the rows
+ * an entry draws from, position bias added.
+ *
+ * csa2_compress_overlap (CSA, two paths a and b, blocks overlapping):
+ *   C^a = H W_aKV, C^b = H W_bKV, Z^a = H W_aZ, Z^b = H W_bZ;
+ *   entry i draws from rows m i .. m i + m - 1 of path a (score Z^a + B^a[r]) and
+ *   rows m (i-1) .. m i - 1 of path b (score Z^b + B^b[r]), 2m rows in all;
+ *   entry 0 has no previous block and draws from its m path-a rows alone.
+ * csa2_compress_hca (HCA, one path, no overlap): C = H W_KV, Z = H W_Z; entry i
+ *   draws from rows m i .. m i + m - 1 (score Z + B[r]); m is m' (128 in V4).
+ *
+ *   H_bf16  [T][d_model] bf16;  W_* [d_model][512] bf16 (row-major, as in H W)
+ *   B_*     [m][512] fp32 position biases (finite)
+ *   out     [T/m][512] fp32, 16-byte aligned; H and the weights 16-byte aligned
+ * T must be a multiple of m (CSA2_ERR_UNSUPPORTED otherwise), 1 <= m <= 1024,
+ * d_model a multiple of 64 and >= 64, T < 2^30.  ws: 256-byte aligned, at least
+ * csa2_compress_workspace_size(T, d_model) bytes (the unpooled projections). */
+csa2_status csa2_compress_overlap(const void* H_bf16, int64_t T, int32_t d_model, const void* Wa_kv,
+                                  const void* Wb_kv, const void* Wa_z, const void* Wb_z, const float* Ba,
+                                  const float* Bb, int32_t m, float* out, void* ws, size_t ws_bytes,
+                                  csa2_stream stream);
+csa2_status csa2_compress_hca(const void* H_bf16, int64_t T, int32_t d_model, const void* W_kv,
+                              const void* W_z, const float* B, int32_t m, float* out, void* ws,
+                              size_t ws_bytes, csa2_stream stream);
+size_t csa2_compress_workspace_size(int64_t T, int32_t d_model);
+
 /* ---------------------------------------------------------- indexer + top-k */
 
 /* Lightning-indexer scores and top-k selection for B decode queries; query b
@@ -302,6 +335,23 @@ csa2_status csa2_sparse_attn_decode(const csa2_kv_planes* kv, int32_t B, const i
                                     const float* sink, float* out, float* lse_out, void* ws,
                                     size_t ws_bytes, csa2_stream stream);
 size_t csa2_sparse_attn_workspace_size(int32_t B, int32_t k, int32_t n_swa);
+
+/* Dense MQA decode over every compressed entry a query sees, joined with the
+ * sliding window: HCA's core attention ("DeepSeek-V4: Towards Highly Efficient
+ * Million-Token Context Intelligence", HCA section: no indexer and no top-k, the
+ * attention reads all compressed entries).  Identical to csa2_sparse_attn_decode
+ * with topk[b] = 0, 1, .., n_entries[b] - 1 (one pass, no index list):
+ *   n_entries  [B] int32 (device): entries visible to query b (slot b of kv);
+ *              values above n_max count as n_max, negative ones as 0
+ *   n_max      host bound, 0 <= n_max <= min(CSA2_MAX_DENSE, kv->seq_stride)
+ * Every other argument as in csa2_sparse_attn_decode; the workspace is
+ * csa2_dense_attn_workspace_size(B, n_max, n_swa) bytes. */
+csa2_status csa2_dense_attn_decode(const csa2_kv_planes* kv, int32_t B, const int32_t* n_entries,
+                                   int64_t n_max, const uint8_t* swa_e4m3, int32_t n_swa,
+                                   const void* q_bf16, float softmax_scale, const csa2_norm_rope* q_nr,
+                                   const int64_t* q_pos, const float* sink, float* out, float* lse_out,
+                                   void* ws, size_t ws_bytes, csa2_stream stream);
+size_t csa2_dense_attn_workspace_size(int32_t B, int64_t n_max, int32_t n_swa);
 
 /* ---------------------------------------------------------------- schedule */
 

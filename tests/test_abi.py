@@ -149,6 +149,36 @@ def test_host_validation_without_gpu(L):
                                   256, 1 << 30, None) == 1
 
 
+def test_v4_compressor_and_dense_validation_without_gpu(L):
+    fake = csa2.KVPlanes(16, 16, 16, 16, 100)
+    args = (16, 16, 16, 16, 16, 16)  # Wa_kv, Wb_kv, Wa_z, Wb_z, Ba, Bb
+    ws = csa2.compress_workspace_size(8, 64)
+    assert L.csa2_compress_overlap(16, 10, 64, *args, 4, 16, 256, ws, None) == 2      # T % m != 0
+    assert L.csa2_compress_overlap(16, 8, 96, *args, 4, 16, 256, ws, None) == 2       # d % 64 != 0
+    assert L.csa2_compress_overlap(16, 8, 64, *args, 0, 16, 256, ws, None) == 1       # m < 1
+    assert L.csa2_compress_overlap(16, 8, 64, *args, 4, None, 256, ws, None) == 1     # no output
+    assert L.csa2_compress_overlap(16, 8, 64, 16, 16, 16, 16, None, 16, 4, 16, 256, ws, None) == 1
+    assert L.csa2_compress_overlap(16, 8, 64, *args, 4, 16, 256, ws - 1, None) == 3   # workspace short
+    assert L.csa2_compress_overlap(16, 8, 64, *args, 4, 16, 128, ws, None) == 3       # misaligned ws
+    assert L.csa2_compress_hca(16, 256, 64, 16, 16, 16, 128, 16, 256, ws, None) == 3
+    assert L.csa2_compress_hca(16, 200, 64, 16, 16, 16, 128, 16, 256, 1 << 30, None) == 2
+    assert L.csa2_compress_hca(16, 256, 64, 8, 16, 16, 128, 16, 256, 1 << 30, None) == 1  # misaligned W
+    assert csa2.compress_workspace_size(65536, 4096) >= 4 * 65536 * 512 * 4
+    # dense attention: n_max beyond the slot or the limit, no counts, bad scale
+    assert L.csa2_dense_attn_decode(ctypes.byref(fake), 1, 16, 101, None, 0, 16, 0.04, None, None, None, 16,
+                                    None, 256, 1 << 30, None) == 1
+    big = csa2.KVPlanes(16, 16, 16, 16, 1 << 20)
+    assert L.csa2_dense_attn_decode(ctypes.byref(big), 1, 16, 65537, None, 0, 16, 0.04, None, None, None, 16,
+                                    None, 256, 1 << 30, None) == 1
+    assert L.csa2_dense_attn_decode(ctypes.byref(fake), 1, None, 50, None, 0, 16, 0.04, None, None, None, 16,
+                                    None, 256, 1 << 30, None) == 1
+    assert L.csa2_dense_attn_decode(ctypes.byref(fake), 1, 16, 50, None, 0, 16, -1.0, None, None, None, 16,
+                                    None, 256, 1 << 30, None) == 1
+    assert L.csa2_dense_attn_decode(ctypes.byref(fake), 1, 16, 50, None, 0, 16, 0.04, None, None, None, 16,
+                                    None, 256, 16, None) == 3
+    assert csa2.dense_attn_workspace_size(1, 8192, 128) > csa2.dense_attn_workspace_size(1, 0, 128) > 0
+
+
 def test_workspace_queries(L):
     assert csa2.index_topk_workspace_size(32, 1 << 20, 512, 8, 2048) >= 32 * (1 << 20) * 4
     assert csa2.sparse_attn_workspace_size(32, 512, 128) > 0
