@@ -85,6 +85,13 @@ class ClockSampler:
                                          stdout=self.file, stderr=subprocess.DEVNULL)
         except (FileNotFoundError, OSError):
             self.proc = None
+        # start timing only once the sampler is up: nvidia-smi's startup can hold the
+        # driver for a second or more, which would land inside a short timed region
+        t0 = time.time()
+        while self.proc and self.proc.poll() is None and time.time() - t0 < 15.0:
+            if os.path.getsize(self.file.name) > 0:
+                break
+            time.sleep(0.05)
         time.sleep(0.3)
         return self
 
