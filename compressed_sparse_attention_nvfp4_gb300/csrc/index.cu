@@ -310,8 +310,9 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
 // that one cluster barrier per pass suffices.  (A single 1024-thread CTA per
 // query for the pool's 16,384 entries measured slower than eight CTAs: the
 // load latency of one query's gather is then hidden by nothing.)
-constexpr int kResMaxPer = 64;  // candidates per thread
+constexpr int kResMaxPer = 64;  // candidates per thread (a thread's keys fit one 64-bit mask)
 constexpr int64_t kResCap = 256 * kResMaxPer;  // candidates per CTA: 64 KB of keys
+constexpr int kCompCap = 4096;  // keys of the first digit's threshold bin kept for the later passes
 
 // keys of candidates c0..c0+3 (c0 a multiple of 4; 0 = not a candidate)
 __device__ __forceinline__ uint4 load_keys4(const SelectArgs& a, int b, int64_t n, int64_t ncand, int64_t c0,
@@ -361,6 +362,8 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
   __shared__ uint32_t s_prefix, s_mask;
   __shared__ int s_need, s_shift0;
   __shared__ int s_base_eq, s_base_out;
+  __shared__ int s_ncomp;                 // keys in the compacted list (may exceed kCompCap: then unused)
+  __shared__ uint32_t comp_s[kCompCap];   // keys in the first pass's threshold bin
 
   cg::cluster_group cluster = cg::this_cluster();
   const int ncl = (int)cluster.num_blocks();
@@ -387,17 +390,43 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
     cvalid = 0;
     ckmin = 0xFFFFFFFFu;
     ckmax = 0;
+    s_ncomp = 0;
   }
   // load the run once, up to kLoadBatch slots in flight per thread
   constexpr int kLoadBatch = NT >= 1024 ? 4 : 16;  // within the register budget of NT threads
   unsigned myvalid = 0;
   uint32_t mykmin = 0xFFFFFFFFu, mykmax = 0;
+  const bool contiguous = !a.pool && vec_ok;  // candidate c's key is keys[b][c]
+  const float* krow = a.keys + (int64_t)b * a.key_stride;
   for (int v0 = 0; v0 < nslot; v0 += kLoadBatch) {
     uint4 k4[kLoadBatch];
+    if (contiguous) {  // every load of the batch in flight before any is used
+      float4 f[kLoadBatch];
 #pragma unroll
-    for (int u = 0; u < kLoadBatch; ++u) {
-      const int64_t c0 = t0 + 4 * (v0 + u);
-      k4[u] = (v0 + u < nslot && c0 < hi) ? load_keys4(a, b, n, hi, c0, vec_ok) : make_uint4(0u, 0u, 0u, 0u);
+      for (int u = 0; u < kLoadBatch; ++u) {
+        const int64_t c0 = t0 + 4 * (v0 + u);
+        f[u] = (v0 + u < nslot && c0 + 4 <= hi) ? __ldg(reinterpret_cast<const float4*>(krow + c0))
+                                                 : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+#pragma unroll
+      for (int u = 0; u < kLoadBatch; ++u) {
+        const int64_t c0 = t0 + 4 * (v0 + u);
+        float v[4] = {f[u].x, f[u].y, f[u].z, f[u].w};
+        if (v0 + u < nslot && c0 < hi && c0 + 4 > hi) {  // the slice's ragged end
+#pragma unroll
+          for (int i = 0; i < 4; ++i) v[i] = c0 + i < hi ? krow[c0 + i] : -INFINITY;
+        }
+        uint32_t kk[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) kk[i] = v[i] == -INFINITY ? 0u : score_key(v[i]);
+        k4[u] = make_uint4(kk[0], kk[1], kk[2], kk[3]);
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < kLoadBatch; ++u) {
+        const int64_t c0 = t0 + 4 * (v0 + u);
+        k4[u] = (v0 + u < nslot && c0 < hi) ? load_keys4(a, b, n, hi, c0, vec_ok) : make_uint4(0u, 0u, 0u, 0u);
+      }
     }
 #pragma unroll
     for (int u = 0; u < kLoadBatch; ++u) {
@@ -455,10 +484,17 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
     for (int d = lane; d < kBins; d += 32) myhist[d] = 0;
     __syncthreads();
     const uint32_t prefix = s_prefix, mask = s_mask;
+    const int ncomp = s_ncomp;
     // four independent run-length counters (one per key of a slot) for ILP
     uint32_t last[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
     unsigned run[4] = {0, 0, 0, 0};
-    for (int v = 0; v < nslot; ++v) {
+    if (pass > 0 && ncomp <= kCompCap) {  // the later digits only split the first digit's bin
+      for (int j = tid; j < ncomp; j += NT) {
+        const uint32_t kk = comp_s[j];
+        if ((kk & mask) == prefix) atomicAdd(&myhist[(shift >= 0 ? kk >> shift : kk << -shift) & 255u], 1u);
+      }
+    }
+    for (int v = 0; v < ((pass > 0 && ncomp <= kCompCap) ? 0 : nslot); ++v) {
       const uint4 k4 = myslots[v ^ swz];
       const uint32_t kk4[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
@@ -510,21 +546,37 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
       s_need = need - (cum - (int)h);
     }
     __syncthreads();
+    if (pass == 0 && shift > 0) {  // more digits follow: keep the threshold bin's keys
+      const uint32_t p2 = s_prefix, m2 = s_mask;
+      for (int v = 0; v < nslot; ++v) {
+        const uint4 k4 = myslots[v ^ swz];
+        const uint32_t kk4[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (kk4[i] != 0u && (kk4[i] & m2) == p2) {
+            const int j = atomicAdd(&s_ncomp, 1);
+            if (j < kCompCap) comp_s[j] = kk4[i];
+          }
+      }
+      __syncthreads();
+    }
   }
   const uint32_t T = s_prefix;
   const int take_eq = s_need;  // candidates equal to T to take (lowest indices first)
 
   if (need_total > 0) {
-    int gt = 0, eq = 0;
+    // bit 4 v + i of gtm / eqm: this thread's candidate t0 + 4 v + i is above / equal to T
+    uint64_t gtm = 0, eqm = 0;
     for (int v = 0; v < nslot; ++v) {
       const uint4 k4 = myslots[v ^ swz];
       const uint32_t kk4[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        gt += kk4[i] != 0u && kk4[i] > T;
-        eq += kk4[i] != 0u && kk4[i] == T;
+        gtm |= (uint64_t)(kk4[i] != 0u && kk4[i] > T) << (4 * v + i);
+        eqm |= (uint64_t)(kk4[i] != 0u && kk4[i] == T) << (4 * v + i);
       }
     }
+    const int gt = __popcll(gtm), eq = __popcll(eqm);
     const int wgt = (int)__reduce_add_sync(0xffffffffu, (unsigned)gt);
     const int weq = (int)__reduce_add_sync(0xffffffffu, (unsigned)eq);
     if (tid == 0) ccount[0] = ccount[1] = 0;
@@ -561,23 +613,16 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
     int pos;
     ScanI(scan_tmp).ExclusiveSum(gt + eq_take, pos);
     pos += s_base_out;
-    int eq_left = eq_take;
-    for (int v = 0; v < nslot; ++v) {
-      const uint4 k4 = myslots[v ^ swz];
-      const uint32_t kk4[4] = {k4.x, k4.y, k4.z, k4.w};
-      const int64_t c0 = t0 + 4 * v;
-      int pb = 0;
-      if (a.pool) pb = c0 < hi ? a.pool[(int64_t)b * a.keep + c0 / 8] : -1;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t kk = kk4[i];
-        bool take = kk != 0u && kk > T;
-        if (kk != 0u && kk == T && eq_left > 0) {
-          take = true;
-          --eq_left;
-        }
-        if (take) out[pos++] = a.pool ? (int32_t)((int64_t)pb * 8 + (c0 + i) % 8) : (int32_t)(c0 + i);
-      }
+    uint64_t take = gtm;
+    for (int q = 0; q < eq_take; ++q) {  // the lowest eq_take candidates equal to T
+      take |= eqm & (~eqm + 1);
+      eqm &= eqm - 1;
+    }
+    while (take) {  // ascending candidate order
+      const int j = __ffsll((long long)take) - 1;
+      take &= take - 1;
+      const int64_t c = t0 + j;
+      out[pos++] = a.pool ? (int32_t)((int64_t)a.pool[(int64_t)b * a.keep + c / 8] * 8 + c % 8) : (int32_t)c;
     }
   }
   if (rank == ncl - 1) {  // padding after the last selected id
