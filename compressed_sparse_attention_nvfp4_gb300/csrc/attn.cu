@@ -339,6 +339,7 @@ __global__ void __launch_bounds__(kAT, 1) k_attn(
     __syncwarp();
     ptx::tmem_alloc(&S.tmem_base, kAttnTmemCols);
   }
+  ptx::griddep_wait();  // q, the indices and the rows may come from the previous kernel
   // q and the first chunk's indices load together; q is converted while the
   // indices arrive, then the rows are requested
   const int r = tid % kRows, half = (tid / kRows) & 1;
@@ -591,6 +592,7 @@ __global__ void __launch_bounds__(128) k_attn_merge(const float* __restrict__ pa
                                                     float* __restrict__ lse) {
   const int bh = blockIdx.x;  // b * 64 + h
   const int b = bh / kHAtt, h = bh % kHAtt;
+  ptx::griddep_wait();  // the partials come from the previous kernel
   float M = -INFINITY;
   for (int c = 0; c < nchunks; ++c) M = fmaxf(M, part_ml[((int64_t)b * nchunks + c) * kHAtt + h].x);
   const float z = sink ? sink[h] : -INFINITY;  // the sink joins the denominator once per query
@@ -698,13 +700,13 @@ csa2_status attn_run(const csa2_kv_planes* kv, int32_t B, const int32_t* topk, c
     return CSA2_ERR_CUDA;
   {
     KernelTimer timer(partial ? "k_attn_part" : "k_attn", st);
-    kern<<<dim3(plan.nsplit, B), kAT, smem, st>>>(kv->kv_codes, kv->kv_scales, kv->seq_stride, topk, dense_n, k,
-                                                   swa_e4m3, n_swa, (const uint16_t*)q_bf16, softmax_scale, ex,
-                                                   plan.nchunks, plan.cps, out, lse_out, L.part_o, L.part_ml, ws);
+    launch_pdl(kern, dim3(plan.nsplit, B), dim3(kAT), (size_t)smem, st, kv->kv_codes, kv->kv_scales, kv->seq_stride,
+               topk, dense_n, k, swa_e4m3, n_swa, (const uint16_t*)q_bf16, softmax_scale, ex, plan.nchunks, plan.cps,
+               out, lse_out, L.part_o, L.part_ml, ws);
   }
   if (partial) {
     KernelTimer timer("k_attn_merge", st);
-    k_attn_merge<<<B * kHAtt, 128, 0, st>>>(L.part_o, L.part_ml, plan.nsplit, sink, out, lse_out);
+    launch_pdl(k_attn_merge, dim3(B * kHAtt), dim3(128), 0, st, L.part_o, L.part_ml, plan.nsplit, sink, out, lse_out);
   }
   return launch_status();
 }

@@ -97,6 +97,26 @@ __host__ __device__ __forceinline__ size_t align_up(size_t x, size_t a) { return
 // Host helpers shared by the entry points.
 namespace csa2 {
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+// Launches kernel k in stream order with programmatic dependent launch: its
+// CTAs may be scheduled while the previous kernel of the stream drains, and
+// every kernel launched this way starts with griddepcontrol.wait (nothing
+// global is touched before the previous kernel has completed).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, static_cast<KArgs>(args)...);
+}
+
 inline csa2_status launch_status() {
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;

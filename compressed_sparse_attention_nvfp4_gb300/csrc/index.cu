@@ -370,6 +370,7 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
   const int rank = (int)cluster.block_rank();
   const int b = blockIdx.x / ncl;
   const int tid = threadIdx.x, lane = threadIdx.x % 32, wid = threadIdx.x / 32;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the keys come from the previous kernel
   const int64_t n = max((int64_t)0, min((int64_t)a.n_entries[b], a.n_max));
   const int64_t ncand = a.pool ? a.ncand_fixed : (a.count_blocks ? cdiv(n, 8) : n);
   const int64_t per = (int64_t)align_up((size_t)cdiv(ncand, ncl), kSelItems);
@@ -644,13 +645,15 @@ void launch_select_res(const SelectArgs& a, int B, int ncl, int64_t per, cudaStr
   cfg.blockDim = dim3(NT);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)ncl;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // starts with griddepcontrol.wait
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   KernelTimer timer("k_select_res", st);
   cudaLaunchKernelEx(&cfg, k_select_res<NT>, a);
 }

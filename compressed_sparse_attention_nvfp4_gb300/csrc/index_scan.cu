@@ -186,6 +186,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   volatile int* abort_flag = &S.abort_flag;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int b = blockIdx.y;
+  ptx::griddep_wait();  // inputs may come from the previous kernel of the stream
 
   int64_t n = p.n_entries ? p.n_entries[b] : p.n_max;  // no counts: every slot holds n_max
   if (n > p.n_max) {
@@ -531,7 +532,7 @@ csa2_status launch_scan(const csa2_kv_planes* kv, int32_t B, const int32_t* n_en
   ScanParams p{kv->ix_codes, kv->ix_scales, kv->seq_stride, n_entries, n_max, q, w, pool, keep,
                ncand_max, S, scores, score_stride, bmax, bmax_stride, ws, shared_slot};
   KernelTimer timer("k_scan_tc", st);
-  k_scan_tc<<<dim3((unsigned)S, (unsigned)B), kThreads, smem, st>>>(p, map_tile, map_block);
+  launch_pdl(k_scan_tc, dim3((unsigned)S, (unsigned)B), dim3(kThreads), (size_t)smem, st, p, map_tile, map_block);
   return cudaGetLastError() == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
 }
 
