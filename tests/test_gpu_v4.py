@@ -273,6 +273,22 @@ def test_dense_attention_beyond_topk_limit(oracle_mod):
         assert np.allclose(lse[b], rl, rtol=1e-4, atol=1e-4)
 
 
+def test_dense_attention_full_size_sampled(oracle_mod):
+    """The benchmarked HCA launch: batch 32, every one of 8,192 entries + 128 window
+    rows (4 CTAs per query and the merge); sampled queries against the oracle."""
+    B, N = 32, 8192
+    c = SmallCache(oracle_mod, 10, B, N)
+    q = W.attn_query(10, 0, B)
+    swa = W.swa_rows(10, 0, B, 128)
+    out, lse = _dense(c, [N] * B, N, swa, q, 128)
+    topk = _arange_topk([N], N)[0]
+    for b in (0, 13, 31):
+        kvc, kvs, _, _ = c.oracle_slot(b)
+        ro, rl = oracle_mod.attention(kvc, kvs, topk, swa[b], q[b], SCALE)
+        check_attention(out[b:b + 1], ro[None])
+        assert np.allclose(lse[b], rl, rtol=1e-4, atol=1e-4)
+
+
 def test_dense_attention_extras_and_empty(oracle_mod):
     c = SmallCache(oracle_mod, 9, 2, 600)
     q = W.attn_query(9, 0, 2)
