@@ -6,18 +6,21 @@
 // The projection runs on the 5th-generation tensor cores (k_cw_tc): a
 // persistent bf16 GEMM whose 128-token x 256-column tiles hold C and Z of the
 // same 128 channels, so that the epilogue can pool them without another pass.
-// Both operands are K-major with 128-byte swizzle: H as given, the weights
-// through a per-call transposed copy Wt[channel block j][C rows | Z rows][d]
-// (k_cw_wt, 2 x d x 512 bf16).  Warp roles: warp 0 loads the A (16 KB) and B
-// (32 KB) tiles of each 64-wide K step with TMA into a 4-stage ring; warp 1
-// allocates tensor memory and issues 4 MMAs (M128 N256 K16, kind::f16, bf16
-// operands, fp32 accumulate) per stage into one of two 256-column accumulators;
-// warps 2-5 read the finished accumulator (thread = token), pool each group of
-// m adjacent tokens with a max-subtracted per-channel softmax through lane
-// shuffles, and write Cbar (fp32).  K^I = Cbar W_IK follows on the tensor cores
-// with every product exact (k_cw_ki_tc: Cbar split into three bf16 terms), then
-// the codec.  A group of 64 tokens spans two lane quarters; m = 64 keeps the
-// CUDA-core kernel k_cw_gemm_pool, which computes the same quantities.
+// H is the K-major A operand; the weights are read as given ([d][512], N
+// contiguous) as an N-major B operand: four 64-column tensor loads per stage
+// (two of W_KV, two of W_Z), 128-byte swizzle.  Warp roles: warp 0 loads the A
+// (16 KB) and B (32 KB) tiles of each 64-wide K step with TMA into a 4-stage
+// ring; warp 1 allocates tensor memory and issues 4 MMAs (M128 N256 K16,
+// kind::f16, bf16 operands, fp32 accumulate) per stage into one of two
+// 256-column accumulators; warps 2-5 read the finished accumulator (thread =
+// token), pool each group of m adjacent tokens with a max-subtracted
+// per-channel softmax through lane shuffles, and write Cbar (fp32).  K^I =
+// Cbar W_IK follows on the tensor cores with every product exact (k_cw_ki_tc:
+// Cbar split into three bf16 terms), then the codec.  A group of 64 tokens
+// spans two lane quarters; m = 64 keeps the CUDA-core kernel k_cw_gemm_pool,
+// which computes the same quantities.  Few tokens (a decode-time append) split
+// the K range over the SMs instead (k_cw_finish_small sums the slices, pools,
+// forms K^I and writes the entries).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -133,34 +136,51 @@ constexpr int kTcM = 128;         // tokens per tile
 constexpr int kTcN = 256;         // C and Z columns of 128 channels
 constexpr int kTcBK = 64;         // K elements per stage (one 128-byte swizzle row)
 constexpr int kTcStages = 4;
+constexpr int kFillSms = 148;     // SMs the split plan fills (a shape-only constant)
 constexpr int kTcThreads = 192;   // producer, MMA, 4 epilogue warps
 constexpr uint32_t kTcTmemCols = 512;
 constexpr long long kTcWaitBudget = 1LL << 32;
 
 struct __align__(1024) TcSmem {
   uint8_t A[kTcStages][kTcM * 128];  // H tile, K-major, 128-byte swizzle
-  uint8_t B[kTcStages][kTcN * 128];  // Wt tile, K-major, 128-byte swizzle
+  // W tile, N-major: four 64-column blocks (W_KV 128 j .. + 127, then W_Z's), each
+  // 64 K rows of 128 bytes with 128-byte swizzle, as the tensor loads write them
+  uint8_t B[kTcStages][kTcN * 128];
   uint64_t full[kTcStages], empty[kTcStages];
   uint64_t acc_full[2], acc_free[2];
   uint32_t tmem_base;
   int abort_flag;
 };
 
-// Wt[j][r][k] (j = 128-channel block, r < 128: W_KV column 128j + r, r >= 128:
-// W_Z column 128j + r - 128), 32 x 32 tiles through shared memory
+// Long inputs read the weights K-major from a per-call transposed copy
+// Wt[channel block j][C rows | Z rows][d] (measured faster than the N-major
+// reads once the transpose is spread over many token tiles): 64 x 64 tiles
+// through shared memory, 16-byte global accesses on both sides.
+constexpr int kWtTile = 64;
+constexpr int64_t kDirectMaxT = 65536;  // tokens up to which W is read N-major as given
 __global__ void __launch_bounds__(256) k_cw_wt(const uint16_t* __restrict__ Wkv,
                                                const uint16_t* __restrict__ Wz, int d,
                                                uint16_t* __restrict__ Wt) {
-  __shared__ uint16_t tile[32][33];
-  const int k0 = blockIdx.x * 32;    // K rows of W
-  const int row0 = blockIdx.y * 32;  // Wt rows (0 .. 1023)
+  __shared__ __align__(16) uint16_t tile[kWtTile][kWtTile + 8];  // [k][column], rows padded by 16 bytes
+  const int k0 = blockIdx.x * kWtTile;    // K rows of W
+  const int row0 = blockIdx.y * kWtTile;  // Wt rows (0 .. 1023)
   const int j = row0 / 256, rr = row0 % 256;
   const uint16_t* src = rr < 128 ? Wkv : Wz;
   const int c0 = 128 * j + (rr % 128);
-  const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
-  for (int i = ty; i < 32; i += 8) tile[i][tx] = src[(int64_t)(k0 + i) * kDMain + c0 + tx];
+  for (int i = threadIdx.x; i < kWtTile * 8; i += 256) {  // row i / 8, 8 columns from 8 (i % 8)
+    const int r = i / 8, ch = i % 8;
+    *reinterpret_cast<uint4*>(&tile[r][ch * 8]) =
+        *reinterpret_cast<const uint4*>(src + (int64_t)(k0 + r) * kDMain + c0 + ch * 8);
+  }
   __syncthreads();
-  for (int i = ty; i < 32; i += 8) Wt[(int64_t)(row0 + i) * d + k0 + tx] = tile[tx][i];
+  for (int i = threadIdx.x; i < kWtTile * 8; i += 256) {  // Wt row row0 + i % 64, K chunk i / 64
+    const int nn = i % kWtTile, kc = i / kWtTile;
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      w[q] = (uint32_t)tile[kc * 8 + 2 * q][nn] | ((uint32_t)tile[kc * 8 + 2 * q + 1][nn] << 16);
+    *reinterpret_cast<uint4*>(Wt + (int64_t)(row0 + nn) * d + k0 + kc * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
 }
 
 __device__ __forceinline__ void tc_abort(TcSmem& S, void* ws, int where) {
@@ -168,9 +188,14 @@ __device__ __forceinline__ void tc_abort(TcSmem& S, void* ws, int where) {
   report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, where);
 }
 
+// kNMajorW: B tiles come N-major from W_KV and W_Z as given (map_wkv, map_wz);
+// otherwise K-major from the transposed copy (map_wkv holds Wt, map_wz unused).
+template <bool kNMajorW>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    k_cw_tc(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w, int64_t T,
-            int d, int m, float* __restrict__ cbar, float* __restrict__ zout, void* ws) {
+    k_cw_tc(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_wkv,
+            const __grid_constant__ CUtensorMap map_wz, int64_t T,
+            int d, int m, float* __restrict__ cbar, float* __restrict__ zout, int ksplit,
+            float* __restrict__ part, void* ws) {
   extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
   TcSmem& S = *reinterpret_cast<TcSmem*>(tc_smem_raw);
   volatile int* abort_flag = &S.abort_flag;
@@ -178,6 +203,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int64_t token_tiles = cdiv(T, kTcM);
   const int64_t ntiles = token_tiles * (kDMain / 128);
   const int nk = d / kTcBK;
+  // work item = (tile, K slice): with ksplit > 1 each item sums K steps
+  // [ks nk / ksplit, (ks + 1) nk / ksplit) and writes raw partial C and Z to part
+  const int64_t nitems = ntiles * ksplit;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTcStages; ++s) {
       ptx::mbar_init(&S.full[s], 1);
@@ -201,16 +229,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       int s = 0;
       uint32_t ph = 0;
-      for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+      for (int64_t item = blockIdx.x; item < nitems; item += gridDim.x) {
+        const int64_t tile = item / ksplit;
+        const int ks = (int)(item % ksplit);
         const int t0 = (int)((tile / 4) * kTcM), j = (int)(tile % 4);
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int kb = ks * nk / ksplit; kb < (ks + 1) * nk / ksplit; ++kb) {
           if (!ptx::mbar_wait(&S.empty[s], ph ^ 1u, abort_flag, kTcWaitBudget)) {
             tc_abort(S, ws, 31);
             goto producer_done;
           }
           ptx::mbar_arrive_expect_tx(&S.full[s], (kTcM + kTcN) * 128);
           ptx::tma_load_2d(S.A[s], &map_h, kb * kTcBK, t0, &S.full[s]);
-          ptx::tma_load_2d(S.B[s], &map_w, kb * kTcBK, j * kTcN, &S.full[s]);
+          if (kNMajorW) {
+            ptx::tma_load_2d(S.B[s], &map_wkv, 128 * j, kb * kTcBK, &S.full[s]);
+            ptx::tma_load_2d(S.B[s] + 8192, &map_wkv, 128 * j + 64, kb * kTcBK, &S.full[s]);
+            ptx::tma_load_2d(S.B[s] + 16384, &map_wz, 128 * j, kb * kTcBK, &S.full[s]);
+            ptx::tma_load_2d(S.B[s] + 24576, &map_wz, 128 * j + 64, kb * kTcBK, &S.full[s]);
+          } else {
+            ptx::tma_load_2d(S.B[s], &map_wkv, kb * kTcBK, j * kTcN, &S.full[s]);
+          }
           if (++s == kTcStages) {
             s = 0;
             ph ^= 1u;
@@ -222,10 +259,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      constexpr uint32_t idesc = ptx::idesc_f16(kTcM, kTcN, 1);
+      constexpr uint32_t idesc = ptx::idesc_f16(kTcM, kTcN, 1) | (kNMajorW ? ptx::kIdescBMajorMN : 0u);
       int s = 0, local = 0;
       uint32_t ph = 0;
-      for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
+      for (int64_t item = blockIdx.x; item < nitems; item += gridDim.x, ++local) {
+        const int ks = (int)(item % ksplit);
+        const int kb0 = ks * nk / ksplit, kb1 = (ks + 1) * nk / ksplit;
         const int a = local & 1;
         const uint32_t u = (uint32_t)(local >> 1) & 1u;
         if (!ptx::mbar_wait(&S.acc_free[a], u ^ 1u, abort_flag, kTcWaitBudget)) {
@@ -235,7 +274,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ptx::tc_fence_after();
         const uint32_t d_t = tmem + (uint32_t)a * kTcN;
         bool ok = true;
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!ptx::mbar_wait(&S.full[s], ph, abort_flag, kTcWaitBudget)) {
             tc_abort(S, ws, 33);
             ok = false;
@@ -243,11 +282,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           ptx::tc_fence_after();
           const uint64_t ad = ptx::smem_desc_sw128(S.A[s], 1024);
-          const uint64_t bd = ptx::smem_desc_sw128(S.B[s], 1024);
+          const uint64_t bd =
+              kNMajorW ? ptx::smem_desc_sw128_mn(S.B[s], 8192, 1024) : ptx::smem_desc_sw128(S.B[s], 1024);
+          // K step: 32 bytes of an A row; of B 16 rows (2 KB) N-major, 32 bytes of a row K-major
+          constexpr uint64_t kBStep = kNMajorW ? 128 : 2;
 #pragma unroll
-          for (int kk = 0; kk < kTcBK / 16; ++kk)  // 16 bf16 = 32 bytes per K step
-            ptx::mma_f16_ss(d_t, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc,
-                            (kb | kk) ? 1u : 0u);
+          for (int kk = 0; kk < kTcBK / 16; ++kk)
+            ptx::mma_f16_ss(d_t, ad + (uint64_t)(2 * kk), bd + kBStep * kk, idesc, (kb != kb0 || kk) ? 1u : 0u);
           ptx::mma_commit(&S.empty[s]);  // the stage is free once these MMAs have read it
           if (++s == kTcStages) {
             s = 0;
@@ -264,7 +305,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t lane_addr = tmem + ((uint32_t)(sub * 32) << 16);
     const int64_t n = T / m;
     int local = 0;
-    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
+    for (int64_t item = blockIdx.x; item < nitems; item += gridDim.x, ++local) {
+      const int64_t tile = item / ksplit;
+      const int ks = (int)(item % ksplit);
       const int a = local & 1;
       const uint32_t u = (uint32_t)(local >> 1) & 1u;
       if (!ptx::mbar_wait_warp(&S.acc_full[a], u, abort_flag, kTcWaitBudget)) {
@@ -283,6 +326,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ptx::tmem_ld_32x32b_x32(base, cr);
         ptx::tmem_ld_32x32b_x32(base + 128u, zr);
         ptx::tmem_wait_ld();
+        if (part) {  // K slice ks of token t: raw C then Z, [ks][t][C 512 | Z 512]
+          if (t < T) {
+            float4* pc = reinterpret_cast<float4*>(part + ((int64_t)ks * T + t) * (2 * kDMain) + ch0 + cb * 32);
+            float4* pz = pc + kDMain / 4;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              pc[q] = make_float4(__uint_as_float(cr[4 * q]), __uint_as_float(cr[4 * q + 1]),
+                                  __uint_as_float(cr[4 * q + 2]), __uint_as_float(cr[4 * q + 3]));
+              pz[q] = make_float4(__uint_as_float(zr[4 * q]), __uint_as_float(zr[4 * q + 1]),
+                                  __uint_as_float(zr[4 * q + 2]), __uint_as_float(zr[4 * q + 3]));
+            }
+          }
+          continue;
+        }
         float v[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
@@ -513,26 +570,137 @@ bool make_bf16_map(CUtensorMap* map, const void* base, int64_t rows, int64_t col
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Few tokens (split-K): one CTA per entry finishes it.  Thread c sums the K
+// slices of channel c of C and Z for each of the entry's m rows, pools them as
+// k_cw_tc's epilogue does (Cbar), then the CTA forms K^I = Cbar W_IK: thread t
+// sums channels 128 (t / 128) .. + 127 for output t % 128 (every product exact
+// inside its fp32 FMA), and the four quarter sums add in a fixed order.  Warp 0
+// then writes the entry's main KV (RMSNorm / RoPE as the codec kernels do) and
+// warp 1 its indexer key into the planes.
+constexpr int kFinThreads = kDMain;
+struct FinishOut {
+  uint8_t *kv_codes, *kv_scales, *ix_codes, *ix_scales;
+  QDest d;
+  const float* norm_w;
+  float eps;
+  int rope;
+};
+__global__ void __launch_bounds__(kFinThreads) k_cw_finish_small(const float* __restrict__ part, int ksplit,
+                                                                 int64_t T, int m,
+                                                                 const uint16_t* __restrict__ Wik,
+                                                                 const __grid_constant__ FinishOut fo,
+                                                                 const __grid_constant__ RopeTheta th) {
+  __shared__ __align__(16) float cb[kDMain];
+  __shared__ __align__(16) float kis[kDIdx];
+  __shared__ float quarter[4][kDIdx];
+  const int64_t e = blockIdx.x;
+  const int c = threadIdx.x;
+  float zmax = -INFINITY, num = 0.0f, den = 0.0f, c0 = 0.0f;
+  // two passes over the rows (max, then weighted sums): the partials are L2-resident
+  for (int pass = 0; pass < (m == 1 ? 1 : 2); ++pass) {
+    for (int r = 0; r < m; ++r) {
+      const float* rowp = part + (e * m + r) * (2 * kDMain) + c;
+      float cs = 0.0f, zs = 0.0f;
+      int k = 0;
+      for (; k + 4 <= ksplit; k += 4) {  // four slices' loads in flight
+        float cv[4], zv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          cv[u] = rowp[(int64_t)(k + u) * T * (2 * kDMain)];
+          zv[u] = rowp[(int64_t)(k + u) * T * (2 * kDMain) + kDMain];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          cs += cv[u];
+          zs += zv[u];
+        }
+      }
+      for (; k < ksplit; ++k) {
+        cs += rowp[(int64_t)k * T * (2 * kDMain)];
+        zs += rowp[(int64_t)k * T * (2 * kDMain) + kDMain];
+      }
+      if (m == 1) {
+        c0 = cs;  // the softmax over one token is exactly 1
+      } else if (pass == 0) {
+        zmax = fmaxf(zmax, zs);
+      } else {
+        const float ez = expf(zs - zmax);
+        num = fmaf(ez, cs, num);
+        den += ez;
+      }
+    }
+  }
+  const float v = m == 1 ? c0 : __fdiv_rn(num, den);
+  cb[c] = v;
+  __syncthreads();
+  const int o = c % kDIdx, qt = c / kDIdx;
+  float acc = 0.0f;
+#pragma unroll 16
+  for (int i = 0; i < kDMain / 4; ++i) {
+    const int ch = qt * (kDMain / 4) + i;
+    acc = fmaf(cb[ch], __uint_as_float((uint32_t)__ldg(Wik + ch * kDIdx + o) << 16), acc);
+  }
+  quarter[qt][o] = acc;
+  __syncthreads();
+  if (c < kDIdx) kis[c] = ((quarter[0][c] + quarter[1][c]) + quarter[2][c]) + quarter[3][c];
+  __syncthreads();
+  const int warp = c / 32, lane = c % 32;
+  if (warp == 0) {
+    const int64_t row = dest_row(fo.d, e);
+    if (row >= 0)
+      quantize_main_entry_warp(cb, fo.norm_w, fo.eps, fo.rope, th, fo.rope ? (double)dest_pos(fo.d, e) : 0.0,
+                               fo.kv_codes + row * 256, fo.kv_scales + row * 32, lane);
+  } else if (warp == 1 && lane < 4) {
+    const int64_t row = dest_row(fo.d, e);
+    if (row >= 0) quantize_index_group(kis + lane * 32, fo.ix_codes + row * 64 + lane * 16, fo.ix_scales + row * 4 + lane);
+  }
+}
+
 struct CwWs {
   float* cbar;
   float* ki;
-  uint16_t* wt;
+  uint16_t* wt;  // transposed weights (long inputs only)
   uint16_t* wikt;
+  float* part;  // split-K partial C and Z [ksplit][T][1024] (few tokens only)
+  int ksplit;
   size_t bytes;
 };
 
-CwWs cw_ws_layout(void* ws, int64_t n, int64_t d_model) {
+// K slices of the projection GEMM: few tokens leave most SMs idle with one CTA
+// per 128 x 256 tile, so the K range is split until about one item per SM
+// (the partials are summed by k_cw_reduce_pool).  Depends only on the shapes.
+constexpr int kMaxKSplit = 32;
+int cw_ksplit(int64_t T, int64_t d_model, int sms) {
+  const int64_t ntiles = cdiv(T, kTcM) * (kDMain / 128);
+  if (T <= 0 || ntiles * 2 > sms) return 1;
+  int64_t ks = sms / ntiles;
+  ks = std::min<int64_t>(ks, d_model / kTcBK);
+  ks = std::min<int64_t>(ks, kMaxKSplit);
+  return (int)std::max<int64_t>(ks, 1);
+}
+
+CwWs cw_ws_layout(void* ws, int64_t n, int64_t d_model, int m = 1) {
   CwWs L;
   char* base = (char*)ws;
   size_t off = kWsHeader;
+  const int64_t T = n * m;
+  L.ksplit = cw_ksplit(T, d_model, kFillSms);
   L.cbar = (float*)(base ? base + off : nullptr);
   off += align_up((size_t)n * kDMain * 4, 256);
   L.ki = (float*)(base ? base + off : nullptr);
   off += align_up((size_t)n * kDIdx * 4, 256);
-  L.wt = (uint16_t*)(base ? base + off : nullptr);
-  off += align_up((size_t)2 * kDMain * d_model * 2, 256);
+  L.wt = nullptr;
+  if (T > kDirectMaxT) {
+    L.wt = (uint16_t*)(base ? base + off : nullptr);
+    off += align_up((size_t)2 * kDMain * d_model * 2, 256);
+  }
   L.wikt = (uint16_t*)(base ? base + off : nullptr);
   off += align_up((size_t)kDIdx * kDMain * 2, 256);
+  L.part = nullptr;
+  if (L.ksplit > 1) {
+    L.part = (float*)(base ? base + off : nullptr);
+    off += align_up((size_t)L.ksplit * T * 2 * kDMain * 4, 256);
+  }
   L.bytes = off;
   return L;
 }
@@ -543,7 +711,7 @@ CwWs cw_ws_layout(void* ws, int64_t n, int64_t d_model) {
 
 extern "C" size_t csa2_cache_write_workspace_size(int64_t T, int32_t d_model, int32_t m) {
   if (T < 0 || m < 1 || d_model < 0) return 0;
-  return csa2::cw_ws_layout(nullptr, T / m, d_model).bytes;
+  return csa2::cw_ws_layout(nullptr, T / m, d_model, m).bytes;
 }
 
 namespace csa2 {
@@ -553,30 +721,57 @@ namespace {
 // groups of m consecutive rows of H into L.cbar, then K^I = Cbar W_IK into L.ki:
 // T / m entries.  Shared by the prefill write (one slot, contiguous entries) and
 // the decode-time append (one group per slot).
+// With few tokens (split-K) the finishing kernel also writes the entries into
+// dst at d (*written = true); otherwise L.cbar and L.ki hold them for the codec.
 csa2_status cw_compute(const void* H_bf16, int64_t T, int32_t d_model, const void* Wkv_bf16,
                        const void* Wz_bf16, const void* Wik_bf16, int32_t m, const CwWs& L, void* ws,
-                       cudaStream_t st) {
+                       cudaStream_t st, const csa2_kv_planes* dst, const QDest& d, const csa2_norm_rope* nr,
+                       bool* written) {
+  *written = false;
   const int64_t n = T / m;
   if (m <= 32 && T < ((int64_t)1 << 31)) {
-    // tensor cores: transposed weights, then the persistent GEMM + pooling
-    {
-      KernelTimer timer("k_cw_wt", st);
-      k_cw_wt<<<dim3((unsigned)(d_model / 32), 2 * kDMain / 32), 256, 0, st>>>(
-          (const uint16_t*)Wkv_bf16, (const uint16_t*)Wz_bf16, d_model, L.wt);
+    // tensor cores: the persistent GEMM + pooling; W read N-major as given, or
+    // (long inputs) K-major from a transposed copy
+    const bool nmajor = T <= kDirectMaxT;
+    CUtensorMap map_h, map_wkv, map_wz;
+    if (nmajor) {
+      if (!make_bf16_map(&map_wkv, Wkv_bf16, d_model, kDMain, kTcBK) ||
+          !make_bf16_map(&map_wz, Wz_bf16, d_model, kDMain, kTcBK))
+        return CSA2_ERR_CUDA;
+    } else {
+      {
+        KernelTimer timer("k_cw_wt", st);
+        k_cw_wt<<<dim3((unsigned)(d_model / kWtTile), 2 * kDMain / kWtTile), 256, 0, st>>>(
+            (const uint16_t*)Wkv_bf16, (const uint16_t*)Wz_bf16, d_model, L.wt);
+      }
+      if (!make_bf16_map(&map_wkv, L.wt, 2 * kDMain, d_model, kTcN)) return CSA2_ERR_CUDA;
+      map_wz = map_wkv;
     }
-    CUtensorMap map_h, map_w;
-    if (!make_bf16_map(&map_h, H_bf16, T, d_model, kTcM) || !make_bf16_map(&map_w, L.wt, 2 * kDMain, d_model, kTcN))
-      return CSA2_ERR_CUDA;
+    if (!make_bf16_map(&map_h, H_bf16, T, d_model, kTcM)) return CSA2_ERR_CUDA;
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) != cudaSuccess) return CSA2_ERR_CUDA;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int smem = (int)sizeof(TcSmem);
-    if (cudaFuncSetAttribute(k_cw_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    auto kern = nmajor ? k_cw_tc<true> : k_cw_tc<false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return CSA2_ERR_CUDA;
-    const int64_t ntiles = cdiv(T, kTcM) * (kDMain / 128);
-    const int grid = (int)std::min<int64_t>(ntiles, sms);
-    KernelTimer timer("k_cw_tc", st);
-    k_cw_tc<<<grid, kTcThreads, smem, st>>>(map_h, map_w, T, d_model, m, L.cbar, nullptr, ws);
+    const int64_t nitems = cdiv(T, kTcM) * (kDMain / 128) * L.ksplit;
+    const int grid = (int)std::min<int64_t>(nitems, sms);
+    {
+      KernelTimer timer("k_cw_tc", st);
+      kern<<<grid, kTcThreads, smem, st>>>(map_h, map_wkv, map_wz, T, d_model, m, L.cbar, nullptr, L.ksplit, L.part,
+                                           ws);
+    }
+    if (L.ksplit > 1) {  // the partials' sums, pooling, K^I and the codec in one kernel
+      FinishOut fo{dst->kv_codes, dst->kv_scales, dst->ix_codes, dst->ix_scales, d,
+                   nr ? nr->norm_weight : nullptr, nr ? nr->norm_eps : 0.0f, nr ? nr->rope : 0};
+      const RopeTheta th = fo.rope ? make_rope_theta(nr->rope_base) : RopeTheta{};
+      KernelTimer timer("k_cw_finish_small", st);
+      k_cw_finish_small<<<(unsigned)n, kFinThreads, 0, st>>>(L.part, L.ksplit, T, m, (const uint16_t*)Wik_bf16, fo,
+                                                             th);
+      *written = true;
+      return CSA2_OK;
+    }
   } else {
     const int smem = (int)sizeof(GemmSmem);
     if (cudaFuncSetAttribute(k_cw_gemm_pool, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
@@ -624,23 +819,25 @@ extern "C" csa2_status csa2_cache_write(const void* H_bf16, int64_t T, int32_t d
   const int64_t n = T / m;
   if (entry_offset + n > dst->seq_stride) return CSA2_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, 256)) return CSA2_ERR_WORKSPACE;
-  CwWs L = cw_ws_layout(ws, n, d_model);
+  CwWs L = cw_ws_layout(ws, n, d_model, m);
   if (ws_bytes < L.bytes) return CSA2_ERR_WORKSPACE;
   if (reset_error(ws, st) != CSA2_OK) return CSA2_ERR_CUDA;
   if (T == 0) return CSA2_OK;
-  const csa2_status rc = cw_compute(H_bf16, T, d_model, Wkv_bf16, Wz_bf16, Wik_bf16, m, L, ws, st);
-  if (rc != CSA2_OK) return rc;
   QDest d{};
   d.e0 = (int64_t)seq * dst->seq_stride + entry_offset;
   d.pos_first = pos_first;
   d.pos_step = m;
-  launch_quantize(L.cbar, L.ki, n, dst, d, st, kv_nr);
+  bool written = false;
+  const csa2_status rc =
+      cw_compute(H_bf16, T, d_model, Wkv_bf16, Wz_bf16, Wik_bf16, m, L, ws, st, dst, d, kv_nr, &written);
+  if (rc != CSA2_OK) return rc;
+  if (!written) launch_quantize(L.cbar, L.ki, n, dst, d, st, kv_nr);
   return launch_status();
 }
 
 extern "C" size_t csa2_cache_append_workspace_size(int32_t G, int32_t d_model, int32_t m) {
   if (G < 0 || d_model <= 0 || m < 1) return 0;
-  return csa2::cw_ws_layout(nullptr, G, d_model).bytes;
+  return csa2::cw_ws_layout(nullptr, G, d_model, m).bytes;
 }
 
 extern "C" csa2_status csa2_cache_append(const void* H_bf16, int32_t G, int32_t d_model, const void* Wkv_bf16,
@@ -659,12 +856,10 @@ extern "C" csa2_status csa2_cache_append(const void* H_bf16, int32_t G, int32_t 
     return CSA2_ERR_INVALID_ARG;
   if (kv_nr && (!norm_rope_ok(kv_nr) || (kv_nr->rope && (!pos || !aligned(pos, 8))))) return CSA2_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, 256)) return CSA2_ERR_WORKSPACE;
-  CwWs L = cw_ws_layout(ws, G, d_model);
+  CwWs L = cw_ws_layout(ws, G, d_model, m);
   if (ws_bytes < L.bytes) return CSA2_ERR_WORKSPACE;
   if (reset_error(ws, st) != CSA2_OK) return CSA2_ERR_CUDA;
   if (G == 0) return CSA2_OK;
-  const csa2_status rc = cw_compute(H_bf16, (int64_t)G * m, d_model, Wkv_bf16, Wz_bf16, Wik_bf16, m, L, ws, st);
-  if (rc != CSA2_OK) return rc;
   QDest d{};
   d.slot = slot;
   d.entry = entry;
@@ -672,7 +867,11 @@ extern "C" csa2_status csa2_cache_append(const void* H_bf16, int32_t G, int32_t 
   d.n_slots = n_slots;
   d.pos = pos;
   d.ws = ws;
-  launch_quantize(L.cbar, L.ki, G, dst, d, st, kv_nr);
+  bool written = false;
+  const csa2_status rc = cw_compute(H_bf16, (int64_t)G * m, d_model, Wkv_bf16, Wz_bf16, Wik_bf16, m, L, ws, st,
+                                    dst, d, kv_nr, &written);
+  if (rc != CSA2_OK) return rc;
+  if (!written) launch_quantize(L.cbar, L.ki, G, dst, d, st, kv_nr);
   return launch_status();
 }
 
@@ -738,7 +937,6 @@ __global__ void k_pool_bias(const float* __restrict__ C, const float* __restrict
 
 struct CmpWs {
   float *c0, *z0, *c1, *z1;  // [T][512] each: the unpooled projections of up to two paths
-  uint16_t* wt;              // transposed weights of one path
   size_t bytes;
 };
 CmpWs cmp_ws_layout(void* ws, int64_t T, int64_t d_model) {
@@ -750,32 +948,28 @@ CmpWs cmp_ws_layout(void* ws, int64_t T, int64_t d_model) {
     *f[i] = (float*)(base ? base + off : nullptr);
     off += align_up((size_t)T * kDMain * 4, 256);
   }
-  L.wt = (uint16_t*)(base ? base + off : nullptr);
-  off += align_up((size_t)2 * kDMain * d_model * 2, 256);
+  (void)d_model;
   L.bytes = off;
   return L;
 }
 
 // C = H Wc, Z = H Wz (unpooled, fp32) on the tensor cores
 csa2_status project_raw(const void* H, int64_t T, int32_t d_model, const void* Wc, const void* Wz, float* C,
-                        float* Z, uint16_t* wt, void* ws, cudaStream_t st) {
-  {
-    KernelTimer timer("k_cw_wt", st);
-    k_cw_wt<<<dim3((unsigned)(d_model / 32), 2 * kDMain / 32), 256, 0, st>>>((const uint16_t*)Wc,
-                                                                            (const uint16_t*)Wz, d_model, wt);
-  }
-  CUtensorMap map_h, map_w;
-  if (!make_bf16_map(&map_h, H, T, d_model, kTcM) || !make_bf16_map(&map_w, wt, 2 * kDMain, d_model, kTcN))
+                        float* Z, void* ws, cudaStream_t st) {
+  CUtensorMap map_h, map_wc, map_wz;
+  if (!make_bf16_map(&map_h, H, T, d_model, kTcM) || !make_bf16_map(&map_wc, Wc, d_model, kDMain, kTcBK) ||
+      !make_bf16_map(&map_wz, Wz, d_model, kDMain, kTcBK))
     return CSA2_ERR_CUDA;
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) != cudaSuccess) return CSA2_ERR_CUDA;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int smem = (int)sizeof(TcSmem);
-  if (cudaFuncSetAttribute(k_cw_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+  if (cudaFuncSetAttribute(k_cw_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return CSA2_ERR_CUDA;
   const int64_t ntiles = cdiv(T, kTcM) * (kDMain / 128);
   KernelTimer timer("k_cw_tc", st);
-  k_cw_tc<<<(int)std::min<int64_t>(ntiles, sms), kTcThreads, smem, st>>>(map_h, map_w, T, d_model, 1, C, Z, ws);
+  k_cw_tc<true><<<(int)std::min<int64_t>(ntiles, sms), kTcThreads, smem, st>>>(map_h, map_wc, map_wz, T, d_model, 1,
+                                                                                C, Z, 1, nullptr, ws);
   return CSA2_OK;
 }
 
@@ -812,8 +1006,8 @@ extern "C" csa2_status csa2_compress_overlap(const void* H_bf16, int64_t T, int3
   cudaStream_t st = (cudaStream_t)stream;
   if (reset_error(ws, st) != CSA2_OK) return CSA2_ERR_CUDA;
   if (T == 0) return CSA2_OK;
-  if ((rc = project_raw(H_bf16, T, d_model, Wa_kv, Wa_z, L.c0, L.z0, L.wt, ws, st)) != CSA2_OK) return rc;
-  if ((rc = project_raw(H_bf16, T, d_model, Wb_kv, Wb_z, L.c1, L.z1, L.wt, ws, st)) != CSA2_OK) return rc;
+  if ((rc = project_raw(H_bf16, T, d_model, Wa_kv, Wa_z, L.c0, L.z0, ws, st)) != CSA2_OK) return rc;
+  if ((rc = project_raw(H_bf16, T, d_model, Wb_kv, Wb_z, L.c1, L.z1, ws, st)) != CSA2_OK) return rc;
   const int64_t n = T / m;
   KernelTimer timer("k_pool_overlap", st);
   k_pool_overlap<<<(unsigned)cdiv(n * kDMain, 256), 256, 0, st>>>(L.c0, L.z0, L.c1, L.z1, Ba, Bb, n, m, out);
@@ -831,7 +1025,7 @@ extern "C" csa2_status csa2_compress_hca(const void* H_bf16, int64_t T, int32_t 
   cudaStream_t st = (cudaStream_t)stream;
   if (reset_error(ws, st) != CSA2_OK) return CSA2_ERR_CUDA;
   if (T == 0) return CSA2_OK;
-  if ((rc = project_raw(H_bf16, T, d_model, W_kv, W_z, L.c0, L.z0, L.wt, ws, st)) != CSA2_OK) return rc;
+  if ((rc = project_raw(H_bf16, T, d_model, W_kv, W_z, L.c0, L.z0, ws, st)) != CSA2_OK) return rc;
   const int64_t n = T / m;
   KernelTimer timer("k_pool_bias", st);
   k_pool_bias<<<(unsigned)cdiv(n * kDMain, 256), 256, 0, st>>>(L.c0, L.z0, Bp, n, m, out);

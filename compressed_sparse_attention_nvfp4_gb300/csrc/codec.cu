@@ -7,23 +7,6 @@
 
 namespace csa2 {
 
-// Entry e of a quantize launch goes to plane row dest_row(d, e): contiguous rows
-// e0 + e, or (scattered) slot[e] * stride + entry[e], skipped and reported when
-// outside the planes.
-__device__ __forceinline__ int64_t dest_row(const QDest& d, int64_t e) {
-  if (!d.slot) return d.e0 + e;
-  const int32_t sl = d.slot[e];
-  const int64_t en = d.entry[e];
-  if (sl < 0 || sl >= d.n_slots || en < 0 || en >= d.stride) {
-    if (d.ws) report_error(d.ws, CSA2_ERR_INDEX_RANGE, sl < 0 || sl >= d.n_slots ? (long long)sl : en);
-    return -1;
-  }
-  return (int64_t)sl * d.stride + en;
-}
-__device__ __forceinline__ int64_t dest_pos(const QDest& d, int64_t e) {
-  return d.pos ? d.pos[e] : d.pos_first + e * d.pos_step;
-}
-
 __global__ void k_quantize_main(const float* __restrict__ x, int64_t n, uint8_t* __restrict__ codes,
                                 uint8_t* __restrict__ scales, QDest d) {
   int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -54,43 +37,8 @@ __global__ void k_quantize_main_nr(const float* __restrict__ x, int64_t n, const
   if (e >= n) return;  // whole warps leave together
   const int64_t row = dest_row(d, e);
   if (row < 0) return;  // the same for the whole warp
-  float v[16];
-  const float4* src = reinterpret_cast<const float4*>(x + e * kDMain + lane * 16);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float4 f = src[i];
-    v[4 * i] = f.x;
-    v[4 * i + 1] = f.y;
-    v[4 * i + 2] = f.z;
-    v[4 * i + 3] = f.w;
-  }
-  if (w) {
-    float ss = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) ss = fmaf(v[i], v[i], ss);
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float inv = 1.0f / sqrtf(ss / (float)kDMain + eps);
-    const float4* wv = reinterpret_cast<const float4*>(w + lane * 16);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 g = wv[i];
-      v[4 * i] = g.x * (v[4 * i] * inv);
-      v[4 * i + 1] = g.y * (v[4 * i + 1] * inv);
-      v[4 * i + 2] = g.z * (v[4 * i + 2] * inv);
-      v[4 * i + 3] = g.w * (v[4 * i + 3] * inv);
-    }
-  }
-  if (rope && lane * 16 >= kRopeFirst) {
-    const double pos = (double)dest_pos(d, e);
-#pragma unroll
-    for (int p = 0; p < 8; ++p) {
-      float c, s;
-      rope_cos_sin(th.t[(lane * 16 - kRopeFirst) / 2 + p], pos, c, s);
-      rope_pair(v[2 * p], v[2 * p + 1], c, s);
-    }
-  }
-  quantize_main_group_vals(v, codes + row * 256 + lane * 8, scales + row * 32 + lane);
+  quantize_main_entry_warp(x + e * kDMain, w, eps, rope, th, rope ? (double)dest_pos(d, e) : 0.0,
+                           codes + row * 256, scales + row * 32, lane);
 }
 
 void launch_quantize(const float* Cbar, const float* KI, int64_t n, const csa2_kv_planes* dst, const QDest& d,

@@ -326,6 +326,17 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(const void* base, uint32_t s
   return d;
 }
 
+// N-major (MN-major) operand in 128-byte swizzled rows: row k (one K index) at
+// 128 k holds 64 consecutive N elements, 16-byte slot c at c ^ (k % 8); blocks
+// of 64 N columns `lbo` bytes apart, 8-row K groups `sbo` bytes apart (checked
+// against a CPU product on the GPU: lbo = N-block stride, sbo = K-group stride).
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(const void* base, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = smem_desc_noswizzle(base, lbo, sbo);
+  d |= (uint64_t)2 << 61;  // 128-byte swizzle
+  return d;
+}
+constexpr uint32_t kIdescBMajorMN = 1u << 16;  // instruction descriptor: B operand N-major
+
 // Instruction descriptor of kind::f16: fp32 accumulate, A/B type (0 = f16,
 // 1 = bf16), both K-major, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_f16(uint32_t M, uint32_t N, uint32_t ab_bf16) {
