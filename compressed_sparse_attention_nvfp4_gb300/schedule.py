@@ -103,3 +103,17 @@ def run_step(buf: StepBuffers, stream=None) -> int:
                            buf.out[l], buf.ws_attn, stream=stream)
         calls += 1
     return calls
+
+
+def capture_step(buf: StepBuffers, stream):
+    """A CUDA graph of one run_step on `stream` (a torch stream): replaying it issues the
+    step's kernels with no host work per call.  The buffers stay bound to the graph."""
+    import torch
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        run_step(buf, stream=stream)  # warm: attributes set and maps built outside the capture
+        torch.cuda.current_stream().synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            run_step(buf, stream=stream)
+    return g
