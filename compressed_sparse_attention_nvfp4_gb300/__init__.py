@@ -101,6 +101,7 @@ def lib() -> ctypes.CDLL:
             "csa2_compress_workspace_size": ([i64, i32], sz),
             "csa2_v41_layer_table": ([i32, vp, vp, vp, vp, vp], ctypes.c_int),
             "csa2_check": ([vp, vp, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
+            "csa2_selftest_wait_timeout": ([ctypes.c_longlong, vp, sz, vp], ctypes.c_int),
             "csa2_status_string": ([ctypes.c_int], ctypes.c_char_p),
             "csa2_timing_enable": ([i32], ctypes.c_int),
             "csa2_kernel_times": ([ctypes.POINTER(KernelTime), i32], i32),
@@ -326,6 +327,12 @@ def check(ws, stream=None) -> tuple[int, int]:
     d = ctypes.c_int64(0)
     rc = lib().csa2_check(_ptr(ws), _stream(stream), ctypes.byref(d))
     return rc, d.value
+
+
+def selftest_wait_timeout(budget_cycles: int, ws, stream=None) -> None:
+    """Runs the bounded-wait self-test; csa2.check(ws) then reports the timeout."""
+    _ok(lib().csa2_selftest_wait_timeout(int(budget_cycles), _ptr(ws), _nbytes(ws), _stream(stream)),
+        "csa2_selftest_wait_timeout")
 
 
 def timing_enable(on: bool) -> None:

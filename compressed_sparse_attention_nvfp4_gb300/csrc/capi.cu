@@ -1,5 +1,16 @@
-// C-ABI odds and ends: error reporting and the V4.1-Flash layer table.
+// C-ABI odds and ends: error reporting, the wait self-test and the V4.1-Flash
+// layer table.
 #include "common.cuh"
+#include "ptx.cuh"
+
+// the self-test's barrier: initialised for one arrival that never comes
+__device__ __forceinline__ void ptx_selftest_init(uint64_t* bar) {
+  csa2::ptx::mbar_init(bar, 1);
+  csa2::ptx::fence_mbar_init();
+}
+__device__ __forceinline__ bool ptx_selftest_wait(uint64_t* bar, volatile int* abort_flag, long long budget) {
+  return csa2::ptx::mbar_wait(bar, 0, abort_flag, budget);
+}
 
 extern "C" const char* csa2_status_string(csa2_status s) {
   switch (s) {
@@ -27,6 +38,34 @@ extern "C" csa2_status csa2_check(void* ws, csa2_stream stream, int64_t* detail)
     if (cudaStreamSynchronize(st) != cudaSuccess) return CSA2_ERR_CUDA;
   }
   return (csa2_status)e.code;
+}
+
+// The bounded-wait mechanism every kernel uses, on a barrier that nothing
+// completes: one thread waits `budget` clock cycles, gives up and records
+// CSA2_ERR_DEVICE_TIMEOUT (detail = the cycles it waited) in the workspace.
+namespace csa2 {
+namespace {
+__global__ void k_wait_selftest(long long budget, void* ws) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  ptx_selftest_init(&bar);
+  const long long t0 = clock64();
+  int z = 0;
+  volatile int* abort_flag = &z;
+  if (!ptx_selftest_wait(&bar, abort_flag, budget)) report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, clock64() - t0);
+}
+}  // namespace
+}  // namespace csa2
+
+extern "C" csa2_status csa2_selftest_wait_timeout(long long budget_cycles, void* ws, size_t ws_bytes,
+                                                  csa2_stream stream) {
+  using namespace csa2;
+  if (budget_cycles < 0 || budget_cycles > (1LL << 32)) return CSA2_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256) || ws_bytes < kWsHeader) return CSA2_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (reset_error(ws, st) != CSA2_OK) return CSA2_ERR_CUDA;
+  k_wait_selftest<<<1, 32, 0, st>>>(budget_cycles, ws);
+  return launch_status();
 }
 
 // Layer layout of "DeepSeek-V4.1-Flash: pushing the limits of KV cache

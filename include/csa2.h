@@ -401,6 +401,13 @@ csa2_status csa2_check(void* ws, csa2_stream stream, int64_t* detail);
 
 const char* csa2_status_string(csa2_status s);
 
+/* Self-test of the bounded device-side waits every kernel uses: one thread waits
+ * on a barrier that nothing completes for `budget_cycles` (0 .. 2^32) clock
+ * cycles, gives up and records CSA2_ERR_DEVICE_TIMEOUT in the workspace error
+ * word (detail = cycles waited), which csa2_check then returns; the context stays
+ * usable.  ws: at least 256 bytes, 256-byte aligned. */
+csa2_status csa2_selftest_wait_timeout(long long budget_cycles, void* ws, size_t ws_bytes, csa2_stream stream);
+
 #ifdef __cplusplus
 }
 #endif
