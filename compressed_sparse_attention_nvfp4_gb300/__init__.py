@@ -54,6 +54,18 @@ def norm_rope(norm_weight=None, eps: float = 1e-6, rope: bool = False, rope_base
     return nr
 
 
+class Window(ctypes.Structure):
+    """csa2_window: per-row positions [B][n_swa] and per-query lowest visible position [B] (int64, device)."""
+    _fields_ = [("row_pos", ctypes.c_void_p), ("lo", ctypes.c_void_p)]
+
+
+def window(row_pos, lo) -> Window:
+    """A csa2_window over device int64 arrays; keeps references to both."""
+    win = Window(_ptr(row_pos), _ptr(lo))
+    win._refs = (row_pos, lo)
+    return win
+
+
 class KernelTime(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char_p), ("launches", ctypes.c_int64), ("total_ms", ctypes.c_double)]
 
@@ -73,6 +85,7 @@ def lib() -> ctypes.CDLL:
                                  ctypes.c_size_t)
         pl = ctypes.POINTER(KVPlanes)
         nr = ctypes.POINTER(NormRope)
+        wn = ctypes.POINTER(Window)
         sig = {
             "csa2_quantize_entries": ([vp, vp, i64, pl, i64, vp], ctypes.c_int),
             "csa2_cache_write": ([vp, i64, i32, vp, vp, vp, i32, pl, i32, i64, nr, i64, vp, sz, vp],
@@ -82,7 +95,7 @@ def lib() -> ctypes.CDLL:
             "csa2_cache_append": ([vp, i32, i32, vp, vp, vp, i32, pl, i32, vp, vp, nr, vp, vp, sz, vp],
                                   ctypes.c_int),
             "csa2_cache_append_workspace_size": ([i32, i32, i32], sz),
-            "csa2_swa_append": ([vp, i32, vp, vp, i32, nr, vp, i32, vp], ctypes.c_int),
+            "csa2_swa_append": ([vp, i32, vp, vp, i32, nr, vp, vp, i32, vp], ctypes.c_int),
             "csa2_index_topk": ([pl, i32, vp, i64, vp, vp, i32, ctypes.c_int, i32, i32, vp, vp, vp,
                                  vp, vp, sz, vp], ctypes.c_int),
             "csa2_index_topk_workspace_size": ([i32, i64, i32, i32, i32], sz),
@@ -90,10 +103,10 @@ def lib() -> ctypes.CDLL:
             "csa2_index_topk_prefill_workspace_size": ([i32, i64, i32], sz),
             "csa2_index_topk_noalloc": ([pl, i32, vp, i64, vp, vp, i32, ctypes.c_int, i32, i32, vp,
                                          vp, vp, vp], ctypes.c_int),
-            "csa2_sparse_attn_decode": ([pl, i32, vp, i32, vp, i32, vp, f32, nr, vp, vp, vp, vp, vp, sz,
+            "csa2_sparse_attn_decode": ([pl, i32, vp, i32, vp, i32, vp, f32, nr, vp, vp, wn, vp, vp, vp, sz,
                                          vp], ctypes.c_int),
             "csa2_sparse_attn_workspace_size": ([i32, i32, i32], sz),
-            "csa2_dense_attn_decode": ([pl, i32, vp, i64, vp, i32, vp, f32, nr, vp, vp, vp, vp, vp, sz, vp],
+            "csa2_dense_attn_decode": ([pl, i32, vp, i64, vp, i32, vp, f32, nr, vp, vp, wn, vp, vp, vp, sz, vp],
                                        ctypes.c_int),
             "csa2_dense_attn_workspace_size": ([i32, i64, i32], sz),
             "csa2_compress_overlap": ([vp, i64, i32, vp, vp, vp, vp, vp, vp, i32, vp, vp, sz, vp], ctypes.c_int),
@@ -226,10 +239,11 @@ def cache_append(H, G: int, d_model: int, Wkv, Wz, Wik, m: int, planes: Planes, 
 
 
 def swa_append(x, R: int, pos, n_queries: int, ring, n_win: int, query=None, nr: NormRope | None = None,
-               stream=None) -> None:
-    """Window ring write: row r of x (fp32 [R][512]) -> E4M3 into ring[query[r] or r][pos[r] % n_win]."""
+               stream=None, ring_pos=None) -> None:
+    """Window ring write: row r of x (fp32 [R][512]) -> E4M3 into ring[query[r] or r][pos[r] % n_win];
+    ring_pos (int64 [n_queries][n_win], optional) records the rows' positions."""
     _ok(lib().csa2_swa_append(_ptr(x), R, _ptr(query), _ptr(pos), n_queries,
-                              ctypes.byref(nr) if nr is not None else None, _ptr(ring), n_win,
+                              ctypes.byref(nr) if nr is not None else None, _ptr(ring), _ptr(ring_pos), n_win,
                               _stream(stream)), "csa2_swa_append")
 
 
@@ -279,14 +293,16 @@ def sparse_attn_workspace_size(B: int, k: int, n_swa: int) -> int:
 
 def sparse_attn_decode(planes: Planes, B: int, topk, k: int, swa, n_swa: int, q,
                        softmax_scale: float, out, ws, lse_out=None, stream=None,
-                       q_nr: NormRope | None = None, q_pos=None, sink=None) -> None:
+                       q_nr: NormRope | None = None, q_pos=None, sink=None, win: Window | None = None) -> None:
     """q_nr (norm_rope(...)): RMSNorm / RoPE of the query heads, q_pos int64 [B] (needed with
-    RoPE; the output turns back by -q_pos); sink fp32 [64] per-head sink logits."""
+    RoPE; the output turns back by -q_pos); sink fp32 [64] per-head sink logits; win (window(...)):
+    only window rows at positions >= lo[b] are seen."""
     _ok(lib().csa2_sparse_attn_decode(ctypes.byref(planes.c), B, _ptr(topk), k, _ptr(swa), n_swa,
                                       _ptr(q), softmax_scale,
                                       ctypes.byref(q_nr) if q_nr is not None else None, _ptr(q_pos),
-                                      _ptr(sink), _ptr(out), _ptr(lse_out), _ptr(ws), _nbytes(ws),
-                                      _stream(stream)), "csa2_sparse_attn_decode")
+                                      _ptr(sink), ctypes.byref(win) if win is not None else None, _ptr(out),
+                                      _ptr(lse_out), _ptr(ws), _nbytes(ws), _stream(stream)),
+        "csa2_sparse_attn_decode")
 
 
 def dense_attn_workspace_size(B: int, n_max: int, n_swa: int) -> int:
@@ -295,13 +311,14 @@ def dense_attn_workspace_size(B: int, n_max: int, n_swa: int) -> int:
 
 def dense_attn_decode(planes: Planes, B: int, n_entries, n_max: int, swa, n_swa: int, q,
                       softmax_scale: float, out, ws, lse_out=None, stream=None,
-                      q_nr: NormRope | None = None, q_pos=None, sink=None) -> None:
+                      q_nr: NormRope | None = None, q_pos=None, sink=None, win: Window | None = None) -> None:
     """HCA attention: every entry [0, n_entries[b]) of slot b plus the window rows."""
     _ok(lib().csa2_dense_attn_decode(ctypes.byref(planes.c), B, _ptr(n_entries), n_max, _ptr(swa), n_swa,
                                      _ptr(q), softmax_scale,
                                      ctypes.byref(q_nr) if q_nr is not None else None, _ptr(q_pos),
-                                     _ptr(sink), _ptr(out), _ptr(lse_out), _ptr(ws), _nbytes(ws),
-                                     _stream(stream)), "csa2_dense_attn_decode")
+                                     _ptr(sink), ctypes.byref(win) if win is not None else None, _ptr(out),
+                                     _ptr(lse_out), _ptr(ws), _nbytes(ws), _stream(stream)),
+        "csa2_dense_attn_decode")
 
 
 def compress_workspace_size(T: int, d_model: int) -> int:

@@ -48,6 +48,8 @@ struct AttnExtras {
   int rope;
   const int64_t* qpos;
   const float* sink;
+  const int64_t* win_pos;  // [B][n_swa] position of each window row (< 0: empty), or null: all visible
+  const int64_t* win_lo;   // [B] lowest visible window position
   RopeTheta th;
 };
 
@@ -221,7 +223,7 @@ __device__ __forceinline__ int64_t fetch_index(const int32_t* __restrict__ topk,
 __device__ __forceinline__ void issue_row(RowFetch& f, int64_t idx, const uint8_t* __restrict__ kv_codes,
                                           const uint8_t* __restrict__ kv_scales, int64_t seq_stride,
                                           const uint8_t* __restrict__ swa, int n_swa, int k, int b, int gr,
-                                          int half, void* ws) {
+                                          int half, void* ws, const int64_t* __restrict__ win_pos, int64_t win_lo) {
   f.kind = 0;
   if (gr < k) {
     if (idx >= 0 && idx < seq_stride) {
@@ -234,7 +236,7 @@ __device__ __forceinline__ void issue_row(RowFetch& f, int64_t idx, const uint8_
     } else if (idx != -1 && half == 0) {
       report_error(ws, CSA2_ERR_INDEX_RANGE, idx);
     }
-  } else if (gr - k < n_swa) {
+  } else if (gr - k < n_swa && (!win_pos || win_pos[(int64_t)b * n_swa + (gr - k)] >= win_lo)) {
     const uint4* src = reinterpret_cast<const uint4*>(swa + ((int64_t)b * n_swa + (gr - k)) * kDMain + half * 256);
 #pragma unroll
     for (int i = 0; i < 16; ++i) f.raw[i] = src[i];
@@ -344,6 +346,7 @@ __global__ void __launch_bounds__(kAT, 1) k_attn(
   // indices arrive, then the rows are requested
   const int r = tid % kRows, half = (tid / kRows) & 1;
   RowFetch rf;
+  const int64_t win_lo = ex.win_pos ? max(ex.win_lo[b], (int64_t)0) : 0;  // window rows below it are not seen
   if (warp < kCtlWarp) {
     const int gr = c0 * kRows + r;
     QFetch qf;
@@ -351,7 +354,7 @@ __global__ void __launch_bounds__(kAT, 1) k_attn(
     const int64_t idx0 = fetch_index(topk, dense_n, k, b, gr);
     stage_q<kEx>(S, qf, scale, warp, lane, ex, b);
     ptx::fence_proxy_async_smem();
-    issue_row(rf, idx0, kv_codes, kv_scales, seq_stride, swa, n_swa, k, b, gr, half, ws);
+    issue_row(rf, idx0, kv_codes, kv_scales, seq_stride, swa, n_swa, k, b, gr, half, ws, ex.win_pos, win_lo);
   }
   ptx::tc_fence_before();
   __syncthreads();  // barriers initialised, tensor memory allocated
@@ -431,7 +434,8 @@ __global__ void __launch_bounds__(kAT, 1) k_attn(
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&S.x_full[half]);
       if (i + 1 < nc)
-        issue_row(rf, idx_next, kv_codes, kv_scales, seq_stride, swa, n_swa, k, b, gr_next, half, ws);
+        issue_row(rf, idx_next, kv_codes, kv_scales, seq_stride, swa, n_swa, k, b, gr_next, half, ws, ex.win_pos,
+                  win_lo);
 
       // ---- chunk softmax
       good = ptx::mbar_wait_warp(&S.s_full, par, abort_flag, kAttnWaitBudget) &&
@@ -672,8 +676,10 @@ namespace {
 // entries 0 .. dense_n[b] - 1) joined with n_swa window rows.
 csa2_status attn_run(const csa2_kv_planes* kv, int32_t B, const int32_t* topk, const int32_t* dense_n, int32_t k,
                      const uint8_t* swa_e4m3, int32_t n_swa, const void* q_bf16, float softmax_scale,
-                     const csa2_norm_rope* q_nr, const int64_t* q_pos, const float* sink, float* out,
-                     float* lse_out, void* ws, size_t ws_bytes, cudaStream_t st) {
+                     const csa2_norm_rope* q_nr, const int64_t* q_pos, const float* sink, const csa2_window* win,
+                     float* out, float* lse_out, void* ws, size_t ws_bytes, cudaStream_t st) {
+  if (win && (!win->row_pos || !win->lo || !aligned(win->row_pos, 8) || !aligned(win->lo, 8)))
+    return CSA2_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.0f) || softmax_scale > 3.0e38f) return CSA2_ERR_INVALID_ARG;  // positive, finite
   if (q_nr && (!norm_rope_ok(q_nr) || (q_nr->rope && !q_pos))) return CSA2_ERR_INVALID_ARG;
   if ((q_pos && !aligned(q_pos, 8)) || (sink && !aligned(sink, 4))) return CSA2_ERR_INVALID_ARG;
@@ -683,6 +689,8 @@ csa2_status attn_run(const csa2_kv_planes* kv, int32_t B, const int32_t* topk, c
   ex.rope = q_nr ? q_nr->rope : 0;
   ex.qpos = ex.rope ? q_pos : nullptr;
   ex.sink = sink;
+  ex.win_pos = win && n_swa > 0 ? win->row_pos : nullptr;
+  ex.win_lo = win && n_swa > 0 ? win->lo : nullptr;
   if (ex.rope) ex.th = make_rope_theta(q_nr->rope_base);
   if (!aligned(q_bf16, 16) || !aligned(out, 16) || (swa_e4m3 && !aligned(swa_e4m3, 16)))
     return CSA2_ERR_INVALID_ARG;
@@ -718,14 +726,14 @@ extern "C" csa2_status csa2_sparse_attn_decode(const csa2_kv_planes* kv, int32_t
                                                int32_t k, const uint8_t* swa_e4m3, int32_t n_swa,
                                                const void* q_bf16, float softmax_scale,
                                                const csa2_norm_rope* q_nr, const int64_t* q_pos,
-                                               const float* sink, float* out, float* lse_out, void* ws,
-                                               size_t ws_bytes, csa2_stream stream) {
+                                               const float* sink, const csa2_window* win, float* out,
+                                               float* lse_out, void* ws, size_t ws_bytes, csa2_stream stream) {
   using namespace csa2;
   if (!planes_ok(kv) || B <= 0 || B > 65535 || k < 0 || k > CSA2_MAX_TOPK || n_swa < 0 || n_swa > CSA2_MAX_SWA)
     return CSA2_ERR_INVALID_ARG;
   if ((k > 0 && !topk) || (n_swa > 0 && !swa_e4m3) || !q_bf16 || !out) return CSA2_ERR_INVALID_ARG;
-  return attn_run(kv, B, topk, nullptr, k, swa_e4m3, n_swa, q_bf16, softmax_scale, q_nr, q_pos, sink, out, lse_out,
-                  ws, ws_bytes, (cudaStream_t)stream);
+  return attn_run(kv, B, topk, nullptr, k, swa_e4m3, n_swa, q_bf16, softmax_scale, q_nr, q_pos, sink, win, out,
+                  lse_out, ws, ws_bytes, (cudaStream_t)stream);
 }
 
 extern "C" size_t csa2_dense_attn_workspace_size(int32_t B, int64_t n_max, int32_t n_swa) {
@@ -737,8 +745,8 @@ extern "C" csa2_status csa2_dense_attn_decode(const csa2_kv_planes* kv, int32_t 
                                               int64_t n_max, const uint8_t* swa_e4m3, int32_t n_swa,
                                               const void* q_bf16, float softmax_scale,
                                               const csa2_norm_rope* q_nr, const int64_t* q_pos,
-                                              const float* sink, float* out, float* lse_out, void* ws,
-                                              size_t ws_bytes, csa2_stream stream) {
+                                              const float* sink, const csa2_window* win, float* out,
+                                              float* lse_out, void* ws, size_t ws_bytes, csa2_stream stream) {
   using namespace csa2;
   if (!planes_ok(kv) || B <= 0 || B > 65535 || n_max < 0 || n_max > CSA2_MAX_DENSE || n_max > kv->seq_stride ||
       n_swa < 0 || n_swa > CSA2_MAX_SWA)
@@ -746,5 +754,5 @@ extern "C" csa2_status csa2_dense_attn_decode(const csa2_kv_planes* kv, int32_t 
   if ((n_max > 0 && !n_entries) || (n_swa > 0 && !swa_e4m3) || !q_bf16 || !out) return CSA2_ERR_INVALID_ARG;
   if (n_entries && !aligned(n_entries, 4)) return CSA2_ERR_INVALID_ARG;
   return attn_run(kv, B, nullptr, n_entries, (int32_t)n_max, swa_e4m3, n_swa, q_bf16, softmax_scale, q_nr, q_pos,
-                  sink, out, lse_out, ws, ws_bytes, (cudaStream_t)stream);
+                  sink, win, out, lse_out, ws, ws_bytes, (cudaStream_t)stream);
 }

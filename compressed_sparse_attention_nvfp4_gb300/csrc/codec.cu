@@ -101,7 +101,8 @@ __global__ void k_quantize_query_mxfp4(const uint16_t* __restrict__ q, int64_t n
 // position or a query outside [0, n_queries) are skipped.
 __global__ void k_swa_append(const float* __restrict__ x, int32_t R, const int32_t* __restrict__ query,
                              const int64_t* __restrict__ pos, int32_t n_queries, const float* __restrict__ w,
-                             float eps, int rope, RopeTheta th, uint8_t* __restrict__ ring, int32_t n_win) {
+                             float eps, int rope, RopeTheta th, uint8_t* __restrict__ ring,
+                             int64_t* __restrict__ ring_pos, int32_t n_win) {
   const int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;
   if (r >= R) return;
@@ -150,17 +151,18 @@ __global__ void k_swa_append(const float* __restrict__ x, int32_t R, const int32
            (float_to_e4m3(v[4 * i + 3]) << 24);
   uint8_t* dst = ring + ((int64_t)b * n_win + p % n_win) * kDMain + lane * 16;
   *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+  if (ring_pos && lane == 0) ring_pos[(int64_t)b * n_win + p % n_win] = p;
 }
 
 }  // namespace csa2
 
 extern "C" csa2_status csa2_swa_append(const float* x, int32_t R, const int32_t* query, const int64_t* pos,
-                                       int32_t n_queries, const csa2_norm_rope* nr, uint8_t* ring, int32_t n_win,
-                                       csa2_stream stream) {
+                                       int32_t n_queries, const csa2_norm_rope* nr, uint8_t* ring,
+                                       int64_t* ring_pos, int32_t n_win, csa2_stream stream) {
   using namespace csa2;
   if (R < 0 || n_queries <= 0 || n_win <= 0) return CSA2_ERR_INVALID_ARG;
   if (R > 0 && (!x || !pos || !ring || !aligned(x, 16) || !aligned(pos, 8) || !aligned(ring, 16) ||
-                (query && !aligned(query, 4))))
+                (query && !aligned(query, 4)) || (ring_pos && !aligned(ring_pos, 8))))
     return CSA2_ERR_INVALID_ARG;
   if (nr && !norm_rope_ok(nr)) return CSA2_ERR_INVALID_ARG;
   if (R == 0) return CSA2_OK;
@@ -169,7 +171,7 @@ extern "C" csa2_status csa2_swa_append(const float* x, int32_t R, const int32_t*
   KernelTimer timer("k_swa_append", st);
   k_swa_append<<<(unsigned)cdiv((int64_t)R * 32, 256), 256, 0, st>>>(
       x, R, query, pos, n_queries, nr ? nr->norm_weight : nullptr, nr ? nr->norm_eps : 0.0f, rope ? 1 : 0,
-      rope ? make_rope_theta(nr->rope_base) : RopeTheta{}, ring, n_win);
+      rope ? make_rope_theta(nr->rope_base) : RopeTheta{}, ring, ring_pos, n_win);
   return launch_status();
 }
 

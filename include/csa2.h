@@ -187,10 +187,12 @@ size_t csa2_cache_append_workspace_size(int32_t G, int32_t d_model, int32_t m);
  * ring[query][pos mod n_win][512] (ring: [n_queries][n_win][512] bytes).  Rows with a
  * negative position or a query outside [0, n_queries) are skipped.  The ring is the
  * swa_e4m3 input of csa2_sparse_attn_decode (n_swa = the rows written so far, at most
- * n_win): the attention does not depend on the order of its rows. */
+ * n_win): the attention does not depend on the order of its rows.  ring_pos (or NULL),
+ * [n_queries][n_win] int64, receives each written row's position: the row positions of
+ * csa2_window (initialise it to -1 for empty slots). */
 csa2_status csa2_swa_append(const float* x, int32_t R, const int32_t* query, const int64_t* pos,
-                            int32_t n_queries, const csa2_norm_rope* nr, uint8_t* ring, int32_t n_win,
-                            csa2_stream stream);
+                            int32_t n_queries, const csa2_norm_rope* nr, uint8_t* ring, int64_t* ring_pos,
+                            int32_t n_win, csa2_stream stream);
 
 /* ------------------------------------------------------- V4 compressors */
 
@@ -306,6 +308,12 @@ csa2_status csa2_index_topk_noalloc(const csa2_kv_planes* kv, int32_t B, const i
 
 /* ------------------------------------------------------- sparse attention */
 
+/* Window bounds of an attention call (device arrays; see csa2_sparse_attn_decode). */
+typedef struct {
+  const int64_t* row_pos; /* [B][n_swa] position of each window row, < 0 = empty */
+  const int64_t* lo;      /* [B] lowest visible position of each query */
+} csa2_window;
+
 /* Sparse MQA decode over the selected entries joined with the sliding window:
  *   X_b = [ dequant(main KV of topk[b][i], i < k, skipping -1) ; SWA rows of b ]
  *   out[b,h,:] = sum_s softmax_s(softmax_scale * q[b,h,:] . X_b[s]) X_b[s]
@@ -327,13 +335,18 @@ csa2_status csa2_index_topk_noalloc(const csa2_kv_planes* kv, int32_t B, const i
  *   q_pos     [B] int64 query positions (required when q_nr->rope);
  *   sink      [64] fp32 per-head logits z'_h: exp(z'_h) joins every softmax
  *             denominator (and lse); with no rows out = 0 and lse = z'_h.
+ *   win       window bounds (SWA bounded replay, "DeepSeek-V4.1-Flash: pushing the
+ *             limits of KV cache compression", section 6: a replay from position s
+ *             lets query i see the window [max(s, i - n_win + 1), i]): window row r
+ *             of query b joins the softmax only if win->row_pos[b][r] >= max(win->lo[b], 0)
+ *             (row_pos < 0 marks an empty row); NULL: every row given is seen.
  * The normalised / rotated q is rounded to f16 for the tensor cores. */
 csa2_status csa2_sparse_attn_decode(const csa2_kv_planes* kv, int32_t B, const int32_t* topk,
                                     int32_t k, const uint8_t* swa_e4m3, int32_t n_swa,
                                     const void* q_bf16, float softmax_scale,
                                     const csa2_norm_rope* q_nr, const int64_t* q_pos,
-                                    const float* sink, float* out, float* lse_out, void* ws,
-                                    size_t ws_bytes, csa2_stream stream);
+                                    const float* sink, const csa2_window* win, float* out,
+                                    float* lse_out, void* ws, size_t ws_bytes, csa2_stream stream);
 size_t csa2_sparse_attn_workspace_size(int32_t B, int32_t k, int32_t n_swa);
 
 /* Dense MQA decode over every compressed entry a query sees, joined with the
@@ -349,8 +362,9 @@ size_t csa2_sparse_attn_workspace_size(int32_t B, int32_t k, int32_t n_swa);
 csa2_status csa2_dense_attn_decode(const csa2_kv_planes* kv, int32_t B, const int32_t* n_entries,
                                    int64_t n_max, const uint8_t* swa_e4m3, int32_t n_swa,
                                    const void* q_bf16, float softmax_scale, const csa2_norm_rope* q_nr,
-                                   const int64_t* q_pos, const float* sink, float* out, float* lse_out,
-                                   void* ws, size_t ws_bytes, csa2_stream stream);
+                                   const int64_t* q_pos, const float* sink, const csa2_window* win,
+                                   float* out, float* lse_out, void* ws, size_t ws_bytes,
+                                   csa2_stream stream);
 size_t csa2_dense_attn_workspace_size(int32_t B, int64_t n_max, int32_t n_swa);
 
 /* ---------------------------------------------------------------- schedule */

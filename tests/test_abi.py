@@ -109,7 +109,7 @@ def test_host_validation_without_gpu(L):
                            None, None, 0, None)
     assert rc == 1
     rc = L.csa2_sparse_attn_decode(ctypes.byref(P), 1, None, 512, None, 0, None, 1.0, None, None,
-                                   None, None, None, None, 0, None)
+                                   None, None, None, None, None, 0, None)
     assert rc == 1
     assert L.csa2_quantize_index_query(None, -1, None, None) == 1
     assert L.csa2_quantize_index_query(16, 4, None, None) == 1      # no output
@@ -132,19 +132,19 @@ def test_host_validation_without_gpu(L):
                              256, 1 << 20, None) == 2  # block != 8
     assert L.csa2_cache_write(16, 64, 5120, 16, 16, 16, 3, ctypes.byref(fake), 0, 0, None, 0, 256,
                               1 << 30, None) == 2  # m = 3
-    assert L.csa2_sparse_attn_decode(ctypes.byref(fake), 1, 16, 512, 16, 129, 16, 1.0, None, None, None,
+    assert L.csa2_sparse_attn_decode(ctypes.byref(fake), 1, 16, 512, 16, 129, 16, 1.0, None, None, None, None,
                                      16, None, 256, 1 << 30, None) == 1  # n_swa > 128
     for bad_scale in (0.0, -0.04, float("inf"), float("nan")):  # the softmax scale must be positive, finite
         assert L.csa2_sparse_attn_decode(ctypes.byref(fake), 1, 16, 512, 16, 128, 16, bad_scale, None, None,
-                                         None, 16, None, 256, 1 << 30, None) == 1
+                                         None, None, 16, None, 256, 1 << 30, None) == 1
     # RoPE of the query needs the positions; a base <= 1 and a negative eps are rejected
     nr = csa2.NormRope(None, 1e-6, 1, 10000.0)
     assert L.csa2_sparse_attn_decode(ctypes.byref(fake), 1, 16, 512, 16, 128, 16, 0.04, ctypes.byref(nr),
-                                     None, None, 16, None, 256, 1 << 30, None) == 1
+                                     None, None, None, 16, None, 256, 1 << 30, None) == 1
     for bad in (csa2.NormRope(None, 1e-6, 1, 1.0), csa2.NormRope(None, -1.0, 0, 10000.0),
                 csa2.NormRope(4, 1e-6, 0, 10000.0)):  # misaligned weight
         assert L.csa2_sparse_attn_decode(ctypes.byref(fake), 1, 16, 512, 16, 128, 16, 0.04, ctypes.byref(bad),
-                                         16, None, 16, None, 256, 1 << 30, None) == 1
+                                         16, None, None, 16, None, 256, 1 << 30, None) == 1
         assert L.csa2_cache_write(16, 64, 5120, 16, 16, 16, 2, ctypes.byref(fake), 0, 0, ctypes.byref(bad), 0,
                                   256, 1 << 30, None) == 1
 
@@ -165,18 +165,22 @@ def test_v4_compressor_and_dense_validation_without_gpu(L):
     assert L.csa2_compress_hca(16, 256, 64, 8, 16, 16, 128, 16, 256, 1 << 30, None) == 1  # misaligned W
     assert csa2.compress_workspace_size(65536, 4096) >= 4 * 65536 * 512 * 4
     # dense attention: n_max beyond the slot or the limit, no counts, bad scale
-    assert L.csa2_dense_attn_decode(ctypes.byref(fake), 1, 16, 101, None, 0, 16, 0.04, None, None, None, 16,
+    assert L.csa2_dense_attn_decode(ctypes.byref(fake), 1, 16, 101, None, 0, 16, 0.04, None, None, None, None, 16,
                                     None, 256, 1 << 30, None) == 1
     big = csa2.KVPlanes(16, 16, 16, 16, 1 << 20)
-    assert L.csa2_dense_attn_decode(ctypes.byref(big), 1, 16, 65537, None, 0, 16, 0.04, None, None, None, 16,
+    assert L.csa2_dense_attn_decode(ctypes.byref(big), 1, 16, 65537, None, 0, 16, 0.04, None, None, None, None, 16,
                                     None, 256, 1 << 30, None) == 1
-    assert L.csa2_dense_attn_decode(ctypes.byref(fake), 1, None, 50, None, 0, 16, 0.04, None, None, None, 16,
+    assert L.csa2_dense_attn_decode(ctypes.byref(fake), 1, None, 50, None, 0, 16, 0.04, None, None, None, None, 16,
                                     None, 256, 1 << 30, None) == 1
-    assert L.csa2_dense_attn_decode(ctypes.byref(fake), 1, 16, 50, None, 0, 16, -1.0, None, None, None, 16,
+    assert L.csa2_dense_attn_decode(ctypes.byref(fake), 1, 16, 50, None, 0, 16, -1.0, None, None, None, None, 16,
                                     None, 256, 1 << 30, None) == 1
-    assert L.csa2_dense_attn_decode(ctypes.byref(fake), 1, 16, 50, None, 0, 16, 0.04, None, None, None, 16,
+    assert L.csa2_dense_attn_decode(ctypes.byref(fake), 1, 16, 50, None, 0, 16, 0.04, None, None, None, None, 16,
                                     None, 256, 16, None) == 3
     assert csa2.dense_attn_workspace_size(1, 8192, 128) > csa2.dense_attn_workspace_size(1, 0, 128) > 0
+    # window bounds need both arrays, 8-byte aligned
+    for bad_win in (csa2.Window(None, 16), csa2.Window(16, None), csa2.Window(12, 16)):
+        assert L.csa2_sparse_attn_decode(ctypes.byref(fake), 1, 16, 512, 16, 128, 16, 0.04, None, None, None,
+                                         ctypes.byref(bad_win), 16, None, 256, 1 << 30, None) == 1
 
 
 def test_workspace_queries(L):

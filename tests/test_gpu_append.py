@@ -4,7 +4,7 @@ one entry of its own slot, computed as the prefill write computes it) and csa2_s
 import numpy as np
 import pytest
 
-from gpu_common import csa2, require_gpu, to_dev, torch
+from gpu_common import SmallCache, csa2, require_gpu, to_dev, torch
 from synth import workloads as W
 from test_gpu_cache_write import U, _decided_index, _decided_main, _error_bounds, _norm_rope_bounds
 
@@ -116,3 +116,67 @@ def test_swa_append_ring(oracle_mod, nr):
                 assert np.all(got[q, s] == 0xA5)
     # the ring is the attention's window input: the order of its rows does not matter
     assert csa2.sparse_attn_workspace_size(nq, 0, n_win) > 0
+
+
+def test_swa_append_records_positions():
+    R, nq, n_win = 10, 3, 8
+    x = np.random.default_rng(6).standard_normal((R, 512)).astype(np.float32)
+    query = np.array([0, 1, 2, 0, 1, 2, 0, 1, 2, 0], np.int32)
+    pos = np.array([0, 1, 2, 9, 12, 1_000_003, 3, -5, 7, 14], np.int64)
+    ring = torch.zeros((nq, n_win, 512), dtype=torch.uint8, device="cuda")
+    ring_pos = torch.full((nq, n_win), -1, dtype=torch.int64, device="cuda")
+    csa2.swa_append(to_dev(x), R, to_dev(pos), nq, ring, n_win, query=to_dev(query), ring_pos=ring_pos)
+    torch.cuda.synchronize()
+    ref = np.full((nq, n_win), -1, np.int64)
+    for r in range(R):
+        if pos[r] >= 0:
+            ref[query[r], pos[r] % n_win] = pos[r]
+    assert np.array_equal(ring_pos.cpu().numpy(), ref)
+
+
+def test_bounded_replay_window(oracle_mod):
+    """SWA bounded replay ("DeepSeek-V4.1-Flash: pushing the limits of KV cache compression",
+    section 6): after a replay from position s the query at position i sees the window rows
+    at [max(s, i - n_win + 1), i] only.  The ring holds stale rows from before s beside the
+    replayed ones; with the window bounds the attention equals the oracle's over exactly the
+    visible rows (built on the host with the oracle's own row encoder)."""
+    from parity import check_attention
+
+    n_win, B, N, k = 128, 2, 700, 64
+    c = SmallCache(oracle_mod, 13, B, N)
+    rng = np.random.default_rng(13)
+    q = W.attn_query(13, 0, B)
+    topk = np.sort(np.stack([rng.choice(N, k, replace=False) for _ in range(B)]), axis=1).astype(np.int32)
+    i_pos = np.array([1150, 1130], np.int64)   # the queries' positions
+    s_rep = np.array([1100, 1000], np.int64)   # where each query's replay started
+    ring = np.zeros((B, n_win, 512), np.uint8)
+    ring_pos = np.full((B, n_win), -1, np.int64)
+    for b in range(B):
+        # stale rows (a pre-miss window), then the replay from s_rep[b] up to the query
+        for p in list(range(int(i_pos[b]) - 250, int(s_rep[b]))) + list(range(int(s_rep[b]), int(i_pos[b]) + 1)):
+            row, _ = oracle_mod.swa_row(2.0 * rng.standard_normal(512))
+            ring[b, p % n_win] = row
+            ring_pos[b, p % n_win] = p
+    lo = np.maximum(s_rep, i_pos - n_win + 1)
+    out = torch.empty((B, 64, 512), dtype=torch.float32, device="cuda")
+    lse = torch.empty((B, 64), dtype=torch.float32, device="cuda")
+    ws = csa2.workspace(csa2.sparse_attn_workspace_size(B, k, n_win))
+    win = csa2.window(to_dev(ring_pos), to_dev(lo))
+    scale = 1.0 / np.sqrt(512.0)
+    csa2.sparse_attn_decode(c.planes, B, to_dev(topk), k, to_dev(ring), n_win, to_dev(q.view(np.int16)), scale, out,
+                            ws, lse_out=lse, win=win)
+    assert csa2.check(ws)[0] == 0
+    got, glse = out.cpu().numpy(), lse.cpu().numpy()
+    for b in range(B):
+        vis = ring_pos[b] >= lo[b]
+        assert vis.sum() == min(n_win, i_pos[b] - lo[b] + 1)
+        kvc, kvs, _, _ = c.oracle_slot(b)
+        ro, rl = oracle_mod.attention(kvc, kvs, topk[b], ring[b][vis], q[b], scale)
+        check_attention(got[b:b + 1], ro[None])
+        assert np.allclose(glse[b], rl, rtol=1e-4, atol=1e-4)
+    # a bound above every row: no window at all (and no entries: out = 0, lse = -inf)
+    none = csa2.window(to_dev(ring_pos), to_dev(np.full(B, 10**9, np.int64)))
+    csa2.sparse_attn_decode(c.planes, B, to_dev(topk), 0, to_dev(ring), n_win, to_dev(q.view(np.int16)), scale, out,
+                            ws, lse_out=lse, win=none)
+    assert csa2.check(ws)[0] == 0
+    assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
