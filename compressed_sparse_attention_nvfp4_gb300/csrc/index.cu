@@ -363,6 +363,7 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
   __shared__ int s_need, s_shift0;
   __shared__ int s_base_eq, s_base_out;
   __shared__ int s_ncomp;                 // keys in the compacted list (may exceed kCompCap: then unused)
+  __shared__ int s_gtotal, s_goff;        // first digit's threshold bin: cluster total, this CTA's offset
   __shared__ uint32_t comp_s[kCompCap];   // keys in the first pass's threshold bin
 
   cg::cluster_group cluster = cg::this_cluster();
@@ -495,7 +496,8 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
         if ((kk & mask) == prefix) atomicAdd(&myhist[(shift >= 0 ? kk >> shift : kk << -shift) & 255u], 1u);
       }
     }
-    for (int v = 0; v < ((pass > 0 && ncomp <= kCompCap) ? 0 : nslot); ++v) {
+    const int vend = (pass > 0 && ncomp <= kCompCap) ? 0 : nslot;
+    for (int v = 0; v < vend; ++v) {
       const uint4 k4 = myslots[v ^ swz];
       const uint32_t kk4[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
@@ -530,13 +532,16 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
     cluster.sync();
     const int need = s_need;
     const int bin = kBins - 1 - tid;  // negative for threads beyond the 256 bins
-    unsigned h = 0;
+    unsigned h = 0, below = 0;  // the bin's cluster total and its count in the ranks before this CTA
     if (bin >= 0) {
       unsigned hr[kSelCluster];
 #pragma unroll
       for (int r = 0; r < kSelCluster; ++r) hr[r] = r < ncl ? *cluster.map_shared_rank(&ch[bin], r) : 0u;
 #pragma unroll
-      for (int r = 0; r < kSelCluster; ++r) h += hr[r];
+      for (int r = 0; r < kSelCluster; ++r) {
+        h += hr[r];
+        below += r < rank ? hr[r] : 0u;
+      }
     }
     int cum = (int)h;
     ScanI(scan_tmp).InclusiveSum(cum, cum);
@@ -545,21 +550,73 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
       s_prefix = prefix | (shift >= 0 ? (uint32_t)bin << shift : (uint32_t)bin >> -shift);
       s_mask = mask | (shift >= 0 ? 255u << shift : 255u >> -shift);
       s_need = need - (cum - (int)h);
+      s_gtotal = (int)h;
+      s_goff = (int)below;
     }
     __syncthreads();
     if (pass == 0 && shift > 0) {  // more digits follow: keep the threshold bin's keys
       const uint32_t p2 = s_prefix, m2 = s_mask;
+      // the bin's keys of the whole cluster fit one CTA: gather them into rank 0,
+      // which finishes the digits alone (no cluster barrier per digit)
+      const bool gather = s_gtotal <= kCompCap;
+      uint32_t* dst = gather ? cluster.map_shared_rank(comp_s, 0) + s_goff : comp_s;
+      // first the matches as a mask (loads and compares only), then one slot
+      // reservation per thread and the few stores
+      uint64_t mm = 0;
       for (int v = 0; v < nslot; ++v) {
         const uint4 k4 = myslots[v ^ swz];
         const uint32_t kk4[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          if (kk4[i] != 0u && (kk4[i] & m2) == p2) {
-            const int j = atomicAdd(&s_ncomp, 1);
-            if (j < kCompCap) comp_s[j] = kk4[i];
-          }
+        for (int i = 0; i < 4; ++i) mm |= (uint64_t)(kk4[i] != 0u && (kk4[i] & m2) == p2) << (4 * v + i);
+      }
+      if (mm) {
+        int j = atomicAdd(&s_ncomp, __popcll(mm));
+        while (mm) {
+          const int bit = __ffsll((long long)mm) - 1;
+          mm &= mm - 1;
+          const uint32_t kk = reinterpret_cast<const uint32_t*>(&myslots[(bit >> 2) ^ swz])[bit & 3];
+          if (j < kCompCap) dst[j] = kk;
+          ++j;
+        }
       }
       __syncthreads();
+      if (gather) {
+        cluster.sync();  // every CTA's keys are in rank 0
+        if (rank == 0) {
+          const int total = s_gtotal;
+          for (int sh = shift - 8; sh > -8; sh -= 8) {
+            for (int d = lane; d < kBins; d += 32) myhist[d] = 0;
+            __syncthreads();
+            const uint32_t pf = s_prefix, mk = s_mask;
+            for (int j = tid; j < total; j += NT) {  // per-warp histograms, as in the cluster passes
+              const uint32_t kk = comp_s[j];
+              if ((kk & mk) == pf) atomicAdd(&myhist[(sh >= 0 ? kk >> sh : kk << -sh) & 255u], 1u);
+            }
+            __syncthreads();
+            const int nd = s_need;
+            unsigned hb = 0;
+            if (bin >= 0) {
+#pragma unroll 8
+              for (int w = 0; w < kWarpsSel; ++w) hb += whist[w][bin];
+            }
+            int cb = (int)hb;
+            ScanI(scan_tmp).InclusiveSum(cb, cb);
+            __syncthreads();
+            if (bin >= 0 && cb >= nd && cb - (int)hb < nd) {
+              s_prefix = pf | (sh >= 0 ? (uint32_t)bin << sh : (uint32_t)bin >> -sh);
+              s_mask = mk | (sh >= 0 ? 255u << sh : 255u >> -sh);
+              s_need = nd - (cb - (int)hb);
+            }
+            __syncthreads();
+          }
+          if (wid == 0 && lane < ncl) {  // the threshold and the ties to take, to every CTA
+            *cluster.map_shared_rank(&s_prefix, lane) = s_prefix;
+            *cluster.map_shared_rank(&s_need, lane) = s_need;
+          }
+        }
+        cluster.sync();
+        break;
+      }
     }
   }
   const uint32_t T = s_prefix;
