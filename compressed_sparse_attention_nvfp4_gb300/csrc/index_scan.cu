@@ -262,7 +262,47 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t tmem = S.tmem_base;
 
   if (my_tiles > 0) {
-    if (warp == 0) {
+    if (warp == 0 && pooled) {
+      // ------------------------------------------------------------ producer (pool)
+      if (lane == 0) {
+        Ring<kStages> st(0);
+        for (int i = 0; i < my_tiles; ++i, st.step(1)) {
+          const int s = st.slot;
+          const uint32_t ph = st.phase;
+          // stage s is free once the MMAs of tile i - kStages completed
+          if (!ptx::mbar_wait(&S.tile_done[s], ph ^ 1u, abort_flag, kWaitBudget)) {
+            scan_abort(S, p.ws, 1);
+            break;
+          }
+          const int64_t t = t_begin + i;
+          int pbv[16];
+          uint32_t cnt[16];
+          uint32_t cbytes = 0, sbytes = 0;
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const int64_t slot = t * 16 + u;
+            pbv[u] = slot < p.keep ? p.pool[(int64_t)b * p.keep + slot] : -1;
+            const int64_t base = (int64_t)pbv[u] * 8;
+            cnt[u] = (pbv[u] >= 0 && base < n) ? (uint32_t)min((int64_t)8, n - base) : 0u;
+            cbytes += cnt[u] ? 8u * 64u : 0u;
+            sbytes += scale_bulk ? (cnt[u] & ~3u) * 4u : 0u;
+          }
+          ptx::mbar_arrive_expect_tx(&S.sfull[s], sbytes);
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const uint32_t c4 = scale_bulk ? (cnt[u] & ~3u) : 0u;
+            if (c4) ptx::bulk_g2s(S.scales[s] + u * 32, scales_b + (int64_t)pbv[u] * 8 * 4, c4 * 4u, &S.sfull[s]);
+          }
+          ptx::mbar_arrive_expect_tx(&S.full[s], cbytes);
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            if (!cnt[u]) continue;
+            const int64_t base = (int64_t)pbv[u] * 8;
+            ptx::tma_load_2d(S.codes[s] + u * 1024, &map_block, 0, (int)(srow + base), &S.full[s]);
+          }
+        }
+      }
+    } else if (warp == 0) {
       // ------------------------------------------------------------ producer
       if (lane == 0) {
         // the keys are read once: keep them from evicting the block maxima and
@@ -277,44 +317,14 @@ __global__ void __launch_bounds__(kThreads, 2)
             scan_abort(S, p.ws, 1);
             break;
           }
-          const int64_t t = t_begin + i;
-          if (!pooled) {
-            const int64_t j0 = t * kTile;
-            const uint32_t cnt = (uint32_t)min((int64_t)kTile, n - j0);
-            const uint32_t cnt4 = scale_bulk ? (cnt & ~3u) : 0u;
-            // scales first, on their own barrier, so that their reorder overlaps the codes' arrival
-            ptx::mbar_arrive_expect_tx(&S.sfull[s], cnt4 * 4u);
-            if (cnt4) ptx::bulk_g2s_hint(S.scales[s], scales_b + j0 * 4, cnt4 * 4u, &S.sfull[s], pol);
-            ptx::mbar_arrive_expect_tx(&S.full[s], kCodeBytes);
-            ptx::tma_load_2d_hint(S.codes[s], &map_tile, 0, (int)(srow + j0), &S.full[s], pol);
-          } else {
-            int pbv[16];
-            uint32_t cnt[16];
-            uint32_t cbytes = 0, sbytes = 0;
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-              const int64_t slot = t * 16 + u;
-              pbv[u] = slot < p.keep ? p.pool[(int64_t)b * p.keep + slot] : -1;
-              const int64_t base = (int64_t)pbv[u] * 8;
-              cnt[u] = (pbv[u] >= 0 && base < n) ? (uint32_t)min((int64_t)8, n - base) : 0u;
-              cbytes += cnt[u] ? 8u * 64u : 0u;
-              sbytes += scale_bulk ? (cnt[u] & ~3u) * 4u : 0u;
-            }
-            ptx::mbar_arrive_expect_tx(&S.sfull[s], sbytes);
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-              const uint32_t c4 = scale_bulk ? (cnt[u] & ~3u) : 0u;
-              if (c4) ptx::bulk_g2s(S.scales[s] + u * 32, scales_b + (int64_t)pbv[u] * 8 * 4, c4 * 4u, &S.sfull[s]);
-            }
-            ptx::mbar_arrive_expect_tx(&S.full[s], cbytes);
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-              if (!cnt[u]) continue;
-              const int64_t base = (int64_t)pbv[u] * 8;
-              ptx::tma_load_2d(S.codes[s] + u * 1024, &map_block, 0, (int)(srow + base),
-                               &S.full[s]);
-            }
-          }
+          const int64_t j0 = (t_begin + i) * kTile;
+          const uint32_t cnt = (uint32_t)min((int64_t)kTile, n - j0);
+          const uint32_t cnt4 = scale_bulk ? (cnt & ~3u) : 0u;
+          // scales first, on their own barrier, so that their reorder overlaps the codes' arrival
+          ptx::mbar_arrive_expect_tx(&S.sfull[s], cnt4 * 4u);
+          if (cnt4) ptx::bulk_g2s_hint(S.scales[s], scales_b + j0 * 4, cnt4 * 4u, &S.sfull[s], pol);
+          ptx::mbar_arrive_expect_tx(&S.full[s], kCodeBytes);
+          ptx::tma_load_2d_hint(S.codes[s], &map_tile, 0, (int)(srow + j0), &S.full[s], pol);
         }
       }
     } else if (warp == 1 || warp == kMmaWarp1) {
