@@ -109,8 +109,8 @@ def lib() -> ctypes.CDLL:
             "csa2_dense_attn_decode": ([pl, i32, vp, i64, vp, i32, vp, f32, nr, vp, vp, wn, vp, vp, vp, sz, vp],
                                        ctypes.c_int),
             "csa2_dense_attn_workspace_size": ([i32, i64, i32], sz),
-            "csa2_compress_overlap": ([vp, i64, i32, vp, vp, vp, vp, vp, vp, i32, vp, vp, sz, vp], ctypes.c_int),
-            "csa2_compress_hca": ([vp, i64, i32, vp, vp, vp, i32, vp, vp, sz, vp], ctypes.c_int),
+            "csa2_compress_overlap": ([vp, i64, i32, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, sz, vp], ctypes.c_int),
+            "csa2_compress_hca": ([vp, i64, i32, vp, vp, vp, i32, i32, vp, vp, sz, vp], ctypes.c_int),
             "csa2_compress_workspace_size": ([i64, i32], sz),
             "csa2_v41_layer_table": ([i32, vp, vp, vp, vp, vp], ctypes.c_int),
             "csa2_check": ([vp, vp, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
@@ -326,17 +326,18 @@ def compress_workspace_size(T: int, d_model: int) -> int:
 
 
 def compress_overlap(H, T: int, d_model: int, Wa_kv, Wb_kv, Wa_z, Wb_z, Ba, Bb, m: int, out, ws,
-                     stream=None) -> None:
-    """Two-path overlapping compressor: out fp32 [T/m][512]."""
+                     stream=None, width: int = 512) -> None:
+    """Two-path overlapping compressor: W_* [d_model][width], out fp32 [T/m][width] (width 512: main
+    latents, 128: V4 indexer keys)."""
     _ok(lib().csa2_compress_overlap(_ptr(H), T, d_model, _ptr(Wa_kv), _ptr(Wb_kv), _ptr(Wa_z), _ptr(Wb_z),
-                                    _ptr(Ba), _ptr(Bb), m, _ptr(out), _ptr(ws), _nbytes(ws), _stream(stream)),
-        "csa2_compress_overlap")
+                                    _ptr(Ba), _ptr(Bb), m, width, _ptr(out), _ptr(ws), _nbytes(ws),
+                                    _stream(stream)), "csa2_compress_overlap")
 
 
-def compress_hca(H, T: int, d_model: int, Wkv, Wz, Bp, m: int, out, ws, stream=None) -> None:
-    """HCA compressor: out fp32 [T/m][512]."""
-    _ok(lib().csa2_compress_hca(_ptr(H), T, d_model, _ptr(Wkv), _ptr(Wz), _ptr(Bp), m, _ptr(out), _ptr(ws),
-                                _nbytes(ws), _stream(stream)), "csa2_compress_hca")
+def compress_hca(H, T: int, d_model: int, Wkv, Wz, Bp, m: int, out, ws, stream=None, width: int = 512) -> None:
+    """HCA compressor: out fp32 [T/m][width]."""
+    _ok(lib().csa2_compress_hca(_ptr(H), T, d_model, _ptr(Wkv), _ptr(Wz), _ptr(Bp), m, width, _ptr(out),
+                                _ptr(ws), _nbytes(ws), _stream(stream)), "csa2_compress_hca")
 
 
 def check(ws, stream=None) -> tuple[int, int]:

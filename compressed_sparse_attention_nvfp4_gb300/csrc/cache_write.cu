@@ -194,14 +194,15 @@ template <bool kNMajorW>
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_cw_tc(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_wkv,
             const __grid_constant__ CUtensorMap map_wz, int64_t T,
-            int d, int m, float* __restrict__ cbar, float* __restrict__ zout, int ksplit,
+            int d, int m, int width, float* __restrict__ cbar, float* __restrict__ zout, int ksplit,
             float* __restrict__ part, void* ws) {
   extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
   TcSmem& S = *reinterpret_cast<TcSmem*>(tc_smem_raw);
   volatile int* abort_flag = &S.abort_flag;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int64_t token_tiles = cdiv(T, kTcM);
-  const int64_t ntiles = token_tiles * (kDMain / 128);
+  const int nblk = width / 128;  // 128-channel blocks of the output (C and Z of the same channels per tile)
+  const int64_t ntiles = token_tiles * nblk;
   const int nk = d / kTcBK;
   // work item = (tile, K slice): with ksplit > 1 each item sums K steps
   // [ks nk / ksplit, (ks + 1) nk / ksplit) and writes raw partial C and Z to part
@@ -232,7 +233,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int64_t item = blockIdx.x; item < nitems; item += gridDim.x) {
         const int64_t tile = item / ksplit;
         const int ks = (int)(item % ksplit);
-        const int t0 = (int)((tile / 4) * kTcM), j = (int)(tile % 4);
+        const int t0 = (int)((tile / nblk) * kTcM), j = (int)(tile % nblk);
         for (int kb = ks * nk / ksplit; kb < (ks + 1) * nk / ksplit; ++kb) {
           if (!ptx::mbar_wait(&S.empty[s], ph ^ 1u, abort_flag, kTcWaitBudget)) {
             tc_abort(S, ws, 31);
@@ -315,8 +316,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       ptx::tc_fence_after();
-      const int64_t t = (tile / 4) * kTcM + sub * 32 + lane;  // this thread's token
-      const int ch0 = (int)(tile % 4) * 128;
+      const int64_t t = (tile / nblk) * kTcM + sub * 32 + lane;  // this thread's token
+      const int ch0 = (int)(tile % nblk) * 128;
       const int64_t e = t / m;                               // its entry
       const bool writer = (lane % m) == 0 && e < n;           // first token of its group
 #pragma unroll 1
@@ -359,11 +360,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         if (writer) {
-          float4* dst = reinterpret_cast<float4*>(cbar + e * kDMain + ch0 + cb * 32);
+          float4* dst = reinterpret_cast<float4*>(cbar + e * width + ch0 + cb * 32);
 #pragma unroll
           for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
           if (zout) {  // unpooled projections (m = 1): Z next to C
-            float4* zd = reinterpret_cast<float4*>(zout + e * kDMain + ch0 + cb * 32);
+            float4* zd = reinterpret_cast<float4*>(zout + e * width + ch0 + cb * 32);
 #pragma unroll
             for (int q = 0; q < 8; ++q)
               zd[q] = make_float4(__uint_as_float(zr[4 * q]), __uint_as_float(zr[4 * q + 1]),
@@ -759,8 +760,8 @@ csa2_status cw_compute(const void* H_bf16, int64_t T, int32_t d_model, const voi
     const int grid = (int)std::min<int64_t>(nitems, sms);
     {
       KernelTimer timer("k_cw_tc", st);
-      kern<<<grid, kTcThreads, smem, st>>>(map_h, map_wkv, map_wz, T, d_model, m, L.cbar, nullptr, L.ksplit, L.part,
-                                           ws);
+      kern<<<grid, kTcThreads, smem, st>>>(map_h, map_wkv, map_wz, T, d_model, m, kDMain, L.cbar, nullptr, L.ksplit,
+                                           L.part, ws);
     }
     if (L.ksplit > 1) {  // the partials' sums, pooling, K^I and the codec in one kernel
       FinishOut fo{dst->kv_codes, dst->kv_scales, dst->ix_codes, dst->ix_scales, d,
@@ -884,59 +885,109 @@ extern "C" csa2_status csa2_cache_append(const void* H_bf16, int32_t G, int32_t 
 namespace csa2 {
 namespace {
 
+// Pools rows 0 .. rows - 1 of a row source for one channel with softmax weights:
+// one pass, eight rows' loads in flight at a time, the running sums rescaled when
+// the maximum grows.  src(r, z, v) gives row r's biased score z and value v.
+template <class Src>
+__device__ __forceinline__ float pool_rows(int rows, const Src& src) {
+  constexpr int kRows = 8;
+  float zmax = -INFINITY, num = 0.0f, den = 0.0f;
+  for (int r = 0; r < rows; r += kRows) {
+    float z[kRows], v[kRows];
+#pragma unroll
+    for (int u = 0; u < kRows; ++u) {
+      z[u] = -INFINITY;
+      v[u] = 0.0f;
+      if (r + u < rows) src(r + u, z[u], v[u]);
+    }
+    float mx = z[0];
+#pragma unroll
+    for (int u = 1; u < kRows; ++u) mx = fmaxf(mx, z[u]);
+    const float nm = fmaxf(zmax, mx);
+    const float sc = expf(zmax - nm);  // 0 on the first chunk (zmax = -inf)
+    num *= sc;
+    den *= sc;
+#pragma unroll
+    for (int u = 0; u < kRows; ++u) {
+      const float e = expf(z[u] - nm);  // 0 for the rows past the end
+      num = fmaf(e, v[u], num);
+      den += e;
+    }
+    zmax = nm;
+  }
+  return __fdiv_rn(num, den);
+}
+
 // overlapping: entry i pools rows m i .. m i + m - 1 of (Ca, Za + Ba) and rows
 // m (i - 1) .. m i - 1 of (Cb, Zb + Bb); entry 0 has only the first part.  One
-// thread per (entry, channel).
+// CTA per entry, one thread per channel.
 __global__ void k_pool_overlap(const float* __restrict__ Ca, const float* __restrict__ Za,
                                const float* __restrict__ Cb, const float* __restrict__ Zb,
                                const float* __restrict__ Ba, const float* __restrict__ Bb, int64_t n, int m,
-                               float* __restrict__ out) {
-  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= n * kDMain) return;
-  const int64_t i = t / kDMain;
-  const int c = (int)(t % kDMain);
-  float zmax = -INFINITY;
-  for (int r = 0; r < m; ++r) zmax = fmaxf(zmax, Za[(i * m + r) * kDMain + c] + Ba[r * kDMain + c]);
-  if (i > 0)
-    for (int r = 0; r < m; ++r) zmax = fmaxf(zmax, Zb[((i - 1) * m + r) * kDMain + c] + Bb[r * kDMain + c]);
-  float num = 0.0f, den = 0.0f;
-  for (int r = 0; r < m; ++r) {
-    const int64_t row = (i * m + r) * kDMain + c;
-    const float e = expf(Za[row] + Ba[r * kDMain + c] - zmax);
-    num = fmaf(e, Ca[row], num);
-    den += e;
-  }
-  if (i > 0)
-    for (int r = 0; r < m; ++r) {
-      const int64_t row = ((i - 1) * m + r) * kDMain + c;
-      const float e = expf(Zb[row] + Bb[r * kDMain + c] - zmax);
-      num = fmaf(e, Cb[row], num);
-      den += e;
+                               int width, float* __restrict__ out) {
+  const int64_t i = blockIdx.x;  // the entry
+  const int c = threadIdx.x;     // its channel (blockDim.x = width)
+  const int64_t a0 = i * m * width + c, b0 = (i - 1) * m * width + c;
+  out[i * width + c] = pool_rows(i > 0 ? 2 * m : m, [&](int r, float& z, float& v) {
+    if (r < m) {
+      const int64_t row = a0 + (int64_t)r * width;
+      z = Za[row] + Ba[(int64_t)r * width + c];
+      v = Ca[row];
+    } else {
+      const int64_t row = b0 + (int64_t)(r - m) * width;
+      z = Zb[row] + Bb[(int64_t)(r - m) * width + c];
+      v = Cb[row];
     }
-  out[t] = __fdiv_rn(num, den);
+  });
 }
 
-// HCA: entry i pools rows m i .. m i + m - 1 of (C, Z + B).
-__global__ void k_pool_bias(const float* __restrict__ C, const float* __restrict__ Z, const float* __restrict__ Bp,
-                            int64_t n, int m, float* __restrict__ out) {
-  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= n * kDMain) return;
-  const int64_t i = t / kDMain;
-  const int c = (int)(t % kDMain);
-  float zmax = -INFINITY;
-  for (int r = 0; r < m; ++r) zmax = fmaxf(zmax, Z[(i * m + r) * kDMain + c] + Bp[r * kDMain + c]);
+// The same for a compression rate M fixed at compile time (V4's CSA runs at m = 4):
+// all 2 M rows' loads are issued before the first use, and no rescaling is needed.
+template <int M>
+__global__ void k_pool_overlap_m(const float* __restrict__ Ca, const float* __restrict__ Za,
+                                 const float* __restrict__ Cb, const float* __restrict__ Zb,
+                                 const float* __restrict__ Ba, const float* __restrict__ Bb, int width,
+                                 float* __restrict__ out) {
+  const int64_t i = blockIdx.x;  // the entry
+  const int c = threadIdx.x;     // its channel (blockDim.x = width)
+  const bool has_b = i > 0;
+  float z[2 * M], v[2 * M];
+#pragma unroll
+  for (int r = 0; r < M; ++r) {
+    const int64_t ra = (i * M + r) * width + c, rb = ((i - 1) * M + r) * width + c;
+    z[r] = Za[ra] + Ba[r * width + c];
+    v[r] = Ca[ra];
+    z[M + r] = has_b ? Zb[rb] + Bb[r * width + c] : -INFINITY;
+    v[M + r] = has_b ? Cb[rb] : 0.0f;
+  }
+  float zmax = z[0];
+#pragma unroll
+  for (int r = 1; r < 2 * M; ++r) zmax = fmaxf(zmax, z[r]);
   float num = 0.0f, den = 0.0f;
-  for (int r = 0; r < m; ++r) {
-    const int64_t row = (i * m + r) * kDMain + c;
-    const float e = expf(Z[row] + Bp[r * kDMain + c] - zmax);
-    num = fmaf(e, C[row], num);
+#pragma unroll
+  for (int r = 0; r < 2 * M; ++r) {
+    const float e = expf(z[r] - zmax);
+    num = fmaf(e, v[r], num);
     den += e;
   }
-  out[t] = __fdiv_rn(num, den);
+  out[i * width + c] = __fdiv_rn(num, den);
+}
+
+// HCA: entry i pools rows m i .. m i + m - 1 of (C, Z + Bp).
+__global__ void k_pool_bias(const float* __restrict__ C, const float* __restrict__ Z, const float* __restrict__ Bp,
+                            int64_t n, int m, int width, float* __restrict__ out) {
+  const int64_t i = blockIdx.x;  // the entry
+  const int c = threadIdx.x;     // its channel (blockDim.x = width)
+  const int64_t r0 = i * m * width + c;
+  out[i * width + c] = pool_rows(m, [&](int r, float& z, float& v) {
+    const int64_t row = r0 + (int64_t)r * width;
+    z = Z[row] + Bp[(int64_t)r * width + c];
+    v = C[row];
+  });
 }
 
 struct CmpWs {
-  float *c0, *z0, *c1, *z1;  // [T][512] each: the unpooled projections of up to two paths
+  float *c0, *z0, *c1, *z1;  // [T][width <= 512] each: the unpooled projections of up to two paths
   size_t bytes;
 };
 CmpWs cmp_ws_layout(void* ws, int64_t T, int64_t d_model) {
@@ -953,12 +1004,12 @@ CmpWs cmp_ws_layout(void* ws, int64_t T, int64_t d_model) {
   return L;
 }
 
-// C = H Wc, Z = H Wz (unpooled, fp32) on the tensor cores
-csa2_status project_raw(const void* H, int64_t T, int32_t d_model, const void* Wc, const void* Wz, float* C,
-                        float* Z, void* ws, cudaStream_t st) {
+// C = H Wc, Z = H Wz (unpooled, fp32, [T][width]) on the tensor cores
+csa2_status project_raw(const void* H, int64_t T, int32_t d_model, int32_t width, const void* Wc, const void* Wz,
+                        float* C, float* Z, void* ws, cudaStream_t st) {
   CUtensorMap map_h, map_wc, map_wz;
-  if (!make_bf16_map(&map_h, H, T, d_model, kTcM) || !make_bf16_map(&map_wc, Wc, d_model, kDMain, kTcBK) ||
-      !make_bf16_map(&map_wz, Wz, d_model, kDMain, kTcBK))
+  if (!make_bf16_map(&map_h, H, T, d_model, kTcM) || !make_bf16_map(&map_wc, Wc, d_model, width, kTcBK) ||
+      !make_bf16_map(&map_wz, Wz, d_model, width, kTcBK))
     return CSA2_ERR_CUDA;
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) != cudaSuccess) return CSA2_ERR_CUDA;
@@ -966,16 +1017,17 @@ csa2_status project_raw(const void* H, int64_t T, int32_t d_model, const void* W
   const int smem = (int)sizeof(TcSmem);
   if (cudaFuncSetAttribute(k_cw_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return CSA2_ERR_CUDA;
-  const int64_t ntiles = cdiv(T, kTcM) * (kDMain / 128);
+  const int64_t ntiles = cdiv(T, kTcM) * (width / 128);
   KernelTimer timer("k_cw_tc", st);
   k_cw_tc<true><<<(int)std::min<int64_t>(ntiles, sms), kTcThreads, smem, st>>>(map_h, map_wc, map_wz, T, d_model, 1,
-                                                                                C, Z, 1, nullptr, ws);
+                                                                                width, C, Z, 1, nullptr, ws);
   return CSA2_OK;
 }
 
-csa2_status compress_checks(const void* H, int64_t T, int32_t d_model, int32_t m, float* out, void* ws,
-                            size_t ws_bytes, size_t need) {
+csa2_status compress_checks(const void* H, int64_t T, int32_t d_model, int32_t m, int32_t width, float* out,
+                            void* ws, size_t ws_bytes, size_t need) {
   if ((!H && T > 0) || !out || T < 0 || m < 1 || m > 1024) return CSA2_ERR_INVALID_ARG;
+  if (width < 128 || width > kDMain || width % 128 != 0) return CSA2_ERR_UNSUPPORTED;
   if (T % m != 0) return CSA2_ERR_UNSUPPORTED;
   if (d_model < kTK || d_model % 64 != 0 || T >= ((int64_t)1 << 30)) return CSA2_ERR_UNSUPPORTED;
   if (!aligned(H, 16) || !aligned(out, 16)) return CSA2_ERR_INVALID_ARG;
@@ -994,11 +1046,11 @@ extern "C" size_t csa2_compress_workspace_size(int64_t T, int32_t d_model) {
 
 extern "C" csa2_status csa2_compress_overlap(const void* H_bf16, int64_t T, int32_t d_model, const void* Wa_kv,
                                              const void* Wb_kv, const void* Wa_z, const void* Wb_z, const float* Ba,
-                                             const float* Bb, int32_t m, float* out, void* ws, size_t ws_bytes,
-                                             csa2_stream stream) {
+                                             const float* Bb, int32_t m, int32_t width, float* out, void* ws,
+                                             size_t ws_bytes, csa2_stream stream) {
   using namespace csa2;
   const CmpWs L = cmp_ws_layout(ws, T, d_model);
-  csa2_status rc = compress_checks(H_bf16, T, d_model, m, out, ws, ws_bytes, L.bytes);
+  csa2_status rc = compress_checks(H_bf16, T, d_model, m, width, out, ws, ws_bytes, L.bytes);
   if (rc != CSA2_OK) return rc;
   if (!Wa_kv || !Wb_kv || !Wa_z || !Wb_z || !Ba || !Bb) return CSA2_ERR_INVALID_ARG;
   if (!aligned(Wa_kv, 16) || !aligned(Wb_kv, 16) || !aligned(Wa_z, 16) || !aligned(Wb_z, 16))
@@ -1006,28 +1058,31 @@ extern "C" csa2_status csa2_compress_overlap(const void* H_bf16, int64_t T, int3
   cudaStream_t st = (cudaStream_t)stream;
   if (reset_error(ws, st) != CSA2_OK) return CSA2_ERR_CUDA;
   if (T == 0) return CSA2_OK;
-  if ((rc = project_raw(H_bf16, T, d_model, Wa_kv, Wa_z, L.c0, L.z0, ws, st)) != CSA2_OK) return rc;
-  if ((rc = project_raw(H_bf16, T, d_model, Wb_kv, Wb_z, L.c1, L.z1, ws, st)) != CSA2_OK) return rc;
+  if ((rc = project_raw(H_bf16, T, d_model, width, Wa_kv, Wa_z, L.c0, L.z0, ws, st)) != CSA2_OK) return rc;
+  if ((rc = project_raw(H_bf16, T, d_model, width, Wb_kv, Wb_z, L.c1, L.z1, ws, st)) != CSA2_OK) return rc;
   const int64_t n = T / m;
   KernelTimer timer("k_pool_overlap", st);
-  k_pool_overlap<<<(unsigned)cdiv(n * kDMain, 256), 256, 0, st>>>(L.c0, L.z0, L.c1, L.z1, Ba, Bb, n, m, out);
+  if (m == 4)
+    k_pool_overlap_m<4><<<(unsigned)n, width, 0, st>>>(L.c0, L.z0, L.c1, L.z1, Ba, Bb, width, out);
+  else
+    k_pool_overlap<<<(unsigned)n, width, 0, st>>>(L.c0, L.z0, L.c1, L.z1, Ba, Bb, n, m, width, out);
   return launch_status();
 }
 
 extern "C" csa2_status csa2_compress_hca(const void* H_bf16, int64_t T, int32_t d_model, const void* W_kv,
-                                         const void* W_z, const float* Bp, int32_t m, float* out, void* ws,
-                                         size_t ws_bytes, csa2_stream stream) {
+                                         const void* W_z, const float* Bp, int32_t m, int32_t width, float* out,
+                                         void* ws, size_t ws_bytes, csa2_stream stream) {
   using namespace csa2;
   const CmpWs L = cmp_ws_layout(ws, T, d_model);
-  csa2_status rc = compress_checks(H_bf16, T, d_model, m, out, ws, ws_bytes, L.bytes);
+  csa2_status rc = compress_checks(H_bf16, T, d_model, m, width, out, ws, ws_bytes, L.bytes);
   if (rc != CSA2_OK) return rc;
   if (!W_kv || !W_z || !Bp || !aligned(W_kv, 16) || !aligned(W_z, 16)) return CSA2_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
   if (reset_error(ws, st) != CSA2_OK) return CSA2_ERR_CUDA;
   if (T == 0) return CSA2_OK;
-  if ((rc = project_raw(H_bf16, T, d_model, W_kv, W_z, L.c0, L.z0, ws, st)) != CSA2_OK) return rc;
+  if ((rc = project_raw(H_bf16, T, d_model, width, W_kv, W_z, L.c0, L.z0, ws, st)) != CSA2_OK) return rc;
   const int64_t n = T / m;
   KernelTimer timer("k_pool_bias", st);
-  k_pool_bias<<<(unsigned)cdiv(n * kDMain, 256), 256, 0, st>>>(L.c0, L.z0, Bp, n, m, out);
+  k_pool_bias<<<(unsigned)n, width, 0, st>>>(L.c0, L.z0, Bp, n, m, width, out);
   return launch_status();
 }

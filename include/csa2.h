@@ -198,7 +198,7 @@ csa2_status csa2_swa_append(const float* x, int32_t R, const int32_t* query, con
 
 /* The V4 compressors ("DeepSeek-V4: Towards Highly Efficient Million-Token Context
  * Intelligence", CSA step 1 and the HCA section), each writing the T/m compressed
- * latents as fp32 out [T/m][512] (quantize them into a cache with
+ * latents as fp32 out [T/m][width] (quantize them into a cache with
  * csa2_quantize_entries).  The projections run on the tensor cores (bf16 operands,
  * fp32 sums); the pools take, per channel, one softmax over the scores of the rows
  * an entry draws from, position bias added.
@@ -211,19 +211,22 @@ csa2_status csa2_swa_append(const float* x, int32_t R, const int32_t* query, con
  * csa2_compress_hca (HCA, one path, no overlap): C = H W_KV, Z = H W_Z; entry i
  *   draws from rows m i .. m i + m - 1 (score Z + B[r]); m is m' (128 in V4).
  *
- *   H_bf16  [T][d_model] bf16;  W_* [d_model][512] bf16 (row-major, as in H W)
- *   B_*     [m][512] fp32 position biases (finite)
- *   out     [T/m][512] fp32, 16-byte aligned; H and the weights 16-byte aligned
+ *   width   output channels c: 512 for the main KV latents, 128 for V4's indexer keys
+ *           ("the same compression, projected to c^I"; CSA step 2) -- a multiple of 128, <= 512
+ *   H_bf16  [T][d_model] bf16;  W_* [d_model][width] bf16 (row-major, as in H W)
+ *   B_*     [m][width] fp32 position biases (finite)
+ *   out     [T/m][width] fp32, 16-byte aligned; H and the weights 16-byte aligned
  * T must be a multiple of m (CSA2_ERR_UNSUPPORTED otherwise), 1 <= m <= 1024,
  * d_model a multiple of 64 and >= 64, T < 2^30.  ws: 256-byte aligned, at least
- * csa2_compress_workspace_size(T, d_model) bytes (the unpooled projections). */
+ * csa2_compress_workspace_size(T, d_model) bytes (the unpooled projections; enough for any
+ * width). */
 csa2_status csa2_compress_overlap(const void* H_bf16, int64_t T, int32_t d_model, const void* Wa_kv,
                                   const void* Wb_kv, const void* Wa_z, const void* Wb_z, const float* Ba,
-                                  const float* Bb, int32_t m, float* out, void* ws, size_t ws_bytes,
-                                  csa2_stream stream);
+                                  const float* Bb, int32_t m, int32_t width, float* out, void* ws,
+                                  size_t ws_bytes, csa2_stream stream);
 csa2_status csa2_compress_hca(const void* H_bf16, int64_t T, int32_t d_model, const void* W_kv,
-                              const void* W_z, const float* B, int32_t m, float* out, void* ws,
-                              size_t ws_bytes, csa2_stream stream);
+                              const void* W_z, const float* B, int32_t m, int32_t width, float* out,
+                              void* ws, size_t ws_bytes, csa2_stream stream);
 size_t csa2_compress_workspace_size(int64_t T, int32_t d_model);
 
 /* ---------------------------------------------------------- indexer + top-k */

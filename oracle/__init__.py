@@ -82,16 +82,17 @@ def _load():
         lib.o_rope.restype = None
         lib.o_swa_row.argtypes = [vp, vp, f64, ctypes.c_int, f64, f64, vp, vp]
         lib.o_swa_row.restype = None
-        lib.o_project.argtypes = [vp, i64, ctypes.c_int, vp, vp, ctypes.c_int]
+        lib.o_project.argtypes = [vp, i64, ctypes.c_int, ctypes.c_int, vp, vp, ctypes.c_int]
         lib.o_project.restype = None
         lib.o_pool_overlap.argtypes = [vp, vp, vp, vp, vp, vp, i64, ctypes.c_int, ctypes.c_int, vp]
         lib.o_pool_overlap.restype = None
         lib.o_pool_bias.argtypes = [vp, vp, vp, i64, ctypes.c_int, ctypes.c_int, vp]
         lib.o_pool_bias.restype = None
-        lib.o_compress_overlap.argtypes = [vp, i64, ctypes.c_int, vp, vp, vp, vp, vp, vp, ctypes.c_int, vp,
-                                           ctypes.c_int]
+        lib.o_compress_overlap.argtypes = [vp, i64, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, vp, vp,
+                                           ctypes.c_int, vp, ctypes.c_int]
         lib.o_compress_overlap.restype = ctypes.c_int
-        lib.o_compress_hca.argtypes = [vp, i64, ctypes.c_int, vp, vp, vp, ctypes.c_int, vp, ctypes.c_int]
+        lib.o_compress_hca.argtypes = [vp, i64, ctypes.c_int, ctypes.c_int, vp, vp, vp, ctypes.c_int, vp,
+                                       ctypes.c_int]
         lib.o_compress_hca.restype = ctypes.c_int
         lib.o_e2m1_encode_array.argtypes = [vp, i64, vp]
         lib.o_e2m1_encode_array.restype = None
@@ -259,11 +260,11 @@ def _f32(a):
 
 
 def project(H: np.ndarray, W: np.ndarray) -> np.ndarray:
-    """H bf16 bits [T,d] times W bf16 bits [d,512], fp64 sums: [T,512]."""
-    H = _u16(H)
+    """H bf16 bits [T,d] times W bf16 bits [d,width], fp64 sums: [T,width]."""
+    H, W = _u16(H), _u16(W)
     T, d = H.shape
-    out = np.empty((T, D_MAIN), np.float64)
-    _load().o_project(_p(H), T, d, _p(_u16(W)), _p(out), _threads())
+    out = np.empty((T, W.shape[1]), np.float64)
+    _load().o_project(_p(H), T, d, W.shape[1], _p(W), _p(out), _threads())
     return out
 
 
@@ -293,11 +294,12 @@ def pool_bias(C, Z, Bp, m: int) -> np.ndarray:
 
 
 def compress_overlap(H, Wa_kv, Wb_kv, Wa_z, Wb_z, Ba, Bb, m: int) -> np.ndarray:
-    """CSA step 1 end to end: [T/m, 512] fp64 compressed entries of H."""
+    """CSA step 1 end to end: [T/m, width] fp64 compressed entries of H (W_* [d, width])."""
     H = _u16(H)
     T, d = H.shape
-    out = np.empty((T // m if m > 0 else 0, D_MAIN), np.float64)
-    rc = _load().o_compress_overlap(_p(H), T, d, _p(_u16(Wa_kv)), _p(_u16(Wb_kv)), _p(_u16(Wa_z)),
+    width = np.asarray(Wa_kv).shape[1]
+    out = np.empty((T // m if m > 0 else 0, width), np.float64)
+    rc = _load().o_compress_overlap(_p(H), T, d, width, _p(_u16(Wa_kv)), _p(_u16(Wb_kv)), _p(_u16(Wa_z)),
                                     _p(_u16(Wb_z)), _p(_f32(Ba)), _p(_f32(Bb)), m, _p(out), _threads())
     if rc != 0:
         raise ValueError("oracle compress_overlap: bad arguments")
@@ -305,11 +307,12 @@ def compress_overlap(H, Wa_kv, Wb_kv, Wa_z, Wb_z, Ba, Bb, m: int) -> np.ndarray:
 
 
 def compress_hca(H, Wkv, Wz, Bp, m: int) -> np.ndarray:
-    """HCA compressor end to end: [T/m, 512] fp64 compressed entries of H."""
+    """HCA compressor end to end: [T/m, width] fp64 compressed entries of H (W [d, width])."""
     H = _u16(H)
     T, d = H.shape
-    out = np.empty((T // m if m > 0 else 0, D_MAIN), np.float64)
-    rc = _load().o_compress_hca(_p(H), T, d, _p(_u16(Wkv)), _p(_u16(Wz)), _p(_f32(Bp)), m, _p(out),
+    width = np.asarray(Wkv).shape[1]
+    out = np.empty((T // m if m > 0 else 0, width), np.float64)
+    rc = _load().o_compress_hca(_p(H), T, d, width, _p(_u16(Wkv)), _p(_u16(Wz)), _p(_f32(Bp)), m, _p(out),
                                 _threads())
     if rc != 0:
         raise ValueError("oracle compress_hca: bad arguments")

@@ -466,31 +466,31 @@ void o_pool(const double* C, const double* Z, int64_t T, int width, int m, doubl
 typedef struct {
   const uint16_t *H, *W;
   int64_t r_lo, r_hi;
-  int d;
+  int d, width;
   double* out;
 } proj_job;
 
 static void* project_worker(void* p) {
   const proj_job* jb = (const proj_job*)p;
-  int d = jb->d;
-  double* W = (double*)malloc(sizeof(double) * (size_t)d * D_MAIN);
-  for (int64_t i = 0; i < (int64_t)d * D_MAIN; ++i) W[i] = bf16_value(jb->W[i]);
+  int d = jb->d, w = jb->width;
+  double* W = (double*)malloc(sizeof(double) * (size_t)d * w);
+  for (int64_t i = 0; i < (int64_t)d * w; ++i) W[i] = bf16_value(jb->W[i]);
   for (int64_t r = jb->r_lo; r < jb->r_hi; ++r) {
-    double* o = jb->out + r * D_MAIN;
-    for (int c = 0; c < D_MAIN; ++c) o[c] = 0.0;
+    double* o = jb->out + r * w;
+    for (int c = 0; c < w; ++c) o[c] = 0.0;
     for (int k = 0; k < d; ++k) {
       double hv = bf16_value(jb->H[r * d + k]);
       if (hv == 0.0) continue;
-      const double* wk = W + (size_t)k * D_MAIN;
-      for (int c = 0; c < D_MAIN; ++c) o[c] += hv * wk[c];
+      const double* wk = W + (size_t)k * w;
+      for (int c = 0; c < w; ++c) o[c] += hv * wk[c];
     }
   }
   free(W);
   return NULL;
 }
 
-/* out [T][512] = H [T][d] W [d][512], bf16 operands, fp64 sums */
-void o_project(const uint16_t* H, int64_t T, int d, const uint16_t* W, double* out, int nthreads) {
+/* out [T][width] = H [T][d] W [d][width], bf16 operands, fp64 sums */
+void o_project(const uint16_t* H, int64_t T, int d, int width, const uint16_t* W, double* out, int nthreads) {
   if (nthreads < 1) nthreads = 1;
   if (nthreads > 128) nthreads = 128;
   if (nthreads > T) nthreads = (int)(T > 0 ? T : 1);
@@ -498,7 +498,7 @@ void o_project(const uint16_t* H, int64_t T, int d, const uint16_t* W, double* o
   proj_job jobs[128];
   int64_t per = (T + nthreads - 1) / nthreads;
   for (int t = 0; t < nthreads; ++t) {
-    proj_job jb = {H, W, (int64_t)t * per, (int64_t)(t + 1) * per, d, out};
+    proj_job jb = {H, W, (int64_t)t * per, (int64_t)(t + 1) * per, d, width, out};
     if (jb.r_hi > T) jb.r_hi = T;
     if (jb.r_lo > T) jb.r_lo = T;
     jobs[t] = jb;
@@ -569,20 +569,20 @@ void o_pool_bias(const double* C, const double* Z, const float* Bp, int64_t T, i
 
 /* The two compressors end to end: projections of H, then the pool.  Returns 1
  * when T is not a multiple of m (or an allocation fails). */
-int o_compress_overlap(const uint16_t* H, int64_t T, int d, const uint16_t* Wa_kv, const uint16_t* Wb_kv,
-                       const uint16_t* Wa_z, const uint16_t* Wb_z, const float* Ba, const float* Bb, int m,
-                       double* out, int nthreads) {
-  if (m < 1 || d < 1 || T < 0 || T % m != 0) return 1;
-  size_t sz = sizeof(double) * (size_t)(T > 0 ? T : 1) * D_MAIN;
+int o_compress_overlap(const uint16_t* H, int64_t T, int d, int width, const uint16_t* Wa_kv,
+                       const uint16_t* Wb_kv, const uint16_t* Wa_z, const uint16_t* Wb_z, const float* Ba,
+                       const float* Bb, int m, double* out, int nthreads) {
+  if (m < 1 || d < 1 || width < 1 || T < 0 || T % m != 0) return 1;
+  size_t sz = sizeof(double) * (size_t)(T > 0 ? T : 1) * width;
   double *Ca = (double*)malloc(sz), *Za = (double*)malloc(sz), *Cb = (double*)malloc(sz),
          *Zb = (double*)malloc(sz);
   int rc = 1;
   if (Ca && Za && Cb && Zb) {
-    o_project(H, T, d, Wa_kv, Ca, nthreads);
-    o_project(H, T, d, Wa_z, Za, nthreads);
-    o_project(H, T, d, Wb_kv, Cb, nthreads);
-    o_project(H, T, d, Wb_z, Zb, nthreads);
-    o_pool_overlap(Ca, Za, Cb, Zb, Ba, Bb, T, D_MAIN, m, out);
+    o_project(H, T, d, width, Wa_kv, Ca, nthreads);
+    o_project(H, T, d, width, Wa_z, Za, nthreads);
+    o_project(H, T, d, width, Wb_kv, Cb, nthreads);
+    o_project(H, T, d, width, Wb_z, Zb, nthreads);
+    o_pool_overlap(Ca, Za, Cb, Zb, Ba, Bb, T, width, m, out);
     rc = 0;
   }
   free(Ca);
@@ -592,16 +592,16 @@ int o_compress_overlap(const uint16_t* H, int64_t T, int d, const uint16_t* Wa_k
   return rc;
 }
 
-int o_compress_hca(const uint16_t* H, int64_t T, int d, const uint16_t* Wkv, const uint16_t* Wz,
+int o_compress_hca(const uint16_t* H, int64_t T, int d, int width, const uint16_t* Wkv, const uint16_t* Wz,
                    const float* Bp, int m, double* out, int nthreads) {
-  if (m < 1 || d < 1 || T < 0 || T % m != 0) return 1;
-  size_t sz = sizeof(double) * (size_t)(T > 0 ? T : 1) * D_MAIN;
+  if (m < 1 || d < 1 || width < 1 || T < 0 || T % m != 0) return 1;
+  size_t sz = sizeof(double) * (size_t)(T > 0 ? T : 1) * width;
   double *C = (double*)malloc(sz), *Z = (double*)malloc(sz);
   int rc = 1;
   if (C && Z) {
-    o_project(H, T, d, Wkv, C, nthreads);
-    o_project(H, T, d, Wz, Z, nthreads);
-    o_pool_bias(C, Z, Bp, T, D_MAIN, m, out);
+    o_project(H, T, d, width, Wkv, C, nthreads);
+    o_project(H, T, d, width, Wz, Z, nthreads);
+    o_pool_bias(C, Z, Bp, T, width, m, out);
     rc = 0;
   }
   free(C);

@@ -153,17 +153,19 @@ def test_v4_compressor_and_dense_validation_without_gpu(L):
     fake = csa2.KVPlanes(16, 16, 16, 16, 100)
     args = (16, 16, 16, 16, 16, 16)  # Wa_kv, Wb_kv, Wa_z, Wb_z, Ba, Bb
     ws = csa2.compress_workspace_size(8, 64)
-    assert L.csa2_compress_overlap(16, 10, 64, *args, 4, 16, 256, ws, None) == 2      # T % m != 0
-    assert L.csa2_compress_overlap(16, 8, 96, *args, 4, 16, 256, ws, None) == 2       # d % 64 != 0
-    assert L.csa2_compress_overlap(16, 8, 64, *args, 0, 16, 256, ws, None) == 1       # m < 1
-    assert L.csa2_compress_overlap(16, 8, 64, *args, 4, None, 256, ws, None) == 1     # no output
-    assert L.csa2_compress_overlap(16, 8, 64, 16, 16, 16, 16, None, 16, 4, 16, 256, ws, None) == 1
-    assert L.csa2_compress_overlap(16, 8, 64, *args, 4, 16, 256, ws - 1, None) == 3   # workspace short
-    assert L.csa2_compress_overlap(16, 8, 64, *args, 4, 16, 128, ws, None) == 3       # misaligned ws
-    assert L.csa2_compress_hca(16, 256, 64, 16, 16, 16, 128, 16, 256, ws, None) == 3
-    assert L.csa2_compress_hca(16, 200, 64, 16, 16, 16, 128, 16, 256, 1 << 30, None) == 2
-    assert L.csa2_compress_hca(16, 256, 64, 8, 16, 16, 128, 16, 256, 1 << 30, None) == 1  # misaligned W
+    assert L.csa2_compress_overlap(16, 10, 64, *args, 4, 512, 16, 256, ws, None) == 2      # T % m != 0
+    assert L.csa2_compress_overlap(16, 8, 96, *args, 4, 512, 16, 256, ws, None) == 2       # d % 64 != 0
+    assert L.csa2_compress_overlap(16, 8, 64, *args, 0, 512, 16, 256, ws, None) == 1       # m < 1
+    assert L.csa2_compress_overlap(16, 8, 64, *args, 4, 512, None, 256, ws, None) == 1     # no output
+    assert L.csa2_compress_overlap(16, 8, 64, 16, 16, 16, 16, None, 16, 4, 512, 16, 256, ws, None) == 1
+    assert L.csa2_compress_overlap(16, 8, 64, *args, 4, 512, 16, 256, ws - 1, None) == 3   # workspace short
+    assert L.csa2_compress_overlap(16, 8, 64, *args, 4, 512, 16, 128, ws, None) == 3       # misaligned ws
+    assert L.csa2_compress_hca(16, 256, 64, 16, 16, 16, 128, 512, 16, 256, ws, None) == 3
+    assert L.csa2_compress_hca(16, 200, 64, 16, 16, 16, 128, 512, 16, 256, 1 << 30, None) == 2
+    assert L.csa2_compress_hca(16, 256, 64, 8, 16, 16, 128, 512, 16, 256, 1 << 30, None) == 1  # misaligned W
     assert csa2.compress_workspace_size(65536, 4096) >= 4 * 65536 * 512 * 4
+    for bad_width in (0, 64, 640, 200):  # a multiple of 128, at most 512
+        assert L.csa2_compress_hca(16, 256, 64, 16, 16, 16, 128, bad_width, 16, 256, 1 << 30, None) == 2
     # dense attention: n_max beyond the slot or the limit, no counts, bad scale
     assert L.csa2_dense_attn_decode(ctypes.byref(fake), 1, 16, 101, None, 0, 16, 0.04, None, None, None, None, 16,
                                     None, 256, 1 << 30, None) == 1

@@ -50,21 +50,23 @@ def _dev16(a):
 
 def _gpu_overlap(H, Wa, Wb, Za, Zb, Ba, Bb, m):
     T, d = H.shape
-    out = torch.full((T // m, 512), float("nan"), dtype=torch.float32, device="cuda")
+    width = Wa.shape[1]
+    out = torch.full((T // m, width), float("nan"), dtype=torch.float32, device="cuda")
     ws = csa2.workspace(csa2.compress_workspace_size(T, d))
     csa2.compress_overlap(_dev16(H), T, d, _dev16(Wa), _dev16(Wb), _dev16(Za), _dev16(Zb),
                           to_dev(np.ascontiguousarray(Ba, np.float32)),
-                          to_dev(np.ascontiguousarray(Bb, np.float32)), m, out, ws)
+                          to_dev(np.ascontiguousarray(Bb, np.float32)), m, out, ws, width=width)
     assert csa2.check(ws)[0] == 0
     return out.cpu().numpy().astype(np.float64)
 
 
 def _gpu_hca(H, Wkv, Wz, Bp, m):
     T, d = H.shape
-    out = torch.full((T // m, 512), float("nan"), dtype=torch.float32, device="cuda")
+    width = Wkv.shape[1]
+    out = torch.full((T // m, width), float("nan"), dtype=torch.float32, device="cuda")
     ws = csa2.workspace(csa2.compress_workspace_size(T, d))
     csa2.compress_hca(_dev16(H), T, d, _dev16(Wkv), _dev16(Wz), to_dev(np.ascontiguousarray(Bp, np.float32)),
-                      m, out, ws)
+                      m, out, ws, width=width)
     assert csa2.check(ws)[0] == 0
     return out.cpu().numpy().astype(np.float64)
 
@@ -166,6 +168,26 @@ def test_hca_gaussian_within_bound(oracle_mod, T, d, m):
     bound = _hca_bound(oracle_mod, H, Wkv, Wz, Bp, m)
     err = np.abs(got - ref)
     assert np.all(err <= bound), float((err / bound).max())
+
+
+@pytest.mark.parametrize("width", [128, 256])
+def test_narrow_widths_within_bound(oracle_mod, width):
+    """V4's indexer keys go through the same compression at c^I = 128 channels (CSA step 2):
+    the compressors at widths 128 and 256 against the oracle, within the same bound."""
+    cut = lambda a: np.ascontiguousarray(a[:, :width])
+    T, d, m = 200, 256, 4
+    H, Wa, Wb, Za, Zb, Ba, Bb = W.overlap_compressor_inputs(23, T, d, m)
+    Wa, Wb, Za, Zb, Ba, Bb = (cut(a) for a in (Wa, Wb, Za, Zb, Ba, Bb))
+    got = _gpu_overlap(H, Wa, Wb, Za, Zb, Ba, Bb, m)
+    ref = oracle_mod.compress_overlap(H, Wa, Wb, Za, Zb, Ba, Bb, m)
+    assert got.shape == (T // m, width)
+    assert np.all(np.abs(got - ref) <= _overlap_bound(oracle_mod, H, Wa, Wb, Za, Zb, Ba, Bb, m))
+    T, m = 256, 128
+    H, Wkv, Wz, Bp = W.hca_compressor_inputs(23, T, d, m)
+    Wkv, Wz, Bp = cut(Wkv), cut(Wz), cut(Bp)
+    got = _gpu_hca(H, Wkv, Wz, Bp, m)
+    ref = oracle_mod.compress_hca(H, Wkv, Wz, Bp, m)
+    assert np.all(np.abs(got - ref) <= _hca_bound(oracle_mod, H, Wkv, Wz, Bp, m))
 
 
 def test_compressors_empty():

@@ -193,3 +193,20 @@ def test_compressors_reject_ragged(oracle_mod):
         oracle_mod.compress_hca(H, W, W, B, 4)
     with pytest.raises(ValueError):
         oracle_mod.compress_overlap(H, W, W, W, W, B, B, 4)
+
+
+def test_compressors_channels_independent_width_128(oracle_mod):
+    """Every output channel pools only its own column: compressing with the first 128
+    columns of the weights and biases (V4's indexer-key width c^I) gives the first 128
+    channels of the 512-wide result, exactly."""
+    m, d = 4, 64
+    T = 6 * m
+    H, Wa, Wb, Za, Zb, Ba, Bb = overlap_compressor_inputs(6, T, d, m)
+    full = oracle_mod.compress_overlap(H, Wa, Wb, Za, Zb, Ba, Bb, m)
+    cut = lambda a: np.ascontiguousarray(a[:, :128])
+    narrow = oracle_mod.compress_overlap(H, cut(Wa), cut(Wb), cut(Za), cut(Zb), cut(Ba), cut(Bb), m)
+    assert narrow.shape == (T // m, 128) and np.array_equal(narrow, full[:, :128])
+    H2, Wkv, Wz, Bp = hca_compressor_inputs(6, 256, d, 128)
+    full = oracle_mod.compress_hca(H2, Wkv, Wz, Bp, 128)
+    narrow = oracle_mod.compress_hca(H2, cut(Wkv), cut(Wz), cut(Bp), 128)
+    assert np.array_equal(narrow, full[:, :128])
