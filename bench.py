@@ -73,6 +73,12 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.file = None
+        self.offset = 0  # samples before this file offset were taken before the timed region
+
+    def mark(self):
+        """Call at the start of the timed region: later samples only are summarised."""
+        if self.proc:
+            self.offset = os.path.getsize(self.file.name)
 
     def __enter__(self):
         self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
@@ -105,7 +111,12 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.file.flush()
         rows = []
-        for line in open(self.file.name):
+        with open(self.file.name) as fh:
+            fh.seek(self.offset)
+            lines = fh.read().splitlines()
+        if self.offset and lines:
+            lines = lines[1:]  # may be a sample cut at the offset
+        for line in lines:
             f = [x.strip() for x in line.split(",")]
             if len(f) >= 8:
                 try:
@@ -118,7 +129,7 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v == "Active"})
         return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows), "window": "timed region only"}
 
 
 # ----------------------------------------------------------------------------- oracle sample
@@ -749,6 +760,7 @@ def run_ours(args, rank, world, local_rank):
     with ClockSampler(local_rank) as clk:
         barrier()
         torch.cuda.synchronize()
+        clk.mark()
         start.record(st)
         for s in range(args.steps):
             index_call()
@@ -890,7 +902,7 @@ def run_ours(args, rank, world, local_rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
