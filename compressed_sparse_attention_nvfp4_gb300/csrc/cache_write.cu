@@ -923,8 +923,8 @@ __device__ __forceinline__ float pool_rows(int rows, const Src& src) {
 // CTA per entry, one thread per channel.
 __global__ void k_pool_overlap(const float* __restrict__ Ca, const float* __restrict__ Za,
                                const float* __restrict__ Cb, const float* __restrict__ Zb,
-                               const float* __restrict__ Ba, const float* __restrict__ Bb, int64_t n, int m,
-                               int width, float* __restrict__ out) {
+                               const float* __restrict__ Ba, const float* __restrict__ Bb, int m, int width,
+                               float* __restrict__ out) {
   const int64_t i = blockIdx.x;  // the entry
   const int c = threadIdx.x;     // its channel (blockDim.x = width)
   const int64_t a0 = i * m * width + c, b0 = (i - 1) * m * width + c;
@@ -975,7 +975,7 @@ __global__ void k_pool_overlap_m(const float* __restrict__ Ca, const float* __re
 
 // HCA: entry i pools rows m i .. m i + m - 1 of (C, Z + Bp).
 __global__ void k_pool_bias(const float* __restrict__ C, const float* __restrict__ Z, const float* __restrict__ Bp,
-                            int64_t n, int m, int width, float* __restrict__ out) {
+                            int m, int width, float* __restrict__ out) {
   const int64_t i = blockIdx.x;  // the entry
   const int c = threadIdx.x;     // its channel (blockDim.x = width)
   const int64_t r0 = i * m * width + c;
@@ -1065,7 +1065,7 @@ extern "C" csa2_status csa2_compress_overlap(const void* H_bf16, int64_t T, int3
   if (m == 4)
     k_pool_overlap_m<4><<<(unsigned)n, width, 0, st>>>(L.c0, L.z0, L.c1, L.z1, Ba, Bb, width, out);
   else
-    k_pool_overlap<<<(unsigned)n, width, 0, st>>>(L.c0, L.z0, L.c1, L.z1, Ba, Bb, n, m, width, out);
+    k_pool_overlap<<<(unsigned)n, width, 0, st>>>(L.c0, L.z0, L.c1, L.z1, Ba, Bb, m, width, out);
   return launch_status();
 }
 
@@ -1083,6 +1083,6 @@ extern "C" csa2_status csa2_compress_hca(const void* H_bf16, int64_t T, int32_t 
   if ((rc = project_raw(H_bf16, T, d_model, width, W_kv, W_z, L.c0, L.z0, ws, st)) != CSA2_OK) return rc;
   const int64_t n = T / m;
   KernelTimer timer("k_pool_bias", st);
-  k_pool_bias<<<(unsigned)n, width, 0, st>>>(L.c0, L.z0, Bp, n, m, width, out);
+  k_pool_bias<<<(unsigned)n, width, 0, st>>>(L.c0, L.z0, Bp, m, width, out);
   return launch_status();
 }
