@@ -718,9 +718,18 @@ void launch_select_res(const SelectArgs& a, int B, int ncl, int64_t per, cudaStr
 void launch_select(const SelectArgs& a, int B, cudaStream_t st) {
   // slice per CTA: the pool candidates, the blocks, or up to n_max entries
   const int64_t ncand_max = a.pool ? a.ncand_fixed : (a.count_blocks ? cdiv(a.n_max, 8) : a.n_max);
-  const int64_t per = (int64_t)align_up((size_t)cdiv(ncand_max, kSelCluster), kSelItems);
+  // 8 CTAs per query, or fewer when the batch alone overfills the resident slots
+  // (two select CTAs per SM) and each CTA's slice still fits its shared memory:
+  // one wave of clusters instead of several
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t slots = 2 * (int64_t)(sms > 0 ? sms : 148);
+  int ncl = kSelCluster;
+  while (ncl > 1 && (int64_t)B * ncl > slots && cdiv(ncand_max, ncl / 2) <= kResCap) ncl /= 2;
+  const int64_t per = (int64_t)align_up((size_t)cdiv(ncand_max, ncl), kSelItems);
   if (per <= kResCap) {
-    launch_select_res<256>(a, B, kSelCluster, per, st);
+    launch_select_res<256>(a, B, ncl, per, st);
   } else {
     KernelTimer timer("k_select", st);
     k_select<<<B * kSelCluster, kSelThreads, 0, st>>>(a);

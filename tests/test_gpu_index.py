@@ -177,11 +177,13 @@ def _prefill(planes, seq, q, w, n_vis, n_max, k=512):
     return topk.cpu().numpy()
 
 
-def test_prefill_indexer_shared_slot(cache, oracle_mod):
+@pytest.mark.parametrize("Q", [40, 100, 160])
+def test_prefill_indexer_shared_slot(cache, oracle_mod, Q):
     """Q queries of one slot, each with its own causal bound: every query's top-512 is the
-    oracle's top-512 of that query over entries [0, n_visible)."""
+    oracle's top-512 of that query over entries [0, n_visible).  The larger batches run the
+    select with 4, 2 and 1 CTAs per query (the batch alone fills the GPU's select slots)."""
     c, _, _ = cache
-    Q, seq = 40, 1
+    seq = 1
     q, w = W.index_query(4, 0, Q)
     rng = np.random.default_rng(2)
     n_vis = np.concatenate([[0, 1, 7, 513, 4133], rng.integers(0, 4134, Q - 5)]).astype(np.int32)
