@@ -202,12 +202,17 @@ def test_compressors_empty():
     assert csa2.check(ws)[0] == 0 and torch.all(out == 0)
 
 
-def test_overlap_full_size_sampled(oracle_mod):
+@pytest.mark.parametrize("width", [512, 128])
+def test_overlap_full_size_sampled(oracle_mod, width):
     """The benchmarked prefill chunk (T = 65,536 tokens, d = 4096, m = 4): sampled
-    entries against the oracle run on the two blocks each one reads."""
+    entries against the oracle run on the two blocks each one reads; at the main-KV
+    width and at V4's indexer-key width c^I = 128 (one channel block per token tile)."""
     T, d, m = 65536, 4096, 4
     H, Wa, Wb, Za, Zb, Ba, Bb = W.overlap_compressor_inputs(7, T, d, m)
+    cut = lambda a: np.ascontiguousarray(a[:, :width])
+    Wa, Wb, Za, Zb, Ba, Bb = (cut(a) for a in (Wa, Wb, Za, Zb, Ba, Bb))
     got = _gpu_overlap(H, Wa, Wb, Za, Zb, Ba, Bb, m)
+    assert got.shape == (T // m, width)
     rng = np.random.default_rng(5)
     for i in [0, 1, T // m - 1] + [int(v) for v in rng.integers(2, T // m - 1, 13)]:
         Hs = H[max(0, (i - 1) * m):(i + 1) * m]  # the blocks entry i reads: it is the slice's last
