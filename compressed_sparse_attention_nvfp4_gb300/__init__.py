@@ -114,6 +114,7 @@ def lib() -> ctypes.CDLL:
             "csa2_compress_workspace_size": ([i64, i32], sz),
             "csa2_v41_layer_table": ([i32, vp, vp, vp, vp, vp], ctypes.c_int),
             "csa2_check": ([vp, vp, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
+            "csa2_index_topk_noalloc_check": ([vp, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
             "csa2_selftest_wait_timeout": ([ctypes.c_longlong, vp, sz, vp], ctypes.c_int),
             "csa2_status_string": ([ctypes.c_int], ctypes.c_char_p),
             "csa2_timing_enable": ([i32], ctypes.c_int),
@@ -285,6 +286,14 @@ def index_topk_noalloc(planes: Planes, B: int, n_entries, n_max: int, qidx, w, k
                                       _ptr(w), k, mode, block, n_blocks_keep, _ptr(pool_in),
                                       _ptr(topk_out), _ptr(pool_out), _stream(stream)),
         "csa2_index_topk_noalloc")
+
+
+def index_topk_noalloc_check(stream=None) -> tuple[int, int]:
+    """Syncs `stream`; (status, detail) of the first device-side error the allocation-free
+    calls recorded since the last call began, then clears it (csa2_index_topk_noalloc_check)."""
+    d = ctypes.c_int64(0)
+    rc = lib().csa2_index_topk_noalloc_check(_stream(stream), ctypes.byref(d))
+    return rc, d.value
 
 
 def sparse_attn_workspace_size(B: int, k: int, n_swa: int) -> int:

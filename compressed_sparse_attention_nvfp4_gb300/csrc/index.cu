@@ -4,6 +4,7 @@
 //   the limits of KV cache compression", 4.1), the hierarchical pool of the first
 //   decoder Full layer and the Reindex layers' pool-restricted top-k (4.3).
 #include <atomic>
+#include <mutex>
 
 #include <cooperative_groups.h>
 #include <cub/block/block_scan.cuh>
@@ -975,19 +976,60 @@ namespace csa2 {
 namespace {
 
 constexpr int kMaxDevices = 64;
-std::atomic<void*> g_noalloc_addr[kMaxDevices];
 
-// Device address of the scratch array on the current device (looked up on the
-// first call per device, with that device current).
+// The array's device address belongs to the CUDA context that loaded this
+// module: after a device reset the next context loads it afresh, possibly at
+// another address.  So the cached address is keyed on the context's unique id
+// (cuCtxGetId), and a call from a new context looks it up again.
+struct NoallocSlot {
+  unsigned long long ctx_id;  // 0: not looked up yet
+  void* addr;
+};
+NoallocSlot g_noalloc_slot[kMaxDevices];
+std::mutex g_noalloc_mu;
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// id of the current thread's CUDA context (0 if it cannot be read)
+unsigned long long current_ctx_id() {
+  static CtxGetCurrentFn get_cur = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return (CtxGetCurrentFn) nullptr;
+    return reinterpret_cast<CtxGetCurrentFn>(f);
+  }();
+  static CtxGetIdFn get_id = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return (CtxGetIdFn) nullptr;
+    return reinterpret_cast<CtxGetIdFn>(f);
+  }();
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_cur || !get_id || get_cur(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the scratch array in the current device's context, looked
+// up with that device current on the first call in each context.
 csa2_status noalloc_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CSA2_ERR_CUDA;
-  void* p = g_noalloc_addr[dev].load(std::memory_order_acquire);
-  if (!p) {
+  unsigned long long id = current_ctx_id();  // 0 before the runtime made a context current here
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoallocSlot& s = g_noalloc_slot[dev];
+  if (id == 0 || s.ctx_id != id || !s.addr) {
+    void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return CSA2_ERR_CUDA;
-    g_noalloc_addr[dev].store(p, std::memory_order_release);
+    s.addr = p;
+    s.ctx_id = current_ctx_id();  // the lookup made the device's primary context current
   }
-  *out = p;
+  *out = s.addr;
   return CSA2_OK;
 }
 
@@ -1024,7 +1066,8 @@ extern "C" csa2_status csa2_index_topk_noalloc(const csa2_kv_planes* kv, int32_t
   const int64_t bmax_cols = mode == CSA2_TOPK_HIER_BUILD ? (int64_t)align_up((size_t)cdiv(n_max, 8), 64) : 0;
   const size_t s_bytes = align_up((size_t)B * score_cols * 4, 256);
   const size_t b_bytes = align_up((size_t)B * bmax_cols * 4, 256);
-  const size_t p_bytes = mode == CSA2_TOPK_HIER_BUILD ? align_up((size_t)B * n_blocks_keep * 4, 256) : 0;
+  const size_t p_bytes =
+      mode == CSA2_TOPK_HIER_BUILD && !pool_out ? align_up((size_t)B * n_blocks_keep * 4, 256) : 0;
   if (kWsHeader + s_bytes + b_bytes + p_bytes > (size_t)CSA2_NOALLOC_SCRATCH_BYTES) return CSA2_ERR_WORKSPACE;
 
   void* ws = nullptr;
@@ -1064,4 +1107,11 @@ extern "C" csa2_status csa2_index_topk_noalloc(const csa2_kv_planes* kv, int32_t
   SelectArgs ta{scores, score_cols, n_entries, pool, n_blocks_keep, 0, keep_c, k, topk_out, k, n_max};
   launch_select(ta, B, st);
   return launch_status();
+}
+
+extern "C" csa2_status csa2_index_topk_noalloc_check(csa2_stream stream, int64_t* detail) {
+  void* ws = nullptr;
+  csa2_status rs = csa2::noalloc_scratch(&ws);
+  if (rs != CSA2_OK) return rs;
+  return csa2_check(ws, stream, detail);
 }

@@ -279,12 +279,16 @@ size_t csa2_index_topk_workspace_size(int32_t B, int64_t n_max, int32_t k, int32
  *    CSA2_NOALLOC_SCRATCH_BYTES returns CSA2_ERR_WORKSPACE before any launch.
  *    (Batch 32 at a 1,048,576-entry context in HIER_BUILD needs about 18 MB.)
  *  - The first call on a device looks up the array's device address with that
- *    device current; make that first call before any stream capture.
+ *    device current; make that first call before any stream capture.  The
+ *    address is cached per CUDA context: after a device reset the first call in
+ *    the new context looks it up again (again: before any capture).
  *  - All calls share the one array and it keeps the last call's contents; the
  *    call clears the part that must start at zero.  Calls that overlap on the
  *    GPU (other streams, other threads) race on it and must be serialised.
- *  - Device-side error reports go to the array's error word and are not
- *    readable through csa2_check; results equal csa2_index_topk's. */
+ *  - Device-side error reports (an n_entries[b] above n_max, clamped, gives
+ *    CSA2_ERR_INDEX_RANGE; a bounded wait that gave up, CSA2_ERR_DEVICE_TIMEOUT)
+ *    go to the array's error word, which each call clears at its start and
+ *    csa2_index_topk_noalloc_check reads; results equal csa2_index_topk's. */
 #define CSA2_NOALLOC_SCRATCH_BYTES (32u << 20)
 
 /* Prefill (encoder) indexer: Q queries of one sequence slot `seq` score its entries
@@ -308,6 +312,13 @@ csa2_status csa2_index_topk_noalloc(const csa2_kv_planes* kv, int32_t B, const i
                                     csa2_topk_mode mode, int32_t block, int32_t n_blocks_keep,
                                     const int32_t* pool_in, int32_t* topk_out, int32_t* pool_out,
                                     csa2_stream stream);
+
+/* Error word of csa2_index_topk_noalloc (no counterpart on the pages, like the entry point
+ * itself): synchronises `stream`, returns the first device-side error recorded by the
+ * allocation-free calls since the last call's start (CSA2_OK if none) and clears it, as
+ * csa2_check does for a workspace.  *detail (host, may be NULL) receives the offending
+ * value (the n_entries value for CSA2_ERR_INDEX_RANGE).  Allocates nothing. */
+csa2_status csa2_index_topk_noalloc_check(csa2_stream stream, int64_t* detail);
 
 /* ------------------------------------------------------- sparse attention */
 

@@ -66,3 +66,21 @@ def test_noalloc_matches_workspace_entry_point(oracle_mod):
         assert np.array_equal(got[0], ref_hier[0]) and np.array_equal(got[1], ref_hier[1])
         got = without(csa2.TOPK_POOL, 128, 100, pool_in)
         assert np.array_equal(got[0], ref_pool[0])
+        assert csa2.index_topk_noalloc_check() == (0, 0)
+
+    # HIER_BUILD with no pool_out keeps the pool inside the scratch array
+    topk = torch.full((B, 64), -7, dtype=torch.int32, device="cuda")
+    csa2.index_topk_noalloc(c.planes, B, ne, n_max, qd, wd, 64, csa2.TOPK_HIER_BUILD, topk, 8, 100)
+    assert csa2.index_topk_noalloc_check()[0] == 0
+    assert np.array_equal(topk.cpu().numpy(), ref_hier[0])
+
+    # an error found on the device: a visible count above n_max is clamped and reported
+    # through the scratch array's error word, which the check reads and clears
+    bad = to_dev(np.array([4133, 5000, 777], np.int32))
+    topk = torch.full((B, 512), -7, dtype=torch.int32, device="cuda")
+    csa2.index_topk_noalloc(c.planes, B, bad, n_max, qd, wd, 512, csa2.TOPK_FLAT, topk)
+    assert csa2.index_topk_noalloc_check() == (6, 5000)  # CSA2_ERR_INDEX_RANGE, the offending count
+    assert csa2.index_topk_noalloc_check() == (0, 0)     # cleared
+    got = without(csa2.TOPK_FLAT, 512, 0)                 # the next call starts clean
+    assert np.array_equal(got[0], ref_flat[0])
+    assert csa2.index_topk_noalloc_check()[0] == 0
