@@ -66,19 +66,157 @@ def peaks():
     return 6800.0, "fallback"
 
 
+NVML_REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                    0x40: "hw_thermal_slowdown"}
+
+
+class NvmlQueries:
+    """Read-only NVML queries (ctypes on the driver's libnvidia-ml): the SM clock, its
+    maximum, the power draw and the active clock-event reasons of one GPU."""
+
+    def __init__(self, uuid=None, index=0, lib=None):
+        import ctypes
+
+        self.ct = ctypes
+        self.L = lib if lib is not None else ctypes.CDLL("libnvidia-ml.so.1")
+        if self.L.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        rc = 1
+        if uuid:
+            rc = self.L.nvmlDeviceGetHandleByUUID(ctypes.c_char_p(uuid.encode()), ctypes.byref(self.h))
+        if rc != 0:
+            rc = self.L.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h))
+        if rc != 0:
+            raise OSError("no NVML handle for the device")
+        v = ctypes.c_uint(0)
+        self.max_mhz = float(v.value) if self.L.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(v)) == 0 else None
+        self._reasons = getattr(self.L, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.L.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sample(self, with_power: bool):
+        """(sm_mhz, power_w or None, reason mask) now."""
+        ct = self.ct
+        mhz, mw, mask = ct.c_uint(0), ct.c_uint(0), ct.c_ulonglong(0)
+        if self.L.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(mhz)) != 0:  # NVML_CLOCK_SM
+            return None
+        if self._reasons(self.h, ct.byref(mask)) != 0:
+            return None
+        pw = None
+        if with_power and self.L.nvmlDeviceGetPowerUsage(self.h, ct.byref(mw)) == 0:
+            pw = mw.value / 1000.0
+        return float(mhz.value), pw, int(mask.value)
+
+
+def cuda_uuid(local_rank: int):
+    """NVML's UUID string of the CUDA device (None if torch does not report one)."""
+    try:
+        import torch
+
+        u = getattr(torch.cuda.get_device_properties(local_rank), "uuid", None)
+    except Exception:  # noqa: BLE001
+        return None
+    if u is None:
+        return None
+    u = str(u)
+    return u if u.startswith("GPU-") else "GPU-" + u
+
+
+def physical_index(local_rank: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    parts = [p.strip() for p in vis.split(",") if p.strip()]
+    if local_rank < len(parts) and parts[local_rank].isdigit():
+        return int(parts[local_rank])
+    return local_rank
+
+
+class FastClockSampler:
+    """SM clock and clock-event reasons sampled every `period_s` (default 1 ms) by a thread
+    calling NVML directly, so that even a timed region of a few milliseconds holds several
+    samples.  mark() opens the timed region and stop() closes it; summary() reports the
+    samples between the two only.  `queries` is an NvmlQueries (or a stand-in in tests)."""
+
+    def __init__(self, queries, period_s: float = 0.001):
+        self.q = queries
+        self.period = period_s
+        self.samples = []  # (sm_mhz, power_w, mask)
+        self.lo = self.hi = None
+        self._run = False
+        self._thread = None
+
+    def _loop(self):
+        n = 0
+        while self._run:
+            s = self.q.sample(with_power=(n % 20 == 0))
+            if s is not None:
+                self.samples.append(s)
+            n += 1
+            time.sleep(self.period)
+
+    def __enter__(self):
+        self._run = True
+        self._thread = threading.Thread(target=self._loop, daemon=True)
+        self._thread.start()
+        t0 = time.time()
+        while not self.samples and time.time() - t0 < 5.0:
+            time.sleep(0.001)
+        return self
+
+    def __exit__(self, *a):
+        self._run = False
+        if self._thread:
+            self._thread.join(timeout=5.0)
+
+    def mark(self):
+        self.lo = len(self.samples)
+
+    def stop(self):
+        self.hi = len(self.samples)
+
+    def summary(self):
+        lo = self.lo or 0
+        hi = self.hi if self.hi is not None else len(self.samples)
+        rows = self.samples[lo:hi]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": self.q.max_mhz, "reasons": ["no samples"]}
+        reasons = sorted({name for _, _, m in rows for bit, name in NVML_REASON_BITS.items() if m & bit})
+        pw = [p for _, p, _ in rows if p is not None]
+        out = {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": self.q.max_mhz,
+               "sm_mhz_min": min(r[0] for r in rows), "reasons": reasons, "samples": len(rows),
+               "window": "timed region only", "source": f"NVML every {self.period * 1e3:g} ms"}
+        if pw:
+            out["power_w_max"] = max(pw)
+        return out
+
+
+def clock_sampler(local_rank: int):
+    """The fast NVML sampler when the driver's NVML loads, else nvidia-smi every 200 ms."""
+    try:
+        return FastClockSampler(NvmlQueries(cuda_uuid(local_rank), physical_index(local_rank)))
+    except (OSError, AttributeError):
+        return ClockSampler(physical_index(local_rank))
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle samples every 200 ms while running."""
+    """nvidia-smi clock / throttle samples every 200 ms while running (the fallback when
+    NVML cannot be loaded directly)."""
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
         self.file = None
         self.offset = 0  # samples before this file offset were taken before the timed region
+        self.end = None  # file size when the timed region closed
 
     def mark(self):
         """Call at the start of the timed region: later samples only are summarised."""
         if self.proc:
             self.offset = os.path.getsize(self.file.name)
+
+    def stop(self):
+        """Call at the end of the timed region: later samples are not summarised."""
+        if self.proc:
+            self.end = os.path.getsize(self.file.name)
 
     def __enter__(self):
         self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
@@ -113,7 +251,8 @@ class ClockSampler:
         rows = []
         with open(self.file.name) as fh:
             fh.seek(self.offset)
-            lines = fh.read().splitlines()
+            text = fh.read() if self.end is None else fh.read(max(self.end - self.offset, 0))
+            lines = text.splitlines()
         if self.offset and lines:
             lines = lines[1:]  # may be a sample cut at the offset
         for line in lines:
@@ -129,66 +268,116 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v == "Active"})
         return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows), "window": "timed region only"}
+                "reasons": reasons, "samples": len(rows), "window": "timed region only",
+                "source": "nvidia-smi every 200 ms"}
 
 
 # ----------------------------------------------------------------------------- oracle sample
 
-def oracle_sample(n_queries: int, steps: int, warmup: int = 0):
-    """Time the CPU oracle on `n_queries` of the workload's queries (full 1M-entry caches),
-    after `warmup` untimed passes.  Returns (queries/s, threads, description).  Setup (input
-    synthesis, encoding) is untimed."""
+def oracle_planes_query(b: int, threads: int):
+    """The oracle's encoding of query b's whole 1,048,576-entry cache, and its inputs."""
     import numpy as np
     from concurrent.futures import ThreadPoolExecutor
 
     import oracle
     from synth import workloads as W
 
-    threads = os.cpu_count() or 1
     q, w = W.index_query(SEED, 0, B)
     hv = W.hot_vectors(q, w, 3.0)
-    qa = W.attn_query(SEED, 0, B)
-    swa = W.swa_rows(SEED, 0, B)
     chunk = 1 << 16
 
-    def encode(b, j0):
+    def encode(j0):
         cnt = min(chunk, N - j0)
         kv = oracle.quantize_main(W.main_latents(SEED, 0, B, N, b, j0, cnt))
         ix = oracle.quantize_index(W.index_latents(SEED, 0, B, N, b, j0, cnt, 0.02, hv[b]))
         return j0, kv, ix
 
-    planes = []
+    kvc = np.empty((N, 256), np.uint8)
+    kvs = np.empty((N, 32), np.uint8)
+    ixc = np.empty((N, 64), np.uint8)
+    ixs = np.empty((N, 4), np.uint8)
     with ThreadPoolExecutor(threads) as ex:
-        for b in range(n_queries):
-            kvc = np.empty((N, 256), np.uint8)
-            kvs = np.empty((N, 32), np.uint8)
-            ixc = np.empty((N, 64), np.uint8)
-            ixs = np.empty((N, 4), np.uint8)
-            for j0, (c1, s1), (c2, s2) in ex.map(lambda j: encode(b, j), range(0, N, chunk)):
-                kvc[j0:j0 + c1.shape[0]] = c1
-                kvs[j0:j0 + c1.shape[0]] = s1
-                ixc[j0:j0 + c2.shape[0]] = c2
-                ixs[j0:j0 + c2.shape[0]] = s2
-            planes.append((kvc, kvs, ixc, ixs))
+        for j0, (c1, s1), (c2, s2) in ex.map(encode, range(0, N, chunk)):
+            kvc[j0:j0 + c1.shape[0]], kvs[j0:j0 + c1.shape[0]] = c1, s1
+            ixc[j0:j0 + c2.shape[0]], ixs[j0:j0 + c2.shape[0]] = c2, s2
+    return (kvc, kvs, ixc, ixs), q[b], w[b], W.attn_query(SEED, 0, B)[b], W.swa_rows(SEED, 0, B)[b]
 
-    def one(b):
-        kvc, kvs, ixc, ixs = planes[b]
-        s = oracle.index_scores(ixc, ixs, q[b], w[b], nthreads=threads)
-        pool = oracle.hier_pool(oracle.block_max(s, BLOCK), KEEP)
-        sel = oracle.pool_topk(s, pool, BLOCK, K_TOP)
-        oracle.attention(kvc, kvs, sel, swa[b], qa[b], 1 / math.sqrt(512))
 
+def oracle_query_path(planes, q, w, qa, swa, threads, scores=None):
+    """One query's whole path in the oracle: scores (unless given), block maxima, pool,
+    top-512 within the pool, attention over the selection and the window."""
+    import oracle
+
+    kvc, kvs, ixc, ixs = planes
+    s = oracle.index_scores(ixc, ixs, q, w, nthreads=threads) if scores is None else scores
+    pool = oracle.hier_pool(oracle.block_max(s, BLOCK), KEEP)
+    sel = oracle.pool_topk(s, pool, BLOCK, K_TOP)
+    oracle.attention(kvc, kvs, sel, swa, qa, 1 / math.sqrt(512))
+
+
+def oracle_sample(n_queries: int, steps: int, warmup: int = 0):
+    """Time the CPU oracle on `n_queries` of the workload's queries (full 1M-entry caches),
+    after `warmup` untimed passes.  Returns (queries/s, threads, description).  Setup (input
+    synthesis, encoding) is untimed."""
+    threads = os.cpu_count() or 1
+    data = [oracle_planes_query(b, threads) for b in range(n_queries)]
     for _ in range(warmup):
-        for b in range(n_queries):
-            one(b)
+        for d in data:
+            oracle_query_path(*d, threads)
     t0 = time.perf_counter()
     for _ in range(steps):
-        for b in range(n_queries):
-            one(b)
+        for d in data:
+            oracle_query_path(*d, threads)
     dt = time.perf_counter() - t0
     desc = (f"{n_queries} of the {B} queries at the full 1,048,576-entry context, {steps} pass(es): "
             f"oracle scores (fp64, {threads} threads), block max, pool, top-512, attention")
     return n_queries * steps / dt, threads, desc
+
+
+REF_BUDGET_S = 150.0  # timed CPU work of the reference arm, at most
+
+
+def oracle_reference_steps(steps: int, warmup: int):
+    """The reference arm: `steps` timed steps of the oracle after `warmup` untimed ones.
+    A step is one query's whole path (query 0 of the workload, full context) while
+    steps x (one query's time) fits REF_BUDGET_S; beyond that each step scores one of f
+    equal slices of the query's entries, and every f-th step also runs the selection and
+    attention of the query just completed, so that f steps do one query's work.
+    Returns (queries/s, threads, description, f)."""
+    import numpy as np
+
+    import oracle
+
+    threads = os.cpu_count() or 1
+    planes, q, w, qa, swa = oracle_planes_query(0, threads)
+    t_q = None
+    for i in range(max(warmup, 1)):  # at least one untimed pass, which also sizes the steps
+        t0 = time.perf_counter()
+        oracle_query_path(planes, q, w, qa, swa, threads)
+        t_q = time.perf_counter() - t0
+    f = max(1, math.ceil(steps * t_q / REF_BUDGET_S))
+    kvc, kvs, ixc, ixs = planes
+    bounds = [N * i // f for i in range(f + 1)]
+    scores = np.empty(N, np.float64)
+    t0 = time.perf_counter()
+    for st in range(steps):
+        if f == 1:
+            oracle_query_path(planes, q, w, qa, swa, threads)
+            continue
+        sl = st % f
+        lo, hi = bounds[sl], bounds[sl + 1]
+        scores[lo:hi] = oracle.index_scores(ixc[lo:hi], ixs[lo:hi], q, w, nthreads=threads)
+        if sl == f - 1:
+            oracle_query_path(planes, q, w, qa, swa, threads, scores=scores)
+    dt = time.perf_counter() - t0
+    if f == 1:
+        desc = (f"query 0 of the {B} at the full 1,048,576-entry context, one query per step: oracle scores "
+                f"(fp64, {threads} threads), block max, pool, top-512, attention")
+    else:
+        desc = (f"query 0 of the {B} at the full 1,048,576-entry context; each step scores 1/{f} of its "
+                f"entries (fp64, {threads} threads) and every {f}th step runs the block max, pool, top-512 and "
+                f"attention of the completed query, so {f} steps = one query (rate = steps / {f} / time)")
+    return steps / f / dt, threads, desc, f
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -677,6 +866,112 @@ def run_v4(dev, st, calls: int, warmup: int):
     return res
 
 
+SMALL_STEPS = 20
+
+
+def run_small_decode(dev, st, wl, steps: int, warmup: int):
+    """A sub-L2 decode workload (one FLAT index call + wl.n_attn attention calls sharing its
+    top-k, each with its own q and window): per-step device time with L2 flushed before
+    every timed step (a write of twice the L2 size) and unflushed (back to back), the HBM
+    roofline of the algorithmic bytes, and the oracle timed on the same queries' work."""
+    import numpy as np
+    import torch
+
+    import compressed_sparse_attention_nvfp4_gb300 as csa2
+    import oracle
+    from compressed_sparse_attention_nvfp4_gb300 import workload as WL
+    from synth import workloads as W
+
+    Bq, Nq, k, n_attn = wl.B, wl.N, wl.k, wl.n_attn
+    with torch.cuda.stream(st):
+        planes = csa2.Planes.empty(Bq, Nq, dev)
+        WL.fill_planes(planes, wl.seed, 0, Bq, Nq, stream=st)
+        qd, wd, q_h, w_h = WL.index_query_dev(wl.seed, 0, Bq, dev)
+        qa = [WL.attn_query_dev(wl.seed, l, Bq, dev) for l in range(n_attn)]
+        swa = [WL.swa_dev(wl.seed, l, Bq, NSWA, dev, stream=st) for l in range(n_attn)]
+        ne = torch.full((Bq,), Nq, dtype=torch.int32, device=dev)
+        topk = torch.empty((Bq, k), dtype=torch.int32, device=dev)
+        outs = [torch.empty((Bq, 64, 512), dtype=torch.float32, device=dev) for _ in range(n_attn)]
+        ws_i = csa2.workspace(csa2.index_topk_workspace_size(Bq, Nq, k, BLOCK, 0), dev)
+        ws_a = csa2.workspace(csa2.sparse_attn_workspace_size(Bq, k, NSWA), dev)
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    scale = 1.0 / math.sqrt(512)
+
+    def step():
+        csa2.index_topk(planes, Bq, ne, Nq, qd, wd, k, csa2.TOPK_FLAT, topk, ws_i, stream=st)
+        for l in range(n_attn):
+            csa2.sparse_attn_decode(planes, Bq, topk, k, swa[l], NSWA, qa[l][0], scale, outs[l], ws_a, stream=st)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    assert csa2.check(ws_i, st)[0] == 0 and csa2.check(ws_a, st)[0] == 0
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with torch.cuda.stream(st):
+        for a, b in ev:
+            flush_buf.fill_(1)  # evicts the cache and the previous step's data from L2
+            a.record(st)
+            step()
+            b.record(st)
+    torch.cuda.synchronize()
+    flushed = sorted(a.elapsed_time(b) for a, b in ev)
+    a0, b0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(st)
+    for _ in range(steps):
+        step()
+    b0.record(st)
+    torch.cuda.synchronize()
+    warm_ms = a0.elapsed_time(b0) / steps
+    assert csa2.check(ws_i, st)[0] == 0 and csa2.check(ws_a, st)[0] == 0
+    csa2.timing_enable(True)
+    step()
+    torch.cuda.synchronize()
+    kt = csa2.kernel_times()
+    csa2.timing_enable(False)
+    med = statistics.median(flushed)
+    step_bytes = Bq * (Nq * IDX_BYTES + n_attn * (k * MAIN_BYTES + NSWA * SWA_ROW))
+    hbm, kind = peaks()
+    achieved = step_bytes / (med * 1e-3) / 1e9
+
+    # the oracle on the same work: query 0's scores, top-k and attention passes
+    kvc, kvs = oracle.quantize_main(W.main_latents(wl.seed, 0, Bq, Nq, 0, 0, Nq))
+    ixc, ixs = oracle.quantize_index(W.index_latents(wl.seed, 0, Bq, Nq, 0, 0, Nq))
+    swa_h = [W.swa_rows(wl.seed, l, Bq)[0] for l in range(n_attn)]
+    threads = os.cpu_count() or 1
+
+    def oracle_query():
+        sc = oracle.index_scores(ixc, ixs, q_h[0], w_h[0], nthreads=threads)
+        sel = oracle.topk(sc, k)
+        for l in range(n_attn):
+            oracle.attention(kvc, kvs, sel, swa_h[l], qa[l][1][0], scale)
+
+    oracle_query()  # warm
+    reps, t0 = 0, time.perf_counter()
+    while reps < 3 or (time.perf_counter() - t0 < 2.0 and reps < 200):
+        oracle_query()
+        reps += 1
+    o_s = (time.perf_counter() - t0) / reps  # seconds per query
+    return {
+        "workload": wl.name, "B": Bq, "N_entries": Nq, "k": k, "n_swa": NSWA, "attention_passes": n_attn,
+        "steps": steps, "warmup": warmup,
+        "us_per_step_l2_flushed": round(med * 1e3, 2), "us_per_step_l2_flushed_mean": round(
+            statistics.mean(flushed) * 1e3, 2),
+        "us_per_step_unflushed": round(warm_ms * 1e3, 2),
+        "queries_per_s_l2_flushed": round(Bq / (med * 1e-3), 1),
+        "l2": f"flushed before each timed step by writing {2 * l2} B (2 x L2); unflushed = back to back",
+        "kernels_ms_per_launch": {kk: round(t / max(n, 1), 4) for kk, (n, t) in sorted(kt.items())},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "peak_kind": kind, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None, "algorithmic_bytes_per_step": step_bytes,
+                     "of": "the whole step (all its kernels), L2 flushed"},
+        "cpu_baseline": {"value": round(1.0 / o_s, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "us_per_query": round(o_s * 1e6, 1),
+                         "sample": f"query 0 of the workload, {reps} passes: fp64 scores over its {Nq} entries, "
+                                   f"top-{k}, {n_attn} attention pass(es)"},
+    }
+
+
 def tensor_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -706,6 +1001,14 @@ def max_over_ranks(times, world: int, device="cpu"):
 def job_rate(world: int, per_rank_units: int, steps: int, ms: float) -> float:
     """Whole-job units per second: every rank processed per_rank_units per step."""
     return world * per_rank_units * steps / (ms * 1e-3)
+
+
+def line_config(world: int) -> dict:
+    """The workload's config object, the same in both arms' lines."""
+    return {"workload": WORKLOAD, "B": B, "N_entries": N, "k": K_TOP, "block": BLOCK,
+            "n_blocks_keep": KEEP, "n_swa": NSWA, "seed": SEED if world == 1 else f"{SEED} + 1000 x rank",
+            "l2": "inputs larger than L2 (11.95 GB cache resident in HBM); no flush",
+            "parallelism": f"replicas x{world}"}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -761,7 +1064,7 @@ def run_ours(args, rank, world, local_rank):
     # timed region: K steps bracketed by one pair of events (nothing else recorded
     # between the kernels, so their launches overlap as in production)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local_rank) as clk:
+    with clock_sampler(local_rank) as clk:
         barrier()
         torch.cuda.synchronize()
         clk.mark()
@@ -771,6 +1074,7 @@ def run_ours(args, rank, world, local_rank):
             attn_call()
         stop.record(st)
         torch.cuda.synchronize()
+        clk.stop()
         barrier()
     elapsed_ms = start.elapsed_time(stop)
     clocks = clk.summary()
@@ -867,10 +1171,7 @@ def run_ours(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": args.dtype_label, "data": "synthetic (seeded counter-based generator)",
-        "config": {"workload": WORKLOAD, "B": B, "N_entries": N, "k": K_TOP, "block": BLOCK,
-                   "n_blocks_keep": KEEP, "n_swa": NSWA, "seed": SEED if world == 1 else f"{SEED} + 1000 x rank",
-                   "l2": "inputs larger than L2 (11.95 GB cache resident in HBM); no flush",
-                   "parallelism": f"replicas x{world}"},
+        "config": line_config(world),
         "step_breakdown_ms": {"index_topk": round(idx_ms, 4), "sparse_attn": round(att_ms, 4)},
         "kernels_ms_per_launch": {k: round(t / max(n, 1), 4) for k, (n, t) in sorted(ktimes.items())},
         "step_hbm": {"algorithmic_bytes": step_bytes,
@@ -889,6 +1190,11 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": launches,
         "clocks": clocks,
     }
+    if not args.no_small:
+        from synth import workloads as W
+
+        line["config0_single_4k"] = run_small_decode(dev, st, W.SINGLE_4K, SMALL_STEPS, 5)
+        line["config1_encoder_b64"] = run_small_decode(dev, st, W.ENCODER_B64, SMALL_STEPS, 5)
     if not args.no_attn:
         line["attention_b128"] = run_attention(dev, st, 50, 3)
     if not args.no_cache_write:
@@ -914,6 +1220,10 @@ def main():
                     help="skip the prefill cache-write measurement (its own object in the line)")
     ap.add_argument("--no-step40", action="store_true",
                     help="skip the 40-layer step measurement (its own object in the line)")
+    ap.add_argument("--no-small", action="store_true",
+                    help="skip the single-query 4K and batch-64 encoder workloads (their own objects)")
+    ap.add_argument("--small-only", action="store_true",
+                    help="profiling case: only the single-query 4K and batch-64 encoder workloads")
     ap.add_argument("--no-attn", action="store_true",
                     help="skip the batch-128 attention measurement (its own object in the line)")
     ap.add_argument("--attn-only", action="store_true",
@@ -945,17 +1255,14 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        steps = max(1, min(args.steps, 5))
-        warm = max(0, min(args.warmup, 10))  # each pass is a few seconds of CPU work
-        v, cores, desc = oracle_sample(1, steps, warm)
+        v, cores, desc, f = oracle_reference_steps(args.steps, args.warmup)
         print(json.dumps({
             "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": UNIT, "n_gpus": 0,
-            "steps": steps, "warmup": warm, "higher_is_better": True, "scaling": "weak",
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded counter-based generator)",
-            "config": {"workload": WORKLOAD, "B": B, "N_entries": N, "k": K_TOP, "block": BLOCK,
-                       "n_blocks_keep": KEEP, "n_swa": NSWA, "seed": SEED},
+            "config": line_config(world),
             "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": desc},
+                             "sample": desc, "steps_per_query": f},
             "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}))
         return
@@ -978,6 +1285,22 @@ def main():
         if rank == 0:
             print(json.dumps({"attention_b128": run_attention(dev, st, max(1, min(args.steps, 200)),
                                                               max(1, args.warmup))}), flush=True)
+        return
+    if args.small_only:
+        import torch
+
+        torch.cuda.set_device(local_rank)
+        import compressed_sparse_attention_nvfp4_gb300 as csa2
+        from synth import workloads as W
+
+        csa2.lib()
+        dev = torch.device("cuda", local_rank)
+        st = torch.cuda.Stream(device=dev)
+        if rank == 0:
+            n = max(1, min(args.steps, SMALL_STEPS))
+            print(json.dumps({"config0_single_4k": run_small_decode(dev, st, W.SINGLE_4K, n, args.warmup),
+                              "config1_encoder_b64": run_small_decode(dev, st, W.ENCODER_B64, n, args.warmup)}),
+                  flush=True)
         return
     if args.step40_only:
         import torch
