@@ -6,18 +6,22 @@
 //
 // k_attn stages q in shared memory as q' = q 2^-s_h in f16 with a power-of-two
 // prescale per head (exact for bf16 q), then runs the query's rows (selected
-// entries, then window rows) in chunks of 128 on the tensor cores (tcgen05,
+// entries, then window rows) in chunks of 64 on the tensor cores (tcgen05,
 // kind::f16, fp32 accumulation in tensor memory):
 //   1. the chunk's rows are dequantized into shared memory as f16 (exact:
 //      E2M1 x E4M3 has at most 6 significant bits), interleaved
 //      X[c/8][row][c%8]: K-major for S, M-major for O;
-//   2. S^T[128 rows x 64 heads] = X q'^T;
+//   2. S[64 heads x 64 rows] = q' X^T (heads as M, so each softmax thread owns
+//      one head and its rows lie in its own registers);
 //   3. online softmax per head, P rounded to f16 once, l = sums of the rounded P;
 //   4. O^T[512 x 64] += X^T P^T (four 128-channel M tiles).
-// One CTA per query keeps O in tensor memory across all its chunks, so no
-// partial result leaves the SM.  When the batch is too small to fill the GPU
-// a query's chunks are split over a few CTAs, which write (max, l, O) partials
-// that a merge kernel combines by log-sum-exp.
+// Two chunk slots (rows, S accumulators, probabilities) let the tensor cores
+// compute S of one chunk while the softmax of the other runs; the MMAs go in
+// pairs S(2p), S(2p+1), O(2p), O(2p+1), so the dequantization of a slot overlaps
+// the MMAs of the other.  One CTA per query keeps O in tensor memory across all
+// its chunks, so no partial result leaves the SM.  When the batch is too small
+// to fill the GPU a query's chunks are split over a few CTAs, which write
+// (max, l, O) partials that a merge kernel combines by log-sum-exp.
 #include "codec.cuh"
 #include "ptx.cuh"
 #include "timing.cuh"
@@ -26,17 +30,22 @@ namespace csa2 {
 
 namespace {
 
-constexpr int kRows = 128;  // rows per CTA: the M of the S MMA
-constexpr int kAT = 288;    // warps 0-7: two threads per row in the gather, the epilogues; warp 8: control
+constexpr int kRows = 64;   // rows per chunk: the N of the S MMA, the K of the O MMAs
+constexpr int kAT = 288;    // warps 0-7: a quarter row each in the gather, the softmax, the epilogue; warp 8: MMAs
 constexpr int kCtlWarp = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 // the softmax reference (log2 units) moves only when a chunk exceeds it by
 // more than 8 nats, so probabilities stay below e^8 (inside f16)
 constexpr float kTau2 = 8.0f * kLog2e;
-// q' plane stride: 64 heads x 16 bytes plus 16 bytes of padding, so that the
-// 16-byte stores of consecutive channel chunks fall in different banks
-constexpr int kQPlane = kHAtt * 8 + 8;  // in f16 elements (1040 bytes)
-constexpr uint32_t kAttnTmemCols = 512;  // O^T 256 columns, S^T 64
+// the reference of a head with no row yet: finite, so that 2^(S c2 - kNoRef) of a
+// missing (-inf) row stays 0, and far below any logit, so that a row exceeds it
+constexpr float kNoRef = -1.0e30f;
+// q' plane stride: 64 heads x 16 bytes, unpadded, so that every core matrix the
+// S MMAs read sits on a 128-byte line
+constexpr int kQPlane = kHAtt * 8;       // in f16 elements (1024 bytes)
+constexpr int kXPlane = kRows * 8;       // f16 elements per 8-channel plane of a slot (1024 bytes)
+constexpr uint32_t kAttnTmemCols = 512;  // O^T 256 columns, two S slots of 64
+constexpr uint32_t kTmemS = 256;         // first column of S slot 0
 constexpr long long kAttnWaitBudget = 1LL << 32;
 
 // In-layer extras ("DeepSeek-V4: ...", CSA, other details), each off when null /
@@ -54,24 +63,33 @@ struct AttnExtras {
 };
 
 struct __align__(1024) AttnSmem {
-  uint16_t X[kDMain / 8][kRows * 8];  // f16 rows [c/8][row][c%8]; planes 0-31 / 32-63 = channel halves
-  uint16_t q[kDMain / 8][kQPlane];    // f16 q' [c/8][head][c%8], planes padded
-  uint16_t P[kHAtt / 8][kRows * 8];   // f16 probabilities [h/8][row][h%8]
-  float c2[kHAtt];                    // log2(e) * softmax_scale * 2^s_h: logit (log2 units) per raw S
-  float m2w[8][32];                   // per warp: the reference of its 32 heads (0 while none)
-  float red[4][kHAtt];                // per lane quarter column maxima of the chunk
-  float red2[4][kHAtt];               // per lane quarter column sums of the chunk's P
-  int valid[kRows];
-  uint64_t q_full;                    // q' and colscale written (8 warps)
-  uint64_t x_full[2];                 // channel half of X written (4 warps each)
-  uint64_t s_full;                    // S^T MMAs complete
-  uint64_t red_full;                  // chunk maxima posted (8 warps)
-  uint64_t p_full;                    // P written, O rescaled, sums posted (8 warps)
-  uint64_t x_free[2];                 // O MMAs reading that channel half of X (and P) complete
-  uint64_t drained;                   // every MMA issued complete
+  uint16_t X[2][kDMain / 8][kXPlane];  // per slot: f16 rows [c/8][row][c%8]; planes 0-31 / 32-63 = channel halves
+  uint16_t q[kDMain / 8][kQPlane];     // f16 q' [c/8][head][c%8]
+  uint16_t P[2][kRows / 8][kHAtt * 8]; // per slot: f16 probabilities [row/8][head][row%8] (P^T K-major)
+  float c2[kHAtt];                     // log2(e) * softmax_scale * 2^s_h: logit (log2 units) per raw S
+  float mx[2][kHAtt];                  // per column half: a chunk's scaled maxima (exact-maximum path)
+  float alpha[kHAtt];                  // factor of O and l when a head's reference moved
+  float lsum[2][kHAtt];                // per column half: the probability sums of every chunk
+  float inv[kHAtt];                    // 1 / softmax denominator (or 1 for partials)
+  int32_t idx[CSA2_MAX_TOPK];          // this CTA's selected-entry indices (its chunks' rows below k)
+  uint32_t vmask[2][2];                // per slot and 32-row half: rows that exist
+  int vote[2][8];                      // per chunk parity and warp: a logit above its head's threshold
+  uint64_t q_load;                     // the query's bf16 rows copied into slot 1 (bulk copy)
+  uint64_t q_full;                     // q' and c2 written (8 warps)
+  uint64_t x_full[2][2];               // per slot, channel half of X written (4 warps each)
+  uint64_t s_full[2];                  // per slot: S MMAs complete
+  uint64_t p_full[2];                  // per slot: P written (8 warps)
+  uint64_t x_free[2];                  // per slot: O MMAs reading its X and P complete
+  uint64_t vote_full;                  // votes / sums / denominators posted (8 warps)
+  uint64_t max_full;                   // maxima / factors posted (8 warps; chunks that need them)
+  uint64_t drained;                    // every MMA issued complete
   uint32_t tmem_base;
   int abort_flag;
 };
+
+// fits the 227 KB of shared memory a CTA may have (and so every MMA operand sits
+// below 256 KB, which the constant-stepped descriptors rely on)
+static_assert(sizeof(AttnSmem) <= 232448, "attention shared memory");
 
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   uint32_t r;
@@ -92,50 +110,16 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
   return h;
 }
 
-struct MaxOp {
-  __device__ __forceinline__ float operator()(float a, float b) const { return fmaxf(a, b); }
-};
-struct AddOp {
-  __device__ __forceinline__ float operator()(float a, float b) const { return a + b; }
-};
-
-// Reduce-scatter over a warp: every lane holds 32 values; afterwards lane l
-// holds op over the 32 lanes of value l (31 shuffles; v is consumed).  The
-// pairing is fixed, so sums are reproducible.
-template <class Op>
-__device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane, Op op) {
-#pragma unroll
-  for (int s = 16; s >= 1; s >>= 1) {
-    const bool up = (lane & s) != 0;
-#pragma unroll
-    for (int j = 0; j < s; ++j) {
-      const float keep = up ? v[j + s] : v[j];
-      const float send = up ? v[j] : v[j + s];
-      v[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, s));
-    }
-  }
-  return v[0];
-}
-
 // q' = q_h 2^-s_h in f16 with 2^s_h bringing the head's largest |q| to
 // [2^14, 2^15), clamped so that both 2^s_h and 2^-s_h are normal fp32 values;
 // bf16 q keeps q' exact and inside the f16 range (with RMSNorm or RoPE the
 // fp32 result is rounded to f16 once).  Warp w converts heads 8w..8w+7: lane l
 // holds channels 8l..8l+7 and 256+8l..256+8l+7 of each, i.e. chunks l and 32+l
 // of the [c/8][head][c%8] image; the rotated pairs sit in lanes 24-31.
-struct QFetch {
-  uint4 raw[8][2];
-};
-__device__ __forceinline__ void fetch_q(QFetch& f, const uint16_t* __restrict__ qg, int b, int warp, int lane) {
-#pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const uint4* src = reinterpret_cast<const uint4*>(qg + ((int64_t)b * kHAtt + warp * 8 + u) * kDMain);
-    f.raw[u][0] = src[lane];
-    f.raw[u][1] = src[32 + lane];
-  }
-}
+// q' is converted from a shared-memory copy of the query's bf16 rows ([64][512],
+// brought in by one bulk copy), one head at a time.
 template <bool kEx>
-__device__ __forceinline__ void stage_q(AttnSmem& S, const QFetch& f, float scale, int warp, int lane,
+__device__ __forceinline__ void stage_q(AttnSmem& S, const uint16_t* qs, float scale, int warp, int lane,
                                         const AttnExtras& ex, int b) {
   // per lane: the RMSNorm weights of its 16 channels, the cos / sin of its 4 pairs
   float wq[16], rc[4], rs[4];
@@ -155,12 +139,14 @@ __device__ __forceinline__ void stage_q(AttnSmem& S, const QFetch& f, float scal
 #pragma unroll
     for (int p = 0; p < 4; ++p) rope_cos_sin(ex.th.t[(256 + lane * 8 - kRopeFirst) / 2 + p], pos, rc[p], rs[p]);
   }
-#pragma unroll
+#pragma unroll 2
   for (int u = 0; u < 8; ++u) {
     float v[16];
+    const uint4* src = reinterpret_cast<const uint4*>(qs + (warp * 8 + u) * kDMain);
+    const uint4 raw[2] = {src[lane], src[32 + lane]};
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      const uint32_t w4[4] = {f.raw[u][i].x, f.raw[u][i].y, f.raw[u][i].z, f.raw[u][i].w};
+      const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         v[8 * i + 2 * j] = __uint_as_float(w4[j] << 16);
@@ -203,10 +189,12 @@ __device__ __forceinline__ void stage_q(AttnSmem& S, const QFetch& f, float scal
   }
 }
 
-// One thread's half row of a chunk, fetched ahead of its dequantization.
+// One thread's quarter row of a chunk (128 channels), fetched ahead of its
+// dequantization: a selected entry's 64 code bytes and 8 scale bytes, or a
+// window row's 128 bytes.
 struct RowFetch {
-  uint4 raw[16];  // main entry: 8 x 16 code bytes + 16 scale bytes; window row: 256 bytes
-  int kind;       // 0 = no row, 1 = main entry, 2 = window row
+  uint4 raw[8];
+  int kind;  // 0 = no row, 1 = main entry, 2 = window row
 };
 
 // entry of chunk row gr (rows gr >= k are window rows or padding): topk[b][gr],
@@ -218,94 +206,121 @@ __device__ __forceinline__ int64_t fetch_index(const int32_t* __restrict__ topk,
   return (int64_t)topk[(int64_t)b * k + gr];
 }
 
-// Starts the loads of half a row: a selected entry (gr < k, index idx), a
-// window row (k <= gr < k + n_swa) or nothing.
+// Starts the loads of quarter `part` (channels 128 part ..) of chunk row gr: a
+// selected entry (gr < k, index idx), a window row (k <= gr < k + n_swa) or nothing.
 __device__ __forceinline__ void issue_row(RowFetch& f, int64_t idx, const uint8_t* __restrict__ kv_codes,
                                           const uint8_t* __restrict__ kv_scales, int64_t seq_stride,
                                           const uint8_t* __restrict__ swa, int n_swa, int k, int b, int gr,
-                                          int half, void* ws, const int64_t* __restrict__ win_pos, int64_t win_lo) {
+                                          int part, void* ws, const int64_t* __restrict__ win_pos, int64_t win_lo) {
   f.kind = 0;
   if (gr < k) {
     if (idx >= 0 && idx < seq_stride) {
       const int64_t e = (int64_t)b * seq_stride + idx;
-      const uint4* cs = reinterpret_cast<const uint4*>(kv_codes + e * 256 + half * 128);
+      const uint4* cs = reinterpret_cast<const uint4*>(kv_codes + e * 256 + part * 64);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) f.raw[i] = cs[i];
-      f.raw[8] = reinterpret_cast<const uint4*>(kv_scales + e * 32)[half];
+      for (int i = 0; i < 4; ++i) f.raw[i] = cs[i];
+      const uint2 sc = reinterpret_cast<const uint2*>(kv_scales + e * 32)[part];
+      f.raw[4].x = sc.x;
+      f.raw[4].y = sc.y;
       f.kind = 1;
-    } else if (idx != -1 && half == 0) {
+    } else if (idx != -1 && part == 0) {
       report_error(ws, CSA2_ERR_INDEX_RANGE, idx);
     }
   } else if (gr - k < n_swa && (!win_pos || win_pos[(int64_t)b * n_swa + (gr - k)] >= win_lo)) {
-    const uint4* src = reinterpret_cast<const uint4*>(swa + ((int64_t)b * n_swa + (gr - k)) * kDMain + half * 256);
+    const uint4* src = reinterpret_cast<const uint4*>(swa + ((int64_t)b * n_swa + (gr - k)) * kDMain + part * 128);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) f.raw[i] = src[i];
+    for (int i = 0; i < 8; ++i) f.raw[i] = src[i];
     f.kind = 2;
   }
 }
 
-// Writes the half row [256 half, 256 half + 256) of row r to X as f16 (zeros
-// when there is no row), 64 channels at a time; returns whether the row exists.
-__device__ __forceinline__ bool dequant_half_row(AttnSmem& S, const RowFetch& f, int r, int half) {
+// Writes channels [128 part, 128 part + 128) of row r to slot `slot` of X as f16
+// (zeros when there is no row); returns whether the row exists.
+__device__ __forceinline__ bool dequant_quarter_row(AttnSmem& S, const RowFetch& f, int slot, int r, int part) {
 #pragma unroll
-  for (int blk = 0; blk < 4; ++blk) {
-    uint32_t w[32];  // channels 64 blk + 2j, 2j + 1 in w[j]
+  for (int g = 0; g < 8; ++g) {  // 16 channels: planes 16 part + 2g, 2g + 1
+    uint32_t w[8];
     if (f.kind == 1) {
-      const uint32_t sw = blk == 0 ? f.raw[8].x : blk == 1 ? f.raw[8].y : blk == 2 ? f.raw[8].z : f.raw[8].w;
+      const uint32_t sb = ((g < 4 ? f.raw[4].x : f.raw[4].y) >> (8 * (g & 3))) & 0xFFu;
+      const uint32_t s2 = e4m3x2_to_f16x2(sb | (sb << 8));
+      const uint4 cw = f.raw[g / 2];
+      const uint32_t w0 = (g & 1) ? cw.z : cw.x, w1 = (g & 1) ? cw.w : cw.y;
+      uint32_t h0[4], h1[4];
+      e2m1x8_to_f16(w0, h0);
+      e2m1x8_to_f16(w1, h1);
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {  // 16 channels: 8 code bytes, one E4M3 scale
-        const int G = blk * 4 + g;
-        const uint32_t sb = (sw >> (8 * g)) & 0xFFu;
-        const uint32_t s2 = e4m3x2_to_f16x2(sb | (sb << 8));
-        const uint4 cw = f.raw[G / 2];
-        const uint32_t w0 = (G & 1) ? cw.z : cw.x, w1 = (G & 1) ? cw.w : cw.y;
-        uint32_t h0[4], h1[4];
-        e2m1x8_to_f16(w0, h0);
-        e2m1x8_to_f16(w1, h1);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          w[8 * g + j] = hmul2_u32(h0[j], s2);
-          w[8 * g + 4 + j] = hmul2_u32(h1[j], s2);
-        }
+      for (int j = 0; j < 4; ++j) {
+        w[j] = hmul2_u32(h0[j], s2);
+        w[4 + j] = hmul2_u32(h1[j], s2);
       }
     } else if (f.kind == 2) {
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {  // 16 channels per uint4
-        const uint4 v = f.raw[blk * 4 + u];
-        w[8 * u + 0] = e4m3x2_to_f16x2(v.x);
-        w[8 * u + 1] = e4m3x2_to_f16x2(v.x >> 16);
-        w[8 * u + 2] = e4m3x2_to_f16x2(v.y);
-        w[8 * u + 3] = e4m3x2_to_f16x2(v.y >> 16);
-        w[8 * u + 4] = e4m3x2_to_f16x2(v.z);
-        w[8 * u + 5] = e4m3x2_to_f16x2(v.z >> 16);
-        w[8 * u + 6] = e4m3x2_to_f16x2(v.w);
-        w[8 * u + 7] = e4m3x2_to_f16x2(v.w >> 16);
-      }
+      const uint4 v = f.raw[g];
+      w[0] = e4m3x2_to_f16x2(v.x);
+      w[1] = e4m3x2_to_f16x2(v.x >> 16);
+      w[2] = e4m3x2_to_f16x2(v.y);
+      w[3] = e4m3x2_to_f16x2(v.y >> 16);
+      w[4] = e4m3x2_to_f16x2(v.z);
+      w[5] = e4m3x2_to_f16x2(v.z >> 16);
+      w[6] = e4m3x2_to_f16x2(v.w);
+      w[7] = e4m3x2_to_f16x2(v.w >> 16);
     } else {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) w[j] = 0u;
+      for (int j = 0; j < 8; ++j) w[j] = 0u;
     }
-#pragma unroll
-    for (int pl = 0; pl < 8; ++pl)
-      *reinterpret_cast<uint4*>(&S.X[half * 32 + blk * 8 + pl][r * 8]) =
-          make_uint4(w[4 * pl], w[4 * pl + 1], w[4 * pl + 2], w[4 * pl + 3]);
+    *reinterpret_cast<uint4*>(&S.X[slot][part * 16 + 2 * g][r * 8]) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(&S.X[slot][part * 16 + 2 * g + 1][r * 8]) = make_uint4(w[4], w[5], w[6], w[7]);
   }
   return f.kind != 0;
 }
 
-// One CTA runs chunks [c0, c1) of query b's rows with an online softmax; the
-// output accumulates in tensor memory across the chunks.
-//   warps 0-3 / 4-7: dequantize channels 0-255 / 256-511 of each chunk into X,
-//     fetching the next chunk's rows while the current one is on the tensor
-//     cores; then all eight run the chunk's softmax (warp w reads tensor-memory
-//     lane quarter w % 4, heads 32 (w / 4) .. +31);
-//   warp 8: barriers, tensor memory, the q' copy and the MMA issue.
-// Per chunk the MMA thread issues S over the first channel half as soon as it
-// is written, then the second; after the softmax, O over the first channel
-// half, whose completion frees that half of X for the next chunk, then the
-// second.  The softmax keeps, per head, a reference m (the running maximum,
-// raised only when a chunk exceeds it by more than kTau2, which then rescales
-// O and l in place), so probabilities stay below e^8.  The softmax runs in
+// The probabilities of one head (this lane) over its 32 rows of a chunk:
+// p = 2^(raw S * c2 - m2) rounded to f16, packed in pairs of rows into ph.
+// Returns whether some logit exceeds the reference by more than kTau2 (a head
+// with no reference yet, kNoRef, is exceeded by any row).
+__device__ __forceinline__ bool head_probs(const float (&sv)[32], float c2h, float m2ref, uint32_t (&ph)[16]) {
+  float tmax = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < 16; ++u) {
+    const float e0 = fmaf(sv[2 * u], c2h, -m2ref), e1 = fmaf(sv[2 * u + 1], c2h, -m2ref);  // -inf rows -> -inf
+    tmax = fmaxf(tmax, fmaxf(e0, e1));
+    const __half2 h2 = __floats2half2_rn(ptx::ex2(e0), ptx::ex2(e1));
+    ph[u] = *reinterpret_cast<const uint32_t*>(&h2);
+  }
+  return tmax > kTau2;
+}
+
+// P^T of slot `slot`: head hd, rows 32 ch .. 32 ch + 31 ([row/8][head][row%8]).
+__device__ __forceinline__ void store_probs(AttnSmem& S, int slot, int ch, int hd, const uint32_t (&ph)[16]) {
+#pragma unroll
+  for (int i4 = 0; i4 < 4; ++i4)
+    *reinterpret_cast<uint4*>(&S.P[slot][ch * 4 + i4][hd * 8]) =
+        make_uint4(ph[4 * i4], ph[4 * i4 + 1], ph[4 * i4 + 2], ph[4 * i4 + 3]);
+}
+
+__device__ __forceinline__ float sum_probs(const uint32_t (&ph)[16]) {
+  float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+  for (int u = 0; u < 16; ++u) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ph[u]));
+    s0 += f.x;
+    s1 += f.y;
+  }
+  return s0 + s1;
+}
+
+// One CTA runs chunks [c0, c0 + nc) of query b's rows (64 each) with an online
+// softmax; the output accumulates in tensor memory across the chunks.
+//   warps 0-7: thread t dequantizes channels 128 (t / 64) .. of chunk row t % 64
+//     into the chunk's slot, fetching the rows of the chunk two ahead meanwhile;
+//     in the softmax warp w owns heads 16 (w % 4) .. + 15 (lanes 0-15, the rows of
+//     an M = 64 accumulator) over the chunk rows 32 (w / 4) .. + 31;
+//   warp 8: barriers, tensor memory, the q' copy and the MMA issue, in pairs of
+//     chunks: S(2p), S(2p+1), O(2p), O(2p+1).
+// The softmax keeps, per head, a reference m (the running maximum, raised only
+// when a chunk exceeds it by more than kTau2, which then rescales O and l), so
+// probabilities stay below e^8.  Each chunk first forms P with the references it
+// has; one vote over the eight warps tells whether some head needs a new one,
+// and only then are the chunk's exact maxima exchanged.  The softmax runs in
 // log2 units: p = 2^(raw S * c2_h - m2_h).
 // kPartial: write the unnormalised O with (m, l) for the merge kernel instead
 // of the normalised output.
@@ -326,14 +341,17 @@ __global__ void __launch_bounds__(kAT, 1) k_attn(
 
   if (warp == kCtlWarp) {
     if (lane == 0) {
+      ptx::mbar_init(&S.q_load, 1);
       ptx::mbar_init(&S.q_full, 8);
-      ptx::mbar_init(&S.x_full[0], 4);
-      ptx::mbar_init(&S.x_full[1], 4);
-      ptx::mbar_init(&S.s_full, 1);
-      ptx::mbar_init(&S.red_full, 8);
-      ptx::mbar_init(&S.p_full, 8);
-      ptx::mbar_init(&S.x_free[0], 1);
-      ptx::mbar_init(&S.x_free[1], 1);
+      for (int s = 0; s < 2; ++s) {
+        ptx::mbar_init(&S.x_full[s][0], 4);
+        ptx::mbar_init(&S.x_full[s][1], 4);
+        ptx::mbar_init(&S.s_full[s], 1);
+        ptx::mbar_init(&S.p_full[s], 8);
+        ptx::mbar_init(&S.x_free[s], 1);
+      }
+      ptx::mbar_init(&S.vote_full, 8);
+      ptx::mbar_init(&S.max_full, 8);
       ptx::mbar_init(&S.drained, 1);
       S.abort_flag = 0;
       ptx::fence_mbar_init();
@@ -342,242 +360,295 @@ __global__ void __launch_bounds__(kAT, 1) k_attn(
     ptx::tmem_alloc(&S.tmem_base, kAttnTmemCols);
   }
   ptx::griddep_wait();  // q, the indices and the rows may come from the previous kernel
-  // q and the first chunk's indices load together; q is converted while the
-  // indices arrive, then the rows are requested
-  const int r = tid % kRows, half = (tid / kRows) & 1;
-  RowFetch rf;
+  // one bulk copy brings the query's bf16 rows into slot 1 of the (still unused) row
+  // buffer while the first two chunks' indices, then rows, are loaded; q' is
+  // converted afterwards
+  if (warp == kCtlWarp && lane == 0) {
+    ptx::mbar_arrive_expect_tx(&S.q_load, kHAtt * kDMain * 2);
+    ptx::bulk_g2s(&S.X[1][0][0], qg + (int64_t)b * kHAtt * kDMain, kHAtt * kDMain * 2, &S.q_load);
+  }
+  const int r = tid & (kRows - 1), part = (tid >> 6) & 3;  // gather: chunk row, channel quarter
+  RowFetch rf0, rf1;                                       // rows of the even / odd chunks
+  rf0.kind = rf1.kind = 0;
   const int64_t win_lo = ex.win_pos ? max(ex.win_lo[b], (int64_t)0) : 0;  // window rows below it are not seen
   if (warp < kCtlWarp) {
-    const int gr = c0 * kRows + r;
-    QFetch qf;
-    fetch_q(qf, qg, b, warp, lane);
-    const int64_t idx0 = fetch_index(topk, dense_n, k, b, gr);
-    stage_q<kEx>(S, qf, scale, warp, lane, ex, b);
-    ptx::fence_proxy_async_smem();
-    issue_row(rf, idx0, kv_codes, kv_scales, seq_stride, swa, n_swa, k, b, gr, half, ws, ex.win_pos, win_lo);
+    const int gr0 = c0 * kRows + r, gr1 = gr0 + kRows;
+    const int64_t idx0 = fetch_index(topk, dense_n, k, b, gr0);
+    const int64_t idx1 = nc > 1 ? fetch_index(topk, dense_n, k, b, gr1) : -1;
+    if (!dense_n) {  // the later chunks' indices wait in shared memory (no dependent global load per chunk)
+      const int n_sel = min(k - c0 * kRows, nc * kRows);
+      for (int i = tid; i < n_sel; i += kCtlWarp * 32) S.idx[i] = topk[(int64_t)b * k + c0 * kRows + i];
+    }
+    issue_row(rf0, idx0, kv_codes, kv_scales, seq_stride, swa, n_swa, k, b, gr0, part, ws, ex.win_pos, win_lo);
+    if (nc > 1)
+      issue_row(rf1, idx1, kv_codes, kv_scales, seq_stride, swa, n_swa, k, b, gr1, part, ws, ex.win_pos, win_lo);
   }
   ptx::tc_fence_before();
   __syncthreads();  // barriers initialised, tensor memory allocated
   ptx::tc_fence_after();
   const uint32_t tmem = S.tmem_base;
-  const uint32_t tS = tmem + 256u;  // S^T: 64 columns after the 256 of O^T
 
   if (warp == kCtlWarp) {
-    if (lane == 0) {
-      // ---------------------------------------------------------- MMA issue
-      bool good = ptx::mbar_wait(&S.q_full, 0, abort_flag, kAttnWaitBudget);
-      constexpr uint32_t idesc_s = ptx::idesc_f16(128, 64, 0);
-      constexpr uint32_t idesc_o = ptx::idesc_f16(128, 64, 0) | (1u << 15) | (1u << 16);  // M/N-major
-      for (int i = 0; i < nc && good; ++i) {
-        const uint32_t par = (uint32_t)(i & 1);
-        // S^T = X q'^T : M = 128 rows, N = 64 heads, K = 512 in two channel halves
+    // ------------------------------------------------------------ MMA issue
+    // The whole warp runs this loop (uniform control flow, uniform descriptors);
+    // one elected lane issues each MMA and commit.
+    bool good = ptx::mbar_wait_warp(&S.q_full, 0, abort_flag, kAttnWaitBudget);
+    constexpr uint32_t idesc_s = ptx::idesc_f16(64, 64, 0);                    // S = q' X^T: heads x rows
+    constexpr uint32_t idesc_o = ptx::idesc_f16(128, 64, 0) | (1u << 15);      // O^T += X^T P^T: A M-major
+    // descriptors of the first K step; later steps add their byte offset / 16 to the
+    // start-address field (every operand lies below 256 KB, so the field cannot carry)
+    const uint64_t dSa = ptx::smem_desc_noswizzle(&S.q[0][0], kQPlane * 2, 128);
+    uint64_t dSb[2], dOa[2], dOb[2];
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      dSb[s] = ptx::smem_desc_noswizzle(&S.X[s][0][0], kXPlane * 2, 128);  // K-major rows
+      dOa[s] = ptx::smem_desc_noswizzle(&S.X[s][0][0], 128, kXPlane * 2);  // M-major channels
+      dOb[s] = ptx::smem_desc_noswizzle(&S.P[s][0][0], kHAtt * 16, 128);   // K-major P^T
+    }
+    for (int p = 0; 2 * p < nc && good; ++p) {
+      const uint32_t ph = (uint32_t)(p & 1);
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {  // S(2p + s) = q' X^T : M = 64 heads, N = 64 rows, K = 512
+        if (2 * p + s >= nc || !good) break;
         for (int h2 = 0; h2 < 2 && good; ++h2) {
-          good = ptx::mbar_wait(&S.x_full[h2], par, abort_flag, kAttnWaitBudget);
+          good = ptx::mbar_wait_warp(&S.x_full[s][h2], ph, abort_flag, kAttnWaitBudget);
           if (!good) break;
           ptx::tc_fence_after();
 #pragma unroll 4
-          for (int ks = h2 * 16; ks < h2 * 16 + 16; ++ks) {
-            const uint64_t ad = ptx::smem_desc_noswizzle(&S.X[2 * ks][0], kRows * 16, 128);
-            const uint64_t bd = ptx::smem_desc_noswizzle(&S.q[2 * ks][0], kQPlane * 2, 128);
-            ptx::mma_f16_ss(tS, ad, bd, idesc_s, ks > 0 ? 1u : 0u);
-          }
+          for (int ks = h2 * 16; ks < h2 * 16 + 16; ++ks)  // q'[2 ks], X[s][2 ks]: ks * 2048 bytes on
+            ptx::mma_f16_ss_elect(tmem + kTmemS + 64u * s, dSa + (uint64_t)(ks * 128), dSb[s] + (uint64_t)(ks * 128),
+                                  idesc_s, ks > 0 ? 1u : 0u);
         }
-        if (!good) break;
-        ptx::mma_commit(&S.s_full);
-        // O^T += X^T P^T : four 128-channel M tiles, N = 64 heads, K = 128 rows
-        good = ptx::mbar_wait(&S.p_full, par, abort_flag, kAttnWaitBudget);
+        if (good) ptx::mma_commit_elect(&S.s_full[s]);
+      }
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {  // O^T += X^T P^T : four 128-channel M tiles, N = 64 heads, K = 64 rows
+        const int j = 2 * p + s;
+        if (j >= nc || !good) break;
+        good = ptx::mbar_wait_warp(&S.p_full[s], ph, abort_flag, kAttnWaitBudget);
         if (!good) break;
         ptx::tc_fence_after();
-        for (int h2 = 0; h2 < 2; ++h2) {
 #pragma unroll
-          for (int mt = 2 * h2; mt < 2 * h2 + 2; ++mt)
+        for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-            for (int ks = 0; ks < kRows / 16; ++ks) {
-              const uint64_t ad = ptx::smem_desc_noswizzle(&S.X[mt * 16][ks * 16 * 8], 128, kRows * 16);
-              const uint64_t bd = ptx::smem_desc_noswizzle(&S.P[0][ks * 16 * 8], 128, kRows * 16);
-              ptx::mma_f16_ss(tmem + (uint32_t)mt * 64u, ad, bd, idesc_o, (i > 0 || ks > 0) ? 1u : 0u);
-            }
-          ptx::mma_commit(&S.x_free[h2]);  // that channel half of X is no longer read
-        }
+          for (int ks = 0; ks < kRows / 16; ++ks)  // X[s][16 mt][128 ks]: mt * 16384 + ks * 256 bytes on;
+                                                  // P[s][2 ks]: ks * 2048 bytes on
+            ptx::mma_f16_ss_elect(tmem + (uint32_t)mt * 64u, dOa[s] + (uint64_t)(mt * 1024 + ks * 16),
+                                  dOb[s] + (uint64_t)(ks * 128), idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
+        ptx::mma_commit_elect(&S.x_free[s]);  // the slot's X and P are no longer read
       }
-      if (!good && !*abort_flag) {
-        *abort_flag = 1;
-        report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 23);
-      }
-      // every MMA issued so far has completed before tensor memory is freed
-      ptx::mma_commit(&S.drained);
-      volatile int keep_waiting = 0;
-      ptx::mbar_wait(&S.drained, 0, &keep_waiting, kAttnWaitBudget);
     }
+    if (!good && lane == 0 && !*abort_flag) {
+      *abort_flag = 1;
+      report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 23);
+    }
+    // every MMA issued so far has completed before tensor memory is freed
+    ptx::mma_commit_elect(&S.drained);
+    volatile int keep_waiting = 0;
+    ptx::mbar_wait_warp(&S.drained, 0, &keep_waiting, kAttnWaitBudget);
   } else {
-    // ------------------------------------------------------ rows and softmax
-    const int q4 = warp & 3, hh = warp >> 2;
-    const int rr = q4 * 32 + lane;  // row of this thread in the softmax (tensor-memory lane)
+    // ------------------------------------------------- rows, softmax, epilogue
+    const int q4 = warp & 3, ch = warp >> 2;  // softmax: lane quarter, column half (chunk rows 32 ch ..)
+    const bool owner = lane < 16;              // the lanes holding a head in an M = 64 accumulator
+    const int hd = (16 * q4 + lane) & (kHAtt - 1);  // this lane's head (meaningful for owners)
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-    float m2 = -INFINITY, l_run = 0.0f;  // this lane's head hh * 32 + lane: reference (log2 units), sum
-    S.m2w[warp][lane] = 0.0f;
+    float m2 = -INFINITY;  // this head's reference (log2 units); both column halves keep the same
+    float lsum = 0.0f;     // this head's rounded probabilities summed over this column half's rows
+    bool good = ptx::mbar_wait_warp(&S.q_load, 0, abort_flag, kAttnWaitBudget);
+    if (good) {
+      stage_q<kEx>(S, &S.X[1][0][0], scale, warp, lane, ex, b);
+    } else if (lane == 0 && !*abort_flag) {
+      *abort_flag = 1;
+      report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 25);
+    }
+    ptx::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(&S.q_full);
-    bool good = true;
-    for (int i = 0; i < nc && good; ++i) {
-      const uint32_t par = (uint32_t)(i & 1);
-      // the next chunk's index, in flight during the wait and the dequantization
-      const int gr_next = (c0 + i + 1) * kRows + r;
-      const int64_t idx_next = i + 1 < nc ? fetch_index(topk, dense_n, k, b, gr_next) : -1;
-      if (i > 0) {
-        good = ptx::mbar_wait_warp(&S.x_free[half], par ^ 1u, abort_flag, kAttnWaitBudget);
+    int nvote = 0, nslow = 0;  // uses of vote_full / max_full so far (the same in every warp)
+    for (int p = 0; 2 * p < nc && good; ++p) {
+      const uint32_t ph = (uint32_t)(p & 1);
+      // ---- rows of chunks 2p and 2p + 1 into slots 0 and 1
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        const int j = 2 * p + s;
+        if (j >= nc || !good) break;
+        RowFetch& f = s ? rf1 : rf0;
+        // the index of the chunk two ahead
+        const int gr2 = (c0 + j + 2) * kRows + r;
+        const int64_t idx2 = j + 2 >= nc || gr2 >= k ? -1
+                             : dense_n ? (gr2 < __ldg(dense_n + b) ? gr2 : -1)
+                                       : (int64_t)S.idx[(j + 2) * kRows + r];
+        if (j >= 2)  // O(j - 2) no longer reads the slot
+          good = ptx::mbar_wait_warp(&S.x_free[s], ph ^ 1u, abort_flag, kAttnWaitBudget);
+        else if (s == 1)  // slot 1 holds the bf16 q copy until every warp staged q'
+          good = ptx::mbar_wait_warp(&S.q_full, 0, abort_flag, kAttnWaitBudget);
         if (!good) break;
-      }
-      const bool valid = dequant_half_row(S, rf, r, half);
-      if (half == 0) S.valid[r] = valid ? 1 : 0;
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&S.x_full[half]);
-      if (i + 1 < nc)
-        issue_row(rf, idx_next, kv_codes, kv_scales, seq_stride, swa, n_swa, k, b, gr_next, half, ws, ex.win_pos,
-                  win_lo);
-
-      // ---- chunk softmax
-      good = ptx::mbar_wait_warp(&S.s_full, par, abort_flag, kAttnWaitBudget) &&
-             ptx::mbar_wait_warp(&S.x_full[0], par, abort_flag, kAttnWaitBudget) &&  // valid[] (acquire)
-             ptx::mbar_wait_warp(&S.q_full, 0, abort_flag, kAttnWaitBudget);         // c2 (acquire)
-      if (!good) break;
-      ptx::tc_fence_after();
-      float sv[32];
-      {
-        uint32_t a[32];
-        ptx::tmem_ld_32x32b_x32(tS + lane_base + (uint32_t)hh * 32u, a);
-        ptx::tmem_wait_ld();
-        const bool v = S.valid[rr] != 0;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) sv[j] = v ? __uint_as_float(a[j]) : -INFINITY;  // raw S
-        float t[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) t[j] = sv[j];
-        S.red[q4][hh * 32 + lane] = warp_reduce_scatter32(t, lane, MaxOp());
-      }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&S.red_full);
-      good = ptx::mbar_wait_warp(&S.red_full, par, abort_flag, kAttnWaitBudget);
-      if (!good) break;
-      const int h = hh * 32 + lane;
-      const float cm = fmaxf(fmaxf(S.red[0][h], S.red[1][h]), fmaxf(S.red[2][h], S.red[3][h])) * S.c2[h];
-      float alpha = 1.0f;
-      if (cm > m2 + kTau2) {  // also the first chunk with a row of this head
-        alpha = m2 == -INFINITY ? 0.0f : ptx::ex2(m2 - cm);
-        m2 = cm;
-      }
-      const bool moved = __any_sync(0xffffffffu, alpha != 1.0f);
-      const bool rescale = i > 0 && moved;
-      if (moved) {  // this warp's copy of its heads' references
-        S.m2w[warp][lane] = m2 == -INFINITY ? 0.0f : m2;
+        const bool valid = dequant_quarter_row(S, f, s, r, part);
+        if (part == 0) {
+          const uint32_t vm = __ballot_sync(0xffffffffu, valid);
+          if (lane == 0) S.vmask[s][warp & 1] = vm;
+        }
+        ptx::fence_proxy_async_smem();
         __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&S.x_full[s][part >> 1]);
+        if (j + 2 < nc)
+          issue_row(f, idx2, kv_codes, kv_scales, seq_stride, swa, n_swa, k, b, gr2, part, ws, ex.win_pos, win_lo);
       }
-      if (i > 0) {  // P and O of the previous chunk are no longer read
-        good = ptx::mbar_wait_warp(&S.x_free[1], par ^ 1u, abort_flag, kAttnWaitBudget);
+      // ---- softmax of chunks 2p and 2p + 1
+      for (int s = 0; s < 2 && good; ++s) {
+        const int j = 2 * p + s;
+        if (j >= nc) break;
+        good = ptx::mbar_wait_warp(&S.s_full[s], ph, abort_flag, kAttnWaitBudget) &&
+               ptx::mbar_wait_warp(&S.x_full[s][0], ph, abort_flag, kAttnWaitBudget);  // vmask (acquire)
         if (!good) break;
         ptx::tc_fence_after();
-      }
-      {
-        float pr[32];  // the probabilities as rounded to f16, for the sums
-        uint32_t ph[16];
-        const float4* m2v = reinterpret_cast<const float4*>(S.m2w[warp]);
-        const float4* c2v = reinterpret_cast<const float4*>(&S.c2[hh * 32]);
-#pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          const float4 mq = m2v[j / 4], cq = c2v[j / 4];
-          const float mm[4] = {mq.x, mq.y, mq.z, mq.w}, cc4[4] = {cq.x, cq.y, cq.z, cq.w};
-#pragma unroll
-          for (int t = 0; t < 4; ++t) pr[j + t] = ptx::ex2(fmaf(sv[j + t], cc4[t], -mm[t]));  // -inf rows -> 0
-        }
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const __half2 h2 = __floats2half2_rn(pr[j], pr[j + 1]);
-          ph[j / 2] = *reinterpret_cast<const uint32_t*>(&h2);
-          const float2 back = __half22float2(h2);
-          pr[j] = back.x;
-          pr[j + 1] = back.y;
-        }
-#pragma unroll
-        for (int i4 = 0; i4 < 4; ++i4)
-          *reinterpret_cast<uint4*>(&S.P[hh * 4 + i4][rr * 8]) =
-              make_uint4(ph[4 * i4], ph[4 * i4 + 1], ph[4 * i4 + 2], ph[4 * i4 + 3]);
-        S.red2[q4][h] = warp_reduce_scatter32(pr, lane, AddOp());
-      }
-      if (rescale) {  // O^T columns of this warp's heads, its lane quarter, all four M tiles
-#pragma unroll 1
-        for (int mt = 0; mt < 4; ++mt) {
+        const uint32_t taS = tmem + lane_base + kTmemS + 64u * (uint32_t)s + 32u * (uint32_t)ch;
+        const uint32_t vm = S.vmask[s][ch];  // chunk rows 32 ch .. 32 ch + 31 that exist
+        const float c2h = S.c2[hd];
+        float sv[32];
+        {
           uint32_t a[32];
-          const uint32_t ta = tmem + lane_base + (uint32_t)mt * 64u + (uint32_t)hh * 32u;
-          ptx::tmem_ld_32x32b_x32(ta, a);
+          ptx::tmem_ld_32x32b_x32(taS, a);
           ptx::tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            a[j] = __float_as_uint(__uint_as_float(a[j]) * __shfl_sync(0xffffffffu, alpha, j));
-          ptx::tmem_st_32x32b_x32(ta, a);
+          for (int i = 0; i < 32; ++i) sv[i] = ((vm >> i) & 1u) ? __uint_as_float(a[i]) : -INFINITY;  // raw S
         }
-        ptx::tmem_wait_st();
+        // P with the references so far: stands unless some head needs a new one.  The
+        // P^T slot is free: S(j) was issued after O(j - 2), and its commit covers that
+        uint32_t ph16[16];
+        const bool over = head_probs(sv, c2h, m2 == -INFINITY ? kNoRef : m2, ph16) && owner;
+        if (owner) store_probs(S, s, ch, hd, ph16);
+        const bool wover = __any_sync(0xffffffffu, over);
+        if (lane == 0) S.vote[nvote & 1][warp] = wover ? 1 : 0;
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&S.vote_full);
+        good = ptx::mbar_wait_warp(&S.vote_full, (uint32_t)(nvote & 1), abort_flag, kAttnWaitBudget);
+        if (!good) break;
+        bool slow = false;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) slow |= S.vote[nvote & 1][w] != 0;
+        ++nvote;
+        float alpha = 1.0f;  // this head's factor for its sums and O
+        if (slow) {
+          // the chunk's exact maxima: this column half's rows, then the other's
+          float cm = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) cm = fmaxf(cm, sv[i]);
+          if (owner) S.mx[ch][hd] = cm * c2h;  // -inf stays -inf (c2 > 0)
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&S.max_full);
+          good = ptx::mbar_wait_warp(&S.max_full, (uint32_t)(nslow & 1), abort_flag, kAttnWaitBudget);
+          if (!good) break;
+          ++nslow;
+          const float cmax = fmaxf(S.mx[0][hd], S.mx[1][hd]);
+          if (cmax > m2 + kTau2) {  // also the first chunk with a row of this head
+            alpha = m2 == -INFINITY ? 0.0f : ptx::ex2(m2 - cmax);
+            m2 = cmax;
+          }
+          (void)head_probs(sv, c2h, m2 == -INFINITY ? kNoRef : m2, ph16);
+          if (owner) store_probs(S, s, ch, hd, ph16);
+          if (j > 0) {  // O^T holds earlier chunks: scale the columns of the heads that moved
+            if (owner && ch == 0) S.alpha[hd] = alpha;
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&S.max_full);
+            good = ptx::mbar_wait_warp(&S.max_full, (uint32_t)(nslow & 1), abort_flag, kAttnWaitBudget) &&
+                   ptx::mbar_wait_warp(&S.x_free[s ^ 1], (uint32_t)(((j - 1) >> 1) & 1), abort_flag,
+                                       kAttnWaitBudget);  // O(j - 1) complete
+            if (!good) break;
+            ++nslow;
+            ptx::tc_fence_after();
+            // this warp's share: O^T lanes of quarter q4 (channels), columns of heads 32 ch ..
+            const float a32 = S.alpha[32 * ch + lane];
+            if (__any_sync(0xffffffffu, a32 != 1.0f)) {
+#pragma unroll 1
+              for (int mt = 0; mt < 4; ++mt) {
+                uint32_t a[32];
+                const uint32_t ta = tmem + lane_base + (uint32_t)mt * 64u + 32u * (uint32_t)ch;
+                ptx::tmem_ld_32x32b_x32(ta, a);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj)
+                  a[jj] = __float_as_uint(__uint_as_float(a[jj]) * __shfl_sync(0xffffffffu, a32, jj));
+                ptx::tmem_st_32x32b_x32(ta, a);
+              }
+              ptx::tmem_wait_st();
+            }
+          }
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&S.p_full[s]);  // the MMA thread waits; the rows go on
+        lsum = fmaf(alpha, lsum, sum_probs(ph16));
       }
-      ptx::fence_proxy_async_smem();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&S.p_full);
-      good = ptx::mbar_wait_warp(&S.p_full, par, abort_flag, kAttnWaitBudget);
-      if (!good) break;
-      l_run = fmaf(alpha, l_run, ((S.red2[0][h] + S.red2[1][h]) + S.red2[2][h]) + S.red2[3][h]);
     }
-    if (good)
-      good = ptx::mbar_wait_warp(&S.x_free[1], (uint32_t)((nc - 1) & 1), abort_flag, kAttnWaitBudget);
+    // ---- the softmax denominators (both column halves), the lse / partials, then
+    // the output: O^T rows = channels of this lane quarter, 32 heads per warp; for
+    // each head the warp stores 32 consecutive channels.  The sink joins the
+    // denominator here (split queries: in the merge); with RoPE the last 64
+    // channels turn back by -qpos (pairs are adjacent lanes; the turn is linear,
+    // so partials may take it before the merge).
+    if (good) {
+      if (owner) S.lsum[ch][hd] = lsum;
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&S.vote_full);
+      good = ptx::mbar_wait_warp(&S.vote_full, (uint32_t)(nvote & 1), abort_flag, kAttnWaitBudget);
+      ++nvote;
+    }
+    if (good) {
+      if (owner && ch == 0) {
+        const float l_run = S.lsum[0][hd] + S.lsum[1][hd];
+        const float m_nat = m2 / kLog2e;  // reference in natural units
+        float den = l_run;
+        if (!kPartial && kEx && ex.sink) den += ptx::ex2(ex.sink[hd] * kLog2e - m2);  // 2^(z2 - m2); m2 = -inf -> inf
+        S.inv[hd] = kPartial ? 1.0f : (den > 0.0f ? 1.0f / den : 0.0f);
+        if (kPartial) {
+          part_ml[((int64_t)b * gridDim.x + split) * kHAtt + hd] = make_float2(m_nat, l_run);
+        } else if (lse) {
+          if (kEx && ex.sink) {
+            const float z = ex.sink[hd], mxv = fmaxf(m_nat, z);
+            lse[b * kHAtt + hd] = mxv + logf(l_run * expf(m_nat - mxv) + expf(z - mxv));
+          } else {
+            lse[b * kHAtt + hd] = l_run > 0.0f ? m_nat + logf(l_run) : -INFINITY;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&S.vote_full);
+      good = ptx::mbar_wait_warp(&S.vote_full, (uint32_t)(nvote & 1), abort_flag, kAttnWaitBudget) &&
+             ptx::mbar_wait_warp(&S.x_free[(nc - 1) & 1], (uint32_t)(((nc - 1) >> 1) & 1), abort_flag,
+                                 kAttnWaitBudget);  // the last O MMAs (their commit covers the others)
+      ++nvote;
+    }
     if (!good && lane == 0 && !*abort_flag) {
       *abort_flag = 1;
       report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 24);
     }
-    // ---- epilogue: O^T rows = channels of this lane quarter, 32 heads per warp;
-    // for each head the warp stores 32 consecutive channels.  The sink joins
-    // the denominator here (split queries: in the merge); with RoPE the last
-    // 64 channels turn back by -qpos (pairs are adjacent lanes; the turn is
-    // linear, so partials may take it before the merge).
     if (good) {
       ptx::tc_fence_after();
-      const int h = hh * 32 + lane;
-      const float m_nat = m2 / kLog2e;  // reference in natural units
-      float den = l_run;
-      if (!kPartial && kEx && ex.sink) den += ptx::ex2(ex.sink[h] * kLog2e - m2);  // 2^(z2 - m2); m2 = -inf -> inf
-      const float inv = kPartial ? 1.0f : (den > 0.0f ? 1.0f / den : 0.0f);
-      if (q4 == 0) {
-        if (kPartial) {
-          part_ml[((int64_t)b * gridDim.x + split) * kHAtt + h] = make_float2(m_nat, l_run);
-        } else if (lse) {
-          if (kEx && ex.sink) {
-            const float z = ex.sink[h], mx = fmaxf(m_nat, z);
-            lse[b * kHAtt + h] = mx + logf(l_run * expf(m_nat - mx) + expf(z - mx));
-          } else {
-            lse[b * kHAtt + h] = l_run > 0.0f ? m_nat + logf(l_run) : -INFINITY;
-          }
-        }
-      }
+      const int rr = q4 * 32 + lane;  // channel of this lane within a 128-channel tile
+      const float inv = S.inv[32 * ch + lane];  // head 32 ch + lane; broadcast per column below
       float* ob = kPartial ? part_o + ((int64_t)b * gridDim.x + split) * kHAtt * kDMain
                            : out + (int64_t)b * kHAtt * kDMain;
       float tc = 1.0f, ts = 0.0f;  // cos / sin of this lane's pair angle (channel c, c ^ 1)
-      if (kEx && ex.rope && 3 * kRows + rr >= kRopeFirst)
-        rope_cos_sin(ex.th.t[(3 * kRows + rr - kRopeFirst) / 2], (double)ex.qpos[b], tc, ts);
+      if (kEx && ex.rope && 3 * 128 + rr >= kRopeFirst)
+        rope_cos_sin(ex.th.t[(3 * 128 + rr - kRopeFirst) / 2], (double)ex.qpos[b], tc, ts);
       if (lane & 1) ts = -ts;  // turning back by -t: x' = x c + y s, y' = y c - x s
 #pragma unroll 1
       for (int mt = 0; mt < 4; ++mt) {
         uint32_t a[32];
-        ptx::tmem_ld_32x32b_x32(tmem + lane_base + (uint32_t)mt * 64u + (uint32_t)hh * 32u, a);
+        ptx::tmem_ld_32x32b_x32(tmem + lane_base + (uint32_t)mt * 64u + 32u * (uint32_t)ch, a);
         ptx::tmem_wait_ld();
-        const int c = mt * kRows + rr;
+        const int c = mt * 128 + rr;
         const bool turn = kEx && ex.rope && mt == 3 && q4 >= 2;  // warp-uniform: channels 448..511
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          float v = __uint_as_float(a[j]) * __shfl_sync(0xffffffffu, inv, j);
+        for (int jj = 0; jj < 32; ++jj) {
+          float v = __uint_as_float(a[jj]) * __shfl_sync(0xffffffffu, inv, jj);
           if (turn) {
             const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
             v = fmaf(v, tc, partner * ts);
           }
-          ob[(hh * 32 + j) * kDMain + c] = v;
+          ob[(32 * ch + jj) * kDMain + c] = v;
         }
       }
     }
@@ -705,7 +776,7 @@ csa2_status attn_run(const csa2_kv_planes* kv, int32_t B, const int32_t* topk, c
   auto kern = partial ? (extras ? k_attn<true, true> : k_attn<true, false>)
                       : (extras ? k_attn<false, true> : k_attn<false, false>);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return CSA2_ERR_CUDA;
+    return launch_status();
   {
     KernelTimer timer(partial ? "k_attn_part" : "k_attn", st);
     launch_pdl(kern, dim3(plan.nsplit, B), dim3(kAT), (size_t)smem, st, kv->kv_codes, kv->kv_scales, kv->seq_stride,

@@ -6,6 +6,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
 
 #include "csa2.h"
 
@@ -117,9 +119,13 @@ inline cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t
   return cudaLaunchKernelEx(&cfg, k, static_cast<KArgs>(args)...);
 }
 
+// Status of the launches just issued.  With CSA2_DEBUG set in the environment the
+// CUDA error string goes to stderr as well.
 inline csa2_status launch_status() {
   cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
+  if (e == cudaSuccess) return CSA2_OK;
+  if (getenv("CSA2_DEBUG")) fprintf(stderr, "csa2: launch failed: %s\n", cudaGetErrorString(e));
+  return CSA2_ERR_CUDA;
 }
 inline bool planes_ok(const csa2_kv_planes* kv) {
   return kv && kv->kv_codes && kv->kv_scales && kv->ix_codes && kv->ix_scales &&

@@ -238,6 +238,29 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uin
       : "memory");
 }
 
+// The same MMA issued from a whole warp in uniform control flow: every lane
+// executes the instruction stream and elect.sync picks the one lane (always the
+// same: the lowest) that issues.  A warp that branches to lane 0 for the issue
+// loses most of its issue slots to busy warps on the same scheduler (measured
+// on sm_103a: M128 N64 K16 every ~150 cycles with one ALU-bound neighbour
+// warp, against ~61 in this form).
+__device__ __forceinline__ void mma_f16_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// tcgen05.commit from the lane elect.sync picks (the lane that issued the MMAs above)
+__device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
 // D[tmem] (+)= (A[tmem] * 2^sfA) * (B[smem desc] * 2^sfB)^T, block-scaled
 // kind::mxf8f6f4 with one UE8M0 scale per row and per 32-element K step
 // (scale_vec::1X).  Tensor-memory layouts (measured on sm_103a):
