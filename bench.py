@@ -734,12 +734,39 @@ def run_prefill_index(dev, st, calls: int, warmup: int):
     csa2.timing_enable(False)
     scored = int(n_vis.astype(np.int64).sum())
     flop = scored * 32 * 128 * 2  # q_h . K_j for 32 heads of 128
+    # the same call with MXFP4 indexer queries (csa2_quantize_index_query, as V4 quantizes
+    # the indexer q): the scan needs only the hi half of each query then
+    with torch.cuda.stream(st):
+        q4 = torch.empty_like(q)
+    csa2.quantize_index_query(q, Q * 32, q4, stream=st)
+
+    def call4():
+        csa2.index_topk_prefill(planes, 0, Q, nv, N, q4, w, K_TOP, topk, ws, stream=st)
+
+    for _ in range(warmup):
+        call4()
+    torch.cuda.synchronize()
+    a.record(st)
+    for _ in range(calls):
+        call4()
+    b.record(st)
+    torch.cuda.synchronize()
+    ms4 = a.elapsed_time(b) / calls
+    csa2.timing_enable(True)
+    call4()
+    torch.cuda.synchronize()
+    kt4 = csa2.kernel_times()
+    csa2.timing_enable(False)
+    assert csa2.check(ws, st)[0] == 0
     return {
         "workload": PF_WORKLOAD, "calls": calls, "ms_per_call": round(ms, 4),
         "queries_per_s": round(Q / (ms * 1e-3), 1), "entries_scored_per_call": scored,
         "entries_scored_per_s": round(scored / (ms * 1e-3), 1),
         "score_tflops": round(flop / (ms * 1e-3) / 1e12, 1),
         "kernels_ms_per_launch": {k: round(t / n, 4) for k, (n, t) in sorted(kt.items())},
+        "mxfp4_query": {"ms_per_call": round(ms4, 4), "queries_per_s": round(Q / (ms4 * 1e-3), 1),
+                        "score_tflops": round(flop / (ms4 * 1e-3) / 1e12, 1),
+                        "kernels_ms_per_launch": {k: round(t / n, 4) for k, (n, t) in sorted(kt4.items())}},
     }
 
 

@@ -219,6 +219,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   // q^I -> E4M3 halves hi, lo with one E8M0 scale per head and 32-element
   // block; lane l holds elements 4l..4l+3 (block l/8)
+  bool lo_nonzero = false;
   for (int h = warp; h < kHIdx; h += kWarps) {
     const uint16_t* qh = p.q + ((int64_t)b * kHIdx + h) * kDIdx;
     const uint2 raw = *reinterpret_cast<const uint2*>(qh + 4 * lane);
@@ -243,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int off = ((lane >> 2) & 1) * 1024 + (h >> 3) * 128 + (h & 7) * 16 + 4 * (lane & 3);
     *reinterpret_cast<uint32_t*>(&S.qB[lane >> 3][off]) = hi4;
     *reinterpret_cast<uint32_t*>(&S.qB[lane >> 3][off + 512]) = lo4;
+    lo_nonzero |= lo4 != 0u;
     const uint32_t byte = (uint32_t)(sb + 127);
     uint32_t word = 0;
 #pragma unroll
@@ -257,7 +259,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   ptx::fence_proxy_async_smem();
   ptx::tc_fence_before();
-  __syncthreads();
+  // A query whose every lo half is zero (an MXFP4 query: E2M1 codes under a
+  // power-of-two scale fit E4M3 exactly) needs only the hi rows: the MMAs run
+  // with N = 32 and the epilogue reads half the columns.
+  const bool hi_only = __syncthreads_or(lo_nonzero ? 1 : 0) == 0;
   ptx::tc_fence_after();
   const uint32_t tmem = S.tmem_base;
 
@@ -361,7 +366,8 @@ __global__ void __launch_bounds__(kThreads, 2)
           const uint64_t ads = ad0 + (uint64_t)(s * (kTile * 128 / 16));
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            const uint32_t idesc = ptx::idesc_block_scaled(128, 64, ptx::kFmtE2M1, ptx::kFmtE4M3, ks, ks);
+            const uint32_t idesc =
+                ptx::idesc_block_scaled(128, hi_only ? 32 : 64, ptx::kFmtE2M1, ptx::kFmtE4M3, ks, ks);
             ptx::mma_mxf8f6f4_ss(d_t, ads + (uint64_t)(2 * ks), bd[ks], idesc, sfa_t, sfb_t, ks > 0 ? 1u : 0u);
           }
           ptx::mma_commit(&S.tile_done[s]);
@@ -424,25 +430,40 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t d_addr = lane_addr + kDCol0 + (uint32_t)a * 64u;
         ptx::tmem_ld_32x32b_x16(d_addr, hi);
         ptx::tmem_ld_32x32b_x16(d_addr + 16u, hi + 16);
-        ptx::tmem_ld_32x32b_x16(d_addr + 32u, lo);
-        ptx::tmem_ld_32x32b_x16(d_addr + 48u, lo + 16);
+        if (!hi_only) {
+          ptx::tmem_ld_32x32b_x16(d_addr + 32u, lo);
+          ptx::tmem_ld_32x32b_x16(d_addr + 48u, lo + 16);
+        }
         ptx::tmem_wait_ld();
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&S.d_free[a]);
         // sum_h w_h max(dot_h, 0) on head pairs, two accumulators
         float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
+        if (hi_only) {
 #pragma unroll
-        for (int h4 = 0; h4 < 8; ++h4) {
-          const float4 wv = make_float4(wr[4 * h4], wr[4 * h4 + 1], wr[4 * h4 + 2], wr[4 * h4 + 3]);
-          float2 x01 = add_f32x2(make_float2(__uint_as_float(hi[4 * h4]), __uint_as_float(hi[4 * h4 + 1])),
-                                 make_float2(__uint_as_float(lo[4 * h4]), __uint_as_float(lo[4 * h4 + 1])));
-          float2 x23 = add_f32x2(make_float2(__uint_as_float(hi[4 * h4 + 2]), __uint_as_float(hi[4 * h4 + 3])),
-                                 make_float2(__uint_as_float(lo[4 * h4 + 2]), __uint_as_float(lo[4 * h4 + 3])));
-          x01 = make_float2(fmaxf(x01.x, 0.0f), fmaxf(x01.y, 0.0f));
-          x23 = make_float2(fmaxf(x23.x, 0.0f), fmaxf(x23.y, 0.0f));
-          acc0 = fma_f32x2(make_float2(wv.x, wv.y), x01, acc0);
-          acc1 = fma_f32x2(make_float2(wv.z, wv.w), x23, acc1);
+          for (int h4 = 0; h4 < 8; ++h4) {
+            const float4 wv = make_float4(wr[4 * h4], wr[4 * h4 + 1], wr[4 * h4 + 2], wr[4 * h4 + 3]);
+            const float2 x01 = make_float2(fmaxf(__uint_as_float(hi[4 * h4]), 0.0f),
+                                           fmaxf(__uint_as_float(hi[4 * h4 + 1]), 0.0f));
+            const float2 x23 = make_float2(fmaxf(__uint_as_float(hi[4 * h4 + 2]), 0.0f),
+                                           fmaxf(__uint_as_float(hi[4 * h4 + 3]), 0.0f));
+            acc0 = fma_f32x2(make_float2(wv.x, wv.y), x01, acc0);
+            acc1 = fma_f32x2(make_float2(wv.z, wv.w), x23, acc1);
+          }
+        } else {
+#pragma unroll
+          for (int h4 = 0; h4 < 8; ++h4) {
+            const float4 wv = make_float4(wr[4 * h4], wr[4 * h4 + 1], wr[4 * h4 + 2], wr[4 * h4 + 3]);
+            float2 x01 = add_f32x2(make_float2(__uint_as_float(hi[4 * h4]), __uint_as_float(hi[4 * h4 + 1])),
+                                   make_float2(__uint_as_float(lo[4 * h4]), __uint_as_float(lo[4 * h4 + 1])));
+            float2 x23 = add_f32x2(make_float2(__uint_as_float(hi[4 * h4 + 2]), __uint_as_float(hi[4 * h4 + 3])),
+                                   make_float2(__uint_as_float(lo[4 * h4 + 2]), __uint_as_float(lo[4 * h4 + 3])));
+            x01 = make_float2(fmaxf(x01.x, 0.0f), fmaxf(x01.y, 0.0f));
+            x23 = make_float2(fmaxf(x23.x, 0.0f), fmaxf(x23.y, 0.0f));
+            acc0 = fma_f32x2(make_float2(wv.x, wv.y), x01, acc0);
+            acc1 = fma_f32x2(make_float2(wv.z, wv.w), x23, acc1);
+          }
         }
         const float sum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
 

@@ -211,3 +211,26 @@ def test_prefill_indexer_batches(cache, oracle_mod):
     for i in range(Q):
         s = oracle_mod.index_scores(ixc, ixs, q[i], w[i], n=int(n_vis[i]))
         check_topk(topk[i], s, 512, what=f"prefill-batched[{i}]")
+
+
+def test_prefill_indexer_mxfp4_queries(cache, oracle_mod):
+    """Half of the queries are MXFP4 (the oracle's quantize-then-decode of their bf16 rows),
+    half plain bf16, in one launch: the scan takes the hi-only path (N = 32) for the former
+    and the hi/lo path for the latter; every query's top-512 matches the oracle's scores of
+    the query it was given."""
+    import synth
+
+    c, _, _ = cache
+    seq, Q = 1, 48
+    q, w = W.index_query(6, 0, Q)
+    codes, scales = oracle_mod.quantize_index(synth.bf16_to_f32(q[:Q // 2]).reshape(-1, 128))
+    vals = oracle_mod.dequant_index(codes, scales).astype(np.float32)
+    assert np.array_equal(vals.view(np.uint32) & 0xFFFF, np.zeros_like(vals.view(np.uint32)))  # exact in bf16
+    q = q.copy()
+    q[:Q // 2] = (vals.view(np.uint32) >> 16).astype(np.uint16).reshape(Q // 2, 32, 128)
+    n_vis = np.random.default_rng(4).integers(1, 4134, Q).astype(np.int32)
+    topk = _prefill(c.planes, seq, q, w, n_vis, c.n_max)
+    _, _, ixc, ixs = c.oracle_slot(seq)
+    for i in range(Q):
+        s = oracle_mod.index_scores(ixc, ixs, q[i], w[i], n=int(n_vis[i]))
+        check_topk(topk[i], s, 512, what=f"prefill-mxfp4[{i}]")
