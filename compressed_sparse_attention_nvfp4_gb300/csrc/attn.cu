@@ -118,9 +118,14 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
 // of the [c/8][head][c%8] image; the rotated pairs sit in lanes 24-31.
 // q' is converted from a shared-memory copy of the query's bf16 rows ([64][512],
 // brought in by one bulk copy), one head at a time.
+// The f16 result goes to `qrot`, a [c/8][head][c%8] image whose head slots are
+// rotated by the chunk (head h of chunk c at slot (h + c) mod 64): the lanes of
+// a store write 32 different chunks, 1024 bytes apart, and without the rotation
+// all of them would hit the same shared-memory banks.  copy_q then writes the
+// unrotated image the MMAs read.
 template <bool kEx>
-__device__ __forceinline__ void stage_q(AttnSmem& S, const uint16_t* qs, float scale, int warp, int lane,
-                                        const AttnExtras& ex, int b) {
+__device__ __forceinline__ void stage_q(AttnSmem& S, const uint16_t* qs, uint16_t* qrot, float scale, int warp,
+                                        int lane, const AttnExtras& ex, int b) {
   // per lane: the RMSNorm weights of its 16 channels, the cos / sin of its 4 pairs
   float wq[16], rc[4], rs[4];
   const bool norm = kEx && ex.qnorm_w != nullptr;
@@ -170,8 +175,8 @@ __device__ __forceinline__ void stage_q(AttnSmem& S, const uint16_t* qs, float s
     float mx = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) mx = fmaxf(mx, fabsf(v[i]));
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    // non-negative floats order as their bit patterns: one warp reduction instruction
+    mx = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mx)));
     const int sig = mx > 0.0f ? min(max(floor_log2_f32(mx) - 14, -126), 126) : 0;
     const float inv = exp2i_f32(-sig);  // exact power of two: q 2^-sig rounds only in the f16 conversion
     const int h = warp * 8 + u;
@@ -183,9 +188,22 @@ __device__ __forceinline__ void stage_q(AttnSmem& S, const uint16_t* qs, float s
         const __half2 h2 = __floats2half2_rn(v[8 * i + 2 * j] * inv, v[8 * i + 2 * j + 1] * inv);
         o[j] = *reinterpret_cast<const uint32_t*>(&h2);
       }
-      *reinterpret_cast<uint4*>(&S.q[i * 32 + lane][h * 8]) = make_uint4(o[0], o[1], o[2], o[3]);
+      const int c = i * 32 + lane;
+      *reinterpret_cast<uint4*>(qrot + c * kQPlane + ((h + c) & (kHAtt - 1)) * 8) = make_uint4(o[0], o[1], o[2], o[3]);
     }
     if (lane == 0) S.c2[h] = kLog2e * scale * exp2i_f32(sig);
+  }
+}
+
+// q' from the rotated image into S.q: thread t moves head t % 64 of chunks
+// 4 i + t / 64, so a warp reads and writes 512 consecutive bytes of one chunk.
+__device__ __forceinline__ void copy_q(AttnSmem& S, const uint16_t* rot, int tid) {
+  const int h = tid & (kHAtt - 1);
+#pragma unroll 4
+  for (int i = 0; i < kDMain / 8 / 4; ++i) {
+    const int c = 4 * i + (tid >> 6);
+    *reinterpret_cast<uint4*>(&S.q[c][h * 8]) =
+        *reinterpret_cast<const uint4*>(rot + c * kQPlane + ((h + c) & (kHAtt - 1)) * 8);
   }
 }
 
@@ -454,13 +472,16 @@ __global__ void __launch_bounds__(kAT, 1) k_attn(
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
     float m2 = -INFINITY;  // this head's reference (log2 units); both column halves keep the same
     float lsum = 0.0f;     // this head's rounded probabilities summed over this column half's rows
+    // q' through the rotated image in slot 0 (free until the first chunk's rows)
     bool good = ptx::mbar_wait_warp(&S.q_load, 0, abort_flag, kAttnWaitBudget);
     if (good) {
-      stage_q<kEx>(S, &S.X[1][0][0], scale, warp, lane, ex, b);
+      stage_q<kEx>(S, &S.X[1][0][0], &S.X[0][0][0], scale, warp, lane, ex, b);
     } else if (lane == 0 && !*abort_flag) {
       *abort_flag = 1;
       report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 25);
     }
+    asm volatile("bar.sync 1, 256;" ::: "memory");  // the eight row warps: every rotated chunk written
+    if (good) copy_q(S, &S.X[0][0][0], tid);
     ptx::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(&S.q_full);
@@ -480,7 +501,7 @@ __global__ void __launch_bounds__(kAT, 1) k_attn(
                                        : (int64_t)S.idx[(j + 2) * kRows + r];
         if (j >= 2)  // O(j - 2) no longer reads the slot
           good = ptx::mbar_wait_warp(&S.x_free[s], ph ^ 1u, abort_flag, kAttnWaitBudget);
-        else if (s == 1)  // slot 1 holds the bf16 q copy until every warp staged q'
+        else  // slot 1 holds the bf16 q copy, slot 0 the rotated q', until every warp staged q'
           good = ptx::mbar_wait_warp(&S.q_full, 0, abort_flag, kAttnWaitBudget);
         if (!good) break;
         const bool valid = dequant_quarter_row(S, f, s, r, part);
