@@ -12,13 +12,15 @@
 //      E2M1 x E4M3 has at most 6 significant bits), interleaved
 //      X[c/8][row][c%8]: K-major for S, M-major for O;
 //   2. S[64 heads x 64 rows] = q' X^T (heads as M, so each softmax thread owns
-//      one head and its rows lie in its own registers);
+//      one head and its rows lie in its own registers), as two accumulators over
+//      the channel halves that the softmax adds;
 //   3. online softmax per head, P rounded to f16 once, l = sums of the rounded P;
 //   4. O^T[512 x 64] += X^T P^T (four 128-channel M tiles).
 // Two chunk slots (rows, S accumulators, probabilities) let the tensor cores
-// compute S of one chunk while the softmax of the other runs; the MMAs go in
-// pairs S(2p), S(2p+1), O(2p), O(2p+1), so the dequantization of a slot overlaps
-// the MMAs of the other.  One CTA per query keeps O in tensor memory across all
+// compute S of one chunk while the softmax of the other runs.  Small MMAs are
+// bound by their issue (one thread issues about one per 44 cycles, fewer when
+// busy warps share its scheduler), so four warps, one per scheduler, issue them:
+// the two S halves and the two channel halves of O.  One CTA per query keeps O in tensor memory across all
 // its chunks, so no partial result leaves the SM.  When the batch is too small
 // to fill the GPU a query's chunks are split over a few CTAs, which write
 // (max, l, O) partials that a merge kernel combines by log-sum-exp.
@@ -31,8 +33,14 @@ namespace csa2 {
 namespace {
 
 constexpr int kRows = 64;   // rows per chunk: the N of the S MMA, the K of the O MMAs
-constexpr int kAT = 288;    // warps 0-7: a quarter row each in the gather, the softmax, the epilogue; warp 8: MMAs
-constexpr int kCtlWarp = 8;
+// warps 0-7: a quarter row each in the gather and dequantization, then the epilogue;
+// warps 8-11: the softmax (one warp per tensor-memory lane quarter); warps 12 and 13:
+// the S MMAs over channels 0-255 / 256-511 (warp 12 also sets up the barriers, tensor
+// memory and the q copy); warps 14 and 15: the O MMAs of channels 0-255 / 256-511
+constexpr int kGatherWarps = 8;
+constexpr int kCtlWarp = 12;
+constexpr int kOWarp = 14;
+constexpr int kAT = 16 * 32;
 constexpr float kLog2e = 1.4426950408889634f;
 // the softmax reference (log2 units) moves only when a chunk exceeds it by
 // more than 8 nats, so probabilities stay below e^8 (inside f16)
@@ -44,8 +52,8 @@ constexpr float kNoRef = -1.0e30f;
 // S MMAs read sits on a 128-byte line
 constexpr int kQPlane = kHAtt * 8;       // in f16 elements (1024 bytes)
 constexpr int kXPlane = kRows * 8;       // f16 elements per 8-channel plane of a slot (1024 bytes)
-constexpr uint32_t kAttnTmemCols = 512;  // O^T 256 columns, two S slots of 64
-constexpr uint32_t kTmemS = 256;         // first column of S slot 0
+constexpr uint32_t kAttnTmemCols = 512;  // O^T 256 columns; per S half, two slots of 64
+constexpr uint32_t kTmemS = 256;         // first column of S half 0, slot 0 (half h, slot s: + 128 h + 64 s)
 constexpr long long kAttnWaitBudget = 1LL << 32;
 
 // In-layer extras ("DeepSeek-V4: ...", CSA, other details), each off when null /
@@ -67,22 +75,21 @@ struct __align__(1024) AttnSmem {
   uint16_t q[kDMain / 8][kQPlane];     // f16 q' [c/8][head][c%8]
   uint16_t P[2][kRows / 8][kHAtt * 8]; // per slot: f16 probabilities [row/8][head][row%8] (P^T K-major)
   float c2[kHAtt];                     // log2(e) * softmax_scale * 2^s_h: logit (log2 units) per raw S
-  float mx[2][kHAtt];                  // per column half: a chunk's scaled maxima (exact-maximum path)
   float alpha[kHAtt];                  // factor of O and l when a head's reference moved
-  float lsum[2][kHAtt];                // per column half: the probability sums of every chunk
   float inv[kHAtt];                    // 1 / softmax denominator (or 1 for partials)
   int32_t idx[CSA2_MAX_TOPK];          // this CTA's selected-entry indices (its chunks' rows below k)
   uint32_t vmask[2][2];                // per slot and 32-row half: rows that exist
-  int vote[2][8];                      // per chunk parity and warp: a logit above its head's threshold
+  int vote[2][4];                      // per chunk parity and softmax warp: a logit above its threshold
   uint64_t q_load;                     // the query's bf16 rows copied into slot 1 (bulk copy)
   uint64_t q_full;                     // q' and c2 written (8 warps)
-  uint64_t x_full[2][2];               // per slot, channel half of X written (4 warps each)
-  uint64_t s_full[2];                  // per slot: S MMAs complete
-  uint64_t p_full[2];                  // per slot: P written (8 warps)
-  uint64_t x_free[2];                  // per slot: O MMAs reading its X and P complete
-  uint64_t vote_full;                  // votes / sums / denominators posted (8 warps)
-  uint64_t max_full;                   // maxima / factors posted (8 warps; chunks that need them)
-  uint64_t drained;                    // every MMA issued complete
+  uint64_t x_full[2][2];               // per slot, channel half of X written (4 row warps each)
+  uint64_t s_full[2];                  // per slot: S MMAs complete (both halves)
+  uint64_t p_full[2];                  // per slot: P written (4 softmax warps)
+  uint64_t x_free[2][2];               // per slot, channel half: the O MMAs reading it complete
+  uint64_t vote_full;                  // votes posted (4 softmax warps)
+  uint64_t max_full;                   // factors posted (4 softmax warps; chunks that need them)
+  uint64_t fin;                        // 1 / denominators posted (4 softmax warps)
+  uint64_t drained;                    // every MMA issued complete (four MMA warps)
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -291,6 +298,19 @@ __device__ __forceinline__ bool dequant_quarter_row(AttnSmem& S, const RowFetch&
   return f.kind != 0;
 }
 
+// Raw S of this lane's head over its 32 rows of a chunk (lanes 0-15: rows 0-31, lanes
+// 16-31: rows 32-63, the head's lane of the M = 64 accumulator): the two channel halves'
+// accumulators (at taddr and taddr + 128) added, -inf for the rows the mask `vm` has not.
+__device__ __forceinline__ void load_scores(uint32_t taddr, uint32_t vm, float (&sv)[32]) {
+  uint32_t a[32], c[32];
+  ptx::tmem_ld_16x32bx2_x32<32>(taddr, a);
+  ptx::tmem_ld_16x32bx2_x32<32>(taddr + 128u, c);
+  ptx::tmem_wait_ld();
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    sv[i] = ((vm >> i) & 1u) ? __uint_as_float(a[i]) + __uint_as_float(c[i]) : -INFINITY;
+}
+
 // The probabilities of one head (this lane) over its 32 rows of a chunk:
 // p = 2^(raw S * c2 - m2) rounded to f16, packed in pairs of rows into ph.
 // Returns whether some logit exceeds the reference by more than kTau2 (a head
@@ -330,10 +350,10 @@ __device__ __forceinline__ float sum_probs(const uint32_t (&ph)[16]) {
 // softmax; the output accumulates in tensor memory across the chunks.
 //   warps 0-7: thread t dequantizes channels 128 (t / 64) .. of chunk row t % 64
 //     into the chunk's slot, fetching the rows of the chunk two ahead meanwhile;
-//     in the softmax warp w owns heads 16 (w % 4) .. + 15 (lanes 0-15, the rows of
-//     an M = 64 accumulator) over the chunk rows 32 (w / 4) .. + 31;
-//   warp 8: barriers, tensor memory, the q' copy and the MMA issue, in pairs of
-//     chunks: S(2p), S(2p+1), O(2p), O(2p+1).
+//     afterwards, the epilogue;
+//   warps 8-11: the softmax; warp 8 + q owns heads 16 q .. + 15 (lanes 0-15 of
+//     lane quarter q, the rows of an M = 64 accumulator) over all of a chunk's rows;
+//   warps 12-15: the MMA issue (S halves, O halves).
 // The softmax keeps, per head, a reference m (the running maximum, raised only
 // when a chunk exceeds it by more than kTau2, which then rescales O and l), so
 // probabilities stay below e^8.  Each chunk first forms P with the references it
@@ -342,8 +362,9 @@ __device__ __forceinline__ float sum_probs(const uint32_t (&ph)[16]) {
 // log2 units: p = 2^(raw S * c2_h - m2_h).
 // kPartial: write the unnormalised O with (m, l) for the merge kernel instead
 // of the normalised output.
+// 16 warps, four per scheduler, whose 16 K registers then allow 128 per thread.
 template <bool kPartial, bool kEx>
-__global__ void __launch_bounds__(kAT, 1) k_attn(
+__global__ void __launch_bounds__(512, 1) k_attn(
     const uint8_t* __restrict__ kv_codes, const uint8_t* __restrict__ kv_scales, int64_t seq_stride,
     const int32_t* __restrict__ topk, const int32_t* __restrict__ dense_n, int k, const uint8_t* __restrict__ swa,
     int n_swa,
@@ -364,13 +385,15 @@ __global__ void __launch_bounds__(kAT, 1) k_attn(
       for (int s = 0; s < 2; ++s) {
         ptx::mbar_init(&S.x_full[s][0], 4);
         ptx::mbar_init(&S.x_full[s][1], 4);
-        ptx::mbar_init(&S.s_full[s], 1);
-        ptx::mbar_init(&S.p_full[s], 8);
-        ptx::mbar_init(&S.x_free[s], 1);
+        ptx::mbar_init(&S.s_full[s], 2);
+        ptx::mbar_init(&S.p_full[s], 4);
+        ptx::mbar_init(&S.x_free[s][0], 1);
+        ptx::mbar_init(&S.x_free[s][1], 1);
       }
-      ptx::mbar_init(&S.vote_full, 8);
-      ptx::mbar_init(&S.max_full, 8);
-      ptx::mbar_init(&S.drained, 1);
+      ptx::mbar_init(&S.vote_full, 4);
+      ptx::mbar_init(&S.max_full, 4);
+      ptx::mbar_init(&S.fin, 4);
+      ptx::mbar_init(&S.drained, 4);  // the four MMA warps
       S.abort_flag = 0;
       ptx::fence_mbar_init();
     }
@@ -389,13 +412,13 @@ __global__ void __launch_bounds__(kAT, 1) k_attn(
   RowFetch rf0, rf1;                                       // rows of the even / odd chunks
   rf0.kind = rf1.kind = 0;
   const int64_t win_lo = ex.win_pos ? max(ex.win_lo[b], (int64_t)0) : 0;  // window rows below it are not seen
-  if (warp < kCtlWarp) {
+  if (warp < kGatherWarps) {
     const int gr0 = c0 * kRows + r, gr1 = gr0 + kRows;
     const int64_t idx0 = fetch_index(topk, dense_n, k, b, gr0);
     const int64_t idx1 = nc > 1 ? fetch_index(topk, dense_n, k, b, gr1) : -1;
     if (!dense_n) {  // the later chunks' indices wait in shared memory (no dependent global load per chunk)
       const int n_sel = min(k - c0 * kRows, nc * kRows);
-      for (int i = tid; i < n_sel; i += kCtlWarp * 32) S.idx[i] = topk[(int64_t)b * k + c0 * kRows + i];
+      for (int i = tid; i < n_sel; i += kGatherWarps * 32) S.idx[i] = topk[(int64_t)b * k + c0 * kRows + i];
     }
     issue_row(rf0, idx0, kv_codes, kv_scales, seq_stride, swa, n_swa, k, b, gr0, part, ws, ex.win_pos, win_lo);
     if (nc > 1)
@@ -406,72 +429,72 @@ __global__ void __launch_bounds__(kAT, 1) k_attn(
   ptx::tc_fence_after();
   const uint32_t tmem = S.tmem_base;
 
-  if (warp == kCtlWarp) {
+  if (warp >= kCtlWarp) {
     // ------------------------------------------------------------ MMA issue
-    // The whole warp runs this loop (uniform control flow, uniform descriptors);
-    // one elected lane issues each MMA and commit.
-    bool good = ptx::mbar_wait_warp(&S.q_full, 0, abort_flag, kAttnWaitBudget);
-    constexpr uint32_t idesc_s = ptx::idesc_f16(64, 64, 0);                    // S = q' X^T: heads x rows
-    constexpr uint32_t idesc_o = ptx::idesc_f16(128, 64, 0) | (1u << 15);      // O^T += X^T P^T: A M-major
-    // descriptors of the first K step; later steps add their byte offset / 16 to the
-    // start-address field (every operand lies below 256 KB, so the field cannot carry)
-    const uint64_t dSa = ptx::smem_desc_noswizzle(&S.q[0][0], kQPlane * 2, 128);
-    uint64_t dSb[2], dOa[2], dOb[2];
+    // One warp per scheduler, each running its loop with the whole warp (uniform control
+    // flow and descriptors; one elected lane issues each MMA and commit).
+    bool good = true;
+    const int h2 = (warp - kCtlWarp) & 1;  // channel half
+    if (warp < kOWarp) {
+      // S half h2 over channels 256 h2 .. + 255: 16 K steps as soon as that half of X is written
+      good = ptx::mbar_wait_warp(&S.q_full, 0, abort_flag, kAttnWaitBudget);
+      constexpr uint32_t idesc_s = ptx::idesc_f16(64, 64, 0);  // S = q' X^T: heads x rows
+      // descriptors of the half's first K step; later steps add their byte offset / 16 to
+      // the start-address field (every operand lies below 256 KB, so the field cannot carry)
+      const uint64_t dSa = ptx::smem_desc_noswizzle(&S.q[32 * h2][0], kQPlane * 2, 128);
+      const uint64_t dSb0 = ptx::smem_desc_noswizzle(&S.X[0][32 * h2][0], kXPlane * 2, 128);  // K-major rows
+      const uint64_t dSb1 = ptx::smem_desc_noswizzle(&S.X[1][32 * h2][0], kXPlane * 2, 128);
+      for (int j = 0; j < nc && good; ++j) {  // S(j) half = q'[:, half] X[:, half]^T : M = 64, N = 64, K = 256
+        const int s = j & 1;
+        const uint32_t ph = (uint32_t)((j >> 1) & 1);
+        const uint64_t dSb = s ? dSb1 : dSb0;
+        const uint32_t dst = tmem + kTmemS + 128u * (uint32_t)h2 + 64u * (uint32_t)s;
+        good = ptx::mbar_wait_warp(&S.x_full[s][h2], ph, abort_flag, kAttnWaitBudget);
+        if (!good) break;
+        ptx::tc_fence_after();
 #pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      dSb[s] = ptx::smem_desc_noswizzle(&S.X[s][0][0], kXPlane * 2, 128);  // K-major rows
-      dOa[s] = ptx::smem_desc_noswizzle(&S.X[s][0][0], 128, kXPlane * 2);  // M-major channels
-      dOb[s] = ptx::smem_desc_noswizzle(&S.P[s][0][0], kHAtt * 16, 128);   // K-major P^T
-    }
-    for (int p = 0; 2 * p < nc && good; ++p) {
-      const uint32_t ph = (uint32_t)(p & 1);
-#pragma unroll
-      for (int s = 0; s < 2; ++s) {  // S(2p + s) = q' X^T : M = 64 heads, N = 64 rows, K = 512
-        if (2 * p + s >= nc || !good) break;
-        for (int h2 = 0; h2 < 2 && good; ++h2) {
-          good = ptx::mbar_wait_warp(&S.x_full[s][h2], ph, abort_flag, kAttnWaitBudget);
-          if (!good) break;
-          ptx::tc_fence_after();
-#pragma unroll 4
-          for (int ks = h2 * 16; ks < h2 * 16 + 16; ++ks)  // q'[2 ks], X[s][2 ks]: ks * 2048 bytes on
-            ptx::mma_f16_ss_elect(tmem + kTmemS + 64u * s, dSa + (uint64_t)(ks * 128), dSb[s] + (uint64_t)(ks * 128),
-                                  idesc_s, ks > 0 ? 1u : 0u);
-        }
-        if (good) ptx::mma_commit_elect(&S.s_full[s]);
+        for (int ks = 0; ks < 16; ++ks)  // q'[2 ks], X[s][2 ks] of the half: ks * 2048 bytes on
+          ptx::mma_f16_ss_elect(dst, dSa + (uint64_t)(ks * 128), dSb + (uint64_t)(ks * 128), idesc_s,
+                                ks > 0 ? 1u : 0u);
+        ptx::mma_commit_elect(&S.s_full[s]);
       }
-#pragma unroll
-      for (int s = 0; s < 2; ++s) {  // O^T += X^T P^T : four 128-channel M tiles, N = 64 heads, K = 64 rows
-        const int j = 2 * p + s;
-        if (j >= nc || !good) break;
+    } else {
+      // O^T tiles 2 h2, 2 h2 + 1 (channels 256 h2 .. + 255)
+      constexpr uint32_t idesc_o = ptx::idesc_f16(128, 64, 0) | (1u << 15);  // O^T += X^T P^T: A M-major
+      const uint64_t dOa0 = ptx::smem_desc_noswizzle(&S.X[0][32 * h2][0], 128, kXPlane * 2);  // M-major channels
+      const uint64_t dOa1 = ptx::smem_desc_noswizzle(&S.X[1][32 * h2][0], 128, kXPlane * 2);
+      const uint64_t dOb0 = ptx::smem_desc_noswizzle(&S.P[0][0][0], kHAtt * 16, 128);  // K-major P^T
+      const uint64_t dOb1 = ptx::smem_desc_noswizzle(&S.P[1][0][0], kHAtt * 16, 128);
+      const uint32_t dst = tmem + 128u * (uint32_t)h2;
+      for (int j = 0; j < nc && good; ++j) {  // O^T += X^T P^T : two 128-channel M tiles, N = 64, K = 64 rows
+        const int s = j & 1;
+        const uint32_t ph = (uint32_t)((j >> 1) & 1);
+        const uint64_t dOa = s ? dOa1 : dOa0, dOb = s ? dOb1 : dOb0;
         good = ptx::mbar_wait_warp(&S.p_full[s], ph, abort_flag, kAttnWaitBudget);
         if (!good) break;
         ptx::tc_fence_after();
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt)
+        for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-          for (int ks = 0; ks < kRows / 16; ++ks)  // X[s][16 mt][128 ks]: mt * 16384 + ks * 256 bytes on;
-                                                  // P[s][2 ks]: ks * 2048 bytes on
-            ptx::mma_f16_ss_elect(tmem + (uint32_t)mt * 64u, dOa[s] + (uint64_t)(mt * 1024 + ks * 16),
-                                  dOb[s] + (uint64_t)(ks * 128), idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
-        ptx::mma_commit_elect(&S.x_free[s]);  // the slot's X and P are no longer read
+          for (int ks = 0; ks < kRows / 16; ++ks)  // X[s][16 mt][128 ks] of the half: mt * 16384 + ks * 256
+                                                  // bytes on; P[s][2 ks]: ks * 2048 bytes on
+            ptx::mma_f16_ss_elect(dst + (uint32_t)mt * 64u, dOa + (uint64_t)(mt * 1024 + ks * 16),
+                                  dOb + (uint64_t)(ks * 128), idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
+        ptx::mma_commit_elect(&S.x_free[s][h2]);  // this half of the slot's X (and P) no longer read
       }
     }
     if (!good && lane == 0 && !*abort_flag) {
       *abort_flag = 1;
       report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 23);
     }
-    // every MMA issued so far has completed before tensor memory is freed
+    // every MMA the four warps issued has completed before tensor memory is freed
     ptx::mma_commit_elect(&S.drained);
     volatile int keep_waiting = 0;
     ptx::mbar_wait_warp(&S.drained, 0, &keep_waiting, kAttnWaitBudget);
-  } else {
-    // ------------------------------------------------- rows, softmax, epilogue
-    const int q4 = warp & 3, ch = warp >> 2;  // softmax: lane quarter, column half (chunk rows 32 ch ..)
-    const bool owner = lane < 16;              // the lanes holding a head in an M = 64 accumulator
-    const int hd = (16 * q4 + lane) & (kHAtt - 1);  // this lane's head (meaningful for owners)
+  } else if (warp < kGatherWarps) {
+    // ------------------------------------------ rows (gather, dequantization), epilogue
+    const int q4 = warp & 3, ch = warp >> 2;  // epilogue: lane quarter, heads 32 ch ..
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-    float m2 = -INFINITY;  // this head's reference (log2 units); both column halves keep the same
-    float lsum = 0.0f;     // this head's rounded probabilities summed over this column half's rows
     // q' through the rotated image in slot 0 (free until the first chunk's rows)
     bool good = ptx::mbar_wait_warp(&S.q_load, 0, abort_flag, kAttnWaitBudget);
     if (good) {
@@ -485,7 +508,6 @@ __global__ void __launch_bounds__(kAT, 1) k_attn(
     ptx::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(&S.q_full);
-    int nvote = 0, nslow = 0;  // uses of vote_full / max_full so far (the same in every warp)
     for (int p = 0; 2 * p < nc && good; ++p) {
       const uint32_t ph = (uint32_t)(p & 1);
       // ---- rows of chunks 2p and 2p + 1 into slots 0 and 1
@@ -499,8 +521,8 @@ __global__ void __launch_bounds__(kAT, 1) k_attn(
         const int64_t idx2 = j + 2 >= nc || gr2 >= k ? -1
                              : dense_n ? (gr2 < __ldg(dense_n + b) ? gr2 : -1)
                                        : (int64_t)S.idx[(j + 2) * kRows + r];
-        if (j >= 2)  // O(j - 2) no longer reads the slot
-          good = ptx::mbar_wait_warp(&S.x_free[s], ph ^ 1u, abort_flag, kAttnWaitBudget);
+        if (j >= 2)  // O(j - 2) no longer reads this thread's channel half of the slot
+          good = ptx::mbar_wait_warp(&S.x_free[s][part >> 1], ph ^ 1u, abort_flag, kAttnWaitBudget);
         else  // slot 1 holds the bf16 q copy, slot 0 the rotated q', until every warp staged q'
           good = ptx::mbar_wait_warp(&S.q_full, 0, abort_flag, kAttnWaitBudget);
         if (!good) break;
@@ -515,132 +537,17 @@ __global__ void __launch_bounds__(kAT, 1) k_attn(
         if (j + 2 < nc)
           issue_row(f, idx2, kv_codes, kv_scales, seq_stride, swa, n_swa, k, b, gr2, part, ws, ex.win_pos, win_lo);
       }
-      // ---- softmax of chunks 2p and 2p + 1
-      for (int s = 0; s < 2 && good; ++s) {
-        const int j = 2 * p + s;
-        if (j >= nc) break;
-        good = ptx::mbar_wait_warp(&S.s_full[s], ph, abort_flag, kAttnWaitBudget) &&
-               ptx::mbar_wait_warp(&S.x_full[s][0], ph, abort_flag, kAttnWaitBudget);  // vmask (acquire)
-        if (!good) break;
-        ptx::tc_fence_after();
-        const uint32_t taS = tmem + lane_base + kTmemS + 64u * (uint32_t)s + 32u * (uint32_t)ch;
-        const uint32_t vm = S.vmask[s][ch];  // chunk rows 32 ch .. 32 ch + 31 that exist
-        const float c2h = S.c2[hd];
-        float sv[32];
-        {
-          uint32_t a[32];
-          ptx::tmem_ld_32x32b_x32(taS, a);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) sv[i] = ((vm >> i) & 1u) ? __uint_as_float(a[i]) : -INFINITY;  // raw S
-        }
-        // P with the references so far: stands unless some head needs a new one.  The
-        // P^T slot is free: S(j) was issued after O(j - 2), and its commit covers that
-        uint32_t ph16[16];
-        const bool over = head_probs(sv, c2h, m2 == -INFINITY ? kNoRef : m2, ph16) && owner;
-        if (owner) store_probs(S, s, ch, hd, ph16);
-        const bool wover = __any_sync(0xffffffffu, over);
-        if (lane == 0) S.vote[nvote & 1][warp] = wover ? 1 : 0;
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&S.vote_full);
-        good = ptx::mbar_wait_warp(&S.vote_full, (uint32_t)(nvote & 1), abort_flag, kAttnWaitBudget);
-        if (!good) break;
-        bool slow = false;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) slow |= S.vote[nvote & 1][w] != 0;
-        ++nvote;
-        float alpha = 1.0f;  // this head's factor for its sums and O
-        if (slow) {
-          // the chunk's exact maxima: this column half's rows, then the other's
-          float cm = -INFINITY;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) cm = fmaxf(cm, sv[i]);
-          if (owner) S.mx[ch][hd] = cm * c2h;  // -inf stays -inf (c2 > 0)
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&S.max_full);
-          good = ptx::mbar_wait_warp(&S.max_full, (uint32_t)(nslow & 1), abort_flag, kAttnWaitBudget);
-          if (!good) break;
-          ++nslow;
-          const float cmax = fmaxf(S.mx[0][hd], S.mx[1][hd]);
-          if (cmax > m2 + kTau2) {  // also the first chunk with a row of this head
-            alpha = m2 == -INFINITY ? 0.0f : ptx::ex2(m2 - cmax);
-            m2 = cmax;
-          }
-          (void)head_probs(sv, c2h, m2 == -INFINITY ? kNoRef : m2, ph16);
-          if (owner) store_probs(S, s, ch, hd, ph16);
-          if (j > 0) {  // O^T holds earlier chunks: scale the columns of the heads that moved
-            if (owner && ch == 0) S.alpha[hd] = alpha;
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&S.max_full);
-            good = ptx::mbar_wait_warp(&S.max_full, (uint32_t)(nslow & 1), abort_flag, kAttnWaitBudget) &&
-                   ptx::mbar_wait_warp(&S.x_free[s ^ 1], (uint32_t)(((j - 1) >> 1) & 1), abort_flag,
-                                       kAttnWaitBudget);  // O(j - 1) complete
-            if (!good) break;
-            ++nslow;
-            ptx::tc_fence_after();
-            // this warp's share: O^T lanes of quarter q4 (channels), columns of heads 32 ch ..
-            const float a32 = S.alpha[32 * ch + lane];
-            if (__any_sync(0xffffffffu, a32 != 1.0f)) {
-#pragma unroll 1
-              for (int mt = 0; mt < 4; ++mt) {
-                uint32_t a[32];
-                const uint32_t ta = tmem + lane_base + (uint32_t)mt * 64u + 32u * (uint32_t)ch;
-                ptx::tmem_ld_32x32b_x32(ta, a);
-                ptx::tmem_wait_ld();
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj)
-                  a[jj] = __float_as_uint(__uint_as_float(a[jj]) * __shfl_sync(0xffffffffu, a32, jj));
-                ptx::tmem_st_32x32b_x32(ta, a);
-              }
-              ptx::tmem_wait_st();
-            }
-          }
-        }
-        ptx::fence_proxy_async_smem();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&S.p_full[s]);  // the MMA thread waits; the rows go on
-        lsum = fmaf(alpha, lsum, sum_probs(ph16));
-      }
     }
-    // ---- the softmax denominators (both column halves), the lse / partials, then
-    // the output: O^T rows = channels of this lane quarter, 32 heads per warp; for
-    // each head the warp stores 32 consecutive channels.  The sink joins the
-    // denominator here (split queries: in the merge); with RoPE the last 64
-    // channels turn back by -qpos (pairs are adjacent lanes; the turn is linear,
-    // so partials may take it before the merge).
-    if (good) {
-      if (owner) S.lsum[ch][hd] = lsum;
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&S.vote_full);
-      good = ptx::mbar_wait_warp(&S.vote_full, (uint32_t)(nvote & 1), abort_flag, kAttnWaitBudget);
-      ++nvote;
-    }
-    if (good) {
-      if (owner && ch == 0) {
-        const float l_run = S.lsum[0][hd] + S.lsum[1][hd];
-        const float m_nat = m2 / kLog2e;  // reference in natural units
-        float den = l_run;
-        if (!kPartial && kEx && ex.sink) den += ptx::ex2(ex.sink[hd] * kLog2e - m2);  // 2^(z2 - m2); m2 = -inf -> inf
-        S.inv[hd] = kPartial ? 1.0f : (den > 0.0f ? 1.0f / den : 0.0f);
-        if (kPartial) {
-          part_ml[((int64_t)b * gridDim.x + split) * kHAtt + hd] = make_float2(m_nat, l_run);
-        } else if (lse) {
-          if (kEx && ex.sink) {
-            const float z = ex.sink[hd], mxv = fmaxf(m_nat, z);
-            lse[b * kHAtt + hd] = mxv + logf(l_run * expf(m_nat - mxv) + expf(z - mxv));
-          } else {
-            lse[b * kHAtt + hd] = l_run > 0.0f ? m_nat + logf(l_run) : -INFINITY;
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&S.vote_full);
-      good = ptx::mbar_wait_warp(&S.vote_full, (uint32_t)(nvote & 1), abort_flag, kAttnWaitBudget) &&
-             ptx::mbar_wait_warp(&S.x_free[(nc - 1) & 1], (uint32_t)(((nc - 1) >> 1) & 1), abort_flag,
-                                 kAttnWaitBudget);  // the last O MMAs (their commit covers the others)
-      ++nvote;
-    }
+    // ---- epilogue: O^T rows = channels of this lane quarter, 32 heads per warp; for each
+    // head the warp stores 32 consecutive channels.  With RoPE the last 64 channels turn
+    // back by -qpos (pairs are adjacent lanes; the turn is linear, so partials may take it
+    // before the merge).  The softmax warps post 1 / denominator per head first.
+    if (good)  // the last O MMAs of both halves (each commit covers its warp's earlier ones)
+      good = ptx::mbar_wait_warp(&S.fin, 0, abort_flag, kAttnWaitBudget) &&
+             ptx::mbar_wait_warp(&S.x_free[(nc - 1) & 1][0], (uint32_t)(((nc - 1) >> 1) & 1), abort_flag,
+                                 kAttnWaitBudget) &&
+             ptx::mbar_wait_warp(&S.x_free[(nc - 1) & 1][1], (uint32_t)(((nc - 1) >> 1) & 1), abort_flag,
+                                 kAttnWaitBudget);
     if (!good && lane == 0 && !*abort_flag) {
       *abort_flag = 1;
       report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 24);
@@ -673,6 +580,133 @@ __global__ void __launch_bounds__(kAT, 1) k_attn(
         }
       }
     }
+  } else {
+    // ---------------------------------------------------------------- softmax
+    // Warp 8 + q reads lane quarter q of tensor memory: heads 16q .. 16q + 15 of each S
+    // accumulator in lanes 0-15.  Lane l takes head 16q + l % 16 over the chunk rows
+    // 32 (l / 16) .. + 31, so the two lanes of a head share its exponentials; its maximum
+    // and sum are combined across the pair (lanes l and l ^ 16).
+    const int q4 = warp & 3, rh = lane >> 4;
+    const bool owner = lane < 16;
+    const int hd = 16 * q4 + (lane & 15);  // this lane's head
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    float m2 = -INFINITY;  // this head's reference (log2 units; the same in both lanes)
+    float lsum = 0.0f;     // rounded probabilities of this lane's rows, summed over every chunk
+    bool good = ptx::mbar_wait_warp(&S.q_full, 0, abort_flag, kAttnWaitBudget);  // c2 (acquire)
+    const float c2h = S.c2[hd];
+    int nvote = 0, nslow = 0;  // uses of vote_full / max_full so far (the same in every softmax warp)
+    for (int j = 0; j < nc && good; ++j) {
+      const int s = j & 1;
+      const uint32_t ph = (uint32_t)((j >> 1) & 1);
+      // x_full of both halves: the row warps wrote X(j) after O(j - 2) released the slot, so
+      // the P^T slot is free too; half 0 also posts the row mask
+      good = ptx::mbar_wait_warp(&S.s_full[s], ph, abort_flag, kAttnWaitBudget) &&
+             ptx::mbar_wait_warp(&S.x_full[s][0], ph, abort_flag, kAttnWaitBudget) &&
+             ptx::mbar_wait_warp(&S.x_full[s][1], ph, abort_flag, kAttnWaitBudget);
+      if (!good) break;
+      ptx::tc_fence_after();
+      const uint32_t taS = tmem + lane_base + kTmemS + 64u * (uint32_t)s;  // half 0; half 1 at + 128
+      const uint32_t vm = S.vmask[s][rh];  // this lane's rows that exist
+      // P with the reference so far: stands unless some head needs a new one
+      uint32_t pp[16];  // this lane's 32 rows, f16 pairs
+      bool over;
+      {
+        const float ref = m2 == -INFINITY ? kNoRef : m2;
+        float sv[32];
+        load_scores(taS, vm, sv);
+        over = head_probs(sv, c2h, ref, pp);
+      }
+      store_probs(S, s, rh, hd, pp);
+      ptx::fence_proxy_async_smem();  // before the vote: its latency overlaps the other warps'
+      const bool wover = __any_sync(0xffffffffu, over);
+      if (lane == 0) S.vote[nvote & 1][q4] = wover ? 1 : 0;
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&S.vote_full);
+      good = ptx::mbar_wait_warp(&S.vote_full, (uint32_t)(nvote & 1), abort_flag, kAttnWaitBudget);
+      if (!good) break;
+      const bool slow = (S.vote[nvote & 1][0] | S.vote[nvote & 1][1] | S.vote[nvote & 1][2] |
+                         S.vote[nvote & 1][3]) != 0;
+      ++nvote;
+      float alpha = 1.0f;  // this head's factor for its sum and O
+      if (slow) {
+        // the chunk's exact maximum of this head (both lanes' rows; S stays in tensor memory
+        // until P is handed over)
+        float sv[32], cm = -INFINITY;
+        load_scores(taS, vm, sv);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) cm = fmaxf(cm, sv[i]);
+        cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16));
+        cm *= c2h;  // -inf stays -inf (c2 > 0)
+        if (cm > m2 + kTau2) {  // also the first chunk with a row of this head
+          alpha = m2 == -INFINITY ? 0.0f : ptx::ex2(m2 - cm);
+          m2 = cm;
+        }
+        const float ref = m2 == -INFINITY ? kNoRef : m2;
+        (void)head_probs(sv, c2h, ref, pp);
+        store_probs(S, s, rh, hd, pp);
+        ptx::fence_proxy_async_smem();
+        if (j > 0) {  // O^T holds earlier chunks: scale the columns of the heads that moved
+          if (owner) S.alpha[hd] = alpha;
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&S.max_full);
+          good = ptx::mbar_wait_warp(&S.max_full, (uint32_t)(nslow & 1), abort_flag, kAttnWaitBudget) &&
+                 ptx::mbar_wait_warp(&S.x_free[s ^ 1][0], (uint32_t)(((j - 1) >> 1) & 1), abort_flag,
+                                     kAttnWaitBudget) &&
+                 ptx::mbar_wait_warp(&S.x_free[s ^ 1][1], (uint32_t)(((j - 1) >> 1) & 1), abort_flag,
+                                     kAttnWaitBudget);  // O(j - 1) complete
+          if (!good) break;
+          ++nslow;
+          ptx::tc_fence_after();
+          // this warp's share: O^T lanes of quarter q4 (channels), the columns of all 64 heads
+#pragma unroll 1
+          for (int c32 = 0; c32 < 2; ++c32) {
+            const float a32 = S.alpha[32 * c32 + lane];
+            if (!__any_sync(0xffffffffu, a32 != 1.0f)) continue;
+#pragma unroll 1
+            for (int mt = 0; mt < 4; ++mt) {
+              uint32_t a[32];
+              const uint32_t ta = tmem + lane_base + (uint32_t)mt * 64u + 32u * (uint32_t)c32;
+              ptx::tmem_ld_32x32b_x32(ta, a);
+              ptx::tmem_wait_ld();
+#pragma unroll
+              for (int jj = 0; jj < 32; ++jj)
+                a[jj] = __float_as_uint(__uint_as_float(a[jj]) * __shfl_sync(0xffffffffu, a32, jj));
+              ptx::tmem_st_32x32b_x32(ta, a);
+            }
+            ptx::tmem_wait_st();
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&S.p_full[s]);  // the MMA warps wait; the softmax goes on
+      lsum = fmaf(alpha, lsum, sum_probs(pp));
+    }
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);  // the head's two lanes: every row
+    if (!good && lane == 0 && !*abort_flag) {
+      *abort_flag = 1;
+      report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 26);
+    }
+    // ---- this head's denominator, the lse / partials, 1 / denominator for the epilogue.
+    // The sink joins the denominator here (split queries: in the merge).
+    if (good && owner) {
+      const float m_nat = m2 / kLog2e;  // reference in natural units
+      float den = lsum;
+      if (!kPartial && kEx && ex.sink) den += ptx::ex2(ex.sink[hd] * kLog2e - m2);  // 2^(z2 - m2); m2 = -inf -> inf
+      S.inv[hd] = kPartial ? 1.0f : (den > 0.0f ? 1.0f / den : 0.0f);
+      if (kPartial) {
+        part_ml[((int64_t)b * gridDim.x + split) * kHAtt + hd] = make_float2(m_nat, lsum);
+      } else if (lse) {
+        if (kEx && ex.sink) {
+          const float z = ex.sink[hd], mxv = fmaxf(m_nat, z);
+          lse[b * kHAtt + hd] = mxv + logf(lsum * expf(m_nat - mxv) + expf(z - mxv));
+        } else {
+          lse[b * kHAtt + hd] = lsum > 0.0f ? m_nat + logf(lsum) : -INFINITY;
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&S.fin);  // also on failure: the row warps then see the abort flag
   }
   ptx::tc_fence_before();
   __syncthreads();
