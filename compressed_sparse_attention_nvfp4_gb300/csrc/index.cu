@@ -301,16 +301,20 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
 }
 
 // Resident form of the same selection, for slices of at most kResCap
-// candidates per CTA: each CTA loads its slice once into shared memory (thread t
-// owns a contiguous run of kper candidates), runs the four digit passes there,
-// and collects with one scan: a thread's run is contiguous, so per-thread counts
-// of keys above / equal to the threshold, scanned in thread order and offset by
-// the cluster's earlier CTAs, place every chosen id in candidate order.
-// Histogram updates are run-length coded per thread (one shared atomic per run
-// of equal digits), and the per-CTA histograms alternate between two buffers so
-// that one cluster barrier per pass suffices.  (A single 1024-thread CTA per
-// query for the pool's 16,384 entries measured slower than eight CTAs: the
-// load latency of one query's gather is then hidden by nothing.)
+// candidates per CTA: each CTA loads its slice once into shared memory (coalesced
+// loads; thread t owns a contiguous run of kper candidates) and collects with one
+// scan: a thread's run is contiguous, so per-thread counts of keys above / equal to
+// the threshold, scanned in thread order and offset by the cluster's earlier CTAs,
+// place every chosen id in candidate order.  The first digit is the key's offset from
+// the cluster's smallest key in units of 2^shift0 (at most 255 units span the keys),
+// which spreads keys that share their top bits over the histogram; each thread keeps
+// its keys' first digits as bytes, so the keys above the threshold's first-digit bin
+// and those in it come from byte-wise compares, and only the latter are looked at
+// again.  When the bin's keys of the whole cluster fit kCompCap they are gathered in
+// rank 0, which finds the remaining digits alone.  The per-CTA histograms alternate
+// between two buffers so that one cluster barrier per pass suffices.  (A single
+// 1024-thread CTA per query for the pool's 16,384 entries measured slower than eight
+// CTAs: the load latency of one query's gather is then hidden by nothing.)
 constexpr int kResMaxPer = 64;  // candidates per thread (a thread's keys fit one 64-bit mask)
 constexpr int64_t kResCap = 256 * kResMaxPer;  // candidates per CTA: 64 KB of keys
 constexpr int kCompCap = 4096;  // keys of the first digit's threshold bin kept for the later passes
@@ -349,6 +353,43 @@ __device__ __forceinline__ uint4 load_keys4(const SelectArgs& a, int b, int64_t 
   return make_uint4(k[0], k[1], k[2], k[3]);
 }
 
+// First digit of every key of a thread's run (NS slots of 4): counted in the warp's
+// histogram and kept, + 1, as a byte in dg (0: no key).
+template <int NS>
+__device__ __forceinline__ void first_digits(const uint4* myslots, int swz, int shift, uint32_t base0,
+                                             unsigned* myhist, uint32_t (&dg)[kResMaxPer / 4]) {
+#pragma unroll
+  for (int v = 0; v < NS; ++v) {
+    const uint4 k4 = myslots[v ^ swz];
+    const uint32_t kk4[4] = {k4.x, k4.y, k4.z, k4.w};
+    uint32_t w = 0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (kk4[i] != 0u) {
+        const uint32_t d = (kk4[i] >> shift) - base0;
+        atomicAdd(&myhist[d], 1u);
+        w |= (d + 1u) << (8 * i);
+      }
+    }
+    dg[v] = w;
+  }
+}
+
+// Bit 4 v + i of gtm / binm: key i of slot v has a first digit above / equal to the
+// threshold's (j4: its digit + 1 in every byte), four keys per byte-wise compare.
+template <int NS>
+__device__ __forceinline__ void digit_masks(const uint32_t (&dg)[kResMaxPer / 4], uint32_t j4, uint64_t& gtm,
+                                            uint64_t& binm) {
+#pragma unroll
+  for (int v = 0; v < NS; ++v) {
+    // 0xFF per byte that compares true; the low bit of each byte moved to bits 24..27
+    const uint32_t gt = ((__vcmpgtu4(dg[v], j4) & 0x01010101u) * 0x01020408u) >> 24;
+    const uint32_t eq = ((__vcmpeq4(dg[v], j4) & 0x01010101u) * 0x01020408u) >> 24;
+    gtm |= (uint64_t)gt << (4 * v);
+    binm |= (uint64_t)eq << (4 * v);
+  }
+}
+
 template <int NT>
 __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
   constexpr int kBins = 256;
@@ -362,6 +403,7 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
   __shared__ int ccount[2];
   __shared__ uint32_t s_prefix, s_mask;
   __shared__ int s_need, s_shift0;
+  __shared__ uint32_t s_base0;            // first digit of a key: (key >> shift0) - s_base0
   __shared__ int s_base_eq, s_base_out;
   __shared__ int s_ncomp;                 // keys in the compacted list (may exceed kCompCap: then unused)
   __shared__ int s_gtotal, s_goff;        // first digit's threshold bin: cluster total, this CTA's offset
@@ -395,7 +437,9 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
     ckmax = 0;
     s_ncomp = 0;
   }
-  // load the run once, up to kLoadBatch slots in flight per thread
+  // load the slice once, up to kLoadBatch 4-key groups in flight per thread.  The loads
+  // are coalesced (group g = tid + NT u: consecutive threads read consecutive 16 bytes)
+  // and each group is stored to its owner's run: owner g / nslot, slot g % nslot
   constexpr int kLoadBatch = NT >= 1024 ? 4 : 16;  // within the register budget of NT threads
   unsigned myvalid = 0;
   uint32_t mykmin = 0xFFFFFFFFu, mykmax = 0;
@@ -407,13 +451,13 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
       float4 f[kLoadBatch];
 #pragma unroll
       for (int u = 0; u < kLoadBatch; ++u) {
-        const int64_t c0 = t0 + 4 * (v0 + u);
+        const int64_t c0 = lo + 4 * ((int64_t)tid + (int64_t)NT * (v0 + u));
         f[u] = (v0 + u < nslot && c0 + 4 <= hi) ? __ldg(reinterpret_cast<const float4*>(krow + c0))
                                                  : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
       }
 #pragma unroll
       for (int u = 0; u < kLoadBatch; ++u) {
-        const int64_t c0 = t0 + 4 * (v0 + u);
+        const int64_t c0 = lo + 4 * ((int64_t)tid + (int64_t)NT * (v0 + u));
         float v[4] = {f[u].x, f[u].y, f[u].z, f[u].w};
         if (v0 + u < nslot && c0 < hi && c0 + 4 > hi) {  // the slice's ragged end
 #pragma unroll
@@ -427,14 +471,16 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
     } else {
 #pragma unroll
       for (int u = 0; u < kLoadBatch; ++u) {
-        const int64_t c0 = t0 + 4 * (v0 + u);
+        const int64_t c0 = lo + 4 * ((int64_t)tid + (int64_t)NT * (v0 + u));
         k4[u] = (v0 + u < nslot && c0 < hi) ? load_keys4(a, b, n, hi, c0, vec_ok) : make_uint4(0u, 0u, 0u, 0u);
       }
     }
 #pragma unroll
     for (int u = 0; u < kLoadBatch; ++u) {
       if (v0 + u < nslot) {
-        myslots[(v0 + u) ^ swz] = k4[u];
+        const int g = tid + NT * (v0 + u);
+        const int o = g / nslot, vs = g % nslot;  // nslot is a power of two
+        keys_s[(int64_t)o * nslot + (vs ^ (o & (nslot - 1)))] = k4[u];
         const uint32_t kv[4] = {k4[u].x, k4[u].y, k4[u].z, k4[u].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -455,9 +501,10 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
     atomicMin(&ckmin, mykmin);
     atomicMax(&ckmax, mykmax);
   }
-  // the cluster's valid count and key range: the bits above the highest bit
-  // where the smallest and largest keys differ are common to every key, so the
-  // digits start below them (the first digit then splits the keys)
+  // the cluster's valid count and key range.  The first digit is the key's offset from
+  // the smallest key in units of 2^shift0, shift0 the least shift that brings the range
+  // within 256 units: it spreads the keys over the range's bins, where the key's own top
+  // bits would put most of them in a few (scores within a few binades share them)
   cluster.sync();
   if (wid == 0) {  // lane r reads CTA r's values: one round trip
     unsigned tv = 0, kmn = 0xFFFFFFFFu, kmx = 0;
@@ -471,33 +518,47 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
     kmx = __reduce_max_sync(0xffffffffu, kmx);
     if (lane == 0) {
       s_need = (int)min((int64_t)a.k, (int64_t)tv);
-      const int top = kmn < kmx ? 31 - __clz((int)(kmn ^ kmx)) : 7;  // highest differing bit
-      s_shift0 = max(top - 7, 0);
-      s_mask = top >= 31 ? 0u : (0xFFFFFFFFu << (top + 1));  // bits shared by every valid key
-      s_prefix = tv ? (kmn & s_mask) : 0u;
+      int sh = 0;
+      if (tv)
+        while ((kmx >> sh) - (kmn >> sh) > 254u) ++sh;  // at most 24; digits 0..254
+      s_shift0 = sh;
+      s_base0 = tv ? kmn >> sh : 0u;
+      s_mask = 0u;  // pass 0 takes every valid key
+      s_prefix = 0u;
     }
   }
   __syncthreads();
   const int need_total = s_need;
   const int shift0 = s_shift0;
+  const uint32_t base0 = s_base0;
 
   int pass = 0;
+  // after the first digit, bit 4 v + i of each: this thread's candidate t0 + 4 v + i lies
+  // above the threshold's first-digit bin / in it (only the latter need the final key)
+  uint64_t gtm0 = 0, binm = 0;
+  uint32_t dg[kResMaxPer / 4];  // first digit + 1 of the keys of slot v, a byte each (0: no key)
   // digit of pass p: bits [shift + 7, shift] (the last pass may reach below bit 0)
   for (int shift = shift0; need_total > 0 && shift > -8; shift -= 8, ++pass) {
     for (int d = lane; d < kBins; d += 32) myhist[d] = 0;
     __syncthreads();
     const uint32_t prefix = s_prefix, mask = s_mask;
     const int ncomp = s_ncomp;
-    // four independent run-length counters (one per key of a slot) for ILP
-    uint32_t last[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
-    unsigned run[4] = {0, 0, 0, 0};
     if (pass > 0 && ncomp <= kCompCap) {  // the later digits only split the first digit's bin
       for (int j = tid; j < ncomp; j += NT) {
         const uint32_t kk = comp_s[j];
         if ((kk & mask) == prefix) atomicAdd(&myhist[(shift >= 0 ? kk >> shift : kk << -shift) & 255u], 1u);
       }
     }
-    const int vend = (pass > 0 && ncomp <= kCompCap) ? 0 : nslot;
+    if (pass == 0) {  // every key: count its first digit and keep it in dg (unrolled per run length)
+      switch (nslot) {
+        case 1: first_digits<1>(myslots, swz, shift, base0, myhist, dg); break;
+        case 2: first_digits<2>(myslots, swz, shift, base0, myhist, dg); break;
+        case 4: first_digits<4>(myslots, swz, shift, base0, myhist, dg); break;
+        case 8: first_digits<8>(myslots, swz, shift, base0, myhist, dg); break;
+        default: first_digits<kResMaxPer / 4>(myslots, swz, shift, base0, myhist, dg); break;
+      }
+    }
+    const int vend = (pass > 0 && ncomp <= kCompCap) || pass == 0 ? 0 : nslot;
     for (int v = 0; v < vend; ++v) {
       const uint4 k4 = myslots[v ^ swz];
       const uint32_t kk4[4] = {k4.x, k4.y, k4.z, k4.w};
@@ -505,20 +566,11 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
       for (int i = 0; i < 4; ++i) {
         const uint32_t kk = kk4[i];
         if (kk != 0u && (kk & mask) == prefix) {
-          const uint32_t d = (shift >= 0 ? kk >> shift : kk << -shift) & 255u;
-          if (d == last[i]) {
-            ++run[i];
-          } else {
-            if (run[i]) atomicAdd(&myhist[last[i]], run[i]);
-            last[i] = d;
-            run[i] = 1;
-          }
+          const uint32_t d = pass == 0 ? (kk >> shift) - base0 : (shift >= 0 ? kk >> shift : kk << -shift) & 255u;
+          atomicAdd(&myhist[d], 1u);
         }
       }
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      if (run[i]) atomicAdd(&myhist[last[i]], run[i]);
     __syncthreads();
     unsigned* ch = chist[pass & 1];
     if (tid < kBins) {  // this CTA's bin totals (thread t <-> bin 255 - t)
@@ -548,28 +600,35 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
     ScanI(scan_tmp).InclusiveSum(cum, cum);
     __syncthreads();  // s_need read above before it is rewritten
     if (bin >= 0 && cum >= need && cum - (int)h < need) {
-      s_prefix = prefix | (shift >= 0 ? (uint32_t)bin << shift : (uint32_t)bin >> -shift);
-      s_mask = mask | (shift >= 0 ? 255u << shift : 255u >> -shift);
+      if (pass == 0) {  // the keys whose bits from shift0 up equal base0 + bin
+        s_prefix = (base0 + (uint32_t)bin) << shift;
+        s_mask = 0xFFFFFFFFu << shift;
+      } else {
+        s_prefix = prefix | (shift >= 0 ? (uint32_t)bin << shift : (uint32_t)bin >> -shift);
+        s_mask = mask | (shift >= 0 ? 255u << shift : 255u >> -shift);
+      }
       s_need = need - (cum - (int)h);
       s_gtotal = (int)h;
       s_goff = (int)below;
     }
     __syncthreads();
+    if (pass == 0) {  // from the kept digits: four keys per byte-wise compare
+      const uint32_t j4 = (((s_prefix >> shift) - base0) + 1u) * 0x01010101u;  // the bin's digit + 1
+      switch (nslot) {
+        case 1: digit_masks<1>(dg, j4, gtm0, binm); break;
+        case 2: digit_masks<2>(dg, j4, gtm0, binm); break;
+        case 4: digit_masks<4>(dg, j4, gtm0, binm); break;
+        case 8: digit_masks<8>(dg, j4, gtm0, binm); break;
+        default: digit_masks<kResMaxPer / 4>(dg, j4, gtm0, binm); break;
+      }
+    }
     if (pass == 0 && shift > 0) {  // more digits follow: keep the threshold bin's keys
-      const uint32_t p2 = s_prefix, m2 = s_mask;
       // the bin's keys of the whole cluster fit one CTA: gather them into rank 0,
       // which finishes the digits alone (no cluster barrier per digit)
       const bool gather = s_gtotal <= kCompCap;
       uint32_t* dst = gather ? cluster.map_shared_rank(comp_s, 0) + s_goff : comp_s;
-      // first the matches as a mask (loads and compares only), then one slot
-      // reservation per thread and the few stores
-      uint64_t mm = 0;
-      for (int v = 0; v < nslot; ++v) {
-        const uint4 k4 = myslots[v ^ swz];
-        const uint32_t kk4[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) mm |= (uint64_t)(kk4[i] != 0u && (kk4[i] & m2) == p2) << (4 * v + i);
-      }
+      // one slot reservation per thread and the few stores of its keys in the bin
+      uint64_t mm = binm;
       if (mm) {
         int j = atomicAdd(&s_ncomp, __popcll(mm));
         while (mm) {
@@ -624,16 +683,14 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
   const int take_eq = s_need;  // candidates equal to T to take (lowest indices first)
 
   if (need_total > 0) {
-    // bit 4 v + i of gtm / eqm: this thread's candidate t0 + 4 v + i is above / equal to T
-    uint64_t gtm = 0, eqm = 0;
-    for (int v = 0; v < nslot; ++v) {
-      const uint4 k4 = myslots[v ^ swz];
-      const uint32_t kk4[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        gtm |= (uint64_t)(kk4[i] != 0u && kk4[i] > T) << (4 * v + i);
-        eqm |= (uint64_t)(kk4[i] != 0u && kk4[i] == T) << (4 * v + i);
-      }
+    // bit 4 v + i of gtm / eqm: this thread's candidate t0 + 4 v + i is above / equal to T.
+    // Keys above the first digit's bin are above T; only the bin's keys are compared
+    uint64_t gtm = gtm0, eqm = 0;
+    for (uint64_t bm = binm; bm; bm &= bm - 1) {
+      const int bit = __ffsll((long long)bm) - 1;
+      const uint32_t kk = reinterpret_cast<const uint32_t*>(&myslots[(bit >> 2) ^ swz])[bit & 3];
+      gtm |= (uint64_t)(kk > T) << bit;
+      eqm |= (uint64_t)(kk == T) << bit;
     }
     const int gt = __popcll(gtm), eq = __popcll(eqm);
     const int wgt = (int)__reduce_add_sync(0xffffffffu, (unsigned)gt);
