@@ -391,161 +391,239 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // (truncated), mid = the next 8 of the remainder, lo = the rest (at most 8
 // bits), so Cbar = hi + mid + lo exactly, and W_IK is bf16 already.  The three
 // terms are three MMA sets into one fp32 accumulator; only the order of the
-// fp32 additions differs from a sequential sum.  One CTA per 128 entries: all
-// of W_IK^T (128 outputs x 512, K-major, 128-byte swizzle) stays in shared
-// memory; threads stream Cbar 64 channels at a time, split it and store the
-// three 128 x 64 operand tiles (two buffers); one thread issues 3 x 4 MMAs
-// (M128 N128 K16) per chunk.
-constexpr int kKtThreads = 256;
+// fp32 additions differs from a sequential sum.  Persistent: one CTA per SM
+// keeps all of W_IK^T (128 outputs x 512, K-major, 128-byte swizzle) in shared
+// memory and runs tiles of 128 entries, 64 channels (a chunk) at a time:
+//   warp 9     tensor-loads each chunk of Cbar (fp32, two 32-channel boxes,
+//              128-byte swizzle) into a three-stage ring;
+//   warps 0-7  thread = (entry row, 32-channel half): read the row's half from
+//              the ring, split it, and store the three bf16 terms as the MMA's A
+//              operand in tensor memory (row m at lane m, two bf16 per column;
+//              two buffers), so the operand never passes through shared memory;
+//              warps 0-3 also read each finished tile's K^I out;
+//   warp 8     issues 3 x 4 MMAs (M128 N128 K16, A from tensor memory, W^T from
+//              shared memory) per chunk into one of two accumulators, so a
+//              tile's K^I is read out while the next tile's chunks run.
+constexpr int kKtStreamWarps = 8;
+constexpr int kKtMmaWarp = 8;
+constexpr int kKtLoadWarp = 9;
+constexpr int kKtThreads = 10 * 32;
+constexpr int kKtStages = 3;
+constexpr uint32_t kKtAcol = 256;  // A operand buffer u: columns 256 + 128 u (term t: + 32 t)
 constexpr long long kKtWaitBudget = 1LL << 32;
 
 struct __align__(1024) KtSmem {
-  uint8_t B[8][128 * 128];         // W_IK^T chunk j: 128 outputs x 64 channels
-  uint8_t A[2][3][128 * 128];      // [buffer][hi, mid, lo]: 128 entries x 64 channels
-  uint64_t b_full, a_free[2], done;
+  uint8_t B[8][128 * 128];                 // W_IK^T chunk j: 128 outputs x 64 channels
+  float X[kKtStages][2][128 * 32];         // Cbar chunk: [half][row][32 channels], 128-byte swizzle
+  uint64_t b_full, x_full[kKtStages], x_free[kKtStages], a_full[2], a_free[2], done[2], acc_free[2], drain;
   uint32_t tmem_base;
   int abort_flag;
 };
 
+// Splits 32 fp32 values into the hi / mid / lo bf16 terms, packed in pairs
+// (element 2c in the low half of word c).
+__device__ __forceinline__ void kt_split(const float (&x)[32], uint32_t (&t3)[3][16]) {
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    uint32_t h[2], md[2], lw[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const float v = x[2 * q + u];
+      const uint32_t hb = __float_as_uint(v) & 0xFFFF0000u;  // top 8 significant bits
+      const float r1 = v - __uint_as_float(hb);               // exact
+      const uint32_t mb = __float_as_uint(r1) & 0xFFFF0000u;
+      const float r2 = r1 - __uint_as_float(mb);              // exact, <= 8 bits left
+      h[u] = hb >> 16;
+      md[u] = mb >> 16;
+      lw[u] = __float_as_uint(r2) >> 16;                      // exact: low half is zero
+    }
+    t3[0][q] = h[0] | (h[1] << 16);
+    t3[1][q] = md[0] | (md[1] << 16);
+    t3[2][q] = lw[0] | (lw[1] << 16);
+  }
+}
+
+// K^I rows of a finished tile (accumulator `acc`): warps 0-3, thread = entry row
+__device__ __forceinline__ bool kt_epilogue(KtSmem& S, uint32_t tmem, int acc, uint32_t par, int64_t e0, int64_t n,
+                                            float* __restrict__ ki, int warp, int lane, volatile int* abort_flag,
+                                            void* ws) {
+  const bool landed = ptx::mbar_wait_warp(&S.done[acc], par, abort_flag, kKtWaitBudget);
+  if (!landed) {
+    if (lane == 0) report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 42);
+    return false;
+  }
+  ptx::tc_fence_after();
+  const int64_t e = e0 + warp * 32 + lane;
+  float4* dst = reinterpret_cast<float4*>(ki + e * kDIdx);
+#pragma unroll 1
+  for (int cb = 0; cb < 4; ++cb) {
+    uint32_t v[32];
+    ptx::tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)acc * 128u + (uint32_t)cb * 32u, v);
+    ptx::tmem_wait_ld();
+    if (e < n) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        dst[8 * cb + q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                      __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+    }
+  }
+  ptx::tc_fence_before();
+  __syncwarp();
+  if (lane == 0) ptx::mbar_arrive(&S.acc_free[acc]);  // the accumulator may take the tile after next
+  return true;
+}
+
 __global__ void __launch_bounds__(kKtThreads, 1)
-    k_cw_ki_tc(const __grid_constant__ CUtensorMap map_wt, const float* __restrict__ cbar, int64_t n,
+    k_cw_ki_tc(const __grid_constant__ CUtensorMap map_wt, const __grid_constant__ CUtensorMap map_cbar, int64_t n,
                float* __restrict__ ki, void* ws) {
   extern __shared__ __align__(1024) unsigned char kt_smem_raw[];
   KtSmem& S = *reinterpret_cast<KtSmem*>(kt_smem_raw);
   volatile int* abort_flag = &S.abort_flag;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const int64_t e0 = (int64_t)blockIdx.x * 128;
+  const int64_t ntiles = cdiv(n, (int64_t)128);
+  const int my = (int)((ntiles - (int64_t)blockIdx.x + gridDim.x - 1) / gridDim.x);  // this CTA's tiles
+  const int nch = 8 * my;                                                            // its chunks
+  auto tile_e0 = [&](int k) { return ((int64_t)blockIdx.x + (int64_t)k * gridDim.x) * 128; };
   if (tid == 0) {
     ptx::mbar_init(&S.b_full, 1);
-    ptx::mbar_init(&S.a_free[0], 1);
-    ptx::mbar_init(&S.a_free[1], 1);
-    ptx::mbar_init(&S.done, 1);
+    for (int i = 0; i < kKtStages; ++i) {
+      ptx::mbar_init(&S.x_full[i], 1);
+      ptx::mbar_init(&S.x_free[i], kKtStreamWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&S.a_full[i], kKtStreamWarps);
+      ptx::mbar_init(&S.a_free[i], 1);
+      ptx::mbar_init(&S.done[i], 1);
+      ptx::mbar_init(&S.acc_free[i], 4);  // the four read-out warps
+    }
+    ptx::mbar_init(&S.drain, 1);
     S.abort_flag = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 0) ptx::tmem_alloc(&S.tmem_base, 128);
+  if (warp == 0) ptx::tmem_alloc(&S.tmem_base, 512);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = S.tmem_base;
-  if (tid == 0) {
-    ptx::mbar_arrive_expect_tx(&S.b_full, 8 * 128 * 128);
-    for (int j = 0; j < 8; ++j) ptx::tma_load_2d(S.B[j], &map_wt, 64 * j, 0, &S.b_full);
-  }
-  // thread -> (entry r = tid / 2 .. in two passes, 32 channels = 4 chunks of 8)
-  bool ok = true;
-  for (int j = 0; j < 8; ++j) {
-    const int buf = j & 1;
-    // buffer `buf` is free once the MMAs of chunk j - 2 completed
-    if (j >= 2 && !ptx::mbar_wait(&S.a_free[buf], (uint32_t)((j - 2) >> 1) & 1u, abort_flag, kKtWaitBudget)) {
-      ok = false;
-      report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 43);
+  bool good = true;
+
+  if (warp == kKtLoadWarp) {
+    // ------------------------------------------------------------ Cbar loads
+    if (lane == 0 && my > 0) {
+      ptx::mbar_arrive_expect_tx(&S.b_full, 8 * 128 * 128);
+      for (int j = 0; j < 8; ++j) ptx::tma_load_2d(S.B[j], &map_wt, 64 * j, 0, &S.b_full);
+      const uint64_t pol = ptx::policy_evict_first();  // Cbar is read once
+      int s = 0;
+      uint32_t ph = 0;
+      for (int g = 0; g < nch; ++g) {
+        if (g >= kKtStages && !ptx::mbar_wait(&S.x_free[s], ph ^ 1u, abort_flag, kKtWaitBudget)) {
+          good = false;
+          break;
+        }
+        const int j = g & 7;
+        const int e0 = (int)tile_e0(g >> 3);
+        ptx::mbar_arrive_expect_tx(&S.x_full[s], 2 * 128 * 32 * 4);
+        ptx::tma_load_2d_hint(S.X[s][0], &map_cbar, 64 * j, e0, &S.x_full[s], pol);
+        ptx::tma_load_2d_hint(S.X[s][1], &map_cbar, 64 * j + 32, e0, &S.x_full[s], pol);
+        if (++s == kKtStages) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
     }
-    if (ok) {
-#pragma unroll
-      for (int pass = 0; pass < 2; ++pass) {
-        const int r = pass * 64 + tid / 4;  // entry row of the tile
-        const int c0 = (tid % 4) * 16;      // 16 channels: two 8-element chunks
-        const int64_t e = e0 + r;
-        float x[16];
-        if (e < n) {
-          const float4* src = reinterpret_cast<const float4*>(cbar + e * kDMain + 64 * j + c0);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float4 v = src[q];
-            x[4 * q] = v.x;
-            x[4 * q + 1] = v.y;
-            x[4 * q + 2] = v.z;
-            x[4 * q + 3] = v.w;
-          }
-        } else {
-#pragma unroll
-          for (int q = 0; q < 16; ++q) x[q] = 0.0f;
-        }
-        uint32_t t3[3][8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          uint32_t h[2], md[2], lw[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const float v = x[2 * q + u];
-            const uint32_t hb = __float_as_uint(v) & 0xFFFF0000u;      // top 8 significant bits
-            const float r1 = v - __uint_as_float(hb);                   // exact
-            const uint32_t mb = __float_as_uint(r1) & 0xFFFF0000u;
-            const float r2 = r1 - __uint_as_float(mb);                  // exact, <= 8 bits left
-            h[u] = hb >> 16;
-            md[u] = mb >> 16;
-            lw[u] = __float_as_uint(r2) >> 16;                          // exact: low half is zero
-          }
-          t3[0][q] = h[0] | (h[1] << 16);
-          t3[1][q] = md[0] | (md[1] << 16);
-          t3[2][q] = lw[0] | (lw[1] << 16);
-        }
+    __syncwarp();
+  } else if (warp == kKtMmaWarp) {
+    // ------------------------------------------------------------ MMA issue
+    good = my <= 0 || ptx::mbar_wait_warp(&S.b_full, 0, abort_flag, kKtWaitBudget);
+    constexpr uint32_t idesc = ptx::idesc_f16(128, 128, 1);
+    for (int k = 0; k < my && good; ++k) {
+      const int acc = k & 1;
+      // the accumulator's previous tile (k - 2) has been read out
+      if (k >= 2) good = ptx::mbar_wait_warp(&S.acc_free[acc], (uint32_t)((k - 2) >> 1) & 1u, abort_flag, kKtWaitBudget);
+      for (int j = 0; j < 8 && good; ++j) {
+        const int buf = j & 1;
+        const int g = 8 * k + j;
+        good = ptx::mbar_wait_warp(&S.a_full[buf], (uint32_t)(g >> 1) & 1u, abort_flag, kKtWaitBudget);
+        if (!good) break;
+        ptx::tc_fence_after();
+        const uint64_t bd = ptx::smem_desc_sw128(S.B[j], 1024);
 #pragma unroll
         for (int t = 0; t < 3; ++t)
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const int chunk = (c0 / 8) + cc;  // 16-byte chunk of the 128-byte row
-            uint8_t* dst = S.A[buf][t] + r * 128 + ((chunk ^ (r & 7)) << 4);
-            *reinterpret_cast<uint4*>(dst) =
-                make_uint4(t3[t][4 * cc], t3[t][4 * cc + 1], t3[t][4 * cc + 2], t3[t][4 * cc + 3]);
-          }
+          for (int kk = 0; kk < 4; ++kk)  // A: 8 columns (16 bf16) per K step; B: 32 bytes per K step
+            ptx::mma_f16_ts_elect(tmem + (uint32_t)acc * 128u, tmem + kKtAcol + 128u * buf + 32u * t + 8u * kk,
+                                  bd + (uint64_t)(2 * kk), idesc, (j | t | kk) ? 1u : 0u);
+        ptx::mma_commit_elect(&S.a_free[buf]);
+        if (j == 7) ptx::mma_commit_elect(&S.done[acc]);
       }
     }
-    ptx::fence_proxy_async_smem();
-    ok = __syncthreads_and(ok) != 0;
-    if (!ok) break;
-    if (tid == 0) {
-      if (j == 0 && !ptx::mbar_wait(&S.b_full, 0, abort_flag, kKtWaitBudget)) {
-        *abort_flag = 1;
-        report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 41);
-      } else {
+    // every MMA issued has completed before tensor memory is freed
+    ptx::mma_commit_elect(&S.drain);
+    volatile int keep_waiting = 0;
+    ptx::mbar_wait_warp(&S.drain, 0, &keep_waiting, kKtWaitBudget);
+  } else {
+    // ------------------------------------------------------------ split, read out
+    const int q4 = warp & 3, h = warp >> 2;   // lane quarter, channel half
+    const int r = 32 * q4 + lane;             // entry row of the tile
+    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+    int s = 0;
+    uint32_t ph = 0;
+    for (int k = 0; k < my && good; ++k) {
+      const int acc = k & 1;
+      for (int j = 0; j < 8; ++j) {
+        const int buf = j & 1;
+        const int g = 8 * k + j;
+        good = ptx::mbar_wait_warp(&S.x_full[s], ph, abort_flag, kKtWaitBudget);
+        if (!good) break;
+        float x[32];
+        const float* row = S.X[s][h] + r * 32;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {  // 16-byte chunk c of the row sits at slot c ^ (r % 8)
+          const float4 v = *reinterpret_cast<const float4*>(row + 4 * (c ^ (r & 7)));
+          x[4 * c] = v.x;
+          x[4 * c + 1] = v.y;
+          x[4 * c + 2] = v.z;
+          x[4 * c + 3] = v.w;
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&S.x_free[s]);
+        if (++s == kKtStages) {
+          s = 0;
+          ph ^= 1u;
+        }
+        uint32_t t3[3][16];
+        kt_split(x, t3);
+        // operand buffer `buf` is free once the MMAs of chunk g - 2 completed
+        if (g >= 2) good = ptx::mbar_wait_warp(&S.a_free[buf], (uint32_t)((g - 2) >> 1) & 1u, abort_flag, kKtWaitBudget);
+        if (!good) break;
         ptx::tc_fence_after();
-        constexpr uint32_t idesc = ptx::idesc_f16(128, 128, 1);
-        const uint64_t bd = ptx::smem_desc_sw128(S.B[j], 1024);
 #pragma unroll
-        for (int t = 0; t < 3; ++t) {
-          const uint64_t ad = ptx::smem_desc_sw128(S.A[buf][t], 1024);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            ptx::mma_f16_ss(tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc,
-                            (j | t | kk) ? 1u : 0u);
-        }
-        ptx::mma_commit(j == 7 ? &S.done : &S.a_free[buf]);
+        for (int t = 0; t < 3; ++t)
+          ptx::tmem_st_32x32b_x16(tmem + lane_base + kKtAcol + 128u * buf + 32u * t + 16u * h, t3[t]);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&S.a_full[buf]);
+        // the previous tile's K^I, read out while this tile's chunks run
+        if (j == 1 && k >= 1 && warp < 4)
+          good = kt_epilogue(S, tmem, acc ^ 1, (uint32_t)((k - 1) >> 1) & 1u, tile_e0(k - 1), n, ki, warp, lane,
+                             abort_flag, ws);
+        if (!good) break;
       }
     }
+    if (good && my > 0 && warp < 4)  // the last tile
+      good = kt_epilogue(S, tmem, (my - 1) & 1, (uint32_t)((my - 1) >> 1) & 1u, tile_e0(my - 1), n, ki, warp, lane,
+                         abort_flag, ws);
   }
-  // after a wait gave up: one commit tracks every MMA already issued, so the
-  // tensor memory is released only once they are done
-  if (!ok && tid == 0) ptx::mma_commit(&S.done);
-  // epilogue: thread = entry row (warps 0-3 own the four lane quarters)
-  if (warp < 4) {
-    const bool landed = ptx::mbar_wait_warp(&S.done, 0, abort_flag, kKtWaitBudget);
-    const bool fin = ok && landed;
-    if (!landed && lane == 0) report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 42);
-    ptx::tc_fence_after();
-    const int64_t e = e0 + warp * 32 + lane;
-    if (fin) {
-#pragma unroll 1
-      for (int cb = 0; cb < 4; ++cb) {
-        uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)cb * 32u, v);
-        ptx::tmem_wait_ld();
-        if (e < n) {
-          float4* dst = reinterpret_cast<float4*>(ki + e * kDIdx + cb * 32);
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                 __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-        }
-      }
-    }
+  if (!good && lane == 0 && !*abort_flag) {
+    *abort_flag = 1;
+    report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 41);
   }
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, 128);
+    ptx::tmem_dealloc(tmem, 512);
   }
 }
 
@@ -557,6 +635,20 @@ __global__ void __launch_bounds__(256) k_cw_wik_t(const uint16_t* __restrict__ W
   for (int i = ty; i < 32; i += 8) tile[i][tx] = Wik[(int64_t)(k0 + i) * kDIdx + o0 + tx];
   __syncthreads();
   for (int i = ty; i < 32; i += 8) Wt[(int64_t)(o0 + i) * kDMain + k0 + tx] = tile[tx][i];
+}
+
+// fp32 [rows][cols] in boxes of 32 columns x box_rows rows (128 bytes per box row), 128-byte swizzle;
+// rows beyond the tensor read as zeros
+bool make_f32_map(CUtensorMap* map, const float* base, int64_t rows, int64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+  cuuint32_t box[2] = {32, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool make_bf16_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, uint32_t box_rows) {
@@ -788,13 +880,18 @@ csa2_status cw_compute(const void* H_bf16, int64_t T, int32_t d_model, const voi
       KernelTimer timer("k_cw_wik_t", st);
       k_cw_wik_t<<<dim3(kDMain / 32, kDIdx / 32), 256, 0, st>>>((const uint16_t*)Wik_bf16, L.wikt);
     }
-    CUtensorMap map_wikt;
-    if (!make_bf16_map(&map_wikt, L.wikt, kDIdx, kDMain, kDIdx)) return CSA2_ERR_CUDA;
+    CUtensorMap map_wikt, map_cbar;
+    if (!make_bf16_map(&map_wikt, L.wikt, kDIdx, kDMain, kDIdx) || !make_f32_map(&map_cbar, L.cbar, n, kDMain, 128))
+      return CSA2_ERR_CUDA;
     const int smem = (int)sizeof(KtSmem);
     if (cudaFuncSetAttribute(k_cw_ki_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return CSA2_ERR_CUDA;
     KernelTimer timer("k_cw_ki_tc", st);
-    k_cw_ki_tc<<<(unsigned)cdiv(n, 128), kKtThreads, smem, st>>>(map_wikt, L.cbar, n, L.ki, ws);
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CSA2_ERR_CUDA;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t kt_tiles = cdiv(n, (int64_t)128);
+    k_cw_ki_tc<<<(unsigned)std::min<int64_t>(kt_tiles, sms), kKtThreads, smem, st>>>(map_wikt, map_cbar, n, L.ki, ws);
   }
   return CSA2_OK;
 }
