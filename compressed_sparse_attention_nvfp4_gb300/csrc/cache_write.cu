@@ -404,6 +404,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 //   warp 8     issues 3 x 4 MMAs (M128 N128 K16, A from tensor memory, W^T from
 //              shared memory) per chunk into one of two accumulators, so a
 //              tile's K^I is read out while the next tile's chunks run.
+// The codec runs here too: the read-out quantizes each K^I row (four MXFP4
+// groups of 32) straight into the indexer-key planes, and, when the main KV
+// takes neither RMSNorm nor RoPE, the split warps quantize each 16-channel group
+// of Cbar they read (E2M1 x E4M3) into the main-KV planes, so Cbar is read once.
+struct KtOut {
+  float* ki;                    // fp32 K^I [n][128], or null
+  uint8_t *ix_codes, *ix_scales;  // indexer-key planes, or null
+  uint8_t *kv_codes, *kv_scales;  // main-KV planes (plain codec), or null
+  QDest d;
+};
 constexpr int kKtStreamWarps = 8;
 constexpr int kKtMmaWarp = 8;
 constexpr int kKtLoadWarp = 9;
@@ -445,8 +455,7 @@ __device__ __forceinline__ void kt_split(const float (&x)[32], uint32_t (&t3)[3]
 
 // K^I rows of a finished tile (accumulator `acc`): warps 0-3, thread = entry row
 __device__ __forceinline__ bool kt_epilogue(KtSmem& S, uint32_t tmem, int acc, uint32_t par, int64_t e0, int64_t n,
-                                            float* __restrict__ ki, int warp, int lane, volatile int* abort_flag,
-                                            void* ws) {
+                                            const KtOut& o, int warp, int lane, volatile int* abort_flag, void* ws) {
   const bool landed = ptx::mbar_wait_warp(&S.done[acc], par, abort_flag, kKtWaitBudget);
   if (!landed) {
     if (lane == 0) report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 42);
@@ -454,17 +463,24 @@ __device__ __forceinline__ bool kt_epilogue(KtSmem& S, uint32_t tmem, int acc, u
   }
   ptx::tc_fence_after();
   const int64_t e = e0 + warp * 32 + lane;
-  float4* dst = reinterpret_cast<float4*>(ki + e * kDIdx);
+  const int64_t row = e < n && o.ix_codes ? dest_row(o.d, e) : -1;  // plane row of the entry
+  float4* dst = reinterpret_cast<float4*>(o.ki + e * kDIdx);
 #pragma unroll 1
   for (int cb = 0; cb < 4; ++cb) {
     uint32_t v[32];
     ptx::tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)acc * 128u + (uint32_t)cb * 32u, v);
     ptx::tmem_wait_ld();
-    if (e < n) {
+    if (e < n && o.ki) {
 #pragma unroll
       for (int q = 0; q < 8; ++q)
         dst[8 * cb + q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
                                       __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+    }
+    if (row >= 0) {  // MXFP4 group cb of the indexer key
+      float g[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) g[i] = __uint_as_float(v[i]);
+      quantize_index_group_vals(g, o.ix_codes + row * 64 + cb * 16, o.ix_scales + row * 4 + cb);
     }
   }
   ptx::tc_fence_before();
@@ -475,7 +491,7 @@ __device__ __forceinline__ bool kt_epilogue(KtSmem& S, uint32_t tmem, int acc, u
 
 __global__ void __launch_bounds__(kKtThreads, 1)
     k_cw_ki_tc(const __grid_constant__ CUtensorMap map_wt, const __grid_constant__ CUtensorMap map_cbar, int64_t n,
-               float* __restrict__ ki, void* ws) {
+               const __grid_constant__ KtOut o, void* ws) {
   extern __shared__ __align__(1024) unsigned char kt_smem_raw[];
   KtSmem& S = *reinterpret_cast<KtSmem*>(kt_smem_raw);
   volatile int* abort_flag = &S.abort_flag;
@@ -570,6 +586,8 @@ __global__ void __launch_bounds__(kKtThreads, 1)
     uint32_t ph = 0;
     for (int k = 0; k < my && good; ++k) {
       const int acc = k & 1;
+      const int64_t e = tile_e0(k) + r;
+      const int64_t mrow = e < n && o.kv_codes ? dest_row(o.d, e) : -1;  // main-KV plane row of the entry
       for (int j = 0; j < 8; ++j) {
         const int buf = j & 1;
         const int g = 8 * k + j;
@@ -591,6 +609,16 @@ __global__ void __launch_bounds__(kKtThreads, 1)
           s = 0;
           ph ^= 1u;
         }
+        if (mrow >= 0) {  // main-KV groups 4 j + 2 h and 4 j + 2 h + 1 of the entry
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            float gv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) gv[i] = x[16 * u + i];
+            const int grp = 4 * j + 2 * h + u;
+            quantize_main_group_vals(gv, o.kv_codes + mrow * 256 + grp * 8, o.kv_scales + mrow * 32 + grp);
+          }
+        }
         uint32_t t3[3][16];
         kt_split(x, t3);
         // operand buffer `buf` is free once the MMAs of chunk g - 2 completed
@@ -606,13 +634,13 @@ __global__ void __launch_bounds__(kKtThreads, 1)
         if (lane == 0) ptx::mbar_arrive(&S.a_full[buf]);
         // the previous tile's K^I, read out while this tile's chunks run
         if (j == 1 && k >= 1 && warp < 4)
-          good = kt_epilogue(S, tmem, acc ^ 1, (uint32_t)((k - 1) >> 1) & 1u, tile_e0(k - 1), n, ki, warp, lane,
+          good = kt_epilogue(S, tmem, acc ^ 1, (uint32_t)((k - 1) >> 1) & 1u, tile_e0(k - 1), n, o, warp, lane,
                              abort_flag, ws);
         if (!good) break;
       }
     }
     if (good && my > 0 && warp < 4)  // the last tile
-      good = kt_epilogue(S, tmem, (my - 1) & 1, (uint32_t)((my - 1) >> 1) & 1u, tile_e0(my - 1), n, ki, warp, lane,
+      good = kt_epilogue(S, tmem, (my - 1) & 1, (uint32_t)((my - 1) >> 1) & 1u, tile_e0(my - 1), n, o, warp, lane,
                          abort_flag, ws);
   }
   if (!good && lane == 0 && !*abort_flag) {
@@ -891,7 +919,13 @@ csa2_status cw_compute(const void* H_bf16, int64_t T, int32_t d_model, const voi
     if (cudaGetDevice(&dev) != cudaSuccess) return CSA2_ERR_CUDA;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t kt_tiles = cdiv(n, (int64_t)128);
-    k_cw_ki_tc<<<(unsigned)std::min<int64_t>(kt_tiles, sms), kKtThreads, smem, st>>>(map_wikt, map_cbar, n, L.ki, ws);
+    // the codec in the same pass: the indexer key always, the main KV when it takes no RMSNorm / RoPE
+    const bool main_here = !(nr && (nr->norm_weight || nr->rope));
+    const KtOut o{nullptr, dst->ix_codes, dst->ix_scales, main_here ? dst->kv_codes : nullptr,
+                  main_here ? dst->kv_scales : nullptr, d};
+    k_cw_ki_tc<<<(unsigned)std::min<int64_t>(kt_tiles, sms), kKtThreads, smem, st>>>(map_wikt, map_cbar, n, o, ws);
+    if (!main_here) launch_quantize(L.cbar, nullptr, n, dst, d, st, nr);
+    *written = true;
   }
   return CSA2_OK;
 }
