@@ -394,30 +394,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // fp32 additions differs from a sequential sum.  Persistent: one CTA per SM
 // keeps all of W_IK^T (128 outputs x 512, K-major, 128-byte swizzle) in shared
 // memory and runs tiles of 128 entries, 64 channels (a chunk) at a time:
-//   warp 9     tensor-loads each chunk of Cbar (fp32, two 32-channel boxes,
+//   warp 17    tensor-loads each chunk of Cbar (fp32, two 32-channel boxes,
 //              128-byte swizzle) into a three-stage ring;
-//   warps 0-7  thread = (entry row, 32-channel half): read the row's half from
-//              the ring, split it, and store the three bf16 terms as the MMA's A
-//              operand in tensor memory (row m at lane m, two bf16 per column;
-//              two buffers), so the operand never passes through shared memory;
-//              warps 0-3 also read each finished tile's K^I out;
-//   warp 8     issues 3 x 4 MMAs (M128 N128 K16, A from tensor memory, W^T from
+//   warps 0-15 thread = (entry row, 16-channel quarter): read the row's quarter
+//              from the ring, split it, and store the three bf16 terms as the
+//              MMA's A operand in tensor memory (row m at lane m, two bf16 per
+//              column; two buffers), so the operand never passes through shared
+//              memory; warps 0-3 also read each finished tile's K^I out;
+//   warp 16    issues 3 x 4 MMAs (M128 N128 K16, A from tensor memory, W^T from
 //              shared memory) per chunk into one of two accumulators, so a
 //              tile's K^I is read out while the next tile's chunks run.
 // The codec runs here too: the read-out quantizes each K^I row (four MXFP4
 // groups of 32) straight into the indexer-key planes, and, when the main KV
 // takes neither RMSNorm nor RoPE, the split warps quantize each 16-channel group
 // of Cbar they read (E2M1 x E4M3) into the main-KV planes, so Cbar is read once.
+// Sixteen split warps (four per scheduler) hide the latency of that arithmetic.
 struct KtOut {
   float* ki;                    // fp32 K^I [n][128], or null
   uint8_t *ix_codes, *ix_scales;  // indexer-key planes, or null
   uint8_t *kv_codes, *kv_scales;  // main-KV planes (plain codec), or null
   QDest d;
 };
-constexpr int kKtStreamWarps = 8;
-constexpr int kKtMmaWarp = 8;
-constexpr int kKtLoadWarp = 9;
-constexpr int kKtThreads = 10 * 32;
+constexpr int kKtStreamWarps = 16;
+constexpr int kKtMmaWarp = 16;
+constexpr int kKtLoadWarp = 17;
+constexpr int kKtThreads = 18 * 32;
+// five warps share two of the schedulers, whose 16 K registers then allow 102 per thread: the
+// bound below makes the compiler keep to that
+constexpr int kKtBoundThreads = 20 * 32;
 constexpr int kKtStages = 3;
 constexpr uint32_t kKtAcol = 256;  // A operand buffer u: columns 256 + 128 u (term t: + 32 t)
 constexpr long long kKtWaitBudget = 1LL << 32;
@@ -430,11 +434,11 @@ struct __align__(1024) KtSmem {
   int abort_flag;
 };
 
-// Splits 32 fp32 values into the hi / mid / lo bf16 terms, packed in pairs
+// Splits 16 fp32 values into the hi / mid / lo bf16 terms, packed in pairs
 // (element 2c in the low half of word c).
-__device__ __forceinline__ void kt_split(const float (&x)[32], uint32_t (&t3)[3][16]) {
+__device__ __forceinline__ void kt_split(const float (&x)[16], uint32_t (&t3)[3][8]) {
 #pragma unroll
-  for (int q = 0; q < 16; ++q) {
+  for (int q = 0; q < 8; ++q) {
     uint32_t h[2], md[2], lw[2];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
@@ -489,7 +493,7 @@ __device__ __forceinline__ bool kt_epilogue(KtSmem& S, uint32_t tmem, int acc, u
   return true;
 }
 
-__global__ void __launch_bounds__(kKtThreads, 1)
+__global__ void __launch_bounds__(kKtBoundThreads, 1)
     k_cw_ki_tc(const __grid_constant__ CUtensorMap map_wt, const __grid_constant__ CUtensorMap map_cbar, int64_t n,
                const __grid_constant__ KtOut o, void* ws) {
   extern __shared__ __align__(1024) unsigned char kt_smem_raw[];
@@ -579,7 +583,8 @@ __global__ void __launch_bounds__(kKtThreads, 1)
     ptx::mbar_wait_warp(&S.drain, 0, &keep_waiting, kKtWaitBudget);
   } else {
     // ------------------------------------------------------------ split, read out
-    const int q4 = warp & 3, h = warp >> 2;   // lane quarter, channel half
+    const int q4 = warp & 3, cq = warp >> 2;  // lane quarter, 16-channel quarter of the chunk
+    const int h = cq >> 1, sub = cq & 1;      // the quarter's half of the ring row, and which 16 of its 32
     const int r = 32 * q4 + lane;             // entry row of the tile
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
     int s = 0;
@@ -593,15 +598,16 @@ __global__ void __launch_bounds__(kKtThreads, 1)
         const int g = 8 * k + j;
         good = ptx::mbar_wait_warp(&S.x_full[s], ph, abort_flag, kKtWaitBudget);
         if (!good) break;
-        float x[32];
+        float x[16];
         const float* row = S.X[s][h] + r * 32;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {  // 16-byte chunk c of the row sits at slot c ^ (r % 8)
+        for (int i = 0; i < 4; ++i) {  // 16-byte chunk c of the row sits at slot c ^ (r % 8)
+          const int c = 4 * sub + i;
           const float4 v = *reinterpret_cast<const float4*>(row + 4 * (c ^ (r & 7)));
-          x[4 * c] = v.x;
-          x[4 * c + 1] = v.y;
-          x[4 * c + 2] = v.z;
-          x[4 * c + 3] = v.w;
+          x[4 * i] = v.x;
+          x[4 * i + 1] = v.y;
+          x[4 * i + 2] = v.z;
+          x[4 * i + 3] = v.w;
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&S.x_free[s]);
@@ -609,17 +615,11 @@ __global__ void __launch_bounds__(kKtThreads, 1)
           s = 0;
           ph ^= 1u;
         }
-        if (mrow >= 0) {  // main-KV groups 4 j + 2 h and 4 j + 2 h + 1 of the entry
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            float gv[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) gv[i] = x[16 * u + i];
-            const int grp = 4 * j + 2 * h + u;
-            quantize_main_group_vals(gv, o.kv_codes + mrow * 256 + grp * 8, o.kv_scales + mrow * 32 + grp);
-          }
+        if (mrow >= 0) {  // main-KV group 4 j + cq of the entry
+          const int grp = 4 * j + cq;
+          quantize_main_group_vals(x, o.kv_codes + mrow * 256 + grp * 8, o.kv_scales + mrow * 32 + grp);
         }
-        uint32_t t3[3][16];
+        uint32_t t3[3][8];
         kt_split(x, t3);
         // operand buffer `buf` is free once the MMAs of chunk g - 2 completed
         if (g >= 2) good = ptx::mbar_wait_warp(&S.a_free[buf], (uint32_t)((g - 2) >> 1) & 1u, abort_flag, kKtWaitBudget);
@@ -627,7 +627,7 @@ __global__ void __launch_bounds__(kKtThreads, 1)
         ptx::tc_fence_after();
 #pragma unroll
         for (int t = 0; t < 3; ++t)
-          ptx::tmem_st_32x32b_x16(tmem + lane_base + kKtAcol + 128u * buf + 32u * t + 16u * h, t3[t]);
+          ptx::tmem_st_32x32b_x8(tmem + lane_base + kKtAcol + 128u * buf + 32u * t + 8u * cq, t3[t]);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();

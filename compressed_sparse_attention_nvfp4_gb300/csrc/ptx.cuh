@@ -343,6 +343,13 @@ __host__ __device__ constexpr uint32_t idesc_block_scaled(uint32_t M, uint32_t N
 }
 
 // one 32-bit column of this warp's lane quarter: thread i <-> lane i
+// 32 lanes x 8 columns (this warp's lane quarter): thread i <-> lane i
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t* v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
 // 32 lanes x 16 columns (this warp's lane quarter): thread i <-> lane i
 __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t* v) {
   asm volatile(
