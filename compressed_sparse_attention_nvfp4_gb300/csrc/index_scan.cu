@@ -19,8 +19,10 @@
 // least 2^-9 of its block maximum this is exact (hi holds the top four
 // significant bits, lo the remaining four of bf16's eight); smaller elements
 // are off by at most 2^-17 of the block maximum.  The halves are stacked along
-// N (rows 0-31 hi, 32-63 lo of each head), so one MMA per 32-element K step
-// covers both, and the epilogue adds the two columns of each head.
+// N (rows 0-31 hi, 32-63 lo of each head) in shared memory; per 32-element K
+// step one MMA takes the hi rows and a second the lo rows into the same 32
+// accumulator columns (both halves have the same scales), so the accumulator
+// holds hi + lo and the epilogue reads one column per head.
 //
 // One CTA streams a contiguous range of 128-entry tiles of one query (or, in
 // pool mode, tiles of 16 pool blocks x 8 entries).  Warp roles:
@@ -28,16 +30,17 @@
 //               scale words (one bulk copy, 512 B) into a shared-memory ring;
 //   warps 1, 7  MMA issue, even and odd tiles (warp 1 also allocates tensor
 //               memory): one thread copies the tile's scales into tensor
-//               memory (tcgen05.cp) and issues the four MMAs
-//               D[128 entries x 64] += A[128 x 32] * B[64 x 32]^T, both
+//               memory (tcgen05.cp) and issues per K step two MMAs
+//               D[128 entries x 32] += A[128 x 32] * B[32 x 32]^T (the hi
+//               rows, then the lo rows; one for an MXFP4 query), both
 //               operands read from shared memory, into one of three
 //               accumulators (tile i -> i mod 3); two issuers and three
 //               accumulators keep the tensor core fed while the epilogue
 //               drains earlier tiles;
 //   warp 2      reorders the tile's 128 scale words into the layout the copy
 //               replicates into the four lane quarters of tensor memory;
-//   warps 3-6   epilogue: read the row's 64 half-dots from tensor memory,
-//               dot_h = hi_h + lo_h, score = sum_h w_h max(dot_h, 0) (packed
+//   warps 3-6   epilogue: read the row's 32 dots from tensor memory,
+//               score = sum_h w_h max(dot_h, 0) (packed
 //               f32x2 arithmetic); write the score and/or the max of each
 //               8-entry block.
 // Every mbarrier wait is bounded; a wait that gives up records
@@ -132,14 +135,6 @@ struct Ring {
 };
 
 // packed fp32 pairs (one instruction for two lanes of arithmetic)
-__device__ __forceinline__ float2 add_f32x2(float2 a, float2 b) {
-  float2 r;
-  asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
-      "add.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
-      : "=f"(r.x), "=f"(r.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return r;
-}
 __device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c) {
   float2 r;
   asm("{\n\t.reg .b64 x, y, z, d;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
@@ -364,11 +359,15 @@ __global__ void __launch_bounds__(kThreads, 2)
           const uint32_t d_t = tmem + kDCol0 + (uint32_t)a * 64u;
           ptx::tmem_cp_32x128b_warpx4(sfa_t, ptx::smem_desc_noswizzle(S.sfT[s], 128, 128));
           const uint64_t ads = ad0 + (uint64_t)(s * (kTile * 128 / 16));
+          // per K step: the hi rows (0-31 of the B tile), then the lo rows (32-63, 512 bytes on)
+          // into the same 32 columns: hi + lo adds in the accumulator (both halves share
+          // their scales)
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            const uint32_t idesc =
-                ptx::idesc_block_scaled(128, hi_only ? 32 : 64, ptx::kFmtE2M1, ptx::kFmtE4M3, ks, ks);
+            const uint32_t idesc = ptx::idesc_block_scaled(128, 32, ptx::kFmtE2M1, ptx::kFmtE4M3, ks, ks);
             ptx::mma_mxf8f6f4_ss(d_t, ads + (uint64_t)(2 * ks), bd[ks], idesc, sfa_t, sfb_t, ks > 0 ? 1u : 0u);
+            if (!hi_only)
+              ptx::mma_mxf8f6f4_ss(d_t, ads + (uint64_t)(2 * ks), bd[ks] + (uint64_t)(512 / 16), idesc, sfa_t, sfb_t, 1u);
           }
           ptx::mma_commit(&S.tile_done[s]);
         }
@@ -425,45 +424,26 @@ __global__ void __launch_bounds__(kThreads, 2)
           break;
         }
         ptx::tc_fence_after();
-        // dot_h = hi_h + lo_h; the accumulator is released as soon as it is read
-        uint32_t hi[32], lo[32];
+        // dot_h (hi + lo summed by the MMAs); the accumulator is released as soon as it is read
+        uint32_t hi[32];
         const uint32_t d_addr = lane_addr + kDCol0 + (uint32_t)a * 64u;
         ptx::tmem_ld_32x32b_x16(d_addr, hi);
         ptx::tmem_ld_32x32b_x16(d_addr + 16u, hi + 16);
-        if (!hi_only) {
-          ptx::tmem_ld_32x32b_x16(d_addr + 32u, lo);
-          ptx::tmem_ld_32x32b_x16(d_addr + 48u, lo + 16);
-        }
         ptx::tmem_wait_ld();
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&S.d_free[a]);
         // sum_h w_h max(dot_h, 0) on head pairs, two accumulators
         float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
-        if (hi_only) {
 #pragma unroll
-          for (int h4 = 0; h4 < 8; ++h4) {
-            const float4 wv = make_float4(wr[4 * h4], wr[4 * h4 + 1], wr[4 * h4 + 2], wr[4 * h4 + 3]);
-            const float2 x01 = make_float2(fmaxf(__uint_as_float(hi[4 * h4]), 0.0f),
-                                           fmaxf(__uint_as_float(hi[4 * h4 + 1]), 0.0f));
-            const float2 x23 = make_float2(fmaxf(__uint_as_float(hi[4 * h4 + 2]), 0.0f),
-                                           fmaxf(__uint_as_float(hi[4 * h4 + 3]), 0.0f));
-            acc0 = fma_f32x2(make_float2(wv.x, wv.y), x01, acc0);
-            acc1 = fma_f32x2(make_float2(wv.z, wv.w), x23, acc1);
-          }
-        } else {
-#pragma unroll
-          for (int h4 = 0; h4 < 8; ++h4) {
-            const float4 wv = make_float4(wr[4 * h4], wr[4 * h4 + 1], wr[4 * h4 + 2], wr[4 * h4 + 3]);
-            float2 x01 = add_f32x2(make_float2(__uint_as_float(hi[4 * h4]), __uint_as_float(hi[4 * h4 + 1])),
-                                   make_float2(__uint_as_float(lo[4 * h4]), __uint_as_float(lo[4 * h4 + 1])));
-            float2 x23 = add_f32x2(make_float2(__uint_as_float(hi[4 * h4 + 2]), __uint_as_float(hi[4 * h4 + 3])),
-                                   make_float2(__uint_as_float(lo[4 * h4 + 2]), __uint_as_float(lo[4 * h4 + 3])));
-            x01 = make_float2(fmaxf(x01.x, 0.0f), fmaxf(x01.y, 0.0f));
-            x23 = make_float2(fmaxf(x23.x, 0.0f), fmaxf(x23.y, 0.0f));
-            acc0 = fma_f32x2(make_float2(wv.x, wv.y), x01, acc0);
-            acc1 = fma_f32x2(make_float2(wv.z, wv.w), x23, acc1);
-          }
+        for (int h4 = 0; h4 < 8; ++h4) {
+          const float4 wv = make_float4(wr[4 * h4], wr[4 * h4 + 1], wr[4 * h4 + 2], wr[4 * h4 + 3]);
+          const float2 x01 = make_float2(fmaxf(__uint_as_float(hi[4 * h4]), 0.0f),
+                                         fmaxf(__uint_as_float(hi[4 * h4 + 1]), 0.0f));
+          const float2 x23 = make_float2(fmaxf(__uint_as_float(hi[4 * h4 + 2]), 0.0f),
+                                         fmaxf(__uint_as_float(hi[4 * h4 + 3]), 0.0f));
+          acc0 = fma_f32x2(make_float2(wv.x, wv.y), x01, acc0);
+          acc1 = fma_f32x2(make_float2(wv.z, wv.w), x23, acc1);
         }
         const float sum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
 
