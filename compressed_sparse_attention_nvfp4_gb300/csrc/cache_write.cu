@@ -392,8 +392,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // bits), so Cbar = hi + mid + lo exactly, and W_IK is bf16 already.  The three
 // terms are three MMA sets into one fp32 accumulator; only the order of the
 // fp32 additions differs from a sequential sum.  Persistent: one CTA per SM
-// keeps all of W_IK^T (128 outputs x 512, K-major, 128-byte swizzle) in shared
-// memory and runs tiles of 128 entries, 64 channels (a chunk) at a time:
+// keeps all of W_IK in shared memory as the MMA's N-major B operand (tensor-loaded
+// as given, [512 channels][128 outputs], 64-output blocks with 128-byte swizzle)
+// and runs tiles of 128 entries, 64 channels (a chunk) at a time:
 //   warp 17    tensor-loads each chunk of Cbar (fp32, two 32-channel boxes,
 //              128-byte swizzle) into a three-stage ring;
 //   warps 0-15 thread = (entry row, 16-channel quarter): read the row's quarter
@@ -401,7 +402,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 //              MMA's A operand in tensor memory (row m at lane m, two bf16 per
 //              column; two buffers), so the operand never passes through shared
 //              memory; warps 0-3 also read each finished tile's K^I out;
-//   warp 16    issues 3 x 4 MMAs (M128 N128 K16, A from tensor memory, W^T from
+//   warp 16    issues 3 x 4 MMAs (M128 N128 K16, A from tensor memory, W from
 //              shared memory) per chunk into one of two accumulators, so a
 //              tile's K^I is read out while the next tile's chunks run.
 // The codec runs here too: the read-out quantizes each K^I row (four MXFP4
@@ -427,7 +428,7 @@ constexpr uint32_t kKtAcol = 256;  // A operand buffer u: columns 256 + 128 u (t
 constexpr long long kKtWaitBudget = 1LL << 32;
 
 struct __align__(1024) KtSmem {
-  uint8_t B[8][128 * 128];                 // W_IK^T chunk j: 128 outputs x 64 channels
+  uint8_t B[8][128 * 128];                 // W_IK chunk j: channels 64 j .. + 63, outputs 0-63 | 64-127
   float X[kKtStages][2][128 * 32];         // Cbar chunk: [half][row][32 channels], 128-byte swizzle
   uint64_t b_full, x_full[kKtStages], x_free[kKtStages], a_full[2], a_free[2], done[2], acc_free[2], drain;
   uint32_t tmem_base;
@@ -494,7 +495,7 @@ __device__ __forceinline__ bool kt_epilogue(KtSmem& S, uint32_t tmem, int acc, u
 }
 
 __global__ void __launch_bounds__(kKtBoundThreads, 1)
-    k_cw_ki_tc(const __grid_constant__ CUtensorMap map_wt, const __grid_constant__ CUtensorMap map_cbar, int64_t n,
+    k_cw_ki_tc(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_cbar, int64_t n,
                const __grid_constant__ KtOut o, void* ws) {
   extern __shared__ __align__(1024) unsigned char kt_smem_raw[];
   KtSmem& S = *reinterpret_cast<KtSmem*>(kt_smem_raw);
@@ -531,7 +532,10 @@ __global__ void __launch_bounds__(kKtBoundThreads, 1)
     // ------------------------------------------------------------ Cbar loads
     if (lane == 0 && my > 0) {
       ptx::mbar_arrive_expect_tx(&S.b_full, 8 * 128 * 128);
-      for (int j = 0; j < 8; ++j) ptx::tma_load_2d(S.B[j], &map_wt, 64 * j, 0, &S.b_full);
+      for (int j = 0; j < 8; ++j) {  // two 64-output blocks of 64 channel rows each
+        ptx::tma_load_2d(S.B[j], &map_w, 0, 64 * j, &S.b_full);
+        ptx::tma_load_2d(S.B[j] + 8192, &map_w, 64, 64 * j, &S.b_full);
+      }
       const uint64_t pol = ptx::policy_evict_first();  // Cbar is read once
       int s = 0;
       uint32_t ph = 0;
@@ -555,7 +559,7 @@ __global__ void __launch_bounds__(kKtBoundThreads, 1)
   } else if (warp == kKtMmaWarp) {
     // ------------------------------------------------------------ MMA issue
     good = my <= 0 || ptx::mbar_wait_warp(&S.b_full, 0, abort_flag, kKtWaitBudget);
-    constexpr uint32_t idesc = ptx::idesc_f16(128, 128, 1);
+    constexpr uint32_t idesc = ptx::idesc_f16(128, 128, 1) | ptx::kIdescBMajorMN;
     for (int k = 0; k < my && good; ++k) {
       const int acc = k & 1;
       // the accumulator's previous tile (k - 2) has been read out
@@ -566,13 +570,14 @@ __global__ void __launch_bounds__(kKtBoundThreads, 1)
         good = ptx::mbar_wait_warp(&S.a_full[buf], (uint32_t)(g >> 1) & 1u, abort_flag, kKtWaitBudget);
         if (!good) break;
         ptx::tc_fence_after();
-        const uint64_t bd = ptx::smem_desc_sw128(S.B[j], 1024);
+        // B N-major: the two 64-output blocks 8 KB apart, 8-row K groups 1 KB apart
+        const uint64_t bd = ptx::smem_desc_sw128_mn(S.B[j], 8192, 1024);
 #pragma unroll
         for (int t = 0; t < 3; ++t)
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)  // A: 8 columns (16 bf16) per K step; B: 32 bytes per K step
+          for (int kk = 0; kk < 4; ++kk)  // A: 8 columns (16 bf16) per K step; B: 16 rows (2 KB) per K step
             ptx::mma_f16_ts_elect(tmem + (uint32_t)acc * 128u, tmem + kKtAcol + 128u * buf + 32u * t + 8u * kk,
-                                  bd + (uint64_t)(2 * kk), idesc, (j | t | kk) ? 1u : 0u);
+                                  bd + (uint64_t)(128 * kk), idesc, (j | t | kk) ? 1u : 0u);
         ptx::mma_commit_elect(&S.a_free[buf]);
         if (j == 7) ptx::mma_commit_elect(&S.done[acc]);
       }
@@ -653,16 +658,6 @@ __global__ void __launch_bounds__(kKtBoundThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
   }
-}
-
-// W_IK^T [128][512] bf16 (K-major) from W_IK [512][128]
-__global__ void __launch_bounds__(256) k_cw_wik_t(const uint16_t* __restrict__ Wik, uint16_t* __restrict__ Wt) {
-  __shared__ uint16_t tile[32][33];
-  const int k0 = blockIdx.x * 32, o0 = blockIdx.y * 32;
-  const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
-  for (int i = ty; i < 32; i += 8) tile[i][tx] = Wik[(int64_t)(k0 + i) * kDIdx + o0 + tx];
-  __syncthreads();
-  for (int i = ty; i < 32; i += 8) Wt[(int64_t)(o0 + i) * kDMain + k0 + tx] = tile[tx][i];
 }
 
 // fp32 [rows][cols] in boxes of 32 columns x box_rows rows (128 bytes per box row), 128-byte swizzle;
@@ -781,7 +776,6 @@ struct CwWs {
   float* cbar;
   float* ki;
   uint16_t* wt;  // transposed weights (long inputs only)
-  uint16_t* wikt;
   float* part;  // split-K partial C and Z [ksplit][T][1024] (few tokens only)
   int ksplit;
   size_t bytes;
@@ -815,8 +809,6 @@ CwWs cw_ws_layout(void* ws, int64_t n, int64_t d_model, int m = 1) {
     L.wt = (uint16_t*)(base ? base + off : nullptr);
     off += align_up((size_t)2 * kDMain * d_model * 2, 256);
   }
-  L.wikt = (uint16_t*)(base ? base + off : nullptr);
-  off += align_up((size_t)kDIdx * kDMain * 2, 256);
   L.part = nullptr;
   if (L.ksplit > 1) {
     L.part = (float*)(base ? base + off : nullptr);
@@ -904,12 +896,8 @@ csa2_status cw_compute(const void* H_bf16, int64_t T, int32_t d_model, const voi
   }
   {
     // K^I on the tensor cores (exact three-way bf16 split of Cbar)
-    {
-      KernelTimer timer("k_cw_wik_t", st);
-      k_cw_wik_t<<<dim3(kDMain / 32, kDIdx / 32), 256, 0, st>>>((const uint16_t*)Wik_bf16, L.wikt);
-    }
-    CUtensorMap map_wikt, map_cbar;
-    if (!make_bf16_map(&map_wikt, L.wikt, kDIdx, kDMain, kDIdx) || !make_f32_map(&map_cbar, L.cbar, n, kDMain, 128))
+    CUtensorMap map_wik, map_cbar;  // W_IK as given: [512][128], 64 x 64 boxes
+    if (!make_bf16_map(&map_wik, Wik_bf16, kDMain, kDIdx, 64) || !make_f32_map(&map_cbar, L.cbar, n, kDMain, 128))
       return CSA2_ERR_CUDA;
     const int smem = (int)sizeof(KtSmem);
     if (cudaFuncSetAttribute(k_cw_ki_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
@@ -923,7 +911,7 @@ csa2_status cw_compute(const void* H_bf16, int64_t T, int32_t d_model, const voi
     const bool main_here = !(nr && (nr->norm_weight || nr->rope));
     const KtOut o{nullptr, dst->ix_codes, dst->ix_scales, main_here ? dst->kv_codes : nullptr,
                   main_here ? dst->kv_scales : nullptr, d};
-    k_cw_ki_tc<<<(unsigned)std::min<int64_t>(kt_tiles, sms), kKtThreads, smem, st>>>(map_wikt, map_cbar, n, o, ws);
+    k_cw_ki_tc<<<(unsigned)std::min<int64_t>(kt_tiles, sms), kKtThreads, smem, st>>>(map_wik, map_cbar, n, o, ws);
     if (!main_here) launch_quantize(L.cbar, nullptr, n, dst, d, st, nr);
     *written = true;
   }
