@@ -203,6 +203,37 @@ def test_gaussian_banded_norm_rope(oracle_mod, T, d, m):
     assert f1 > 0.8 * (f1 + b1) and f2 > 0.8 * (f2 + b2), (f1, b1, f2, b2)
 
 
+def test_many_tiles_ragged_sampled(oracle_mod):
+    """K^I and the fused codec with several 128-entry tiles per CTA and a ragged last tile
+    (40,000 entries: 313 tiles on at most a few hundred CTAs, the last one half full):
+    sampled entries, among them every row of the last tile's edge, each against the
+    oracle's write of its own two tokens, exact in every decided group."""
+    T, d, m = 80000, 1024, 2
+    H, Wkv, Wz, Wik = W.cache_write_inputs(5, T, d)
+    n = T // m
+    P = csa2.Planes.empty(1, n)
+    ws = csa2.workspace(csa2.cache_write_workspace_size(T, d, m))
+    csa2.cache_write(to_dev(H.view(np.int16)), T, d, to_dev(Wkv.view(np.int16)), to_dev(Wz.view(np.int16)),
+                     to_dev(Wik.view(np.int16)), m, P, 0, 0, ws)
+    assert csa2.check(ws)[0] == 0
+    got = [t.cpu().numpy() for t in (P.kv_codes, P.kv_scales, P.ix_codes, P.ix_scales)]
+    e4m3_mids = np.array([0.5 * (oracle_mod.e4m3_value(c) + oracle_mod.e4m3_value(c + 1)) for c in range(126)])
+    rng = np.random.default_rng(12)
+    picks = [0, 127, 128, n - 65, n - 64, n - 2, n - 1] + [int(v) for v in rng.integers(1, n - 1, 25)]
+    f1 = b1 = f2 = b2 = 0
+    for j in picks:
+        Hs = H[j * m:(j + 1) * m]
+        kvc, kvs, ixc, ixs, cb, ki, _ = oracle_mod.cache_write(Hs, Wkv, Wz, Wik, m, return_prequant=True)
+        eCb, eKI = _error_bounds(Hs, Wkv, Wz, Wik, m, cb)
+        cb32 = cb.astype(np.float32).astype(np.float64)
+        ki32 = ki.astype(np.float32).astype(np.float64)
+        a, b = _group_bytes_ok(got[0][j:j + 1], got[1][j:j + 1], kvc, kvs,
+                               _decided_main(cb32, eCb, e4m3_mids, oracle_mod), 8)
+        c, e = _group_bytes_ok(got[2][j:j + 1], got[3][j:j + 1], ixc, ixs, _decided_index(ki32, eKI), 16)
+        f1, b1, f2, b2 = f1 + a, b1 + b, f2 + c, b2 + e
+    assert f1 > 0.8 * (f1 + b1) and f2 > 0.8 * (f2 + b2), (f1, b1, f2, b2)
+
+
 def test_full_size_sampled(oracle_mod):
     """The benchmarked prefill write (T = 131,072 tokens, d_model 5120, m = 2: the
     transposed-weight path of the projection): sampled entries, each against the
