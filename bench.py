@@ -1065,22 +1065,33 @@ def run_ours(args, rank, world, local_rank):
         lse = torch.empty((B, 64), dtype=torch.float32, device=dev)
         ws_i = csa2.workspace(csa2.index_topk_workspace_size(B, N, K_TOP, BLOCK, KEEP), dev)
         ws_a = csa2.workspace(csa2.sparse_attn_workspace_size(B, K_TOP, NSWA), dev)
+        # a second batch's buffers: two independent batches in flight on two streams, as a
+        # server keeps two micro-batches of decode requests in flight
+        st2 = torch.cuda.Stream(device=dev)
+        bufs = [dict(topk=topk, pool=pool, out=out, lse=lse, ws_i=ws_i, ws_a=ws_a, st=st),
+                dict(topk=torch.empty_like(topk), pool=torch.empty_like(pool), out=torch.empty_like(out),
+                     lse=torch.empty_like(lse), ws_i=csa2.workspace(ws_i.numel(), dev),
+                     ws_a=csa2.workspace(ws_a.numel(), dev), st=st2)]
     torch.cuda.synchronize()
     scale = 1.0 / math.sqrt(512)
 
-    def index_call():
-        csa2.index_topk(planes, B, ne, N, qd, wd, K_TOP, csa2.TOPK_HIER_BUILD, topk, ws_i, BLOCK, KEEP,
-                        pool_out=pool, stream=st)
+    def index_call(bf=None):
+        bf = bf or bufs[0]
+        csa2.index_topk(planes, B, ne, N, qd, wd, K_TOP, csa2.TOPK_HIER_BUILD, bf["topk"], bf["ws_i"], BLOCK,
+                        KEEP, pool_out=bf["pool"], stream=bf["st"])
 
-    def attn_call():
-        csa2.sparse_attn_decode(planes, B, topk, K_TOP, swa_d, NSWA, qa_d, scale, out, ws_a,
-                                lse_out=lse, stream=st)
+    def attn_call(bf=None):
+        bf = bf or bufs[0]
+        csa2.sparse_attn_decode(planes, B, bf["topk"], K_TOP, swa_d, NSWA, qa_d, scale, bf["out"], bf["ws_a"],
+                                lse_out=bf["lse"], stream=bf["st"])
 
     for _ in range(args.warmup):
-        index_call()
-        attn_call()
+        for bf in bufs:
+            index_call(bf)
+            attn_call(bf)
     torch.cuda.synchronize()
-    assert csa2.check(ws_i, st)[0] == 0 and csa2.check(ws_a, st)[0] == 0
+    for bf in bufs:
+        assert csa2.check(bf["ws_i"], bf["st"])[0] == 0 and csa2.check(bf["ws_a"], bf["st"])[0] == 0
 
     def barrier():
         if world > 1:
@@ -1089,22 +1100,37 @@ def run_ours(args, rank, world, local_rank):
             dist.barrier()
 
     # timed region: K steps bracketed by one pair of events (nothing else recorded
-    # between the kernels, so their launches overlap as in production)
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # between the kernels, so their launches overlap as in production).  Step s runs
+    # batch s % 2 on stream s % 2: two independent batches in flight, so one batch's
+    # latency-bound selects and attention overlap the other's HBM-bound scan
+    def timed(k, in_flight):
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        st2.wait_event(a)
+        for s in range(k):
+            bf = bufs[s % in_flight]
+            index_call(bf)
+            attn_call(bf)
+        j = torch.cuda.Event()
+        j.record(st2)
+        st.wait_event(j)
+        z.record(st)
+        return a, z
+
     with clock_sampler(local_rank) as clk:
         barrier()
         torch.cuda.synchronize()
         clk.mark()
-        start.record(st)
-        for s in range(args.steps):
-            index_call()
-            attn_call()
-        stop.record(st)
+        start, stop = timed(args.steps, 2)
         torch.cuda.synchronize()
         clk.stop()
         barrier()
     elapsed_ms = start.elapsed_time(stop)
     clocks = clk.summary()
+    # the same K steps with one batch in flight (each step waits for the one before)
+    a1, z1 = timed(args.steps, 1)
+    torch.cuda.synchronize()
+    serial_ms = a1.elapsed_time(z1)
 
     # instrumented pass over the same K steps: events around each call, and the
     # library's per-kernel events (each adds a few microseconds at a kernel
@@ -1137,8 +1163,8 @@ def run_ours(args, rank, world, local_rank):
     d2h = out.numel() * 4 + lse.numel() * 4
     up_s, down_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     sets = []
-    for _ in range(2):
-        sets.append({"q": torch.empty_like(qd), "w": torch.empty_like(wd), "qa": torch.empty_like(qa_d),
+    for i in range(2):
+        sets.append({"bf": bufs[i], "q": torch.empty_like(qd), "w": torch.empty_like(wd), "qa": torch.empty_like(qa_d),
                      "swa": torch.empty_like(swa_d), "out": torch.empty_like(out), "lse": torch.empty_like(lse),
                      "h_out": torch.empty(out.shape, dtype=torch.float32).pin_memory(),
                      "h_lse": torch.empty(lse.shape, dtype=torch.float32).pin_memory(),
@@ -1147,6 +1173,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e_start.record(st)
     up_s.wait_event(e_start)
+    st2.wait_event(e_start)
     for s_i in range(args.steps):
         S = sets[s_i % 2]
         with torch.cuda.stream(up_s):
@@ -1157,14 +1184,15 @@ def run_ours(args, rank, world, local_rank):
             S["qa"].copy_(h_qa, non_blocking=True)
             S["swa"].copy_(h_swa, non_blocking=True)
             S["up"].record(up_s)
-        st.wait_event(S["up"])
+        bf, cs = S["bf"], S["bf"]["st"]  # set s % 2 computes on its own stream (two batches in flight)
+        cs.wait_event(S["up"])
         if s_i >= 2:
-            st.wait_event(S["down"])  # step s-2's output has been read back
-        csa2.index_topk(planes, B, ne, N, S["q"], S["w"], K_TOP, csa2.TOPK_HIER_BUILD, topk, ws_i, BLOCK, KEEP,
-                        pool_out=pool, stream=st)
-        csa2.sparse_attn_decode(planes, B, topk, K_TOP, S["swa"], NSWA, S["qa"], scale, S["out"], ws_a,
-                                lse_out=S["lse"], stream=st)
-        S["done"].record(st)
+            cs.wait_event(S["down"])  # step s-2's output has been read back
+        csa2.index_topk(planes, B, ne, N, S["q"], S["w"], K_TOP, csa2.TOPK_HIER_BUILD, bf["topk"], bf["ws_i"],
+                        BLOCK, KEEP, pool_out=bf["pool"], stream=cs)
+        csa2.sparse_attn_decode(planes, B, bf["topk"], K_TOP, S["swa"], NSWA, S["qa"], scale, S["out"], bf["ws_a"],
+                                lse_out=S["lse"], stream=cs)
+        S["done"].record(cs)
         with torch.cuda.stream(down_s):
             down_s.wait_event(S["done"])
             S["h_out"].copy_(S["out"], non_blocking=True)
@@ -1174,11 +1202,12 @@ def run_ours(args, rank, world, local_rank):
     e_stop.record(st)
     torch.cuda.synchronize()
     e2e_ms = e_start.elapsed_time(e_stop)
-    assert csa2.check(ws_i, st)[0] == 0 and csa2.check(ws_a, st)[0] == 0
+    for bf in bufs:
+        assert csa2.check(bf["ws_i"], bf["st"])[0] == 0 and csa2.check(bf["ws_a"], bf["st"])[0] == 0
     last = sets[(args.steps - 1) % 2]
     e2e_same = bool(torch.equal(last["h_out"], out.cpu()) and torch.equal(last["h_lse"], lse.cpu()))
 
-    elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], world, dev)
+    elapsed_ms, e2e_ms, serial_ms = max_over_ranks([elapsed_ms, e2e_ms, serial_ms], world, dev)
     if rank != 0:
         return None
     hbm, peak_kind = peaks()
@@ -1212,10 +1241,15 @@ def run_ours(args, rank, world, local_rank):
                                     "frac": round(idx_achieved / hbm, 4)}},
         "e2e": {"value": round(job_rate(world, B, args.steps, e2e_ms), 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "copies": "overlapped with compute (two buffer sets, upload and download streams)",
+                "copies": "overlapped with compute (two buffer sets, upload and download streams; "
+                          "each set computes on its own stream, two batches in flight)",
                 "result_equals_device_run": e2e_same},
         "gpu_launches": launches,
         "clocks": clocks,
+        "in_flight": {"batches": 2, "how": "step s runs batch s % 2 on stream s % 2 (independent batches, "
+                                           "separate outputs and workspaces)",
+                      "one_batch_ms_per_step": round(serial_ms / args.steps, 4),
+                      "one_batch_value": round(job_rate(world, B, args.steps, serial_ms), 2)},
     }
     if not args.no_small:
         from synth import workloads as W
@@ -1230,7 +1264,7 @@ def run_ours(args, rank, world, local_rank):
         line["prefill_indexer"] = run_prefill_index(dev, st, 5, 2)
         line["v4_variants"] = run_v4(dev, st, 5, 2)
     if not args.no_step40:
-        del planes, ws_i, ws_a
+        del planes, ws_i, ws_a, bufs, sets
         torch.cuda.empty_cache()
         line["step_40_layers"] = run_step40(dev, st, 5, 2)
     return line
