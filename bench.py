@@ -485,18 +485,38 @@ def run_step40(dev, st, steps: int, warmup: int):
         buf = SCH.StepBuffers(B=B, kv=kv, n_entries=ne, n_max=nm, qidx=qidx, w=w, q=q, swa=swa, out=out,
                               k=K_TOP, n_blocks_keep=KEEP)
         SCH.allocate_scratch(buf, dev)
+        # a second batch's outputs and scratch: two independent batches in flight on two
+        # streams (the inputs are shared; each batch writes its own outputs and workspaces)
+        import dataclasses
+        buf2 = dataclasses.replace(buf, out={l: torch.empty_like(o) for l, o in out.items()}, topk={}, pool={})
+        SCH.allocate_scratch(buf2, dev)
+        st2 = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
     for _ in range(warmup):
         SCH.run_step(buf, stream=st)
+        SCH.run_step(buf2, stream=st2)
     torch.cuda.synchronize()
-    assert csa2.check(buf.ws_index, st)[0] == 0 and csa2.check(buf.ws_attn, st)[0] == 0
+    for bb, ss in ((buf, st), (buf2, st2)):
+        assert csa2.check(bb.ws_index, ss)[0] == 0 and csa2.check(bb.ws_attn, ss)[0] == 0
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # two batches in flight: step s runs batch s % 2 on stream s % 2
     a.record(st)
-    for _ in range(steps):
-        calls = SCH.run_step(buf, stream=st)
+    st2.wait_event(a)
+    for s_i in range(steps):
+        calls = SCH.run_step(buf if s_i % 2 == 0 else buf2, stream=st if s_i % 2 == 0 else st2)
+    j = torch.cuda.Event()
+    j.record(st2)
+    st.wait_event(j)
     b.record(st)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
+    # one batch in flight: each step after the one before
+    a.record(st)
+    for _ in range(steps):
+        SCH.run_step(buf, stream=st)
+    b.record(st)
+    torch.cuda.synchronize()
+    ms1 = a.elapsed_time(b) / steps
     csa2.timing_enable(True)
     SCH.run_step(buf, stream=st)
     torch.cuda.synchronize()
@@ -532,6 +552,8 @@ def run_step40(dev, st, steps: int, warmup: int):
     return {
         "workload": ST_WORKLOAD, "steps": steps, "library_calls_per_step": calls,
         "ms_per_step": round(ms, 4), "queries_per_s": round(B / (ms * 1e-3), 1),
+        "in_flight": {"batches": 2, "one_batch_ms_per_step": round(ms1, 4),
+                      "one_batch_queries_per_s": round(B / (ms1 * 1e-3), 1)},
         "kernels_ms_per_step": {k: round(tm, 4) for k, (n, tm) in sorted(kt.items())},
         "hbm": {"algorithmic_bytes": step_bytes, "achieved_gbs": round(achieved, 1), "peak": hbm,
                 "peak_kind": kind, "frac": round(achieved / hbm, 4)},
