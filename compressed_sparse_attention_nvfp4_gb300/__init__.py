@@ -116,6 +116,8 @@ def lib() -> ctypes.CDLL:
             "csa2_check": ([vp, vp, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
             "csa2_index_topk_noalloc_check": ([vp, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
             "csa2_selftest_wait_timeout": ([ctypes.c_longlong, vp, sz, vp], ctypes.c_int),
+            "csa2_selftest_codec_division": ([vp, sz, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64),
+                                              vp], ctypes.c_int),
             "csa2_status_string": ([ctypes.c_int], ctypes.c_char_p),
             "csa2_timing_enable": ([i32], ctypes.c_int),
             "csa2_kernel_times": ([ctypes.POINTER(KernelTime), i32], i32),
@@ -360,6 +362,16 @@ def selftest_wait_timeout(budget_cycles: int, ws, stream=None) -> None:
     """Runs the bounded-wait self-test; csa2.check(ws) then reports the timeout."""
     _ok(lib().csa2_selftest_wait_timeout(int(budget_cycles), _ptr(ws), _nbytes(ws), _stream(stream)),
         "csa2_selftest_wait_timeout")
+
+
+def selftest_codec_division(ws, stream=None) -> tuple[int, int]:
+    """(differing quotients, comparisons) of the codec's division against the correctly
+    rounded one over every positive E4M3 scale and fp32 significand in its range."""
+    bad, n = ctypes.c_int64(0), ctypes.c_int64(0)
+    _ok(lib().csa2_selftest_codec_division(_ptr(ws), _nbytes(ws), ctypes.byref(bad), ctypes.byref(n),
+                                           _stream(stream)),
+        "csa2_selftest_codec_division")
+    return bad.value, n.value
 
 
 def timing_enable(on: bool) -> None:

@@ -41,6 +41,27 @@ __global__ void k_quantize_main_nr(const float* __restrict__ x, int64_t n, const
                            codes + row * 256, scales + row * 32, lane);
 }
 
+// Self-test of div_by_e4m3: for positive E4M3 scale byte blockIdx.y + 1 and every fp32
+// significand of x at the 12 binades around x / s in [2^-5, 2^7), the corrected quotient
+// against __fdiv_rn; mismatches counted into *bad, comparisons into *n.
+__global__ void __launch_bounds__(256) k_selftest_division(unsigned long long* bad, unsigned long long* n) {
+  const int sb = blockIdx.y + 1;  // E4M3 bytes 1..126: the positive finite values
+  const float s = e4m3_to_float((uint32_t)sb);
+  const float r = __frcp_rn(s);
+  const int es = ilogbf(s);
+  unsigned long long nb = 0, nn = 0;
+  for (uint32_t m = blockIdx.x * blockDim.x + threadIdx.x; m < (1u << 23); m += gridDim.x * blockDim.x) {
+    const float sig = 1.0f + (float)m * 0x1p-23f;
+    for (int e = -5; e < 7; ++e) {
+      const float x = ldexpf(sig, es + e);
+      nb += __float_as_uint(div_by_e4m3(x, s, r)) != __float_as_uint(__fdiv_rn(x, s)) ? 1u : 0u;
+      ++nn;
+    }
+  }
+  atomicAdd(bad, nb);
+  atomicAdd(n, nn);
+}
+
 void launch_quantize(const float* Cbar, const float* KI, int64_t n, const csa2_kv_planes* dst, const QDest& d,
                      cudaStream_t st, const csa2_norm_rope* nr) {
   if (n <= 0) return;
@@ -202,4 +223,21 @@ extern "C" csa2_status csa2_quantize_entries(const float* Cbar, const float* KI,
   d.e0 = e0;
   launch_quantize(Cbar, KI, n, dst, d, (cudaStream_t)stream, nullptr);
   return launch_status();
+}
+
+extern "C" csa2_status csa2_selftest_codec_division(void* ws, size_t ws_bytes, int64_t* mismatches,
+                                                    int64_t* compared, csa2_stream stream) {
+  using namespace csa2;
+  if (!mismatches || !compared) return CSA2_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256) || ws_bytes < kWsHeader + 2 * sizeof(unsigned long long)) return CSA2_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  unsigned long long* d = reinterpret_cast<unsigned long long*>((char*)ws + kWsHeader);  // two counters
+  if (cudaMemsetAsync(d, 0, 2 * sizeof(unsigned long long), st) != cudaSuccess) return CSA2_ERR_CUDA;
+  k_selftest_division<<<dim3(512, 126), 256, 0, st>>>(d, d + 1);
+  unsigned long long h[2] = {0, 0};
+  if (cudaMemcpyAsync(h, d, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess) return CSA2_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return CSA2_ERR_CUDA;
+  *mismatches = (int64_t)h[0];
+  *compared = (int64_t)h[1];
+  return CSA2_OK;
 }

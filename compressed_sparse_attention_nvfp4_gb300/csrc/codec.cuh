@@ -8,6 +8,18 @@ namespace csa2 {
 
 // Main KV: 16 channels -> 8 bytes of E2M1 codes + 1 E4M3 scale byte.
 // x16 must be 16-byte aligned; codes8 8-byte aligned.
+// x / s correctly rounded, for a positive E4M3 scale s and r = RN(1 / s), by Markstein's
+// FMA correction of the reciprocal product (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990):
+// q0 = x r, then q = q0 + (x - q0 s) r in two fused steps.  For every positive E4M3 s and
+// every fp32 significand of x with x / s in [2^-5, 2^7) -- the range a group's values take,
+// below which the E2M1 code is 0 either way -- it equals the correctly rounded division bit
+// for bit: csa2_selftest_codec_division checks exactly that set.
+__device__ __forceinline__ float div_by_e4m3(float x, float s, float r) {
+  const float q0 = x * r;
+  return fmaf(fmaf(-q0, s, x), r, q0);
+}
+
 __device__ __forceinline__ void quantize_main_group_vals(const float (&v)[16], uint8_t* codes8,
                                                          uint8_t* scale1) {
   float amax = 0.0f;
@@ -18,12 +30,14 @@ __device__ __forceinline__ void quantize_main_group_vals(const float (&v)[16], u
   float s = e4m3_to_float(sb);
   uint32_t c0 = 0, c1 = 0;
   if (s != 0.0f) {
+    const float r = __frcp_rn(s);
+    auto quo = [&](float x) { return div_by_e4m3(x, s, r); };
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      c0 |= float2_to_e2m1x2(__fdiv_rn(v[2 * i], s), __fdiv_rn(v[2 * i + 1], s)) << (8 * i);
+      c0 |= float2_to_e2m1x2(quo(v[2 * i]), quo(v[2 * i + 1])) << (8 * i);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      c1 |= float2_to_e2m1x2(__fdiv_rn(v[8 + 2 * i], s), __fdiv_rn(v[9 + 2 * i], s)) << (8 * i);
+      c1 |= float2_to_e2m1x2(quo(v[8 + 2 * i]), quo(v[9 + 2 * i])) << (8 * i);
   }
   *reinterpret_cast<uint2*>(codes8) = make_uint2(c0, c1);
   *scale1 = (uint8_t)sb;

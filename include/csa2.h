@@ -436,6 +436,17 @@ const char* csa2_status_string(csa2_status s);
  * usable.  ws: at least 256 bytes, 256-byte aligned. */
 csa2_status csa2_selftest_wait_timeout(long long budget_cycles, void* ws, size_t ws_bytes, csa2_stream stream);
 
+/* Self-test of the main-KV codec's division x / s ("DeepSeek-V4.1-Flash: pushing the limits
+ * of KV cache compression", section 5: E2M1(x / s_g)): the codec divides by the group's E4M3
+ * scale with an FMA-corrected reciprocal product.  This runs it against the correctly
+ * rounded fp32 division for every positive finite E4M3 scale and every fp32 significand of
+ * x at the twelve binades where x / s lies in [2^-5, 2^7) (12,683,575,296 comparisons),
+ * synchronises `stream`, and writes the number of differing quotients to *mismatches and
+ * of comparisons to *compared (host pointers).  ws: device, 256-byte aligned, at least
+ * 272 bytes (its counters sit after the 256-byte error header). */
+csa2_status csa2_selftest_codec_division(void* ws, size_t ws_bytes, int64_t* mismatches, int64_t* compared,
+                                         csa2_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

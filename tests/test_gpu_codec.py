@@ -143,3 +143,13 @@ def test_device_generator_matches_host():
     assert np.array_equal(t.cpu().numpy(),
                           synth.keys_f32(5, 20, 21, t.numel(), 128, offset=256, hot_prob=0.3,
                                          hotvec=hv))
+
+
+def test_codec_division_exhaustive():
+    """The main-KV codec divides each value by its group's E4M3 scale with an FMA-corrected
+    reciprocal product; for every positive E4M3 scale and every fp32 significand of x with
+    x / s in [2^-5, 2^7) it must equal the correctly rounded division bit for bit."""
+    ws = csa2.workspace(512)
+    bad, n = csa2.selftest_codec_division(ws)
+    assert n == 126 * (1 << 23) * 12
+    assert bad == 0, bad
