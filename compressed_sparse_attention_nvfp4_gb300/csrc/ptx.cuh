@@ -146,22 +146,6 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// ------------------------------------------------------------------ cluster
-// address of the same shared-memory variable in CTA `rank` of the cluster
-__device__ __forceinline__ uint32_t mapa_cluster(uint32_t smem_addr, int rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-
 // ------------------------------------------------------------------ tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot_smem, uint32_t cols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -235,16 +219,6 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t* r) 
       : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16, issued by one thread.
-__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                           uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16, issued by one thread.
 __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                            uint32_t idesc, uint32_t accumulate) {
@@ -288,29 +262,14 @@ __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
       : "memory");
 }
 
-// D[tmem] (+)= (A[tmem] * 2^sfA) * (B[smem desc] * 2^sfB)^T, block-scaled
+// D[tmem] (+)= (A[smem desc] * 2^sfA) * (B[smem desc] * 2^sfB)^T, block-scaled
 // kind::mxf8f6f4 with one UE8M0 scale per row and per 32-element K step
-// (scale_vec::1X).  Tensor-memory layouts (measured on sm_103a):
-//   A (8-bit containers, K-major): element k of row m at lane m, column k/4,
-//     byte k%4; an E2M1 code sits in bits [5:2] of its byte;
-//   scale of A row m: lane m, column sfa + m/32, byte a_sf_id;
-//   scale of B column n: lane 32*(m/32) + n%32 for the lane quarter of every
-//     row m (so it is replicated in all four quarters), column sfb + n/32,
-//     byte b_sf_id.
-__device__ __forceinline__ void mma_mxf8f6f4_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                                uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                                uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], [%1], %2, %3, [%4], [%5], "
-      "p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-      : "memory");
-}
-
-// Same with A read from shared memory.  For an E2M1 A the shared-memory
-// layout is the one the tensor-memory-access unit writes for its packed 4-bit
-// type: 16 codes (8 bytes, element 2i in the low nibble) per 16-byte slot.
+// (scale_vec::1X), issued by one thread.  For an E2M1 A the shared-memory layout
+// is the one the tensor-memory-access unit writes for its packed 4-bit type: 16
+// codes (8 bytes, element 2i in the low nibble) per 16-byte slot.  Scale layouts
+// in tensor memory (measured on sm_103a): the scale of A row m at lane m, column
+// sfa + m/32, byte a_sf_id; the scale of B column n at lane 32 q + n%32 of every
+// lane quarter q (replicated), column sfb + n/32, byte b_sf_id.
 __device__ __forceinline__ void mma_mxf8f6f4_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                 uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
                                                 uint32_t accumulate) {
@@ -348,20 +307,6 @@ __device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t
   asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
                "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                : "memory");
-}
-
-// 32 lanes x 16 columns (this warp's lane quarter): thread i <-> lane i
-__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t* v) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::
-          "r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
-      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_st_32x32b_x1(uint32_t taddr, uint32_t v) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
 }
 
 // Arrive on `bar` once all previously issued tcgen05.mma of this thread completed.
