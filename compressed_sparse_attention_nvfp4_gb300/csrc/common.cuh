@@ -79,10 +79,6 @@ __device__ __forceinline__ uint32_t float2_to_e2m1x2(float lo, float hi) {
   return r & 0xFFu;
 }
 
-__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
-  return __uint_as_float((uint32_t)b << 16);
-}
-
 // order-preserving map of fp32 to u32 (larger score -> larger key); -inf -> 0
 __device__ __forceinline__ uint32_t score_key(float s) {
   if (s == -INFINITY) return 0u;
