@@ -1174,9 +1174,10 @@ def run_ours(args, rank, world, local_rank):
     csa2.timing_enable(False)
 
     # end to end through the same C-ABI calls with host buffers: per step the
-    # query-side inputs go up from pinned memory and the output comes back.  Two
-    # device buffer sets, an upload and a download stream: step s+1's inputs travel
-    # while step s computes, and step s's output comes back during step s+1.
+    # query-side inputs go up from pinned memory and the output comes back.  Three
+    # device input / output sets, an upload and a download stream, and step s
+    # computing on stream s % 2 as in the timed region: the next steps' inputs travel
+    # while step s computes, and step s's output comes back during the following ones.
     h_q = torch.from_numpy(q_h.view(np.int16)).pin_memory()
     h_w = torch.from_numpy(w_h).pin_memory()
     h_qa = torch.from_numpy(qa_h.view(np.int16)).pin_memory()
@@ -1185,8 +1186,9 @@ def run_ours(args, rank, world, local_rank):
     d2h = out.numel() * 4 + lse.numel() * 4
     up_s, down_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     sets = []
-    for i in range(2):
-        sets.append({"bf": bufs[i], "q": torch.empty_like(qd), "w": torch.empty_like(wd), "qa": torch.empty_like(qa_d),
+    n_sets = 3  # three input / output sets: each step's copies have two steps' time to finish
+    for i in range(n_sets):
+        sets.append({"q": torch.empty_like(qd), "w": torch.empty_like(wd), "qa": torch.empty_like(qa_d),
                      "swa": torch.empty_like(swa_d), "out": torch.empty_like(out), "lse": torch.empty_like(lse),
                      "h_out": torch.empty(out.shape, dtype=torch.float32).pin_memory(),
                      "h_lse": torch.empty(lse.shape, dtype=torch.float32).pin_memory(),
@@ -1197,19 +1199,20 @@ def run_ours(args, rank, world, local_rank):
     up_s.wait_event(e_start)
     st2.wait_event(e_start)
     for s_i in range(args.steps):
-        S = sets[s_i % 2]
+        S = sets[s_i % n_sets]
         with torch.cuda.stream(up_s):
-            if s_i >= 2:
-                up_s.wait_event(S["done"])  # step s-2 no longer reads this set's inputs
+            if s_i >= n_sets:
+                up_s.wait_event(S["done"])  # the set's previous step no longer reads its inputs
             S["q"].copy_(h_q, non_blocking=True)
             S["w"].copy_(h_w, non_blocking=True)
             S["qa"].copy_(h_qa, non_blocking=True)
             S["swa"].copy_(h_swa, non_blocking=True)
             S["up"].record(up_s)
-        bf, cs = S["bf"], S["bf"]["st"]  # set s % 2 computes on its own stream (two batches in flight)
+        bf = bufs[s_i % 2]  # step s computes on stream s % 2 (two batches in flight)
+        cs = bf["st"]
         cs.wait_event(S["up"])
-        if s_i >= 2:
-            cs.wait_event(S["down"])  # step s-2's output has been read back
+        if s_i >= n_sets:
+            cs.wait_event(S["down"])  # the set's previous output has been read back
         csa2.index_topk(planes, B, ne, N, S["q"], S["w"], K_TOP, csa2.TOPK_HIER_BUILD, bf["topk"], bf["ws_i"],
                         BLOCK, KEEP, pool_out=bf["pool"], stream=cs)
         csa2.sparse_attn_decode(planes, B, bf["topk"], K_TOP, S["swa"], NSWA, S["qa"], scale, S["out"], bf["ws_a"],
@@ -1226,7 +1229,7 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = e_start.elapsed_time(e_stop)
     for bf in bufs:
         assert csa2.check(bf["ws_i"], bf["st"])[0] == 0 and csa2.check(bf["ws_a"], bf["st"])[0] == 0
-    last = sets[(args.steps - 1) % 2]
+    last = sets[(args.steps - 1) % n_sets]
     e2e_same = bool(torch.equal(last["h_out"], out.cpu()) and torch.equal(last["h_lse"], lse.cpu()))
 
     elapsed_ms, e2e_ms, serial_ms = max_over_ranks([elapsed_ms, e2e_ms, serial_ms], world, dev)
@@ -1263,8 +1266,8 @@ def run_ours(args, rank, world, local_rank):
                                     "frac": round(idx_achieved / hbm, 4)}},
         "e2e": {"value": round(job_rate(world, B, args.steps, e2e_ms), 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "copies": "overlapped with compute (two buffer sets, upload and download streams; "
-                          "each set computes on its own stream, two batches in flight)",
+                "copies": "overlapped with compute (three input/output sets, upload and download streams; "
+                          "step s computes on stream s % 2, two batches in flight)",
                 "result_equals_device_run": e2e_same},
         "gpu_launches": launches,
         "clocks": clocks,
