@@ -77,17 +77,13 @@ struct __align__(1024) AttnSmem {
   float c2[kHAtt];                     // log2(e) * softmax_scale * 2^s_h: logit (log2 units) per raw S
   float alpha[kHAtt];                  // factor of O and l when a head's reference moved
   float inv[kHAtt];                    // 1 / softmax denominator (or 1 for partials)
-  int32_t idx[CSA2_MAX_TOPK];          // this CTA's selected-entry indices (its chunks' rows below k)
   uint32_t vmask[2][2];                // per slot and 32-row half: rows that exist
-  int vote[2][4];                      // per chunk parity and softmax warp: a logit above its threshold
   uint64_t q_load;                     // the query's bf16 rows copied into slot 1 (bulk copy)
-  uint64_t q_full;                     // q' and c2 written (8 warps)
-  uint64_t x_full[2][2];               // per slot, channel half of X written (4 row warps each)
+  uint64_t q_full;                     // q' and c2 written (the 8 softmax and MMA warps)
+  uint64_t x_full[2][2];               // per slot, channel half of X written (8 row warps each)
   uint64_t s_full[2];                  // per slot: S MMAs complete (both halves)
   uint64_t p_full[2];                  // per slot: P written (4 softmax warps)
   uint64_t x_free[2][2];               // per slot, channel half: the O MMAs reading it complete
-  uint64_t vote_full;                  // votes posted (4 softmax warps)
-  uint64_t max_full;                   // factors posted (4 softmax warps; chunks that need them)
   uint64_t fin;                        // 1 / denominators posted (4 softmax warps)
   uint64_t drained;                    // every MMA issued complete (four MMA warps)
   uint32_t tmem_base;
@@ -120,106 +116,141 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
 // q' = q_h 2^-s_h in f16 with 2^s_h bringing the head's largest |q| to
 // [2^14, 2^15), clamped so that both 2^s_h and 2^-s_h are normal fp32 values;
 // bf16 q keeps q' exact and inside the f16 range (with RMSNorm or RoPE the
-// fp32 result is rounded to f16 once).  Warp w converts heads 8w..8w+7: lane l
-// holds channels 8l..8l+7 and 256+8l..256+8l+7 of each, i.e. chunks l and 32+l
-// of the [c/8][head][c%8] image; the rotated pairs sit in lanes 24-31.
-// q' is converted from a shared-memory copy of the query's bf16 rows ([64][512],
-// brought in by one bulk copy), one head at a time.
-// The f16 result goes to `qrot`, a [c/8][head][c%8] image whose head slots are
-// rotated by the chunk (head h of chunk c at slot (h + c) mod 64): the lanes of
-// a store write 32 different chunks, 1024 bytes apart, and without the rotation
-// all of them would hit the same shared-memory banks.  copy_q then writes the
-// unrotated image the MMAs read.
+// fp32 result is rounded to f16 once).  One bulk copy brings the query's bf16
+// rows ([64][512]) into row slot 1; the softmax and MMA warps, idle until the
+// first chunk's rows are written, convert them from there while the row warps
+// dequantize chunk 0 into slot 0.  Warp 8 + w takes heads 8w .. 8w + 7: lane
+// l = 8g + t head 8w + t over the 8-channel planes (t + 4i + g) mod 64, i < 16.
+// The eight lanes of a phase then read eight different banks of the bf16 rows
+// (their planes differ mod 8) and write eight consecutive head slots of the
+// [c/8][head][c%8] image, so neither side conflicts; the values are read again
+// for each pass rather than held (a pass holding all 64 registers spills other
+// warps' state), and the four lanes of a head combine its maximum (and sum of
+// squares) with two shuffles.
 template <bool kEx>
-__device__ __forceinline__ void stage_q(AttnSmem& S, const uint16_t* qs, uint16_t* qrot, float scale, int warp,
-                                        int lane, const AttnExtras& ex, int b) {
-  // per lane: the RMSNorm weights of its 16 channels, the cos / sin of its 4 pairs
-  float wq[16], rc[4], rs[4];
+__device__ __forceinline__ void stage_q(AttnSmem& S, const uint16_t* qs, float scale, int w, int lane,
+                                        const AttnExtras& ex, int b) {
+  const int t = lane & 7, g = lane >> 3, h = 8 * w + t;
+  const uint4* src = reinterpret_cast<const uint4*>(qs + h * kDMain);
   const bool norm = kEx && ex.qnorm_w != nullptr;
+  const bool rot = kEx && ex.rope;
+  float r = 1.0f;  // 1 / RMS of the head
   if (norm) {
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const float4* wv = reinterpret_cast<const float4*>(ex.qnorm_w + i * 256 + lane * 8);
-      const float4 a = wv[0], c = wv[1];
-      wq[8 * i] = a.x, wq[8 * i + 1] = a.y, wq[8 * i + 2] = a.z, wq[8 * i + 3] = a.w;
-      wq[8 * i + 4] = c.x, wq[8 * i + 5] = c.y, wq[8 * i + 6] = c.z, wq[8 * i + 7] = c.w;
-    }
-  }
-  const bool rot = kEx && ex.rope && 256 + lane * 8 >= kRopeFirst;
-  if (rot) {
-    const double pos = (double)ex.qpos[b];
-#pragma unroll
-    for (int p = 0; p < 4; ++p) rope_cos_sin(ex.th.t[(256 + lane * 8 - kRopeFirst) / 2 + p], pos, rc[p], rs[p]);
-  }
-#pragma unroll 2
-  for (int u = 0; u < 8; ++u) {
-    float v[16];
-    const uint4* src = reinterpret_cast<const uint4*>(qs + (warp * 8 + u) * kDMain);
-    const uint4 raw[2] = {src[lane], src[32 + lane]};
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+    float ss = 0.0f;
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+      const uint4 q4 = src[(t + 4 * i + g) & 63];
+      const uint32_t w4[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        v[8 * i + 2 * j] = __uint_as_float(w4[j] << 16);
-        v[8 * i + 2 * j + 1] = __uint_as_float(w4[j] & 0xFFFF0000u);
+        const float v0 = __uint_as_float(w4[j] << 16), v1 = __uint_as_float(w4[j] & 0xFFFF0000u);
+        ss = fmaf(v0, v0, ss);
+        ss = fmaf(v1, v1, ss);
       }
     }
+    ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 16);
+    r = 1.0f / sqrtf(ss / (float)kDMain + ex.eps);
+  }
+  // RoPE turns planes 56 .. 63 (pairs 4 (p - 56) + pr); lane l keeps the cosine and
+  // sine of pair l (every head turns by the same angles)
+  float rcos = 1.0f, rsin = 0.0f;
+  if (rot) rope_cos_sin(ex.th.t[lane], (double)ex.qpos[b], rcos, rsin);
+  // the 8 channels of plane p after RMSNorm and RoPE
+  auto plane = [&](int p, float (&v)[8]) {
+    const uint4 q4 = src[p];
+    const uint32_t w4[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[2 * j] = __uint_as_float(w4[j] << 16);
+      v[2 * j + 1] = __uint_as_float(w4[j] & 0xFFFF0000u);
+    }
     if (norm) {
-      float ss = 0.0f;
+      const float4* wv = reinterpret_cast<const float4*>(ex.qnorm_w + 8 * p);
+      const float4 a = __ldg(wv), c = __ldg(wv + 1);
+      const float wq[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
 #pragma unroll
-      for (int i = 0; i < 16; ++i) ss = fmaf(v[i], v[i], ss);
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      const float r = 1.0f / sqrtf(ss / (float)kDMain + ex.eps);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = wq[i] * (v[i] * r);
+      for (int k = 0; k < 8; ++k) v[k] = wq[k] * (v[k] * r);
     }
     if (rot) {
 #pragma unroll
-      for (int p = 0; p < 4; ++p) rope_pair(v[8 + 2 * p], v[9 + 2 * p], rc[p], rs[p]);
-    }
-    float mx = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) mx = fmaxf(mx, fabsf(v[i]));
-    // non-negative floats order as their bit patterns: one warp reduction instruction
-    mx = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(mx)));
-    const int sig = mx > 0.0f ? min(max(floor_log2_f32(mx) - 14, -126), 126) : 0;
-    const float inv = exp2i_f32(-sig);  // exact power of two: q 2^-sig rounds only in the f16 conversion
-    const int h = warp * 8 + u;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      uint32_t o[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const __half2 h2 = __floats2half2_rn(v[8 * i + 2 * j] * inv, v[8 * i + 2 * j + 1] * inv);
-        o[j] = *reinterpret_cast<const uint32_t*>(&h2);
+      for (int pr = 0; pr < 4; ++pr) {  // every lane shuffles; only planes 56 .. 63 turn
+        const int pair = (4 * (p - 56) + pr) & 31;
+        const float c = __shfl_sync(0xffffffffu, rcos, pair), sn = __shfl_sync(0xffffffffu, rsin, pair);
+        if (p >= 56) rope_pair(v[2 * pr], v[2 * pr + 1], c, sn);
       }
-      const int c = i * 32 + lane;
-      *reinterpret_cast<uint4*>(qrot + c * kQPlane + ((h + c) & (kHAtt - 1)) * 8) = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    if (lane == 0) S.c2[h] = kLog2e * scale * exp2i_f32(sig);
-  }
-}
-
-// q' from the rotated image into S.q: thread t moves head t % 64 of chunks
-// 4 i + t / 64, so a warp reads and writes 512 consecutive bytes of one chunk.
-__device__ __forceinline__ void copy_q(AttnSmem& S, const uint16_t* rot, int tid) {
-  const int h = tid & (kHAtt - 1);
+  };
+  float mx = 0.0f;
+  if (kEx) {
+#pragma unroll 2
+    for (int i = 0; i < 16; ++i) {
+      float v[8];
+      plane((t + 4 * i + g) & 63, v);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx = fmaxf(mx, fabsf(v[k]));
+    }
+  } else {  // |bf16| orders as its bit pattern: a packed 16-bit maximum over the raw words
+    uint32_t m2 = 0;
 #pragma unroll 4
-  for (int i = 0; i < kDMain / 8 / 4; ++i) {
-    const int c = 4 * i + (tid >> 6);
-    *reinterpret_cast<uint4*>(&S.q[c][h * 8]) =
-        *reinterpret_cast<const uint4*>(rot + c * kQPlane + ((h + c) & (kHAtt - 1)) * 8);
+    for (int i = 0; i < 16; ++i) {
+      const uint4 q4 = src[(t + 4 * i + g) & 63];
+      const uint32_t w4[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) asm("max.u16x2 %0, %0, %1;" : "+r"(m2) : "r"(w4[j] & 0x7FFF7FFFu));
+    }
+    mx = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
   }
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+  const int sig = mx > 0.0f ? min(max(floor_log2_f32(mx) - 14, -126), 126) : 0;
+  const float inv = exp2i_f32(-sig);  // exact power of two: q 2^-sig rounds only in the f16 conversion
+#pragma unroll 4
+  for (int i = 0; i < 16; ++i) {
+    const int p = (t + 4 * i + g) & 63;
+    float v[8];
+    plane(p, v);
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __half2 h2 = __floats2half2_rn(v[2 * j] * inv, v[2 * j + 1] * inv);
+      o[j] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    *reinterpret_cast<uint4*>(&S.q[p][h * 8]) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (g == 0) S.c2[h] = kLog2e * scale * exp2i_f32(sig);
 }
 
-// One thread's quarter row of a chunk (128 channels), fetched ahead of its
-// dequantization: a selected entry's 64 code bytes and 8 scale bytes, or a
-// window row's 128 bytes.
+// Whether some of the four softmax warps (named barrier 2, 128 threads) saw a
+// logit above its head's reference (lane 0 of each warp posts `wover`) and
+// whether one of them gave up waiting (lanes 1-8 post `wbad`): one barrier, the
+// count of posted predicates below 8 for the first, at least 8 for the second.
+// Every softmax warp passes it once per chunk, also after a failed wait, so no
+// warp is left at the barrier.
+__device__ __forceinline__ uint32_t softmax_vote(bool wover, bool wbad, int lane) {
+  const uint32_t pred = lane == 0 ? (wover ? 1u : 0u) : (lane <= 8 && wbad ? 1u : 0u);
+  uint32_t n;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.popc.u32 %0, 2, 128, p;\n\t}"
+      : "=r"(n)
+      : "r"(pred)
+      : "memory");
+  return n;
+}
+// the four softmax warps (named barrier 2): shared-memory writes before it are seen after it
+__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+
+// One thread's share of a chunk row, fetched two chunks ahead of its
+// dequantization.  Gather warp w takes chunk rows 8w .. 8w + 7: lane l row
+// 8w + l % 8 and column block cb = l / 8, so each load instruction reads 64
+// contiguous bytes of eight rows (eight cache lines, not one line per lane).  A
+// selected entry: 16-byte code chunks 4i + cb (i < 4; channels 32 (4i + cb) ..)
+// and the entry's 32 scale bytes; a window row: 16-byte chunks 4i + cb (i < 8;
+// channels 16 (4i + cb) ..).  Channels below 256 (channel half 0) come from i < 2
+// (entries) or i < 4 (window rows).
 struct RowFetch {
-  uint4 raw[8];
-  int kind;  // 0 = no row, 1 = main entry, 2 = window row
+  uint4 raw[8];  // entry: raw[0..3] codes, raw[4..5] scales; window row: raw[0..7]
+  int kind;      // 0 = no row, 1 = selected entry, 2 = window row
 };
 
 // entry of chunk row gr (rows gr >= k are window rows or padding): topk[b][gr],
@@ -231,71 +262,81 @@ __device__ __forceinline__ int64_t fetch_index(const int32_t* __restrict__ topk,
   return (int64_t)topk[(int64_t)b * k + gr];
 }
 
-// Starts the loads of quarter `part` (channels 128 part ..) of chunk row gr: a
-// selected entry (gr < k, index idx), a window row (k <= gr < k + n_swa) or nothing.
+// Starts this lane's loads of chunk row gr: a selected entry (gr < k, index idx),
+// a window row (k <= gr < k + n_swa, visible) or nothing.
 __device__ __forceinline__ void issue_row(RowFetch& f, int64_t idx, const uint8_t* __restrict__ kv_codes,
                                           const uint8_t* __restrict__ kv_scales, int64_t seq_stride,
                                           const uint8_t* __restrict__ swa, int n_swa, int k, int b, int gr,
-                                          int part, void* ws, const int64_t* __restrict__ win_pos, int64_t win_lo) {
+                                          int cb, void* ws, const int64_t* __restrict__ win_pos, int64_t win_lo) {
   f.kind = 0;
   if (gr < k) {
     if (idx >= 0 && idx < seq_stride) {
       const int64_t e = (int64_t)b * seq_stride + idx;
-      const uint4* cs = reinterpret_cast<const uint4*>(kv_codes + e * 256 + part * 64);
+      const uint4* cs = reinterpret_cast<const uint4*>(kv_codes + e * 256);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) f.raw[i] = cs[i];
-      const uint2 sc = reinterpret_cast<const uint2*>(kv_scales + e * 32)[part];
-      f.raw[4].x = sc.x;
-      f.raw[4].y = sc.y;
+      for (int i = 0; i < 4; ++i) f.raw[i] = cs[4 * i + cb];
+      const uint4* sc = reinterpret_cast<const uint4*>(kv_scales + e * 32);
+      f.raw[4] = sc[0];
+      f.raw[5] = sc[1];
       f.kind = 1;
-    } else if (idx != -1 && part == 0) {
+    } else if (idx != -1 && cb == 0) {
       report_error(ws, CSA2_ERR_INDEX_RANGE, idx);
     }
   } else if (gr - k < n_swa && (!win_pos || win_pos[(int64_t)b * n_swa + (gr - k)] >= win_lo)) {
-    const uint4* src = reinterpret_cast<const uint4*>(swa + ((int64_t)b * n_swa + (gr - k)) * kDMain + part * 128);
+    const uint4* src = reinterpret_cast<const uint4*>(swa + ((int64_t)b * n_swa + (gr - k)) * kDMain);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) f.raw[i] = src[i];
+    for (int i = 0; i < 8; ++i) f.raw[i] = src[4 * i + cb];
     f.kind = 2;
   }
 }
 
-// Writes channels [128 part, 128 part + 128) of row r to slot `slot` of X as f16
-// (zeros when there is no row); returns whether the row exists.
-__device__ __forceinline__ bool dequant_quarter_row(AttnSmem& S, const RowFetch& f, int slot, int r, int part) {
+// Writes this lane's channels of channel half h of row r (see RowFetch) to slot
+// `slot` of X as f16 (zeros when there is no row): 32 channels per code chunk of
+// an entry (planes 4c .. 4c + 3), 16 per chunk of a window row (planes 2k, 2k + 1).
+// The eight lanes of a store phase write eight rows of one plane: no bank conflict.
+__device__ __forceinline__ void dequant_half_row(AttnSmem& S, const RowFetch& f, int slot, int r, int cb, int h) {
+  if (f.kind == 1) {
 #pragma unroll
-  for (int g = 0; g < 8; ++g) {  // 16 channels: planes 16 part + 2g, 2g + 1
-    uint32_t w[8];
-    if (f.kind == 1) {
-      const uint32_t sb = ((g < 4 ? f.raw[4].x : f.raw[4].y) >> (8 * (g & 3))) & 0xFFu;
-      const uint32_t s2 = e4m3x2_to_f16x2(sb | (sb << 8));
-      const uint4 cw = f.raw[g / 2];
-      const uint32_t w0 = (g & 1) ? cw.z : cw.x, w1 = (g & 1) ? cw.w : cw.y;
-      uint32_t h0[4], h1[4];
-      e2m1x8_to_f16(w0, h0);
-      e2m1x8_to_f16(w1, h1);
+    for (int i = 2 * h; i < 2 * h + 2; ++i) {
+      const int c = 4 * i + cb;  // code chunk: channels 32c .., scale groups 2c, 2c + 1
+      const uint32_t sw = i == 0 ? f.raw[4].x : i == 1 ? f.raw[4].z : i == 2 ? f.raw[5].x : f.raw[5].z;
+      const uint32_t sw1 = i == 0 ? f.raw[4].y : i == 1 ? f.raw[4].w : i == 2 ? f.raw[5].y : f.raw[5].w;
+      // scale bytes 2c, 2c + 1 = bytes 2 cb, 2 cb + 1 of the word pair covering bytes 8i .. 8i + 7
+      const uint32_t pair = ((cb < 2 ? sw : sw1) >> (16 * (cb & 1))) & 0xFFFFu;
+      const uint32_t s0 = e4m3x2_to_f16x2((pair & 0xFFu) * 0x0101u);
+      const uint32_t s1 = e4m3x2_to_f16x2((pair >> 8) * 0x0101u);
+      const uint4 cw = f.raw[i];
+      const uint32_t wq[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        w[j] = hmul2_u32(h0[j], s2);
-        w[4 + j] = hmul2_u32(h1[j], s2);
+      for (int q = 0; q < 4; ++q) {  // 8 channels: plane 4c + q
+        uint32_t hq[4];
+        e2m1x8_to_f16(wq[q], hq);
+        const uint32_t sq = q < 2 ? s0 : s1;
+        *reinterpret_cast<uint4*>(&S.X[slot][4 * c + q][r * 8]) =
+            make_uint4(hmul2_u32(hq[0], sq), hmul2_u32(hq[1], sq), hmul2_u32(hq[2], sq), hmul2_u32(hq[3], sq));
       }
-    } else if (f.kind == 2) {
-      const uint4 v = f.raw[g];
-      w[0] = e4m3x2_to_f16x2(v.x);
-      w[1] = e4m3x2_to_f16x2(v.x >> 16);
-      w[2] = e4m3x2_to_f16x2(v.y);
-      w[3] = e4m3x2_to_f16x2(v.y >> 16);
-      w[4] = e4m3x2_to_f16x2(v.z);
-      w[5] = e4m3x2_to_f16x2(v.z >> 16);
-      w[6] = e4m3x2_to_f16x2(v.w);
-      w[7] = e4m3x2_to_f16x2(v.w >> 16);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) w[j] = 0u;
     }
-    *reinterpret_cast<uint4*>(&S.X[slot][part * 16 + 2 * g][r * 8]) = make_uint4(w[0], w[1], w[2], w[3]);
-    *reinterpret_cast<uint4*>(&S.X[slot][part * 16 + 2 * g + 1][r * 8]) = make_uint4(w[4], w[5], w[6], w[7]);
+  } else if (f.kind == 2) {
+#pragma unroll
+    for (int i = 4 * h; i < 4 * h + 4; ++i) {
+      const int kc = 4 * i + cb;  // channels 16 kc ..
+      const uint4 v = f.raw[i];
+      *reinterpret_cast<uint4*>(&S.X[slot][2 * kc][r * 8]) =
+          make_uint4(e4m3x2_to_f16x2(v.x), e4m3x2_to_f16x2(v.x >> 16), e4m3x2_to_f16x2(v.y),
+                     e4m3x2_to_f16x2(v.y >> 16));
+      *reinterpret_cast<uint4*>(&S.X[slot][2 * kc + 1][r * 8]) =
+          make_uint4(e4m3x2_to_f16x2(v.z), e4m3x2_to_f16x2(v.z >> 16), e4m3x2_to_f16x2(v.w),
+                     e4m3x2_to_f16x2(v.w >> 16));
+    }
+  } else {
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int i = 2 * h; i < 2 * h + 2; ++i) {
+      const int c = 4 * i + cb;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(&S.X[slot][4 * c + q][r * 8]) = z;
+    }
   }
-  return f.kind != 0;
 }
 
 // Raw S of this lane's head over its 32 rows of a chunk (lanes 0-15: rows 0-31, lanes
@@ -351,14 +392,17 @@ __device__ __forceinline__ float sum_probs(const uint32_t (&ph)[16]) {
 //   warps 0-7: thread t dequantizes channels 128 (t / 64) .. of chunk row t % 64
 //     into the chunk's slot, fetching the rows of the chunk two ahead meanwhile;
 //     afterwards, the epilogue;
+//   warps 8-15 first stage q' (while warps 0-7 dequantize the first two chunks),
+//     then take their roles:
 //   warps 8-11: the softmax; warp 8 + q owns heads 16 q .. + 15 (lanes 0-15 of
 //     lane quarter q, the rows of an M = 64 accumulator) over all of a chunk's rows;
 //   warps 12-15: the MMA issue (S halves, O halves).
 // The softmax keeps, per head, a reference m (the running maximum, raised only
 // when a chunk exceeds it by more than kTau2, which then rescales O and l), so
 // probabilities stay below e^8.  Each chunk first forms P with the references it
-// has; one vote over the eight warps tells whether some head needs a new one,
-// and only then are the chunk's exact maxima exchanged.  The softmax runs in
+// has; one vote over the four softmax warps (a reducing named barrier) tells
+// whether some head needs a new one, and only then are the chunk's exact maxima
+// exchanged.  The softmax runs in
 // log2 units: p = 2^(raw S * c2_h - m2_h).
 // kPartial: write the unnormalised O with (m, l) for the merge kernel instead
 // of the normalised output.
@@ -383,15 +427,13 @@ __global__ void __launch_bounds__(512, 1) k_attn(
       ptx::mbar_init(&S.q_load, 1);
       ptx::mbar_init(&S.q_full, 8);
       for (int s = 0; s < 2; ++s) {
-        ptx::mbar_init(&S.x_full[s][0], 4);
-        ptx::mbar_init(&S.x_full[s][1], 4);
+        ptx::mbar_init(&S.x_full[s][0], kGatherWarps);
+        ptx::mbar_init(&S.x_full[s][1], kGatherWarps);
         ptx::mbar_init(&S.s_full[s], 2);
         ptx::mbar_init(&S.p_full[s], 4);
         ptx::mbar_init(&S.x_free[s][0], 1);
         ptx::mbar_init(&S.x_free[s][1], 1);
       }
-      ptx::mbar_init(&S.vote_full, 4);
-      ptx::mbar_init(&S.max_full, 4);
       ptx::mbar_init(&S.fin, 4);
       ptx::mbar_init(&S.drained, 4);  // the four MMA warps
       S.abort_flag = 0;
@@ -401,33 +443,33 @@ __global__ void __launch_bounds__(512, 1) k_attn(
     ptx::tmem_alloc(&S.tmem_base, kAttnTmemCols);
   }
   ptx::griddep_wait();  // q, the indices and the rows may come from the previous kernel
-  // one bulk copy brings the query's bf16 rows into slot 1 of the (still unused) row
-  // buffer while the first two chunks' indices, then rows, are loaded; q' is
-  // converted afterwards
-  if (warp == kCtlWarp && lane == 0) {
+  if (warp == kCtlWarp && lane == 0) {  // the query's bf16 rows into slot 1 (free until chunk 1)
     ptx::mbar_arrive_expect_tx(&S.q_load, kHAtt * kDMain * 2);
     ptx::bulk_g2s(&S.X[1][0][0], qg + (int64_t)b * kHAtt * kDMain, kHAtt * kDMain * 2, &S.q_load);
   }
-  const int r = tid & (kRows - 1), part = (tid >> 6) & 3;  // gather: chunk row, channel quarter
-  RowFetch rf0, rf1;                                       // rows of the even / odd chunks
-  rf0.kind = rf1.kind = 0;
+  const int r = 8 * (warp & 7) + (lane & 7), cb = lane >> 3;  // gather: chunk row, column block
   const int64_t win_lo = ex.win_pos ? max(ex.win_lo[b], (int64_t)0) : 0;  // window rows below it are not seen
+  int64_t idx0 = -1, idx1 = -1;
   if (warp < kGatherWarps) {
     const int gr0 = c0 * kRows + r, gr1 = gr0 + kRows;
-    const int64_t idx0 = fetch_index(topk, dense_n, k, b, gr0);
-    const int64_t idx1 = nc > 1 ? fetch_index(topk, dense_n, k, b, gr1) : -1;
-    if (!dense_n) {  // the later chunks' indices wait in shared memory (no dependent global load per chunk)
-      const int n_sel = min(k - c0 * kRows, nc * kRows);
-      for (int i = tid; i < n_sel; i += kGatherWarps * 32) S.idx[i] = topk[(int64_t)b * k + c0 * kRows + i];
-    }
-    issue_row(rf0, idx0, kv_codes, kv_scales, seq_stride, swa, n_swa, k, b, gr0, part, ws, ex.win_pos, win_lo);
-    if (nc > 1)
-      issue_row(rf1, idx1, kv_codes, kv_scales, seq_stride, swa, n_swa, k, b, gr1, part, ws, ex.win_pos, win_lo);
+    idx0 = fetch_index(topk, dense_n, k, b, gr0);
+    idx1 = nc > 1 ? fetch_index(topk, dense_n, k, b, gr1) : -1;
   }
   ptx::tc_fence_before();
   __syncthreads();  // barriers initialised, tensor memory allocated
   ptx::tc_fence_after();
   const uint32_t tmem = S.tmem_base;
+  if (warp >= kGatherWarps) {  // q' and c2 from slot 1, while the row warps dequantize chunk 0
+    if (ptx::mbar_wait_warp(&S.q_load, 0, abort_flag, kAttnWaitBudget)) {
+      stage_q<kEx>(S, &S.X[1][0][0], scale, warp - kGatherWarps, lane, ex, b);
+    } else if (lane == 0 && !*abort_flag) {
+      *abort_flag = 1;
+      report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 25);
+    }
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&S.q_full);
+  }
 
   if (warp >= kCtlWarp) {
     // ------------------------------------------------------------ MMA issue
@@ -495,19 +537,17 @@ __global__ void __launch_bounds__(512, 1) k_attn(
     // ------------------------------------------ rows (gather, dequantization), epilogue
     const int q4 = warp & 3, ch = warp >> 2;  // epilogue: lane quarter, heads 32 ch ..
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-    // q' through the rotated image in slot 0 (free until the first chunk's rows)
-    bool good = ptx::mbar_wait_warp(&S.q_load, 0, abort_flag, kAttnWaitBudget);
-    if (good) {
-      stage_q<kEx>(S, &S.X[1][0][0], &S.X[0][0][0], scale, warp, lane, ex, b);
-    } else if (lane == 0 && !*abort_flag) {
-      *abort_flag = 1;
-      report_error(ws, CSA2_ERR_DEVICE_TIMEOUT, 25);
-    }
-    asm volatile("bar.sync 1, 256;" ::: "memory");  // the eight row warps: every rotated chunk written
-    if (good) copy_q(S, &S.X[0][0][0], tid);
-    ptx::fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(&S.q_full);
+    RowFetch rf0, rf1;  // rows of the even / odd chunks
+    const int gr0 = c0 * kRows + r;
+    rf1.kind = 0;
+    issue_row(rf0, idx0, kv_codes, kv_scales, seq_stride, swa, n_swa, k, b, gr0, cb, ws, ex.win_pos, win_lo);
+    if (nc > 1)
+      issue_row(rf1, idx1, kv_codes, kv_scales, seq_stride, swa, n_swa, k, b, gr0 + kRows, cb, ws, ex.win_pos,
+                win_lo);
+    // this lane's entries in chunks j + 2 (loaded after chunk j) and j + 3 (index read then)
+    int64_t idx2 = nc > 2 ? fetch_index(topk, dense_n, k, b, gr0 + 2 * kRows) : -1;
+    int64_t idx3 = nc > 3 ? fetch_index(topk, dense_n, k, b, gr0 + 3 * kRows) : -1;
+    bool good = true;
     for (int p = 0; 2 * p < nc && good; ++p) {
       const uint32_t ph = (uint32_t)(p & 1);
       // ---- rows of chunks 2p and 2p + 1 into slots 0 and 1
@@ -516,26 +556,31 @@ __global__ void __launch_bounds__(512, 1) k_attn(
         const int j = 2 * p + s;
         if (j >= nc || !good) break;
         RowFetch& f = s ? rf1 : rf0;
-        // the index of the chunk two ahead
-        const int gr2 = (c0 + j + 2) * kRows + r;
-        const int64_t idx2 = j + 2 >= nc || gr2 >= k ? -1
-                             : dense_n ? (gr2 < __ldg(dense_n + b) ? gr2 : -1)
-                                       : (int64_t)S.idx[(j + 2) * kRows + r];
-        if (j >= 2)  // O(j - 2) no longer reads this thread's channel half of the slot
-          good = ptx::mbar_wait_warp(&S.x_free[s][part >> 1], ph ^ 1u, abort_flag, kAttnWaitBudget);
-        else  // slot 1 holds the bf16 q copy, slot 0 the rotated q', until every warp staged q'
-          good = ptx::mbar_wait_warp(&S.q_full, 0, abort_flag, kAttnWaitBudget);
-        if (!good) break;
-        const bool valid = dequant_quarter_row(S, f, s, r, part);
-        if (part == 0) {
-          const uint32_t vm = __ballot_sync(0xffffffffu, valid);
-          if (lane == 0) S.vmask[s][warp & 1] = vm;
+        const int gr = (c0 + j) * kRows + r;
+        // each channel half as soon as O(j - 2) no longer reads it; half 0 also posts the rows
+        // that exist (lanes 0-7 hold this warp's eight rows)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (j >= 2)
+            good = ptx::mbar_wait_warp(&S.x_free[s][h], ph ^ 1u, abort_flag, kAttnWaitBudget);
+          else if (j == 1 && h == 0)  // slot 1 holds the bf16 query until q' is staged
+            good = ptx::mbar_wait_warp(&S.q_full, 0, abort_flag, kAttnWaitBudget);
+          if (!good) break;
+          dequant_half_row(S, f, s, r, cb, h);
+          if (h == 0) {
+            const uint32_t vm = __ballot_sync(0xffffffffu, f.kind != 0) & 0xFFu;
+            if (lane == 0) reinterpret_cast<uint8_t*>(&S.vmask[s][(warp & 7) >> 2])[warp & 3] = (uint8_t)vm;
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&S.x_full[s][h]);
         }
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&S.x_full[s][part >> 1]);
+        if (!good) break;
         if (j + 2 < nc)
-          issue_row(f, idx2, kv_codes, kv_scales, seq_stride, swa, n_swa, k, b, gr2, part, ws, ex.win_pos, win_lo);
+          issue_row(f, idx2, kv_codes, kv_scales, seq_stride, swa, n_swa, k, b, gr + 2 * kRows, cb, ws, ex.win_pos,
+                    win_lo);
+        idx2 = idx3;
+        idx3 = j + 4 < nc ? fetch_index(topk, dense_n, k, b, gr + 4 * kRows) : -1;
       }
     }
     // ---- epilogue: O^T rows = channels of this lane quarter, 32 heads per warp; for each
@@ -594,41 +639,38 @@ __global__ void __launch_bounds__(512, 1) k_attn(
     float lsum = 0.0f;     // rounded probabilities of this lane's rows, summed over every chunk
     bool good = ptx::mbar_wait_warp(&S.q_full, 0, abort_flag, kAttnWaitBudget);  // c2 (acquire)
     const float c2h = S.c2[hd];
-    int nvote = 0, nslow = 0;  // uses of vote_full / max_full so far (the same in every softmax warp)
-    for (int j = 0; j < nc && good; ++j) {
+    // Every softmax warp runs every chunk up to its vote, also after a failed wait: the
+    // vote tells all four of them at once to stop.
+    for (int j = 0; j < nc; ++j) {
       const int s = j & 1;
       const uint32_t ph = (uint32_t)((j >> 1) & 1);
       // x_full of both halves: the row warps wrote X(j) after O(j - 2) released the slot, so
       // the P^T slot is free too; half 0 also posts the row mask
-      good = ptx::mbar_wait_warp(&S.s_full[s], ph, abort_flag, kAttnWaitBudget) &&
+      good = good && ptx::mbar_wait_warp(&S.s_full[s], ph, abort_flag, kAttnWaitBudget) &&
              ptx::mbar_wait_warp(&S.x_full[s][0], ph, abort_flag, kAttnWaitBudget) &&
              ptx::mbar_wait_warp(&S.x_full[s][1], ph, abort_flag, kAttnWaitBudget);
-      if (!good) break;
-      ptx::tc_fence_after();
       const uint32_t taS = tmem + lane_base + kTmemS + 64u * (uint32_t)s;  // half 0; half 1 at + 128
-      const uint32_t vm = S.vmask[s][rh];  // this lane's rows that exist
+      uint32_t vm = 0;  // this lane's rows that exist
       // P with the reference so far: stands unless some head needs a new one
       uint32_t pp[16];  // this lane's 32 rows, f16 pairs
-      bool over;
-      {
+      bool over = false;
+      if (good) {
+        ptx::tc_fence_after();
+        vm = S.vmask[s][rh];
         const float ref = m2 == -INFINITY ? kNoRef : m2;
         float sv[32];
         load_scores(taS, vm, sv);
         over = head_probs(sv, c2h, ref, pp);
+        store_probs(S, s, rh, hd, pp);
+        ptx::fence_proxy_async_smem();  // before the vote: its latency overlaps the other warps'
       }
-      store_probs(S, s, rh, hd, pp);
-      ptx::fence_proxy_async_smem();  // before the vote: its latency overlaps the other warps'
-      const bool wover = __any_sync(0xffffffffu, over);
-      if (lane == 0) S.vote[nvote & 1][q4] = wover ? 1 : 0;
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&S.vote_full);
-      good = ptx::mbar_wait_warp(&S.vote_full, (uint32_t)(nvote & 1), abort_flag, kAttnWaitBudget);
-      if (!good) break;
-      const bool slow = (S.vote[nvote & 1][0] | S.vote[nvote & 1][1] | S.vote[nvote & 1][2] |
-                         S.vote[nvote & 1][3]) != 0;
-      ++nvote;
+      const uint32_t nv = softmax_vote(__any_sync(0xffffffffu, over), !good || *abort_flag != 0, lane);
+      if (nv >= 8) {
+        good = false;
+        break;
+      }
       float alpha = 1.0f;  // this head's factor for its sum and O
-      if (slow) {
+      if (nv != 0) {
         // the chunk's exact maximum of this head (both lanes' rows; S stays in tensor memory
         // until P is handed over)
         float sv[32], cm = -INFINITY;
@@ -647,39 +689,40 @@ __global__ void __launch_bounds__(512, 1) k_attn(
         ptx::fence_proxy_async_smem();
         if (j > 0) {  // O^T holds earlier chunks: scale the columns of the heads that moved
           if (owner) S.alpha[hd] = alpha;
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&S.max_full);
-          good = ptx::mbar_wait_warp(&S.max_full, (uint32_t)(nslow & 1), abort_flag, kAttnWaitBudget) &&
-                 ptx::mbar_wait_warp(&S.x_free[s ^ 1][0], (uint32_t)(((j - 1) >> 1) & 1), abort_flag,
+          softmax_sync();
+          // O(j - 1) complete; a wait that gives up stops the loop at the next vote
+          good = ptx::mbar_wait_warp(&S.x_free[s ^ 1][0], (uint32_t)(((j - 1) >> 1) & 1), abort_flag,
                                      kAttnWaitBudget) &&
                  ptx::mbar_wait_warp(&S.x_free[s ^ 1][1], (uint32_t)(((j - 1) >> 1) & 1), abort_flag,
-                                     kAttnWaitBudget);  // O(j - 1) complete
-          if (!good) break;
-          ++nslow;
-          ptx::tc_fence_after();
-          // this warp's share: O^T lanes of quarter q4 (channels), the columns of all 64 heads
+                                     kAttnWaitBudget);
+          if (good) {
+            ptx::tc_fence_after();
+            // this warp's share: O^T lanes of quarter q4 (channels), the columns of all 64 heads
 #pragma unroll 1
-          for (int c32 = 0; c32 < 2; ++c32) {
-            const float a32 = S.alpha[32 * c32 + lane];
-            if (!__any_sync(0xffffffffu, a32 != 1.0f)) continue;
+            for (int c32 = 0; c32 < 2; ++c32) {
+              const float a32 = S.alpha[32 * c32 + lane];
+              if (!__any_sync(0xffffffffu, a32 != 1.0f)) continue;
 #pragma unroll 1
-            for (int mt = 0; mt < 4; ++mt) {
-              uint32_t a[32];
-              const uint32_t ta = tmem + lane_base + (uint32_t)mt * 64u + 32u * (uint32_t)c32;
-              ptx::tmem_ld_32x32b_x32(ta, a);
-              ptx::tmem_wait_ld();
+              for (int mt = 0; mt < 4; ++mt) {
+                uint32_t a[32];
+                const uint32_t ta = tmem + lane_base + (uint32_t)mt * 64u + 32u * (uint32_t)c32;
+                ptx::tmem_ld_32x32b_x32(ta, a);
+                ptx::tmem_wait_ld();
 #pragma unroll
-              for (int jj = 0; jj < 32; ++jj)
-                a[jj] = __float_as_uint(__uint_as_float(a[jj]) * __shfl_sync(0xffffffffu, a32, jj));
-              ptx::tmem_st_32x32b_x32(ta, a);
+                for (int jj = 0; jj < 32; ++jj)
+                  a[jj] = __float_as_uint(__uint_as_float(a[jj]) * __shfl_sync(0xffffffffu, a32, jj));
+                ptx::tmem_st_32x32b_x32(ta, a);
+              }
+              ptx::tmem_wait_st();
             }
-            ptx::tmem_wait_st();
           }
         }
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&S.p_full[s]);  // the MMA warps wait; the softmax goes on
+      if (good) {
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&S.p_full[s]);  // the MMA warps wait; the softmax goes on
+      }
       lsum = fmaf(alpha, lsum, sum_probs(pp));
     }
     lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);  // the head's two lanes: every row
