@@ -914,8 +914,8 @@ extern "C" csa2_status csa2_index_topk_prefill(const csa2_kv_planes* kv, int32_t
   const uint16_t* q = (const uint16_t*)qidx_bf16;
   for (int64_t q0 = 0; q0 < Q; q0 += qb) {
     const int32_t nb = (int32_t)std::min<int64_t>(qb, Q - q0);
-    csa2_status rs = launch_scan(kv, nb, n_visible + q0, n_max, n_max, q + q0 * kHIdx * kDIdx, w + q0 * kHIdx,
-                                 nullptr, 0, scores, cols, nullptr, 0, ws, st, seq);
+    csa2_status rs = launch_scan_prefill(kv, nb, n_visible + q0, n_max, q + q0 * kHIdx * kDIdx, w + q0 * kHIdx,
+                                         scores, cols, ws, st, seq);
     if (rs != CSA2_OK) return rs;
     SelectArgs a{scores, cols, n_visible + q0, nullptr, 0, 0, 0, k, topk_out + q0 * k, k, n_max};
     launch_select(a, nb, st);

@@ -281,12 +281,34 @@ __device__ __forceinline__ void mma_mxf8f6f4_ss(uint32_t d_tmem, uint64_t a_desc
       : "memory");
 }
 
+// mma_mxf8f6f4_ss issued by the lane elect.sync picks (the warp runs the loop together)
+__device__ __forceinline__ void mma_mxf8f6f4_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                      uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                      uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], "
+      "p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 // Copies a 32-row x 16-byte shared-memory matrix (descriptor `src`) into
 // tensor memory at columns taddr..taddr+3 of all four lane quarters: lane
 // 32 q + l, column taddr + j receives bytes 4j..4j+3 of row l.  Asynchronous,
 // ordered with the MMAs the same thread issues afterwards.
 __device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t src) {
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src) : "memory");
+}
+
+// tmem_cp_32x128b_warpx4 issued by the lane elect.sync picks
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4_elect(uint32_t taddr, uint64_t src) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\t"
+      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
+      "l"(src)
+      : "memory");
 }
 
 // Element types of the block-scaled kinds (A/B format fields).

@@ -177,11 +177,12 @@ def _prefill(planes, seq, q, w, n_vis, n_max, k=512):
     return topk.cpu().numpy()
 
 
-@pytest.mark.parametrize("Q", [40, 100, 160])
+@pytest.mark.parametrize("Q", [40, 43, 100, 160])
 def test_prefill_indexer_shared_slot(cache, oracle_mod, Q):
     """Q queries of one slot, each with its own causal bound: every query's top-512 is the
     oracle's top-512 of that query over entries [0, n_visible).  The larger batches run the
-    select with 4, 2 and 1 CTAs per query (the batch alone fills the GPU's select slots)."""
+    select with 4, 2 and 1 CTAs per query (the batch alone fills the GPU's select slots);
+    43 queries leave the scan a last group of three (it scans four queries per key tile)."""
     c, _, _ = cache
     seq = 1
     q, w = W.index_query(4, 0, Q)
@@ -234,3 +235,24 @@ def test_prefill_indexer_mxfp4_queries(cache, oracle_mod):
     for i in range(Q):
         s = oracle_mod.index_scores(ixc, ixs, q[i], w[i], n=int(n_vis[i]))
         check_topk(topk[i], s, 512, what=f"prefill-mxfp4[{i}]")
+
+
+def test_prefill_indexer_mixed_groups(cache, oracle_mod):
+    """MXFP4 and bf16 queries alternate, so every four-query group of the scan mixes them
+    (the group takes the hi/lo path, exact for both), and 42 queries end in a group of two;
+    the visible counts differ inside each group.  Every top-512 matches the oracle's."""
+    import synth
+
+    c, _, _ = cache
+    seq, Q = 1, 42
+    q, w = W.index_query(7, 0, Q)
+    codes, scales = oracle_mod.quantize_index(synth.bf16_to_f32(q[::2]).reshape(-1, 128))
+    vals = oracle_mod.dequant_index(codes, scales).astype(np.float32)
+    q = q.copy()
+    q[::2] = (vals.view(np.uint32) >> 16).astype(np.uint16).reshape(-1, 32, 128)
+    n_vis = np.random.default_rng(5).integers(1, 4134, Q).astype(np.int32)
+    topk = _prefill(c.planes, seq, q, w, n_vis, c.n_max)
+    _, _, ixc, ixs = c.oracle_slot(seq)
+    for i in range(Q):
+        s = oracle_mod.index_scores(ixc, ixs, q[i], w[i], n=int(n_vis[i]))
+        check_topk(topk[i], s, 512, what=f"prefill-mixed[{i}]")
