@@ -488,7 +488,8 @@ def run_step40(dev, st, steps: int, warmup: int):
         # a second batch's outputs and scratch: two independent batches in flight on two
         # streams (the inputs are shared; each batch writes its own outputs and workspaces)
         import dataclasses
-        buf2 = dataclasses.replace(buf, out={l: torch.empty_like(o) for l, o in out.items()}, topk={}, pool={})
+        buf2 = dataclasses.replace(buf, out={l: torch.empty_like(o) for l, o in out.items()}, topk={}, pool={},
+                                   stage={})
         SCH.allocate_scratch(buf2, dev)
         st2 = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()

@@ -99,6 +99,9 @@ def lib() -> ctypes.CDLL:
             "csa2_index_topk": ([pl, i32, vp, i64, vp, vp, i32, ctypes.c_int, i32, i32, vp, vp, vp,
                                  vp, vp, sz, vp], ctypes.c_int),
             "csa2_index_topk_workspace_size": ([i32, i64, i32, i32, i32], sz),
+            "csa2_pool_stage": ([pl, i32, vp, i64, i32, i32, vp, vp, vp, vp], ctypes.c_int),
+            "csa2_index_topk_staged": ([vp, vp, i32, vp, i64, vp, vp, i32, i32, i32, vp, vp, vp, vp, sz, vp],
+                                       ctypes.c_int),
             "csa2_index_topk_prefill": ([pl, i32, i32, vp, i64, vp, vp, i32, vp, vp, sz, vp], ctypes.c_int),
             "csa2_index_topk_prefill_workspace_size": ([i32, i64, i32], sz),
             "csa2_index_topk_noalloc": ([pl, i32, vp, i64, vp, vp, i32, ctypes.c_int, i32, i32, vp,
@@ -262,6 +265,38 @@ def index_topk(planes: Planes, B: int, n_entries, n_max: int, qidx, w, k: int, m
                               k, mode, block, n_blocks_keep, _ptr(pool_in), _ptr(topk_out),
                               _ptr(pool_out), _ptr(scores_out), _ptr(ws), _nbytes(ws),
                               _stream(stream)), "csa2_index_topk")
+
+
+@dataclass
+class PoolStage:
+    """Staged indexer keys of a candidate pool: codes [B][keep*block][64], scales [B][keep*block][4]."""
+    codes: object
+    scales: object
+
+    @staticmethod
+    def empty(B: int, n_blocks_keep: int, block: int = 8, device="cuda") -> "PoolStage":
+        import torch
+
+        n = B * n_blocks_keep * block
+        u8 = dict(dtype=torch.uint8, device=device)
+        return PoolStage(torch.empty((n, 64), **u8), torch.empty((n, 4), **u8))
+
+
+def pool_stage(planes: Planes, B: int, n_entries, n_max: int, pool, stage: PoolStage, block: int = 8,
+               n_blocks_keep: int = 0, stream=None) -> None:
+    """Gathers the pool's blocks of indexer keys once (csa2_pool_stage), for index_topk_staged."""
+    _ok(lib().csa2_pool_stage(ctypes.byref(planes.c), B, _ptr(n_entries), n_max, block, n_blocks_keep,
+                              _ptr(pool), _ptr(stage.codes), _ptr(stage.scales), _stream(stream)),
+        "csa2_pool_stage")
+
+
+def index_topk_staged(stage: PoolStage, B: int, n_entries, n_max: int, qidx, w, k: int, pool_in, topk_out,
+                      ws, block: int = 8, n_blocks_keep: int = 0, scores_out=None, stream=None) -> None:
+    """POOL-mode top-k over a pool staged by pool_stage (csa2_index_topk_staged)."""
+    _ok(lib().csa2_index_topk_staged(_ptr(stage.codes), _ptr(stage.scales), B, _ptr(n_entries), n_max,
+                                     _ptr(qidx), _ptr(w), k, block, n_blocks_keep, _ptr(pool_in),
+                                     _ptr(topk_out), _ptr(scores_out), _ptr(ws), _nbytes(ws),
+                                     _stream(stream)), "csa2_index_topk_staged")
 
 
 def index_topk_prefill_workspace_size(Q: int, n_max: int, k: int) -> int:

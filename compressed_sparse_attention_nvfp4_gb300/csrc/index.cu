@@ -805,7 +805,10 @@ struct IndexWs {
   size_t bytes;
 };
 
-static IndexWs index_ws_layout(void* ws, int32_t B, int64_t n_max, int32_t block, int32_t keep) {
+// with_stage = false: the layout without the POOL-mode staging part (which sits last),
+// for a POOL call over planes the caller staged once (csa2_index_topk_staged)
+static IndexWs index_ws_layout(void* ws, int32_t B, int64_t n_max, int32_t block, int32_t keep,
+                               bool with_stage = true) {
   IndexWs L;
   L.score_cols = (int64_t)align_up((size_t)std::max<int64_t>(n_max, (int64_t)keep * block), 64);
   L.bmax_cols = (int64_t)align_up((size_t)cdiv(n_max, block), 64);
@@ -820,7 +823,7 @@ static IndexWs index_ws_layout(void* ws, int32_t B, int64_t n_max, int32_t block
   off += align_up(b_bytes, 256);
   L.pool = (int32_t*)(base ? base + off : nullptr);
   off += p_bytes;
-  const size_t stage_rows = (size_t)B * keep * block;
+  const size_t stage_rows = with_stage ? (size_t)B * keep * block : 0;
   L.stage_codes = (uint8_t*)(base ? base + off : nullptr);
   off += align_up(stage_rows * 64, 256);
   L.stage_scales = (uint8_t*)(base ? base + off : nullptr);
@@ -868,6 +871,37 @@ __global__ void __launch_bounds__(256) k_pool_gather(const uint8_t* __restrict__
     if (cp_code[g]) reinterpret_cast<uint4*>(st_codes + wg * 8 * 64)[lane] = code[g];
     if (cp_scale[g]) reinterpret_cast<uint32_t*>(st_scales + wg * 8 * 4)[lane] = scale[g];
   }
+}
+
+void launch_pool_gather(const csa2_kv_planes* kv, int32_t B, const int32_t* n_entries, int64_t n_max, int32_t keep,
+                        const int32_t* pool, uint8_t* st_codes, uint8_t* st_scales, cudaStream_t st) {
+  KernelTimer timer("k_pool_gather", st);
+  const int64_t warps = cdiv((int64_t)B * keep, kGatherBlocks);
+  k_pool_gather<<<(unsigned)cdiv(warps * 32, 256), 256, 0, st>>>(kv->ix_codes, kv->ix_scales, kv->seq_stride,
+                                                                 n_entries, n_max, pool, keep, B, st_codes,
+                                                                 st_scales);
+}
+
+// POOL mode over staged planes ([B][keep * block] entries): the scan scores every
+// staged entry as a flat slot, the select keeps the k best of the pool's visible
+// blocks (padding and blocks at or beyond n_entries[b] are masked by their ids)
+csa2_status pool_scan_select(const uint8_t* st_codes, const uint8_t* st_scales, int32_t B,
+                             const int32_t* n_entries, int64_t n_max, const uint16_t* q, const float* w, int32_t k,
+                             int32_t block, int32_t keep, const int32_t* pool, int32_t* topk_out,
+                             float* scores_out, const IndexWs& L, void* ws, cudaStream_t st) {
+  const int64_t keep_c = (int64_t)keep * block;
+  float* sc = scores_out ? scores_out : L.scores;
+  const int64_t sc_stride = scores_out ? keep_c : L.score_cols;
+  csa2_kv_planes staged{};
+  staged.ix_codes = const_cast<uint8_t*>(st_codes);
+  staged.ix_scales = const_cast<uint8_t*>(st_scales);
+  staged.seq_stride = keep_c;
+  csa2_status rs = launch_scan(&staged, B, nullptr, keep_c, keep_c, q, w, nullptr, 0, sc, sc_stride, nullptr,
+                               0, ws, st);
+  if (rs != CSA2_OK) return rs;
+  SelectArgs a{sc, sc_stride, n_entries, pool, keep, 0, keep_c, k, topk_out, k, n_max};
+  launch_select(a, B, st);
+  return CSA2_OK;
 }
 
 }  // namespace csa2
@@ -961,27 +995,13 @@ extern "C" csa2_status csa2_index_topk(const csa2_kv_planes* kv, int32_t B, cons
   const int64_t keep_c = (int64_t)n_blocks_keep * block;
 
   if (mode == CSA2_TOPK_POOL) {
-    float* sc = scores_out ? scores_out : L.scores;
-    int64_t sc_stride = scores_out ? keep_c : L.score_cols;
     // gather the pool's blocks into contiguous staged entries, then scan those
     // as flat slots of keep_c entries (one tensor load per 128 entries instead
     // of one per 8-entry block)
-    {
-      KernelTimer timer("k_pool_gather", st);
-      const int64_t warps = cdiv((int64_t)B * n_blocks_keep, kGatherBlocks);
-      k_pool_gather<<<(unsigned)cdiv(warps * 32, 256), 256, 0, st>>>(
-          kv->ix_codes, kv->ix_scales, kv->seq_stride, n_entries, n_max, pool_in, n_blocks_keep, B,
-          L.stage_codes, L.stage_scales);
-    }
-    csa2_kv_planes staged = *kv;
-    staged.ix_codes = L.stage_codes;
-    staged.ix_scales = L.stage_scales;
-    staged.seq_stride = keep_c;
-    csa2_status rs = launch_scan(&staged, B, nullptr, keep_c, keep_c, q, w, nullptr, 0, sc, sc_stride,
-                                 nullptr, 0, ws, st);
+    launch_pool_gather(kv, B, n_entries, n_max, n_blocks_keep, pool_in, L.stage_codes, L.stage_scales, st);
+    csa2_status rs = pool_scan_select(L.stage_codes, L.stage_scales, B, n_entries, n_max, q, w, k, block,
+                                      n_blocks_keep, pool_in, topk_out, scores_out, L, ws, st);
     if (rs != CSA2_OK) return rs;
-    SelectArgs a{sc, sc_stride, n_entries, pool_in, n_blocks_keep, 0, keep_c, k, topk_out, k, n_max};
-    launch_select(a, B, st);
     return launch_status();
   }
 
@@ -1011,6 +1031,44 @@ extern "C" csa2_status csa2_index_topk(const csa2_kv_planes* kv, int32_t B, cons
   launch_select(pa, B, st);
   SelectArgs ta{sc, sc_stride, n_entries, pool, n_blocks_keep, 0, keep_c, k, topk_out, k, n_max, 1};
   launch_select(ta, B, st);
+  return launch_status();
+}
+
+extern "C" csa2_status csa2_pool_stage(const csa2_kv_planes* kv, int32_t B, const int32_t* n_entries,
+                                       int64_t n_max, int32_t block, int32_t n_blocks_keep, const int32_t* pool,
+                                       uint8_t* stage_codes, uint8_t* stage_scales, csa2_stream stream) {
+  using namespace csa2;
+  if (!planes_ok(kv) || B <= 0 || !n_entries || !pool || !stage_codes || !stage_scales) return CSA2_ERR_INVALID_ARG;
+  if (n_max < 0 || n_max > kv->seq_stride || n_max >= ((int64_t)1 << 31)) return CSA2_ERR_INVALID_ARG;
+  if (block != 8) return CSA2_ERR_UNSUPPORTED;
+  if (n_blocks_keep < 1 || (int64_t)n_blocks_keep * block > 16384) return CSA2_ERR_INVALID_ARG;
+  if (!aligned(stage_codes, 32) || !aligned(stage_scales, 16)) return CSA2_ERR_INVALID_ARG;
+  launch_pool_gather(kv, B, n_entries, n_max, n_blocks_keep, pool, stage_codes, stage_scales,
+                     (cudaStream_t)stream);
+  return launch_status();
+}
+
+extern "C" csa2_status csa2_index_topk_staged(const uint8_t* stage_codes, const uint8_t* stage_scales, int32_t B,
+                                              const int32_t* n_entries, int64_t n_max, const void* qidx_bf16,
+                                              const float* w, int32_t k, int32_t block, int32_t n_blocks_keep,
+                                              const int32_t* pool_in, int32_t* topk_out, float* scores_out,
+                                              void* ws, size_t ws_bytes, csa2_stream stream) {
+  using namespace csa2;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (!stage_codes || !stage_scales || B <= 0 || !n_entries || !qidx_bf16 || !w || !pool_in || !topk_out)
+    return CSA2_ERR_INVALID_ARG;
+  if (k < 1 || k > CSA2_MAX_TOPK || n_max < 0 || n_max >= ((int64_t)1 << 31)) return CSA2_ERR_INVALID_ARG;
+  if (block != 8) return CSA2_ERR_UNSUPPORTED;
+  if (n_blocks_keep < 1 || (int64_t)n_blocks_keep * block > 16384) return CSA2_ERR_INVALID_ARG;
+  if (!aligned(stage_codes, 32) || !aligned(stage_scales, 16)) return CSA2_ERR_INVALID_ARG;
+  if (!aligned(qidx_bf16, 16) || !aligned(w, 16)) return CSA2_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256)) return CSA2_ERR_WORKSPACE;
+  IndexWs L = index_ws_layout(ws, B, n_max, block, n_blocks_keep, false);
+  if (ws_bytes < L.bytes) return CSA2_ERR_WORKSPACE;
+  if (reset_error(ws, st) != CSA2_OK) return CSA2_ERR_CUDA;
+  csa2_status rs = pool_scan_select(stage_codes, stage_scales, B, n_entries, n_max, (const uint16_t*)qidx_bf16, w,
+                                    k, block, n_blocks_keep, pool_in, topk_out, scores_out, L, ws, st);
+  if (rs != CSA2_OK) return rs;
   return launch_status();
 }
 

@@ -4,7 +4,9 @@ The layer table comes from the library (``csa2_v41_layer_table``): layers 0-1
 attend only to their sliding window; Full layers {2, 8, 14, 20} own a global KV
 and run the indexer (the encoder's at m=2 with a flat top-k, the decoder's at
 m=1 with the hierarchical pool); Reindex layers {24, 28, 32, 36} re-score the
-decoder Full layer's pool with their own query; Reuse layers take the top-k of
+decoder Full layer's pool with their own query (the pool's indexer keys are
+gathered once, right after the pool is built, and every Reindex layer scans
+that staged copy); Reuse layers take the top-k of
 the nearest Full/Reindex layer.  Every layer runs its own 64-head attention over
 its top-k entries of the KV it shares plus its own window
 ("DeepSeek-V4.1-Flash: pushing the limits of KV cache compression", sections 2,
@@ -19,8 +21,8 @@ from __future__ import annotations
 from dataclasses import dataclass, field
 
 from . import (LAYER_FULL, LAYER_REINDEX, LAYER_REUSE, LAYER_SWA, TOPK_FLAT, TOPK_HIER_BUILD,
-               TOPK_POOL, Planes, index_topk, index_topk_workspace_size, sparse_attn_decode,
-               sparse_attn_workspace_size, v41_layer_table, workspace)
+               Planes, PoolStage, index_topk, index_topk_staged, index_topk_workspace_size, pool_stage,
+               sparse_attn_decode, sparse_attn_workspace_size, v41_layer_table, workspace)
 
 
 @dataclass
@@ -49,6 +51,7 @@ class StepBuffers:
     softmax_scale: float = 512 ** -0.5
     topk: dict = field(default_factory=dict)
     pool: dict = field(default_factory=dict)
+    stage: dict = field(default_factory=dict)
     ws_index: object = None
     ws_attn: object = None
 
@@ -64,6 +67,8 @@ def allocate_scratch(buf: StepBuffers, device="cuda") -> None:
             buf.topk[l] = torch.empty((buf.B, buf.k), dtype=torch.int32, device=device)
         if t["mode"][l] == LAYER_FULL and t["m"][l] == 1:
             buf.pool[l] = torch.empty((buf.B, buf.n_blocks_keep), dtype=torch.int32, device=device)
+            if any(t["pool_src"][r] == l for r in range(40) if t["mode"][r] == LAYER_REINDEX):
+                buf.stage[l] = PoolStage.empty(buf.B, buf.n_blocks_keep, buf.block, device)
     buf.ws_index = workspace(index_topk_workspace_size(buf.B, n_max_all, buf.k, buf.block,
                                                        buf.n_blocks_keep), device)
     buf.ws_attn = workspace(sparse_attn_workspace_size(buf.B, buf.k, buf.n_swa), device)
@@ -89,14 +94,18 @@ def run_step(buf: StepBuffers, stream=None) -> int:
                 index_topk(kv, buf.B, ne, nm, buf.qidx[l], buf.w[l], buf.k, TOPK_HIER_BUILD, buf.topk[l],
                            buf.ws_index, buf.block, buf.n_blocks_keep, pool_out=buf.pool[l],
                            stream=stream)
+                if l in buf.stage:  # one gather of the pool's keys serves every Reindex layer
+                    pool_stage(kv, buf.B, ne, nm, buf.pool[l], buf.stage[l], buf.block, buf.n_blocks_keep,
+                               stream=stream)
+                    calls += 1
             else:
                 index_topk(kv, buf.B, ne, nm, buf.qidx[l], buf.w[l], buf.k, TOPK_FLAT, buf.topk[l],
                            buf.ws_index, stream=stream)
             calls += 1
         elif mode == LAYER_REINDEX:
-            index_topk(kv, buf.B, ne, nm, buf.qidx[l], buf.w[l], buf.k, TOPK_POOL, buf.topk[l],
-                       buf.ws_index, buf.block, buf.n_blocks_keep, pool_in=buf.pool[t["pool_src"][l]],
-                       stream=stream)
+            p = t["pool_src"][l]
+            index_topk_staged(buf.stage[p], buf.B, ne, nm, buf.qidx[l], buf.w[l], buf.k, buf.pool[p],
+                              buf.topk[l], buf.ws_index, buf.block, buf.n_blocks_keep, stream=stream)
             calls += 1
         topk = buf.topk[t["topk_src"][l]]
         sparse_attn_decode(kv, buf.B, topk, buf.k, buf.swa[l], buf.n_swa, buf.q[l], buf.softmax_scale,

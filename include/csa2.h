@@ -264,6 +264,39 @@ csa2_status csa2_index_topk(const csa2_kv_planes* kv, int32_t B, const int32_t* 
 size_t csa2_index_topk_workspace_size(int32_t B, int64_t n_max, int32_t k, int32_t block,
                                       int32_t n_blocks_keep);
 
+/* The Reindex layers of one decode step re-score one shared candidate pool -- the
+ * decoder Full layer's n_blocks_keep blocks -- over the same indexer keys, each with
+ * its own query ("DeepSeek-V4.1-Flash: pushing the limits of KV cache compression",
+ * 4.2 Full/Reindex/Reuse table and 4.3: the pool built once is shared by the Reindex
+ * layers).  csa2_index_topk in POOL mode gathers the pool's keys on every call; these
+ * two calls split that: csa2_pool_stage gathers them once, and every Reindex layer
+ * calls csa2_index_topk_staged on the staged copy.  Results are identical to POOL mode.
+ *
+ * csa2_pool_stage: block u of pool[b] (entries u*8 .. u*8+7 of slot b) goes to staged
+ * entries (b*n_blocks_keep + u)*8 .. +7 of
+ *   stage_codes  [B][n_blocks_keep*block][64] bytes (MXFP4 codes), 32-byte aligned;
+ *   stage_scales [B][n_blocks_keep*block][4] bytes (E8M0), 16-byte aligned;
+ * caller-owned device buffers.  Padding (-1) and blocks starting at or beyond
+ * n_entries[b] are not copied (their staged bytes stay as they were; the select
+ * masks them by their ids).  n_entries, n_max, block, n_blocks_keep as for
+ * csa2_index_topk; pool is the [B][n_blocks_keep] pool_out of a HIER_BUILD call.
+ * The staged copy is valid while the pool and the slot's indexer keys stay unchanged. */
+csa2_status csa2_pool_stage(const csa2_kv_planes* kv, int32_t B, const int32_t* n_entries, int64_t n_max,
+                            int32_t block, int32_t n_blocks_keep, const int32_t* pool,
+                            uint8_t* stage_codes, uint8_t* stage_scales, csa2_stream stream);
+
+/* POOL-mode top-k over planes staged by csa2_pool_stage with the same pool_in,
+ * n_entries, n_max, block and n_blocks_keep: the k best entries of the pool's blocks
+ * under this call's q and w.  Arguments as for csa2_index_topk (scores_out, if given,
+ * [B][n_blocks_keep*block] in pool order); ws: a workspace of
+ * csa2_index_topk_workspace_size(B, n_max, k, block, n_blocks_keep) bytes is enough
+ * (this call does not use that size's staging part, so less is accepted). */
+csa2_status csa2_index_topk_staged(const uint8_t* stage_codes, const uint8_t* stage_scales, int32_t B,
+                                   const int32_t* n_entries, int64_t n_max, const void* qidx_bf16,
+                                   const float* w, int32_t k, int32_t block, int32_t n_blocks_keep,
+                                   const int32_t* pool_in, int32_t* topk_out, float* scores_out, void* ws,
+                                   size_t ws_bytes, csa2_stream stream);
+
 /* Allocation-free form of csa2_index_topk (the design pages have no counterpart;
  * this exists for the library's users).  Some callers cannot allocate device
  * memory where they run the indexer -- a plugin handed only its input and output

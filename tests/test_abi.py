@@ -149,6 +149,29 @@ def test_host_validation_without_gpu(L):
                                   256, 1 << 30, None) == 1
 
 
+def test_pool_stage_validation_without_gpu(L):
+    fake = csa2.KVPlanes(16, 16, 32, 16, 100)  # aligned non-null pointers, never dereferenced
+    vp = ctypes.c_void_p
+    # csa2_pool_stage: missing pool, block != 8, pool larger than 16,384 entries, misaligned codes
+    assert L.csa2_pool_stage(ctypes.byref(fake), 1, 16, 100, 8, 4, None, vp(64), vp(64), None) == 1
+    assert L.csa2_pool_stage(ctypes.byref(fake), 1, 16, 100, 4, 4, vp(16), vp(64), vp(64), None) == 2
+    assert L.csa2_pool_stage(ctypes.byref(fake), 1, 16, 100, 8, 2049, vp(16), vp(64), vp(64), None) == 1
+    assert L.csa2_pool_stage(ctypes.byref(fake), 1, 16, 100, 8, 4, vp(16), vp(48), vp(64), None) == 1
+    assert L.csa2_pool_stage(ctypes.byref(fake), 1, 16, 101, 8, 4, vp(16), vp(64), vp(64), None) == 1  # n_max > stride
+    # csa2_index_topk_staged: k = 0, no pool, block != 8, no workspace, a workspace too small
+    args = lambda k=8, pool=16, block=8, ws=None, nb=0: (vp(64), vp(64), 1, vp(16), 100, vp(16), vp(16), k, block,
+                                                         4, vp(pool) if pool else None, vp(16), None,
+                                                         vp(ws) if ws else None, nb, None)
+    assert L.csa2_index_topk_staged(*args(k=0)) == 1
+    assert L.csa2_index_topk_staged(*args(pool=0)) == 1
+    assert L.csa2_index_topk_staged(*args(block=4)) == 2
+    assert L.csa2_index_topk_staged(*args()) == 3
+    assert L.csa2_index_topk_staged(*args(ws=256, nb=512)) == 3
+    # a workspace sized for csa2_index_topk is enough (more than the staged call needs)
+    full = L.csa2_index_topk_workspace_size(1, 100, 8, 8, 4)
+    assert full > 0
+
+
 def test_v4_compressor_and_dense_validation_without_gpu(L):
     fake = csa2.KVPlanes(16, 16, 16, 16, 100)
     args = (16, 16, 16, 16, 16, 16)  # Wa_kv, Wb_kv, Wa_z, Wb_z, Ba, Bb

@@ -102,6 +102,53 @@ def test_pool_mode(cache, oracle_mod):
         assert agree >= min(512, valid.sum()) - 2
 
 
+def test_staged_pool_equals_pool_mode(cache, oracle_mod):
+    """The pool's keys staged once (csa2_pool_stage) and re-scored by two Reindex queries
+    (csa2_index_topk_staged) give exactly POOL mode's top-k and candidate scores; padded
+    pool slots and blocks beyond n_entries stay masked although their staged bytes are
+    left as garbage."""
+    c, q, w = cache
+    n_entries = [4133, 4096, 700]
+    keep, k, B = 600, 512, 3
+    q2, w2 = W.index_query(0, 1, 3)
+    q3, w3 = W.index_query(0, 2, 3)
+    pools = []
+    for b, n in enumerate(n_entries):
+        _, _, ixc, ixs = c.oracle_slot(b)
+        pools.append(oracle_mod.hier_pool(oracle_mod.block_max(
+            oracle_mod.index_scores(ixc, ixs, q2[b], w2[b], n=n), 8), keep))
+    pools = np.stack(pools)
+    assert (pools[2] < 0).any() and (pools[0] < 0).any()  # padding present
+    pool_d = to_dev(pools.astype(np.int32))
+    ne = to_dev(np.array(n_entries, np.int32))
+    stage = csa2.PoolStage.empty(B, keep)
+    stage.codes.fill_(0xFF)
+    stage.scales.fill_(0xFF)
+    csa2.pool_stage(c.planes, B, ne, c.n_max, pool_d, stage, 8, keep)
+    ws = csa2.workspace(csa2.index_topk_workspace_size(B, c.n_max, k, 8, keep))
+    for qq, ww in ((q, w), (q3, w3)):
+        topk = torch.empty((B, k), dtype=torch.int32, device="cuda")
+        scores = torch.empty((B, keep * 8), dtype=torch.float32, device="cuda")
+        csa2.index_topk_staged(stage, B, ne, c.n_max, to_dev(qq.view(np.int16)), to_dev(ww), k, pool_d, topk,
+                               ws, 8, keep, scores_out=scores)
+        assert csa2.check(ws)[0] == 0
+        ref_topk, _, ref_scores = _run(c, qq, ww, n_entries, k, csa2.TOPK_POOL, keep=keep, pool_in=pools)
+        topk, scores = topk.cpu().numpy(), scores.cpu().numpy()
+        assert np.array_equal(topk, ref_topk)
+        for b, n in enumerate(n_entries):
+            cand = np.full(keep * 8, False)
+            for u_i, u in enumerate(pools[b]):
+                if u >= 0:
+                    cand[u_i * 8:u_i * 8 + min(8, n - 8 * u)] = True
+            assert np.array_equal(scores[b][cand], ref_scores[b][cand])
+            _, _, ixc, ixs = c.oracle_slot(b)
+            s = oracle_mod.index_scores(ixc, ixs, qq[b], ww[b], n=n)
+            valid = np.zeros(n, bool)
+            for u in pools[b][pools[b] >= 0]:
+                valid[8 * u:min(8 * u + 8, n)] = True
+            check_topk(topk[b], s, k, valid=valid, what=f"staged[{b}]")
+
+
 def test_degenerate_sizes(cache, oracle_mod):
     c, q, w = cache
     for n_entries in ([1, 511, 513], [0, 8, 7]):

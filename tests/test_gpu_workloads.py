@@ -164,7 +164,7 @@ def forty_layer_step(oracle_mod, seed, B, T, keep, check_queries, k=512):
     SCH.allocate_scratch(buf)
     calls = SCH.run_step(buf)
     torch.cuda.synchronize()
-    assert calls == 40 + 8  # 40 attention calls, 8 indexer calls
+    assert calls == 40 + 8 + 1  # 40 attention calls, 8 indexer calls, one gather of the shared pool
     assert csa2.check(buf.ws_index)[0] == 0 and csa2.check(buf.ws_attn)[0] == 0
     gtopk = {l: buf.topk[l].cpu().numpy() for l in buf.topk}
     dec_full = [f for f in full if t["m"][f] == 1][0]
