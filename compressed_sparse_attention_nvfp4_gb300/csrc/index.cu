@@ -39,6 +39,10 @@ struct SelectArgs {
   int64_t out_stride;
   int64_t n_max;        // visible entries are clamped to this bound
   int keys_by_entry;    // pool mode: keys are indexed by entry id, not by candidate
+  // queries whose candidate count lies outside [band_lo, band_hi] leave at once (all
+  // CTAs of their cluster alike), so a launch can serve the queries of one size band
+  int64_t band_lo = 0;
+  int64_t band_hi = INT64_MAX;
 };
 
 constexpr int kSelItems = 4;   // consecutive candidates per thread per chunk
@@ -136,6 +140,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThread
   const int tid = threadIdx.x, lane = threadIdx.x % 32, wid = threadIdx.x / 32;
   const int64_t n = max((int64_t)0, min((int64_t)a.n_entries[b], a.n_max));
   const int64_t ncand = a.pool ? a.ncand_fixed : (a.count_blocks ? cdiv(n, 8) : n);
+  if (ncand < a.band_lo || ncand > a.band_hi) return;  // another launch's query (uniform per cluster)
   const int64_t per = (int64_t)align_up((size_t)cdiv(ncand, kSelCluster), kSelItems);
   const int64_t lo = min(ncand, rank * per), hi = min(ncand, lo + per);
   const int64_t nchunks = cdiv(hi - lo, kChunk);
@@ -417,6 +422,7 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the keys come from the previous kernel
   const int64_t n = max((int64_t)0, min((int64_t)a.n_entries[b], a.n_max));
   const int64_t ncand = a.pool ? a.ncand_fixed : (a.count_blocks ? cdiv(n, 8) : n);
+  if (ncand < a.band_lo || ncand > a.band_hi) return;  // another launch's query (uniform per cluster)
   const int64_t per = (int64_t)align_up((size_t)cdiv(ncand, ncl), kSelItems);
   const int64_t lo = min(ncand, rank * per), hi = min(ncand, lo + per);
   // candidates per thread: a power of two >= 4 covering the slice (the launch
@@ -794,6 +800,28 @@ void launch_select(const SelectArgs& a, int B, cudaStream_t st) {
   }
 }
 
+// FLAT selects of queries whose candidate counts differ widely (the prefill
+// indexer's causal bounds): one launch per size band, each with the smallest
+// cluster whose CTAs hold a query's slice (1, 2, 4 CTAs for up to 1, 2, 4 x kResCap
+// candidates, then launch_select's choice), so a query of few candidates does not
+// hold eight CTAs through the cluster's barriers; a query outside a launch's band
+// leaves that launch at once.
+void launch_select_banded(SelectArgs a, int B, int64_t n_max, cudaStream_t st) {
+  int64_t lo = 0;
+  for (int ncl = 1; ncl < kSelCluster; ncl *= 2) {
+    const int64_t hi = std::min<int64_t>(n_max, (int64_t)ncl * kResCap);
+    a.band_lo = lo;
+    a.band_hi = hi;
+    launch_select_res<256>(a, B, ncl, (int64_t)align_up((size_t)cdiv(std::max<int64_t>(hi, 1), ncl), kSelItems),
+                           st);
+    if (hi >= n_max) return;
+    lo = hi + 1;
+  }
+  a.band_lo = lo;
+  a.band_hi = INT64_MAX;
+  launch_select(a, B, st);
+}
+
 // ------------------------------------------------------------------ workspace
 struct IndexWs {
   float* scores;
@@ -951,8 +979,8 @@ extern "C" csa2_status csa2_index_topk_prefill(const csa2_kv_planes* kv, int32_t
     csa2_status rs = launch_scan_prefill(kv, nb, n_visible + q0, n_max, q + q0 * kHIdx * kDIdx, w + q0 * kHIdx,
                                          scores, cols, ws, st, seq);
     if (rs != CSA2_OK) return rs;
-    SelectArgs a{scores, cols, n_visible + q0, nullptr, 0, 0, 0, k, topk_out + q0 * k, k, n_max};
-    launch_select(a, nb, st);
+    launch_select_banded(SelectArgs{scores, cols, n_visible + q0, nullptr, 0, 0, 0, k, topk_out + q0 * k, k, n_max},
+                         nb, n_max, st);
   }
   return launch_status();
 }

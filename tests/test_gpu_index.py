@@ -227,9 +227,9 @@ def _prefill(planes, seq, q, w, n_vis, n_max, k=512):
 @pytest.mark.parametrize("Q", [40, 43, 100, 160])
 def test_prefill_indexer_shared_slot(cache, oracle_mod, Q):
     """Q queries of one slot, each with its own causal bound: every query's top-512 is the
-    oracle's top-512 of that query over entries [0, n_visible).  The larger batches run the
-    select with 4, 2 and 1 CTAs per query (the batch alone fills the GPU's select slots);
-    43 queries leave the scan a last group of three (it scans four queries per key tile)."""
+    oracle's top-512 of that query over entries [0, n_visible).  Every count fits one
+    select CTA, so the selects run in the one-CTA band; 43 queries leave the scan a last
+    group of three (it scans four queries per key tile)."""
     c, _, _ = cache
     seq = 1
     q, w = W.index_query(4, 0, Q)

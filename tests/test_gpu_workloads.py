@@ -228,3 +228,39 @@ def test_v41_forty_layer_step_full_size(oracle_mod):
     and 127 are checked against the oracle over their whole caches in every layer
     ("DeepSeek-V4.1-Flash: pushing the limits of KV cache compression", 4.2 and 4.3)."""
     forty_layer_step(oracle_mod, seed=4, B=128, T=262144, keep=2048, check_queries=(0, 127))
+
+
+def test_prefill_indexer_full_size_sampled(oracle_mod):
+    """The prefill indexer at the benchmark's shape: 2,048 queries over one 131,072-entry
+    slot, query i seeing its first 64 (i + 1) entries (the causal bound of token 128 (i + 1)
+    at m = 2), in one call as bench.py times it.  The selects then run in four launches by
+    candidate count (clusters of 1, 2, 4 and 8 CTAs); queries on both sides of each band's
+    edge and the longest are checked against the oracle's scores of their visible prefix
+    ("DeepSeek-V4: Towards Highly Efficient Million-Token Context Intelligence", CSA step 2)."""
+    from compressed_sparse_attention_nvfp4_gb300 import workload as WL
+
+    N, Q, seed, k = 131072, 2048, 6, 512
+    n_vis = (np.arange(Q, dtype=np.int64) + 1) * 64
+    planes = csa2.Planes.empty(1, N)
+    WL.fill_planes(planes, seed, 0, 1, N)
+    qd, wd, q, w = WL.index_query_dev(seed, 0, Q)
+    topk = torch.empty((Q, k), dtype=torch.int32, device="cuda")
+    ws = csa2.workspace(csa2.index_topk_prefill_workspace_size(Q, N, k))
+    csa2.index_topk_prefill(planes, 0, Q, to_dev(n_vis.astype(np.int32)), N, qd, wd, k, topk, ws)
+    assert csa2.check(ws)[0] == 0
+    topk = topk.cpu().numpy()
+    del planes, ws
+    torch.cuda.empty_cache()
+
+    ixc = np.empty((N, 64), np.uint8)
+    ixs = np.empty((N, 4), np.uint8)
+
+    def enc(j0, cnt=1 << 16):
+        return j0, oracle_mod.quantize_index(W.index_latents(seed, 0, 1, N, 0, j0, cnt, 0.0, None))
+
+    with ThreadPoolExecutor(4) as ex:
+        for j0, (c2, s2) in ex.map(enc, range(0, N, 1 << 16)):
+            ixc[j0:j0 + (1 << 16)], ixs[j0:j0 + (1 << 16)] = c2, s2
+    for i in (0, 7, 255, 256, 511, 512, 1023, 1024, 2047):
+        s = oracle_mod.index_scores(ixc, ixs, q[i], w[i], n=int(n_vis[i]))
+        check_topk(topk[i], s, k, what=f"prefill-full[{i}]")
