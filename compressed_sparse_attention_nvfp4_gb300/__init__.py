@@ -121,6 +121,7 @@ def lib() -> ctypes.CDLL:
             "csa2_selftest_wait_timeout": ([ctypes.c_longlong, vp, sz, vp], ctypes.c_int),
             "csa2_selftest_codec_division": ([vp, sz, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64),
                                               vp], ctypes.c_int),
+            "csa2_selftest_encode_sweep": ([ctypes.c_uint32, ctypes.c_uint32, vp, sz, vp, vp], ctypes.c_int),
             "csa2_status_string": ([ctypes.c_int], ctypes.c_char_p),
             "csa2_timing_enable": ([i32], ctypes.c_int),
             "csa2_kernel_times": ([ctypes.POINTER(KernelTime), i32], i32),
@@ -407,6 +408,18 @@ def selftest_codec_division(ws, stream=None) -> tuple[int, int]:
                                            _stream(stream)),
         "csa2_selftest_codec_division")
     return bad.value, n.value
+
+
+def selftest_encode_sweep(ws, chunk0: int = 0, nchunks: int = 4096, stream=None):
+    """uint64 [nchunks, 2]: per chunk of 2^20 fp32 bit patterns (c << 20 | i), the sums of
+    the codec's E2M1 codes and E4M3 bytes of its non-NaN values weighted by 2 i + 1
+    (mod 2^64) -- csa2_selftest_encode_sweep."""
+    import numpy as np
+
+    out = np.zeros((nchunks, 2), np.uint64)
+    _ok(lib().csa2_selftest_encode_sweep(chunk0, nchunks, _ptr(ws), _nbytes(ws), out.ctypes.data,
+                                         _stream(stream)), "csa2_selftest_encode_sweep")
+    return out
 
 
 def timing_enable(on: bool) -> None:

@@ -62,6 +62,35 @@ __global__ void __launch_bounds__(256) k_selftest_division(unsigned long long* b
   atomicAdd(n, nn);
 }
 
+// Self-test of the codec's element encoders over every fp32 bit pattern: chunk c
+// (blockIdx.y + chunk0) holds the 2^20 patterns (c << 20) | i.  For each pattern that is
+// not a NaN, the E2M1 code (the codec's fp32 -> E2M1 conversion) and the E4M3 byte (its
+// fp32 -> E4M3 scale conversion) are summed with weight 2 i + 1 modulo 2^64 into
+// sums[c - chunk0][0] and [1]: any single differing code changes its chunk's sum.
+constexpr int kSweepChunkBits = 20;
+__global__ void __launch_bounds__(256) k_selftest_encode_sweep(uint32_t chunk0, unsigned long long* sums) {
+  const uint32_t c = chunk0 + blockIdx.y;
+  constexpr uint32_t per_cta = (1u << kSweepChunkBits) / 64;  // gridDim.x == 64
+  unsigned long long s2 = 0, s4 = 0;
+  for (uint32_t j = threadIdx.x; j < per_cta; j += blockDim.x) {
+    const uint32_t i = blockIdx.x * per_cta + j;
+    const uint32_t bits = (c << kSweepChunkBits) | i;
+    if ((bits & 0x7F800000u) == 0x7F800000u && (bits & 0x007FFFFFu) != 0u) continue;  // NaN
+    const float x = __uint_as_float(bits);
+    const unsigned long long wgt = 2ull * i + 1ull;
+    s2 += (unsigned long long)(float2_to_e2m1x2(x, 0.0f) & 0xFu) * wgt;
+    s4 += (unsigned long long)float_to_e4m3(x) * wgt;
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+    s4 += __shfl_xor_sync(0xffffffffu, s4, o);
+  }
+  if (threadIdx.x % 32 == 0) {
+    atomicAdd(&sums[2 * blockIdx.y], s2);
+    atomicAdd(&sums[2 * blockIdx.y + 1], s4);
+  }
+}
+
 void launch_quantize(const float* Cbar, const float* KI, int64_t n, const csa2_kv_planes* dst, const QDest& d,
                      cudaStream_t st, const csa2_norm_rope* nr) {
   if (n <= 0) return;
@@ -239,5 +268,25 @@ extern "C" csa2_status csa2_selftest_codec_division(void* ws, size_t ws_bytes, i
   if (cudaStreamSynchronize(st) != cudaSuccess) return CSA2_ERR_CUDA;
   *mismatches = (int64_t)h[0];
   *compared = (int64_t)h[1];
+  return CSA2_OK;
+}
+
+extern "C" csa2_status csa2_selftest_encode_sweep(uint32_t chunk0, uint32_t nchunks, void* ws, size_t ws_bytes,
+                                                  uint64_t* sums, csa2_stream stream) {
+  using namespace csa2;
+  constexpr uint32_t kChunks = 1u << (32 - kSweepChunkBits);
+  if (!sums || nchunks == 0 || chunk0 >= kChunks || nchunks > kChunks - chunk0) return CSA2_ERR_INVALID_ARG;
+  const size_t need = kWsHeader + (size_t)nchunks * 2 * sizeof(unsigned long long);
+  if (!ws || !aligned(ws, 256) || ws_bytes < need) return CSA2_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  unsigned long long* d = reinterpret_cast<unsigned long long*>((char*)ws + kWsHeader);
+  if (cudaMemsetAsync(d, 0, (size_t)nchunks * 2 * sizeof(unsigned long long), st) != cudaSuccess)
+    return CSA2_ERR_CUDA;
+  k_selftest_encode_sweep<<<dim3(64, nchunks), 256, 0, st>>>(chunk0, d);
+  if (cudaGetLastError() != cudaSuccess) return CSA2_ERR_CUDA;
+  if (cudaMemcpyAsync(sums, d, (size_t)nchunks * 2 * sizeof(unsigned long long), cudaMemcpyDeviceToHost, st) !=
+      cudaSuccess)
+    return CSA2_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return CSA2_ERR_CUDA;
   return CSA2_OK;
 }

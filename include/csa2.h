@@ -480,6 +480,18 @@ csa2_status csa2_selftest_wait_timeout(long long budget_cycles, void* ws, size_t
 csa2_status csa2_selftest_codec_division(void* ws, size_t ws_bytes, int64_t* mismatches, int64_t* compared,
                                          csa2_stream stream);
 
+/* Self-test of the codec's two element encoders over all 2^32 fp32 bit patterns (the
+ * cache format's E2M1 and E4M3 roundings: "DeepSeek-V4.1-Flash: pushing the limits of KV
+ * cache compression", section 5; round to nearest even, saturating).  Chunk c
+ * (chunk0 <= c < chunk0 + nchunks <= 4096) holds the patterns (c << 20) | i; for every
+ * one that is not a NaN, the E2M1 code the codec gives it and the E4M3 byte are summed
+ * with weight 2 i + 1 modulo 2^64 into sums[2 (c - chunk0)] and sums[2 (c - chunk0) + 1]
+ * (host, 2 * nchunks values), so a reference encoder's sums, formed the same way, must
+ * equal them chunk by chunk.  Synchronises `stream`.  ws: device, 256-byte aligned, at
+ * least 256 + 16 * nchunks bytes. */
+csa2_status csa2_selftest_encode_sweep(uint32_t chunk0, uint32_t nchunks, void* ws, size_t ws_bytes,
+                                       uint64_t* sums, csa2_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

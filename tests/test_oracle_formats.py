@@ -109,3 +109,67 @@ def test_fp4_range_pin(oracle_mod):
     tab = {k: v for k, v in rt("bytes_per_token.txt")}
     assert oracle_mod.e4m3_value(0x7E) * oracle_mod.e2m1_value(7) == float(tab["fp4_max_magnitude"])
     assert abs(np.sqrt(512) - float(tab["latent_norm_bound"])) < 0.05
+
+
+def _all_fp32_chunks(bits_per_chunk=17):
+    n = 1 << bits_per_chunk
+    for c in range(1 << (32 - bits_per_chunk)):
+        yield (np.uint32(c) << np.uint32(bits_per_chunk)) | np.arange(n, dtype=np.uint32)
+
+
+def test_e2m1_encode_all_fp32(oracle_mod):
+    """Every fp32 bit pattern but the NaNs: the code's sign bit is the input's (a value
+    that rounds to zero keeps its sign), its magnitude is the nearest E2M1 magnitude with
+    ties to the even code, and everything beyond 6 (infinities too) saturates to 6."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    mags = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+    def check(bits):
+        x = bits.view(np.float32)
+        x = x[~np.isnan(x)]
+        codes = oracle_mod.e2m1_encode_array(x)
+        if not np.array_equal(codes >> 3, np.signbit(x).astype(np.uint8)):
+            return "sign"
+        a = np.abs(x.astype(np.float64))
+        c = (codes & 7).astype(np.int64)
+        if not np.all(c[a >= 6.0] == 7):
+            return "saturation"
+        f = a < 6.0
+        a, c = a[f], c[f]
+        err = np.abs(a - mags[c])
+        up, dn = np.minimum(c + 1, 7), np.maximum(c - 1, 0)
+        eu, ed = np.abs(a - mags[up]), np.abs(a - mags[dn])
+        if not (np.all(err <= eu) and np.all(err <= ed)):
+            return "nearest"
+        if not (np.all(c[(err == eu) & (up != c)] % 2 == 0) and np.all(c[(err == ed) & (dn != c)] % 2 == 0)):
+            return "ties"
+        return None
+
+    with ThreadPoolExecutor(8) as ex:
+        fails = [r for r in ex.map(check, _all_fp32_chunks()) if r]
+    assert not fails, fails[:4]
+
+
+def test_e4m3_encode_all_fp32(oracle_mod):
+    """Every fp32 bit pattern but the NaNs: equal to torch's fp32 -> float8_e4m3fn cast
+    (round to nearest even) wherever that cast is finite (|x| <= 464, where 464 rounds to
+    448), and saturated to +-448 (bytes 0x7E / 0xFE) beyond it, infinities included."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    def check(bits):
+        x = bits.view(np.float32)
+        x = x[~np.isnan(x)]
+        got = oracle_mod.e4m3_encode_array(x)
+        small = np.abs(x) <= 464.0
+        ref = torch.from_numpy(x[small]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        if not np.array_equal(got[small], ref):
+            return "rounding"
+        big = ~small
+        if not np.array_equal(got[big], np.where(np.signbit(x[big]), 0xFE, 0x7E).astype(np.uint8)):
+            return "saturation"
+        return None
+
+    with ThreadPoolExecutor(8) as ex:
+        fails = [r for r in ex.map(check, _all_fp32_chunks()) if r]
+    assert not fails, fails[:4]
