@@ -58,6 +58,30 @@ def recorded_traffic(fp: str):
     return None
 
 
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal bandwidth (context next to the measured peak)
+
+
+def host_cpu() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    import platform
+    import subprocess
+
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -1261,6 +1285,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"kernel": "k_scan_tc (indexer scan, block-scaled FP4 MMA)", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": hbm, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                      "traffic": traffic, "algorithmic_bytes_per_launch": idx_bytes,
                      "launch_ms": round(scan_avg_ms, 4), "sources": fp,
                      "index_call": {"achieved": round(idx_achieved, 1),
@@ -1349,7 +1374,7 @@ def main():
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded counter-based generator)",
             "config": line_config(world),
             "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": desc, "steps_per_query": f},
+                             "sample": desc, "steps_per_query": f, "cpu_model": host_cpu()},
             "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}))
         return
@@ -1459,7 +1484,7 @@ def main():
         if world == 1 and not args.no_cpu_baseline:
             v, cores, desc = oracle_sample(2, 1)
             line["cpu_baseline"] = {"value": round(v, 4), "unit": UNIT, "cores": cores,
-                                    "kind": "oracle", "sample": desc}
+                                    "kind": "oracle", "sample": desc, "cpu_model": host_cpu()}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
