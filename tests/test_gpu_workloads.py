@@ -264,3 +264,50 @@ def test_prefill_indexer_full_size_sampled(oracle_mod):
     for i in (0, 7, 255, 256, 511, 512, 1023, 1024, 2047):
         s = oracle_mod.index_scores(ixc, ixs, q[i], w[i], n=int(n_vis[i]))
         check_topk(topk[i], s, k, what=f"prefill-full[{i}]")
+
+
+def test_select_bands_and_streaming_select(oracle_mod):
+    """Selections past 8 x 16,384 candidates, which no benchmarked shape reaches: a FLAT
+    decode over 150,016 entries (the streaming select, `k_select`, whose slices exceed a
+    CTA's shared memory) and a prefill whose visible counts sit on both sides of every
+    size-band edge (16,384, 32,768, 65,536, 131,072), the last band again streaming.
+    Every top-512 against the oracle's scores ("DeepSeek-V4: Towards Highly Efficient
+    Million-Token Context Intelligence", CSA step 2)."""
+    from compressed_sparse_attention_nvfp4_gb300 import workload as WL
+
+    N, B, seed, k = 150016, 2, 11, 512
+    planes = csa2.Planes.empty(B, N)
+    WL.fill_planes(planes, seed, 0, B, N)
+    ixc = np.empty((B, N, 64), np.uint8)
+    ixs = np.empty((B, N, 4), np.uint8)
+    for b in range(B):
+        for j0 in range(0, N, 1 << 16):
+            cnt = min(1 << 16, N - j0)
+            c2, s2 = oracle_mod.quantize_index(W.index_latents(seed, 0, B, N, b, j0, cnt, 0.0, None))
+            ixc[b, j0:j0 + cnt], ixs[b, j0:j0 + cnt] = c2, s2
+
+    # FLAT decode, both queries streaming
+    n_entries = [N, 140000]
+    qd, wd, q, w = WL.index_query_dev(seed, 0, B)
+    topk = torch.empty((B, k), dtype=torch.int32, device="cuda")
+    ws = csa2.workspace(csa2.index_topk_workspace_size(B, N, k))
+    csa2.index_topk(planes, B, to_dev(np.array(n_entries, np.int32)), N, qd, wd, k, csa2.TOPK_FLAT, topk, ws)
+    assert csa2.check(ws)[0] == 0
+    topk = topk.cpu().numpy()
+    for b, n in enumerate(n_entries):
+        s = oracle_mod.index_scores(ixc[b], ixs[b], q[b], w[b], n=n)
+        check_topk(topk[b], s, k, what=f"flat-streaming[{b}]")
+
+    # prefill over slot 1 with visible counts around every band edge
+    n_vis = np.array([N, 131073, 131072, 65537, 65536, 32769, 32768, 16385, 16384, 7, 0], np.int32)
+    Q = n_vis.shape[0]
+    qd, wd, q, w = WL.index_query_dev(seed, 1, Q)
+    topk = torch.empty((Q, k), dtype=torch.int32, device="cuda")
+    ws = csa2.workspace(csa2.index_topk_prefill_workspace_size(Q, N, k))
+    csa2.index_topk_prefill(planes, 1, Q, to_dev(n_vis), N, qd, wd, k, topk, ws)
+    assert csa2.check(ws)[0] == 0
+    topk = topk.cpu().numpy()
+    for i in range(Q):
+        n = int(n_vis[i])
+        s = oracle_mod.index_scores(ixc[1], ixs[1], q[i], w[i], n=n) if n else np.zeros(0)
+        check_topk(topk[i], s, k, what=f"prefill-band[{i}] n={n}")
