@@ -833,9 +833,18 @@ struct IndexWs {
   size_t bytes;
 };
 
+// FLAT over this many entries or more selects through the 8-entry block maxima: the k
+// best blocks hold the k best entries (a block holding one of them has its own best
+// entry among them, and blocks rank as their best entries do: by maximum, then block
+// id, i.e. entry id), so a pool of k blocks and a select over its 8k entries give the
+// flat top-k exactly, from two selections of n/8 and 8k keys instead of one of n.
+constexpr int64_t kFlatViaPoolMin = 65536;
+inline int32_t flat_pool_blocks(int64_t n_max, int32_t k) { return n_max >= kFlatViaPoolMin ? k : 0; }
+
 // with_stage = false: the layout without the POOL-mode staging part (which sits last),
-// for a POOL call over planes the caller staged once (csa2_index_topk_staged)
-static IndexWs index_ws_layout(void* ws, int32_t B, int64_t n_max, int32_t block, int32_t keep,
+// for a POOL call over planes the caller staged once (csa2_index_topk_staged).
+// The pool part also holds a FLAT call's k blocks (flat_pool_blocks).
+static IndexWs index_ws_layout(void* ws, int32_t B, int64_t n_max, int32_t block, int32_t keep, int32_t k,
                                bool with_stage = true) {
   IndexWs L;
   L.score_cols = (int64_t)align_up((size_t)std::max<int64_t>(n_max, (int64_t)keep * block), 64);
@@ -843,7 +852,7 @@ static IndexWs index_ws_layout(void* ws, int32_t B, int64_t n_max, int32_t block
   size_t off = kWsHeader;
   size_t s_bytes = (size_t)B * L.score_cols * 4;
   size_t b_bytes = (size_t)B * L.bmax_cols * 4;
-  size_t p_bytes = align_up((size_t)B * keep * 4, 256);
+  size_t p_bytes = align_up((size_t)B * std::max(keep, flat_pool_blocks(n_max, k)) * 4, 256);
   char* base = (char*)ws;
   L.scores = (float*)(base ? base + off : nullptr);
   off += align_up(s_bytes, 256);
@@ -987,9 +996,8 @@ extern "C" csa2_status csa2_index_topk_prefill(const csa2_kv_planes* kv, int32_t
 
 extern "C" size_t csa2_index_topk_workspace_size(int32_t B, int64_t n_max, int32_t k, int32_t block,
                                                  int32_t n_blocks_keep) {
-  (void)k;
-  if (B <= 0 || n_max < 0 || block <= 0 || n_blocks_keep < 0) return 0;
-  return csa2::index_ws_layout(nullptr, B, n_max, block, n_blocks_keep).bytes;
+  if (B <= 0 || n_max < 0 || block <= 0 || n_blocks_keep < 0 || k < 0) return 0;
+  return csa2::index_ws_layout(nullptr, B, n_max, block, n_blocks_keep, k).bytes;
 }
 
 extern "C" csa2_status csa2_index_topk(const csa2_kv_planes* kv, int32_t B, const int32_t* n_entries,
@@ -1015,7 +1023,7 @@ extern "C" csa2_status csa2_index_topk(const csa2_kv_planes* kv, int32_t B, cons
   }
   if (!aligned(qidx_bf16, 16) || !aligned(w, 16)) return CSA2_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, 256)) return CSA2_ERR_WORKSPACE;
-  IndexWs L = index_ws_layout(ws, B, n_max, block, n_blocks_keep);
+  IndexWs L = index_ws_layout(ws, B, n_max, block, n_blocks_keep, k);
   if (ws_bytes < L.bytes) return CSA2_ERR_WORKSPACE;
   if (reset_error(ws, st) != CSA2_OK) return CSA2_ERR_CUDA;
 
@@ -1033,7 +1041,10 @@ extern "C" csa2_status csa2_index_topk(const csa2_kv_planes* kv, int32_t B, cons
     return launch_status();
   }
 
-  if (mode == CSA2_TOPK_FLAT) {
+  if (mode == CSA2_TOPK_FLAT && flat_pool_blocks(n_max, k) > 0) {
+    // long contexts: the same top-k through a pool of k blocks (flat_pool_blocks)
+    n_blocks_keep = flat_pool_blocks(n_max, k);
+  } else if (mode == CSA2_TOPK_FLAT) {
     float* sc = scores_out ? scores_out : L.scores;
     int64_t sc_stride = scores_out ? n_max : L.score_cols;
     csa2_status rs = launch_scan(kv, B, n_entries, n_max, n_max, q, w, nullptr, 0, sc, sc_stride,
@@ -1044,20 +1055,21 @@ extern "C" csa2_status csa2_index_topk(const csa2_kv_planes* kv, int32_t B, cons
     return launch_status();
   }
 
-  // HIER_BUILD: one full scan writes every entry's score and the block maxima;
-  // the pool is selected from the maxima, and the token top-k reads the scores
-  // of the pool's entries where the scan left them (4 bytes written per entry
-  // instead of a second pass over the pool's keys).
+  // HIER_BUILD (and FLAT over long contexts): one full scan writes every entry's
+  // score and the block maxima; the pool is selected from the maxima, and the token
+  // top-k reads the scores of the pool's entries where the scan left them (4 bytes
+  // written per entry instead of a second pass over the pool's keys).
+  const int64_t keep_p = (int64_t)n_blocks_keep * 8;
   float* sc = scores_out ? scores_out : L.scores;
   const int64_t sc_stride = scores_out ? n_max : L.score_cols;
   csa2_status rs = launch_scan(kv, B, n_entries, n_max, n_max, q, w, nullptr, 0, sc, sc_stride, L.bmax,
                                L.bmax_cols, ws, st);
   if (rs != CSA2_OK) return rs;
-  int32_t* pool = pool_out ? pool_out : L.pool;
+  int32_t* pool = pool_out && mode == CSA2_TOPK_HIER_BUILD ? pool_out : L.pool;
   SelectArgs pa{L.bmax, L.bmax_cols, n_entries, nullptr, 0, 1, 0, n_blocks_keep, pool, n_blocks_keep,
                 n_max};
   launch_select(pa, B, st);
-  SelectArgs ta{sc, sc_stride, n_entries, pool, n_blocks_keep, 0, keep_c, k, topk_out, k, n_max, 1};
+  SelectArgs ta{sc, sc_stride, n_entries, pool, n_blocks_keep, 0, keep_p, k, topk_out, k, n_max, 1};
   launch_select(ta, B, st);
   return launch_status();
 }
@@ -1091,7 +1103,7 @@ extern "C" csa2_status csa2_index_topk_staged(const uint8_t* stage_codes, const 
   if (!aligned(stage_codes, 32) || !aligned(stage_scales, 16)) return CSA2_ERR_INVALID_ARG;
   if (!aligned(qidx_bf16, 16) || !aligned(w, 16)) return CSA2_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, 256)) return CSA2_ERR_WORKSPACE;
-  IndexWs L = index_ws_layout(ws, B, n_max, block, n_blocks_keep, false);
+  IndexWs L = index_ws_layout(ws, B, n_max, block, n_blocks_keep, k, false);
   if (ws_bytes < L.bytes) return CSA2_ERR_WORKSPACE;
   if (reset_error(ws, st) != CSA2_OK) return CSA2_ERR_CUDA;
   csa2_status rs = pool_scan_select(stage_codes, stage_scales, B, n_entries, n_max, (const uint16_t*)qidx_bf16, w,

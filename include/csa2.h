@@ -236,7 +236,10 @@ size_t csa2_compress_workspace_size(int64_t T, int32_t d_model);
  *   I_j = sum_h w[b,h] * ReLU(q[b,h,:] . K^I_j),  h over 32 heads of dim 128,
  *   K^I_j the dequantized MXFP4 key of entry j.
  * Selection order: score descending, then entry index ascending.
- *   FLAT:       the k best of entries [0, n_entries[b]).
+ *   FLAT:       the k best of entries [0, n_entries[b]).  For n_max >= 65,536 the call
+ *               selects them through the 8-entry block maxima: the k best blocks hold the
+ *               k best entries, so a pool of k blocks gives the same set exactly, from two
+ *               small selections instead of one over every entry.
  *   HIER_BUILD: block score s_u = max of I_j over block u = [u*block, u*block+block)
  *               (partial last block allowed); the pool is the n_blocks_keep best
  *               blocks (ties to the lower block); topk = the k best entries of the

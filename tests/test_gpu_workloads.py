@@ -268,11 +268,13 @@ def test_prefill_indexer_full_size_sampled(oracle_mod):
 
 def test_select_bands_and_streaming_select(oracle_mod):
     """Selections past 8 x 16,384 candidates, which no benchmarked shape reaches: a FLAT
-    decode over 150,016 entries (the streaming select, `k_select`, whose slices exceed a
-    CTA's shared memory) and a prefill whose visible counts sit on both sides of every
-    size-band edge (16,384, 32,768, 65,536, 131,072), the last band again streaming.
-    Every top-512 against the oracle's scores ("DeepSeek-V4: Towards Highly Efficient
-    Million-Token Context Intelligence", CSA step 2)."""
+    decode over 150,016 entries, selected through a pool of k blocks by csa2_index_topk and
+    directly by the streaming select (`k_select`, whose slices exceed a CTA's shared memory)
+    in the allocation-free entry point -- the two must give the same ids exactly -- and a
+    prefill whose visible counts sit on both sides of every size-band edge (16,384, 32,768,
+    65,536, 131,072), the last band again streaming.  Every top-512 against the oracle's
+    scores ("DeepSeek-V4: Towards Highly Efficient Million-Token Context Intelligence",
+    CSA step 2)."""
     from compressed_sparse_attention_nvfp4_gb300 import workload as WL
 
     N, B, seed, k = 150016, 2, 11, 512
@@ -291,9 +293,14 @@ def test_select_bands_and_streaming_select(oracle_mod):
     qd, wd, q, w = WL.index_query_dev(seed, 0, B)
     topk = torch.empty((B, k), dtype=torch.int32, device="cuda")
     ws = csa2.workspace(csa2.index_topk_workspace_size(B, N, k))
-    csa2.index_topk(planes, B, to_dev(np.array(n_entries, np.int32)), N, qd, wd, k, csa2.TOPK_FLAT, topk, ws)
+    ne = to_dev(np.array(n_entries, np.int32))
+    csa2.index_topk(planes, B, ne, N, qd, wd, k, csa2.TOPK_FLAT, topk, ws)
     assert csa2.check(ws)[0] == 0
+    direct = torch.full((B, k), -7, dtype=torch.int32, device="cuda")
+    csa2.index_topk_noalloc(planes, B, ne, N, qd, wd, k, csa2.TOPK_FLAT, direct)
+    assert csa2.index_topk_noalloc_check()[0] == 0
     topk = topk.cpu().numpy()
+    assert np.array_equal(topk, direct.cpu().numpy())  # the pool of k blocks loses nothing
     for b, n in enumerate(n_entries):
         s = oracle_mod.index_scores(ixc[b], ixs[b], q[b], w[b], n=n)
         check_topk(topk[b], s, k, what=f"flat-streaming[{b}]")
