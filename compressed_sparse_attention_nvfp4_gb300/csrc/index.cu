@@ -945,24 +945,36 @@ csa2_status pool_scan_select(const uint8_t* st_codes, const uint8_t* st_scales, 
 
 namespace csa2 {
 namespace {
-// Prefill indexer: queries per scan launch, so that their fp32 scores fit in
-// about 1 GB of workspace (at least one query, at most all of them).
-constexpr int64_t kPrefillScoreBytes = (int64_t)1 << 30;
-int64_t prefill_batch(int32_t Q, int64_t n_max) {
-  const int64_t cols = (int64_t)align_up((size_t)std::max<int64_t>(n_max, 1), 64);
-  return std::max<int64_t>(1, std::min<int64_t>(Q, kPrefillScoreBytes / (cols * 4)));
-}
-size_t prefill_ws_bytes(int32_t Q, int64_t n_max) {
-  const int64_t cols = (int64_t)align_up((size_t)std::max<int64_t>(n_max, 1), 64);
-  return kWsHeader + align_up((size_t)prefill_batch(Q, n_max) * cols * 4, 256);
+// Prefill indexer: queries per scan launch, so that their fp32 scores (and, over long
+// slots, their block maxima and pools) fit in about 1.25 GiB of workspace (at least one
+// query, at most all of them; 2,048 queries over 131,072 entries take one launch).
+// Slots of kFlatViaPoolMin entries or more select each query's top-k through a pool of
+// k blocks, as csa2_index_topk's FLAT mode does.
+constexpr int64_t kPrefillScoreBytes = (int64_t)5 << 28;
+struct PrefillWs {
+  int64_t cols, bcols, qb;
+  bool pooled;
+  size_t score_bytes, bmax_bytes, pool_bytes, bytes;
+};
+PrefillWs prefill_ws(int32_t Q, int64_t n_max, int32_t k) {
+  PrefillWs L;
+  L.cols = (int64_t)align_up((size_t)std::max<int64_t>(n_max, 1), 64);
+  L.pooled = flat_pool_blocks(n_max, k) > 0;
+  L.bcols = L.pooled ? (int64_t)align_up((size_t)cdiv(n_max, 8), 64) : 0;
+  const int64_t per_query = (L.cols + L.bcols + (L.pooled ? k : 0)) * 4;
+  L.qb = std::max<int64_t>(1, std::min<int64_t>(Q, kPrefillScoreBytes / per_query));
+  L.score_bytes = align_up((size_t)L.qb * L.cols * 4, 256);
+  L.bmax_bytes = align_up((size_t)L.qb * L.bcols * 4, 256);
+  L.pool_bytes = L.pooled ? align_up((size_t)L.qb * k * 4, 256) : 0;
+  L.bytes = kWsHeader + L.score_bytes + L.bmax_bytes + L.pool_bytes;
+  return L;
 }
 }  // namespace
 }  // namespace csa2
 
 extern "C" size_t csa2_index_topk_prefill_workspace_size(int32_t Q, int64_t n_max, int32_t k) {
-  (void)k;
-  if (Q <= 0 || n_max < 0) return 0;
-  return csa2::prefill_ws_bytes(Q, n_max);
+  if (Q <= 0 || n_max < 0 || k < 0) return 0;
+  return csa2::prefill_ws(Q, n_max, k).bytes;
 }
 
 extern "C" csa2_status csa2_index_topk_prefill(const csa2_kv_planes* kv, int32_t seq, int32_t Q,
@@ -977,19 +989,29 @@ extern "C" csa2_status csa2_index_topk_prefill(const csa2_kv_planes* kv, int32_t
     return CSA2_ERR_INVALID_ARG;
   if (!aligned(qidx_bf16, 16) || !aligned(w, 16)) return CSA2_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, 256)) return CSA2_ERR_WORKSPACE;
-  if (ws_bytes < prefill_ws_bytes(Q, n_max)) return CSA2_ERR_WORKSPACE;
+  const PrefillWs L = prefill_ws(Q, n_max, k);
+  if (ws_bytes < L.bytes) return CSA2_ERR_WORKSPACE;
   if (reset_error(ws, st) != CSA2_OK) return CSA2_ERR_CUDA;
-  const int64_t qb = prefill_batch(Q, n_max);
-  const int64_t cols = (int64_t)align_up((size_t)std::max<int64_t>(n_max, 1), 64);
-  float* scores = (float*)((char*)ws + kWsHeader);
+  char* base = (char*)ws + kWsHeader;
+  float* scores = (float*)base;
+  float* bmax = L.pooled ? (float*)(base + L.score_bytes) : nullptr;
+  int32_t* pool = L.pooled ? (int32_t*)(base + L.score_bytes + L.bmax_bytes) : nullptr;
   const uint16_t* q = (const uint16_t*)qidx_bf16;
-  for (int64_t q0 = 0; q0 < Q; q0 += qb) {
-    const int32_t nb = (int32_t)std::min<int64_t>(qb, Q - q0);
+  for (int64_t q0 = 0; q0 < Q; q0 += L.qb) {
+    const int32_t nb = (int32_t)std::min<int64_t>(L.qb, Q - q0);
     csa2_status rs = launch_scan_prefill(kv, nb, n_visible + q0, n_max, q + q0 * kHIdx * kDIdx, w + q0 * kHIdx,
-                                         scores, cols, ws, st, seq);
+                                         scores, L.cols, bmax, L.bcols, ws, st, seq);
     if (rs != CSA2_OK) return rs;
-    launch_select_banded(SelectArgs{scores, cols, n_visible + q0, nullptr, 0, 0, 0, k, topk_out + q0 * k, k, n_max},
-                         nb, n_max, st);
+    if (L.pooled) {  // the k best blocks by maximum, then the k best entries of those blocks
+      SelectArgs pa{bmax, L.bcols, n_visible + q0, nullptr, 0, 1, 0, k, pool, k, n_max};
+      launch_select(pa, nb, st);
+      SelectArgs ta{scores, L.cols, n_visible + q0, pool, k, 0, (int64_t)k * 8, k, topk_out + q0 * k, k, n_max, 1};
+      launch_select(ta, nb, st);
+    } else {
+      launch_select_banded(
+          SelectArgs{scores, L.cols, n_visible + q0, nullptr, 0, 0, 0, k, topk_out + q0 * k, k, n_max}, nb, n_max,
+          st);
+    }
   }
   return launch_status();
 }

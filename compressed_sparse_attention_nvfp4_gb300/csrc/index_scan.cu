@@ -744,6 +744,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // the first buffer while query 1 is summed and 3 into the second; the accumulator is
         // released once the last read lands, before the last two sums
         uint32_t da[32], db[32];
+        float bm[kPG];  // this entry's visible score per query (-inf if not visible), for the block maxima
         auto score = [&](int qi, const uint32_t (&d)[32]) {
           float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
           const float4* wq = reinterpret_cast<const float4*>(S.w[qi]);
@@ -758,7 +759,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
             acc1 = fma_f32x2(make_float2(wv.z, wv.w), x23, acc1);
           }
           const float sum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
-          if (c < nqv[qi]) __stcs(p.scores + (int64_t)(b0 + qi) * p.score_stride + c, sum);
+          const bool vis = c < nqv[qi];
+          if (vis) __stcs(p.scores + (int64_t)(b0 + qi) * p.score_stride + c, sum);
+          bm[qi] = vis ? sum : -INFINITY;
         };
         static_assert(kPG == 4, "the epilogue reads the queries in pairs");
         ptx::tmem_ld_32x32b_x32(lane_addr, da);
@@ -774,6 +777,17 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (lane == 0) ptx::mbar_arrive(&S.d_free[g]);  // every column read: the accumulator is free
         score(2, da);
         score(3, db);
+        if (p.bmax) {  // maxima of the 8-entry blocks (lanes 8 j .. 8 j + 7 hold one), the four queries interleaved
+#pragma unroll
+          for (int o = 1; o < 8; o <<= 1)
+#pragma unroll
+            for (int qi = 0; qi < kPG; ++qi) bm[qi] = fmaxf(bm[qi], __shfl_xor_sync(0xffffffffu, bm[qi], o));
+          if ((lane & 7) == 0) {
+#pragma unroll
+            for (int qi = 0; qi < kPG; ++qi)
+              if (c < nqv[qi]) p.bmax[(int64_t)(b0 + qi) * p.bmax_stride + c / 8] = bm[qi];
+          }
+        }
       }
     }
   }
@@ -860,8 +874,8 @@ csa2_status launch_scan(const csa2_kv_planes* kv, int32_t B, const int32_t* n_en
 }
 
 csa2_status launch_scan_prefill(const csa2_kv_planes* kv, int32_t Q, const int32_t* n_visible, int64_t n_max,
-                                const uint16_t* q, const float* w, float* scores, int64_t score_stride, void* ws,
-                                cudaStream_t st, int slot) {
+                                const uint16_t* q, const float* w, float* scores, int64_t score_stride, float* bmax,
+                                int64_t bmax_stride, void* ws, cudaStream_t st, int slot) {
   if (n_max <= 0) return CSA2_OK;
   const int64_t rows = (int64_t)(slot + 1) * kv->seq_stride;
   if (rows >= ((int64_t)1 << 31)) return CSA2_ERR_UNSUPPORTED;
@@ -876,7 +890,7 @@ csa2_status launch_scan_prefill(const csa2_kv_planes* kv, int32_t Q, const int32
   const int groups = (int)cdiv(Q, kPG);
   const int S = (int)std::max<int64_t>(1, cdiv(cdiv(n_max, kTile), kPTilesPerCta));
   ScanParams p{kv->ix_codes, kv->ix_scales, kv->seq_stride, n_visible, n_max, q, w, nullptr, 0,
-               n_max, S, scores, score_stride, nullptr, 0, ws, slot};
+               n_max, S, scores, score_stride, bmax, bmax_stride, ws, slot};
   KernelTimer timer("k_scan_prefill", st);
   launch_pdl(k_scan_prefill, dim3((unsigned)S, (unsigned)groups), dim3(kPThreads), (size_t)smem, st, p, map_tile,
              (int)Q);

@@ -26,9 +26,11 @@ csa2_status launch_scan(const csa2_kv_planes* kv, int32_t B, const int32_t* n_en
 
 // Prefill scores: Q queries over sequence slot `slot` (query b sees its first
 // n_visible[b] <= n_max entries), four queries per key tile; scores[b][j] for
-// j < n_visible[b] (the rest of each row is left as it was).
+// j < n_visible[b] (the rest of each row is left as it was), and with bmax non-null
+// bmax[b][u] = the maximum of the visible scores of block u = [8 u, 8 u + 8) for the
+// blocks that start below n_visible[b].
 csa2_status launch_scan_prefill(const csa2_kv_planes* kv, int32_t Q, const int32_t* n_visible, int64_t n_max,
-                                const uint16_t* q, const float* w, float* scores, int64_t score_stride, void* ws,
-                                cudaStream_t st, int slot);
+                                const uint16_t* q, const float* w, float* scores, int64_t score_stride, float* bmax,
+                                int64_t bmax_stride, void* ws, cudaStream_t st, int slot);
 
 }  // namespace csa2

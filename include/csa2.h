@@ -335,7 +335,9 @@ csa2_status csa2_index_topk_staged(const uint8_t* stage_codes, const uint8_t* st
  * encoder's prefill indexer stays O(N^2), about 3072 N^2 multiply-adds over 3 Full
  * layers).  Every query streams the slot's keys (68 bytes per entry; after the
  * first query they come from L2 when the slot fits).  Queries run in batches whose
- * fp32 scores take about 1 GB of workspace.
+ * fp32 scores (with, for n_max >= 65,536, their 8-entry block maxima and a pool of k
+ * blocks each, through which the top-k is then selected exactly as FLAT mode does)
+ * take about 1.25 GiB of workspace.
  *   qidx [Q][32][128] bf16; w [Q][32] fp32; n_visible [Q] int32 (device);
  *   topk_out [Q][k] int32. */
 csa2_status csa2_index_topk_prefill(const csa2_kv_planes* kv, int32_t seq, int32_t Q,

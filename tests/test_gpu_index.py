@@ -243,8 +243,10 @@ def test_prefill_indexer_shared_slot(cache, oracle_mod, Q):
 
 
 def test_prefill_indexer_batches(cache, oracle_mod):
-    """A 2^24-entry bound makes the scores of only 16 queries fit the workspace's 1 GB, so
-    40 queries run in three launches (the visible entries are the cache's first 4,133)."""
+    """A 2^24-entry bound makes the scores, block maxima and pools of only 17 queries fit
+    the workspace's 1.25 GiB, so 40 queries run in three launches, each selecting through
+    a pool of 512 blocks whose maxima go through the streaming select (the visible entries
+    are the cache's first 4,133)."""
     c, _, _ = cache
     Q, stride = 40, 1 << 24
     big = csa2.Planes.empty(1, stride)
