@@ -395,7 +395,43 @@ __device__ __forceinline__ void digit_masks(const uint32_t (&dg)[kResMaxPer / 4]
   }
 }
 
-template <int NT>
+// The same two steps as rolled loops, the digits kept in shared memory (word v of a
+// thread at dg[v * stride]).  A select that runs once per SM executes its code once per
+// warp, so the unrolled form's length, not its trip count, sets how long the warps wait
+// for instructions; a large grid keeps the code in the instruction caches instead, and
+// the unrolled form is faster there.
+__device__ __forceinline__ void first_digits_rolled(const uint4* myslots, int nslot, int swz, int shift,
+                                                    uint32_t base0, unsigned* myhist, uint32_t* dg, int stride) {
+#pragma unroll 1
+  for (int v = 0; v < nslot; ++v) {
+    const uint4 k4 = myslots[v ^ swz];
+    const uint32_t kk4[4] = {k4.x, k4.y, k4.z, k4.w};
+    uint32_t w = 0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (kk4[i] != 0u) {
+        const uint32_t d = (kk4[i] >> shift) - base0;
+        atomicAdd(&myhist[d], 1u);
+        w |= (d + 1u) << (8 * i);
+      }
+    }
+    dg[v * stride] = w;
+  }
+}
+__device__ __forceinline__ void digit_masks_rolled(const uint32_t* dg, int stride, int nslot, uint32_t j4,
+                                                   uint64_t& gtm, uint64_t& binm) {
+#pragma unroll 1
+  for (int v = 0; v < nslot; ++v) {
+    const uint32_t d = dg[v * stride];
+    const uint32_t gt = ((__vcmpgtu4(d, j4) & 0x01010101u) * 0x01020408u) >> 24;
+    const uint32_t eq = ((__vcmpeq4(d, j4) & 0x01010101u) * 0x01020408u) >> 24;
+    gtm |= (uint64_t)gt << (4 * v);
+    binm |= (uint64_t)eq << (4 * v);
+  }
+}
+
+// kRolled: the first-digit steps as rolled loops (grids of at most two CTAs per SM)
+template <int NT, bool kRolled>
 __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
   constexpr int kBins = 256;
   constexpr int kWarpsSel = NT / 32;
@@ -543,6 +579,11 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
   // above the threshold's first-digit bin / in it (only the latter need the final key)
   uint64_t gtm0 = 0, binm = 0;
   uint32_t dg[kResMaxPer / 4];  // first digit + 1 of the keys of slot v, a byte each (0: no key)
+  uint32_t* dgr = nullptr;      // the same in shared memory (rolled form)
+  if constexpr (kRolled) {
+    __shared__ uint32_t dg_s[kResMaxPer / 4][NT];
+    dgr = &dg_s[0][tid];
+  }
   // digit of pass p: bits [shift + 7, shift] (the last pass may reach below bit 0)
   for (int shift = shift0; need_total > 0 && shift > -8; shift -= 8, ++pass) {
     for (int d = lane; d < kBins; d += 32) myhist[d] = 0;
@@ -556,12 +597,16 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
       }
     }
     if (pass == 0) {  // every key: count its first digit and keep it in dg (unrolled per run length)
-      switch (nslot) {
-        case 1: first_digits<1>(myslots, swz, shift, base0, myhist, dg); break;
-        case 2: first_digits<2>(myslots, swz, shift, base0, myhist, dg); break;
-        case 4: first_digits<4>(myslots, swz, shift, base0, myhist, dg); break;
-        case 8: first_digits<8>(myslots, swz, shift, base0, myhist, dg); break;
-        default: first_digits<kResMaxPer / 4>(myslots, swz, shift, base0, myhist, dg); break;
+      if constexpr (kRolled) {
+        first_digits_rolled(myslots, nslot, swz, shift, base0, myhist, dgr, NT);
+      } else {
+        switch (nslot) {
+          case 1: first_digits<1>(myslots, swz, shift, base0, myhist, dg); break;
+          case 2: first_digits<2>(myslots, swz, shift, base0, myhist, dg); break;
+          case 4: first_digits<4>(myslots, swz, shift, base0, myhist, dg); break;
+          case 8: first_digits<8>(myslots, swz, shift, base0, myhist, dg); break;
+          default: first_digits<kResMaxPer / 4>(myslots, swz, shift, base0, myhist, dg); break;
+        }
       }
     }
     const int vend = (pass > 0 && ncomp <= kCompCap) || pass == 0 ? 0 : nslot;
@@ -620,12 +665,16 @@ __global__ void __launch_bounds__(NT) k_select_res(SelectArgs a) {
     __syncthreads();
     if (pass == 0) {  // from the kept digits: four keys per byte-wise compare
       const uint32_t j4 = (((s_prefix >> shift) - base0) + 1u) * 0x01010101u;  // the bin's digit + 1
-      switch (nslot) {
-        case 1: digit_masks<1>(dg, j4, gtm0, binm); break;
-        case 2: digit_masks<2>(dg, j4, gtm0, binm); break;
-        case 4: digit_masks<4>(dg, j4, gtm0, binm); break;
-        case 8: digit_masks<8>(dg, j4, gtm0, binm); break;
-        default: digit_masks<kResMaxPer / 4>(dg, j4, gtm0, binm); break;
+      if constexpr (kRolled) {
+        digit_masks_rolled(dgr, NT, nslot, j4, gtm0, binm);
+      } else {
+        switch (nslot) {
+          case 1: digit_masks<1>(dg, j4, gtm0, binm); break;
+          case 2: digit_masks<2>(dg, j4, gtm0, binm); break;
+          case 4: digit_masks<4>(dg, j4, gtm0, binm); break;
+          case 8: digit_masks<8>(dg, j4, gtm0, binm); break;
+          default: digit_masks<kResMaxPer / 4>(dg, j4, gtm0, binm); break;
+        }
       }
     }
     if (pass == 0 && shift > 0) {  // more digits follow: keep the threshold bin's keys
@@ -760,7 +809,13 @@ void launch_select_res(const SelectArgs& a, int B, int ncl, int64_t per, cudaStr
   while ((int64_t)kper * NT < per) kper *= 2;
   const int smem = NT * kper * 4;
   // a failure here surfaces as the launch error that launch_status() reports
-  cudaFuncSetAttribute(k_select_res<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kResCap * 4));
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // one CTA per select slot or fewer: the rolled form (its code runs once per warp)
+  const bool rolled = (int64_t)B * ncl <= 2 * (int64_t)(sms > 0 ? sms : 148);
+  auto kern = rolled ? k_select_res<NT, true> : k_select_res<NT, false>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kResCap * 4));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(B * ncl));
   cfg.blockDim = dim3(NT);
@@ -776,7 +831,7 @@ void launch_select_res(const SelectArgs& a, int B, int ncl, int64_t per, cudaStr
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   KernelTimer timer("k_select_res", st);
-  cudaLaunchKernelEx(&cfg, k_select_res<NT>, a);
+  cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 void launch_select(const SelectArgs& a, int B, cudaStream_t st) {
