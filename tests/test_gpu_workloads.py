@@ -233,9 +233,10 @@ def test_v41_forty_layer_step_full_size(oracle_mod):
 def test_prefill_indexer_full_size_sampled(oracle_mod):
     """The prefill indexer at the benchmark's shape: 2,048 queries over one 131,072-entry
     slot, query i seeing its first 64 (i + 1) entries (the causal bound of token 128 (i + 1)
-    at m = 2), in one call as bench.py times it.  The selects then run in four launches by
-    candidate count (clusters of 1, 2, 4 and 8 CTAs); queries on both sides of each band's
-    edge and the longest are checked against the oracle's scores of their visible prefix
+    at m = 2), in one call as bench.py times it: the scan writes the scores and the 8-entry
+    block maxima, and each query's top-512 is selected through a pool of its 512 best blocks.
+    Queries from the shortest to the longest (on both sides of 16,384, 32,768 and 65,536
+    visible entries) are checked against the oracle's scores of their visible prefix
     ("DeepSeek-V4: Towards Highly Efficient Million-Token Context Intelligence", CSA step 2)."""
     from compressed_sparse_attention_nvfp4_gb300 import workload as WL
 
