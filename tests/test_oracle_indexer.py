@@ -95,6 +95,29 @@ def test_hierarchy_invariant_flat_in_pool(oracle_mod):
         assert np.array_equal(flat, hier)
 
 
+def test_flat_topk_through_a_pool_of_k_blocks(oracle_mod):
+    """The smallest pool that keeps the invariant: k blocks.  The flat top-k equals the
+    top-k of the k best blocks' entries exactly, with heavy ties (a few distinct values,
+    all-equal scores), partial last blocks and fewer blocks than k -- the identity the
+    library's FLAT selection over long contexts relies on."""
+    rng = np.random.default_rng(16)
+    for trial in range(40):
+        n = int(rng.integers(1, 5000))
+        k = int(rng.integers(1, 700))
+        kind = trial % 4
+        if kind == 0:
+            s = rng.standard_normal(n)
+        elif kind == 1:
+            s = rng.integers(0, 4, n).astype(np.float64)
+        elif kind == 2:
+            s = np.full(n, 2.5)
+        else:
+            s = np.repeat(rng.standard_normal((n + 7) // 8), 8)[:n]  # every block constant
+        flat = oracle_mod.topk(s, k)
+        pool = oracle_mod.hier_pool(oracle_mod.block_max(s, 8), k)
+        assert np.array_equal(flat, oracle_mod.pool_topk(s, pool, 8, k)), (trial, n, k)
+
+
 def test_hierarchy_sizes():
     """2048 blocks of 8 positions give at most 16,384 candidates; 1M entries make
     131,072 blocks (the hierarchical indexer's sizes)."""
