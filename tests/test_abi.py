@@ -214,6 +214,32 @@ def test_workspace_queries(L):
     assert csa2.cache_write_workspace_size(131072, 5120, 2) >= 65536 * 640 * 4
 
 
+def test_flat_workspace_holds_the_pool_from_65536_entries():
+    """FLAT over 65,536 entries or more selects through a pool of k blocks, so its
+    workspace (the same query as every mode's) holds B x k pool ids from there on."""
+    B, k = 128, 512
+    below = csa2.index_topk_workspace_size(B, 65535, k)
+    at = csa2.index_topk_workspace_size(B, 65536, k)
+    assert at - below >= B * k * 4
+    # a HIER_BUILD workspace with a larger pool already covers it
+    assert csa2.index_topk_workspace_size(B, 65536, k, 8, 2048) >= at
+
+
+def test_prefill_workspace_budget():
+    """The prefill indexer's batches hold the scores, the block maxima and the pools of as
+    many queries as fit about 1.25 GiB: 2,048 queries over 131,072 entries in one batch,
+    and at least one query whatever the slot."""
+    one = csa2.index_topk_prefill_workspace_size(2048, 131072, 512)
+    per_query = (131072 + 131072 // 8 + 512) * 4
+    assert one >= 2048 * per_query
+    assert one <= (5 << 28) + 64 * 1024
+    # a 2^24-entry slot: batches of 17 queries
+    big = csa2.index_topk_prefill_workspace_size(40, 1 << 24, 512)
+    assert 17 * ((1 << 24) + (1 << 21) + 512) * 4 <= big <= (5 << 28) + 64 * 1024
+    # shorter slots keep no maxima or pools
+    assert csa2.index_topk_prefill_workspace_size(100, 4224, 512) < 100 * 4288 * 4 + 64 * 1024
+
+
 def test_kernel_timing_switch_without_gpu(L):
     """Switching timing on and off and reading totals touch no device when
     nothing was launched: no totals, status ok."""
